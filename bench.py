@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked gated delta rule on GB300.
+
+One step = gdn_chunk_fwd (keeping the saved tensors) + gdn_chunk_bwd on the
+packed varlen workload (32768 tokens, lengths ~U[1,8192], H=16, HV=32,
+K=V=128, fp32 initial state, dh0 out), inputs resident in HBM.  The same JSON
+line carries the decode-step bandwidth on the 256-row / [512,32,128,128]
+pool workload, the per-kernel roofline of the dominant kernel, an end-to-end
+number through host buffers, and the fp64 CPU oracle as a baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica of the workload (no data-path
+collective: the (sequence, head) units are independent); the time is the max
+over ranks and `value` counts every rank's tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd tokens/s (T=32K packed, H=16, HV=32, K=V=128); decode state GB/s"
+C, D = 64, 128
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# fp32 CUDA-core peak: 152 SMs x 128 FP32 lanes x 2 flop x 2.070 GHz (max SM clock)
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+# ---------------------------------------------------------------------------- algorithmic work
+def kernel_work(name, T, H, HV, N, C_total):
+    """Algorithmic (flops, bytes) of one launch of a kernel on a problem.
+
+    Flops count the contractions of the chunked form per (token, value head)
+    with chunk C = 64, K = V = 128, r = HV / H (masking and padding excluded);
+    bytes count the tensors the kernel must read or write once."""
+    r = HV // H
+    TV = T * HV
+    f = dict(
+        intra=(2 * C * D / r + 2 * C * D + 2 * C * D + 2 * C * C / 3) * TV,
+        state=4 * D * D * TV,
+        out=(2 * C * D / r + 2 * C * D + 2 * D * D) * TV,
+        dvloc=(2 * C * D / r + 2 * C * D) * TV,
+        bstate=6 * D * D * TV,
+        bintra_a=6 * D * D * TV,
+        bintra_b=(6 * C * D + 12 * C * D + 4 * C * C + 2 * C * D / r) * TV,
+    ).get(name, 0.0)
+    bf = 2
+    b = dict(
+        plan=4 * (N + 1 + 3 * C_total),
+        prep=T * H * D * bf * 2 + TV * 4 * 2 + T * H * 8,
+        intra=T * H * D * bf + TV * D * bf + TV * 6 + TV * D * bf * 2 + C_total * HV * C * C * 4,
+        state=TV * D * bf * 3 + T * H * D * bf + C_total * HV * D * D * bf + N * HV * D * D * 8,
+        out=T * H * D * bf * 2 + TV * D * bf * 2 + C_total * HV * D * D * bf,
+        dvloc=T * H * D * bf * 2 + TV * D * (bf + 4),
+        bstate=T * H * D * bf * 2 + TV * D * (bf * 2 + 4 * 2) + C_total * HV * D * D * bf,
+        bintra_a=TV * D * (bf * 2 + 4 * 4) + C_total * HV * D * D * bf * 2,
+        bintra_b=T * H * D * bf * 2 + TV * D * (bf * 3 + 4 * 4) + C_total * HV * C * C * 4,
+        bnorm=TV * D * 4 * 2 + T * H * D * bf * 4,
+    ).get(name, 0.0)
+    return f, b
+
+
+def decode_bytes(n_active, B, H, HV):
+    return n_active * HV * 2 * D * D * 4 + B * (2 * H * D * 2 + HV * D * 2 * 2 + HV * 8)
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- helpers
+def _bf(torch, bits, dev):
+    return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+class ChunkRunner:
+    """Device buffers of one chunk workload and one fwd+bwd step through the C ABI."""
+
+    def __init__(self, torch, wl, dev):
+        import chunked_gated_delta_06_gb300 as gdn
+        self.torch, self.gdn, self.wl, self.dev = torch, gdn, wl, dev
+        T, H, HV, N = wl.T, wl.H, wl.HV, wl.N
+        self.q, self.k, self.v = _bf(torch, wl.q_bits, dev), _bf(torch, wl.k_bits, dev), _bf(torch, wl.v_bits, dev)
+        self.g = torch.from_numpy(wl.g).to(dev)
+        self.beta = _bf(torch, wl.beta_bits, dev)
+        self.h0 = None if wl.h0 is None else torch.from_numpy(wl.h0).to(dev)
+        self.d_o = _bf(torch, wl.do_bits, dev)
+        self.d_ht = None if wl.d_ht is None else torch.from_numpy(wl.d_ht).to(dev)
+        self.cu_dev = torch.from_numpy(wl.cu_seqlens).to(dev)
+        self.p, self._keep = gdn.make_problem(wl.cu_seqlens, H, HV, cu_dev_ptr=self.cu_dev.data_ptr())
+        e = lambda *s, dt=torch.float32: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+        self.o = e(T, HV, D, dt=torch.bfloat16)
+        self.ht = e(N, HV, D, D)
+        self.saved = e(gdn.gdn_chunk_saved_bytes(self.p), dt=torch.uint8)
+        self.ws_f = e(gdn.gdn_chunk_workspace_bytes(self.p, 0), dt=torch.uint8)
+        self.ws_b = e(gdn.gdn_chunk_workspace_bytes(self.p, 1), dt=torch.uint8)
+        self.dq, self.dk = torch.empty_like(self.q), torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.v)
+        self.dg = e(T, HV)
+        self.dbeta = e(T, HV, dt=torch.bfloat16)
+        self.dh0 = e(N, HV, D, D)
+
+    def step(self, timer=None):
+        gdn, P = self.gdn, lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        s = self.torch.cuda.current_stream().cuda_stream
+        st = gdn.gdn_chunk_fwd(self.p, P(self.q), P(self.k), P(self.v), P(self.g), P(self.beta),
+                               P(self.h0), P(self.o), P(self.ht), P(self.saved), P(self.ws_f),
+                               self.ws_f.numel(), s, timer)
+        if st:
+            raise gdn.GdnError(st, "gdn_chunk_fwd")
+        st = gdn.gdn_chunk_bwd(self.p, P(self.q), P(self.k), P(self.v), P(self.g), P(self.beta),
+                               P(self.h0), P(self.saved), P(self.d_o), P(self.d_ht), P(self.dq),
+                               P(self.dk), P(self.dv), P(self.dg), P(self.dbeta), P(self.dh0),
+                               P(self.ws_b), self.ws_b.numel(), s, timer)
+        if st:
+            raise gdn.GdnError(st, "gdn_chunk_bwd")
+
+    def inputs(self):
+        return [x for x in (self.q, self.k, self.v, self.g, self.beta, self.h0, self.d_o, self.d_ht)
+                if x is not None]
+
+    def outputs(self):
+        return [self.o, self.ht, self.dq, self.dk, self.dv, self.dg, self.dbeta, self.dh0]
+
+
+def _time_loop(torch, fn, steps):
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def _kernel_table(torch, runner_step, steps, capacity):
+    from chunked_gated_delta_06_gb300.binding import KernelTimer
+    timer = KernelTimer(capacity)
+    per = {}
+    for _ in range(steps):
+        timer.reset()
+        runner_step(timer)
+        for name, ms in timer.records():
+            per.setdefault(name, []).append(ms)
+    return per
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, target_tokens):
+    """A bounded sample of a chunk workload: whole sequences in packing order until
+    target_tokens (the last one cut), every value head."""
+    from chunked_gated_delta_06_gb300 import workloads as W
+    cu = wl.cu_seqlens
+    lens, tot = [], 0
+    for n in range(wl.N):
+        L = int(cu[n + 1] - cu[n])
+        take = min(L, target_tokens - tot)
+        if take <= 0:
+            break
+        lens.append(take)
+        tot += take
+    idx = np.concatenate([np.arange(cu[n], cu[n] + lens[n]) for n in range(len(lens))])
+    return idx, lens
+
+
+def run_oracle_sample(wl, target_tokens, threads=None):
+    import oracle
+    idx, lens = oracle_sample(wl, target_tokens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    n = len(lens)
+    h0 = None if wl.h0 is None else wl.h0[:n]
+    d_ht = None if wl.d_ht is None else wl.d_ht[:n]
+    q, k, v, g, beta, d_o = wl.q[idx], wl.k[idx], wl.v[idx], wl.g[idx], wl.beta[idx], wl.d_o[idx]
+    threads = threads or os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, g, beta, cu, h0=h0, threads=threads)
+    oracle.bwd(q, k, v, g, beta, cu, d_o, d_ht=d_ht, h0=h0, threads=threads)
+    dt = time.perf_counter() - t0
+    return int(cu[-1]), dt, threads, min(threads, n * wl.HV)
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def bench_reference(args):
+    """The oracle (fp64 CPU) on the same workload, metric and unit."""
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from chunked_gated_delta_06_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    wl = W.fb_32k_varlen(seed=0)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        tok, dt, thr, used = run_oracle_sample(wl, args.ref_tokens)
+        if i >= args.warmup:
+            vals.append(tok / dt)
+    v = statistics.median(vals)
+    sample = ("first %d tokens of the packed fb_32k_varlen workload (whole sequences in packing "
+              "order, last cut), all 32 value heads, fwd+bwd per step" % args.ref_tokens)
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 32768 / v * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": "fb_32k_varlen", "T": 32768, "H": 16, "HV": 32, "K": 128,
+                       "V": 128, "chunk": 64, "parallelism": "replicas"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- main bench
+def bench_ours(args):
+    import torch
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    from chunked_gated_delta_06_gb300 import build as B
+    B.build()
+    from chunked_gated_delta_06_gb300 import workloads as W
+    peaks = _peaks()
+
+    wl = W.fb_32k_varlen(seed=rank)
+    T, H, HV, N = wl.T, wl.H, wl.HV, wl.N
+    C_total = int(sum((int(wl.cu_seqlens[i + 1] - wl.cu_seqlens[i]) + C - 1) // C for i in range(N)))
+    run = ChunkRunner(torch, wl, dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        run.step()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = _time_loop(torch, run.step, args.steps)
+    clk = clocks.stop()
+    barrier()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = T * world / (ms / 1e3)
+
+    # per-kernel durations (same steps with the kernel timer), launches per step
+    per = _kernel_table(torch, run.step, max(3, min(args.steps, 10)), 64)
+    launches_per_step = sum(len(v) for v in per.values()) // max(3, min(args.steps, 10))
+    ktab = {k: {"ms": statistics.mean(v), "launches_per_step": len(v) // max(3, min(args.steps, 10))}
+            for k, v in per.items()}
+    dom = max(ktab, key=lambda k: ktab[k]["ms"] * ktab[k]["launches_per_step"])
+    fl, by = kernel_work(dom, T, H, HV, N, C_total)
+    dur = ktab[dom]["ms"] / 1e3
+    simt = True  # the chunk kernels of this build run on CUDA cores (fp32 FMA)
+    if fl > 0:
+        roof = {"kernel": dom, "bound": "alu" if simt else "tensor",
+                "achieved": fl / dur / 1e12,
+                "peak": FP32_SIMT_TFLOPS if simt else peaks["bf16_sustained"],
+                "unit": "TFLOP/s", "traffic": None,
+                "peak_source": ("fp32 CUDA-core peak from unit counts and the max SM clock"
+                                if simt else "bf16_tflops_sustained of %s" % peaks["source"]),
+                "algorithmic_flops": fl}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": by / dur / 1e9, "peak": peaks["hbm"],
+                "unit": "GB/s", "traffic": None,
+                "peak_source": "hbm_gbs of %s" % peaks["source"], "algorithmic_bytes": by}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    for k in ktab:
+        f_, b_ = kernel_work(k, T, H, HV, N, C_total)
+        ktab[k]["tflops"] = f_ / (ktab[k]["ms"] / 1e3) / 1e12 if f_ else None
+        ktab[k]["gbs"] = b_ / (ktab[k]["ms"] / 1e3) / 1e9 if b_ else None
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "fb_32k_varlen", "T": T, "num_seqs": N, "H": H, "HV": HV,
+                       "K": D, "V": D, "chunk": C, "chunks": C_total,
+                       "step": "gdn_chunk_fwd (saving for backward) + gdn_chunk_bwd",
+                       "l2": "inputs larger than L2 (q,k,v,dO = %.0f MB)" % (
+                           (2 * T * H + 2 * T * HV) * D * 2 / 1e6),
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "roofline": roof, "kernels": ktab, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk}
+
+    # decode state bandwidth
+    if not args.no_decode:
+        dw = W.decode_workload(seed=rank)
+        pool = torch.from_numpy(dw.pool).to(dev)
+        qd, kd, vd = _bf(torch, dw.q_bits, dev), _bf(torch, dw.k_bits, dev), _bf(torch, dw.v_bits, dev)
+        gd, bd = torch.from_numpy(dw.g).to(dev), torch.from_numpy(dw.beta).to(dev)
+        idx = torch.from_numpy(dw.state_indices).to(dev)
+        od = torch.empty((dw.B, dw.HV, D), dtype=torch.bfloat16, device=dev)
+        import chunked_gated_delta_06_gb300 as gdn
+
+        def dstep(timer=None):
+            st = gdn.gdn_decode_step(dw.B, dw.H, dw.HV, D, D, 0.0, qd.data_ptr(), kd.data_ptr(),
+                                     vd.data_ptr(), gd.data_ptr(), bd.data_ptr(), pool.data_ptr(),
+                                     pool.shape[0], idx.data_ptr(), od.data_ptr(), None,
+                                     torch.cuda.current_stream().cuda_stream, timer)
+            if st:
+                raise gdn.GdnError(st, "gdn_decode_step")
+
+        for _ in range(max(3, args.warmup)):
+            dstep()
+        dsteps = max(args.steps, 20)
+        dms = _time_loop(torch, dstep, dsteps)
+        n_active = int((dw.state_indices > 0).sum())
+        nb = decode_bytes(n_active, dw.B, dw.H, dw.HV)
+        dper = _kernel_table(torch, dstep, 10, 4)
+        kms = statistics.mean(dper["decode"])
+        line["decode"] = {
+            "metric": "decode state GB/s", "value": nb / (dms / 1e3) / 1e9, "unit": "GB/s",
+            "ms_per_step": dms, "steps": dsteps,
+            "config": {"workload": "decode_256", "B": dw.B, "active": n_active, "H": dw.H,
+                       "HV": dw.HV, "pool": list(dw.pool.shape), "bytes_per_step": nb,
+                       "l2": "state pool (1.07 GB) larger than L2"},
+            "roofline": {"kernel": "decode", "bound": "hbm", "achieved": nb / (kms / 1e3) / 1e9,
+                         "peak": peaks["hbm"], "unit": "GB/s", "frac": nb / (kms / 1e3) / 1e9 / peaks["hbm"],
+                         "traffic": None, "peak_source": "hbm_gbs of %s" % peaks["source"]}}
+        del pool
+
+    # end to end through host buffers
+    if not args.no_e2e:
+        ins = run.inputs()
+        outs = run.outputs()
+        h_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x.cpu()) for x in ins]
+        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+
+        def e2e_step():
+            for d_, h_ in zip(ins, h_in):
+                d_.copy_(h_, non_blocking=True)
+            run.step()
+            for h_, d_ in zip(h_out, outs):
+                h_.copy_(d_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        ems = _time_loop(torch, e2e_step, max(3, min(args.steps, 10)))
+        line["e2e"] = {"value": T * world / (ems / 1e3), "unit": "tokens/s",
+                       "ms_per_step": ems,
+                       "h2d_bytes_per_step": int(sum(x.numel() * x.element_size() for x in ins)),
+                       "d2h_bytes_per_step": int(sum(x.numel() * x.element_size() for x in outs))}
+
+    # the oracle on the host cores (rank 0, single GPU only)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, dt, thr, used = run_oracle_sample(wl, args.ref_tokens)
+        line["cpu_baseline"] = {
+            "value": tok / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": "first %d tokens of the workload (whole sequences in packing order), all "
+                      "32 value heads, fwd+bwd, %.1f s on %d threads" % (tok, dt, used)}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=2048,
+                    help="tokens of the workload the oracle runs per baseline sample")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

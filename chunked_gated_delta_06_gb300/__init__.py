@@ -1,0 +1,12 @@
+"""Chunked gated delta rule (GDN) on NVIDIA GB300: a C-ABI CUDA library (libgdn.so,
+include/gdn.h) with a thin ctypes binding.
+
+    from chunked_gated_delta_06_gb300 import chunk_fwd, chunk_bwd, decode_step
+
+The library is loaded on first use; it must have been built with
+``python -m chunked_gated_delta_06_gb300.build``.
+"""
+from .binding import (GdnError, GdnProblem, chunk_bwd, chunk_fwd, decode_step,  # noqa: F401
+                      gdn_chunk_bwd, gdn_chunk_fwd, gdn_chunk_saved_bytes,
+                      gdn_chunk_workspace_bytes, gdn_decode_step, lib, make_problem,
+                      status_string)

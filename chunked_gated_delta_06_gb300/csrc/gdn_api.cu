@@ -1,0 +1,300 @@
+// gdn_api.cu -- the extern "C" entry points declared in include/gdn.h: host-side
+// validation (before any launch), carving of the caller's saved / workspace
+// buffers, and the launch order of the chunk and decode kernels.
+#include <math.h>
+#include <string.h>
+
+#include "../../include/gdn.h"
+#include "gdn_kernels.h"
+
+namespace {
+
+using gdn::bf16;
+constexpr size_t kAlign = 256;
+
+// Sequential sub-allocator over a caller buffer; with base == nullptr it only counts.
+struct Carver {
+    char *base;
+    size_t off = 0;
+    explicit Carver(void *b) : base(static_cast<char *>(b)) {}
+    template <typename T>
+    T *take(size_t count) {
+        off = (off + kAlign - 1) / kAlign * kAlign;
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+    size_t used() const { return (off + kAlign - 1) / kAlign * kAlign; }
+};
+
+struct Dims {
+    int N, T, H, HV, C;  // C = chunk count
+    float scale;
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status check_problem(const gdn_problem *p, Dims *d) {
+    if (!p) return GDN_ERR_INVALID_ARG;
+    if (p->num_seqs < 1 || p->total_tokens < 0 || p->total_tokens > 0x7fffffffLL)
+        return GDN_ERR_INVALID_ARG;
+    if (p->num_k_heads < 1 || p->num_v_heads < 1 || p->num_k_heads > 65535 ||
+        p->num_v_heads > 65535)
+        return GDN_ERR_INVALID_ARG;
+    if (p->head_dim_k != 128 || p->head_dim_v != 128) return GDN_ERR_UNSUPPORTED;
+    if (p->num_v_heads % p->num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+    if (!p->cu_seqlens_host || !p->cu_seqlens_dev) return GDN_ERR_INVALID_ARG;
+    const int32_t *cu = p->cu_seqlens_host;
+    if (cu[0] != 0 || (int64_t)cu[p->num_seqs] != p->total_tokens) return GDN_ERR_INVALID_ARG;
+    int64_t chunks = 0;
+    for (int n = 0; n < p->num_seqs; ++n) {
+        if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARG;
+        chunks += (cu[n + 1] - cu[n] + gdn::kChunk - 1) / gdn::kChunk;
+    }
+    d->N = p->num_seqs;
+    d->T = (int)p->total_tokens;
+    d->H = p->num_k_heads;
+    d->HV = p->num_v_heads;
+    d->C = (int)chunks;
+    d->scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->head_dim_k);
+    return GDN_OK;
+}
+
+// The tensors gdn_chunk_fwd keeps for gdn_chunk_bwd, in a fixed order.
+void carve_saved(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
+    const size_t D = gdn::kDim;
+    a.hc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
+    a.vnew = cv.take<bf16>((size_t)d.T * d.HV * D);
+    a.w = cv.take<bf16>((size_t)d.T * d.HV * D);
+    a.Tm = cv.take<float>((size_t)d.C * d.HV * gdn::kChunk * gdn::kChunk);
+    a.rq = cv.take<float>((size_t)d.T * d.H);
+    a.rk = cv.take<float>((size_t)d.T * d.H);
+    a.G = cv.take<float>((size_t)d.T * d.HV);
+}
+
+void carve_table(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
+    a.seq_chunk_off = cv.take<int>((size_t)d.N + 1);
+    a.chunk_seq = cv.take<int>((size_t)d.C);
+    a.chunk_start = cv.take<int>((size_t)d.C);
+    a.chunk_len = cv.take<int>((size_t)d.C);
+    a.status = cv.take<int>(1);
+}
+
+void carve_fwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a, bool with_saved) {
+    carve_table(cv, d, a);
+    a.u = cv.take<bf16>((size_t)d.T * d.HV * gdn::kDim);
+    if (with_saved) carve_saved(cv, d, a);
+}
+
+void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
+    const size_t D = gdn::kDim;
+    carve_table(cv, d, a);
+    a.dvloc = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dvnew = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dhc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
+    a.dW = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dqp = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dkp = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dGp = cv.take<float>((size_t)d.T * d.HV);
+}
+
+size_t saved_bytes(const Dims &d) {
+    Carver cv(nullptr);
+    gdn::ChunkArgs a{};
+    carve_saved(cv, d, a);
+    return cv.used();
+}
+
+size_t ws_bytes(const Dims &d, int for_backward) {
+    Carver cv(nullptr);
+    gdn::ChunkArgs a{};
+    if (for_backward) carve_bwd_ws(cv, d, a);
+    else carve_fwd_ws(cv, d, a, true);
+    return cv.used();
+}
+
+void fill_common(gdn::ChunkArgs &a, const Dims &d, const gdn_problem *p, const void *q,
+                 const void *k, const void *v, const float *g, const void *beta,
+                 const float *h0) {
+    a.N = d.N;
+    a.T = d.T;
+    a.H = d.H;
+    a.HV = d.HV;
+    a.num_chunks = d.C;
+    a.scale = d.scale;
+    a.q = static_cast<const bf16 *>(q);
+    a.k = static_cast<const bf16 *>(k);
+    a.v = static_cast<const bf16 *>(v);
+    a.g = g;
+    a.beta = static_cast<const bf16 *>(beta);
+    a.h0 = h0;
+    a.cu_dev = p->cu_seqlens_dev;
+}
+
+gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: K and V must be 128 and HV % H == 0";
+        case GDN_ERR_WORKSPACE_TOO_SMALL: return "GDN_ERR_WORKSPACE_TOO_SMALL: workspace below the size query";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA launch failed";
+    }
+    return "unknown gdn_status";
+}
+
+size_t gdn_chunk_saved_bytes(const gdn_problem *p) {
+    Dims d;
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    return saved_bytes(d);
+}
+
+size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward) {
+    Dims d;
+    if (check_problem(p, &d) != GDN_OK) return 0;
+    return ws_bytes(d, for_backward);
+}
+
+gdn_status gdn_chunk_fwd_timed(const gdn_problem *p, const void *q, const void *k,
+                               const void *v, const float *g, const void *beta,
+                               const float *initial_state, void *o, float *final_state,
+                               void *saved, void *workspace, size_t ws_size,
+                               gdn_stream_t stream, gdn_kernel_timer *timer) {
+    Dims d;
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    if (d.T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, initial_state, o, final_state, saved, workspace};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+        (saved && (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0))
+        return GDN_ERR_INVALID_ARG;
+    if (ws_size < ws_bytes(d, 0)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    gdn::ChunkArgs a{};
+    fill_common(a, d, p, q, k, v, g, beta, initial_state);
+    a.timer = timer;
+    a.o = static_cast<bf16 *>(o);
+    a.ht = final_state;
+    Carver wc(workspace);
+    carve_fwd_ws(wc, d, a, saved == nullptr);
+    if (saved) {
+        Carver sc(saved);
+        carve_saved(sc, d, a);
+    }
+    cudaError_t e;
+    if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = gdn::launch_fwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_bwd_timed(const gdn_problem *p, const void *q, const void *k,
+                               const void *v, const float *g, const void *beta,
+                               const float *initial_state, const void *saved, const void *d_o,
+                               const float *d_final_state, void *dq, void *dk, void *dv,
+                               float *dg, void *dbeta, float *dh0, void *workspace,
+                               size_t ws_size, gdn_stream_t stream, gdn_kernel_timer *timer) {
+    Dims d;
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    if (!saved) return GDN_ERR_INVALID_ARG;
+    if (d.T > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta))
+        return GDN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, initial_state, saved, d_o, d_final_state, dq, dk, dv, dh0,
+                          workspace};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+        (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0)
+        return GDN_ERR_INVALID_ARG;
+    if (ws_size < ws_bytes(d, 1)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    gdn::ChunkArgs a{};
+    fill_common(a, d, p, q, k, v, g, beta, initial_state);
+    a.timer = timer;
+    Carver sc(const_cast<void *>(saved));
+    carve_saved(sc, d, a);
+    Carver wc(workspace);
+    carve_bwd_ws(wc, d, a);
+    a.d_o = static_cast<const bf16 *>(d_o);
+    a.d_ht = d_final_state;
+    a.dq = static_cast<bf16 *>(dq);
+    a.dk = static_cast<bf16 *>(dk);
+    a.dv = static_cast<bf16 *>(dv);
+    a.dbeta = static_cast<bf16 *>(dbeta);
+    a.dg = dg;
+    a.dh0 = dh0;
+    cudaError_t e;
+    if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = gdn::launch_bwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
+    return GDN_OK;
+}
+
+gdn_status gdn_decode_step_timed(int32_t batch, int32_t num_k_heads, int32_t num_v_heads,
+                                 int32_t head_dim_k, int32_t head_dim_v, float scale,
+                                 const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, float *state_pool, int32_t num_slots,
+                                 const int32_t *state_indices, void *o, int32_t *device_status,
+                                 gdn_stream_t stream, gdn_kernel_timer *timer) {
+    if (batch < 0 || num_k_heads < 1 || num_v_heads < 1 || num_slots < 1)
+        return GDN_ERR_INVALID_ARG;
+    if (head_dim_k != 128 || head_dim_v != 128) return GDN_ERR_UNSUPPORTED;
+    if (num_v_heads % num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)batch * num_v_heads > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+    if (batch == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state_pool || !state_indices || !o)
+        return GDN_ERR_INVALID_ARG;
+    if (!aligned16(state_pool)) return GDN_ERR_INVALID_ARG;
+    const float s = scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim_k);
+    cudaError_t e = gdn::launch_decode(
+        batch, num_k_heads, num_v_heads, s, static_cast<const bf16 *>(q),
+        static_cast<const bf16 *>(k), static_cast<const bf16 *>(v), g, beta, state_pool, num_slots,
+        state_indices, static_cast<bf16 *>(o), device_status,
+        reinterpret_cast<cudaStream_t>(stream), timer);
+    return cuda_status(e);
+}
+
+gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g, const void *beta, const float *initial_state, void *o,
+                         float *final_state, void *saved, void *workspace, size_t ws_size,
+                         gdn_stream_t stream) {
+    return gdn_chunk_fwd_timed(p, q, k, v, g, beta, initial_state, o, final_state, saved,
+                               workspace, ws_size, stream, nullptr);
+}
+
+gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g, const void *beta, const float *initial_state,
+                         const void *saved, const void *d_o, const float *d_final_state,
+                         void *dq, void *dk, void *dv, float *dg, void *dbeta, float *dh0,
+                         void *workspace, size_t ws_size, gdn_stream_t stream) {
+    return gdn_chunk_bwd_timed(p, q, k, v, g, beta, initial_state, saved, d_o, d_final_state,
+                               dq, dk, dv, dg, dbeta, dh0, workspace, ws_size, stream, nullptr);
+}
+
+gdn_status gdn_decode_step(int32_t batch, int32_t num_k_heads, int32_t num_v_heads,
+                           int32_t head_dim_k, int32_t head_dim_v, float scale, const void *q,
+                           const void *k, const void *v, const float *g, const float *beta,
+                           float *state_pool, int32_t num_slots, const int32_t *state_indices,
+                           void *o, int32_t *device_status, gdn_stream_t stream) {
+    return gdn_decode_step_timed(batch, num_k_heads, num_v_heads, head_dim_k, head_dim_v, scale,
+                                 q, k, v, g, beta, state_pool, num_slots, state_indices, o,
+                                 device_status, stream, nullptr);
+}
+
+const char *gdn_kernel_name(int32_t id) {
+    static const char *names[GDN_KERNEL_COUNT] = {
+        "plan", "prep", "intra", "state", "out", "dvloc", "bstate", "bintra_a", "bintra_b",
+        "bnorm", "decode"};
+    return (id >= 0 && id < GDN_KERNEL_COUNT) ? names[id] : "unknown";
+}
+
+}  // extern "C"

@@ -1,0 +1,33 @@
+// gdn_common.cuh -- small device helpers shared by the libgdn kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kChunk = 64;   // chunk length C
+constexpr int kDim = 128;    // K = V = 128
+constexpr float kNormEps = 1e-6f;
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ float bf2f(bf16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ bf16 f2bf(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Chunk table built on the device from cu_seqlens (see k_plan).
+struct ChunkTable {
+    const int *seq_chunk_off;  // [N+1] first chunk of each sequence
+    const int *chunk_seq;      // [C_total] sequence of each chunk
+    const int *chunk_start;    // [C_total] first token (packed index)
+    const int *chunk_len;      // [C_total] 1..64
+};
+
+}  // namespace gdn

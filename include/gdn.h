@@ -1,0 +1,205 @@
+/*
+ * gdn.h -- C ABI of libgdn: the chunked gated delta rule (GDN) forward and
+ * backward over packed variable-length sequences, and the single-token decode
+ * step over a slot-indexed state pool, on NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  Per sequence n and value head hv, with key head
+ * h = hv / (HV / H):
+ *     qhat_t = scale * q_t / sqrt(sum_i q_{t,i}^2 + 1e-6)
+ *     khat_t =         k_t / sqrt(sum_i k_{t,i}^2 + 1e-6)     (k is never scaled)
+ *     S_t    = exp(g_t) S_{t-1} (I - beta_t khat_t khat_t^T) + beta_t v_t khat_t^T
+ *     o_t    = S_t qhat_t
+ * with S (V x K) starting from the transpose of initial_state[n, hv] (or 0).
+ * Sources (page title, section):
+ *   - "cake_gdn: deterministic chunked GDN training kernels" (miles #3597),
+ *     Summary: chunk 64, K = V = 128, in-kernel q/k L2 norm, cu_seqlens
+ *     packing, per-chunk state h stored in bf16 with an fp32 running state,
+ *     reductions without device atomics (bit-identical repeats).
+ *   - "[Cake 1/13] gdn: chunked gated delta rule, det and fast, with KCP and
+ *     FLA-CP" (miles-ext-kernels #1), API and flags: q/k [B,T,H,K],
+ *     v [B,T,HV,V], HV % H == 0, bf16 q/k/v, packed varlen B = 1, fp32
+ *     initial/final state [N,HV,K,V], host cu_seqlens with no device-to-host
+ *     sync, a call without tokens passes the state through; extents checked
+ *     before any launch.
+ *   - "C6: GDN decode-step goldens and recurrent/conv state contract"
+ *     (RL-Kernel #469), What / Provider: the L2 norm divides by the sqrt,
+ *     scale multiplies q after the norm, key head = hv // (HV // H), state pool
+ *     [num_blocks, HV, V, K] addressed by ssm_state_indices, every index <= 0
+ *     is skipped and its output row written as zeros, fp32 accumulator.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are dense, row-major, on the device of the current CUDA
+ *     context, except cu_seqlens_host (host memory).  bf16 = IEEE bfloat16 bits.
+ *   - Calls are asynchronous and ordered on `stream`.  The library allocates
+ *     no memory, keeps no pointer after it returns and has no global mutable
+ *     state; the caller owns every buffer.
+ *   - Arguments are validated on the host before any launch; an invalid call
+ *     returns an error and launches nothing.  GDN_ERR_CUDA reports a failed
+ *     launch (cudaGetLastError) and may leave outputs partly written.
+ *   - Results are deterministic: the same inputs give the same bits on any
+ *     stream and in any process (no device atomics, fixed reduction orders).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL = the legacy default stream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,          /* null pointer, bad extents, bad cu_seqlens */
+    GDN_ERR_UNSUPPORTED = 2,          /* K or V != 128, HV % H != 0 */
+    GDN_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below the size query */
+    GDN_ERR_CUDA = 4                  /* a CUDA launch or call failed */
+} gdn_status;
+
+/* A packed variable-length problem (B = 1).  Sequence n holds tokens
+ * [cu[n], cu[n+1]) of the packed arrays.  Chunks of 64 tokens never span two
+ * sequences; the last chunk of a sequence may be partial. */
+typedef struct {
+    int32_t num_seqs;                 /* N >= 1 */
+    int64_t total_tokens;             /* T >= 0, T == cu[N]; T < 2^31 */
+    int32_t num_k_heads;              /* H >= 1 */
+    int32_t num_v_heads;              /* HV >= 1, HV % H == 0 */
+    int32_t head_dim_k;               /* K, must be 128 */
+    int32_t head_dim_v;               /* V, must be 128 */
+    float scale;                      /* > 0, or <= 0 to select 1/sqrt(K) */
+    const int32_t *cu_seqlens_host;   /* host [N+1]: 0 = c0 <= c1 <= ... <= cN = T */
+    const int32_t *cu_seqlens_dev;    /* device [N+1], the same values */
+} gdn_problem;
+
+/* Bytes of the `saved` buffer gdn_chunk_fwd fills for gdn_chunk_bwd (per-chunk
+ * states in bf16, the WY matrices, v_new and the norm / gate prefix sums).
+ * Returns 0 for an invalid problem.  Pure host function. */
+size_t gdn_chunk_saved_bytes(const gdn_problem *p);
+
+/* Bytes of scratch the calls need.  for_backward = 0: gdn_chunk_fwd (this
+ * includes room for the saved tensors, used when `saved` is NULL);
+ * for_backward = 1: gdn_chunk_bwd.  Returns 0 for an invalid problem. */
+size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward);
+
+/* Forward of chunk_gated_delta_rule.
+ *   q, k           bf16 [T, H, 128]
+ *   v              bf16 [T, HV, 128]
+ *   g              fp32 [T, HV]  log decay per token and value head
+ *   beta           bf16 [T, HV]
+ *   initial_state  fp32 [N, HV, 128(K), 128(V)] K-major, or NULL for zeros
+ *   o              bf16 [T, HV, 128]           (out)
+ *   final_state    fp32 [N, HV, 128, 128] (out), or NULL
+ *   saved          gdn_chunk_saved_bytes() bytes (out), or NULL when no
+ *                  backward follows
+ *   workspace      ws_bytes >= gdn_chunk_workspace_bytes(p, 0), 256-byte aligned
+ * T == 0 writes final_state = initial_state (or zeros) and nothing else. */
+gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g, const void *beta, const float *initial_state,
+                         void *o, float *final_state, void *saved, void *workspace,
+                         size_t ws_bytes, gdn_stream_t stream);
+
+/* Backward of chunk_gated_delta_rule.  q ... initial_state exactly as passed
+ * to the gdn_chunk_fwd that filled `saved` (not modified since).
+ *   d_o            bf16 [T, HV, 128]
+ *   d_final_state  fp32 [N, HV, 128, 128], or NULL for zeros
+ *   dq, dk         bf16 [T, H, 128]   (out; summed over the HV/H value heads)
+ *   dv             bf16 [T, HV, 128]  (out)
+ *   dg             fp32 [T, HV]       (out)
+ *   dbeta          bf16 [T, HV]       (out)
+ *   dh0            fp32 [N, HV, 128, 128] (out), or NULL
+ *   workspace      ws_bytes >= gdn_chunk_workspace_bytes(p, 1), 256-byte aligned
+ * The reverse state recurrence follows "Qwen3.5-397B RL trainer on 128 v7x"
+ * (maxtext #5799), GDN context-parallel dh-scan commit. */
+gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                         const float *g, const void *beta, const float *initial_state,
+                         const void *saved, const void *d_o, const float *d_final_state,
+                         void *dq, void *dk, void *dv, float *dg, void *dbeta, float *dh0,
+                         void *workspace, size_t ws_bytes, gdn_stream_t stream);
+
+/* One decode token per row over a slot-indexed fp32 state pool
+ * ("C6: GDN decode-step goldens ...", Provider and State contract).
+ *   q, k           bf16 [batch, H, K]
+ *   v              bf16 [batch, HV, V]
+ *   g, beta        fp32 [batch, HV]
+ *   state_pool     fp32 [num_slots, HV, V, K] (V-major: row v of S holds K
+ *                  floats), updated in place
+ *   state_indices  int32 [batch] on the device: the slot of each row; a slot
+ *                  <= 0 is null: the row is skipped, its output row is zeros
+ *                  and no slot is touched
+ *   o              bf16 [batch, HV, V] (out)
+ *   device_status  int32 on the device, or NULL: set to 1 when a row's slot
+ *                  was >= num_slots (that row is then treated as null)
+ * Two active rows naming the same slot race (undefined result): a caller error.
+ * K and V must be 128. */
+gdn_status gdn_decode_step(int32_t batch, int32_t num_k_heads, int32_t num_v_heads,
+                           int32_t head_dim_k, int32_t head_dim_v, float scale,
+                           const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float *state_pool, int32_t num_slots,
+                           const int32_t *state_indices, void *o, int32_t *device_status,
+                           gdn_stream_t stream);
+
+/* Optional per-kernel timing, for profiling tools and benchmarks.  The caller
+ * creates `capacity` pairs of CUDA events (cudaEvent_t, passed as void*) and
+ * passes the struct to a *_timed entry point; the library records
+ * start_events[i] / stop_events[i] on `stream` around the i-th kernel it
+ * launches, stores that kernel's id (GDN_KERNEL_*) in kernel_ids[i] and the
+ * number of pairs used in `count`.  Launches past `capacity` are not timed.
+ * Recording adds one event pair per launch; results are unchanged. */
+typedef struct {
+    int32_t capacity;
+    int32_t count;           /* out */
+    void **start_events;     /* cudaEvent_t[capacity] */
+    void **stop_events;      /* cudaEvent_t[capacity] */
+    int32_t *kernel_ids;     /* out, [capacity] */
+} gdn_kernel_timer;
+
+enum {
+    GDN_KERNEL_PLAN = 0,     /* chunk table from cu_seqlens */
+    GDN_KERNEL_PREP,         /* q/k norms, chunk-local cumsum of g */
+    GDN_KERNEL_INTRA,        /* WY pass: A, (I + A)^-1, w, u */
+    GDN_KERNEL_STATE,        /* forward state scan: v_new, per-chunk h, final state */
+    GDN_KERNEL_OUT,          /* output o */
+    GDN_KERNEL_DVLOC,        /* backward: tril(Qhat Khat^T (.) decay)^T dO */
+    GDN_KERNEL_BSTATE,       /* backward reverse state scan: dh, dv_new, dh0 */
+    GDN_KERNEL_BINTRA_A,     /* backward: terms through h and dh */
+    GDN_KERNEL_BINTRA_B,     /* backward: intra-chunk terms, WY pullback, dg */
+    GDN_KERNEL_BNORM,        /* backward: sum over value heads, L2-norm backward */
+    GDN_KERNEL_DECODE,       /* decode step */
+    GDN_KERNEL_COUNT
+};
+
+/* Name of a GDN_KERNEL_* id ("unknown" otherwise). */
+const char *gdn_kernel_name(int32_t kernel_id);
+
+/* gdn_chunk_fwd / gdn_chunk_bwd / gdn_decode_step with a kernel timer
+ * (timer may be NULL, then identical to the plain call). */
+gdn_status gdn_chunk_fwd_timed(const gdn_problem *p, const void *q, const void *k,
+                               const void *v, const float *g, const void *beta,
+                               const float *initial_state, void *o, float *final_state,
+                               void *saved, void *workspace, size_t ws_bytes,
+                               gdn_stream_t stream, gdn_kernel_timer *timer);
+gdn_status gdn_chunk_bwd_timed(const gdn_problem *p, const void *q, const void *k,
+                               const void *v, const float *g, const void *beta,
+                               const float *initial_state, const void *saved, const void *d_o,
+                               const float *d_final_state, void *dq, void *dk, void *dv,
+                               float *dg, void *dbeta, float *dh0, void *workspace,
+                               size_t ws_bytes, gdn_stream_t stream, gdn_kernel_timer *timer);
+gdn_status gdn_decode_step_timed(int32_t batch, int32_t num_k_heads, int32_t num_v_heads,
+                                 int32_t head_dim_k, int32_t head_dim_v, float scale,
+                                 const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, float *state_pool, int32_t num_slots,
+                                 const int32_t *state_indices, void *o, int32_t *device_status,
+                                 gdn_stream_t stream, gdn_kernel_timer *timer);
+
+/* A static, human-readable name of a status code. */
+const char *gdn_status_string(gdn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,119 @@
+"""Host-only checks of the C ABI: the library loads, exports every function
+include/gdn.h declares, sizes its buffers as documented and rejects invalid
+arguments before any CUDA call (no GPU needed: no call here reaches a launch)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import chunked_gated_delta_06_gb300 as gdn
+from chunked_gated_delta_06_gb300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def test_library_exports_every_declared_function(lib):
+    names = binding.header_functions()
+    assert {"gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_decode_step", "gdn_chunk_saved_bytes",
+            "gdn_chunk_workspace_bytes", "gdn_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert gdn.status_string(s).startswith("GDN_")
+    assert "unknown" in gdn.status_string(99)
+
+
+def _problem(cu, H=2, HV=4, K=128, V=128, scale=0.0, dev=0x1000):
+    return binding.make_problem(cu, H, HV, K, V, scale, cu_dev_ptr=dev)
+
+
+def test_saved_and_workspace_sizes(lib):
+    cu = [0, 1, 64, 200]  # chunks: 1 + 1 + 3 = 5
+    p, keep = _problem(cu)
+    T, H, HV, C = 200, 2, 4, 5
+    D = 128
+
+    def al(x):
+        return (x + 255) // 256 * 256
+    saved = (al(C * HV * D * D * 2) + al(T * HV * D * 2) + al(T * HV * D * 2)
+             + al(C * HV * 64 * 64 * 4) + al(T * H * 4) + al(T * H * 4) + al(T * HV * 4))
+    assert gdn.gdn_chunk_saved_bytes(p) == saved
+    fwd_ws = gdn.gdn_chunk_workspace_bytes(p, 0)
+    assert fwd_ws >= saved + T * HV * D * 2
+    bwd_ws = gdn.gdn_chunk_workspace_bytes(p, 1)
+    assert bwd_ws >= 5 * T * HV * D * 4 + C * HV * D * D * 2
+
+
+@pytest.mark.parametrize("mut, status", [
+    (dict(K=64), binding.GDN_ERR_UNSUPPORTED),
+    (dict(V=256), binding.GDN_ERR_UNSUPPORTED),
+    (dict(H=3, HV=4), binding.GDN_ERR_UNSUPPORTED),
+    (dict(cu=[0, 5, 3]), binding.GDN_ERR_INVALID_ARG),
+    (dict(cu=[1, 5]), binding.GDN_ERR_INVALID_ARG),
+    (dict(dev=0), binding.GDN_ERR_INVALID_ARG),
+])
+def test_invalid_problems_are_rejected_before_any_launch(lib, mut, status):
+    kw = dict(cu=[0, 5, 9], H=2, HV=4, K=128, V=128, dev=0x1000)
+    kw.update(mut)
+    p, keep = _problem(kw.pop("cu"), **kw)
+    assert gdn.gdn_chunk_saved_bytes(p) == 0
+    assert gdn.gdn_chunk_workspace_bytes(p, 0) == 0
+    fake = 0x10000  # never dereferenced: validation fails first
+    st = gdn.gdn_chunk_fwd(p, fake, fake, fake, fake, fake, None, fake, None, None, fake, 1 << 40, None)
+    assert st == status
+    st = gdn.gdn_chunk_bwd(p, fake, fake, fake, fake, fake, None, fake, fake, None, fake, fake, fake,
+                           fake, fake, None, fake, 1 << 40, None)
+    assert st == status
+
+
+def test_missing_buffers_are_rejected(lib):
+    p, keep = _problem([0, 5])
+    fake = 0x10000
+    # null q
+    assert gdn.gdn_chunk_fwd(p, None, fake, fake, fake, fake, None, fake, None, None, fake, 1 << 40,
+                             None) == binding.GDN_ERR_INVALID_ARG
+    # misaligned workspace
+    assert gdn.gdn_chunk_fwd(p, fake, fake, fake, fake, fake, None, fake, None, None, fake + 16,
+                             1 << 40, None) == binding.GDN_ERR_INVALID_ARG
+    # workspace too small
+    assert gdn.gdn_chunk_fwd(p, fake, fake, fake, fake, fake, None, fake, None, None, fake, 1024,
+                             None) == binding.GDN_ERR_WORKSPACE_TOO_SMALL
+    # backward without the saved buffer
+    assert gdn.gdn_chunk_bwd(p, fake, fake, fake, fake, fake, None, None, fake, None, fake, fake,
+                             fake, fake, fake, None, fake, 1 << 40, None) == binding.GDN_ERR_INVALID_ARG
+    # null problem
+    assert lib.gdn_chunk_saved_bytes(None) == 0
+
+
+def test_decode_argument_checks(lib):
+    fake = 0x10000
+    args = dict(batch=4, H=2, HV=4, K=128, V=128, scale=0.0)
+
+    def call(**over):
+        a = dict(args); a.update(over)
+        return gdn.gdn_decode_step(a["batch"], a["H"], a["HV"], a["K"], a["V"], a["scale"], fake, fake,
+                                   fake, fake, fake, a.get("pool", fake), a.get("slots", 8),
+                                   a.get("idx", fake), fake, None, None)
+    assert call(K=64) == binding.GDN_ERR_UNSUPPORTED
+    assert call(H=3) == binding.GDN_ERR_UNSUPPORTED
+    assert call(batch=-1) == binding.GDN_ERR_INVALID_ARG
+    assert call(slots=0) == binding.GDN_ERR_INVALID_ARG
+    assert call(idx=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(pool=fake + 4) == binding.GDN_ERR_INVALID_ARG
+    assert call(batch=0) == binding.GDN_OK  # nothing to do, nothing launched
+
+
+def test_problem_struct_layout_matches_the_header(lib):
+    # int32, int64, 4 x int32, float, 2 pointers: offsets as a C compiler lays them out
+    P = binding.GdnProblem
+    assert P.total_tokens.offset == 8
+    assert P.scale.offset == 32
+    assert P.cu_seqlens_host.offset == 40
+    assert ctypes.sizeof(P) == 56

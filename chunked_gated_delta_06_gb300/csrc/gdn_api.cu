@@ -90,7 +90,7 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     const size_t D = gdn::kDim;
     carve_table(cv, d, a);
     a.dvloc = cv.take<float>((size_t)d.T * d.HV * D);
-    a.dvnew = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dvnew = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dhc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
     a.dW = cv.take<float>((size_t)d.T * d.HV * D);
     a.dqp = cv.take<float>((size_t)d.T * d.HV * D);
@@ -205,7 +205,7 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem *p, const void *q, const void *
     Dims d;
     gdn_status st = check_problem(p, &d);
     if (st != GDN_OK) return st;
-    if (!saved) return GDN_ERR_INVALID_ARG;
+    if (!saved && saved_bytes(d) > 0) return GDN_ERR_INVALID_ARG;  // T == 0 saves nothing
     if (d.T > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta))
         return GDN_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, initial_state, saved, d_o, d_final_state, dq, dk, dv, dh0,

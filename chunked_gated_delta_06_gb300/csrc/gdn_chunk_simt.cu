@@ -29,7 +29,7 @@ constexpr int kSlab = 32;
 // ---------------------------------------------------------------------------
 // Chunk table from the device cu_seqlens (one block).  Host code computed the
 // chunk count from the host copy; a mismatch sets *status.
-__global__ void k_plan(const int *__restrict__ cu, int N, int total_chunks, int *seq_off,
+__global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunks, int *seq_off,
                        int *chunk_seq, int *chunk_start, int *chunk_len, int *status) {
     __shared__ int sums[1024];
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -52,17 +52,24 @@ __global__ void k_plan(const int *__restrict__ cu, int N, int total_chunks, int 
         for (int j = 0; j * kChunk < L; ++j) {
             int c = base + j;
             if (c < total_chunks) {
+                // clamp to [0, T): a device copy of cu_seqlens that disagrees with
+                // the host copy yields empty chunks and a status flag, never an
+                // out-of-bounds access
+                const int st = min(max(cu[n] + j * kChunk, 0), T);
                 chunk_seq[c] = n;
-                chunk_start[c] = cu[n] + j * kChunk;
-                chunk_len[c] = min(kChunk, L - j * kChunk);
+                chunk_start[c] = st;
+                chunk_len[c] = max(0, min(min(kChunk, L - j * kChunk), T - st));
             }
         }
         base += (L + kChunk - 1) / kChunk;
     }
+    __syncthreads();
     if (tid == nt - 1) {
-        seq_off[N] = sums[tid];
-        if (status) *status = (sums[tid] != total_chunks) ? 1 : 0;
+        seq_off[N] = min(sums[tid], total_chunks);
+        if (status) *status = (sums[tid] != total_chunks || cu[N] != T) ? 1 : 0;
     }
+    // keep every sequence's chunk range inside [0, total_chunks]
+    for (int n = b; n < e; ++n) seq_off[n] = min(seq_off[n], total_chunks);
 }
 
 // ---------------------------------------------------------------------------
@@ -70,6 +77,7 @@ __global__ void k_plan(const int *__restrict__ cu, int N, int total_chunks, int 
 __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
     const int c = blockIdx.x, h = blockIdx.y;
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
+    if (L <= 0) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = warp; i < L; i += kThreads / 32) {
         const size_t row = ((size_t)(t0 + i) * a.H + h) * kDim;
@@ -134,6 +142,7 @@ __global__ void __launch_bounds__(kThreads) k_intra(ChunkArgs a) {
     float *ws = bs + kChunk;
     const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
+    if (L <= 0) return;
     const int r = a.HV / a.H;
     load_rows_norm(Kn, a.k, a.rk, t0, L, a.H, h, 1.f);
     __syncthreads();
@@ -192,63 +201,6 @@ __global__ void __launch_bounds__(kThreads) k_intra(ChunkArgs a) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// Forward state scan.  grid (N, HV, V / 32): one 128 x 32 slab of the fp32
-// state per block, sequential over the sequence's chunks.
-__global__ void __launch_bounds__(kThreads) k_state(ChunkArgs a) {
-    extern __shared__ float sm[];
-    float *hs = sm;                 // [128][33]
-    float *vn = hs + kDim * 33;     // [64][33]
-    float *kt = vn + kChunk * 33;   // [64][129]
-    const int n = blockIdx.x, hv = blockIdx.y, v0 = blockIdx.z * kSlab, tid = threadIdx.x;
-    const int h = hv / (a.HV / a.H);
-    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim;
-    for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-        int r = idx >> 5, j = idx & 31;
-        hs[r * 33 + j] = a.h0 ? a.h0[sbase + (size_t)r * kDim + v0 + j] : 0.f;
-    }
-    __syncthreads();
-    const int cb = a.seq_chunk_off[n], ce = a.seq_chunk_off[n + 1];
-    for (int c = cb; c < ce; ++c) {
-        const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-        bf16 *hdst = a.hc + ((size_t)c * a.HV + hv) * kDim * kDim;
-        for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-            int r = idx >> 5, j = idx & 31;
-            hdst[(size_t)r * kDim + v0 + j] = f2bf(hs[r * 33 + j]);
-        }
-        for (int idx = tid; idx < L * kSlab; idx += kThreads) {
-            int i = idx >> 5, j = idx & 31;
-            size_t row = ((size_t)(t0 + i) * a.HV + hv) * kDim;
-            float s = bf2f(a.u[row + v0 + j]);
-            for (int e = 0; e < kDim; ++e) s -= bf2f(a.w[row + e]) * hs[e * 33 + j];
-            vn[i * 33 + j] = s;
-            a.vnew[row + v0 + j] = f2bf(s);
-        }
-        const float Gl = a.G[(size_t)(t0 + L - 1) * a.HV + hv];
-        for (int idx = tid; idx < L * kDim; idx += kThreads) {
-            int i = idx >> 7, e = idx & 127;
-            size_t t = (size_t)(t0 + i) * a.H + h;
-            kt[i * kP + e] = expf(Gl - a.G[(size_t)(t0 + i) * a.HV + hv]) / a.rk[t] *
-                             bf2f(a.k[t * kDim + e]);
-        }
-        __syncthreads();
-        const float egl = expf(Gl);
-        for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-            int r = idx >> 5, j = idx & 31;
-            float s = egl * hs[r * 33 + j];
-            for (int i = 0; i < L; ++i) s += kt[i * kP + r] * vn[i * 33 + j];
-            hs[r * 33 + j] = s;
-        }
-        __syncthreads();
-    }
-    if (a.ht) {
-        for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-            int r = idx >> 5, j = idx & 31;
-            a.ht[sbase + (size_t)r * kDim + v0 + j] = hs[r * 33 + j];
-        }
-    }
-}
-
 // M[i][j] = (Qn_i . Kn_j) exp(G_i - G_j) for j <= i < L, else 0.
 __device__ void build_M(float *M, const float *Qn, const float *Kn, const float *Gs, int L) {
     for (int idx = threadIdx.x; idx < kChunk * kChunk; idx += kThreads) {
@@ -274,6 +226,7 @@ __global__ void __launch_bounds__(kThreads) k_out(ChunkArgs a) {
     const int c = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
     const int h = hv / (a.HV / a.H);
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
+    if (L <= 0) return;
     load_rows_norm(Qn, a.q, a.rq, t0, L, a.H, h, a.scale);
     load_rows_norm(Kn, a.k, a.rk, t0, L, a.H, h, 1.f);
     for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
@@ -307,6 +260,7 @@ __global__ void __launch_bounds__(kThreads) k_dvloc(ChunkArgs a) {
     const int c = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
     const int h = hv / (a.HV / a.H);
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
+    if (L <= 0) return;
     load_rows_norm(Qn, a.q, a.rq, t0, L, a.H, h, a.scale);
     load_rows_norm(Kn, a.k, a.rk, t0, L, a.H, h, 1.f);
     for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
@@ -325,234 +279,93 @@ __global__ void __launch_bounds__(kThreads) k_dvloc(ChunkArgs a) {
     }
 }
 
-// Backward, step 2: reverse state scan ("dhu").  grid (N, HV, V / 32).
-//   dv_new = dv_local + Ktil dh',  Ktil_i = exp(G_L - G_i) khat_i
-//   dh     = e^{G_L} dh' + Qtil^T dO - w^T dv_new,  Qtil_i = e^{G_i} qhat_i
-__global__ void __launch_bounds__(kThreads) k_bstate(ChunkArgs a) {
-    extern __shared__ float sm[];
-    float *dh = sm;                  // [128][33]
-    float *dvn = dh + kDim * 33;     // [64][33]
-    float *dos = dvn + kChunk * 33;  // [64][33]
-    float *kt = dos + kChunk * 33;   // [64][129]
-    float *qt = kt + kChunk * kP;    // [64][129]
-    const int n = blockIdx.x, hv = blockIdx.y, v0 = blockIdx.z * kSlab, tid = threadIdx.x;
-    const int h = hv / (a.HV / a.H);
-    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim;
-    for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-        int r = idx >> 5, j = idx & 31;
-        dh[r * 33 + j] = a.d_ht ? a.d_ht[sbase + (size_t)r * kDim + v0 + j] : 0.f;
-    }
-    __syncthreads();
-    const int cb = a.seq_chunk_off[n], ce = a.seq_chunk_off[n + 1];
-    for (int c = ce - 1; c >= cb; --c) {
-        const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-        bf16 *ddst = a.dhc + ((size_t)c * a.HV + hv) * kDim * kDim;
-        for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-            int r = idx >> 5, j = idx & 31;
-            ddst[(size_t)r * kDim + v0 + j] = f2bf(dh[r * 33 + j]);
-        }
-        const float Gl = a.G[(size_t)(t0 + L - 1) * a.HV + hv];
-        for (int idx = tid; idx < L * kDim; idx += kThreads) {
-            int i = idx >> 7, e = idx & 127;
-            size_t t = (size_t)(t0 + i) * a.H + h;
-            float Gi = a.G[(size_t)(t0 + i) * a.HV + hv];
-            kt[i * kP + e] = expf(Gl - Gi) / a.rk[t] * bf2f(a.k[t * kDim + e]);
-            qt[i * kP + e] = expf(Gi) * a.scale / a.rq[t] * bf2f(a.q[t * kDim + e]);
-        }
-        for (int idx = tid; idx < L * kSlab; idx += kThreads) {
-            int i = idx >> 5, j = idx & 31;
-            dos[i * 33 + j] = bf2f(a.d_o[((size_t)(t0 + i) * a.HV + hv) * kDim + v0 + j]);
-        }
-        __syncthreads();
-        for (int idx = tid; idx < L * kSlab; idx += kThreads) {
-            int i = idx >> 5, j = idx & 31;
-            size_t row = ((size_t)(t0 + i) * a.HV + hv) * kDim;
-            float s = a.dvloc[row + v0 + j];
-            for (int e = 0; e < kDim; ++e) s += kt[i * kP + e] * dh[e * 33 + j];
-            dvn[i * 33 + j] = s;
-            a.dvnew[row + v0 + j] = s;
-        }
-        __syncthreads();
-        const float egl = expf(Gl);
-        for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-            int r = idx >> 5, j = idx & 31;
-            float s = egl * dh[r * 33 + j];
-            for (int i = 0; i < L; ++i) {
-                float wv = bf2f(a.w[((size_t)(t0 + i) * a.HV + hv) * kDim + r]);
-                s += qt[i * kP + r] * dos[i * 33 + j] - wv * dvn[i * 33 + j];
-            }
-            dh[r * 33 + j] = s;
-        }
-        __syncthreads();
-    }
-    if (a.dh0) {
-        for (int idx = tid; idx < kDim * kSlab; idx += kThreads) {
-            int r = idx >> 5, j = idx & 31;
-            a.dh0[sbase + (size_t)r * kDim + v0 + j] = dh[r * 33 + j];
-        }
-    }
-}
-
-// Deterministic block sum (fixed tree) of one float per thread.
-__device__ float block_sum(float v, float *red) {
-    v = warp_sum(v);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float s = 0.f;
-    if (threadIdx.x == 0) {
-        for (int w = 0; w < kThreads / 32; ++w) s += red[w];
-        red[kThreads / 32] = s;
-    }
-    __syncthreads();
-    return red[kThreads / 32];
-}
-
-// ---------------------------------------------------------------------------
-// Backward, step 3 ("dqkwg", the terms with h and dh').  grid (chunks, HV).
-//   dqhat_i  = e^{G_i} dO_i h^T                        -> dqp
-//   dW       = -dv_new h^T                             -> dW
-//   dKtil_j  = v_new_j dh'^T; dkhat_j = e^{G_L-G_j} dKtil_j  -> dkp
-//   dG_i    += qhat_i . dqhat_i
-//   dG_j    -= xi_j,  dG_L += sum_j xi_j + e^{G_L} <h, dh'>,  xi_j = khat_j . dkhat_j
-__global__ void __launch_bounds__(kThreads) k_bintra_a(ChunkArgs a) {
-    extern __shared__ float sm[];
-    float *dO = sm;                  // [64][129]
-    float *dvn = dO + kChunk * kP;   // [64][129]
-    float *vn = dvn + kChunk * kP;   // [64][129]
-    float *Gs = vn + kChunk * kP;    // [64]
-    float *dG = Gs + kChunk;         // [64]
-    float *red = dG + kChunk;        // [9]
-    const int c = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
-    const int h = hv / (a.HV / a.H);
-    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-    for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
-        int i = idx >> 7, e = idx & 127;
-        size_t o = ((size_t)(t0 + i) * a.HV + hv) * kDim + e;
-        bool in = i < L;
-        dO[i * kP + e] = in ? bf2f(a.d_o[o]) : 0.f;
-        dvn[i * kP + e] = in ? a.dvnew[o] : 0.f;
-        vn[i * kP + e] = in ? bf2f(a.vnew[o]) : 0.f;
-    }
-    if (tid < kChunk) Gs[tid] = tid < L ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
-    __syncthreads();
-    const bf16 *hc = a.hc + ((size_t)c * a.HV + hv) * kDim * kDim;
-    const bf16 *dhc = a.dhc + ((size_t)c * a.HV + hv) * kDim * kDim;
-    const float Gl = Gs[L - 1];
-    // thread -> (i = idx % 64, r = idx / 64): h / dh' rows r are warp-uniform
-    for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
-        int i = idx & 63, r = idx >> 6;
-        if (i >= L) continue;
-        float sq = 0.f, sw = 0.f, sk = 0.f;
-        for (int e = 0; e < kDim; ++e) {
-            float hv_ = bf2f(hc[(size_t)r * kDim + e]);
-            float dh_ = bf2f(dhc[(size_t)r * kDim + e]);
-            sq += dO[i * kP + e] * hv_;
-            sw += dvn[i * kP + e] * hv_;
-            sk += vn[i * kP + e] * dh_;
-        }
-        size_t o = ((size_t)(t0 + i) * a.HV + hv) * kDim + r;
-        a.dqp[o] = expf(Gs[i]) * sq;
-        a.dW[o] = -sw;
-        a.dkp[o] = expf(Gl - Gs[i]) * sk;
-    }
-    // <h, dh'>
-    float part = 0.f;
-    for (int idx = tid; idx < kDim * kDim; idx += kThreads) part += bf2f(hc[idx]) * bf2f(dhc[idx]);
-    float hdh = block_sum(part, red);  // includes __syncthreads: dqp / dkp visible
-    if (tid < kChunk) {
-        const int i = tid;
-        float dg = 0.f, xi = 0.f;
-        if (i < L) {
-            size_t t = (size_t)(t0 + i) * a.H + h;
-            size_t o = ((size_t)(t0 + i) * a.HV + hv) * kDim;
-            float qi = 0.f;
-            const float qs = a.scale / a.rq[t], ks = 1.f / a.rk[t];
-            for (int e = 0; e < kDim; ++e) {
-                qi += bf2f(a.q[t * kDim + e]) * qs * a.dqp[o + e];
-                xi += bf2f(a.k[t * kDim + e]) * ks * a.dkp[o + e];
-            }
-            dg = qi - xi;
-            a.dGp[(size_t)(t0 + i) * a.HV + hv] = dg;
-        }
-        dG[i] = xi;  // 0 past L
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float sx = 0.f;
-        for (int i = 0; i < L; ++i) sx += dG[i];
-        size_t o = (size_t)(t0 + L - 1) * a.HV + hv;
-        a.dGp[o] += sx + expf(Gl) * hdh;
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Backward, step 4 (the intra-chunk terms and the WY pullback).  grid (chunks, HV).
+// Every operand is staged in shared memory first (bf16 tiles with a 130-element
+// pitch so that column walks over consecutive rows hit distinct banks).
+constexpr int kB = 130;
+
+__device__ __forceinline__ void stage_rows(bf16 *dst, const bf16 *src, int t0, int L, int nh,
+                                           int hh) {
+    for (int idx = threadIdx.x; idx < kChunk * 64; idx += kThreads) {
+        const int i = idx >> 6, e2 = (idx & 63) * 2;
+        __nv_bfloat162 x = __floats2bfloat162_rn(0.f, 0.f);
+        if (i < L)
+            x = *reinterpret_cast<const __nv_bfloat162 *>(src + ((size_t)(t0 + i) * nh + hh) * kDim + e2);
+        *reinterpret_cast<__nv_bfloat162 *>(dst + i * kB + e2) = x;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) k_bintra_b(ChunkArgs a) {
     extern __shared__ float sm[];
-    float *Qn = sm;                    // [64][129]
-    float *Kn = Qn + kChunk * kP;      // [64][129]
-    float *Tm = Kn + kChunk * kP;      // [64][65]
-    float *dMG = Tm + kChunk * kQ;     // [64][65]  dM (.) Gamma, j <= i
-    float *P = dMG + kChunk * kQ;      // [64][65]  work
-    float *dT = P + kChunk * kQ;       // [64][65]
-    float *B = dT + kChunk * kQ;       // [64][65]  dA (.) beta_i Gamma, j < i
-    float *Gs = B + kChunk * kQ;       // [64]
-    float *bs = Gs + kChunk;           // [64]
-    float *dG = bs + kChunk;           // [64]
-    float *dbs = dG + kChunk;          // [64]
+    float *Tm = sm;                    // [64][65]
+    float *dMG = Tm + kChunk * kQ;     // dM (.) Gamma, j <= i
+    float *P = dMG + kChunk * kQ;      // work
+    float *dT = P + kChunk * kQ;       // dT, then dA
+    float *B = dT + kChunk * kQ;       // X, then dA (.) beta_i Gamma
+    float *Gs = B + kChunk * kQ;
+    float *bs = Gs + kChunk;
+    float *dG = bs + kChunk;
+    float *dbs = dG + kChunk;
+    float *qsc = dbs + kChunk;         // scale / r_q
+    float *ksc = qsc + kChunk;         // 1 / r_k
+    bf16 *Qb = reinterpret_cast<bf16 *>(ksc + kChunk);
+    bf16 *Kb = Qb + kChunk * kB;
+    bf16 *Vb = Kb + kChunk * kB;
+    bf16 *dOb = Vb + kChunk * kB;
+    bf16 *vnb = dOb + kChunk * kB;
+    bf16 *dvb = vnb + kChunk * kB;
+    bf16 *dWb = dvb + kChunk * kB;
     const int c = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
     const int h = hv / (a.HV / a.H);
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-    load_rows_norm(Qn, a.q, a.rq, t0, L, a.H, h, a.scale);
-    load_rows_norm(Kn, a.k, a.rk, t0, L, a.H, h, 1.f);
+    if (L <= 0) return;
+    stage_rows(Qb, a.q, t0, L, a.H, h);
+    stage_rows(Kb, a.k, t0, L, a.H, h);
+    stage_rows(Vb, a.v, t0, L, a.HV, hv);
+    stage_rows(dOb, a.d_o, t0, L, a.HV, hv);
+    stage_rows(vnb, a.vnew, t0, L, a.HV, hv);
+    stage_rows(dvb, a.dvnew, t0, L, a.HV, hv);
+    for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
+        const int i = idx >> 7, e = idx & 127;
+        dWb[i * kB + e] = f2bf(i < L ? a.dW[((size_t)(t0 + i) * a.HV + hv) * kDim + e] : 0.f);
+    }
     const float *Tsrc = a.Tm + ((size_t)c * a.HV + hv) * kChunk * kChunk;
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads)
         Tm[(idx >> 6) * kQ + (idx & 63)] = Tsrc[idx];
     if (tid < kChunk) {
-        bool in = tid < L;
+        const bool in = tid < L;
+        const size_t r = (size_t)(t0 + tid) * a.H + h;
         Gs[tid] = in ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
         bs[tid] = in ? bf2f(a.beta[(size_t)(t0 + tid) * a.HV + hv]) : 0.f;
         dG[tid] = in ? a.dGp[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
+        qsc[tid] = in ? a.scale / a.rq[r] : 0.f;
+        ksc[tid] = in ? 1.f / a.rk[r] : 0.f;
         dbs[tid] = 0.f;
     }
     __syncthreads();
-    auto rowv = [&](const bf16 *base, int i) { return base + ((size_t)(t0 + i) * a.HV + hv) * kDim; };
-    auto rowf = [&](const float *base, int i) { return base + ((size_t)(t0 + i) * a.HV + hv) * kDim; };
-    // dM (.) Gamma and P1 = dM (.) M
+    // dM (.) Gamma and P1 = dM (.) M ; dT (strictly lower) = dW_i . Wt_j + dv_new_i . Ut_j
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        int i = idx >> 6, j = idx & 63;
-        float dmg = 0.f, p1 = 0.f;
+        const int i = idx >> 6, j = idx & 63;
+        float dmg = 0.f, p1 = 0.f, dt = 0.f;
         if (j <= i && i < L) {
-            const bf16 *dOi = rowv(a.d_o, i), *vj = rowv(a.vnew, j);
-            float dm = 0.f, qk = 0.f;
+            float dm = 0.f, qk = 0.f, s1 = 0.f, s2 = 0.f;
             for (int e = 0; e < kDim; ++e) {
-                dm += bf2f(dOi[e]) * bf2f(vj[e]);
-                qk += Qn[i * kP + e] * Kn[j * kP + e];
+                const float kj = bf2f(Kb[j * kB + e]);
+                dm += bf2f(dOb[i * kB + e]) * bf2f(vnb[j * kB + e]);
+                qk += bf2f(Qb[i * kB + e]) * kj;
+                s1 += bf2f(dWb[i * kB + e]) * kj;
+                s2 += bf2f(dvb[i * kB + e]) * bf2f(Vb[j * kB + e]);
             }
-            float gam = expf(Gs[i] - Gs[j]);
+            qk *= qsc[i] * ksc[j];
+            const float gam = expf(Gs[i] - Gs[j]);
             dmg = dm * gam;
             p1 = dm * qk * gam;
+            if (j < i) dt = bs[j] * (expf(Gs[j]) * ksc[j] * s1 + s2);
         }
         dMG[i * kQ + j] = dmg;
         P[i * kQ + j] = p1;
-    }
-    // dT (strictly lower) = dW_i . Wt_j + dv_new_i . Ut_j
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        int i = idx >> 6, j = idx & 63;
-        float s = 0.f;
-        if (j < i && i < L) {
-            const float *dWi = rowf(a.dW, i), *dvi = rowf(a.dvnew, i);
-            const bf16 *vj = rowv(a.v, j);
-            float s1 = 0.f, s2 = 0.f;
-            for (int e = 0; e < kDim; ++e) {
-                s1 += dWi[e] * Kn[j * kP + e];
-                s2 += dvi[e] * bf2f(vj[e]);
-            }
-            s = bs[j] * (expf(Gs[j]) * s1 + s2);
-        }
-        dT[i * kQ + j] = s;
+        dT[i * kQ + j] = dt;
     }
     __syncthreads();
     if (tid < kChunk) {  // dG from P1: row sums minus column sums
@@ -561,34 +374,35 @@ __global__ void __launch_bounds__(kThreads) k_bintra_b(ChunkArgs a) {
         for (int j = 0; j < kChunk; ++j) s += P[i * kQ + j] - P[j * kQ + i];
         dG[i] += s;
     }
-    // X = dT Tm^T  (into B temporarily):  X_aj = sum_b dT_ab Tm_jb
+    // X = dT Tm^T:  X_rj = sum_b dT_rb Tm_jb
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        int r = idx >> 6, j = idx & 63;
+        const int r = idx >> 6, j = idx & 63;
         float s = 0.f;
-        for (int b = 0; b < kChunk; ++b) s += dT[r * kQ + b] * Tm[j * kQ + b];
+        for (int b = 0; b <= j; ++b) s += dT[r * kQ + b] * Tm[j * kQ + b];
         B[r * kQ + j] = s;
     }
     __syncthreads();
-    // dA_ij = -sum_r Tm_ri X_rj, strictly lower; then B = dA (.) beta_i Gamma, P2 = dA (.) A
+    // dA_ij = -sum_{r >= i} Tm_ri X_rj, strictly lower
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        int i = idx >> 6, j = idx & 63;
+        const int i = idx >> 6, j = idx & 63;
         float da = 0.f;
-        if (j < i && i < L) {
+        if (j < i && i < L)
             for (int r = i; r < L; ++r) da -= Tm[r * kQ + i] * B[r * kQ + j];
-        }
-        dT[i * kQ + j] = da;  // dT now holds dA
+        dT[i * kQ + j] = da;
     }
     __syncthreads();
+    // B = dA (.) beta_i Gamma ; P2 = dA (.) (A / beta_i)
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        int i = idx >> 6, j = idx & 63;
+        const int i = idx >> 6, j = idx & 63;
         float b = 0.f, p2 = 0.f;
         if (j < i && i < L) {
             float kk = 0.f;
-            for (int e = 0; e < kDim; ++e) kk += Kn[i * kP + e] * Kn[j * kP + e];
-            float gam = expf(Gs[i] - Gs[j]);
-            float da = dT[i * kQ + j];
+            for (int e = 0; e < kDim; ++e) kk += bf2f(Kb[i * kB + e]) * bf2f(Kb[j * kB + e]);
+            kk *= ksc[i] * ksc[j];
+            const float gam = expf(Gs[i] - Gs[j]);
+            const float da = dT[i * kQ + j];
             b = da * bs[i] * gam;
-            p2 = da * kk * gam;  // dA_ij * (A_ij / beta_i)
+            p2 = da * kk * gam;
         }
         B[i * kQ + j] = b;
         P[i * kQ + j] = p2;
@@ -601,8 +415,8 @@ __global__ void __launch_bounds__(kThreads) k_bintra_b(ChunkArgs a) {
             rs += P[i * kQ + j];
             cs += bs[j] * P[j * kQ + i];
         }
-        dbs[i] += rs;                 // d beta_i from A
-        dG[i] += bs[i] * rs - cs;     // P2 = dA (.) A: row sums minus column sums
+        dbs[i] += rs;
+        dG[i] += bs[i] * rs - cs;
     }
     __syncthreads();
     // per-row outputs: warp w takes rows m = w, w + 8, ...; lane takes 4 columns
@@ -616,18 +430,20 @@ __global__ void __launch_bounds__(kThreads) k_bintra_b(ChunkArgs a) {
             const int e = lane * 4 + u;
             float q_ = 0.f, k_ = 0.f, wt = 0.f, ut = 0.f;
             for (int j = 0; j <= m; ++j) {
-                q_ += dMG[m * kQ + j] * Kn[j * kP + e];
-                k_ += B[m * kQ + j] * Kn[j * kP + e];
+                const float kj = bf2f(Kb[j * kB + e]) * ksc[j];
+                q_ += dMG[m * kQ + j] * kj;
+                k_ += B[m * kQ + j] * kj;
             }
             for (int i = m; i < L; ++i) {
-                k_ += dMG[i * kQ + m] * Qn[i * kP + e] + B[i * kQ + m] * Kn[i * kP + e];
+                k_ += dMG[i * kQ + m] * bf2f(Qb[i * kB + e]) * qsc[i] +
+                      B[i * kQ + m] * bf2f(Kb[i * kB + e]) * ksc[i];
                 const float t = Tm[i * kQ + m];
-                wt += t * rowf(a.dW, i)[e];
-                ut += t * rowf(a.dvnew, i)[e];
+                wt += t * bf2f(dWb[i * kB + e]);
+                ut += t * bf2f(dvb[i * kB + e]);
             }
             k_ += bs[m] * egm * wt;
-            sk += Kn[m * kP + e] * wt;
-            su += bf2f(rowv(a.v, m)[e]) * ut;
+            sk += bf2f(Kb[m * kB + e]) * ksc[m] * wt;
+            su += bf2f(Vb[m * kB + e]) * ut;
             dq[u] = q_;
             dk[u] = k_;
             dv[u] = bs[m] * ut;
@@ -702,17 +518,14 @@ cudaError_t set_smem(Kern k, size_t bytes) {
 }
 
 constexpr size_t kSmemIntra = sizeof(float) * (kChunk * kP + 3 * kChunk * kQ + 3 * kChunk);
-constexpr size_t kSmemState = sizeof(float) * (kDim * 33 + kChunk * 33 + kChunk * kP);
 constexpr size_t kSmemOut = sizeof(float) * (3 * kChunk * kP + kChunk * kQ + kChunk);
-constexpr size_t kSmemBstate = sizeof(float) * (kDim * 33 + 2 * kChunk * 33 + 2 * kChunk * kP);
-constexpr size_t kSmemBa = sizeof(float) * (3 * kChunk * kP + 2 * kChunk + 16);
-constexpr size_t kSmemBb = sizeof(float) * (2 * kChunk * kP + 5 * kChunk * kQ + 4 * kChunk);
+constexpr size_t kSmemBb = sizeof(float) * (5 * kChunk * kQ + 6 * kChunk) + sizeof(bf16) * 7 * kChunk * kB;
 
 }  // namespace
 
 cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s) {
     TimerScope ts(a.timer, GDN_KERNEL_PLAN, s);
-    k_plan<<<1, 1024, 0, s>>>(a.cu_dev, a.N, a.num_chunks, a.seq_chunk_off, a.chunk_seq,
+    k_plan<<<1, 1024, 0, s>>>(a.cu_dev, a.N, a.T, a.num_chunks, a.seq_chunk_off, a.chunk_seq,
                               a.chunk_start, a.chunk_len, a.status);
     return cudaGetLastError();
 }
@@ -727,48 +540,23 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s) {
 cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e;
     if ((e = set_smem(k_intra, kSmemIntra)) != cudaSuccess) return e;
-    if ((e = set_smem(k_state, kSmemState)) != cudaSuccess) return e;
-    if ((e = set_smem(k_out, kSmemOut)) != cudaSuccess) return e;
     if (a.num_chunks > 0) {
         TimerScope ts(a.timer, GDN_KERNEL_INTRA, s);
         k_intra<<<dim3(a.num_chunks, a.H), kThreads, kSmemIntra, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    {
-        TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
-        k_state<<<dim3(a.N, a.HV, kDim / kSlab), kThreads, kSmemState, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    if (a.num_chunks > 0) {
-        TimerScope ts(a.timer, GDN_KERNEL_OUT, s);
-        k_out<<<dim3(a.num_chunks, a.HV), kThreads, kSmemOut, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_state_tc(a, s)) != cudaSuccess) return e;
+    if ((e = launch_out_tc(a, s)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e;
-    if ((e = set_smem(k_dvloc, kSmemOut)) != cudaSuccess) return e;
-    if ((e = set_smem(k_bstate, kSmemBstate)) != cudaSuccess) return e;
-    if ((e = set_smem(k_bintra_a, kSmemBa)) != cudaSuccess) return e;
     if ((e = set_smem(k_bintra_b, kSmemBb)) != cudaSuccess) return e;
-    if (a.num_chunks > 0) {
-        TimerScope ts(a.timer, GDN_KERNEL_DVLOC, s);
-        k_dvloc<<<dim3(a.num_chunks, a.HV), kThreads, kSmemOut, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    {
-        TimerScope ts(a.timer, GDN_KERNEL_BSTATE, s);
-        k_bstate<<<dim3(a.N, a.HV, kDim / kSlab), kThreads, kSmemBstate, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_dvloc_tc(a, s)) != cudaSuccess) return e;
+    if ((e = launch_bstate_tc(a, s)) != cudaSuccess) return e;
     if (a.num_chunks == 0) return cudaSuccess;
-    {
-        TimerScope ts(a.timer, GDN_KERNEL_BINTRA_A, s);
-        k_bintra_a<<<dim3(a.num_chunks, a.HV), kThreads, kSmemBa, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_bintra_a_tc(a, s)) != cudaSuccess) return e;
     {
         TimerScope ts(a.timer, GDN_KERNEL_BINTRA_B, s);
         k_bintra_b<<<dim3(a.num_chunks, a.HV), kThreads, kSmemBb, s>>>(a);

@@ -41,7 +41,7 @@ struct ChunkArgs {
     bf16 *dq, *dk, *dv, *dbeta;
     float *dg, *dh0;        // dh0 may be null
     float *dvloc;           // [T,HV,V]  tril(M)^T dO
-    float *dvnew;           // [T,HV,V]  full gradient of v_new
+    bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
     bf16 *dhc;              // [C_total,HV,K,V] gradient of the state after each chunk
     float *dW;              // [T,HV,K]
     float *dqp, *dkp;       // [T,HV,K] per-value-head gradients of qhat, khat
@@ -70,6 +70,11 @@ cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_out_tc(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_dvloc_tc(const ChunkArgs &a, cudaStream_t s);
 
 cudaError_t launch_decode(int B, int H, int HV, float scale, const bf16 *q, const bf16 *k,
                           const bf16 *v, const float *g, const float *beta, float *pool,

@@ -1,0 +1,224 @@
+// gdn_out_tc.cu -- chunk output o (forward) and dv_local (backward) on the
+// tensor cores.
+//
+// One CTA of 128 threads per (chunk, value head).  Both modes start from the
+// intra-chunk attention matrix
+//   M[t][j] = (qhat_t . khat_j) exp(G_t - G_j),  j <= t < L   (else 0)
+// formed by one product D1 = [K; Q] K^T (M=128 N=64 K=128: rows 64..127 are
+// Q K^T; rows 0..63, K K^T, are not used here) and scaled by
+// scale / (r_q,t r_k,j) in the epilogue.
+//   forward : o^T[v][t] = c_t (h^T Q^T)[v][t] + (v_new^T M^T)[v][t],
+//             c_t = e^{G_t} scale / r_q,t            (o = diag(e^G) Qhat h + M v_new)
+//   backward: dv_loc^T[v][t] = (dO^T M)[v][t]        (dv_loc = M^T dO)
+// h_c, v_new and dO are read as MN-major operands straight from their TMA
+// tiles; thread v owns row v of the results and writes o[t][hv][v] /
+// dv_loc[t][hv][v] with coalesced stores.
+#include <string.h>
+
+#include "gdn_kernels.h"
+#include "gdn_tma.h"
+#include "gdn_umma.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace umma;
+
+constexpr int kThr = 128;
+constexpr uint32_t kBox = 64 * 128;    // 64 rows x 128 B
+constexpr uint32_t kBig = 128 * 128;   // 128 rows x 128 B
+
+struct OutSmem {
+    unsigned char kq[2 * kBig];   // [K; Q] per k-half: K rows 0..63, Q rows 64..127
+    unsigned char hc[2 * kBig];   // h_c [k][v] per v-half (forward)
+    unsigned char tv[2 * kBox];   // v_new (forward) or dO (backward) [t][v] per v-half
+    unsigned char mm[kBox];       // M, row i at row i (bf16)
+    float G[64], rq[64], rk[64];
+    uint64_t tma_bar, mma_bar;
+    uint32_t tmem_base;
+};
+
+struct OutMaps {
+    CUtensorMap q, k, h, tv;
+};
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
+template <bool kForward>
+__global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
+                                                    const __grid_constant__ OutMaps maps) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    OutSmem &sm = *reinterpret_cast<OutSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int c = blockIdx.x, hv = blockIdx.y;
+    const int h = hv / (a.HV / a.H);
+    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
+    if (L <= 0) return;
+
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&sm.tma_bar, 1);
+        mbar_init(&sm.mma_bar, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint32_t bytes = 2 * kBig + 2 * kBox + (kForward ? 2 * kBig : 0);
+        mbar_arrive_expect_tx(&sm.tma_bar, bytes);
+        tma_load_3d(sm.kq, &maps.k, 0, h, t0, &sm.tma_bar);
+        tma_load_3d(sm.kq + kBox, &maps.q, 0, h, t0, &sm.tma_bar);
+        tma_load_3d(sm.kq + kBig, &maps.k, 64, h, t0, &sm.tma_bar);
+        tma_load_3d(sm.kq + kBig + kBox, &maps.q, 64, h, t0, &sm.tma_bar);
+        tma_load_3d(sm.tv, &maps.tv, 0, hv, t0, &sm.tma_bar);
+        tma_load_3d(sm.tv + kBox, &maps.tv, 64, hv, t0, &sm.tma_bar);
+        if (kForward) {
+            const int row = (c * a.HV + hv) * 128;
+            tma_load_3d(sm.hc, &maps.h, 0, 0, row, &sm.tma_bar);
+            tma_load_3d(sm.hc + kBig, &maps.h, 64, 0, row, &sm.tma_bar);
+        }
+    }
+    if (tid < 64) {
+        const bool in = tid < L;
+        const size_t r = (size_t)(t0 + tid) * a.H + h;
+        sm.G[tid] = in ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
+        sm.rq[tid] = in ? a.rq[r] : 1.f;
+        sm.rk[tid] = in ? a.rk[r] : 1.f;
+    }
+    bool ok = mbar_wait(&sm.tma_bar, 0);
+    __syncthreads();
+    const uint32_t tb = sm.tmem_base;
+    const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
+    uint32_t phase = 0;
+    // D1 = [K; Q] K^T
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+        const uint32_t as = smem_u32(sm.kq);
+        for (int s = 0; s < 8; ++s)
+            mma_bf16(tb, sdesc(as + (s >> 2) * kBig + (s & 3) * 32, 16, 1024),
+                     sdesc(as + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id, s > 0);
+        mma_commit(&sm.mma_bar);
+    }
+    ok = ok && mbar_wait(&sm.mma_bar, phase);
+    phase ^= 1;
+    tc_fence_after();
+    if (ok && tid >= 64) {  // thread 64 + t: row t of Q K^T  ->  M row t
+        const int t = tid - 64;
+        float r[32];
+        for (int half = 0; half < 2; ++half) {
+            tmem_ld32(t_row + half * 32, r);
+            tmem_ld_wait();
+            float m[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = half * 32 + jj;
+                m[jj] = (j <= t && t < L)
+                            ? r[jj] * a.scale / (sm.rq[t] * sm.rk[j]) * expf(sm.G[t] - sm.G[j])
+                            : 0.f;
+            }
+            // row t of M at row t: the forward reads it as K-major [t][j] (B = M^T
+            // operand of v_new^T M^T), the backward as MN-major [j][t] (B = M of dO^T M)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(sm.mm + sw128_off(t, half * 32 + q * 8)) =
+                    make_uint4(pack_bf2(m[q * 8 + 0], m[q * 8 + 1]), pack_bf2(m[q * 8 + 2], m[q * 8 + 3]),
+                               pack_bf2(m[q * 8 + 4], m[q * 8 + 5]), pack_bf2(m[q * 8 + 6], m[q * 8 + 7]));
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 1, 0);    // A MN-major, B K-major
+        const uint32_t tvs = smem_u32(sm.tv), mms = smem_u32(sm.mm);
+        if (kForward) {
+            // O1 = h^T Q^T : A = h_c [k][v] (MN-major, v atoms 16 KB apart), B = Q [t][k]
+            const uint32_t hs = smem_u32(sm.hc), qs = smem_u32(sm.kq + kBox);
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tb + 64, sdesc(hs + s * 2048, kBig, 1024),
+                         sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id, s > 0);
+            // O2 = v_new^T M^T : A = v_new [j][v] (MN-major, v atoms 8 KB apart), B = M [t][j]
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tb + 128, sdesc(tvs + s * 2048, kBox, 1024), sdesc(mms + s * 32, 16, 1024), id,
+                         s > 0);
+        } else {
+            // DL = dO^T M : A = dO [j][v] (MN-major), B = M [j][t] (MN-major)
+            const uint32_t id2 = idesc_bf16(128, 64, 1, 1);
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tb + 64, sdesc(tvs + s * 2048, kBox, 1024), sdesc(mms + s * 2048, kBox, 1024),
+                         id2, s > 0);
+        }
+        mma_commit(&sm.mma_bar);
+    }
+    ok = ok && mbar_wait(&sm.mma_bar, phase);
+    tc_fence_after();
+    if (ok) {
+        const int v = tid;
+        for (int half = 0; half < 2; ++half) {
+            float r1[32], r2[32];
+            tmem_ld32(t_row + 64 + half * 32, r1);
+            if (kForward) tmem_ld32(t_row + 128 + half * 32, r2);
+            tmem_ld_wait();
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j) {
+                const int t = half * 32 + j;
+                if (t < L) {
+                    const size_t o = ((size_t)(t0 + t) * a.HV + hv) * kDim + v;
+                    if (kForward) {
+                        const float ct = expf(sm.G[t]) * a.scale / sm.rq[t];
+                        a.o[o] = f2bf(ct * r1[j] + r2[j]);
+                    } else {
+                        a.dvloc[o] = r1[j];
+                    }
+                }
+            }
+        }
+    } else if (tid == 0 && a.status) {
+        atomicOr(a.status, 2);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+template <bool kForward>
+cudaError_t launch_out_mode(const ChunkArgs &a, cudaStream_t s) {
+    if (a.num_chunks == 0) return cudaSuccess;
+    OutMaps m;
+    memset(&m, 0, sizeof(m));
+    const uint64_t rowb = 256;
+    const uint64_t hrows = (uint64_t)a.num_chunks * a.HV * 128;
+    if (!encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
+        !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
+        !encode_rows_bf16(&m.tv, kForward ? (const void *)a.vnew : (const void *)a.d_o, a.HV, a.T,
+                          rowb, rowb * a.HV, 64))
+        return cudaErrorInvalidValue;
+    if (kForward && !encode_rows_bf16(&m.h, a.hc, 1, hrows, rowb, rowb, 128))
+        return cudaErrorInvalidValue;
+    const size_t smem = sizeof(OutSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_out_tc<kForward>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    TimerScope ts(a.timer, kForward ? GDN_KERNEL_OUT : GDN_KERNEL_DVLOC, s);
+    k_out_tc<kForward><<<dim3(a.num_chunks, a.HV), kThr, smem, s>>>(a, m);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_out_tc(const ChunkArgs &a, cudaStream_t s) { return launch_out_mode<true>(a, s); }
+cudaError_t launch_dvloc_tc(const ChunkArgs &a, cudaStream_t s) {
+    return launch_out_mode<false>(a, s);
+}
+
+}  // namespace gdn

@@ -89,6 +89,8 @@ def lib():
             L.gdn_chunk_bwd_timed.restype = ctypes.c_int
             L.gdn_decode_step_timed.argtypes = L.gdn_decode_step.argtypes + [T]
             L.gdn_decode_step_timed.restype = ctypes.c_int
+            L.gdn_chunk_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
+            L.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
             L.gdn_kernel_name.argtypes = [ctypes.c_int32]
             L.gdn_kernel_name.restype = ctypes.c_char_p
             _lib = L
@@ -167,6 +169,11 @@ def gdn_chunk_fwd(p, q, k, v, g, beta, initial_state, o, final_state, saved, wor
                                              ctypes.byref(timer.struct)))
     return int(lib().gdn_chunk_fwd(ctypes.byref(p), q, k, v, g, beta, initial_state, o,
                                    final_state, saved, workspace, ws_bytes, stream))
+
+
+def gdn_chunk_fwd_noalloc(p, q, k, v, g, beta, initial_state, o, final_state, stream) -> int:
+    return int(lib().gdn_chunk_fwd_noalloc(ctypes.byref(p), q, k, v, g, beta, initial_state, o,
+                                           final_state, stream))
 
 
 def gdn_chunk_bwd(p, q, k, v, g, beta, initial_state, saved, d_o, d_final_state, dq, dk, dv, dg,

@@ -102,6 +102,27 @@ gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, con
                          void *o, float *final_state, void *saved, void *workspace,
                          size_t ws_bytes, gdn_stream_t stream);
 
+/* gdn_chunk_fwd for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this entry point; it exists for callers such as code
+ * inside a pre-planned memory arena that forbids new allocations after
+ * start-up, host plugins that receive only their input and output buffers, and
+ * latency-critical paths that must avoid the synchronisation cudaMalloc and
+ * cudaFree can cause.  Inputs and outputs are as in gdn_chunk_fwd; no `saved`
+ * buffer is produced (forward only).  The scratch is a fixed 64 MiB device
+ * array inside the library (every GPU that loads libgdn.so holds it until the
+ * process exits); a problem whose forward workspace
+ * (gdn_chunk_workspace_bytes(p, 0)) exceeds 64 MiB is rejected with
+ * GDN_ERR_WORKSPACE_TOO_SMALL before any launch.  Nothing is allocated.  The
+ * first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the array: calls
+ * that overlap on the GPU race and give undefined results, so order them on
+ * one stream. */
+gdn_status gdn_chunk_fwd_noalloc(const gdn_problem *p, const void *q, const void *k,
+                                 const void *v, const float *g, const void *beta,
+                                 const float *initial_state, void *o, float *final_state,
+                                 gdn_stream_t stream);
+
 /* Backward of chunk_gated_delta_rule.  q ... initial_state exactly as passed
  * to the gdn_chunk_fwd that filled `saved` (not modified since).
  *   d_o            bf16 [T, HV, 128]

@@ -92,7 +92,7 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.dvloc = cv.take<float>((size_t)d.T * d.HV * D);
     a.dvnew = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dhc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
-    a.dW = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dW = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dqp = cv.take<float>((size_t)d.T * d.HV * D);
     a.dkp = cv.take<float>((size_t)d.T * d.HV * D);
     a.dGp = cv.take<float>((size_t)d.T * d.HV);

@@ -1,0 +1,387 @@
+// gdn_bintra_b_tc.cu -- intra-chunk backward and WY pullback on the tensor
+// cores ("dqkwg" / "WY pullback" of "cake_gdn: deterministic chunked GDN
+// training kernels", section 2 and the round-11 kernel notes).
+//
+// One CTA of 128 threads per (chunk, value head).  All products are M=64
+// tcgen05 MMAs whose rows are tokens; an M=64 result row m lives in TMEM lane
+// 32 (m / 16) + m % 16, so lanes 0..15 of warp w own rows 16w..16w+15.
+// With Qhat = diag(scale / r_q) Q, Khat = diag(1 / r_k) K, Gamma_ij =
+// exp(G_i - G_j) and the WY inverse T (saved by the forward):
+//   phase 1 (K = 128):  dM = dO v_new^T, QK = Q K^T, KK = K K^T,
+//                       D1 = dW K^T, D2 = dv_new V^T
+//     M_ij  = QK_ij scale / (r_q,i r_k,j) Gamma_ij       (j <= i)
+//     dMG   = dM (.) Gamma,  P1 = dM (.) M  -> dG
+//     dT_ij = beta_j (e^{G_j} D1_ij / r_k,j + D2_ij)     (j < i)
+//   CUDA cores (fp32):  X = dT T^T,  dA = -T^T X (strictly lower),
+//     B = dA (.) beta_i Gamma,  P2 = dA (.) KKhat Gamma -> dbeta, dG
+//   phase 2 (K = 64):   dq  = dMG diag(1/r_k) K
+//                       dk  = (diag(scale/r_q) dMG)^T Q + B diag(1/r_k) K
+//                             + (diag(1/r_k) B)^T K
+//                       dWt = T^T dW,   dUt = T^T dv_new
+//     dkhat_m += beta_m e^{G_m} dWt_m,  dv_m = beta_m dUt_m,
+//     dbeta_m += e^{G_m} khat_m . dWt_m + v_m . dUt_m,
+//     dG_m    += beta_m e^{G_m} khat_m . dWt_m,   dg = reverse cumsum of dG.
+// dq / dk are added to the per-value-head gradients of qhat / khat that the
+// h / dh' kernel wrote; the L2-norm backward and the head sum follow.
+#include <string.h>
+
+#include "gdn_kernels.h"
+#include "gdn_tma.h"
+#include "gdn_umma.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace umma;
+
+constexpr int kThr = 128;
+constexpr uint32_t kTile = 2 * 64 * 128;  // 64 rows x 128 bf16: two 8 KB k-halves
+constexpr uint32_t kHalf = 64 * 128;
+constexpr int kF = 65;                     // fp32 64 x 64 pitch
+
+struct BbSmem {
+    unsigned char q[kTile], k[kTile], v[kTile], dO[kTile], vn[kTile], dvn[kTile], dw[kTile];
+    unsigned char op_dmg[kHalf];    // dMG_ij / r_k,j        [m][j]  K-major A
+    unsigned char op_dmgt[kHalf];   // dMG_ij scale / r_q,i  [i][m]  MN-major A
+    unsigned char op_b[kHalf];      // B_mj / r_k,j          [m][j]  K-major A
+    unsigned char op_bt[kHalf];     // B_im / r_k,i          [i][m]  MN-major A
+    unsigned char op_t[kHalf];      // T_im                  [i][m]  MN-major A
+    float T[64 * kF];
+    float dT[64 * kF];              // dT, then dA
+    float X[64 * kF];               // P1, then X, then P2
+    float KG[64 * kF];              // KKhat (.) Gamma, strictly lower
+    float G[64], beta[64], rq[64], rk[64], dG[64], dbeta[64];
+    uint64_t tma_bar, mma_bar;
+    uint32_t tmem_base;
+};
+
+struct BbMaps {
+    CUtensorMap q, k, v, dO, vn, dvn, dw;
+};
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// Write 32 consecutive fp32 values of row `row`, columns [col0, col0 + 32), as
+// bf16 into a 64-wide SW128 tile.
+__device__ __forceinline__ void put_row32(unsigned char *tile, int row, int col0, const float *x) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(tile + sw128_off(row, col0 + q * 8)) =
+            make_uint4(pack_bf2(x[q * 8 + 0], x[q * 8 + 1]), pack_bf2(x[q * 8 + 2], x[q * 8 + 3]),
+                       pack_bf2(x[q * 8 + 4], x[q * 8 + 5]), pack_bf2(x[q * 8 + 6], x[q * 8 + 7]));
+}
+
+__device__ __forceinline__ float tile_at(const unsigned char *tile, int row, int col) {
+    return bf2f(*reinterpret_cast<const bf16 *>(tile + (col >> 6) * kHalf + sw128_off(row, col & 63)));
+}
+
+__global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
+                                                         const __grid_constant__ BbMaps maps) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    BbSmem &sm = *reinterpret_cast<BbSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, hv = blockIdx.y;
+    const int h = hv / (a.HV / a.H);
+    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
+    if (L <= 0) return;
+    const bool active = lane < 16;   // lane holds an M=64 result row
+    const int row = warp * 16 + lane;  // that row (valid when active)
+
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&sm.tma_bar, 1);
+        mbar_init(&sm.mma_bar, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&sm.tma_bar, 7 * kTile);
+        const CUtensorMap *mk[7] = {&maps.q, &maps.k, &maps.v, &maps.dO, &maps.vn, &maps.dvn, &maps.dw};
+        unsigned char *dst[7] = {sm.q, sm.k, sm.v, sm.dO, sm.vn, sm.dvn, sm.dw};
+        const int hh[7] = {h, h, hv, hv, hv, hv, hv};
+        for (int i = 0; i < 7; ++i) {
+            tma_load_3d(dst[i], mk[i], 0, hh[i], t0, &sm.tma_bar);
+            tma_load_3d(dst[i] + kHalf, mk[i], 64, hh[i], t0, &sm.tma_bar);
+        }
+    }
+    if (tid < 64) {
+        const bool in = tid < L;
+        const size_t r = (size_t)(t0 + tid) * a.H + h;
+        const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
+        sm.G[tid] = in ? a.G[gi] : 0.f;
+        sm.beta[tid] = in ? bf2f(a.beta[gi]) : 0.f;
+        sm.rq[tid] = in ? a.rq[r] : 1.f;
+        sm.rk[tid] = in ? a.rk[r] : 1.f;
+        sm.dG[tid] = in ? a.dGp[gi] : 0.f;
+        sm.dbeta[tid] = 0.f;
+    }
+    const float *Tsrc = a.Tm + ((size_t)c * a.HV + hv) * 64 * 64;
+    for (int idx = tid; idx < 64 * 64; idx += kThr) sm.T[(idx >> 6) * kF + (idx & 63)] = Tsrc[idx];
+    bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
+    const uint32_t tb = sm.tmem_base;
+    const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
+    uint32_t phase = 0;
+    // ---- phase 1: five 64 x 64 products, contraction 128
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(64, 64, 0, 0);
+        const uint32_t A[5] = {smem_u32(sm.dO), smem_u32(sm.q), smem_u32(sm.k), smem_u32(sm.dw),
+                               smem_u32(sm.dvn)};
+        const uint32_t B[5] = {smem_u32(sm.vn), smem_u32(sm.k), smem_u32(sm.k), smem_u32(sm.k),
+                               smem_u32(sm.v)};
+        for (int p = 0; p < 5; ++p)
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
+                mma_bf16(tb + 64 * p, sdesc(A[p] + off, 16, 1024), sdesc(B[p] + off, 16, 1024), id,
+                         s > 0);
+            }
+        mma_commit(&sm.mma_bar);
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
+    phase ^= 1;
+    tc_fence_after();
+    if (ok) {
+        const int i = row;
+        const bool live = active && i < L;
+        const float Gi = active ? sm.G[i] : 0.f;
+        const float qsi = active ? a.scale / sm.rq[i] : 0.f;
+        float rsum = 0.f;
+        for (int half = 0; half < 2; ++half) {
+            float dm[32], qk[32];
+            tmem_ld32(t_row + 0 + half * 32, dm);
+            tmem_ld32(t_row + 64 + half * 32, qk);
+            tmem_ld_wait();
+            float x1[32], x2[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = half * 32 + jj;
+                float dmg = 0.f, p1 = 0.f;
+                if (live && j <= i) {
+                    const float gam = expf(Gi - sm.G[j]);
+                    const float m = qk[jj] * qsi / sm.rk[j] * gam;
+                    dmg = dm[jj] * gam;
+                    p1 = dm[jj] * m;
+                }
+                rsum += p1;
+                if (active) sm.X[i * kF + j] = p1;
+                x1[jj] = dmg / sm.rk[j];
+                x2[jj] = dmg * qsi;
+            }
+            if (active) {
+                put_row32(sm.op_dmg, i, half * 32, x1);
+                put_row32(sm.op_dmgt, i, half * 32, x2);
+            }
+        }
+        for (int half = 0; half < 2; ++half) {
+            float kk[32], d1[32], d2[32];
+            tmem_ld32(t_row + 128 + half * 32, kk);
+            tmem_ld32(t_row + 192 + half * 32, d1);
+            tmem_ld32(t_row + 256 + half * 32, d2);
+            tmem_ld_wait();
+            if (active) {
+#pragma unroll 8
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = half * 32 + jj;
+                    float kg = 0.f, dt = 0.f;
+                    if (live && j < i) {
+                        const float Gj = sm.G[j];
+                        kg = kk[jj] / (sm.rk[i] * sm.rk[j]) * expf(Gi - Gj);
+                        dt = sm.beta[j] * (expf(Gj) / sm.rk[j] * d1[jj] + d2[jj]);
+                    }
+                    sm.KG[i * kF + j] = kg;
+                    sm.dT[i * kF + j] = dt;
+                }
+            }
+        }
+        if (active) sm.dG[i] += rsum;
+    }
+    tc_fence_before();
+    __syncthreads();
+    // ---- CUDA-core part
+    if (ok) {
+        if (tid < 64) {  // column sums of P1
+            float cs = 0.f;
+            for (int r = 0; r < 64; ++r) cs += sm.X[r * kF + tid];
+            sm.dG[tid] -= cs;
+        }
+        __syncthreads();
+        // X = dT T^T
+        for (int idx = tid; idx < 64 * 64; idx += kThr) {
+            const int r = idx >> 6, j = idx & 63;
+            float s = 0.f;
+            for (int b = 0; b <= j; ++b) s += sm.dT[r * kF + b] * sm.T[j * kF + b];
+            sm.X[r * kF + j] = s;
+        }
+        __syncthreads();
+        // dA = -T^T X, strictly lower (into dT)
+        for (int idx = tid; idx < 64 * 64; idx += kThr) {
+            const int i = idx >> 6, j = idx & 63;
+            float da = 0.f;
+            if (j < i && i < L)
+                for (int r = i; r < L; ++r) da -= sm.T[r * kF + i] * sm.X[r * kF + j];
+            sm.dT[i * kF + j] = da;
+        }
+        __syncthreads();
+        // B = dA (.) beta_i Gamma (operands), P2 = dA (.) KG (into X)
+        for (int idx = tid; idx < 64 * 64; idx += kThr) {
+            const int i = idx >> 6, j = idx & 63;
+            const float da = sm.dT[i * kF + j];
+            float b = 0.f;
+            if (j < i && i < L) b = da * sm.beta[i] * expf(sm.G[i] - sm.G[j]);
+            sm.X[i * kF + j] = da * sm.KG[i * kF + j];
+            sm.KG[i * kF + j] = b;  // KG now holds B
+        }
+        __syncthreads();
+        if (tid < 64) {
+            const int i = tid;
+            float rs = 0.f, cs = 0.f;
+            for (int j = 0; j < 64; ++j) {
+                rs += sm.X[i * kF + j];
+                cs += sm.beta[j] * sm.X[j * kF + i];
+            }
+            sm.dbeta[i] += rs;
+            sm.dG[i] += sm.beta[i] * rs - cs;
+        }
+        // operands B', Bt', T (bf16 rows)
+        if (active) {
+            const int m = row;
+            for (int half = 0; half < 2; ++half) {
+                float b1[32], b2[32], tt[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = half * 32 + jj;
+                    const float b = sm.KG[m * kF + j];
+                    b1[jj] = b / sm.rk[j];
+                    b2[jj] = b / sm.rk[m];
+                    tt[jj] = sm.T[m * kF + j];
+                }
+                put_row32(sm.op_b, m, half * 32, b1);
+                put_row32(sm.op_bt, m, half * 32, b2);
+                put_row32(sm.op_t, m, half * 32, tt);
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- phase 2: 64 x 128 products, contraction 64
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t kA = smem_u32(sm.k), qA = smem_u32(sm.q), dwA = smem_u32(sm.dw),
+                       dvA = smem_u32(sm.dvn);
+        const uint32_t id_km = idesc_bf16(64, 128, 0, 1);  // A K-major, B MN-major
+        const uint32_t id_mm = idesc_bf16(64, 128, 1, 1);  // A MN-major, B MN-major
+        for (int s = 0; s < 4; ++s) {
+            const uint64_t bK = sdesc(kA + s * 2048, kHalf, 1024), bQ = sdesc(qA + s * 2048, kHalf, 1024);
+            const uint64_t bW = sdesc(dwA + s * 2048, kHalf, 1024), bV = sdesc(dvA + s * 2048, kHalf, 1024);
+            const bool acc = s > 0;
+            mma_bf16(tb + 0, sdesc(smem_u32(sm.op_dmg) + s * 32, 16, 1024), bK, id_km, acc);
+            mma_bf16(tb + 128, sdesc(smem_u32(sm.op_dmgt) + s * 2048, kHalf, 1024), bQ, id_mm, acc);
+            mma_bf16(tb + 128, sdesc(smem_u32(sm.op_b) + s * 32, 16, 1024), bK, id_km, true);
+            mma_bf16(tb + 128, sdesc(smem_u32(sm.op_bt) + s * 2048, kHalf, 1024), bK, id_mm, true);
+            mma_bf16(tb + 256, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024), bW, id_mm, acc);
+            mma_bf16(tb + 384, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024), bV, id_mm, acc);
+        }
+        mma_commit(&sm.mma_bar);
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
+    tc_fence_after();
+    if (ok) {
+        const int m = row;
+        const bool live = active && m < L;
+        const float em = live ? expf(sm.G[m]) : 0.f;
+        const float bm = live ? sm.beta[m] : 0.f;
+        const float rkm = active ? sm.rk[m] : 1.f;
+        float sk = 0.f, su = 0.f;
+        const size_t o = ((size_t)(t0 + (live ? m : 0)) * a.HV + hv) * kDim;
+        for (int cc = 0; cc < 4; ++cc) {
+            float dq[32], dk[32], wt[32], ut[32];
+            tmem_ld32(t_row + 0 + cc * 32, dq);
+            tmem_ld32(t_row + 128 + cc * 32, dk);
+            tmem_ld32(t_row + 256 + cc * 32, wt);
+            tmem_ld32(t_row + 384 + cc * 32, ut);
+            tmem_ld_wait();
+            if (live) {
+                float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
+                float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    float4 x = qp[u], y = kp[u];
+                    x.x += dq[4 * u + 0]; x.y += dq[4 * u + 1]; x.z += dq[4 * u + 2]; x.w += dq[4 * u + 3];
+                    y.x += dk[4 * u + 0] + bm * em * wt[4 * u + 0];
+                    y.y += dk[4 * u + 1] + bm * em * wt[4 * u + 1];
+                    y.z += dk[4 * u + 2] + bm * em * wt[4 * u + 2];
+                    y.w += dk[4 * u + 3] + bm * em * wt[4 * u + 3];
+                    qp[u] = x;
+                    kp[u] = y;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) pk[j / 2] = pack_bf2(bm * ut[j], bm * ut[j + 1]);
+                uint4 *dvp = reinterpret_cast<uint4 *>(a.dv + o + cc * 32);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) dvp[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    sk += tile_at(sm.k, m, cc * 32 + j) * wt[j];
+                    su += tile_at(sm.v, m, cc * 32 + j) * ut[j];
+                }
+            }
+        }
+        if (live) {
+            sk /= rkm;
+            sm.dbeta[m] += em * sk + su;
+            sm.dG[m] += bm * em * sk;
+        }
+    } else if (tid == 0 && a.status) {
+        atomicOr(a.status, 2);
+    }
+    __syncthreads();
+    if (ok && tid == 0) {  // dg = reverse cumsum of dG within the chunk
+        float acc = 0.f;
+        for (int i = L - 1; i >= 0; --i) {
+            acc += sm.dG[i];
+            const size_t gi = (size_t)(t0 + i) * a.HV + hv;
+            a.dg[gi] = acc;
+            a.dbeta[gi] = f2bf(sm.dbeta[i]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
+    if (a.num_chunks == 0) return cudaSuccess;
+    BbMaps m;
+    memset(&m, 0, sizeof(m));
+    const uint64_t rowb = 256;
+    if (!encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
+        !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
+        !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.dO, a.d_o, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.vn, a.vnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64))
+        return cudaErrorInvalidValue;
+    const size_t smem = sizeof(BbSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_bintra_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    TimerScope ts(a.timer, GDN_KERNEL_BINTRA_B, s);
+    k_bintra_b_tc<<<dim3(a.num_chunks, a.HV), kThr, smem, s>>>(a, m);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

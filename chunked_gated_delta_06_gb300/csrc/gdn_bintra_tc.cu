@@ -94,8 +94,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         sm.eg[tid] = e1;
         sm.egl_g[tid] = e2;
     }
-    const bool got = mbar_wait(&sm.tma_bar, 0);
-    __syncthreads();
+    const bool got = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t t_row = sm.tmem_base + ((uint32_t)(warp * 32) << 16);
     if (tid == 0 && got) {
         tc_fence_after();
@@ -119,7 +118,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                    bf2f(*reinterpret_cast<const bf16 *>(sm.dh + off));
         }
     }
-    const bool done = got && mbar_wait(&sm.mma_bar, 0);
+    const bool done = __syncthreads_and(got && mbar_wait(&sm.mma_bar, 0));
     tc_fence_after();
     if (!done) {
         if (tid == 0 && a.status) atomicOr(a.status, 2);
@@ -140,7 +139,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                     const float dq = sm.eg[t] * rq_[j];
                     const float dk = sm.egl_g[t] * rk_[j];
                     a.dqp[o] = dq;
-                    a.dW[o] = -rw_[j];
+                    a.dW[o] = f2bf(-rw_[j]);
                     a.dkp[o] = dk;
                     xq = bf2f(a.q[qrow]) * dq;
                     xk = bf2f(a.k[qrow]) * dk;

@@ -186,9 +186,14 @@ __global__ void __launch_bounds__(kThr, 1)
         if (!mbar_wait(&sm.mma_bar, mma_phase)) sm.error = 1;
         mma_phase ^= 1;
         tc_fence_after();
-        // 3. dv_new^T = dv_loc^T + kc_t Pd
+        // 3. dv_new^T = dv_loc^T + kc_t Pd  (dv_loc loads issued before any store)
         for (int tc = 0; tc < 2; ++tc) {
-            float p[32];
+            float p[32], dl[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = tc * 32 + j;
+                dl[j] = t < L ? __ldg(a.dvloc + ((size_t)(t0 + t) * a.HV + hv) * kDim + v) : 0.f;
+            }
             tmem_ld32(tP + tc * 32, p);
             tmem_ld_wait();
 #pragma unroll
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kThr, 1)
                         float dvn = 0.f;
                         if (t < L) {
                             const size_t o = ((size_t)(t0 + t) * a.HV + hv) * kDim + v;
-                            dvn = a.dvloc[o] + sm.kc[t] * p[q * 8 + 2 * e + z];
+                            dvn = dl[q * 8 + 2 * e + z] + sm.kc[t] * p[q * 8 + 2 * e + z];
                             a.dvnew[o] = f2bf(dvn);
                         }
                         x2[z] = -dvn;

@@ -280,200 +280,6 @@ __global__ void __launch_bounds__(kThreads) k_dvloc(ChunkArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward, step 4 (the intra-chunk terms and the WY pullback).  grid (chunks, HV).
-// Every operand is staged in shared memory first (bf16 tiles with a 130-element
-// pitch so that column walks over consecutive rows hit distinct banks).
-constexpr int kB = 130;
-
-__device__ __forceinline__ void stage_rows(bf16 *dst, const bf16 *src, int t0, int L, int nh,
-                                           int hh) {
-    for (int idx = threadIdx.x; idx < kChunk * 64; idx += kThreads) {
-        const int i = idx >> 6, e2 = (idx & 63) * 2;
-        __nv_bfloat162 x = __floats2bfloat162_rn(0.f, 0.f);
-        if (i < L)
-            x = *reinterpret_cast<const __nv_bfloat162 *>(src + ((size_t)(t0 + i) * nh + hh) * kDim + e2);
-        *reinterpret_cast<__nv_bfloat162 *>(dst + i * kB + e2) = x;
-    }
-}
-
-__global__ void __launch_bounds__(kThreads) k_bintra_b(ChunkArgs a) {
-    extern __shared__ float sm[];
-    float *Tm = sm;                    // [64][65]
-    float *dMG = Tm + kChunk * kQ;     // dM (.) Gamma, j <= i
-    float *P = dMG + kChunk * kQ;      // work
-    float *dT = P + kChunk * kQ;       // dT, then dA
-    float *B = dT + kChunk * kQ;       // X, then dA (.) beta_i Gamma
-    float *Gs = B + kChunk * kQ;
-    float *bs = Gs + kChunk;
-    float *dG = bs + kChunk;
-    float *dbs = dG + kChunk;
-    float *qsc = dbs + kChunk;         // scale / r_q
-    float *ksc = qsc + kChunk;         // 1 / r_k
-    bf16 *Qb = reinterpret_cast<bf16 *>(ksc + kChunk);
-    bf16 *Kb = Qb + kChunk * kB;
-    bf16 *Vb = Kb + kChunk * kB;
-    bf16 *dOb = Vb + kChunk * kB;
-    bf16 *vnb = dOb + kChunk * kB;
-    bf16 *dvb = vnb + kChunk * kB;
-    bf16 *dWb = dvb + kChunk * kB;
-    const int c = blockIdx.x, hv = blockIdx.y, tid = threadIdx.x;
-    const int h = hv / (a.HV / a.H);
-    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-    if (L <= 0) return;
-    stage_rows(Qb, a.q, t0, L, a.H, h);
-    stage_rows(Kb, a.k, t0, L, a.H, h);
-    stage_rows(Vb, a.v, t0, L, a.HV, hv);
-    stage_rows(dOb, a.d_o, t0, L, a.HV, hv);
-    stage_rows(vnb, a.vnew, t0, L, a.HV, hv);
-    stage_rows(dvb, a.dvnew, t0, L, a.HV, hv);
-    for (int idx = tid; idx < kChunk * kDim; idx += kThreads) {
-        const int i = idx >> 7, e = idx & 127;
-        dWb[i * kB + e] = f2bf(i < L ? a.dW[((size_t)(t0 + i) * a.HV + hv) * kDim + e] : 0.f);
-    }
-    const float *Tsrc = a.Tm + ((size_t)c * a.HV + hv) * kChunk * kChunk;
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads)
-        Tm[(idx >> 6) * kQ + (idx & 63)] = Tsrc[idx];
-    if (tid < kChunk) {
-        const bool in = tid < L;
-        const size_t r = (size_t)(t0 + tid) * a.H + h;
-        Gs[tid] = in ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
-        bs[tid] = in ? bf2f(a.beta[(size_t)(t0 + tid) * a.HV + hv]) : 0.f;
-        dG[tid] = in ? a.dGp[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
-        qsc[tid] = in ? a.scale / a.rq[r] : 0.f;
-        ksc[tid] = in ? 1.f / a.rk[r] : 0.f;
-        dbs[tid] = 0.f;
-    }
-    __syncthreads();
-    // dM (.) Gamma and P1 = dM (.) M ; dT (strictly lower) = dW_i . Wt_j + dv_new_i . Ut_j
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        float dmg = 0.f, p1 = 0.f, dt = 0.f;
-        if (j <= i && i < L) {
-            float dm = 0.f, qk = 0.f, s1 = 0.f, s2 = 0.f;
-            for (int e = 0; e < kDim; ++e) {
-                const float kj = bf2f(Kb[j * kB + e]);
-                dm += bf2f(dOb[i * kB + e]) * bf2f(vnb[j * kB + e]);
-                qk += bf2f(Qb[i * kB + e]) * kj;
-                s1 += bf2f(dWb[i * kB + e]) * kj;
-                s2 += bf2f(dvb[i * kB + e]) * bf2f(Vb[j * kB + e]);
-            }
-            qk *= qsc[i] * ksc[j];
-            const float gam = expf(Gs[i] - Gs[j]);
-            dmg = dm * gam;
-            p1 = dm * qk * gam;
-            if (j < i) dt = bs[j] * (expf(Gs[j]) * ksc[j] * s1 + s2);
-        }
-        dMG[i * kQ + j] = dmg;
-        P[i * kQ + j] = p1;
-        dT[i * kQ + j] = dt;
-    }
-    __syncthreads();
-    if (tid < kChunk) {  // dG from P1: row sums minus column sums
-        const int i = tid;
-        float s = 0.f;
-        for (int j = 0; j < kChunk; ++j) s += P[i * kQ + j] - P[j * kQ + i];
-        dG[i] += s;
-    }
-    // X = dT Tm^T:  X_rj = sum_b dT_rb Tm_jb
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int r = idx >> 6, j = idx & 63;
-        float s = 0.f;
-        for (int b = 0; b <= j; ++b) s += dT[r * kQ + b] * Tm[j * kQ + b];
-        B[r * kQ + j] = s;
-    }
-    __syncthreads();
-    // dA_ij = -sum_{r >= i} Tm_ri X_rj, strictly lower
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        float da = 0.f;
-        if (j < i && i < L)
-            for (int r = i; r < L; ++r) da -= Tm[r * kQ + i] * B[r * kQ + j];
-        dT[i * kQ + j] = da;
-    }
-    __syncthreads();
-    // B = dA (.) beta_i Gamma ; P2 = dA (.) (A / beta_i)
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        float b = 0.f, p2 = 0.f;
-        if (j < i && i < L) {
-            float kk = 0.f;
-            for (int e = 0; e < kDim; ++e) kk += bf2f(Kb[i * kB + e]) * bf2f(Kb[j * kB + e]);
-            kk *= ksc[i] * ksc[j];
-            const float gam = expf(Gs[i] - Gs[j]);
-            const float da = dT[i * kQ + j];
-            b = da * bs[i] * gam;
-            p2 = da * kk * gam;
-        }
-        B[i * kQ + j] = b;
-        P[i * kQ + j] = p2;
-    }
-    __syncthreads();
-    if (tid < kChunk) {
-        const int i = tid;
-        float rs = 0.f, cs = 0.f;
-        for (int j = 0; j < kChunk; ++j) {
-            rs += P[i * kQ + j];
-            cs += bs[j] * P[j * kQ + i];
-        }
-        dbs[i] += rs;
-        dG[i] += bs[i] * rs - cs;
-    }
-    __syncthreads();
-    // per-row outputs: warp w takes rows m = w, w + 8, ...; lane takes 4 columns
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int m = warp; m < L; m += kThreads / 32) {
-        float sk = 0.f, su = 0.f;
-        const float egm = expf(Gs[m]);
-        float dq[4], dk[4], dv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = lane * 4 + u;
-            float q_ = 0.f, k_ = 0.f, wt = 0.f, ut = 0.f;
-            for (int j = 0; j <= m; ++j) {
-                const float kj = bf2f(Kb[j * kB + e]) * ksc[j];
-                q_ += dMG[m * kQ + j] * kj;
-                k_ += B[m * kQ + j] * kj;
-            }
-            for (int i = m; i < L; ++i) {
-                k_ += dMG[i * kQ + m] * bf2f(Qb[i * kB + e]) * qsc[i] +
-                      B[i * kQ + m] * bf2f(Kb[i * kB + e]) * ksc[i];
-                const float t = Tm[i * kQ + m];
-                wt += t * bf2f(dWb[i * kB + e]);
-                ut += t * bf2f(dvb[i * kB + e]);
-            }
-            k_ += bs[m] * egm * wt;
-            sk += bf2f(Kb[m * kB + e]) * ksc[m] * wt;
-            su += bf2f(Vb[m * kB + e]) * ut;
-            dq[u] = q_;
-            dk[u] = k_;
-            dv[u] = bs[m] * ut;
-        }
-        sk = warp_sum(sk);
-        su = warp_sum(su);
-        const size_t o = ((size_t)(t0 + m) * a.HV + hv) * kDim + lane * 4;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            a.dqp[o + u] += dq[u];
-            a.dkp[o + u] += dk[u];
-            a.dv[o + u] = f2bf(dv[u]);
-        }
-        if (lane == 0) {
-            dbs[m] += egm * sk + su;
-            dG[m] += bs[m] * egm * sk;
-        }
-    }
-    __syncthreads();
-    if (tid == 0) {  // dg = reverse cumsum of dG within the chunk
-        float acc = 0.f;
-        for (int i = L - 1; i >= 0; --i) {
-            acc += dG[i];
-            a.dg[(size_t)(t0 + i) * a.HV + hv] = acc;
-            a.dbeta[(size_t)(t0 + i) * a.HV + hv] = f2bf(dbs[i]);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Backward, step 5: sum the per-value-head gradients of qhat / khat over the
 // HV / H value heads of each key head (fixed order) and apply the L2-norm
 // backward dx = (dn - n (n . dn)) / r.  One warp per (token, key head).
@@ -519,7 +325,6 @@ cudaError_t set_smem(Kern k, size_t bytes) {
 
 constexpr size_t kSmemIntra = sizeof(float) * (kChunk * kP + 3 * kChunk * kQ + 3 * kChunk);
 constexpr size_t kSmemOut = sizeof(float) * (3 * kChunk * kP + kChunk * kQ + kChunk);
-constexpr size_t kSmemBb = sizeof(float) * (5 * kChunk * kQ + 6 * kChunk) + sizeof(bf16) * 7 * kChunk * kB;
 
 }  // namespace
 
@@ -539,12 +344,7 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s) {
 
 cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e;
-    if ((e = set_smem(k_intra, kSmemIntra)) != cudaSuccess) return e;
-    if (a.num_chunks > 0) {
-        TimerScope ts(a.timer, GDN_KERNEL_INTRA, s);
-        k_intra<<<dim3(a.num_chunks, a.H), kThreads, kSmemIntra, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_intra_tc(a, s)) != cudaSuccess) return e;
     if ((e = launch_state_tc(a, s)) != cudaSuccess) return e;
     if ((e = launch_out_tc(a, s)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -552,16 +352,11 @@ cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s) {
 
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e;
-    if ((e = set_smem(k_bintra_b, kSmemBb)) != cudaSuccess) return e;
     if ((e = launch_dvloc_tc(a, s)) != cudaSuccess) return e;
     if ((e = launch_bstate_tc(a, s)) != cudaSuccess) return e;
     if (a.num_chunks == 0) return cudaSuccess;
     if ((e = launch_bintra_a_tc(a, s)) != cudaSuccess) return e;
-    {
-        TimerScope ts(a.timer, GDN_KERNEL_BINTRA_B, s);
-        k_bintra_b<<<dim3(a.num_chunks, a.HV), kThreads, kSmemBb, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_bintra_b_tc(a, s)) != cudaSuccess) return e;
     {
         const size_t items = (size_t)a.T * a.H;
         const unsigned blocks = (unsigned)((items + kThreads / 32 - 1) / (kThreads / 32));

@@ -43,7 +43,7 @@ struct ChunkArgs {
     float *dvloc;           // [T,HV,V]  tril(M)^T dO
     bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
     bf16 *dhc;              // [C_total,HV,K,V] gradient of the state after each chunk
-    float *dW;              // [T,HV,K]
+    bf16 *dW;               // [T,HV,K]
     float *dqp, *dkp;       // [T,HV,K] per-value-head gradients of qhat, khat
     float *dGp;             // [T,HV]
     gdn_kernel_timer *timer;  // optional per-kernel events
@@ -75,6 +75,8 @@ cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_out_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_dvloc_tc(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_intra_tc(const ChunkArgs &a, cudaStream_t s);
 
 cudaError_t launch_decode(int B, int H, int HV, float scale, const bf16 *q, const bf16 *k,
                           const bf16 *v, const float *g, const float *beta, float *pool,

@@ -93,8 +93,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
         sm.rq[tid] = in ? a.rq[r] : 1.f;
         sm.rk[tid] = in ? a.rk[r] : 1.f;
     }
-    bool ok = mbar_wait(&sm.tma_bar, 0);
-    __syncthreads();
+    bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
     uint32_t phase = 0;
@@ -108,7 +107,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
                      sdesc(as + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id, s > 0);
         mma_commit(&sm.mma_bar);
     }
-    ok = ok && mbar_wait(&sm.mma_bar, phase);
+    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
     phase ^= 1;
     tc_fence_after();
     if (ok && tid >= 64) {  // thread 64 + t: row t of Q K^T  ->  M row t
@@ -160,7 +159,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
         }
         mma_commit(&sm.mma_bar);
     }
-    ok = ok && mbar_wait(&sm.mma_bar, phase);
+    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
     tc_fence_after();
     if (ok) {
         const int v = tid;

@@ -301,7 +301,7 @@ def bench_ours(args):
     from chunked_gated_delta_06_gb300 import workloads as W
     peaks = _peaks()
 
-    wl = W.fb_32k_varlen(seed=rank)
+    wl = W.CHUNK_CONFIGS[args.workload](seed=rank)
     T, H, HV, N = wl.T, wl.H, wl.HV, wl.N
     C_total = int(sum((int(wl.cu_seqlens[i + 1] - wl.cu_seqlens[i]) + C - 1) // C for i in range(N)))
     run = ChunkRunner(torch, wl, dev)
@@ -356,7 +356,7 @@ def bench_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "fb_32k_varlen", "T": T, "num_seqs": N, "H": H, "HV": HV,
+            "config": {"workload": args.workload, "T": T, "num_seqs": N, "H": H, "HV": HV,
                        "K": D, "V": D, "chunk": C, "chunks": C_total,
                        "step": "gdn_chunk_fwd (saving for backward) + gdn_chunk_bwd",
                        "l2": "inputs larger than L2 (q,k,v,dO = %.0f MB)" % (
@@ -443,6 +443,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="fb_32k_varlen",
+                    choices=["fb_32k_varlen", "fb_4x4096", "fb_65536_long", "fb_8192"],
+                    help="chunk workload of the fwd+bwd step (the headline is fb_32k_varlen)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

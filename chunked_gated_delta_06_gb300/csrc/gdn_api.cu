@@ -89,7 +89,7 @@ void carve_fwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a, bool with_saved)
 void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     const size_t D = gdn::kDim;
     carve_table(cv, d, a);
-    a.dvloc = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dvloc = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dvnew = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dhc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
     a.dW = cv.take<bf16>((size_t)d.T * d.HV * D);

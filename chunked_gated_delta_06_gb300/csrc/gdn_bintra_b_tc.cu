@@ -34,7 +34,7 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThr = 128;
+constexpr int kThr = 256;   // two warpgroups share the 128 TMEM lanes
 constexpr uint32_t kTile = 2 * 64 * 128;  // 64 rows x 128 bf16: two 8 KB k-halves
 constexpr uint32_t kHalf = 64 * 128;
 constexpr int kF = 65;                     // fp32 64 x 64 pitch
@@ -51,6 +51,7 @@ struct BbSmem {
     float X[64 * kF];               // P1, then X, then P2
     float KG[64 * kF];              // KKhat (.) Gamma, strictly lower
     float G[64], beta[64], rq[64], rk[64], dG[64], dbeta[64];
+    float sk[2][64], su[2][64];     // per-warpgroup partial row dots
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
 };
@@ -88,8 +89,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
     const int h = hv / (a.HV / a.H);
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
     if (L <= 0) return;
-    const bool active = lane < 16;   // lane holds an M=64 result row
-    const int row = warp * 16 + lane;  // that row (valid when active)
+    const bool active = lane < 16;          // lane holds an M=64 result row
+    const int grp = warp >> 2;              // warpgroup: which half of the work
+    const int row = (warp & 3) * 16 + lane; // that row (valid when active)
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
     for (int idx = tid; idx < 64 * 64; idx += kThr) sm.T[(idx >> 6) * kF + (idx & 63)] = Tsrc[idx];
     bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t tb = sm.tmem_base;
-    const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_row = tb + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t phase = 0;
     // ---- phase 1: five 64 x 64 products, contraction 128
     if (tid == 0 && ok) {
@@ -153,56 +155,59 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
         const int i = row;
         const bool live = active && i < L;
         const float Gi = active ? sm.G[i] : 0.f;
-        const float qsi = active ? a.scale / sm.rq[i] : 0.f;
-        float rsum = 0.f;
-        for (int half = 0; half < 2; ++half) {
-            float dm[32], qk[32];
-            tmem_ld32(t_row + 0 + half * 32, dm);
-            tmem_ld32(t_row + 64 + half * 32, qk);
-            tmem_ld_wait();
-            float x1[32], x2[32];
+        if (grp == 0) {  // dM, QK -> M, dMG, P1 and the dMG operands
+            const float qsi = active ? a.scale / sm.rq[i] : 0.f;
+            float rsum = 0.f;
+            for (int half = 0; half < 2; ++half) {
+                float dm[32], qk[32];
+                tmem_ld32(t_row + 0 + half * 32, dm);
+                tmem_ld32(t_row + 64 + half * 32, qk);
+                tmem_ld_wait();
+                float x1[32], x2[32];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = half * 32 + jj;
-                float dmg = 0.f, p1 = 0.f;
-                if (live && j <= i) {
-                    const float gam = expf(Gi - sm.G[j]);
-                    const float m = qk[jj] * qsi / sm.rk[j] * gam;
-                    dmg = dm[jj] * gam;
-                    p1 = dm[jj] * m;
-                }
-                rsum += p1;
-                if (active) sm.X[i * kF + j] = p1;
-                x1[jj] = dmg / sm.rk[j];
-                x2[jj] = dmg * qsi;
-            }
-            if (active) {
-                put_row32(sm.op_dmg, i, half * 32, x1);
-                put_row32(sm.op_dmgt, i, half * 32, x2);
-            }
-        }
-        for (int half = 0; half < 2; ++half) {
-            float kk[32], d1[32], d2[32];
-            tmem_ld32(t_row + 128 + half * 32, kk);
-            tmem_ld32(t_row + 192 + half * 32, d1);
-            tmem_ld32(t_row + 256 + half * 32, d2);
-            tmem_ld_wait();
-            if (active) {
-#pragma unroll 8
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = half * 32 + jj;
-                    float kg = 0.f, dt = 0.f;
-                    if (live && j < i) {
-                        const float Gj = sm.G[j];
-                        kg = kk[jj] / (sm.rk[i] * sm.rk[j]) * expf(Gi - Gj);
-                        dt = sm.beta[j] * (expf(Gj) / sm.rk[j] * d1[jj] + d2[jj]);
+                    float dmg = 0.f, p1 = 0.f;
+                    if (live && j <= i) {
+                        const float gam = expf(Gi - sm.G[j]);
+                        const float m = qk[jj] * qsi / sm.rk[j] * gam;
+                        dmg = dm[jj] * gam;
+                        p1 = dm[jj] * m;
                     }
-                    sm.KG[i * kF + j] = kg;
-                    sm.dT[i * kF + j] = dt;
+                    rsum += p1;
+                    if (active) sm.X[i * kF + j] = p1;
+                    x1[jj] = dmg / sm.rk[j];
+                    x2[jj] = dmg * qsi;
+                }
+                if (active) {
+                    put_row32(sm.op_dmg, i, half * 32, x1);
+                    put_row32(sm.op_dmgt, i, half * 32, x2);
+                }
+            }
+            if (active) sm.dG[i] += rsum;
+        } else {  // KK, dW K^T, dv_new V^T -> KKhat Gamma, dT
+            for (int half = 0; half < 2; ++half) {
+                float kk[32], d1[32], d2[32];
+                tmem_ld32(t_row + 128 + half * 32, kk);
+                tmem_ld32(t_row + 192 + half * 32, d1);
+                tmem_ld32(t_row + 256 + half * 32, d2);
+                tmem_ld_wait();
+                if (active) {
+#pragma unroll 8
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int j = half * 32 + jj;
+                        float kg = 0.f, dt = 0.f;
+                        if (live && j < i) {
+                            const float Gj = sm.G[j];
+                            kg = kk[jj] / (sm.rk[i] * sm.rk[j]) * expf(Gi - Gj);
+                            dt = sm.beta[j] * (expf(Gj) / sm.rk[j] * d1[jj] + d2[jj]);
+                        }
+                        sm.KG[i * kF + j] = kg;
+                        sm.dT[i * kF + j] = dt;
+                    }
                 }
             }
         }
-        if (active) sm.dG[i] += rsum;
     }
     tc_fence_before();
     __syncthreads();
@@ -251,22 +256,26 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
             sm.dbeta[i] += rs;
             sm.dG[i] += sm.beta[i] * rs - cs;
         }
-        // operands B', Bt', T (bf16 rows)
+        // operands B', Bt' (warpgroup 0) and T (warpgroup 1), bf16 rows
         if (active) {
             const int m = row;
             for (int half = 0; half < 2; ++half) {
-                float b1[32], b2[32], tt[32];
+                if (grp == 0) {
+                    float b1[32], b2[32];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = half * 32 + jj;
-                    const float b = sm.KG[m * kF + j];
-                    b1[jj] = b / sm.rk[j];
-                    b2[jj] = b / sm.rk[m];
-                    tt[jj] = sm.T[m * kF + j];
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const float b = sm.KG[m * kF + half * 32 + jj];
+                        b1[jj] = b / sm.rk[half * 32 + jj];
+                        b2[jj] = b / sm.rk[m];
+                    }
+                    put_row32(sm.op_b, m, half * 32, b1);
+                    put_row32(sm.op_bt, m, half * 32, b2);
+                } else {
+                    float tt[32];
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) tt[jj] = sm.T[m * kF + half * 32 + jj];
+                    put_row32(sm.op_t, m, half * 32, tt);
                 }
-                put_row32(sm.op_b, m, half * 32, b1);
-                put_row32(sm.op_bt, m, half * 32, b2);
-                put_row32(sm.op_t, m, half * 32, tt);
             }
         }
     }
@@ -300,10 +309,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
         const bool live = active && m < L;
         const float em = live ? expf(sm.G[m]) : 0.f;
         const float bm = live ? sm.beta[m] : 0.f;
-        const float rkm = active ? sm.rk[m] : 1.f;
         float sk = 0.f, su = 0.f;
         const size_t o = ((size_t)(t0 + (live ? m : 0)) * a.HV + hv) * kDim;
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {  // this warpgroup's 64 columns
             float dq[32], dk[32], wt[32], ut[32];
             tmem_ld32(t_row + 0 + cc * 32, dq);
             tmem_ld32(t_row + 128 + cc * 32, dk);
@@ -313,9 +321,15 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
             if (live) {
                 float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
                 float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
+                float4 xs[8], ys[8];  // all loads before any store
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    float4 x = qp[u], y = kp[u];
+                    xs[u] = __ldg(qp + u);
+                    ys[u] = __ldg(kp + u);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    float4 x = xs[u], y = ys[u];
                     x.x += dq[4 * u + 0]; x.y += dq[4 * u + 1]; x.z += dq[4 * u + 2]; x.w += dq[4 * u + 3];
                     y.x += dk[4 * u + 0] + bm * em * wt[4 * u + 0];
                     y.y += dk[4 * u + 1] + bm * em * wt[4 * u + 1];
@@ -337,13 +351,21 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
                 }
             }
         }
-        if (live) {
-            sk /= rkm;
-            sm.dbeta[m] += em * sk + su;
-            sm.dG[m] += bm * em * sk;
+        if (active) {
+            sm.sk[grp][m] = sk;
+            sm.su[grp][m] = su;
         }
     } else if (tid == 0 && a.status) {
         atomicOr(a.status, 2);
+    }
+    __syncthreads();
+    if (ok && tid < 64 && tid < L) {
+        const int m = tid;
+        const float em = expf(sm.G[m]), bm = sm.beta[m];
+        const float sk = (sm.sk[0][m] + sm.sk[1][m]) / sm.rk[m];
+        const float su = sm.su[0][m] + sm.su[1][m];
+        sm.dbeta[m] += em * sk + su;
+        sm.dG[m] += bm * em * sk;
     }
     __syncthreads();
     if (ok && tid == 0) {  // dg = reverse cumsum of dG within the chunk
@@ -376,6 +398,7 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BbSmem) + 1024;
+    static_assert(sizeof(BbSmem) + 1024 <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(k_bintra_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -34,6 +34,8 @@ struct BaSmem {
     unsigned char dO[2 * kBox];   // [t][v]
     unsigned char dvn[2 * kBox];
     unsigned char vn[2 * kBox];
+    unsigned char q[2 * kBox];    // [t][k]
+    unsigned char k[2 * kBox];
     float red[4][2][64];          // per-warp partial column sums
     float part[kThr / 32];
     float eg[64], egl_g[64];      // e^{G_t}, e^{G_L - G_t} (0 past L)
@@ -42,7 +44,7 @@ struct BaSmem {
 };
 
 struct BaMaps {
-    CUtensorMap h, dh, dO, dvn, vn;
+    CUtensorMap h, dh, dO, dvn, vn, q, k;
 };
 
 __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
@@ -71,7 +73,11 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     tc_fence_after();
     if (tid == 0) {
         const int row = (c * a.HV + hv) * 128;
-        mbar_arrive_expect_tx(&sm.tma_bar, 4 * kBig + 6 * kBox);
+        mbar_arrive_expect_tx(&sm.tma_bar, 4 * kBig + 10 * kBox);
+        tma_load_3d(sm.q, &maps.q, 0, h, t0, &sm.tma_bar);
+        tma_load_3d(sm.q + kBox, &maps.q, 64, h, t0, &sm.tma_bar);
+        tma_load_3d(sm.k, &maps.k, 0, h, t0, &sm.tma_bar);
+        tma_load_3d(sm.k + kBox, &maps.k, 64, h, t0, &sm.tma_bar);
         tma_load_3d(sm.h, &maps.h, 0, 0, row, &sm.tma_bar);
         tma_load_3d(sm.h + kBig, &maps.h, 64, 0, row, &sm.tma_bar);
         tma_load_3d(sm.dh, &maps.dh, 0, 0, row, &sm.tma_bar);
@@ -135,14 +141,14 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 float xq = 0.f, xk = 0.f;
                 if (t < L) {
                     const size_t o = ((size_t)(t0 + t) * a.HV + hv) * kDim + kk;
-                    const size_t qrow = ((size_t)(t0 + t) * a.H + h) * kDim + kk;
+                    const uint32_t so = (kk >> 6) * kBox + sw128_off(t, kk & 63);
                     const float dq = sm.eg[t] * rq_[j];
                     const float dk = sm.egl_g[t] * rk_[j];
                     a.dqp[o] = dq;
                     a.dW[o] = f2bf(-rw_[j]);
                     a.dkp[o] = dk;
-                    xq = bf2f(a.q[qrow]) * dq;
-                    xk = bf2f(a.k[qrow]) * dk;
+                    xq = bf2f(*reinterpret_cast<const bf16 *>(sm.q + so)) * dq;
+                    xk = bf2f(*reinterpret_cast<const bf16 *>(sm.k + so)) * dk;
                 }
                 xq = warp_sum(xq);
                 xk = warp_sum(xk);
@@ -194,7 +200,9 @@ cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.dh, a.dhc, 1, hrows, rowb, rowb, 128) ||
         !encode_rows_bf16(&m.dO, a.d_o, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.vn, a.vnew, a.HV, a.T, rowb, rowb * a.HV, 64))
+        !encode_rows_bf16(&m.vn, a.vnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
+        !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BaSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(k_bintra_a_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -29,7 +29,7 @@ using namespace umma;
 
 constexpr int kThr = 128;
 constexpr uint32_t kTileBytes = 64 * 128;
-constexpr uint32_t kStageBytes = 8 * kTileBytes;  // K, Q, w, dO: two boxes each
+constexpr uint32_t kStageBytes = 10 * kTileBytes;  // K, Q, w, dO, dv_loc: two boxes each
 
 struct BStateSmem {
     unsigned char a_ds[2 * 128 * 128];  // dS' bf16 [v][k]
@@ -38,6 +38,7 @@ struct BStateSmem {
     unsigned char stage[2][kStageBytes];
     float kc[64];                       // e^{G_L - G_t} / r_k,t (0 past L)
     float qc[64];                       // e^{G_t} scale / r_q,t (0 past L)
+    float gt[64], rkt[64], rqt[64];     // this chunk's G, r_k, r_q (prefetched)
     uint64_t tma_bar[2];
     uint64_t mma_bar;
     uint32_t tmem_base;
@@ -45,7 +46,7 @@ struct BStateSmem {
 };
 
 struct BStateMaps {
-    CUtensorMap k, q, w, dO;
+    CUtensorMap k, q, w, dO, dl;
 };
 
 __device__ __forceinline__ void issue_stage(const BStateMaps &m, BStateSmem &sm, int st, int t0,
@@ -61,6 +62,8 @@ __device__ __forceinline__ void issue_stage(const BStateMaps &m, BStateSmem &sm,
     tma_load_3d(b + 5 * kTileBytes, &m.w, 64, hv, t0, bar);
     tma_load_3d(b + 6 * kTileBytes, &m.dO, 0, hv, t0, bar);
     tma_load_3d(b + 7 * kTileBytes, &m.dO, 64, hv, t0, bar);
+    tma_load_3d(b + 8 * kTileBytes, &m.dl, 0, hv, t0, bar);
+    tma_load_3d(b + 9 * kTileBytes, &m.dl, 64, hv, t0, bar);
 }
 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -114,17 +117,37 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t idS = idesc_bf16(128, 128, 0, 1);
     uint32_t mma_phase = 0;
     bool ok = true;
+    // per-token scalars of the next chunk, loaded one chunk ahead
+    float pg = 0.f, prk = 1.f, prq = 1.f;
+    auto fetch = [&](int cc) {
+        const int tt0 = a.chunk_start[cc], LL = a.chunk_len[cc];
+        if (tid < LL) {
+            const size_t t = (size_t)(tt0 + tid);
+            pg = a.G[t * a.HV + hv];
+            prk = a.rk[t * a.H + h];
+            prq = a.rq[t * a.H + h];
+        } else {
+            pg = 0.f; prk = 1.f; prq = 1.f;
+        }
+    };
+    if (tid < 64 && nch > 0) fetch(ce - 1);
     for (int i = 0; i < nch; ++i) {
         const int c = ce - 1 - i, st = i & 1;
         const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-        const float Gl = L > 0 ? a.G[(size_t)(t0 + L - 1) * a.HV + hv] : 0.f;
+        if (tid < 64) {
+            sm.gt[tid] = pg;
+            sm.rkt[tid] = prk;
+            sm.rqt[tid] = prq;
+            if (i + 1 < nch) fetch(c - 1);
+        }
+        __syncthreads();
+        const float Gl = L > 0 ? sm.gt[L - 1] : 0.f;
         if (tid < 64) {
             float kk = 0.f, qq = 0.f;
             if (tid < L) {
-                const size_t t = (size_t)(t0 + tid);
-                const float Gt = a.G[t * a.HV + hv];
-                kk = expf(Gl - Gt) / a.rk[t * a.H + h];
-                qq = expf(Gt) * a.scale / a.rq[t * a.H + h];
+                const float Gt = sm.gt[tid];
+                kk = expf(Gl - Gt) / sm.rkt[tid];
+                qq = expf(Gt) * a.scale / sm.rqt[tid];
             }
             sm.kc[tid] = kk;
             sm.qc[tid] = qq;
@@ -186,14 +209,13 @@ __global__ void __launch_bounds__(kThr, 1)
         if (!mbar_wait(&sm.mma_bar, mma_phase)) sm.error = 1;
         mma_phase ^= 1;
         tc_fence_after();
-        // 3. dv_new^T = dv_loc^T + kc_t Pd  (dv_loc loads issued before any store)
+        // 3. dv_new^T = dv_loc^T + kc_t Pd  (dv_loc from the chunk's TMA tile)
+        const unsigned char *dls = sm.stage[st] + 8 * kTileBytes + (v >> 6) * kTileBytes;
         for (int tc = 0; tc < 2; ++tc) {
             float p[32], dl[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = tc * 32 + j;
-                dl[j] = t < L ? __ldg(a.dvloc + ((size_t)(t0 + t) * a.HV + hv) * kDim + v) : 0.f;
-            }
+            for (int j = 0; j < 32; ++j)
+                dl[j] = bf2f(*reinterpret_cast<const bf16 *>(dls + sw128_off(tc * 32 + j, v & 63)));
             tmem_ld32(tP + tc * 32, p);
             tmem_ld_wait();
 #pragma unroll
@@ -271,9 +293,11 @@ cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s) {
     if (a.T > 0 && (!encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
                     !encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
                     !encode_rows_bf16(&m.w, a.w, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-                    !encode_rows_bf16(&m.dO, a.d_o, a.HV, a.T, rowb, rowb * a.HV, 64)))
+                    !encode_rows_bf16(&m.dO, a.d_o, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+                    !encode_rows_bf16(&m.dl, a.dvloc, a.HV, a.T, rowb, rowb * a.HV, 64)))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BStateSmem) + 1024;
+    static_assert(sizeof(BStateSmem) + 1024 <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(k_bstate_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

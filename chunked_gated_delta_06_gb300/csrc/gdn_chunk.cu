@@ -1,0 +1,192 @@
+// gdn_chunk.cu -- the small CUDA-core kernels of the chunk path and the launch
+// order of the forward and backward.
+//
+//   k_plan   chunk table from the device copy of cu_seqlens (chunks of 64
+//            tokens never span sequences, the last one of a sequence may be
+//            partial), "[Cake 1/13] gdn: chunked gated delta rule ...", API;
+//   k_prep   q / k norms r = sqrt(sum x^2 + 1e-6) ("C6: GDN decode-step
+//            goldens ...", Provider: divide by the sqrt) and the chunk-local
+//            cumulative sum G of g;
+//   k_bnorm  fixed-order sum of the per-value-head gradients of qhat / khat
+//            over the HV / H value heads of each key head, then the L2-norm
+//            backward dx = (dn - n (n . dn)) / r.
+// The tensor-core kernels of the chunked (WY) form live in gdn_*_tc.cu.
+// Every reduction runs in a fixed order and no kernel uses atomics, so results
+// are bit-identical from run to run.
+#include "gdn_kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+
+// ---------------------------------------------------------------------------
+// Chunk table from the device cu_seqlens (one block).  Host code computed the
+// chunk count from the host copy; a mismatch sets *status.
+__global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunks, int *seq_off,
+                       int *chunk_seq, int *chunk_start, int *chunk_len, int *status) {
+    __shared__ int sums[1024];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (N + nt - 1) / nt;
+    const int b = min(N, tid * per), e = min(N, b + per);
+    int cnt = 0;
+    for (int n = b; n < e; ++n) cnt += (max(cu[n + 1] - cu[n], 0) + kChunk - 1) / kChunk;
+    sums[tid] = cnt;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {
+        int x = tid >= off ? sums[tid - off] : 0;
+        __syncthreads();
+        sums[tid] += x;
+        __syncthreads();
+    }
+    int base = sums[tid] - cnt;
+    for (int n = b; n < e; ++n) {
+        seq_off[n] = base;
+        int L = max(cu[n + 1] - cu[n], 0);
+        for (int j = 0; j * kChunk < L; ++j) {
+            int c = base + j;
+            if (c < total_chunks) {
+                // clamp to [0, T): a device copy of cu_seqlens that disagrees with
+                // the host copy yields empty chunks and a status flag, never an
+                // out-of-bounds access
+                const int st = min(max(cu[n] + j * kChunk, 0), T);
+                chunk_seq[c] = n;
+                chunk_start[c] = st;
+                chunk_len[c] = max(0, min(min(kChunk, L - j * kChunk), T - st));
+            }
+        }
+        base += (L + kChunk - 1) / kChunk;
+    }
+    __syncthreads();
+    if (tid == nt - 1) {
+        seq_off[N] = min(sums[tid], total_chunks);
+        if (status) *status = (sums[tid] != total_chunks || cu[N] != T) ? 1 : 0;
+    }
+    // keep every sequence's chunk range inside [0, total_chunks]
+    for (int n = b; n < e; ++n) seq_off[n] = min(seq_off[n], total_chunks);
+}
+
+// ---------------------------------------------------------------------------
+// Norms of q and k rows and the chunk-local cumsum of g.  grid (chunks, H).
+__global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
+    const int c = blockIdx.x, h = blockIdx.y;
+    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
+    if (L <= 0) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = warp; i < L; i += kThreads / 32) {
+        const size_t row = ((size_t)(t0 + i) * a.H + h) * kDim;
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float x = bf2f(a.q[row + lane * 4 + e]);
+            float y = bf2f(a.k[row + lane * 4 + e]);
+            sq += x * x;
+            sk += y * y;
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        if (lane == 0) {
+            a.rq[(size_t)(t0 + i) * a.H + h] = sqrtf(sq + kNormEps);
+            a.rk[(size_t)(t0 + i) * a.H + h] = sqrtf(sk + kNormEps);
+        }
+    }
+    const int r = a.HV / a.H;
+    for (int j = warp; j < r; j += kThreads / 32) {
+        const int hv = h * r + j;
+        const int i0 = 2 * lane, i1 = 2 * lane + 1;
+        float x0 = i0 < L ? a.g[(size_t)(t0 + i0) * a.HV + hv] : 0.f;
+        float x1 = i1 < L ? a.g[(size_t)(t0 + i1) * a.HV + hv] : 0.f;
+        float s = x0 + x1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            float y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        float excl = s - (x0 + x1);
+        if (i0 < L) a.G[(size_t)(t0 + i0) * a.HV + hv] = excl + x0;
+        if (i1 < L) a.G[(size_t)(t0 + i1) * a.HV + hv] = excl + x0 + x1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward, step 5: sum the per-value-head gradients of qhat / khat over the
+// HV / H value heads of each key head (fixed order) and apply the L2-norm
+// backward dx = (dn - n (n . dn)) / r.  One warp per (token, key head).
+__global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t item = (size_t)blockIdx.x * (kThreads / 32) + warp;
+    if (item >= (size_t)a.T * a.H) return;
+    const int t = (int)(item / a.H), h = (int)(item % a.H);
+    const int r = a.HV / a.H;
+    float dq[4] = {0, 0, 0, 0}, dk[4] = {0, 0, 0, 0}, xq[4], xk[4];
+    for (int j = 0; j < r; ++j) {
+        const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + lane * 4;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            dq[u] += a.dqp[o + u];
+            dk[u] += a.dkp[o + u];
+        }
+    }
+    const size_t row = ((size_t)t * a.H + h) * kDim + lane * 4;
+    const float rq = a.rq[(size_t)t * a.H + h], rk = a.rk[(size_t)t * a.H + h];
+    float nq = 0.f, nk = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        xq[u] = bf2f(a.q[row + u]) / rq;
+        xk[u] = bf2f(a.k[row + u]) / rk;
+        dq[u] *= a.scale;
+        nq += xq[u] * dq[u];
+        nk += xk[u] * dk[u];
+    }
+    nq = warp_sum(nq);
+    nk = warp_sum(nk);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        a.dq[row + u] = f2bf((dq[u] - xq[u] * nq) / rq);
+        a.dk[row + u] = f2bf((dk[u] - xk[u] * nk) / rk);
+    }
+}
+
+
+}  // namespace
+
+cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s) {
+    TimerScope ts(a.timer, GDN_KERNEL_PLAN, s);
+    k_plan<<<1, 1024, 0, s>>>(a.cu_dev, a.N, a.T, a.num_chunks, a.seq_chunk_off, a.chunk_seq,
+                              a.chunk_start, a.chunk_len, a.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s) {
+    if (a.num_chunks == 0) return cudaSuccess;
+    TimerScope ts(a.timer, GDN_KERNEL_PREP, s);
+    k_prep<<<dim3(a.num_chunks, a.H), kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = launch_intra_tc(a, s)) != cudaSuccess) return e;
+    if ((e = launch_state_tc(a, s)) != cudaSuccess) return e;
+    if ((e = launch_out_tc(a, s)) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = launch_dvloc_tc(a, s)) != cudaSuccess) return e;
+    if ((e = launch_bstate_tc(a, s)) != cudaSuccess) return e;
+    if (a.num_chunks == 0) return cudaSuccess;
+    if ((e = launch_bintra_a_tc(a, s)) != cudaSuccess) return e;
+    if ((e = launch_bintra_b_tc(a, s)) != cudaSuccess) return e;
+    {
+        const size_t items = (size_t)a.T * a.H;
+        const unsigned blocks = (unsigned)((items + kThreads / 32 - 1) / (kThreads / 32));
+        TimerScope ts(a.timer, GDN_KERNEL_BNORM, s);
+        k_bnorm<<<blocks, kThreads, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace gdn

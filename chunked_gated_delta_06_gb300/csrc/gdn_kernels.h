@@ -40,7 +40,7 @@ struct ChunkArgs {
     const float *d_ht;      // or null
     bf16 *dq, *dk, *dv, *dbeta;
     float *dg, *dh0;        // dh0 may be null
-    float *dvloc;           // [T,HV,V]  tril(M)^T dO
+    bf16 *dvloc;            // [T,HV,V]  tril(M)^T dO
     bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
     bf16 *dhc;              // [C_total,HV,K,V] gradient of the state after each chunk
     bf16 *dW;               // [T,HV,K]

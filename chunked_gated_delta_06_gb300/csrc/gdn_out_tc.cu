@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
                         const float ct = expf(sm.G[t]) * a.scale / sm.rq[t];
                         a.o[o] = f2bf(ct * r1[j] + r2[j]);
                     } else {
-                        a.dvloc[o] = r1[j];
+                        a.dvloc[o] = f2bf(r1[j]);
                     }
                 }
             }

@@ -38,6 +38,7 @@ struct StateSmem {
     unsigned char a_v[128 * 128];       // A_V bf16 [v][t]: 128 x 128 B
     unsigned char stage[2][kStageBytes];
     float coef[2][64];                  // e^{G_L - G_t} / r_k,t, 0 past L
+    float gt[64], rkt[64];              // this chunk's G and r_k (prefetched)
     uint64_t tma_bar[2];
     uint64_t mma_bar;
     uint32_t tmem_base;
@@ -109,18 +110,30 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t idS = idesc_bf16(128, 128, 0, 1);   // S += A_V K  (K MN-major)
     uint32_t mma_phase = 0;
     bool ok = true;
+    // per-token scalars of the next chunk, loaded one chunk ahead
+    float pg = 0.f, prk = 1.f;
+    auto fetch = [&](int cc) {
+        const int tt0 = a.chunk_start[cc], LL = a.chunk_len[cc];
+        if (tid < LL) {
+            const size_t t = (size_t)(tt0 + tid);
+            pg = a.G[t * a.HV + hv];
+            prk = a.rk[t * a.H + h];
+        } else {
+            pg = 0.f; prk = 1.f;
+        }
+    };
+    if (tid < 64 && nch > 0) fetch(cb);
     for (int i = 0; i < nch && ok; ++i) {
         const int c = cb + i, st = i & 1;
         const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-        const float Gl = L > 0 ? a.G[(size_t)(t0 + L - 1) * a.HV + hv] : 0.f;
         if (tid < 64) {
-            float cf = 0.f;
-            if (tid < L) {
-                const size_t t = (size_t)(t0 + tid);
-                cf = expf(Gl - a.G[t * a.HV + hv]) / a.rk[t * a.H + h];
-            }
-            sm.coef[st][tid] = cf;
+            sm.gt[tid] = pg;
+            sm.rkt[tid] = prk;
+            if (i + 1 < nch) fetch(c + 1);
         }
+        __syncthreads();
+        const float Gl = L > 0 ? sm.gt[L - 1] : 0.f;
+        if (tid < 64) sm.coef[st][tid] = tid < L ? expf(Gl - sm.gt[tid]) / sm.rkt[tid] : 0.f;
         const float egl = expf(Gl);
         // 1. S -> bf16 operand + h_c, then S <- e^{G_L} S
         bf16 *hdst = a.hc + ((size_t)c * a.HV + hv) * kDim * kDim;

@@ -256,9 +256,17 @@ def decode_workload(name: str = "decode_256", B: int = 256, H: int = 16, HV: int
                           beta=beta, pool=pool, state_indices=idx)
 
 
+def fb_8192(seed: int = 0) -> ChunkWorkload:
+    """1 x 8192 tokens, H=16, HV=32, initial state: a profiling-size case of the same
+    value recipe (inputs about 200 MB, above the 129 MB L2)."""
+    return chunk_workload("fb_8192", [8192], 16, 32, seed=seed, gate="softplus", h0=True,
+                          backward=True, d_ht=False)
+
+
 CHUNK_CONFIGS = {
     "fwd_t256": fwd_t256,
     "fb_4x4096": fb_4x4096,
     "fb_32k_varlen": fb_32k_varlen,
     "fb_65536_long": fb_65536_long,
+    "fb_8192": fb_8192,
 }

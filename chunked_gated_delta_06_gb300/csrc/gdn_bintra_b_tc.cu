@@ -12,7 +12,7 @@
 //     M_ij  = QK_ij scale / (r_q,i r_k,j) Gamma_ij       (j <= i)
 //     dMG   = dM (.) Gamma,  P1 = dM (.) M  -> dG
 //     dT_ij = beta_j (e^{G_j} D1_ij / r_k,j + D2_ij)     (j < i)
-//   CUDA cores (fp32):  X = dT T^T,  dA = -T^T X (strictly lower),
+//   phase 1b/1c (K = 64): X = dT T^T,  dA = -T^T X (strictly lower)
 //     B = dA (.) beta_i Gamma,  P2 = dA (.) KKhat Gamma -> dbeta, dG
 //   phase 2 (K = 64):   dq  = dMG diag(1/r_k) K
 //                       dk  = (diag(scale/r_q) dMG)^T Q + B diag(1/r_k) K
@@ -39,18 +39,23 @@ constexpr uint32_t kTile = 2 * 64 * 128;  // 64 rows x 128 bf16: two 8 KB k-halv
 constexpr uint32_t kHalf = 64 * 128;
 constexpr int kF = 65;                     // fp32 64 x 64 pitch
 
+// TMEM columns
+constexpr uint32_t cDM = 0, cQK = 64, cKK = 128, cD1 = 192, cD2 = 256, cX = 320, cA = 384;
+constexpr uint32_t cDQ = 0, cDK = 128, cWT = 256, cUT = 384;
+
 struct BbSmem {
     unsigned char q[kTile], k[kTile], v[kTile], dO[kTile], vn[kTile], dvn[kTile], dw[kTile];
     unsigned char op_dmg[kHalf];    // dMG_ij / r_k,j        [m][j]  K-major A
     unsigned char op_dmgt[kHalf];   // dMG_ij scale / r_q,i  [i][m]  MN-major A
     unsigned char op_b[kHalf];      // B_mj / r_k,j          [m][j]  K-major A
     unsigned char op_bt[kHalf];     // B_im / r_k,i          [i][m]  MN-major A
-    unsigned char op_t[kHalf];      // T_im                  [i][m]  MN-major A
-    float T[64 * kF];
-    float dT[64 * kF];              // dT, then dA
-    float X[64 * kF];               // P1, then X, then P2
-    float KG[64 * kF];              // KKhat (.) Gamma, strictly lower
+    unsigned char op_t[kHalf];      // T_ij rows i: K-major B of X, MN-major A of T^T X, T^T dW
+    unsigned char op_dt[kHalf];     // dT_rb rows r: K-major A of X = dT T^T
+    unsigned char op_x[kHalf];      // X_rj rows r: MN-major B of T^T X
+    float C[64 * kF];               // P1_ij + beta_i P2_ij (column sums give dG)
     float G[64], beta[64], rq[64], rk[64], dG[64], dbeta[64];
+    float rs[2][64];                // per-warpgroup partial row sums of P2
+    float cs[4][64];                // partial column sums of C
     float sk[2][64], su[2][64];     // per-warpgroup partial row dots
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
@@ -126,12 +131,24 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
         sm.dG[tid] = in ? a.dGp[gi] : 0.f;
         sm.dbeta[tid] = 0.f;
     }
-    const float *Tsrc = a.Tm + ((size_t)c * a.HV + hv) * 64 * 64;
-    for (int idx = tid; idx < 64 * 64; idx += kThr) sm.T[(idx >> 6) * kF + (idx & 63)] = Tsrc[idx];
+    {  // T (fp32, saved by the forward) -> bf16 rows
+        const float *Tsrc = a.Tm + ((size_t)c * a.HV + hv) * 64 * 64;
+        for (int idx = tid; idx < 64 * 32; idx += kThr) {
+            const int i = idx >> 5, j2 = (idx & 31) * 2;
+            const float2 t2 = __ldg(reinterpret_cast<const float2 *>(Tsrc + i * 64 + j2));
+            *reinterpret_cast<uint32_t *>(sm.op_t + sw128_off(i, j2)) = pack_bf2(t2.x, t2.y);
+        }
+    }
+    fence_proxy_async_smem();
     bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t phase = 0;
+    auto commit_wait = [&](bool &okr) {
+        okr = __syncthreads_and(okr && mbar_wait(&sm.mma_bar, phase));
+        phase ^= 1;
+        tc_fence_after();
+    };
     // ---- phase 1: five 64 x 64 products, contraction 128
     if (tid == 0 && ok) {
         tc_fence_after();
@@ -140,28 +157,27 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
                                smem_u32(sm.dvn)};
         const uint32_t B[5] = {smem_u32(sm.vn), smem_u32(sm.k), smem_u32(sm.k), smem_u32(sm.k),
                                smem_u32(sm.v)};
+        const uint32_t col[5] = {cDM, cQK, cKK, cD1, cD2};
         for (int p = 0; p < 5; ++p)
             for (int s = 0; s < 8; ++s) {
                 const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-                mma_bf16(tb + 64 * p, sdesc(A[p] + off, 16, 1024), sdesc(B[p] + off, 16, 1024), id,
+                mma_bf16(tb + col[p], sdesc(A[p] + off, 16, 1024), sdesc(B[p] + off, 16, 1024), id,
                          s > 0);
             }
         mma_commit(&sm.mma_bar);
     }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
-    phase ^= 1;
-    tc_fence_after();
+    commit_wait(ok);
+    const int i = row;
+    const bool live = active && i < L;
+    const float Gi = active ? sm.G[i] : 0.f;
     if (ok) {
-        const int i = row;
-        const bool live = active && i < L;
-        const float Gi = active ? sm.G[i] : 0.f;
         if (grp == 0) {  // dM, QK -> M, dMG, P1 and the dMG operands
             const float qsi = active ? a.scale / sm.rq[i] : 0.f;
             float rsum = 0.f;
             for (int half = 0; half < 2; ++half) {
                 float dm[32], qk[32];
-                tmem_ld32(t_row + 0 + half * 32, dm);
-                tmem_ld32(t_row + 64 + half * 32, qk);
+                tmem_ld32(t_row + cDM + half * 32, dm);
+                tmem_ld32(t_row + cQK + half * 32, qk);
                 tmem_ld_wait();
                 float x1[32], x2[32];
 #pragma unroll
@@ -175,7 +191,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
                         p1 = dm[jj] * m;
                     }
                     rsum += p1;
-                    if (active) sm.X[i * kF + j] = p1;
+                    if (active) sm.C[i * kF + j] = p1;
                     x1[jj] = dmg / sm.rk[j];
                     x2[jj] = dmg * qsi;
                 }
@@ -185,98 +201,81 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
                 }
             }
             if (active) sm.dG[i] += rsum;
-        } else {  // KK, dW K^T, dv_new V^T -> KKhat Gamma, dT
+        } else {  // dW K^T, dv_new V^T -> dT row (bf16 operand)
             for (int half = 0; half < 2; ++half) {
-                float kk[32], d1[32], d2[32];
-                tmem_ld32(t_row + 128 + half * 32, kk);
-                tmem_ld32(t_row + 192 + half * 32, d1);
-                tmem_ld32(t_row + 256 + half * 32, d2);
+                float d1[32], d2[32];
+                tmem_ld32(t_row + cD1 + half * 32, d1);
+                tmem_ld32(t_row + cD2 + half * 32, d2);
                 tmem_ld_wait();
-                if (active) {
-#pragma unroll 8
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = half * 32 + jj;
-                        float kg = 0.f, dt = 0.f;
-                        if (live && j < i) {
-                            const float Gj = sm.G[j];
-                            kg = kk[jj] / (sm.rk[i] * sm.rk[j]) * expf(Gi - Gj);
-                            dt = sm.beta[j] * (expf(Gj) / sm.rk[j] * d1[jj] + d2[jj]);
-                        }
-                        sm.KG[i * kF + j] = kg;
-                        sm.dT[i * kF + j] = dt;
-                    }
+                float dt[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = half * 32 + jj;
+                    dt[jj] = (live && j < i) ? sm.beta[j] * (expf(sm.G[j]) / sm.rk[j] * d1[jj] + d2[jj]) : 0.f;
                 }
+                if (active) put_row32(sm.op_dt, i, half * 32, dt);
             }
         }
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---- CUDA-core part
-    if (ok) {
-        if (tid < 64) {  // column sums of P1
-            float cs = 0.f;
-            for (int r = 0; r < 64; ++r) cs += sm.X[r * kF + tid];
-            sm.dG[tid] -= cs;
-        }
-        __syncthreads();
-        // X = dT T^T
-        for (int idx = tid; idx < 64 * 64; idx += kThr) {
-            const int r = idx >> 6, j = idx & 63;
-            float s = 0.f;
-            for (int b = 0; b <= j; ++b) s += sm.dT[r * kF + b] * sm.T[j * kF + b];
-            sm.X[r * kF + j] = s;
-        }
-        __syncthreads();
-        // dA = -T^T X, strictly lower (into dT)
-        for (int idx = tid; idx < 64 * 64; idx += kThr) {
-            const int i = idx >> 6, j = idx & 63;
-            float da = 0.f;
-            if (j < i && i < L)
-                for (int r = i; r < L; ++r) da -= sm.T[r * kF + i] * sm.X[r * kF + j];
-            sm.dT[i * kF + j] = da;
-        }
-        __syncthreads();
-        // B = dA (.) beta_i Gamma (operands), P2 = dA (.) KG (into X)
-        for (int idx = tid; idx < 64 * 64; idx += kThr) {
-            const int i = idx >> 6, j = idx & 63;
-            const float da = sm.dT[i * kF + j];
-            float b = 0.f;
-            if (j < i && i < L) b = da * sm.beta[i] * expf(sm.G[i] - sm.G[j]);
-            sm.X[i * kF + j] = da * sm.KG[i * kF + j];
-            sm.KG[i * kF + j] = b;  // KG now holds B
-        }
-        __syncthreads();
-        if (tid < 64) {
-            const int i = tid;
-            float rs = 0.f, cs = 0.f;
-            for (int j = 0; j < 64; ++j) {
-                rs += sm.X[i * kF + j];
-                cs += sm.beta[j] * sm.X[j * kF + i];
+    // ---- phase 1b: X = dT T^T  (A = dT rows, B = T rows as [N][K])
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(64, 64, 0, 0);
+        for (int s = 0; s < 4; ++s)
+            mma_bf16(tb + cX, sdesc(smem_u32(sm.op_dt) + s * 32, 16, 1024),
+                     sdesc(smem_u32(sm.op_t) + s * 32, 16, 1024), id, s > 0);
+        mma_commit(&sm.mma_bar);
+    }
+    commit_wait(ok);
+    if (ok) {  // X rows -> bf16 (each warpgroup one half of the columns)
+        float x[32];
+        tmem_ld32(t_row + cX + grp * 32, x);
+        tmem_ld_wait();
+        if (active) put_row32(sm.op_x, i, grp * 32, x);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- phase 1c: T^T X  (A = T rows read MN-major, B = X rows read MN-major)
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(64, 64, 1, 1);
+        for (int s = 0; s < 4; ++s)
+            mma_bf16(tb + cA, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024),
+                     sdesc(smem_u32(sm.op_x) + s * 2048, kHalf, 1024), id, s > 0);
+        mma_commit(&sm.mma_bar);
+    }
+    commit_wait(ok);
+    if (ok) {  // dA = -(T^T X): B, P2, and their operands; warpgroup g takes columns [32g, 32g+32)
+        float ta[32], kk[32];
+        tmem_ld32(t_row + cA + grp * 32, ta);
+        tmem_ld32(t_row + cKK + grp * 32, kk);
+        tmem_ld_wait();
+        float b1[32], b2[32], rsp = 0.f;
+        const float bi = active ? sm.beta[i] : 0.f;
+        const float rki = active ? sm.rk[i] : 1.f;
+#pragma unroll 8
+        for (int jj = 0; jj < 32; ++jj) {
+            const int j = grp * 32 + jj;
+            float b = 0.f, p2 = 0.f;
+            if (live && j < i) {
+                const float da = -ta[jj];
+                const float gam = expf(Gi - sm.G[j]);
+                b = da * bi * gam;
+                p2 = da * kk[jj] / (rki * sm.rk[j]) * gam;
             }
-            sm.dbeta[i] += rs;
-            sm.dG[i] += sm.beta[i] * rs - cs;
+            rsp += p2;
+            if (active) sm.C[i * kF + j] += bi * p2;
+            b1[jj] = b / sm.rk[j];
+            b2[jj] = b / rki;
         }
-        // operands B', Bt' (warpgroup 0) and T (warpgroup 1), bf16 rows
         if (active) {
-            const int m = row;
-            for (int half = 0; half < 2; ++half) {
-                if (grp == 0) {
-                    float b1[32], b2[32];
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const float b = sm.KG[m * kF + half * 32 + jj];
-                        b1[jj] = b / sm.rk[half * 32 + jj];
-                        b2[jj] = b / sm.rk[m];
-                    }
-                    put_row32(sm.op_b, m, half * 32, b1);
-                    put_row32(sm.op_bt, m, half * 32, b2);
-                } else {
-                    float tt[32];
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) tt[jj] = sm.T[m * kF + half * 32 + jj];
-                    put_row32(sm.op_t, m, half * 32, tt);
-                }
-            }
+            put_row32(sm.op_b, i, grp * 32, b1);
+            put_row32(sm.op_bt, i, grp * 32, b2);
+            sm.rs[grp][i] = rsp;
         }
     }
     fence_proxy_async_smem();
@@ -293,32 +292,45 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
             const uint64_t bK = sdesc(kA + s * 2048, kHalf, 1024), bQ = sdesc(qA + s * 2048, kHalf, 1024);
             const uint64_t bW = sdesc(dwA + s * 2048, kHalf, 1024), bV = sdesc(dvA + s * 2048, kHalf, 1024);
             const bool acc = s > 0;
-            mma_bf16(tb + 0, sdesc(smem_u32(sm.op_dmg) + s * 32, 16, 1024), bK, id_km, acc);
-            mma_bf16(tb + 128, sdesc(smem_u32(sm.op_dmgt) + s * 2048, kHalf, 1024), bQ, id_mm, acc);
-            mma_bf16(tb + 128, sdesc(smem_u32(sm.op_b) + s * 32, 16, 1024), bK, id_km, true);
-            mma_bf16(tb + 128, sdesc(smem_u32(sm.op_bt) + s * 2048, kHalf, 1024), bK, id_mm, true);
-            mma_bf16(tb + 256, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024), bW, id_mm, acc);
-            mma_bf16(tb + 384, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024), bV, id_mm, acc);
+            mma_bf16(tb + cDQ, sdesc(smem_u32(sm.op_dmg) + s * 32, 16, 1024), bK, id_km, acc);
+            mma_bf16(tb + cDK, sdesc(smem_u32(sm.op_dmgt) + s * 2048, kHalf, 1024), bQ, id_mm, acc);
+            mma_bf16(tb + cDK, sdesc(smem_u32(sm.op_b) + s * 32, 16, 1024), bK, id_km, true);
+            mma_bf16(tb + cDK, sdesc(smem_u32(sm.op_bt) + s * 2048, kHalf, 1024), bK, id_mm, true);
+            mma_bf16(tb + cWT, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024), bW, id_mm, acc);
+            mma_bf16(tb + cUT, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024), bV, id_mm, acc);
         }
         mma_commit(&sm.mma_bar);
     }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
-    tc_fence_after();
+    // meanwhile: row sums of P2 and column sums of C = P1 + beta_i P2
+    if (ok) {
+        if (tid < 64 && tid < L) {
+            const float r2 = sm.rs[0][tid] + sm.rs[1][tid];
+            sm.dbeta[tid] += r2;
+            sm.dG[tid] += sm.beta[tid] * r2;
+        }
+        const int jcol = tid & 63, part = tid >> 6;
+        float cs = 0.f;
+        for (int r = part * 16; r < part * 16 + 16; ++r) cs += sm.C[r * kF + jcol];
+        sm.cs[part][jcol] = cs;
+    }
+    __syncthreads();
+    if (ok && tid < 64) sm.dG[tid] -= sm.cs[0][tid] + sm.cs[1][tid] + sm.cs[2][tid] + sm.cs[3][tid];
+    commit_wait(ok);
     if (ok) {
         const int m = row;
-        const bool live = active && m < L;
-        const float em = live ? expf(sm.G[m]) : 0.f;
-        const float bm = live ? sm.beta[m] : 0.f;
+        const bool mlive = active && m < L;
+        const float em = mlive ? expf(sm.G[m]) : 0.f;
+        const float bm = mlive ? sm.beta[m] : 0.f;
         float sk = 0.f, su = 0.f;
-        const size_t o = ((size_t)(t0 + (live ? m : 0)) * a.HV + hv) * kDim;
+        const size_t o = ((size_t)(t0 + (mlive ? m : 0)) * a.HV + hv) * kDim;
         for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {  // this warpgroup's 64 columns
             float dq[32], dk[32], wt[32], ut[32];
-            tmem_ld32(t_row + 0 + cc * 32, dq);
-            tmem_ld32(t_row + 128 + cc * 32, dk);
-            tmem_ld32(t_row + 256 + cc * 32, wt);
-            tmem_ld32(t_row + 384 + cc * 32, ut);
+            tmem_ld32(t_row + cDQ + cc * 32, dq);
+            tmem_ld32(t_row + cDK + cc * 32, dk);
+            tmem_ld32(t_row + cWT + cc * 32, wt);
+            tmem_ld32(t_row + cUT + cc * 32, ut);
             tmem_ld_wait();
-            if (live) {
+            if (mlive) {
                 float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
                 float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
                 float4 xs[8], ys[8];  // all loads before any store
@@ -359,22 +371,39 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
         atomicOr(a.status, 2);
     }
     __syncthreads();
-    if (ok && tid < 64 && tid < L) {
-        const int m = tid;
-        const float em = expf(sm.G[m]), bm = sm.beta[m];
-        const float sk = (sm.sk[0][m] + sm.sk[1][m]) / sm.rk[m];
-        const float su = sm.su[0][m] + sm.su[1][m];
-        sm.dbeta[m] += em * sk + su;
-        sm.dG[m] += bm * em * sk;
-    }
-    __syncthreads();
-    if (ok && tid == 0) {  // dg = reverse cumsum of dG within the chunk
-        float acc = 0.f;
-        for (int i = L - 1; i >= 0; --i) {
-            acc += sm.dG[i];
-            const size_t gi = (size_t)(t0 + i) * a.HV + hv;
-            a.dg[gi] = acc;
-            a.dbeta[gi] = f2bf(sm.dbeta[i]);
+    if (ok && warp == 0) {  // dbeta, dG of the WY terms; dg = reverse cumsum of dG (warp scan)
+        float dgv[2], dbv[2];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+            const int m = 2 * lane + z;
+            float dgm = 0.f, dbm = 0.f;
+            if (m < L) {
+                const float em = expf(sm.G[m]), bm = sm.beta[m];
+                const float sk = (sm.sk[0][m] + sm.sk[1][m]) / sm.rk[m];
+                const float su = sm.su[0][m] + sm.su[1][m];
+                dbm = sm.dbeta[m] + em * sk + su;
+                dgm = sm.dG[m] + bm * em * sk;
+            }
+            dgv[z] = dgm;
+            dbv[z] = dbm;
+        }
+        // suffix sums over m: reverse inclusive scan of dG
+        float pair = dgv[0] + dgv[1];
+        float suf = pair;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_down_sync(0xffffffffu, suf, off);
+            if (lane + off < 32) suf += y;
+        }
+        const float after = suf - pair;  // sum over elements 2*lane+2 ...
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+            const int m = 2 * lane + z;
+            if (m < L) {
+                const size_t gi = (size_t)(t0 + m) * a.HV + hv;
+                a.dg[gi] = (z == 0 ? dgv[0] + dgv[1] : dgv[1]) + after;
+                a.dbeta[gi] = f2bf(dbv[z]);
+            }
         }
     }
     tc_fence_before();

@@ -27,7 +27,7 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThr = 128;
+constexpr int kThr = 256;   // two warpgroups share the 128 TMEM lanes
 constexpr uint32_t kHalf = 64 * 128;
 constexpr uint32_t kTile = 2 * kHalf;
 constexpr int kF = 65;
@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
     if (L <= 0) return;
     const bool active = lane < 16;
-    const int row = warp * 16 + lane;
+    const int grp = warp >> 2;              // warpgroup: which half of the columns
+    const int row = (warp & 3) * 16 + lane;
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
     if (tid < 64) sm.rk[tid] = tid < L ? a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
     bool ok = __syncthreads_and(mbar_wait(&sm.k_bar, 0));
     const uint32_t tb = sm.tmem_base;
-    const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t_row = tb + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t mphase = 0;
     if (tid == 0 && ok) {  // KK = K K^T into columns 0..63
         tc_fence_after();
@@ -152,21 +153,14 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
     ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
     mphase ^= 1;
     tc_fence_after();
-    // KKhat row i stays in registers of its owner thread for all value heads
-    float kk[64];
+    // KKhat row i, columns [32 grp, 32 grp + 32), stays in registers for all value heads
+    float kk[32];
     if (ok) {
-        float k0[32], k1[32];
-        tmem_ld32(t_row, k0);
-        tmem_ld32(t_row + 32, k1);
+        tmem_ld32(t_row + grp * 32, kk);
         tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            kk[j] = k0[j];
-            kk[32 + j] = k1[j];
-        }
         if (active) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) kk[j] /= (sm.rk[row] * sm.rk[j]);
+            for (int j = 0; j < 32; ++j) kk[j] /= (sm.rk[row] * sm.rk[grp * 32 + j]);
         }
     }
     for (int jv = 0; jv < r && ok; ++jv) {
@@ -183,39 +177,44 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
             sm.beta[tid] = in ? bf2f(a.beta[gi]) : 0.f;
         }
         __syncthreads();
-        if (active) {  // A row i
+        if (active) {  // A row i, this warpgroup's 32 columns
             const int i = row;
             const float Gi = sm.G[i], bi = sm.beta[i];
 #pragma unroll 8
-            for (int j = 0; j < 64; ++j)
-                sm.A[i * kF + j] = (j < i && i < L) ? bi * kk[j] * expf(Gi - sm.G[j]) : 0.f;
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = grp * 32 + jj;
+                sm.A[i * kF + j] = (j < i && i < L) ? bi * kk[jj] * expf(Gi - sm.G[j]) : 0.f;
+            }
         }
         __syncthreads();
         tri_inverse(sm.A, sm.T, sm.X);
-        // operands T diag(beta e^G / r_k) and T diag(beta), and T to HBM
+        // operands T diag(beta e^G / r_k) (warpgroup 0, also T to HBM) and T diag(beta) (warpgroup 1)
         if (active) {
             const int i = row;
-            float *Tdst = a.Tm + ((size_t)c * a.HV + hv) * 64 * 64 + (size_t)i * 64;
+            float4 *Tdst = reinterpret_cast<float4 *>(a.Tm + ((size_t)c * a.HV + hv) * 64 * 64 + (size_t)i * 64);
             for (int half = 0; half < 2; ++half) {
-                float xw[32], xu[32];
+                float x[32];
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = half * 32 + jj;
                     const float t = sm.T[i * kF + j];
                     const float bj = sm.beta[j];
-                    xu[jj] = t * bj;
-                    xw[jj] = (j < L) ? t * bj * expf(sm.G[j]) / sm.rk[j] : 0.f;
-                    Tdst[j] = t;
+                    if (grp == 0) x[jj] = (j < L) ? t * bj * expf(sm.G[j]) / sm.rk[j] : 0.f;
+                    else x[jj] = t * bj;
                 }
+                if (grp == 0) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        Tdst[half * 8 + q] = make_float4(sm.T[i * kF + half * 32 + 4 * q], sm.T[i * kF + half * 32 + 4 * q + 1],
+                                                         sm.T[i * kF + half * 32 + 4 * q + 2], sm.T[i * kF + half * 32 + 4 * q + 3]);
+                }
+                unsigned char *op = grp == 0 ? sm.op_w : sm.op_u;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int col = half * 32 + q * 8;
-                    *reinterpret_cast<uint4 *>(sm.op_w + sw128_off(i, col)) =
-                        make_uint4(pack_bf2(xw[q * 8], xw[q * 8 + 1]), pack_bf2(xw[q * 8 + 2], xw[q * 8 + 3]),
-                                   pack_bf2(xw[q * 8 + 4], xw[q * 8 + 5]), pack_bf2(xw[q * 8 + 6], xw[q * 8 + 7]));
-                    *reinterpret_cast<uint4 *>(sm.op_u + sw128_off(i, col)) =
-                        make_uint4(pack_bf2(xu[q * 8], xu[q * 8 + 1]), pack_bf2(xu[q * 8 + 2], xu[q * 8 + 3]),
-                                   pack_bf2(xu[q * 8 + 4], xu[q * 8 + 5]), pack_bf2(xu[q * 8 + 6], xu[q * 8 + 7]));
+                    *reinterpret_cast<uint4 *>(op + sw128_off(i, col)) =
+                        make_uint4(pack_bf2(x[q * 8], x[q * 8 + 1]), pack_bf2(x[q * 8 + 2], x[q * 8 + 3]),
+                                   pack_bf2(x[q * 8 + 4], x[q * 8 + 5]), pack_bf2(x[q * 8 + 6], x[q * 8 + 7]));
                 }
             }
         }
@@ -236,25 +235,22 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
         ok = __syncthreads_and(mbar_wait(&sm.mma_bar, mphase));
         mphase ^= 1;
         tc_fence_after();
-        if (ok) {
+        if (ok) {  // warpgroup 0 writes w, warpgroup 1 writes u
             const int i = row;
             const bool live = active && i < L;
             const size_t o = ((size_t)(t0 + (live ? i : 0)) * a.HV + hv) * kDim;
+            bf16 *dst = grp == 0 ? a.w : a.u;
+            const uint32_t col0 = grp == 0 ? 64 : 192;
             for (int cc = 0; cc < 4; ++cc) {
-                float w[32], u[32];
-                tmem_ld32(t_row + 64 + cc * 32, w);
-                tmem_ld32(t_row + 192 + cc * 32, u);
+                float w[32];
+                tmem_ld32(t_row + col0 + cc * 32, w);
                 tmem_ld_wait();
                 if (live) {
-                    uint4 *wp = reinterpret_cast<uint4 *>(a.w + o + cc * 32);
-                    uint4 *up = reinterpret_cast<uint4 *>(a.u + o + cc * 32);
+                    uint4 *wp = reinterpret_cast<uint4 *>(dst + o + cc * 32);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 4; ++q)
                         wp[q] = make_uint4(pack_bf2(w[q * 8], w[q * 8 + 1]), pack_bf2(w[q * 8 + 2], w[q * 8 + 3]),
                                            pack_bf2(w[q * 8 + 4], w[q * 8 + 5]), pack_bf2(w[q * 8 + 6], w[q * 8 + 7]));
-                        up[q] = make_uint4(pack_bf2(u[q * 8], u[q * 8 + 1]), pack_bf2(u[q * 8 + 2], u[q * 8 + 3]),
-                                           pack_bf2(u[q * 8 + 4], u[q * 8 + 5]), pack_bf2(u[q * 8 + 6], u[q * 8 + 7]));
-                    }
                 }
             }
         }

@@ -1,9 +1,13 @@
-"""Summarise an ncu launch list (--metrics gpu__time_duration.sum --csv) per kernel.
+"""Summaries of ncu output.
 
     python -m chunked_gated_delta_06_gb300.ncu_summary launches.csv [--skip-first N]
-
-Prints, per kernel name, the number of launches, the total and mean device time
-and the share of the total, largest first.
+        per kernel of a launch list (--metrics gpu__time_duration.sum --csv):
+        launches, total and mean device time, share of the total;
+    python -m chunked_gated_delta_06_gb300.ncu_summary --report prof.ncu-rep
+        per captured launch of a --set full report: duration, DRAM bytes read and
+        written, DRAM throughput, tensor-pipe activity, achieved occupancy,
+        registers, and the largest warp-stall reasons (cycles per issued
+        instruction).
 """
 import csv
 import re
@@ -36,7 +40,42 @@ def summarise(path, skip_first=0):
     return "\n".join(out)
 
 
+def report(path):
+    import subprocess
+    out = subprocess.run(["ncu", "-i", path, "--page", "raw", "--csv"], capture_output=True,
+                         text=True, check=True).stdout
+    rows = list(csv.reader(out.splitlines()))
+    hdr, units, data = rows[0], rows[1], rows[2:]
+
+    def get(r, m):
+        return r[hdr.index(m)] if m in hdr else ""
+
+    stall = [c for c in hdr if c.startswith("smsp__average_warps_issue_stalled_")
+             and c.endswith("_per_issue_active.ratio")]
+    lines = []
+    for r in data:
+        name = re.sub(r"\(.*", "", r[hdr.index("Kernel Name")].replace("(anonymous namespace)", "anon"))
+        name = name.split("::")[-1].strip()
+        tops = sorted(((float(get(r, c) or 0), c[len("smsp__average_warps_issue_stalled_"):-len(
+            "_per_issue_active.ratio")]) for c in stall), reverse=True)[:4]
+        lines.append(
+            "%s: %s ms; DRAM read %s MB, write %s MB (%s %% of peak); tensor pipe %s %% of active; "
+            "warps active %s %%; %s regs/thread; grid %s block %s; stalls (cycles/issue): %s" % (
+                name, get(r, "gpu__time_duration.sum"), get(r, "dram__bytes_read.sum"),
+                get(r, "dram__bytes_write.sum"),
+                get(r, "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed"),
+                get(r, "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"),
+                get(r, "sm__warps_active.avg.pct_of_peak_sustained_active"),
+                get(r, "launch__registers_per_thread"), get(r, "launch__grid_size"),
+                get(r, "launch__block_size"),
+                ", ".join("%s %.2f" % (n, v) for v, n in tops)))
+    return "\n".join(lines)
+
+
 if __name__ == "__main__":
+    if "--report" in sys.argv:
+        print(report(sys.argv[sys.argv.index("--report") + 1]))
+        sys.exit(0)
     skip = 0
     if "--skip-first" in sys.argv:
         skip = int(sys.argv[sys.argv.index("--skip-first") + 1])

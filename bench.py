@@ -44,10 +44,6 @@ def _peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-# fp32 CUDA-core peak: 152 SMs x 128 FP32 lanes x 2 flop x 2.070 GHz (max SM clock)
-FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
-
-
 # ---------------------------------------------------------------------------- algorithmic work
 def kernel_work(name, T, H, HV, N, C_total):
     """Algorithmic (flops, bytes) of one launch of a kernel on a problem.
@@ -80,6 +76,57 @@ def kernel_work(name, T, H, HV, N, C_total):
         bnorm=TV * D * 4 * 2 + T * H * D * bf * 4,
     ).get(name, 0.0)
     return f, b
+
+
+# kernel name -> source file (the DRAM-traffic record is valid only for the source it was taken on)
+KERNEL_SOURCE = {
+    "intra": "gdn_intra_tc.cu", "state": "gdn_state_tc.cu", "out": "gdn_out_tc.cu",
+    "dvloc": "gdn_out_tc.cu", "bstate": "gdn_bstate_tc.cu", "bintra_a": "gdn_bintra_tc.cu",
+    "bintra_b": "gdn_bintra_b_tc.cu", "decode": "gdn_decode.cu", "prep": "gdn_chunk.cu",
+    "bnorm": "gdn_chunk.cu", "plan": "gdn_chunk.cu",
+}
+
+
+def _source_hash(kernel):
+    import hashlib
+    f = KERNEL_SOURCE.get(kernel)
+    if not f:
+        return None
+    path = os.path.join(ROOT, "chunked_gated_delta_06_gb300", "csrc", f)
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel, units):
+    """DRAM bytes per launch from the committed ncu record (profiles/kernel_traffic.json),
+    scaled by the work units of this launch; None when the kernel source changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "kernel_traffic.json")) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_sha256_16") != _source_hash(kernel):
+        return None
+    return rec["bytes_per_unit"] * units
+
+
+def roofline(kernel, flops, nbytes, seconds, peaks, units):
+    """Roofline of one kernel: bound = the resource its algorithmic work needs the
+    longest on (tensor at the sustained bf16 peak, HBM at the copy peak)."""
+    t_tc = flops / (peaks["bf16_sustained"] * 1e12) if flops else 0.0
+    t_hbm = nbytes / (peaks["hbm"] * 1e9) if nbytes else 0.0
+    if t_tc >= t_hbm and flops:
+        r = {"kernel": kernel, "bound": "tensor", "achieved": flops / seconds / 1e12,
+             "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+             "peak_source": "bf16_tflops_sustained (%s)" % peaks["source"],
+             "algorithmic_flops": flops}
+    else:
+        r = {"kernel": kernel, "bound": "hbm", "achieved": nbytes / seconds / 1e9,
+             "peak": peaks["hbm"], "unit": "GB/s", "peak_source": "hbm_gbs (%s)" % peaks["source"]}
+    r["algorithmic_bytes"] = nbytes
+    r["frac"] = r["achieved"] / r["peak"]
+    r["traffic"] = measured_traffic(kernel, units)
+    return r
 
 
 def decode_bytes(n_active, B, H, HV):
@@ -250,6 +297,23 @@ def run_oracle_sample(wl, target_tokens, threads=None):
     return int(cu[-1]), dt, threads, min(threads, n * wl.HV)
 
 
+def aggregate_over_ranks(ms_per_step, tokens_per_rank):
+    """Whole-job timing of replicas: the step time is the max over ranks (the job
+    finishes with its slowest rank) and the token count is the sum over ranks.
+    Uses the default torch.distributed group when one is initialised (NCCL on
+    GPUs, gloo on CPU); a single process returns its own numbers."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms_per_step, tokens_per_rank
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
+    n = torch.tensor([tokens_per_rank], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -319,11 +383,8 @@ def bench_ours(args):
     ms = _time_loop(torch, run.step, args.steps)
     clk = clocks.stop()
     barrier()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = T * world / (ms / 1e3)
+    ms, total_tokens = aggregate_over_ranks(ms, T)
+    value = total_tokens / (ms / 1e3)
 
     # per-kernel durations (same steps with the kernel timer), launches per step
     per = _kernel_table(torch, run.step, max(3, min(args.steps, 10)), 64)
@@ -332,25 +393,13 @@ def bench_ours(args):
             for k, v in per.items()}
     dom = max(ktab, key=lambda k: ktab[k]["ms"] * ktab[k]["launches_per_step"])
     fl, by = kernel_work(dom, T, H, HV, N, C_total)
-    dur = ktab[dom]["ms"] / 1e3
-    simt = True  # the chunk kernels of this build run on CUDA cores (fp32 FMA)
-    if fl > 0:
-        roof = {"kernel": dom, "bound": "alu" if simt else "tensor",
-                "achieved": fl / dur / 1e12,
-                "peak": FP32_SIMT_TFLOPS if simt else peaks["bf16_sustained"],
-                "unit": "TFLOP/s", "traffic": None,
-                "peak_source": ("fp32 CUDA-core peak from unit counts and the max SM clock"
-                                if simt else "bf16_tflops_sustained of %s" % peaks["source"]),
-                "algorithmic_flops": fl}
-    else:
-        roof = {"kernel": dom, "bound": "hbm", "achieved": by / dur / 1e9, "peak": peaks["hbm"],
-                "unit": "GB/s", "traffic": None,
-                "peak_source": "hbm_gbs of %s" % peaks["source"], "algorithmic_bytes": by}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = roofline(dom, fl, by, ktab[dom]["ms"] / 1e3, peaks, C_total * HV)
     for k in ktab:
         f_, b_ = kernel_work(k, T, H, HV, N, C_total)
         ktab[k]["tflops"] = f_ / (ktab[k]["ms"] / 1e3) / 1e12 if f_ else None
         ktab[k]["gbs"] = b_ / (ktab[k]["ms"] / 1e3) / 1e9 if b_ else None
+        ktab[k]["tensor_frac"] = (ktab[k]["tflops"] / peaks["bf16_sustained"]) if f_ else None
+        ktab[k]["hbm_frac"] = (ktab[k]["gbs"] / peaks["hbm"]) if b_ else None
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -399,7 +448,8 @@ def bench_ours(args):
                        "l2": "state pool (1.07 GB) larger than L2"},
             "roofline": {"kernel": "decode", "bound": "hbm", "achieved": nb / (kms / 1e3) / 1e9,
                          "peak": peaks["hbm"], "unit": "GB/s", "frac": nb / (kms / 1e3) / 1e9 / peaks["hbm"],
-                         "traffic": None, "peak_source": "hbm_gbs of %s" % peaks["source"]}}
+                         "traffic": measured_traffic("decode", n_active * dw.HV),
+                         "peak_source": "hbm_gbs (%s)" % peaks["source"]}}
         del pool
 
     # end to end through host buffers

@@ -54,6 +54,7 @@ struct BbSmem {
     unsigned char op_x[kHalf];      // X_rj rows r: MN-major B of T^T X
     float C[64 * kF];               // P1_ij + beta_i P2_ij (column sums give dG)
     float G[64], beta[64], rq[64], rk[64], dG[64], dbeta[64];
+    float rki[64], eg[64], qsc[64];  // 1 / r_k, e^{G}, scale / r_q (0 / 1 past L)
     float rs[2][64];                // per-warpgroup partial row sums of P2
     float cs[4][64];                // partial column sums of C
     float sk[2][64], su[2][64];     // per-warpgroup partial row dots
@@ -130,6 +131,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
         sm.rk[tid] = in ? a.rk[r] : 1.f;
         sm.dG[tid] = in ? a.dGp[gi] : 0.f;
         sm.dbeta[tid] = 0.f;
+        sm.rki[tid] = 1.f / sm.rk[tid];
+        sm.eg[tid] = in ? __expf(sm.G[tid]) : 0.f;
+        sm.qsc[tid] = in ? a.scale / sm.rq[tid] : 0.f;
     }
     {  // T (fp32, saved by the forward) -> bf16 rows
         const float *Tsrc = a.Tm + ((size_t)c * a.HV + hv) * 64 * 64;
@@ -172,7 +176,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
     const float Gi = active ? sm.G[i] : 0.f;
     if (ok) {
         if (grp == 0) {  // dM, QK -> M, dMG, P1 and the dMG operands
-            const float qsi = active ? a.scale / sm.rq[i] : 0.f;
+            const float qsi = active ? sm.qsc[i] : 0.f;
             float rsum = 0.f;
             for (int half = 0; half < 2; ++half) {
                 float dm[32], qk[32];
@@ -183,16 +187,16 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = half * 32 + jj;
-                    float dmg = 0.f, p1 = 0.f;
-                    if (live && j <= i) {
-                        const float gam = expf(Gi - sm.G[j]);
-                        const float m = qk[jj] * qsi / sm.rk[j] * gam;
-                        dmg = dm[jj] * gam;
-                        p1 = dm[jj] * m;
-                    }
+                    // branch-free mask; the exponent is clamped to <= 0 so masked
+                    // entries never form inf * 0
+                    const float msk = (live && j <= i) ? 1.f : 0.f;
+                    const float gam = msk * __expf(fminf(Gi - sm.G[j], 0.f));
+                    const float rkj = sm.rki[j];
+                    const float dmg = dm[jj] * gam;
+                    const float p1 = dmg * qk[jj] * qsi * rkj;
                     rsum += p1;
                     if (active) sm.C[i * kF + j] = p1;
-                    x1[jj] = dmg / sm.rk[j];
+                    x1[jj] = dmg * rkj;
                     x2[jj] = dmg * qsi;
                 }
                 if (active) {
@@ -211,7 +215,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = half * 32 + jj;
-                    dt[jj] = (live && j < i) ? sm.beta[j] * (expf(sm.G[j]) / sm.rk[j] * d1[jj] + d2[jj]) : 0.f;
+                    const float msk = (live && j < i) ? 1.f : 0.f;
+                    dt[jj] = msk * sm.beta[j] * (sm.eg[j] * sm.rki[j] * d1[jj] + d2[jj]);
                 }
                 if (active) put_row32(sm.op_dt, i, half * 32, dt);
             }
@@ -256,21 +261,19 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
         tmem_ld_wait();
         float b1[32], b2[32], rsp = 0.f;
         const float bi = active ? sm.beta[i] : 0.f;
-        const float rki = active ? sm.rk[i] : 1.f;
+        const float rkii = active ? sm.rki[i] : 1.f;
 #pragma unroll 8
         for (int jj = 0; jj < 32; ++jj) {
             const int j = grp * 32 + jj;
-            float b = 0.f, p2 = 0.f;
-            if (live && j < i) {
-                const float da = -ta[jj];
-                const float gam = expf(Gi - sm.G[j]);
-                b = da * bi * gam;
-                p2 = da * kk[jj] / (rki * sm.rk[j]) * gam;
-            }
+            const float msk = (live && j < i) ? 1.f : 0.f;
+            const float dag = -ta[jj] * msk * __expf(fminf(Gi - sm.G[j], 0.f));
+            const float rkj = sm.rki[j];
+            const float b = dag * bi;
+            const float p2 = dag * kk[jj] * rkii * rkj;
             rsp += p2;
             if (active) sm.C[i * kF + j] += bi * p2;
-            b1[jj] = b / sm.rk[j];
-            b2[jj] = b / rki;
+            b1[jj] = b * rkj;
+            b2[jj] = b * rkii;
         }
         if (active) {
             put_row32(sm.op_b, i, grp * 32, b1);
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
     if (ok) {
         const int m = row;
         const bool mlive = active && m < L;
-        const float em = mlive ? expf(sm.G[m]) : 0.f;
+        const float em = mlive ? sm.eg[m] : 0.f;
         const float bm = mlive ? sm.beta[m] : 0.f;
         float sk = 0.f, su = 0.f;
         const size_t o = ((size_t)(t0 + (mlive ? m : 0)) * a.HV + hv) * kDim;
@@ -378,8 +381,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
             const int m = 2 * lane + z;
             float dgm = 0.f, dbm = 0.f;
             if (m < L) {
-                const float em = expf(sm.G[m]), bm = sm.beta[m];
-                const float sk = (sm.sk[0][m] + sm.sk[1][m]) / sm.rk[m];
+                const float em = sm.eg[m], bm = sm.beta[m];
+                const float sk = (sm.sk[0][m] + sm.sk[1][m]) * sm.rki[m];
                 const float su = sm.su[0][m] + sm.su[1][m];
                 dbm = sm.dbeta[m] + em * sk + su;
                 dgm = sm.dG[m] + bm * em * sk;

@@ -7,8 +7,9 @@
 // reverse.  dS = dh^T (V x K) lives in TMEM as fp32 (lane v = row v), seeded
 // with d(final state)^T.  Per chunk, with dh' the gradient of the state after
 // the chunk (= the current dS^T):
-//   1. thread v writes row v of dS as bf16 to shared memory and to
-//      dh_c[chunk][hv][k][v] (HBM), then dS <- e^{G_L} dS;
+//   1. thread v writes row v of dS as bf16 to shared memory (copied to
+//      dh_c[chunk][hv], stored transposed [v][k], by one TMA store), then
+//      dS <- e^{G_L} dS;
 //   2. Pd = dS'_bf16 K^T                          (M=128 N=64 K=128)
 //   3. dv_new^T[v][t] = dv_loc[t][v] + e^{G_L-G_t}/r_k,t Pd[v][t]  -> HBM (fp32)
 //   4. dS += (c_t dO[t][v])^T Q - dv_new^T w,  c_t = e^{G_t} scale / r_q,t
@@ -46,7 +47,7 @@ struct BStateSmem {
 };
 
 struct BStateMaps {
-    CUtensorMap k, q, w, dO, dl;
+    CUtensorMap k, q, w, dO, dl, dhc;
 };
 
 __device__ __forceinline__ void issue_stage(const BStateMaps &m, BStateSmem &sm, int st, int t0,
@@ -153,8 +154,9 @@ __global__ void __launch_bounds__(kThr, 1)
             sm.qc[tid] = qq;
         }
         const float egl = expf(Gl);
-        // 1. dS' -> bf16 operand + dh_c, then dS <- e^{G_L} dS'
-        bf16 *ddst = a.dhc + ((size_t)c * a.HV + hv) * kDim * kDim;
+        // 1. dS' -> bf16 operand (copied to dh_c by TMA below), then dS <- e^{G_L} dS'
+        if (tid == 0) tma_store_wait_read();  // the previous chunk's dh_c store has read a_ds
+        __syncthreads();
         for (int kc = 0; kc < 4; ++kc) {
             float r[32];
             tmem_ld32(tS + kc * 32, r);
@@ -168,10 +170,7 @@ __global__ void __launch_bounds__(kThr, 1)
                     pack_bf2(r[q * 8 + 4], r[q * 8 + 5]), pack_bf2(r[q * 8 + 6], r[q * 8 + 7]));
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                ddst[(size_t)(kc * 32 + j) * kDim + v] = f2bf(r[j]);
-                r[j] *= egl;
-            }
+            for (int j = 0; j < 32; ++j) r[j] *= egl;
             tmem_st32(tS + kc * 32, r);
         }
         tmem_st_wait();
@@ -189,6 +188,10 @@ __global__ void __launch_bounds__(kThr, 1)
                 mma_bf16(tP, sdesc(as + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
                          sdesc(ks + (s >> 2) * kTileBytes + (s & 3) * 32, 16, 1024), idP, s > 0);
             mma_commit(&sm.mma_bar);
+            const int hrow = (c * a.HV + hv) * 128;  // dh_c^T rows of this chunk
+            tma_store_3d(&maps.dhc, 0, 0, hrow, sm.a_ds);
+            tma_store_3d(&maps.dhc, 64, 0, hrow, sm.a_ds + 128 * 128);
+            tma_store_commit();
         }
         // meanwhile: A_DO[v][t] = qc_t dO[t][v]
         {
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(kThr, 1)
             for (int j = 0; j < 32; ++j) a.dh0[sbase + (size_t)(kc * 32 + j) * kDim + v] = r[j];
         }
     }
+    if (tid == 0) tma_store_wait_all();
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         mbar_wait(&sm.tma_bar[0], 0, 1u << 20);
@@ -294,7 +298,9 @@ cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s) {
                     !encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
                     !encode_rows_bf16(&m.w, a.w, a.HV, a.T, rowb, rowb * a.HV, 64) ||
                     !encode_rows_bf16(&m.dO, a.d_o, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-                    !encode_rows_bf16(&m.dl, a.dvloc, a.HV, a.T, rowb, rowb * a.HV, 64)))
+                    !encode_rows_bf16(&m.dl, a.dvloc, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+                    !encode_rows_bf16(&m.dhc, a.dhc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb,
+                                      rowb, 128)))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BStateSmem) + 1024;
     static_assert(sizeof(BStateSmem) + 1024 <= 232448, "shared memory budget");

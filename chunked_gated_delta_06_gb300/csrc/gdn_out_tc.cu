@@ -30,10 +30,11 @@ constexpr uint32_t kBig = 128 * 128;   // 128 rows x 128 B
 
 struct OutSmem {
     unsigned char kq[2 * kBig];   // [K; Q] per k-half: K rows 0..63, Q rows 64..127
-    unsigned char hc[2 * kBig];   // h_c [k][v] per v-half (forward)
+    unsigned char hc[2 * kBig];   // h_c^T [v][k] per k-half (forward)
     unsigned char tv[2 * kBox];   // v_new (forward) or dO (backward) [t][v] per v-half
     unsigned char mm[kBox];       // M, row i at row i (bf16)
     float G[64], rq[64], rk[64];
+    float qsc[64], rki[64], ct[64];  // scale / r_q, 1 / r_k, e^{G} scale / r_q
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
 };
@@ -92,6 +93,9 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
         sm.G[tid] = in ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
         sm.rq[tid] = in ? a.rq[r] : 1.f;
         sm.rk[tid] = in ? a.rk[r] : 1.f;
+        sm.qsc[tid] = a.scale / sm.rq[tid];
+        sm.rki[tid] = 1.f / sm.rk[tid];
+        sm.ct[tid] = in ? __expf(sm.G[tid]) * sm.qsc[tid] : 0.f;
     }
     bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t tb = sm.tmem_base;
@@ -120,9 +124,8 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
                 const int j = half * 32 + jj;
-                m[jj] = (j <= t && t < L)
-                            ? r[jj] * a.scale / (sm.rq[t] * sm.rk[j]) * expf(sm.G[t] - sm.G[j])
-                            : 0.f;
+                const float msk = (j <= t && t < L) ? 1.f : 0.f;
+                m[jj] = msk * r[jj] * sm.qsc[t] * sm.rki[j] * __expf(fminf(sm.G[t] - sm.G[j], 0.f));
             }
             // row t of M at row t: the forward reads it as K-major [t][j] (B = M^T
             // operand of v_new^T M^T), the backward as MN-major [j][t] (B = M of dO^T M)
@@ -141,11 +144,12 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
         const uint32_t id = idesc_bf16(128, 64, 1, 0);    // A MN-major, B K-major
         const uint32_t tvs = smem_u32(sm.tv), mms = smem_u32(sm.mm);
         if (kForward) {
-            // O1 = h^T Q^T : A = h_c [k][v] (MN-major, v atoms 16 KB apart), B = Q [t][k]
+            // O1 = h^T Q^T : A = h_c^T [v][k] (K-major), B = Q [t][k] (K-major)
+            const uint32_t id1 = idesc_bf16(128, 64, 0, 0);
             const uint32_t hs = smem_u32(sm.hc), qs = smem_u32(sm.kq + kBox);
             for (int s = 0; s < 8; ++s)
-                mma_bf16(tb + 64, sdesc(hs + s * 2048, kBig, 1024),
-                         sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id, s > 0);
+                mma_bf16(tb + 64, sdesc(hs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024),
+                         sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id1, s > 0);
             // O2 = v_new^T M^T : A = v_new [j][v] (MN-major, v atoms 8 KB apart), B = M [t][j]
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tb + 128, sdesc(tvs + s * 2048, kBox, 1024), sdesc(mms + s * 32, 16, 1024), id,
@@ -174,8 +178,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
                 if (t < L) {
                     const size_t o = ((size_t)(t0 + t) * a.HV + hv) * kDim + v;
                     if (kForward) {
-                        const float ct = expf(sm.G[t]) * a.scale / sm.rq[t];
-                        a.o[o] = f2bf(ct * r1[j] + r2[j]);
+                        a.o[o] = f2bf(sm.ct[t] * r1[j] + r2[j]);
                     } else {
                         a.dvloc[o] = f2bf(r1[j]);
                     }

@@ -8,7 +8,8 @@
 // (L <= 64 tokens starting at t0, G the chunk-local cumsum of g, G_L its last
 // value):
 //   1. thread v reads row v of S, writes it as bf16 to shared memory (MMA
-//      operand) and to h_c[chunk][hv][k][v] in HBM, and writes e^{G_L} S back;
+//      operand) and e^{G_L} S back to TMEM; one TMA store copies the bf16 tile
+//      to h_c[chunk][hv] (stored transposed, [v][k]);
 //   2. P = S_bf16 w^T                      (tcgen05, M=128 N=64 K=128)
 //   3. v_new^T[v][t] = u[t][v] - P[v][t]  -> v_new in HBM (bf16), and the
 //      operand A_V[v][t] = v_new^T[v][t] e^{G_L - G_t} / r_k,t (bf16, smem)
@@ -46,7 +47,7 @@ struct StateSmem {
 };
 
 struct StateMaps {
-    CUtensorMap w, k, u;
+    CUtensorMap w, k, u, hc;
 };
 
 __device__ __forceinline__ void issue_stage(const StateMaps &m, StateSmem &sm, int st, int t0, int h,
@@ -135,8 +136,9 @@ __global__ void __launch_bounds__(kThr, 1)
         const float Gl = L > 0 ? sm.gt[L - 1] : 0.f;
         if (tid < 64) sm.coef[st][tid] = tid < L ? expf(Gl - sm.gt[tid]) / sm.rkt[tid] : 0.f;
         const float egl = expf(Gl);
-        // 1. S -> bf16 operand + h_c, then S <- e^{G_L} S
-        bf16 *hdst = a.hc + ((size_t)c * a.HV + hv) * kDim * kDim;
+        // 1. S -> bf16 operand (copied to h_c by TMA below), then S <- e^{G_L} S
+        if (tid == 0) tma_store_wait_read();  // the previous chunk's h_c store has read a_s
+        __syncthreads();
         for (int kc = 0; kc < 4; ++kc) {
             float r[32];
             tmem_ld32(tS + kc * 32, r);
@@ -154,10 +156,7 @@ __global__ void __launch_bounds__(kThr, 1)
                 *reinterpret_cast<uint4 *>(sub + sw128_off(v, col)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                hdst[(size_t)(kc * 32 + j) * kDim + v] = f2bf(r[j]);
-                r[j] *= egl;
-            }
+            for (int j = 0; j < 32; ++j) r[j] *= egl;
             tmem_st32(tS + kc * 32, r);
         }
         tmem_st_wait();
@@ -176,6 +175,10 @@ __global__ void __launch_bounds__(kThr, 1)
                     mma_bf16(tP, sdesc(as + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
                              sdesc(ws + (s >> 2) * kTileBytes + (s & 3) * 32, 16, 1024), idP, s > 0);
                 mma_commit(&sm.mma_bar);
+                const int hrow = (c * a.HV + hv) * 128;  // h_c^T rows of this chunk
+                tma_store_3d(&maps.hc, 0, 0, hrow, sm.a_s);
+                tma_store_3d(&maps.hc, 64, 0, hrow, sm.a_s + 128 * 128);
+                tma_store_commit();
             }
         }
         __syncthreads();
@@ -243,6 +246,7 @@ __global__ void __launch_bounds__(kThr, 1)
             for (int j = 0; j < 32; ++j) a.ht[sbase + (size_t)(kc * 32 + j) * kDim + v] = r[j];
         }
     }
+    if (tid == 0) tma_store_wait_all();
     if (!ok) {
         // drain outstanding TMA copies (bounded) before leaving
         if (tid == 0) {
@@ -264,7 +268,8 @@ cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
     const uint64_t rowb = 128 * 2;
     if (a.T > 0 && (!encode_rows_bf16(&m.w, a.w, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
-        !encode_rows_bf16(&m.u, a.u, a.HV, a.T, rowb, rowb * a.HV, 64)))
+        !encode_rows_bf16(&m.u, a.u, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.hc, a.hc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb, rowb, 128)))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(StateSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(k_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,

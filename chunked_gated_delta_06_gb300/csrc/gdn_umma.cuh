@@ -183,5 +183,28 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
         : "memory");
 }
 
+// Tile store shared -> global (bulk async group of the issuing thread).  The
+// writing threads must have made the tile visible to the async proxy
+// (fence_proxy_async_smem + barrier) before one thread issues the store.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2,
+                                             const void *src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            tmap),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the committed stores of this thread have read their shared source.
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until the committed stores of this thread are complete.
+__device__ __forceinline__ void tma_store_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 }  // namespace umma
 }  // namespace gdn

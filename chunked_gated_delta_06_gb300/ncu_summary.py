@@ -3,6 +3,11 @@
     python -m chunked_gated_delta_06_gb300.ncu_summary launches.csv [--skip-first N]
         per kernel of a launch list (--metrics gpu__time_duration.sum --csv):
         launches, total and mean device time, share of the total;
+    python -m chunked_gated_delta_06_gb300.ncu_summary --traffic prof.ncu-rep UNITS
+        JSON record of DRAM bytes per work unit (UNITS = chunk x value-head units,
+        or active decode rows x value heads, of the captured launches) with the
+        hash of each kernel's source file at capture time (bench.py reports the
+        traffic only while the source is unchanged);
     python -m chunked_gated_delta_06_gb300.ncu_summary --report prof.ncu-rep
         per captured launch of a --set full report: duration, DRAM bytes read and
         written, DRAM throughput, tensor-pipe activity, achieved occupancy,
@@ -72,7 +77,48 @@ def report(path):
     return "\n".join(lines)
 
 
+KERNELS = {  # ncu kernel name -> (bench kernel name, source file)
+    "k_intra_tc": ("intra", "gdn_intra_tc.cu"), "k_state_tc": ("state", "gdn_state_tc.cu"),
+    "k_out_tc<1>": ("out", "gdn_out_tc.cu"), "k_out_tc<0>": ("dvloc", "gdn_out_tc.cu"),
+    "k_out_tc<true>": ("out", "gdn_out_tc.cu"), "k_out_tc<false>": ("dvloc", "gdn_out_tc.cu"),
+    "k_bstate_tc": ("bstate", "gdn_bstate_tc.cu"), "k_bintra_a_tc": ("bintra_a", "gdn_bintra_tc.cu"),
+    "k_bintra_b_tc": ("bintra_b", "gdn_bintra_b_tc.cu"), "k_decode": ("decode", "gdn_decode.cu"),
+}
+
+
+def traffic(path, units):
+    import hashlib
+    import json
+    import os
+    import subprocess
+    out = subprocess.run(["ncu", "-i", path, "--page", "raw", "--csv"], capture_output=True,
+                         text=True, check=True).stdout
+    rows = list(csv.reader(out.splitlines()))
+    hdr, data = rows[0], rows[2:]
+    units_row = rows[1]
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc")
+    rec = {}
+    for r in data:
+        name = re.sub(r"\(.*", "", r[hdr.index("Kernel Name")].replace("(anonymous namespace)", "anon"))
+        name = name.split("::")[-1].strip()
+        if name not in KERNELS:
+            continue
+        kname, src = KERNELS[name]
+        rd = float(r[hdr.index("dram__bytes_read.sum")]) * scale[units_row[hdr.index("dram__bytes_read.sum")]]
+        wr = float(r[hdr.index("dram__bytes_write.sum")]) * scale[units_row[hdr.index("dram__bytes_write.sum")]]
+        with open(os.path.join(csrc, src), "rb") as fh:
+            sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+        rec[kname] = {"bytes_per_unit": (rd + wr) / units, "captured_units": units,
+                      "capture": os.path.basename(path), "source_sha256_16": sha}
+    return json.dumps(rec, indent=1, sort_keys=True)
+
+
 if __name__ == "__main__":
+    if "--traffic" in sys.argv:
+        i = sys.argv.index("--traffic")
+        print(traffic(sys.argv[i + 1], float(sys.argv[i + 2])))
+        sys.exit(0)
     if "--report" in sys.argv:
         print(report(sys.argv[sys.argv.index("--report") + 1]))
         sys.exit(0)

@@ -77,6 +77,7 @@ void carve_table(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.chunk_seq = cv.take<int>((size_t)d.C);
     a.chunk_start = cv.take<int>((size_t)d.C);
     a.chunk_len = cv.take<int>((size_t)d.C);
+    a.seq_order = cv.take<int>((size_t)d.N);
     a.status = cv.take<int>(1);
 }
 
@@ -95,6 +96,8 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.dW = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dqp = cv.take<float>((size_t)d.T * d.HV * D);
     a.dkp = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dqp2 = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dkp2 = cv.take<float>((size_t)d.T * d.HV * D);
     a.dGp = cv.take<float>((size_t)d.T * d.HV);
 }
 

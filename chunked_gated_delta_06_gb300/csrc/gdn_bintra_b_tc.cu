@@ -21,8 +21,9 @@
 //     dkhat_m += beta_m e^{G_m} dWt_m,  dv_m = beta_m dUt_m,
 //     dbeta_m += e^{G_m} khat_m . dWt_m + v_m . dUt_m,
 //     dG_m    += beta_m e^{G_m} khat_m . dWt_m,   dg = reverse cumsum of dG.
-// dq / dk are added to the per-value-head gradients of qhat / khat that the
-// h / dh' kernel wrote; the L2-norm backward and the head sum follow.
+// dq / dk go to their own buffers; the head-sum kernel adds them to the
+// per-value-head gradients of qhat / khat that the h / dh' kernel wrote, then
+// applies the L2-norm backward.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
         float b1[32], b2[32], rsp = 0.f;
         const float bi = active ? sm.beta[i] : 0.f;
         const float rkii = active ? sm.rki[i] : 1.f;
-#pragma unroll 8
+#pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
             const int j = grp * 32 + jj;
             const float msk = (live && j < i) ? 1.f : 0.f;
@@ -333,25 +334,16 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
             tmem_ld32(t_row + cWT + cc * 32, wt);
             tmem_ld32(t_row + cUT + cc * 32, ut);
             tmem_ld_wait();
-            if (mlive) {
-                float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
-                float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
-                float4 xs[8], ys[8];  // all loads before any store
+            if (mlive) {  // plain stores: the head-sum kernel adds them to the h / dh' terms
+                float4 *qp = reinterpret_cast<float4 *>(a.dqp2 + o + cc * 32);
+                float4 *kp = reinterpret_cast<float4 *>(a.dkp2 + o + cc * 32);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    xs[u] = __ldg(qp + u);
-                    ys[u] = __ldg(kp + u);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float4 x = xs[u], y = ys[u];
-                    x.x += dq[4 * u + 0]; x.y += dq[4 * u + 1]; x.z += dq[4 * u + 2]; x.w += dq[4 * u + 3];
-                    y.x += dk[4 * u + 0] + bm * em * wt[4 * u + 0];
-                    y.y += dk[4 * u + 1] + bm * em * wt[4 * u + 1];
-                    y.z += dk[4 * u + 2] + bm * em * wt[4 * u + 2];
-                    y.w += dk[4 * u + 3] + bm * em * wt[4 * u + 3];
-                    qp[u] = x;
-                    kp[u] = y;
+                    qp[u] = make_float4(dq[4 * u + 0], dq[4 * u + 1], dq[4 * u + 2], dq[4 * u + 3]);
+                    kp[u] = make_float4(dk[4 * u + 0] + bm * em * wt[4 * u + 0],
+                                        dk[4 * u + 1] + bm * em * wt[4 * u + 1],
+                                        dk[4 * u + 2] + bm * em * wt[4 * u + 2],
+                                        dk[4 * u + 3] + bm * em * wt[4 * u + 3]);
                 }
                 uint32_t pk[16];
 #pragma unroll
@@ -359,7 +351,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_b_tc(const ChunkArgs a,
                 uint4 *dvp = reinterpret_cast<uint4 *>(a.dv + o + cc * 32);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) dvp[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-#pragma unroll 8
+#pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     sk += tile_at(sm.k, m, cc * 32 + j) * wt[j];
                     su += tile_at(sm.v, m, cc * 32 + j) * ut[j];

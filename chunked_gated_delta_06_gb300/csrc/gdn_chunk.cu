@@ -24,7 +24,8 @@ constexpr int kThreads = 256;
 // Chunk table from the device cu_seqlens (one block).  Host code computed the
 // chunk count from the host copy; a mismatch sets *status.
 __global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunks, int *seq_off,
-                       int *chunk_seq, int *chunk_start, int *chunk_len, int *status) {
+                       int *chunk_seq, int *chunk_start, int *chunk_len, int *seq_order,
+                       int *status) {
     __shared__ int sums[1024];
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (N + nt - 1) / nt;
@@ -64,6 +65,20 @@ __global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunk
     }
     // keep every sequence's chunk range inside [0, total_chunks]
     for (int n = b; n < e; ++n) seq_off[n] = min(seq_off[n], total_chunks);
+    // longest sequences first (ties by index), so the scans start the longest
+    // chunk chains first; identity order beyond 4096 sequences
+    for (int n = b; n < e; ++n) {
+        int rank = n;
+        if (N <= 4096) {
+            const int Ln = max(cu[n + 1] - cu[n], 0);
+            rank = 0;
+            for (int m = 0; m < N; ++m) {
+                const int Lm = max(cu[m + 1] - cu[m], 0);
+                rank += (Lm > Ln || (Lm == Ln && m < n)) ? 1 : 0;
+            }
+        }
+        seq_order[rank] = n;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -121,11 +136,12 @@ __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
     float dq[4] = {0, 0, 0, 0}, dk[4] = {0, 0, 0, 0}, xq[4], xk[4];
     for (int j = 0; j < r; ++j) {
         const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + lane * 4;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            dq[u] += a.dqp[o + u];
-            dk[u] += a.dkp[o + u];
-        }
+        const float4 q1 = *reinterpret_cast<const float4 *>(a.dqp + o);
+        const float4 q2 = *reinterpret_cast<const float4 *>(a.dqp2 + o);
+        const float4 k1 = *reinterpret_cast<const float4 *>(a.dkp + o);
+        const float4 k2 = *reinterpret_cast<const float4 *>(a.dkp2 + o);
+        dq[0] += q1.x + q2.x; dq[1] += q1.y + q2.y; dq[2] += q1.z + q2.z; dq[3] += q1.w + q2.w;
+        dk[0] += k1.x + k2.x; dk[1] += k1.y + k2.y; dk[2] += k1.z + k2.z; dk[3] += k1.w + k2.w;
     }
     const size_t row = ((size_t)t * a.H + h) * kDim + lane * 4;
     const float rq = a.rq[(size_t)t * a.H + h], rk = a.rk[(size_t)t * a.H + h];
@@ -153,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
 cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s) {
     TimerScope ts(a.timer, GDN_KERNEL_PLAN, s);
     k_plan<<<1, 1024, 0, s>>>(a.cu_dev, a.N, a.T, a.num_chunks, a.seq_chunk_off, a.chunk_seq,
-                              a.chunk_start, a.chunk_len, a.status);
+                              a.chunk_start, a.chunk_len, a.seq_order, a.status);
     return cudaGetLastError();
 }
 

@@ -3,9 +3,8 @@
 // chunk form of the GDN context-parallel scans in "Qwen3.5-397B RL trainer on
 // 128 v7x", maxtext #5799).
 //
-// One CTA of 256 threads per (chunk, key head).  Its two warpgroups work on
-// two value heads of the key head at once (value heads 2p and 2p + 1), each
-// with its own tiles, TMEM columns and named barrier.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
+// One CTA of 128 threads per (chunk, key head); it walks the HV/H value heads
+// of the key head.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
 //   KK = K K^T                                   (tcgen05, M=64 N=64 K=128, once)
 //   A  = strict_tril(diag(beta) KKhat (.) Gamma) (CUDA cores, fp32)
 //   T  = (I + A)^-1                              (fp32, recursive 2x2 blocking:
@@ -28,23 +27,22 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThr = 256;   // two warpgroups, each working on its own value head
+constexpr int kThr = 256;   // two warpgroups share the 128 TMEM lanes
 constexpr uint32_t kHalf = 64 * 128;
 constexpr uint32_t kTile = 2 * kHalf;
 constexpr int kF = 65;
 
 struct IntraSmem {
     unsigned char k[kTile];
-    unsigned char v[2][2][kTile];     // [warpgroup][buffer] value tiles
-    unsigned char op_w[2][kHalf];     // T_ij beta_j e^{G_j} / r_k,j  [i][j] K-major
-    unsigned char op_u[2][kHalf];     // T_ij beta_j                  [i][j] K-major
-    float A[2][64 * kF];
-    float T[2][64 * kF];
-    float X[2][64 * kF];
-    float G[2][64], beta[2][64], wc[2][64], rk[64];
-    uint64_t k_bar, v_bar[2][2], mma_bar[3];
+    unsigned char v[2][kTile];     // double-buffered value tiles
+    unsigned char op_w[kHalf];     // T_ij beta_j e^{G_j} / r_k,j  [i][j] K-major
+    unsigned char op_u[kHalf];     // T_ij beta_j                  [i][j] K-major
+    float A[64 * kF];
+    float T[64 * kF];
+    float X[64 * kF];
+    float G[64], beta[64], wc[64], rk[64];
+    uint64_t k_bar, v_bar[2], mma_bar;
     uint32_t tmem_base;
-    int err[2];
 };
 
 struct IntraMaps {
@@ -56,20 +54,14 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&t);
 }
 
-// Barrier over the 128 threads of warpgroup g (named barrier 1 + g).
-__device__ __forceinline__ void group_sync(int g) {
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
-}
-
-// T = (I + A)^-1 for a strictly lower A (64 x 64, rows/cols >= L are zero),
-// by the 128 threads of warpgroup g (gt = thread index within the group):
-// 8x8 diagonal blocks by substitution, then T21 = -T22 (A21 T11) at block
-// sizes 8, 16 and 32.
-__device__ void tri_inverse(const float *A, float *T, float *X, int gt, int g) {
-    for (int idx = gt; idx < 64 * 64; idx += 128) T[(idx >> 6) * kF + (idx & 63)] = 0.f;
-    group_sync(g);
-    if (gt < 64) {
-        const int b = gt >> 3, cc = gt & 7, base = b * 8;
+// T = (I + A)^-1 for a strictly lower A (64 x 64, rows/cols >= L are zero).
+// All 128 threads take part.
+__device__ void tri_inverse(const float *A, float *T, float *X) {
+    const int tid = threadIdx.x;
+    for (int idx = tid; idx < 64 * 64; idx += kThr) T[(idx >> 6) * kF + (idx & 63)] = 0.f;
+    __syncthreads();
+    if (tid < 64) {  // 8 diagonal 8x8 blocks, one column per thread
+        const int b = tid >> 3, cc = tid & 7, base = b * 8;
         float col[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
@@ -84,25 +76,26 @@ __device__ void tri_inverse(const float *A, float *T, float *X, int gt, int g) {
 #pragma unroll
         for (int r = 0; r < 8; ++r) T[(base + r) * kF + base + cc] = col[r];
     }
-    group_sync(g);
+    __syncthreads();
     for (int s = 8; s < 64; s *= 2) {
+        // for every merged block p of size 2s: X = A21 T11, then T21 = -T22 X
         const int nb = 64 / (2 * s), ent = nb * s * s;
-        for (int e = gt; e < ent; e += 128) {
+        for (int e = tid; e < ent; e += kThr) {
             const int p = e / (s * s), rr = (e / s) % s, cc = e % s;
             const int r0 = p * 2 * s + s, c0 = p * 2 * s;
             float acc = 0.f;
             for (int m = cc; m < s; ++m) acc += A[(r0 + rr) * kF + c0 + m] * T[(c0 + m) * kF + c0 + cc];
             X[(r0 + rr) * kF + c0 + cc] = acc;
         }
-        group_sync(g);
-        for (int e = gt; e < ent; e += 128) {
+        __syncthreads();
+        for (int e = tid; e < ent; e += kThr) {
             const int p = e / (s * s), rr = (e / s) % s, cc = e % s;
             const int r0 = p * 2 * s + s, c0 = p * 2 * s;
             float acc = 0.f;
             for (int m = 0; m <= rr; ++m) acc += T[(r0 + rr) * kF + r0 + m] * X[(r0 + m) * kF + c0 + cc];
             T[(r0 + rr) * kF + c0 + cc] = -acc;
         }
-        group_sync(g);
+        __syncthreads();
     }
 }
 
@@ -116,10 +109,9 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
     const int r = a.HV / a.H;
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
     if (L <= 0) return;
-    const int g = warp >> 2, gt = tid & 127;  // warpgroup, thread within it
     const bool active = lane < 16;
+    const int grp = warp >> 2;              // warpgroup: which half of the columns
     const int row = (warp & 3) * 16 + lane;
-    const int npairs = (r + 1) / 2;
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -127,13 +119,10 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
     }
     if (tid == 0) {
         mbar_init(&sm.k_bar, 1);
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(&sm.v_bar[x][0], 1);
-            mbar_init(&sm.v_bar[x][1], 1);
-        }
-        for (int x = 0; x < 3; ++x) mbar_init(&sm.mma_bar[x], 1);
+        mbar_init(&sm.v_bar[0], 1);
+        mbar_init(&sm.v_bar[1], 1);
+        mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
-        sm.err[0] = sm.err[1] = 0;
     }
     tc_fence_before();
     __syncthreads();
@@ -142,17 +131,15 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
         mbar_arrive_expect_tx(&sm.k_bar, kTile);
         tma_load_3d(sm.k, &maps.k, 0, h, t0, &sm.k_bar);
         tma_load_3d(sm.k + kHalf, &maps.k, 64, h, t0, &sm.k_bar);
-    }
-    if (gt == 0 && g < r) {  // each warpgroup's first value-head tile
-        const int hv = h * r + g;
-        mbar_arrive_expect_tx(&sm.v_bar[g][0], kTile);
-        tma_load_3d(sm.v[g][0], &maps.v, 0, hv, t0, &sm.v_bar[g][0]);
-        tma_load_3d(sm.v[g][0] + kHalf, &maps.v, 64, hv, t0, &sm.v_bar[g][0]);
+        mbar_arrive_expect_tx(&sm.v_bar[0], kTile);
+        tma_load_3d(sm.v[0], &maps.v, 0, h * r, t0, &sm.v_bar[0]);
+        tma_load_3d(sm.v[0] + kHalf, &maps.v, 64, h * r, t0, &sm.v_bar[0]);
     }
     if (tid < 64) sm.rk[tid] = tid < L ? a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
     bool ok = __syncthreads_and(mbar_wait(&sm.k_bar, 0));
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t mphase = 0;
     if (tid == 0 && ok) {  // KK = K K^T into columns 0..63
         tc_fence_after();
         const uint32_t ks = smem_u32(sm.k);
@@ -161,133 +148,119 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
             const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
             mma_bf16(tb, sdesc(ks + off, 16, 1024), sdesc(ks + off, 16, 1024), id, s > 0);
         }
-        mma_commit(&sm.mma_bar[2]);
+        mma_commit(&sm.mma_bar);
     }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar[2], 0));
+    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
+    mphase ^= 1;
     tc_fence_after();
-    // KKhat row i stays in registers for all value heads of this warpgroup
-    float kk[64];
+    // KKhat row i, columns [32 grp, 32 grp + 32), stays in registers for all value heads
+    float kk[32];
     if (ok) {
-        float k0[32], k1[32];
-        tmem_ld32(t_row, k0);
-        tmem_ld32(t_row + 32, k1);
+        tmem_ld32(t_row + grp * 32, kk);
         tmem_ld_wait();
-        const float rki = active ? 1.f / sm.rk[row] : 0.f;
+        if (active) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            kk[j] = k0[j] * rki / sm.rk[j];
-            kk[32 + j] = k1[j] * rki / sm.rk[32 + j];
+            for (int j = 0; j < 32; ++j) kk[j] /= (sm.rk[row] * sm.rk[grp * 32 + j]);
         }
     }
-    tc_fence_before();
-    __syncthreads();  // KK columns are free from here on
-    tc_fence_after();
-    const uint32_t cw = tb + g * 256, cu = tb + g * 256 + 128;   // this group's w / u columns
-    uint32_t mphase = 0;
-    for (int p = 0; p < npairs && ok; ++p) {
-        const int jv = 2 * p + g;
-        if (jv >= r) break;  // odd r: the second warpgroup has no last value head
-        const int hv = h * r + jv, vb = p & 1;
-        if (gt == 0 && jv + 2 < r) {  // prefetch this group's next value head
-            mbar_arrive_expect_tx(&sm.v_bar[g][vb ^ 1], kTile);
-            tma_load_3d(sm.v[g][vb ^ 1], &maps.v, 0, hv + 2, t0, &sm.v_bar[g][vb ^ 1]);
-            tma_load_3d(sm.v[g][vb ^ 1] + kHalf, &maps.v, 64, hv + 2, t0, &sm.v_bar[g][vb ^ 1]);
+    for (int jv = 0; jv < r && ok; ++jv) {
+        const int hv = h * r + jv, vb = jv & 1;
+        if (tid == 0 && jv + 1 < r) {  // prefetch the next value head's tile
+            mbar_arrive_expect_tx(&sm.v_bar[vb ^ 1], kTile);
+            tma_load_3d(sm.v[vb ^ 1], &maps.v, 0, hv + 1, t0, &sm.v_bar[vb ^ 1]);
+            tma_load_3d(sm.v[vb ^ 1] + kHalf, &maps.v, 64, hv + 1, t0, &sm.v_bar[vb ^ 1]);
         }
-        if (gt < 64) {
-            const bool in = gt < L;
-            const size_t gi = (size_t)(t0 + gt) * a.HV + hv;
+        if (tid < 64) {
+            const bool in = tid < L;
+            const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
             const float gg = in ? a.G[gi] : 0.f, bb = in ? bf2f(a.beta[gi]) : 0.f;
-            sm.G[g][gt] = gg;
-            sm.beta[g][gt] = bb;
-            sm.wc[g][gt] = in ? bb * __expf(gg) / sm.rk[gt] : 0.f;
+            sm.G[tid] = gg;
+            sm.beta[tid] = bb;
+            sm.wc[tid] = in ? bb * __expf(gg) / sm.rk[tid] : 0.f;
         }
-        group_sync(g);
-        float *A = sm.A[g], *T = sm.T[g];
-        if (active) {  // A row i
+        __syncthreads();
+        if (active) {  // A row i, this warpgroup's 32 columns
             const int i = row;
-            const float Gi = sm.G[g][i], bi = sm.beta[g][i];
-#pragma unroll 8
-            for (int j = 0; j < 64; ++j) {
+            const float Gi = sm.G[i], bi = sm.beta[i];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = grp * 32 + jj;
                 const float msk = (j < i && i < L) ? 1.f : 0.f;
-                A[i * kF + j] = msk * bi * kk[j] * __expf(fminf(Gi - sm.G[g][j], 0.f));
+                sm.A[i * kF + j] = msk * bi * kk[jj] * __expf(fminf(Gi - sm.G[j], 0.f));
             }
         }
-        group_sync(g);
-        tri_inverse(A, T, sm.X[g], gt, g);
-        if (active) {  // operands, and T to HBM
+        __syncthreads();
+        tri_inverse(sm.A, sm.T, sm.X);
+        // operands T diag(beta e^G / r_k) (warpgroup 0, also T to HBM) and T diag(beta) (warpgroup 1)
+        if (active) {
             const int i = row;
             float4 *Tdst = reinterpret_cast<float4 *>(a.Tm + ((size_t)c * a.HV + hv) * 64 * 64 + (size_t)i * 64);
             for (int half = 0; half < 2; ++half) {
-                float xw[32], xu[32];
+                float x[32];
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = half * 32 + jj;
-                    const float t = T[i * kF + j];
-                    xw[jj] = t * sm.wc[g][j];
-                    xu[jj] = t * sm.beta[g][j];
+                    const float t = sm.T[i * kF + j];
+                    const float bj = sm.beta[j];
+                    if (grp == 0) x[jj] = t * sm.wc[j];
+                    else x[jj] = t * bj;
                 }
+                if (grp == 0) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    Tdst[half * 8 + q] = make_float4(T[i * kF + half * 32 + 4 * q], T[i * kF + half * 32 + 4 * q + 1],
-                                                     T[i * kF + half * 32 + 4 * q + 2], T[i * kF + half * 32 + 4 * q + 3]);
+                    for (int q = 0; q < 8; ++q)
+                        Tdst[half * 8 + q] = make_float4(sm.T[i * kF + half * 32 + 4 * q], sm.T[i * kF + half * 32 + 4 * q + 1],
+                                                         sm.T[i * kF + half * 32 + 4 * q + 2], sm.T[i * kF + half * 32 + 4 * q + 3]);
+                }
+                unsigned char *op = grp == 0 ? sm.op_w : sm.op_u;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int col = half * 32 + q * 8;
-                    *reinterpret_cast<uint4 *>(sm.op_w[g] + sw128_off(i, col)) =
-                        make_uint4(pack_bf2(xw[q * 8], xw[q * 8 + 1]), pack_bf2(xw[q * 8 + 2], xw[q * 8 + 3]),
-                                   pack_bf2(xw[q * 8 + 4], xw[q * 8 + 5]), pack_bf2(xw[q * 8 + 6], xw[q * 8 + 7]));
-                    *reinterpret_cast<uint4 *>(sm.op_u[g] + sw128_off(i, col)) =
-                        make_uint4(pack_bf2(xu[q * 8], xu[q * 8 + 1]), pack_bf2(xu[q * 8 + 2], xu[q * 8 + 3]),
-                                   pack_bf2(xu[q * 8 + 4], xu[q * 8 + 5]), pack_bf2(xu[q * 8 + 6], xu[q * 8 + 7]));
+                    *reinterpret_cast<uint4 *>(op + sw128_off(i, col)) =
+                        make_uint4(pack_bf2(x[q * 8], x[q * 8 + 1]), pack_bf2(x[q * 8 + 2], x[q * 8 + 3]),
+                                   pack_bf2(x[q * 8 + 4], x[q * 8 + 5]), pack_bf2(x[q * 8 + 6], x[q * 8 + 7]));
                 }
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (!mbar_wait(&sm.v_bar[g][vb], (p >> 1) & 1)) sm.err[g] = 1;
-        group_sync(g);
-        if (sm.err[g]) { ok = false; break; }
-        if (gt == 0) {  // w and u of this value head
+        if (!__syncthreads_and(mbar_wait(&sm.v_bar[vb], (jv >> 1) & 1))) { ok = false; break; }
+        if (tid == 0) {  // w -> columns 64..191, u -> 192..319
             tc_fence_after();
             const uint32_t id = idesc_bf16(64, 128, 0, 1);
-            const uint32_t ks = smem_u32(sm.k), vs = smem_u32(sm.v[g][vb]);
-            const uint32_t ws = smem_u32(sm.op_w[g]), us = smem_u32(sm.op_u[g]);
+            const uint32_t ks = smem_u32(sm.k), vs = smem_u32(sm.v[vb]);
+            const uint32_t ws = smem_u32(sm.op_w), us = smem_u32(sm.op_u);
             for (int s = 0; s < 4; ++s) {
-                mma_bf16(cw, sdesc(ws + s * 32, 16, 1024), sdesc(ks + s * 2048, kHalf, 1024), id, s > 0);
-                mma_bf16(cu, sdesc(us + s * 32, 16, 1024), sdesc(vs + s * 2048, kHalf, 1024), id, s > 0);
+                mma_bf16(tb + 64, sdesc(ws + s * 32, 16, 1024), sdesc(ks + s * 2048, kHalf, 1024), id, s > 0);
+                mma_bf16(tb + 192, sdesc(us + s * 32, 16, 1024), sdesc(vs + s * 2048, kHalf, 1024), id, s > 0);
             }
-            mma_commit(&sm.mma_bar[g]);
+            mma_commit(&sm.mma_bar);
         }
-        if (!mbar_wait(&sm.mma_bar[g], mphase)) sm.err[g] = 1;
+        ok = __syncthreads_and(mbar_wait(&sm.mma_bar, mphase));
         mphase ^= 1;
         tc_fence_after();
-        group_sync(g);
-        if (sm.err[g]) { ok = false; break; }
-        {
+        if (ok) {  // warpgroup 0 writes w, warpgroup 1 writes u
             const int i = row;
             const bool live = active && i < L;
             const size_t o = ((size_t)(t0 + (live ? i : 0)) * a.HV + hv) * kDim;
-            for (int wu = 0; wu < 2; ++wu) {
-                bf16 *dst = wu == 0 ? a.w : a.u;
-                const uint32_t col0 = (wu == 0 ? cw : cu) - tb;
-                for (int cc = 0; cc < 4; ++cc) {
-                    float w[32];
-                    tmem_ld32(t_row + col0 + cc * 32, w);
-                    tmem_ld_wait();
-                    if (live) {
-                        uint4 *wp = reinterpret_cast<uint4 *>(dst + o + cc * 32);
+            bf16 *dst = grp == 0 ? a.w : a.u;
+            const uint32_t col0 = grp == 0 ? 64 : 192;
+            for (int cc = 0; cc < 4; ++cc) {
+                float w[32];
+                tmem_ld32(t_row + col0 + cc * 32, w);
+                tmem_ld_wait();
+                if (live) {
+                    uint4 *wp = reinterpret_cast<uint4 *>(dst + o + cc * 32);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            wp[q] = make_uint4(pack_bf2(w[q * 8], w[q * 8 + 1]), pack_bf2(w[q * 8 + 2], w[q * 8 + 3]),
-                                               pack_bf2(w[q * 8 + 4], w[q * 8 + 5]), pack_bf2(w[q * 8 + 6], w[q * 8 + 7]));
-                    }
+                    for (int q = 0; q < 4; ++q)
+                        wp[q] = make_uint4(pack_bf2(w[q * 8], w[q * 8 + 1]), pack_bf2(w[q * 8 + 2], w[q * 8 + 3]),
+                                           pack_bf2(w[q * 8 + 4], w[q * 8 + 5]), pack_bf2(w[q * 8 + 6], w[q * 8 + 7]));
                 }
             }
         }
         tc_fence_before();
-        group_sync(g);
+        __syncthreads();
     }
-    if (!ok && gt == 0 && a.status) atomicOr(a.status, 2);
+    if (!ok && tid == 0 && a.status) atomicOr(a.status, 2);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
@@ -304,7 +277,6 @@ cudaError_t launch_intra_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(IntraSmem) + 1024;
-    static_assert(sizeof(IntraSmem) + 1024 <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(k_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -32,6 +32,7 @@ struct ChunkArgs {
     float *G;               // [T,HV] chunk-local cumulative log decay
     // chunk table (device, rebuilt by every call)
     int *seq_chunk_off, *chunk_seq, *chunk_start, *chunk_len;
+    int *seq_order;         // [N] sequences by decreasing length (scans start the longest first)
     int *status;            // device int, nonzero = inconsistent device cu_seqlens
     // forward scratch
     bf16 *u;                // [T,HV,V]
@@ -44,7 +45,8 @@ struct ChunkArgs {
     bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
     bf16 *dhc;              // [C_total,HV,K,V] gradient of the state after each chunk
     bf16 *dW;               // [T,HV,K]
-    float *dqp, *dkp;       // [T,HV,K] per-value-head gradients of qhat, khat
+    float *dqp, *dkp;       // [T,HV,K] per-value-head gradients of qhat, khat (h / dh' terms)
+    float *dqp2, *dkp2;     // [T,HV,K] the intra-chunk / WY terms of the same gradients
     float *dGp;             // [T,HV]
     gdn_kernel_timer *timer;  // optional per-kernel events
 };

@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
             tmem_ld32(t_row + 64 + half * 32, r1);
             if (kForward) tmem_ld32(t_row + 128 + half * 32, r2);
             tmem_ld_wait();
-#pragma unroll 4
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int t = half * 32 + j;
                 if (t < L) {

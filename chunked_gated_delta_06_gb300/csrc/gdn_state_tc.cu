@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThr, 1)
     StateSmem &sm = *reinterpret_cast<StateSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int hv = blockIdx.x, n = blockIdx.y;
+    const int hv = blockIdx.x, n = a.seq_order[blockIdx.y];  // longest sequences first
     const int h = hv / (a.HV / a.H);
     const int v = tid;  // the state row this thread owns
     const int cb = a.seq_chunk_off[n];

@@ -3,19 +3,20 @@
 // chunk form of the GDN context-parallel scans in "Qwen3.5-397B RL trainer on
 // 128 v7x", maxtext #5799).
 //
-// One CTA of 128 threads per (chunk, key head); it walks the HV/H value heads
-// of the key head.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
-//   KK = K K^T                                   (tcgen05, M=64 N=64 K=128, once)
+// One CTA of 128 threads per (chunk, value head), sized so that three CTAs share
+// an SM (about 72 KB of shared memory and 128 TMEM columns each): the pass is a
+// chain of short dependent steps, and co-resident CTAs hide one another's
+// latencies.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
+//   KK = K K^T                                   (tcgen05, M=64 N=64 K=128)
 //   A  = strict_tril(diag(beta) KKhat (.) Gamma) (CUDA cores, fp32)
-//   T  = (I + A)^-1                              (fp32, recursive 2x2 blocking:
-//        8x8 diagonal blocks by substitution, then T21 = -T22 (A21 T11) at block
-//        sizes 8, 16 and 32)
-//   w  = (T diag(beta e^G / r_k)) K,  u = (T diag(beta)) V
-//                                                (tcgen05, M=64 N=128 K=64; K and
-//                                                 V are raw MN-major TMA tiles)
-// w and u go to HBM in bf16, T in fp32 (kept for the backward).  M=64 results
-// sit in TMEM lanes 32 (m / 16) + m % 16: lanes 0..15 of warp w own rows
-// 16w..16w+15.
+//   T  = (I + A)^-1                              (fp32, in place over A:
+//        16x16 diagonal blocks by substitution, then T21 = -T22 (A21 T11) at
+//        block sizes 16 and 32, register-tiled)
+//   w^T = K^T (T diag(beta e^G / r_k))^T,  u^T = V^T (T diag(beta))^T
+//                                                (tcgen05, M=128 N=64 K=64; the K
+//                                                 and V tiles are read MN-major, so
+//                                                 row d of w^T / u^T is TMEM lane d)
+// w and u go to HBM in bf16, T in fp32 (kept for the backward).
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -27,21 +28,21 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThr = 256;   // two warpgroups share the 128 TMEM lanes
-constexpr uint32_t kHalf = 64 * 128;
-constexpr uint32_t kTile = 2 * kHalf;
-constexpr int kF = 65;
+constexpr int kThr = 128;
+constexpr uint32_t kHalf = 64 * 128;   // 64 rows x 128 bytes (one SW128 column half)
+constexpr uint32_t kTile = 2 * kHalf;  // 64 rows x 128 bf16
+constexpr int kS = 68;                 // fp32 row stride of the A / T array (16-byte rows)
+constexpr int kXs = 36;                // fp32 row stride of the X scratch
 
 struct IntraSmem {
-    unsigned char k[kTile];
-    unsigned char v[2][kTile];     // double-buffered value tiles
-    unsigned char op_w[kHalf];     // T_ij beta_j e^{G_j} / r_k,j  [i][j] K-major
-    unsigned char op_u[kHalf];     // T_ij beta_j                  [i][j] K-major
-    float A[64 * kF];
-    float T[64 * kF];
-    float X[64 * kF];
-    float G[64], beta[64], wc[64], rk[64];
-    uint64_t k_bar, v_bar[2], mma_bar;
+    unsigned char k[kTile];     // K rows [t][d] (TMA, SW128, two 64-column halves)
+    unsigned char v[kTile];     // V rows [t][d]
+    unsigned char op_w[kHalf];  // T_ij beta_j e^{G_j} / r_k,j  [i][j] K-major
+    unsigned char op_u[kHalf];  // T_ij beta_j                  [i][j] K-major
+    float M[64 * kS];           // A (strictly lower, zeros elsewhere), then T in place
+    float X[32 * kXs];          // A21 T11 of the current merge level
+    float G[64], beta[64], wc[64], rki[64];
+    uint64_t ld_bar, mma_bar;
     uint32_t tmem_base;
 };
 
@@ -54,94 +55,137 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&t);
 }
 
-// T = (I + A)^-1 for a strictly lower A (64 x 64, rows/cols >= L are zero).
-// All 128 threads take part.
-__device__ void tri_inverse(const float *A, float *T, float *X) {
-    const int tid = threadIdx.x;
-    for (int idx = tid; idx < 64 * 64; idx += kThr) T[(idx >> 6) * kF + (idx & 63)] = 0.f;
-    __syncthreads();
-    if (tid < 64) {  // 8 diagonal 8x8 blocks, one column per thread
-        const int b = tid >> 3, cc = tid & 7, base = b * 8;
-        float col[8];
+// T = (I + A)^-1 in place over M (64 x 64 fp32, row stride kS).  On entry M holds A
+// strictly below the diagonal and zeros on and above it; on exit it holds T below
+// and on the diagonal and zeros above, so every product below may run over full
+// block ranges.  All 128 threads call it; X is scratch.
+__device__ __forceinline__ void tri_inverse(float *M, float *X, int tid) {
+    // 16x16 diagonal blocks: thread (b, c) forward-substitutes column c of block b.
+    // t[m] stays 0 for m < c, so the fixed-range sums need no masks.
+    float t[16];
+    if (tid < 64) {
+        const int base = (tid >> 4) * 16, c = tid & 15;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            float x = (r == cc) ? 1.f : 0.f;
-            if (r > cc) {
+        for (int r = 0; r < 16; ++r) {
+            float x = (r == c) ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    if (m >= cc && m < r) x -= A[(base + r) * kF + base + m] * col[m];
-            }
-            col[r] = x;
+            for (int m = 0; m < r; ++m) x -= M[(base + r) * kS + base + m] * t[m];
+            t[r] = x;
         }
+    }
+    __syncthreads();  // every read of the diagonal blocks' A is done
+    if (tid < 64) {
+        const int base = (tid >> 4) * 16, c = tid & 15;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) T[(base + r) * kF + base + cc] = col[r];
+        for (int r = 0; r < 16; ++r) M[(base + r) * kS + base + c] = t[r];
     }
     __syncthreads();
-    for (int s = 8; s < 64; s *= 2) {
-        // for every merged block p of size 2s: X = A21 T11, then T21 = -T22 X
-        const int nb = 64 / (2 * s), ent = nb * s * s;
-        for (int e = tid; e < ent; e += kThr) {
-            const int p = e / (s * s), rr = (e / s) % s, cc = e % s;
-            const int r0 = p * 2 * s + s, c0 = p * 2 * s;
-            float acc = 0.f;
-            for (int m = cc; m < s; ++m) acc += A[(r0 + rr) * kF + c0 + m] * T[(c0 + m) * kF + c0 + cc];
-            X[(r0 + rr) * kF + c0 + cc] = acc;
+    // block size 16: pairs p = 0, 1 (rows 32p+16.., columns 32p..); 2x2 outputs a thread
+    {
+        const int p = tid >> 6, tt = tid & 63;
+        const int r0 = 32 * p + 16, c0 = 32 * p;
+        const int rr = 2 * (tt >> 3), cc = 2 * (tt & 7);
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float a0 = M[(r0 + rr) * kS + c0 + m], a1 = M[(r0 + rr + 1) * kS + c0 + m];
+            const float b0 = M[(c0 + m) * kS + c0 + cc], b1 = M[(c0 + m) * kS + c0 + cc + 1];
+            x00 += a0 * b0;
+            x01 += a0 * b1;
+            x10 += a1 * b0;
+            x11 += a1 * b1;
         }
+        X[(16 * p + rr) * kXs + cc] = x00;
+        X[(16 * p + rr) * kXs + cc + 1] = x01;
+        X[(16 * p + rr + 1) * kXs + cc] = x10;
+        X[(16 * p + rr + 1) * kXs + cc + 1] = x11;
         __syncthreads();
-        for (int e = tid; e < ent; e += kThr) {
-            const int p = e / (s * s), rr = (e / s) % s, cc = e % s;
-            const int r0 = p * 2 * s + s, c0 = p * 2 * s;
-            float acc = 0.f;
-            for (int m = 0; m <= rr; ++m) acc += T[(r0 + rr) * kF + r0 + m] * X[(r0 + m) * kF + c0 + cc];
-            T[(r0 + rr) * kF + c0 + cc] = -acc;
+        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float a0 = M[(r0 + rr) * kS + r0 + m], a1 = M[(r0 + rr + 1) * kS + r0 + m];
+            const float b0 = X[(16 * p + m) * kXs + cc], b1 = X[(16 * p + m) * kXs + cc + 1];
+            y00 += a0 * b0;
+            y01 += a0 * b1;
+            y10 += a1 * b0;
+            y11 += a1 * b1;
         }
+        M[(r0 + rr) * kS + c0 + cc] = -y00;
+        M[(r0 + rr) * kS + c0 + cc + 1] = -y01;
+        M[(r0 + rr + 1) * kS + c0 + cc] = -y10;
+        M[(r0 + rr + 1) * kS + c0 + cc + 1] = -y11;
+        __syncthreads();
+    }
+    // block size 32: rows 32.., columns 0..; 2x4 outputs a thread
+    {
+        const int rr = 2 * (tid >> 3), cc = 4 * (tid & 7);
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const float a0 = M[(32 + rr) * kS + m], a1 = M[(32 + rr + 1) * kS + m];
+            const float4 b = *reinterpret_cast<const float4 *>(&M[m * kS + cc]);
+            x0.x += a0 * b.x; x0.y += a0 * b.y; x0.z += a0 * b.z; x0.w += a0 * b.w;
+            x1.x += a1 * b.x; x1.y += a1 * b.y; x1.z += a1 * b.z; x1.w += a1 * b.w;
+        }
+        *reinterpret_cast<float4 *>(&X[rr * kXs + cc]) = x0;
+        *reinterpret_cast<float4 *>(&X[(rr + 1) * kXs + cc]) = x1;
+        __syncthreads();
+        float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const float a0 = M[(32 + rr) * kS + 32 + m], a1 = M[(32 + rr + 1) * kS + 32 + m];
+            const float4 b = *reinterpret_cast<const float4 *>(&X[m * kXs + cc]);
+            y0.x += a0 * b.x; y0.y += a0 * b.y; y0.z += a0 * b.z; y0.w += a0 * b.w;
+            y1.x += a1 * b.x; y1.y += a1 * b.y; y1.z += a1 * b.z; y1.w += a1 * b.w;
+        }
+        *reinterpret_cast<float4 *>(&M[(32 + rr) * kS + cc]) = make_float4(-y0.x, -y0.y, -y0.z, -y0.w);
+        *reinterpret_cast<float4 *>(&M[(32 + rr + 1) * kS + cc]) = make_float4(-y1.x, -y1.y, -y1.z, -y1.w);
         __syncthreads();
     }
 }
 
-__global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
+__global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
                                                       const __grid_constant__ IntraMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     IntraSmem &sm = *reinterpret_cast<IntraSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                    ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, h = blockIdx.y;
-    const int r = a.HV / a.H;
+    const int c = blockIdx.x, hv = blockIdx.y;
+    const int h = hv / (a.HV / a.H);
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
     if (L <= 0) return;
-    const bool active = lane < 16;
-    const int grp = warp >> 2;              // warpgroup: which half of the columns
-    const int row = (warp & 3) * 16 + lane;
 
     if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 512);
+        tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&sm.k_bar, 1);
-        mbar_init(&sm.v_bar[0], 1);
-        mbar_init(&sm.v_bar[1], 1);
+        mbar_init(&sm.ld_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.ld_bar, 2 * kTile);
+        tma_load_3d(sm.k, &maps.k, 0, h, t0, &sm.ld_bar);
+        tma_load_3d(sm.k + kHalf, &maps.k, 64, h, t0, &sm.ld_bar);
+        tma_load_3d(sm.v, &maps.v, 0, hv, t0, &sm.ld_bar);
+        tma_load_3d(sm.v + kHalf, &maps.v, 64, hv, t0, &sm.ld_bar);
+    }
+    if (tid < 64) {  // per-token scalars; tokens past L get beta = 0 and 1 / r_k = 1
+        const bool in = tid < L;
+        const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
+        const float gg = in ? a.G[gi] : 0.f, bb = in ? bf2f(a.beta[gi]) : 0.f;
+        const float ri = in ? 1.f / a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
+        sm.G[tid] = gg;
+        sm.beta[tid] = bb;
+        sm.rki[tid] = ri;
+        sm.wc[tid] = bb * __expf(gg) * ri;
     }
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // the barriers are initialised before anyone waits on them
+    bool ok = __syncthreads_and(mbar_wait(&sm.ld_bar, 0));
     tc_fence_after();
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&sm.k_bar, kTile);
-        tma_load_3d(sm.k, &maps.k, 0, h, t0, &sm.k_bar);
-        tma_load_3d(sm.k + kHalf, &maps.k, 64, h, t0, &sm.k_bar);
-        mbar_arrive_expect_tx(&sm.v_bar[0], kTile);
-        tma_load_3d(sm.v[0], &maps.v, 0, h * r, t0, &sm.v_bar[0]);
-        tma_load_3d(sm.v[0] + kHalf, &maps.v, 64, h * r, t0, &sm.v_bar[0]);
-    }
-    if (tid < 64) sm.rk[tid] = tid < L ? a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
-    bool ok = __syncthreads_and(mbar_wait(&sm.k_bar, 0));
     const uint32_t tb = sm.tmem_base;
-    const uint32_t t_row = tb + ((uint32_t)((warp & 3) * 32) << 16);
-    uint32_t mphase = 0;
-    if (tid == 0 && ok) {  // KK = K K^T into columns 0..63
-        tc_fence_after();
+    const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
+    if (tid == 0 && ok) {  // KK = K K^T into columns 0..63 (M=64: row m at lane 32 (m / 16) + m % 16)
         const uint32_t ks = smem_u32(sm.k);
         const uint32_t id = idesc_bf16(64, 64, 0, 0);
         for (int s = 0; s < 8; ++s) {
@@ -150,120 +194,104 @@ __global__ void __launch_bounds__(kThr, 1) k_intra_tc(const ChunkArgs a,
         }
         mma_commit(&sm.mma_bar);
     }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
-    mphase ^= 1;
+    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, 0));
     tc_fence_after();
-    // KKhat row i, columns [32 grp, 32 grp + 32), stays in registers for all value heads
-    float kk[32];
-    if (ok) {
-        tmem_ld32(t_row + grp * 32, kk);
+    if (ok) {  // A row i = 16 warp + lane (lanes 0..15): zeros on and above the diagonal
+        float k0[32], k1[32];
+        tmem_ld32(t_row, k0);
+        tmem_ld32(t_row + 32, k1);
         tmem_ld_wait();
-        if (active) {
+        if (lane < 16) {
+            const int i = 16 * warp + lane;
+            const float Gi = sm.G[i], ai = sm.beta[i] * sm.rki[i];
+            float *Mi = sm.M + i * kS;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) kk[j] /= (sm.rk[row] * sm.rk[grp * 32 + j]);
+            for (int q = 0; q < 8; ++q) {
+                float e[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const int j = 4 * q + z;
+                    const float msk = j < i ? 1.f : 0.f;
+                    e[z] = msk * ai * k0[j] * sm.rki[j] * __expf(fminf(Gi - sm.G[j], 0.f));
+                }
+                *reinterpret_cast<float4 *>(Mi + 4 * q) = make_float4(e[0], e[1], e[2], e[3]);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float e[4];
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const int j = 32 + 4 * q + z;
+                    const float msk = j < i ? 1.f : 0.f;
+                    e[z] = msk * ai * k1[4 * q + z] * sm.rki[j] * __expf(fminf(Gi - sm.G[j], 0.f));
+                }
+                *reinterpret_cast<float4 *>(Mi + 32 + 4 * q) = make_float4(e[0], e[1], e[2], e[3]);
+            }
         }
     }
-    for (int jv = 0; jv < r && ok; ++jv) {
-        const int hv = h * r + jv, vb = jv & 1;
-        if (tid == 0 && jv + 1 < r) {  // prefetch the next value head's tile
-            mbar_arrive_expect_tx(&sm.v_bar[vb ^ 1], kTile);
-            tma_load_3d(sm.v[vb ^ 1], &maps.v, 0, hv + 1, t0, &sm.v_bar[vb ^ 1]);
-            tma_load_3d(sm.v[vb ^ 1] + kHalf, &maps.v, 64, hv + 1, t0, &sm.v_bar[vb ^ 1]);
-        }
-        if (tid < 64) {
-            const bool in = tid < L;
-            const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
-            const float gg = in ? a.G[gi] : 0.f, bb = in ? bf2f(a.beta[gi]) : 0.f;
-            sm.G[tid] = gg;
-            sm.beta[tid] = bb;
-            sm.wc[tid] = in ? bb * __expf(gg) / sm.rk[tid] : 0.f;
-        }
-        __syncthreads();
-        if (active) {  // A row i, this warpgroup's 32 columns
-            const int i = row;
-            const float Gi = sm.G[i], bi = sm.beta[i];
+    tc_fence_before();
+    __syncthreads();  // KK has been read: its TMEM columns are free
+    tri_inverse(sm.M, sm.X, tid);
+    {  // operands T diag(c) as bf16 rows, and T to HBM: thread -> row tid / 2, 32 columns
+        const int i = tid >> 1, j0 = 32 * (tid & 1);
+        const float *Mi = sm.M + i * kS + j0;
+        float4 *Tdst = reinterpret_cast<float4 *>(a.Tm + (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = grp * 32 + jj;
-                const float msk = (j < i && i < L) ? 1.f : 0.f;
-                sm.A[i * kF + j] = msk * bi * kk[jj] * __expf(fminf(Gi - sm.G[j], 0.f));
+        for (int q = 0; q < 4; ++q) {
+            const float4 t0v = *reinterpret_cast<const float4 *>(Mi + 8 * q);
+            const float4 t1v = *reinterpret_cast<const float4 *>(Mi + 8 * q + 4);
+            Tdst[2 * q] = t0v;
+            Tdst[2 * q + 1] = t1v;
+            const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+            const int jb = j0 + 8 * q;
+            uint32_t pw[4], pu[4];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                pw[z] = pack_bf2(tv[2 * z] * sm.wc[jb + 2 * z], tv[2 * z + 1] * sm.wc[jb + 2 * z + 1]);
+                pu[z] = pack_bf2(tv[2 * z] * sm.beta[jb + 2 * z], tv[2 * z + 1] * sm.beta[jb + 2 * z + 1]);
             }
+            *reinterpret_cast<uint4 *>(sm.op_w + sw128_off(i, jb)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4 *>(sm.op_u + sw128_off(i, jb)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
         }
-        __syncthreads();
-        tri_inverse(sm.A, sm.T, sm.X);
-        // operands T diag(beta e^G / r_k) (warpgroup 0, also T to HBM) and T diag(beta) (warpgroup 1)
-        if (active) {
-            const int i = row;
-            float4 *Tdst = reinterpret_cast<float4 *>(a.Tm + ((size_t)c * a.HV + hv) * 64 * 64 + (size_t)i * 64);
-            for (int half = 0; half < 2; ++half) {
-                float x[32];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = half * 32 + jj;
-                    const float t = sm.T[i * kF + j];
-                    const float bj = sm.beta[j];
-                    if (grp == 0) x[jj] = t * sm.wc[j];
-                    else x[jj] = t * bj;
-                }
-                if (grp == 0) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        Tdst[half * 8 + q] = make_float4(sm.T[i * kF + half * 32 + 4 * q], sm.T[i * kF + half * 32 + 4 * q + 1],
-                                                         sm.T[i * kF + half * 32 + 4 * q + 2], sm.T[i * kF + half * 32 + 4 * q + 3]);
-                }
-                unsigned char *op = grp == 0 ? sm.op_w : sm.op_u;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = half * 32 + q * 8;
-                    *reinterpret_cast<uint4 *>(op + sw128_off(i, col)) =
-                        make_uint4(pack_bf2(x[q * 8], x[q * 8 + 1]), pack_bf2(x[q * 8 + 2], x[q * 8 + 3]),
-                                   pack_bf2(x[q * 8 + 4], x[q * 8 + 5]), pack_bf2(x[q * 8 + 6], x[q * 8 + 7]));
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (!__syncthreads_and(mbar_wait(&sm.v_bar[vb], (jv >> 1) & 1))) { ok = false; break; }
-        if (tid == 0) {  // w -> columns 64..191, u -> 192..319
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(64, 128, 0, 1);
-            const uint32_t ks = smem_u32(sm.k), vs = smem_u32(sm.v[vb]);
-            const uint32_t ws = smem_u32(sm.op_w), us = smem_u32(sm.op_u);
-            for (int s = 0; s < 4; ++s) {
-                mma_bf16(tb + 64, sdesc(ws + s * 32, 16, 1024), sdesc(ks + s * 2048, kHalf, 1024), id, s > 0);
-                mma_bf16(tb + 192, sdesc(us + s * 32, 16, 1024), sdesc(vs + s * 2048, kHalf, 1024), id, s > 0);
-            }
-            mma_commit(&sm.mma_bar);
-        }
-        ok = __syncthreads_and(mbar_wait(&sm.mma_bar, mphase));
-        mphase ^= 1;
-        tc_fence_after();
-        if (ok) {  // warpgroup 0 writes w, warpgroup 1 writes u
-            const int i = row;
-            const bool live = active && i < L;
-            const size_t o = ((size_t)(t0 + (live ? i : 0)) * a.HV + hv) * kDim;
-            bf16 *dst = grp == 0 ? a.w : a.u;
-            const uint32_t col0 = grp == 0 ? 64 : 192;
-            for (int cc = 0; cc < 4; ++cc) {
-                float w[32];
-                tmem_ld32(t_row + col0 + cc * 32, w);
-                tmem_ld_wait();
-                if (live) {
-                    uint4 *wp = reinterpret_cast<uint4 *>(dst + o + cc * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        wp[q] = make_uint4(pack_bf2(w[q * 8], w[q * 8 + 1]), pack_bf2(w[q * 8 + 2], w[q * 8 + 3]),
-                                           pack_bf2(w[q * 8 + 4], w[q * 8 + 5]), pack_bf2(w[q * 8 + 6], w[q * 8 + 7]));
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
     }
-    if (!ok && tid == 0 && a.status) atomicOr(a.status, 2);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, 512);
+    if (tid == 0 && ok) {  // w^T -> columns 0..63, u^T -> 64..127 (lane d, column i)
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 1, 0);
+        const uint32_t ks = smem_u32(sm.k), vs = smem_u32(sm.v);
+        const uint32_t ws = smem_u32(sm.op_w), us = smem_u32(sm.op_u);
+        for (int s = 0; s < 4; ++s) {
+            mma_bf16(tb, sdesc(ks + s * 2048, kHalf, 1024), sdesc(ws + s * 32, 16, 1024), id, s > 0);
+            mma_bf16(tb + 64, sdesc(vs + s * 2048, kHalf, 1024), sdesc(us + s * 32, 16, 1024), id, s > 0);
+        }
+        mma_commit(&sm.mma_bar);
+    }
+    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, 1));
+    tc_fence_after();
+    if (ok) {  // thread d writes element d of every live token row of w and u
+        const size_t base = ((size_t)t0 * a.HV + hv) * kDim + tid;
+        const size_t tstride = (size_t)a.HV * kDim;
+        for (int part = 0; part < 2; ++part) {
+            bf16 *dst = (part == 0 ? a.w : a.u) + base;
+            float x0[32], x1[32];
+            tmem_ld32(t_row + 64 * part, x0);
+            tmem_ld32(t_row + 64 * part + 32, x1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < L) dst[(size_t)i * tstride] = __float2bfloat16_rn(x0[i]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (32 + i < L) dst[(size_t)(32 + i) * tstride] = __float2bfloat16_rn(x1[i]);
+        }
+    } else if (tid == 0 && a.status) {
+        atomicOr(a.status, 2);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 128);
 }
 
 }  // namespace
@@ -277,11 +305,12 @@ cudaError_t launch_intra_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(IntraSmem) + 1024;
+    static_assert(3 * (sizeof(IntraSmem) + 2048) <= 233472, "three CTAs per SM");
     cudaError_t e = cudaFuncSetAttribute(k_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     TimerScope ts(a.timer, GDN_KERNEL_INTRA, s);
-    k_intra_tc<<<dim3(a.num_chunks, a.H), kThr, smem, s>>>(a, m);
+    k_intra_tc<<<dim3(a.num_chunks, a.HV), kThr, smem, s>>>(a, m);
     return cudaGetLastError();
 }
 

@@ -55,6 +55,9 @@ def report(path):
     def get(r, m):
         return r[hdr.index(m)] if m in hdr else ""
 
+    def unit(r, m):
+        return units[hdr.index(m)] if m in hdr else ""
+
     stall = [c for c in hdr if c.startswith("smsp__average_warps_issue_stalled_")
              and c.endswith("_per_issue_active.ratio")]
     lines = []
@@ -64,10 +67,11 @@ def report(path):
         tops = sorted(((float(get(r, c) or 0), c[len("smsp__average_warps_issue_stalled_"):-len(
             "_per_issue_active.ratio")]) for c in stall), reverse=True)[:4]
         lines.append(
-            "%s: %s ms; DRAM read %s MB, write %s MB (%s %% of peak); tensor pipe %s %% of active; "
+            "%s: %s %s; DRAM read %s %s, write %s %s (%s %% of peak); tensor pipe %s %% of active; "
             "warps active %s %%; %s regs/thread; grid %s block %s; stalls (cycles/issue): %s" % (
-                name, get(r, "gpu__time_duration.sum"), get(r, "dram__bytes_read.sum"),
-                get(r, "dram__bytes_write.sum"),
+                name, get(r, "gpu__time_duration.sum"), unit(r, "gpu__time_duration.sum"),
+                get(r, "dram__bytes_read.sum"), unit(r, "dram__bytes_read.sum"),
+                get(r, "dram__bytes_write.sum"), unit(r, "dram__bytes_write.sum"),
                 get(r, "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed"),
                 get(r, "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"),
                 get(r, "sm__warps_active.avg.pct_of_peak_sustained_active"),

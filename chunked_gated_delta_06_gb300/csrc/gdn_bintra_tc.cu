@@ -9,8 +9,8 @@
 //   Dw[t][k] = sum_v dv_new[t][v] h[k][v]     dW_t    = -Dw[t]
 //   Dk[t][k] = sum_v v_new[t][v] dh'[k][v]    dkhat_t = e^{G_L - G_t} Dk[t]
 // three M=64 N=128 K=128 tcgen05 products (A = the token tiles, K-major;
-// B = h / dh' read as [N=k][K=v] from their transposed [v][k] copies, i.e.
-// MN-major; all loaded by TMA).  An M=64 result row t
+// B = h / dh' as [N=k][K=v], i.e. their [k][v] tiles read K-major; all loaded
+// by TMA).  An M=64 result row t
 // sits in TMEM lane 32 (t / 16) + t % 16; the two warpgroups each take 64 of
 // its 128 columns.  It also forms the gate-gradient pieces of these terms:
 //   dG_t  = qhat_t . dqhat_t - xi_t,  xi_t = khat_t . dkhat_t,
@@ -31,8 +31,8 @@ constexpr uint32_t kBox = 64 * 128;       // 64 rows x 128 B
 constexpr uint32_t kBig = 128 * 128;      // 128 rows x 128 B
 
 struct BaSmem {
-    unsigned char h[2 * kBig];    // h_c^T [v][k]: two k-halves of 128 rows
-    unsigned char dh[2 * kBig];   // dh_c^T [v][k]
+    unsigned char h[2 * kBig];    // h_c [k][v]: two v-halves of 128 rows
+    unsigned char dh[2 * kBig];   // dh_c [k][v]
     unsigned char dO[2 * kBox];   // [t][v]
     unsigned char dvn[2 * kBox];
     unsigned char vn[2 * kBox];
@@ -114,14 +114,14 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     const uint32_t t_row = tb + ((uint32_t)((warp & 3) * 32) << 16);
     if (tid == 0 && got) {
         tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 128, 0, 1);
+        const uint32_t id = idesc_bf16(64, 128, 0, 0);
         const uint32_t hs = smem_u32(sm.h), dhs = smem_u32(sm.dh);
         const uint32_t os = smem_u32(sm.dO), ds = smem_u32(sm.dvn), vs = smem_u32(sm.vn);
         for (int s = 0; s < 8; ++s) {
-            const uint32_t ao = (s >> 2) * kBox + (s & 3) * 32, bo = s * 2048;
-            mma_bf16(tb + 0, sdesc(os + ao, 16, 1024), sdesc(hs + bo, kBig, 1024), id, s > 0);
-            mma_bf16(tb + 128, sdesc(ds + ao, 16, 1024), sdesc(hs + bo, kBig, 1024), id, s > 0);
-            mma_bf16(tb + 256, sdesc(vs + ao, 16, 1024), sdesc(dhs + bo, kBig, 1024), id, s > 0);
+            const uint32_t ao = (s >> 2) * kBox + (s & 3) * 32, bo = (s >> 2) * kBig + (s & 3) * 32;
+            mma_bf16(tb + 0, sdesc(os + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id, s > 0);
+            mma_bf16(tb + 128, sdesc(ds + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id, s > 0);
+            mma_bf16(tb + 256, sdesc(vs + ao, 16, 1024), sdesc(dhs + bo, 16, 1024), id, s > 0);
         }
         mma_commit(&sm.mma_bar);
     }

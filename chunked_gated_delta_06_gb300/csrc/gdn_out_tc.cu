@@ -10,7 +10,7 @@
 //   forward : o^T[v][t] = c_t (h^T Q^T)[v][t] + (v_new^T M^T)[v][t],
 //             c_t = e^{G_t} scale / r_q,t            (o = diag(e^G) Qhat h + M v_new)
 //   backward: dv_loc^T[v][t] = (dO^T M)[v][t]        (dv_loc = M^T dO)
-// h_c, v_new and dO are read as MN-major operands straight from their TMA
+// h_c [k][v], v_new and dO are read as MN-major operands straight from their TMA
 // tiles; thread v owns row v of the results and writes o[t][hv][v] /
 // dv_loc[t][hv][v] with coalesced stores.
 #include <string.h>
@@ -30,7 +30,7 @@ constexpr uint32_t kBig = 128 * 128;   // 128 rows x 128 B
 
 struct OutSmem {
     unsigned char kq[2 * kBig];   // [K; Q] per k-half: K rows 0..63, Q rows 64..127
-    unsigned char hc[2 * kBig];   // h_c^T [v][k] per k-half (forward)
+    unsigned char hc[2 * kBig];   // h_c [k][v] per v-half (forward)
     unsigned char tv[2 * kBox];   // v_new (forward) or dO (backward) [t][v] per v-half
     unsigned char mm[kBox];       // M, row i at row i (bf16)
     float G[64], rq[64], rk[64];
@@ -144,11 +144,11 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
         const uint32_t id = idesc_bf16(128, 64, 1, 0);    // A MN-major, B K-major
         const uint32_t tvs = smem_u32(sm.tv), mms = smem_u32(sm.mm);
         if (kForward) {
-            // O1 = h^T Q^T : A = h_c^T [v][k] (K-major), B = Q [t][k] (K-major)
-            const uint32_t id1 = idesc_bf16(128, 64, 0, 0);
+            // O1 = h^T Q^T : A = h_c [k][v] (MN-major, v halves 16 KB apart), B = Q [t][k] (K-major)
+            const uint32_t id1 = idesc_bf16(128, 64, 1, 0);
             const uint32_t hs = smem_u32(sm.hc), qs = smem_u32(sm.kq + kBox);
             for (int s = 0; s < 8; ++s)
-                mma_bf16(tb + 64, sdesc(hs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024),
+                mma_bf16(tb + 64, sdesc(hs + s * 2048, kBig, 1024),
                          sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id1, s > 0);
             // O2 = v_new^T M^T : A = v_new [j][v] (MN-major, v atoms 8 KB apart), B = M [t][j]
             for (int s = 0; s < 4; ++s)

@@ -1,23 +1,25 @@
 // gdn_state_tc.cu -- forward inter-chunk state scan on the tensor cores.
 //
-// One CTA of 128 threads per (sequence, value head) walks the sequence's
-// chunks in order ("cake_gdn: deterministic chunked GDN training kernels",
-// Summary: fp32 running state across chunks, per-chunk h stored in bf16).
-// The running state is kept transposed, S = h^T (V x K), as an fp32
-// accumulator in TMEM: lane v holds row v, columns 0..127 hold k.  Per chunk
-// (L <= 64 tokens starting at t0, G the chunk-local cumsum of g, G_L its last
+// The chunks of one sequence are walked in order ("cake_gdn: deterministic
+// chunked GDN training kernels", Summary: fp32 running state across chunks,
+// per-chunk h stored in bf16).  The value columns of the state never mix
+// (v_new[:, v] and h[:, v] depend only on column v), so one CTA of 128 threads
+// owns one (sequence, value head, value half): h[k][v'] for the 64 columns
+// v' = 64 vb .. 64 vb + 63, as an fp32 accumulator in TMEM (lane k, 64 columns).
+// Per chunk (L <= 64 tokens from t0, G the chunk-local cumsum of g, G_L its last
 // value):
-//   1. thread v reads row v of S, writes it as bf16 to shared memory (MMA
-//      operand) and e^{G_L} S back to TMEM; one TMA store copies the bf16 tile
-//      to h_c[chunk][hv] (stored transposed, [v][k]);
-//   2. P = S_bf16 w^T                      (tcgen05, M=128 N=64 K=128)
-//   3. v_new^T[v][t] = u[t][v] - P[v][t]  -> v_new in HBM (bf16), and the
-//      operand A_V[v][t] = v_new^T[v][t] e^{G_L - G_t} / r_k,t (bf16, smem)
-//   4. S += A_V K                           (tcgen05, M=128 N=128 K=64; K is the
-//      raw key tile read as an MN-major operand)
-// which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with
-// Khat = diag(1 / r_k) K.  w, u and K tiles stream in by TMA two chunks ahead.
-// Every wait is bounded; a timeout sets status bit 2 and the CTA unwinds.
+//   1. thread k writes row k of h as bf16 to shared memory (MMA operand; one TMA
+//      store copies it to h_c[chunk][hv][k][v']), and e^{G_L} h back to TMEM;
+//   2. P[t][v'] = sum_k w[t][k] h[k][v']          (tcgen05, M=64 N=64 K=128)
+//   3. thread t (TMEM lane 32 (t / 16) + t % 16) forms v_new[t][v'] = u - P as
+//      whole rows: to HBM (bf16), and A_V[t][v'] = v_new e^{G_L - G_t} / r_k,t
+//      (bf16, shared memory);
+//   4. h[k][v'] += sum_t K[t][k] A_V[t][v']        (tcgen05, M=128 N=64 K=64; the
+//      raw key tile is read MN-major)
+// which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with Khat =
+// diag(1 / r_k) K.  w, K and this half of u stream in by TMA two chunks ahead.
+// Two CTAs share an SM.  Every wait is bounded; a timeout sets status bit 2 and
+// the CTA unwinds.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -30,15 +32,15 @@ namespace {
 using namespace umma;
 
 constexpr int kThr = 128;
-constexpr uint32_t kTileBytes = 64 * 128;          // one 64 x 64 bf16 SW128 box
-constexpr uint32_t kStageBytes = 6 * kTileBytes;   // w (2 boxes), K (2), u (2)
+constexpr uint32_t kBox = 64 * 128;             // one 64-row x 128-byte SW128 box
+constexpr uint32_t kStageBytes = 5 * kBox;      // w (2 boxes), K (2), u half (1)
 
 struct StateSmem {
     // 1024-byte aligned operand tiles first
-    unsigned char a_s[2 * 128 * 128];   // S bf16 [v][k]: two k-halves of 128 x 128 B
-    unsigned char a_v[128 * 128];       // A_V bf16 [v][t]: 128 x 128 B
+    unsigned char a_s[128 * 128];       // h bf16 [k][v']: 128 rows x 128 B
+    unsigned char a_v[64 * 128];        // A_V bf16 [t][v']: 64 rows x 128 B
     unsigned char stage[2][kStageBytes];
-    float coef[2][64];                  // e^{G_L - G_t} / r_k,t, 0 past L
+    float coef[64];                     // e^{G_L - G_t} / r_k,t, 0 past L
     float gt[64], rkt[64];              // this chunk's G and r_k (prefetched)
     uint64_t tma_bar[2];
     uint64_t mma_bar;
@@ -51,32 +53,39 @@ struct StateMaps {
 };
 
 __device__ __forceinline__ void issue_stage(const StateMaps &m, StateSmem &sm, int st, int t0, int h,
-                                            int hv) {
+                                            int hv, int vb) {
     unsigned char *b = sm.stage[st];
     mbar_arrive_expect_tx(&sm.tma_bar[st], kStageBytes);
-    tma_load_3d(b + 0 * kTileBytes, &m.w, 0, hv, t0, &sm.tma_bar[st]);
-    tma_load_3d(b + 1 * kTileBytes, &m.w, 64, hv, t0, &sm.tma_bar[st]);
-    tma_load_3d(b + 2 * kTileBytes, &m.k, 0, h, t0, &sm.tma_bar[st]);
-    tma_load_3d(b + 3 * kTileBytes, &m.k, 64, h, t0, &sm.tma_bar[st]);
-    tma_load_3d(b + 4 * kTileBytes, &m.u, 0, hv, t0, &sm.tma_bar[st]);
-    tma_load_3d(b + 5 * kTileBytes, &m.u, 64, hv, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 0 * kBox, &m.w, 0, hv, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 1 * kBox, &m.w, 64, hv, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 2 * kBox, &m.k, 0, h, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 3 * kBox, &m.k, 64, h, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 4 * kBox, &m.u, 64 * vb, hv, t0, &sm.tma_bar[st]);
 }
 
-__global__ void __launch_bounds__(kThr, 1)
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
+__global__ void __launch_bounds__(kThr, 2)
     k_state_tc(const ChunkArgs a, const __grid_constant__ StateMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     StateSmem &sm = *reinterpret_cast<StateSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int hv = blockIdx.x, n = a.seq_order[blockIdx.y];  // longest sequences first
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hv = blockIdx.x >> 1, vb = blockIdx.x & 1;
+    const int n = a.seq_order[blockIdx.y];  // longest sequences first
     const int h = hv / (a.HV / a.H);
-    const int v = tid;  // the state row this thread owns
     const int cb = a.seq_chunk_off[n];
     const int ce = min(a.seq_chunk_off[n + 1], a.num_chunks);
     const int nch = max(ce - cb, 0);
+    const int kr = tid;                         // the state row this thread owns (S pass)
+    const int tr = 16 * warp + lane;            // the token row it owns (lanes 0..15)
+    const bool trow = lane < 16;
 
     if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 256);
+        tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -89,26 +98,34 @@ __global__ void __launch_bounds__(kThr, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = sm.tmem_base;
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
-    const uint32_t tS = t_row, tP = t_row + 128;
+    const uint32_t t_row = sm.tmem_base + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+    const uint32_t tH = t_row, tP = t_row + 64;
 
     if (tid == 0) {
-        for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, i, a.chunk_start[cb + i], h, hv);
+        for (int i = 0; i < 2 && i < nch; ++i)
+            issue_stage(maps, sm, i, a.chunk_start[cb + i], h, hv, vb);
     }
-    // S <- h0^T (row v = column v of h0[n][hv])
-    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim;
-    for (int kc = 0; kc < 4; ++kc) {
+    // h <- h0[n][hv][k][v'] (row kr, this half's 64 columns)
+    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb;
+    for (int half = 0; half < 2; ++half) {
         float r[32];
+        if (a.h0) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.h0 + sbase + 32 * half);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            r[j] = a.h0 ? a.h0[sbase + (size_t)(kc * 32 + j) * kDim + v] : 0.f;
-        tmem_st32(tS + kc * 32, r);
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = src[q];
+                r[4 * q] = x.x; r[4 * q + 1] = x.y; r[4 * q + 2] = x.z; r[4 * q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0.f;
+        }
+        tmem_st32(tH + 32 * half, r);
     }
     tmem_st_wait();
 
-    const uint32_t idP = idesc_bf16(128, 64, 0, 0);    // P = S w^T
-    const uint32_t idS = idesc_bf16(128, 128, 0, 1);   // S += A_V K  (K MN-major)
+    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // P = w h       (h MN-major)
+    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // h += K^T A_V  (both MN-major)
     uint32_t mma_phase = 0;
     bool ok = true;
     // per-token scalars of the next chunk, loaded one chunk ahead
@@ -132,101 +149,105 @@ __global__ void __launch_bounds__(kThr, 1)
             sm.rkt[tid] = prk;
             if (i + 1 < nch) fetch(c + 1);
         }
-        __syncthreads();
-        const float Gl = L > 0 ? sm.gt[L - 1] : 0.f;
-        if (tid < 64) sm.coef[st][tid] = tid < L ? expf(Gl - sm.gt[tid]) / sm.rkt[tid] : 0.f;
-        const float egl = expf(Gl);
-        // 1. S -> bf16 operand (copied to h_c by TMA below), then S <- e^{G_L} S
         if (tid == 0) tma_store_wait_read();  // the previous chunk's h_c store has read a_s
         __syncthreads();
-        for (int kc = 0; kc < 4; ++kc) {
-            float r[32];
-            tmem_ld32(tS + kc * 32, r);
+        const float Gl = L > 0 ? sm.gt[L - 1] : 0.f;
+        if (tid < 64) sm.coef[tid] = tid < L ? __expf(fminf(Gl - sm.gt[tid], 0.f)) / sm.rkt[tid] : 0.f;
+        const float egl = __expf(Gl);
+        // 1. h -> bf16 operand row kr (copied to h_c by TMA below), then h <- e^{G_L} h
+        {
+            float r0[32], r1[32];
+            tmem_ld32(tH, r0);
+            tmem_ld32(tH + 32, r1);
             tmem_ld_wait();
-            unsigned char *sub = sm.a_s + (kc >> 1) * (128 * 128);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 4 chunks of 8 columns
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 two = __floats2bfloat162_rn(r[q * 8 + 2 * e], r[q * 8 + 2 * e + 1]);
-                    pk[e] = *reinterpret_cast<uint32_t *>(&two);
-                }
-                const int col = (kc & 1) * 32 + q * 8;
-                *reinterpret_cast<uint4 *>(sub + sw128_off(v, col)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int q = 0; q < 4; ++q) {
+                *reinterpret_cast<uint4 *>(sm.a_s + sw128_off(kr, 8 * q)) =
+                    make_uint4(pack_bf2(r0[8 * q], r0[8 * q + 1]), pack_bf2(r0[8 * q + 2], r0[8 * q + 3]),
+                               pack_bf2(r0[8 * q + 4], r0[8 * q + 5]), pack_bf2(r0[8 * q + 6], r0[8 * q + 7]));
+                *reinterpret_cast<uint4 *>(sm.a_s + sw128_off(kr, 32 + 8 * q)) =
+                    make_uint4(pack_bf2(r1[8 * q], r1[8 * q + 1]), pack_bf2(r1[8 * q + 2], r1[8 * q + 3]),
+                               pack_bf2(r1[8 * q + 4], r1[8 * q + 5]), pack_bf2(r1[8 * q + 6], r1[8 * q + 7]));
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] *= egl;
-            tmem_st32(tS + kc * 32, r);
+            for (int j = 0; j < 32; ++j) {
+                r0[j] *= egl;
+                r1[j] *= egl;
+            }
+            tmem_st32(tH, r0);
+            tmem_st32(tH + 32, r1);
         }
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        // 2. P = S_bf16 w^T (every thread waits for the chunk's tiles: u is read below)
+        // every thread waits for the chunk's tiles (u is read below)
         if (!mbar_wait(&sm.tma_bar[st], (i >> 1) & 1)) sm.error = 1;
         __syncthreads();
+        // 2. P = w h
         if (tid == 0) {
             tc_fence_after();
             if (!sm.error) {
                 const uint32_t as = smem_u32(sm.a_s), ws = smem_u32(sm.stage[st]);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_bf16(tP, sdesc(as + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024),
-                             sdesc(ws + (s >> 2) * kTileBytes + (s & 3) * 32, 16, 1024), idP, s > 0);
+                    mma_bf16(tP, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
+                             sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
                 mma_commit(&sm.mma_bar);
-                const int hrow = (c * a.HV + hv) * 128;  // h_c^T rows of this chunk
-                tma_store_3d(&maps.hc, 0, 0, hrow, sm.a_s);
-                tma_store_3d(&maps.hc, 64, 0, hrow, sm.a_s + 128 * 128);
+                const int hrow = (c * a.HV + hv) * 128;  // h_c rows (k) of this chunk
+                tma_store_3d(&maps.hc, 64 * vb, 0, hrow, sm.a_s);
                 tma_store_commit();
             }
         }
         __syncthreads();
         if (sm.error) { ok = false; break; }
-        if (!mbar_wait(&sm.mma_bar, mma_phase)) { sm.error = 1; }
+        if (!mbar_wait(&sm.mma_bar, mma_phase)) sm.error = 1;
         mma_phase ^= 1;
         tc_fence_after();
-        // 3. v_new^T = u^T - P
-        const unsigned char *us = sm.stage[st] + 4 * kTileBytes + (v >> 6) * kTileBytes;
-        unsigned char *avs = sm.a_v;
-        for (int tc = 0; tc < 2; ++tc) {
-            float p[32];
-            tmem_ld32(tP + tc * 32, p);
+        // 3. v_new = u - P, row tr
+        {
+            float p0[32], p1[32];
+            tmem_ld32(tP, p0);
+            tmem_ld32(tP + 32, p1);
             tmem_ld_wait();
+            if (trow) {
+                const bool live = tr < L;
+                const float cf = sm.coef[tr];
+                const unsigned char *us = sm.stage[st] + 4 * kBox;
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    a.vnew + ((size_t)(t0 + (live ? tr : 0)) * a.HV + hv) * kDim + 64 * vb);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t pk[4];
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 ux = *reinterpret_cast<const uint4 *>(us + sw128_off(tr, 8 * q));
+                    const __nv_bfloat162 *ub = reinterpret_cast<const __nv_bfloat162 *>(&ux);
+                    float vn[8];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float x2[2];
-#pragma unroll
-                    for (int z = 0; z < 2; ++z) {
-                        const int t = tc * 32 + q * 8 + 2 * e + z;
-                        float vn = 0.f;
-                        if (t < L) {
-                            const float uu = bf2f(*reinterpret_cast<const bf16 *>(us + sw128_off(t, v & 63)));
-                            vn = uu - p[q * 8 + 2 * e + z];
-                            a.vnew[((size_t)(t0 + t) * a.HV + hv) * kDim + v] = f2bf(vn);
-                        }
-                        x2[z] = vn * sm.coef[st][t];
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 uf = __bfloat1622float2(ub[e]);
+                        const int j = 8 * q + 2 * e;
+                        const float pa = j < 32 ? p0[j & 31] : p1[j & 31];
+                        const float pb = j + 1 < 32 ? p0[(j + 1) & 31] : p1[(j + 1) & 31];
+                        vn[2 * e] = live ? uf.x - pa : 0.f;
+                        vn[2 * e + 1] = live ? uf.y - pb : 0.f;
                     }
-                    __nv_bfloat162 two = __floats2bfloat162_rn(x2[0], x2[1]);
-                    pk[e] = *reinterpret_cast<uint32_t *>(&two);
+                    if (live)
+                        dst[q] = make_uint4(pack_bf2(vn[0], vn[1]), pack_bf2(vn[2], vn[3]),
+                                            pack_bf2(vn[4], vn[5]), pack_bf2(vn[6], vn[7]));
+                    *reinterpret_cast<uint4 *>(sm.a_v + sw128_off(tr, 8 * q)) =
+                        make_uint4(pack_bf2(vn[0] * cf, vn[1] * cf), pack_bf2(vn[2] * cf, vn[3] * cf),
+                                   pack_bf2(vn[4] * cf, vn[5] * cf), pack_bf2(vn[6] * cf, vn[7] * cf));
                 }
-                *reinterpret_cast<uint4 *>(avs + sw128_off(v, tc * 32 + q * 8)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // 4. S += A_V K
+        // 4. h += K^T A_V
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t av = smem_u32(sm.a_v), ks = smem_u32(sm.stage[st] + 2 * kTileBytes);
+            const uint32_t av = smem_u32(sm.a_v), ks = smem_u32(sm.stage[st] + 2 * kBox);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tS, sdesc(av + s * 32, 16, 1024), sdesc(ks + s * 2048, kTileBytes, 1024), idS,
+                mma_bf16(tH, sdesc(ks + s * 2048, kBox, 1024), sdesc(av + s * 2048, kBox, 1024), idS,
                          true);
             mma_commit(&sm.mma_bar);
         }
@@ -235,15 +256,16 @@ __global__ void __launch_bounds__(kThr, 1)
         tc_fence_after();
         __syncthreads();
         if (sm.error) { ok = false; break; }
-        if (tid == 0 && i + 2 < nch) issue_stage(maps, sm, st, a.chunk_start[c + 2], h, hv);
+        if (tid == 0 && i + 2 < nch) issue_stage(maps, sm, st, a.chunk_start[c + 2], h, hv, vb);
     }
     if (ok && a.ht) {
-        for (int kc = 0; kc < 4; ++kc) {
+        for (int half = 0; half < 2; ++half) {
             float r[32];
-            tmem_ld32(tS + kc * 32, r);
+            tmem_ld32(tH + 32 * half, r);
             tmem_ld_wait();
+            float4 *dst = reinterpret_cast<float4 *>(a.ht + sbase + 32 * half);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a.ht[sbase + (size_t)(kc * 32 + j) * kDim + v] = r[j];
+            for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
         }
     }
     if (tid == 0) tma_store_wait_all();
@@ -257,7 +279,7 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(sm.tmem_base, 128);
 }
 
 }  // namespace
@@ -272,11 +294,12 @@ cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.hc, a.hc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb, rowb, 128)))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(StateSmem) + 1024;
+    static_assert(2 * (sizeof(StateSmem) + 2048) <= 233472, "two CTAs per SM");
     cudaError_t e = cudaFuncSetAttribute(k_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
-    k_state_tc<<<dim3(a.HV, a.N), kThr, smem, s>>>(a, m);
+    k_state_tc<<<dim3(2 * a.HV, a.N), kThr, smem, s>>>(a, m);
     return cudaGetLastError();
 }
 

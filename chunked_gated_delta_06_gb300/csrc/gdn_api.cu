@@ -96,7 +96,6 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.dW = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dqp = cv.take<float>((size_t)d.T * d.HV * D);
     a.dkp = cv.take<float>((size_t)d.T * d.HV * D);
-    a.dqp2 = cv.take<float>((size_t)d.T * d.HV * D);
     a.dkp2 = cv.take<float>((size_t)d.T * d.HV * D);
     a.dGp = cv.take<float>((size_t)d.T * d.HV);
 }

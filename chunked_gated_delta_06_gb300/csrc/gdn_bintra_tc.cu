@@ -1,22 +1,29 @@
 // gdn_bintra_tc.cu -- backward terms of a chunk that go through the per-chunk
-// states h (chunk start) and dh' (gradient of the state after the chunk), on
-// the tensor cores ("dqkwg" of "cake_gdn: deterministic chunked GDN training
-// kernels", section 2).
+// states h (chunk start) and dh' (gradient of the state after the chunk) and
+// through the intra-chunk attention matrix, on the tensor cores ("dqkwg" of
+// "cake_gdn: deterministic chunked GDN training kernels", section 2).
 //
-// One CTA of 256 threads per (chunk, value head).  With h_c, dh_c [k][v]
-// (bf16, from the forward and reverse scans) and dO, dv_new, v_new [t][v]:
-//   Dq[t][k] = sum_v dO[t][v] h[k][v]         dqhat_t = e^{G_t} Dq[t]
-//   Dw[t][k] = sum_v dv_new[t][v] h[k][v]     dW_t    = -Dw[t]
-//   Dk[t][k] = sum_v v_new[t][v] dh'[k][v]    dkhat_t = e^{G_L - G_t} Dk[t]
-// three M=64 N=128 K=128 tcgen05 products (A = the token tiles, K-major;
-// B = h / dh' as [N=k][K=v], i.e. their [k][v] tiles read K-major; all loaded
-// by TMA).  An M=64 result row t
-// sits in TMEM lane 32 (t / 16) + t % 16; the two warpgroups each take 64 of
-// its 128 columns.  It also forms the gate-gradient pieces of these terms:
-//   dG_t  = qhat_t . dqhat_t - xi_t,  xi_t = khat_t . dkhat_t,
-//   dG_L += sum_t xi_t + e^{G_L} <h, dh'>.
+// One CTA of 256 threads per (chunk, value head).  With h_c, dh_c [k][v] (bf16,
+// from the forward and reverse scans), dO, dv_new, v_new [t][v], Qhat =
+// diag(scale / r_q) Q, Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
+//   batch 1 (M=64, rows = tokens, contraction 128):
+//     Dq = dO h^T,  Dw = dv_new h^T,  Dk = v_new dh'^T     (N = 128)
+//     QK = Q K^T,   dM = dO v_new^T                         (N = 64)
+//   dW = -Dw (to HBM, for the WY pullback);
+//   M_ij = QK_ij scale / (r_q,i r_k,j) Gamma_ij,  dMG = dM (.) Gamma,  P1 = dM (.) M
+//   (j <= i);
+//   batch 2 (M=64, contraction 64): dMG Khat and dMG^T Qhat;
+//   dqhat_t = e^{G_t} Dq_t + (dMG Khat)_t                  -> HBM (fp32, per value head)
+//   dkhat_t = e^{G_L - G_t} Dk_t + (dMG^T Qhat)_t           -> HBM (fp32, the rest comes
+//                                                              from the WY pullback)
+//   dG_t    = qhat_t . e^{G_t} Dq_t - xi_t + sum_j P1_tj - sum_i P1_it,
+//   xi_t = khat_t . e^{G_L - G_t} Dk_t,   dG_L += sum_t xi_t + e^{G_L} <h, dh'>.
+// h / dh' are read as [N=k][K=v], i.e. their [k][v] tiles K-major; all tiles
+// come by TMA.  An M=64 result row t sits in TMEM lane 32 (t / 16) + t % 16; the
+// two warpgroups split the columns.  Column sums are warp butterflies.
 #include <string.h>
 
+#include "gdn_epi.cuh"
 #include "gdn_kernels.h"
 #include "gdn_tma.h"
 #include "gdn_umma.cuh"
@@ -25,10 +32,17 @@ namespace gdn {
 namespace {
 
 using namespace umma;
+using epi::colsum16;
+using epi::pack_bf2;
+using epi::put_row32;
 
 constexpr int kThr = 256;
 constexpr uint32_t kBox = 64 * 128;       // 64 rows x 128 B
 constexpr uint32_t kBig = 128 * 128;      // 128 rows x 128 B
+
+// TMEM columns (512 allocated)
+constexpr uint32_t cDQ = 0, cDW = 128, cDK = 256, cQK = 384, cDM = 448;   // batch 1
+constexpr uint32_t cQI = 384, cKI = 128;                                   // batch 2
 
 struct BaSmem {
     unsigned char h[2 * kBig];    // h_c [k][v]: two v-halves of 128 rows
@@ -38,9 +52,13 @@ struct BaSmem {
     unsigned char vn[2 * kBox];
     unsigned char q[2 * kBox];    // [t][k]
     unsigned char k[2 * kBox];
+    unsigned char op_dmg[kBox];   // dMG_tj / r_k,j        [t][j]  K-major A of dMG Khat
+    unsigned char op_dmgt[kBox];  // dMG_it scale / r_q,i  [i][t]  MN-major A of dMG^T Qhat
     float pq[2][64], pk[2][64];   // per-warpgroup partial row dots
+    float rp[2][64];              // per-warpgroup partial row sums of P1
+    float cp[4][64];              // per-row-block column sums of P1
     float hdh[kThr / 32];
-    float eg[64], egl_g[64];      // e^{G_t}, e^{G_L - G_t} (0 past L)
+    float G[64], eg[64], egl_g[64];  // G, e^{G_t}, e^{G_L - G_t} (0 past L)
     float qsc[64], rki[64];       // scale / r_q, 1 / r_k
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
@@ -49,11 +67,6 @@ struct BaSmem {
 struct BaMaps {
     CUtensorMap h, dh, dO, dvn, vn, q, k;
 };
-
-__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&t);
-}
 
 __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                                                          const __grid_constant__ BaMaps maps) {
@@ -67,7 +80,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     if (L <= 0) return;
     const bool active = lane < 16;
     const int grp = warp >> 2;
-    const int t = (warp & 3) * 16 + lane;  // the token row this lane owns (valid when active)
+    const int sub = warp & 3;
+    const int t = sub * 16 + lane;  // the token row this lane owns (valid when active)
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -104,6 +118,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         const bool in = tid < L;
         const size_t r = (size_t)(t0 + tid) * a.H + h;
         const float Gt = in ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
+        sm.G[tid] = Gt;
         sm.eg[tid] = in ? __expf(Gt) : 0.f;
         sm.egl_g[tid] = in ? __expf(fminf(Gl - Gt, 0.f)) : 0.f;
         sm.qsc[tid] = in ? a.scale / a.rq[r] : 0.f;
@@ -111,17 +126,22 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     }
     const bool got = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t tb = sm.tmem_base;
-    const uint32_t t_row = tb + ((uint32_t)((warp & 3) * 32) << 16);
-    if (tid == 0 && got) {
+    const uint32_t t_row = tb + ((uint32_t)(sub * 32) << 16);
+    uint32_t phase = 0;
+    if (tid == 0 && got) {  // batch 1
         tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 128, 0, 0);
+        const uint32_t id128 = idesc_bf16(64, 128, 0, 0), id64 = idesc_bf16(64, 64, 0, 0);
         const uint32_t hs = smem_u32(sm.h), dhs = smem_u32(sm.dh);
         const uint32_t os = smem_u32(sm.dO), ds = smem_u32(sm.dvn), vs = smem_u32(sm.vn);
+        const uint32_t qs = smem_u32(sm.q), ks = smem_u32(sm.k);
+#pragma unroll
         for (int s = 0; s < 8; ++s) {
             const uint32_t ao = (s >> 2) * kBox + (s & 3) * 32, bo = (s >> 2) * kBig + (s & 3) * 32;
-            mma_bf16(tb + 0, sdesc(os + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id, s > 0);
-            mma_bf16(tb + 128, sdesc(ds + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id, s > 0);
-            mma_bf16(tb + 256, sdesc(vs + ao, 16, 1024), sdesc(dhs + bo, 16, 1024), id, s > 0);
+            mma_bf16(tb + cDQ, sdesc(os + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
+            mma_bf16(tb + cDW, sdesc(ds + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
+            mma_bf16(tb + cDK, sdesc(vs + ao, 16, 1024), sdesc(dhs + bo, 16, 1024), id128, s > 0);
+            mma_bf16(tb + cQK, sdesc(qs + ao, 16, 1024), sdesc(ks + ao, 16, 1024), id64, s > 0);
+            mma_bf16(tb + cDM, sdesc(os + ao, 16, 1024), sdesc(vs + ao, 16, 1024), id64, s > 0);
         }
         mma_commit(&sm.mma_bar);
     }
@@ -146,51 +166,133 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     }
     hdh = warp_sum(hdh);
     if (lane == 0) sm.hdh[warp] = hdh;
-    const bool done = __syncthreads_and(got && mbar_wait(&sm.mma_bar, 0));
+    bool done = __syncthreads_and(got && mbar_wait(&sm.mma_bar, phase));
+    phase ^= 1;
     tc_fence_after();
+    const bool live = active && t < L;
     if (done) {
-        const bool live = active && t < L;
-        const float eg = live ? sm.eg[t] : 0.f, el = live ? sm.egl_g[t] : 0.f;
+        // (a) QK, dM -> P1 (row and column sums) and the two dMG operand rows
+        const int j0 = 32 * grp;
+        float qk[32], dm[32];
+        tmem_ld32(t_row + cQK + j0, qk);
+        tmem_ld32(t_row + cDM + j0, dm);
+        tmem_ld_wait();
+        const float Gi = active ? sm.G[t] : 0.f;
+        const float qsi = active ? sm.qsc[t] : 0.f;
+        float rsum = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {  // in place: dm <- dMG, qk <- P1
+            const int j = j0 + jj;
+            const float msk = (live && j <= t) ? 1.f : 0.f;
+            dm[jj] *= msk * __expf(fminf(Gi - sm.G[j], 0.f));
+            qk[jj] = dm[jj] * qk[jj] * qsi * sm.rki[j];
+            rsum += qk[jj];
+        }
+        float s0, s1;
+        colsum16(qk, lane, s0, s1);
+        if (active) {
+            sm.cp[sub][j0 + 2 * lane] = s0;
+            sm.cp[sub][j0 + 2 * lane + 1] = s1;
+            sm.rp[grp][t] = rsum;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * sm.rki[j0 + jj];
+        if (active) put_row32(sm.op_dmg, t, j0, qk);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * qsi;
+        if (active) put_row32(sm.op_dmgt, t, j0, qk);
+        // (b) dW = -Dw rows, this warpgroup's 64 columns
         const size_t o = ((size_t)(t0 + (live ? t : 0)) * a.HV + hv) * kDim;
-        float xq = 0.f, xk = 0.f;
-        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {  // this warpgroup's 64 columns
-            float dq[32], dw[32], dk[32];
-            tmem_ld32(t_row + 0 + cc * 32, dq);
-            tmem_ld32(t_row + 128 + cc * 32, dw);
-            tmem_ld32(t_row + 256 + cc * 32, dk);
+#pragma unroll
+        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
+            float dw[32];
+            tmem_ld32(t_row + cDW + cc * 32, dw);
             tmem_ld_wait();
             if (live) {
-                float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
-                float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
-                const unsigned char *qrow = sm.q + (cc >> 1) * kBox, *krow = sm.k + (cc >> 1) * kBox;
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per step
-                    const int col = (cc & 1) * 32 + q8 * 8;
-                    const uint4 qx = *reinterpret_cast<const uint4 *>(qrow + sw128_off(t, col));
-                    const uint4 kx = *reinterpret_cast<const uint4 *>(krow + sw128_off(t, col));
-                    const __nv_bfloat162 *qb = reinterpret_cast<const __nv_bfloat162 *>(&qx);
-                    const __nv_bfloat162 *kb = reinterpret_cast<const __nv_bfloat162 *>(&kx);
-                    float dqv[8], dkv[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 qf = __bfloat1622float2(qb[e]), kf = __bfloat1622float2(kb[e]);
-                        dqv[2 * e] = eg * dq[q8 * 8 + 2 * e];
-                        dqv[2 * e + 1] = eg * dq[q8 * 8 + 2 * e + 1];
-                        dkv[2 * e] = el * dk[q8 * 8 + 2 * e];
-                        dkv[2 * e + 1] = el * dk[q8 * 8 + 2 * e + 1];
-                        xq += qf.x * dqv[2 * e] + qf.y * dqv[2 * e + 1];
-                        xk += kf.x * dkv[2 * e] + kf.y * dkv[2 * e + 1];
-                    }
-                    qp[q8 * 2] = make_float4(dqv[0], dqv[1], dqv[2], dqv[3]);
-                    qp[q8 * 2 + 1] = make_float4(dqv[4], dqv[5], dqv[6], dqv[7]);
-                    kp[q8 * 2] = make_float4(dkv[0], dkv[1], dkv[2], dkv[3]);
-                    kp[q8 * 2 + 1] = make_float4(dkv[4], dkv[5], dkv[6], dkv[7]);
-                }
                 uint4 *wp = reinterpret_cast<uint4 *>(a.dW + o + cc * 32);
 #pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8)
                     wp[q8] = make_uint4(pack_bf2(-dw[q8 * 8], -dw[q8 * 8 + 1]), pack_bf2(-dw[q8 * 8 + 2], -dw[q8 * 8 + 3]),
                                         pack_bf2(-dw[q8 * 8 + 4], -dw[q8 * 8 + 5]), pack_bf2(-dw[q8 * 8 + 6], -dw[q8 * 8 + 7]));
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && done) {  // batch 2: dMG Khat -> cQI, dMG^T Qhat -> cKI (over the Dw columns)
+        tc_fence_after();
+        const uint32_t id_km = idesc_bf16(64, 128, 0, 1);  // A K-major, B MN-major
+        const uint32_t id_mm = idesc_bf16(64, 128, 1, 1);  // A MN-major, B MN-major
+        const uint32_t ks = smem_u32(sm.k), qs = smem_u32(sm.q);
+        const uint32_t g1 = smem_u32(sm.op_dmg), g2 = smem_u32(sm.op_dmgt);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            mma_bf16(tb + cQI, sdesc(g1 + s * 32, 16, 1024), sdesc(ks + s * 2048, kBox, 1024), id_km, s > 0);
+            mma_bf16(tb + cKI, sdesc(g2 + s * 2048, kBox, 1024), sdesc(qs + s * 2048, kBox, 1024), id_mm, s > 0);
+        }
+        mma_commit(&sm.mma_bar);
+    }
+    done = __syncthreads_and(done && mbar_wait(&sm.mma_bar, phase));
+    tc_fence_after();
+    if (done) {  // dqhat, dkhat rows (this warpgroup's 64 columns) and the inter-term row dots
+        const float eg = live ? sm.eg[t] : 0.f, el = live ? sm.egl_g[t] : 0.f;
+        const size_t o = ((size_t)(t0 + (live ? t : 0)) * a.HV + hv) * kDim;
+        float xq = 0.f, xk = 0.f;
+#pragma unroll
+        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
+            float dq[32], qi[32];
+            tmem_ld32(t_row + cDQ + cc * 32, dq);
+            tmem_ld32(t_row + cQI + cc * 32, qi);
+            tmem_ld_wait();
+            const unsigned char *qrow = sm.q + (cc >> 1) * kBox;
+            float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per step
+                const int col = (cc & 1) * 32 + q8 * 8;
+                const uint4 qx = *reinterpret_cast<const uint4 *>(qrow + sw128_off(t, col));
+                const __nv_bfloat162 *qb = reinterpret_cast<const __nv_bfloat162 *>(&qx);
+                float v8[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 qf = __bfloat1622float2(qb[e]);
+                    const float a0 = eg * dq[q8 * 8 + 2 * e], a1 = eg * dq[q8 * 8 + 2 * e + 1];
+                    xq += qf.x * a0 + qf.y * a1;
+                    v8[2 * e] = a0 + qi[q8 * 8 + 2 * e];
+                    v8[2 * e + 1] = a1 + qi[q8 * 8 + 2 * e + 1];
+                }
+                if (live) {
+                    qp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+                    qp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+                }
+            }
+        }
+#pragma unroll
+        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
+            float dk[32], ki[32];
+            tmem_ld32(t_row + cDK + cc * 32, dk);
+            tmem_ld32(t_row + cKI + cc * 32, ki);
+            tmem_ld_wait();
+            const unsigned char *krow = sm.k + (cc >> 1) * kBox;
+            float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                const int col = (cc & 1) * 32 + q8 * 8;
+                const uint4 kx = *reinterpret_cast<const uint4 *>(krow + sw128_off(t, col));
+                const __nv_bfloat162 *kb = reinterpret_cast<const __nv_bfloat162 *>(&kx);
+                float v8[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 kf = __bfloat1622float2(kb[e]);
+                    const float a0 = el * dk[q8 * 8 + 2 * e], a1 = el * dk[q8 * 8 + 2 * e + 1];
+                    xk += kf.x * a0 + kf.y * a1;
+                    v8[2 * e] = a0 + ki[q8 * 8 + 2 * e];
+                    v8[2 * e + 1] = a1 + ki[q8 * 8 + 2 * e + 1];
+                }
+                if (live) {
+                    kp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+                    kp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+                }
             }
         }
         if (active) {
@@ -209,7 +311,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             float dg = 0.f, xi = 0.f;
             if (tt < L) {
                 xi = (sm.pk[0][tt] + sm.pk[1][tt]) * sm.rki[tt];
-                dg = (sm.pq[0][tt] + sm.pq[1][tt]) * sm.qsc[tt] - xi;
+                const float cps = ((sm.cp[0][tt] + sm.cp[1][tt]) + sm.cp[2][tt]) + sm.cp[3][tt];
+                dg = (sm.pq[0][tt] + sm.pq[1][tt]) * sm.qsc[tt] - xi + (sm.rp[0][tt] + sm.rp[1][tt]) - cps;
             }
             sx += xi;
             dgz[z] = dg;

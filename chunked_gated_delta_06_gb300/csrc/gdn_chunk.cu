@@ -137,10 +137,9 @@ __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
     for (int j = 0; j < r; ++j) {
         const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + lane * 4;
         const float4 q1 = *reinterpret_cast<const float4 *>(a.dqp + o);
-        const float4 q2 = *reinterpret_cast<const float4 *>(a.dqp2 + o);
         const float4 k1 = *reinterpret_cast<const float4 *>(a.dkp + o);
         const float4 k2 = *reinterpret_cast<const float4 *>(a.dkp2 + o);
-        dq[0] += q1.x + q2.x; dq[1] += q1.y + q2.y; dq[2] += q1.z + q2.z; dq[3] += q1.w + q2.w;
+        dq[0] += q1.x; dq[1] += q1.y; dq[2] += q1.z; dq[3] += q1.w;
         dk[0] += k1.x + k2.x; dk[1] += k1.y + k2.y; dk[2] += k1.z + k2.z; dk[3] += k1.w + k2.w;
     }
     const size_t row = ((size_t)t * a.H + h) * kDim + lane * 4;

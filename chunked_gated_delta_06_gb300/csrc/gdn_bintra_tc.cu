@@ -3,7 +3,10 @@
 // through the intra-chunk attention matrix, on the tensor cores ("dqkwg" of
 // "cake_gdn: deterministic chunked GDN training kernels", section 2).
 //
-// One CTA of 256 threads per (chunk, value head).  With h_c, dh_c [k][v] (bf16,
+// Persistent: one CTA of 256 threads per SM walks a contiguous run of (chunk,
+// value head) units, and the next unit's h, dh', dO, dv_new and v_new tiles load
+// as soon as batch 1 has consumed the current ones (q and k only when the key
+// head changes), so the loads run under the epilogues.  With h_c, dh_c [k][v] (bf16,
 // from the forward and reverse scans), dO, dv_new, v_new [t][v], Qhat =
 // diag(scale / r_q) Q, Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
 //   batch 1 (M=64, rows = tokens, contraction 128):
@@ -60,7 +63,7 @@ struct BaSmem {
     float hdh[kThr / 32];
     float G[64], eg[64], egl_g[64];  // G, e^{G_t}, e^{G_L - G_t} (0 past L)
     float qsc[64], rki[64];       // scale / r_q, 1 / r_k
-    uint64_t tma_bar, mma_bar;
+    uint64_t a_bar, b_bar, mma_bar;   // group A (h, dh, dO, dv_new, v_new), group B (q, k)
     uint32_t tmem_base;
 };
 
@@ -68,16 +71,53 @@ struct BaMaps {
     CUtensorMap h, dh, dO, dvn, vn, q, k;
 };
 
+struct Unit {
+    int c, hv, h, t0, L;
+};
+
+__device__ __forceinline__ Unit unit_of(const ChunkArgs &a, int u) {
+    Unit x;
+    x.c = u / a.HV;
+    x.hv = u - x.c * a.HV;
+    x.h = x.hv / (a.HV / a.H);
+    x.t0 = a.chunk_start[x.c];
+    x.L = a.chunk_len[x.c];
+    return x;
+}
+
+__device__ __forceinline__ void issue_a(const BaMaps &m, BaSmem &sm, const ChunkArgs &a, const Unit &x) {
+    const int row = (x.c * a.HV + x.hv) * 128;
+    mbar_arrive_expect_tx(&sm.a_bar, 4 * kBig + 6 * kBox);
+    tma_load_3d(sm.h, &m.h, 0, 0, row, &sm.a_bar);
+    tma_load_3d(sm.h + kBig, &m.h, 64, 0, row, &sm.a_bar);
+    tma_load_3d(sm.dh, &m.dh, 0, 0, row, &sm.a_bar);
+    tma_load_3d(sm.dh + kBig, &m.dh, 64, 0, row, &sm.a_bar);
+    tma_load_3d(sm.dO, &m.dO, 0, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.dO + kBox, &m.dO, 64, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.dvn, &m.dvn, 0, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.dvn + kBox, &m.dvn, 64, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.vn, &m.vn, 0, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.vn + kBox, &m.vn, 64, x.hv, x.t0, &sm.a_bar);
+}
+
+__device__ __forceinline__ void issue_b(const BaMaps &m, BaSmem &sm, const Unit &x) {
+    mbar_arrive_expect_tx(&sm.b_bar, 4 * kBox);
+    tma_load_3d(sm.q, &m.q, 0, x.h, x.t0, &sm.b_bar);
+    tma_load_3d(sm.q + kBox, &m.q, 64, x.h, x.t0, &sm.b_bar);
+    tma_load_3d(sm.k, &m.k, 0, x.h, x.t0, &sm.b_bar);
+    tma_load_3d(sm.k + kBox, &m.k, 64, x.h, x.t0, &sm.b_bar);
+}
+
+
 __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
-                                                         const __grid_constant__ BaMaps maps) {
+                                                         const __grid_constant__ BaMaps maps, int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BaSmem &sm = *reinterpret_cast<BaSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hv = blockIdx.y;
-    const int h = hv / (a.HV / a.H);
-    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-    if (L <= 0) return;
+    const int nunits = a.num_chunks * a.HV;
+    const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
+    if (ub >= ue) return;
     const bool active = lane < 16;
     const int grp = warp >> 2;
     const int sub = warp & 3;
@@ -88,247 +128,284 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&sm.tma_bar, 1);
+        mbar_init(&sm.a_bar, 1);
+        mbar_init(&sm.b_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {
-        const int row = (c * a.HV + hv) * 128;
-        mbar_arrive_expect_tx(&sm.tma_bar, 4 * kBig + 10 * kBox);
-        tma_load_3d(sm.h, &maps.h, 0, 0, row, &sm.tma_bar);
-        tma_load_3d(sm.h + kBig, &maps.h, 64, 0, row, &sm.tma_bar);
-        tma_load_3d(sm.dh, &maps.dh, 0, 0, row, &sm.tma_bar);
-        tma_load_3d(sm.dh + kBig, &maps.dh, 64, 0, row, &sm.tma_bar);
-        tma_load_3d(sm.dO, &maps.dO, 0, hv, t0, &sm.tma_bar);
-        tma_load_3d(sm.dO + kBox, &maps.dO, 64, hv, t0, &sm.tma_bar);
-        tma_load_3d(sm.dvn, &maps.dvn, 0, hv, t0, &sm.tma_bar);
-        tma_load_3d(sm.dvn + kBox, &maps.dvn, 64, hv, t0, &sm.tma_bar);
-        tma_load_3d(sm.vn, &maps.vn, 0, hv, t0, &sm.tma_bar);
-        tma_load_3d(sm.vn + kBox, &maps.vn, 64, hv, t0, &sm.tma_bar);
-        tma_load_3d(sm.q, &maps.q, 0, h, t0, &sm.tma_bar);
-        tma_load_3d(sm.q + kBox, &maps.q, 64, h, t0, &sm.tma_bar);
-        tma_load_3d(sm.k, &maps.k, 0, h, t0, &sm.tma_bar);
-        tma_load_3d(sm.k + kBox, &maps.k, 64, h, t0, &sm.tma_bar);
-    }
-    const float Gl = a.G[(size_t)(t0 + L - 1) * a.HV + hv];
-    if (tid < 64) {
-        const bool in = tid < L;
-        const size_t r = (size_t)(t0 + tid) * a.H + h;
-        const float Gt = in ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
-        sm.G[tid] = Gt;
-        sm.eg[tid] = in ? __expf(Gt) : 0.f;
-        sm.egl_g[tid] = in ? __expf(fminf(Gl - Gt, 0.f)) : 0.f;
-        sm.qsc[tid] = in ? a.scale / a.rq[r] : 0.f;
-        sm.rki[tid] = in ? 1.f / a.rk[r] : 0.f;
-    }
-    const bool got = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(sub * 32) << 16);
+    Unit x = unit_of(a, ub);
+    if (tid == 0) {
+        issue_a(maps, sm, a, x);
+        issue_b(maps, sm, x);
+    }
+    int a_issued = 1, a_waited = 0, b_issued = 1, b_waited = 0;  // same on every thread
+    bool need_b = true;  // the current unit waits for a q / k load
+    // per-token scalars, fetched one unit ahead (threads 0..63)
+    float pG = 0.f, pRq = 1.f, pRk = 1.f;
+    auto fetch = [&](const Unit &y) {
+        if (tid < y.L && tid < 64) {
+            const size_t r = (size_t)(y.t0 + tid) * a.H + y.h;
+            pG = a.G[(size_t)(y.t0 + tid) * a.HV + y.hv];
+            pRq = a.rq[r];
+            pRk = a.rk[r];
+        } else {
+            pG = 0.f; pRq = 1.f; pRk = 1.f;
+        }
+    };
+    fetch(x);
+    bool ok = true;
     uint32_t phase = 0;
-    if (tid == 0 && got) {  // batch 1
-        tc_fence_after();
-        const uint32_t id128 = idesc_bf16(64, 128, 0, 0), id64 = idesc_bf16(64, 64, 0, 0);
-        const uint32_t hs = smem_u32(sm.h), dhs = smem_u32(sm.dh);
-        const uint32_t os = smem_u32(sm.dO), ds = smem_u32(sm.dvn), vs = smem_u32(sm.vn);
-        const uint32_t qs = smem_u32(sm.q), ks = smem_u32(sm.k);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint32_t ao = (s >> 2) * kBox + (s & 3) * 32, bo = (s >> 2) * kBig + (s & 3) * 32;
-            mma_bf16(tb + cDQ, sdesc(os + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
-            mma_bf16(tb + cDW, sdesc(ds + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
-            mma_bf16(tb + cDK, sdesc(vs + ao, 16, 1024), sdesc(dhs + bo, 16, 1024), id128, s > 0);
-            mma_bf16(tb + cQK, sdesc(qs + ao, 16, 1024), sdesc(ks + ao, 16, 1024), id64, s > 0);
-            mma_bf16(tb + cDM, sdesc(os + ao, 16, 1024), sdesc(vs + ao, 16, 1024), id64, s > 0);
+    for (int u = ub; u < ue; ++u) {
+        const bool has_next = u + 1 < ue;
+        const Unit nx = has_next ? unit_of(a, u + 1) : x;
+        const int L = x.L;
+        if (tid < 64) {
+            const bool in = tid < L;
+            sm.G[tid] = pG;
+            sm.qsc[tid] = in ? a.scale / pRq : 0.f;
+            sm.rki[tid] = in ? 1.f / pRk : 0.f;
         }
-        mma_commit(&sm.mma_bar);
-    }
-    // <h, dh'> while the products run: thread tid takes half a row of h and dh'
-    float hdh = 0.f;
-    if (got) {
-        const int kr = tid >> 1, half = tid & 1;
-        const unsigned char *hr = sm.h + half * kBig, *dr = sm.dh + half * kBig;
+        if (has_next) fetch(nx);
+        bool got = mbar_wait(&sm.a_bar, a_waited & 1);
+        if (need_b) got = mbar_wait(&sm.b_bar, b_waited & 1) && got;
+        got = __syncthreads_and(got);
+        ++a_waited;
+        if (need_b) ++b_waited;
+        if (!got) { ok = false; break; }
+        const float Gl = L > 0 ? sm.G[L - 1] : 0.f;
+        if (tid < 64) {
+            const bool in = tid < L;
+            const float Gt = sm.G[tid];
+            sm.eg[tid] = in ? __expf(Gt) : 0.f;
+            sm.egl_g[tid] = in ? __expf(fminf(Gl - Gt, 0.f)) : 0.f;
+        }
+        if (tid == 0) {  // batch 1
+            tc_fence_after();
+            const uint32_t id128 = idesc_bf16(64, 128, 0, 0), id64 = idesc_bf16(64, 64, 0, 0);
+            const uint32_t hs = smem_u32(sm.h), dhs = smem_u32(sm.dh);
+            const uint32_t os = smem_u32(sm.dO), ds = smem_u32(sm.dvn), vs = smem_u32(sm.vn);
+            const uint32_t qs = smem_u32(sm.q), ks = smem_u32(sm.k);
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-            const uint32_t off = sw128_off(kr, q8 * 8);
-            const uint4 x = *reinterpret_cast<const uint4 *>(hr + off);
-            const uint4 y = *reinterpret_cast<const uint4 *>(dr + off);
-            const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&x);
-            const __nv_bfloat162 *yb = reinterpret_cast<const __nv_bfloat162 *>(&y);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 xf = __bfloat1622float2(xb[e]), yf = __bfloat1622float2(yb[e]);
-                hdh += xf.x * yf.x + xf.y * yf.y;
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t ao = (s >> 2) * kBox + (s & 3) * 32, bo = (s >> 2) * kBig + (s & 3) * 32;
+                mma_bf16(tb + cDQ, sdesc(os + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
+                mma_bf16(tb + cDW, sdesc(ds + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
+                mma_bf16(tb + cDK, sdesc(vs + ao, 16, 1024), sdesc(dhs + bo, 16, 1024), id128, s > 0);
+                mma_bf16(tb + cQK, sdesc(qs + ao, 16, 1024), sdesc(ks + ao, 16, 1024), id64, s > 0);
+                mma_bf16(tb + cDM, sdesc(os + ao, 16, 1024), sdesc(vs + ao, 16, 1024), id64, s > 0);
             }
+            mma_commit(&sm.mma_bar);
         }
-    }
-    hdh = warp_sum(hdh);
-    if (lane == 0) sm.hdh[warp] = hdh;
-    bool done = __syncthreads_and(got && mbar_wait(&sm.mma_bar, phase));
-    phase ^= 1;
-    tc_fence_after();
-    const bool live = active && t < L;
-    if (done) {
-        // (a) QK, dM -> P1 (row and column sums) and the two dMG operand rows
-        const int j0 = 32 * grp;
-        float qk[32], dm[32];
-        tmem_ld32(t_row + cQK + j0, qk);
-        tmem_ld32(t_row + cDM + j0, dm);
-        tmem_ld_wait();
-        const float Gi = active ? sm.G[t] : 0.f;
-        const float qsi = active ? sm.qsc[t] : 0.f;
-        float rsum = 0.f;
+        // <h, dh'> while the products run: thread tid takes half a row of h and dh'
+        float hdh = 0.f;
+        {
+            const int kr = tid >> 1, half = tid & 1;
+            const unsigned char *hr = sm.h + half * kBig, *dr = sm.dh + half * kBig;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {  // in place: dm <- dMG, qk <- P1
-            const int j = j0 + jj;
-            const float msk = (live && j <= t) ? 1.f : 0.f;
-            dm[jj] *= msk * __expf(fminf(Gi - sm.G[j], 0.f));
-            qk[jj] = dm[jj] * qk[jj] * qsi * sm.rki[j];
-            rsum += qk[jj];
-        }
-        float s0, s1;
-        colsum16(qk, lane, s0, s1);
-        if (active) {
-            sm.cp[sub][j0 + 2 * lane] = s0;
-            sm.cp[sub][j0 + 2 * lane + 1] = s1;
-            sm.rp[grp][t] = rsum;
-        }
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * sm.rki[j0 + jj];
-        if (active) put_row32(sm.op_dmg, t, j0, qk);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * qsi;
-        if (active) put_row32(sm.op_dmgt, t, j0, qk);
-        // (b) dW = -Dw rows, this warpgroup's 64 columns
-        const size_t o = ((size_t)(t0 + (live ? t : 0)) * a.HV + hv) * kDim;
-#pragma unroll
-        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
-            float dw[32];
-            tmem_ld32(t_row + cDW + cc * 32, dw);
-            tmem_ld_wait();
-            if (live) {
-                uint4 *wp = reinterpret_cast<uint4 *>(a.dW + o + cc * 32);
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8)
-                    wp[q8] = make_uint4(pack_bf2(-dw[q8 * 8], -dw[q8 * 8 + 1]), pack_bf2(-dw[q8 * 8 + 2], -dw[q8 * 8 + 3]),
-                                        pack_bf2(-dw[q8 * 8 + 4], -dw[q8 * 8 + 5]), pack_bf2(-dw[q8 * 8 + 6], -dw[q8 * 8 + 7]));
-            }
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && done) {  // batch 2: dMG Khat -> cQI, dMG^T Qhat -> cKI (over the Dw columns)
-        tc_fence_after();
-        const uint32_t id_km = idesc_bf16(64, 128, 0, 1);  // A K-major, B MN-major
-        const uint32_t id_mm = idesc_bf16(64, 128, 1, 1);  // A MN-major, B MN-major
-        const uint32_t ks = smem_u32(sm.k), qs = smem_u32(sm.q);
-        const uint32_t g1 = smem_u32(sm.op_dmg), g2 = smem_u32(sm.op_dmgt);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            mma_bf16(tb + cQI, sdesc(g1 + s * 32, 16, 1024), sdesc(ks + s * 2048, kBox, 1024), id_km, s > 0);
-            mma_bf16(tb + cKI, sdesc(g2 + s * 2048, kBox, 1024), sdesc(qs + s * 2048, kBox, 1024), id_mm, s > 0);
-        }
-        mma_commit(&sm.mma_bar);
-    }
-    done = __syncthreads_and(done && mbar_wait(&sm.mma_bar, phase));
-    tc_fence_after();
-    if (done) {  // dqhat, dkhat rows (this warpgroup's 64 columns) and the inter-term row dots
-        const float eg = live ? sm.eg[t] : 0.f, el = live ? sm.egl_g[t] : 0.f;
-        const size_t o = ((size_t)(t0 + (live ? t : 0)) * a.HV + hv) * kDim;
-        float xq = 0.f, xk = 0.f;
-#pragma unroll
-        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
-            float dq[32], qi[32];
-            tmem_ld32(t_row + cDQ + cc * 32, dq);
-            tmem_ld32(t_row + cQI + cc * 32, qi);
-            tmem_ld_wait();
-            const unsigned char *qrow = sm.q + (cc >> 1) * kBox;
-            float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per step
-                const int col = (cc & 1) * 32 + q8 * 8;
-                const uint4 qx = *reinterpret_cast<const uint4 *>(qrow + sw128_off(t, col));
-                const __nv_bfloat162 *qb = reinterpret_cast<const __nv_bfloat162 *>(&qx);
-                float v8[8];
+            for (int q8 = 0; q8 < 8; ++q8) {
+                const uint32_t off = sw128_off(kr, q8 * 8);
+                const uint4 xx = *reinterpret_cast<const uint4 *>(hr + off);
+                const uint4 yy = *reinterpret_cast<const uint4 *>(dr + off);
+                const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xx);
+                const __nv_bfloat162 *yb = reinterpret_cast<const __nv_bfloat162 *>(&yy);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 qf = __bfloat1622float2(qb[e]);
-                    const float a0 = eg * dq[q8 * 8 + 2 * e], a1 = eg * dq[q8 * 8 + 2 * e + 1];
-                    xq += qf.x * a0 + qf.y * a1;
-                    v8[2 * e] = a0 + qi[q8 * 8 + 2 * e];
-                    v8[2 * e + 1] = a1 + qi[q8 * 8 + 2 * e + 1];
-                }
-                if (live) {
-                    qp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
-                    qp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+                    const float2 xf = __bfloat1622float2(xb[e]), yf = __bfloat1622float2(yb[e]);
+                    hdh += xf.x * yf.x + xf.y * yf.y;
                 }
             }
         }
-#pragma unroll
-        for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
-            float dk[32], ki[32];
-            tmem_ld32(t_row + cDK + cc * 32, dk);
-            tmem_ld32(t_row + cKI + cc * 32, ki);
+        hdh = warp_sum(hdh);
+        if (lane == 0) sm.hdh[warp] = hdh;
+        bool done = __syncthreads_and(mbar_wait(&sm.mma_bar, phase));
+        phase ^= 1;
+        tc_fence_after();
+        if (!done) { ok = false; break; }
+        // group A has been consumed (batch 1 and the dot): load the next unit's
+        if (has_next) {
+            if (tid == 0) issue_a(maps, sm, a, nx);
+            ++a_issued;
+        }
+        const bool live = active && t < L;
+        {
+            // (a) QK, dM -> P1 (row and column sums) and the two dMG operand rows
+            const int j0 = 32 * grp;
+            float qk[32], dm[32];
+            tmem_ld32(t_row + cQK + j0, qk);
+            tmem_ld32(t_row + cDM + j0, dm);
             tmem_ld_wait();
-            const unsigned char *krow = sm.k + (cc >> 1) * kBox;
-            float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
+            const float Gi = active ? sm.G[t] : 0.f;
+            const float qsi = active ? sm.qsc[t] : 0.f;
+            float rsum = 0.f;
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                const int col = (cc & 1) * 32 + q8 * 8;
-                const uint4 kx = *reinterpret_cast<const uint4 *>(krow + sw128_off(t, col));
-                const __nv_bfloat162 *kb = reinterpret_cast<const __nv_bfloat162 *>(&kx);
-                float v8[8];
+            for (int jj = 0; jj < 32; ++jj) {  // in place: dm <- dMG, qk <- P1
+                const int j = j0 + jj;
+                const float msk = (live && j <= t) ? 1.f : 0.f;
+                dm[jj] *= msk * __expf(fminf(Gi - sm.G[j], 0.f));
+                qk[jj] = dm[jj] * qk[jj] * qsi * sm.rki[j];
+                rsum += qk[jj];
+            }
+            float s0, s1;
+            colsum16(qk, lane, s0, s1);
+            if (active) {
+                sm.cp[sub][j0 + 2 * lane] = s0;
+                sm.cp[sub][j0 + 2 * lane + 1] = s1;
+                sm.rp[grp][t] = rsum;
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 kf = __bfloat1622float2(kb[e]);
-                    const float a0 = el * dk[q8 * 8 + 2 * e], a1 = el * dk[q8 * 8 + 2 * e + 1];
-                    xk += kf.x * a0 + kf.y * a1;
-                    v8[2 * e] = a0 + ki[q8 * 8 + 2 * e];
-                    v8[2 * e + 1] = a1 + ki[q8 * 8 + 2 * e + 1];
-                }
+            for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * sm.rki[j0 + jj];
+            if (active) put_row32(sm.op_dmg, t, j0, qk);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * qsi;
+            if (active) put_row32(sm.op_dmgt, t, j0, qk);
+            // (b) dW = -Dw rows, this warpgroup's 64 columns
+            const size_t o = ((size_t)(x.t0 + (live ? t : 0)) * a.HV + x.hv) * kDim;
+#pragma unroll
+            for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
+                float dw[32];
+                tmem_ld32(t_row + cDW + cc * 32, dw);
+                tmem_ld_wait();
                 if (live) {
-                    kp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
-                    kp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+                    uint4 *wp = reinterpret_cast<uint4 *>(a.dW + o + cc * 32);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        wp[q8] = make_uint4(pack_bf2(-dw[q8 * 8], -dw[q8 * 8 + 1]), pack_bf2(-dw[q8 * 8 + 2], -dw[q8 * 8 + 3]),
+                                            pack_bf2(-dw[q8 * 8 + 4], -dw[q8 * 8 + 5]), pack_bf2(-dw[q8 * 8 + 6], -dw[q8 * 8 + 7]));
                 }
             }
         }
-        if (active) {
-            sm.pq[grp][t] = xq;
-            sm.pk[grp][t] = xk;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {  // batch 2: dMG Khat -> cQI, dMG^T Qhat -> cKI (over the Dw columns)
+            tc_fence_after();
+            const uint32_t id_km = idesc_bf16(64, 128, 0, 1);  // A K-major, B MN-major
+            const uint32_t id_mm = idesc_bf16(64, 128, 1, 1);  // A MN-major, B MN-major
+            const uint32_t ks = smem_u32(sm.k), qs = smem_u32(sm.q);
+            const uint32_t g1 = smem_u32(sm.op_dmg), g2 = smem_u32(sm.op_dmgt);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                mma_bf16(tb + cQI, sdesc(g1 + s * 32, 16, 1024), sdesc(ks + s * 2048, kBox, 1024), id_km, s > 0);
+                mma_bf16(tb + cKI, sdesc(g2 + s * 2048, kBox, 1024), sdesc(qs + s * 2048, kBox, 1024), id_mm, s > 0);
+            }
+            mma_commit(&sm.mma_bar);
         }
-    } else if (tid == 0 && a.status) {
-        atomicOr(a.status, 2);
+        done = __syncthreads_and(mbar_wait(&sm.mma_bar, phase));
+        phase ^= 1;
+        tc_fence_after();
+        if (!done) { ok = false; break; }
+        {  // dqhat, dkhat rows (this warpgroup's 64 columns) and the inter-term row dots
+            const float eg = live ? sm.eg[t] : 0.f, el = live ? sm.egl_g[t] : 0.f;
+            const size_t o = ((size_t)(x.t0 + (live ? t : 0)) * a.HV + x.hv) * kDim;
+            float xq = 0.f, xk = 0.f;
+#pragma unroll
+            for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
+                float dq[32], qi[32];
+                tmem_ld32(t_row + cDQ + cc * 32, dq);
+                tmem_ld32(t_row + cQI + cc * 32, qi);
+                tmem_ld_wait();
+                const unsigned char *qrow = sm.q + (cc >> 1) * kBox;
+                float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per step
+                    const int col = (cc & 1) * 32 + q8 * 8;
+                    const uint4 qx = *reinterpret_cast<const uint4 *>(qrow + sw128_off(t, col));
+                    const __nv_bfloat162 *qb = reinterpret_cast<const __nv_bfloat162 *>(&qx);
+                    float v8[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 qf = __bfloat1622float2(qb[e]);
+                        const float a0 = eg * dq[q8 * 8 + 2 * e], a1 = eg * dq[q8 * 8 + 2 * e + 1];
+                        xq += qf.x * a0 + qf.y * a1;
+                        v8[2 * e] = a0 + qi[q8 * 8 + 2 * e];
+                        v8[2 * e + 1] = a1 + qi[q8 * 8 + 2 * e + 1];
+                    }
+                    if (live) {
+                        qp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+                        qp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
+                float dk[32], ki[32];
+                tmem_ld32(t_row + cDK + cc * 32, dk);
+                tmem_ld32(t_row + cKI + cc * 32, ki);
+                tmem_ld_wait();
+                const unsigned char *krow = sm.k + (cc >> 1) * kBox;
+                float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const int col = (cc & 1) * 32 + q8 * 8;
+                    const uint4 kx = *reinterpret_cast<const uint4 *>(krow + sw128_off(t, col));
+                    const __nv_bfloat162 *kb = reinterpret_cast<const __nv_bfloat162 *>(&kx);
+                    float v8[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 kf = __bfloat1622float2(kb[e]);
+                        const float a0 = el * dk[q8 * 8 + 2 * e], a1 = el * dk[q8 * 8 + 2 * e + 1];
+                        xk += kf.x * a0 + kf.y * a1;
+                        v8[2 * e] = a0 + ki[q8 * 8 + 2 * e];
+                        v8[2 * e + 1] = a1 + ki[q8 * 8 + 2 * e + 1];
+                    }
+                    if (live) {
+                        kp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
+                        kp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
+                    }
+                }
+            }
+            if (active) {
+                sm.pq[grp][t] = xq;
+                sm.pk[grp][t] = xk;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // q / k tiles, TMEM and the row sums are all read or written
+        need_b = has_next && (nx.c != x.c || nx.h != x.h);
+        if (need_b) {
+            if (tid == 0) issue_b(maps, sm, nx);
+            ++b_issued;
+        }
+        if (warp == 0) {  // dG_t, and the G_L terms summed in a fixed order
+            float dgz[2], sx = 0.f;
+#pragma unroll
+            for (int z = 0; z < 2; ++z) {
+                const int tt = 2 * lane + z;
+                float dg = 0.f, xi = 0.f;
+                if (tt < L) {
+                    xi = (sm.pk[0][tt] + sm.pk[1][tt]) * sm.rki[tt];
+                    const float cps = ((sm.cp[0][tt] + sm.cp[1][tt]) + sm.cp[2][tt]) + sm.cp[3][tt];
+                    dg = (sm.pq[0][tt] + sm.pq[1][tt]) * sm.qsc[tt] - xi + (sm.rp[0][tt] + sm.rp[1][tt]) - cps;
+                }
+                sx += xi;
+                dgz[z] = dg;
+            }
+            sx = warp_sum(sx);
+            float hd = 0.f;
+#pragma unroll
+            for (int w = 0; w < kThr / 32; ++w) hd += sm.hdh[w];
+#pragma unroll
+            for (int z = 0; z < 2; ++z) {
+                const int tt = 2 * lane + z;
+                if (tt < L) {
+                    const float extra = (tt == L - 1) ? sx + __expf(Gl) * hd : 0.f;
+                    a.dGp[(size_t)(x.t0 + tt) * a.HV + x.hv] = dgz[z] + extra;
+                }
+            }
+        }
+        __syncthreads();  // the per-unit scalars are free for the next unit
+        x = nx;
     }
-    __syncthreads();
-    if (done && warp == 0) {  // dG_t, and the G_L terms summed in a fixed order
-        float dgz[2], sx = 0.f;
-#pragma unroll
-        for (int z = 0; z < 2; ++z) {
-            const int tt = 2 * lane + z;
-            float dg = 0.f, xi = 0.f;
-            if (tt < L) {
-                xi = (sm.pk[0][tt] + sm.pk[1][tt]) * sm.rki[tt];
-                const float cps = ((sm.cp[0][tt] + sm.cp[1][tt]) + sm.cp[2][tt]) + sm.cp[3][tt];
-                dg = (sm.pq[0][tt] + sm.pq[1][tt]) * sm.qsc[tt] - xi + (sm.rp[0][tt] + sm.rp[1][tt]) - cps;
-            }
-            sx += xi;
-            dgz[z] = dg;
-        }
-        sx = warp_sum(sx);
-        float hd = 0.f;
-#pragma unroll
-        for (int w = 0; w < kThr / 32; ++w) hd += sm.hdh[w];
-#pragma unroll
-        for (int z = 0; z < 2; ++z) {
-            const int tt = 2 * lane + z;
-            if (tt < L) {
-                const float extra = (tt == L - 1) ? sx + __expf(Gl) * hd : 0.f;
-                a.dGp[(size_t)(t0 + tt) * a.HV + hv] = dgz[z] + extra;
-            }
-        }
+    if (!ok && tid == 0) {
+        if (a.status) atomicOr(a.status, 2);
+        // drain the loads still in flight (bounded) before leaving
+        if (a_issued > a_waited) mbar_wait(&sm.a_bar, a_waited & 1, 1u << 20);
+        if (b_issued > b_waited) mbar_wait(&sm.b_bar, b_waited & 1, 1u << 20);
     }
     tc_fence_before();
     __syncthreads();
@@ -357,8 +434,14 @@ cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_bintra_a_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int nunits = a.num_chunks * a.HV;
+    const int grid = nunits < sms ? nunits : sms;
+    const int per = (nunits + grid - 1) / grid;
     TimerScope ts(a.timer, GDN_KERNEL_BINTRA_A, s);
-    k_bintra_a_tc<<<dim3(a.num_chunks, a.HV), kThr, smem, s>>>(a, m);
+    k_bintra_a_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
     return cudaGetLastError();
 }
 

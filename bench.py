@@ -59,8 +59,8 @@ def kernel_work(name, T, H, HV, N, C_total):
         out=(2 * C * D / r + 2 * C * D + 2 * D * D) * TV,
         dvloc=(2 * C * D / r + 2 * C * D) * TV,
         bstate=6 * D * D * TV,
-        bintra_a=6 * D * D * TV,
-        bintra_b=(6 * C * D + 12 * C * D + 4 * C * C + 2 * C * D / r) * TV,
+        bintra_a=(6 * D * D + 8 * C * D) * TV,
+        bintra_b=(14 * C * D + 4 * C * C) * TV,
     ).get(name, 0.0)
     bf = 2
     b = dict(
@@ -69,11 +69,11 @@ def kernel_work(name, T, H, HV, N, C_total):
         intra=T * H * D * bf + TV * D * bf + TV * 6 + TV * D * bf * 2 + C_total * HV * C * C * 4,
         state=TV * D * bf * 3 + T * H * D * bf + C_total * HV * D * D * bf + N * HV * D * D * 8,
         out=T * H * D * bf * 2 + TV * D * bf * 2 + C_total * HV * D * D * bf,
-        dvloc=T * H * D * bf * 2 + TV * D * (bf + 4),
-        bstate=T * H * D * bf * 2 + TV * D * (bf * 2 + 4 * 2) + C_total * HV * D * D * bf,
-        bintra_a=TV * D * (bf * 2 + 4 * 4) + C_total * HV * D * D * bf * 2,
-        bintra_b=T * H * D * bf * 2 + TV * D * (bf * 3 + 4 * 4) + C_total * HV * C * C * 4,
-        bnorm=TV * D * 4 * 2 + T * H * D * bf * 4,
+        dvloc=T * H * D * bf * 2 + TV * D * bf * 2,
+        bstate=T * H * D * bf * 2 + TV * D * bf * 4 + C_total * HV * D * D * bf,
+        bintra_a=T * H * D * bf * 2 + TV * D * (bf * 4 + 4 * 2) + TV * 4 + C_total * HV * D * D * bf * 2,
+        bintra_b=T * H * D * bf + TV * D * (bf * 4 + 4) + TV * 12 + C_total * HV * C * C * 4,
+        bnorm=TV * D * 4 * 3 + T * H * D * bf * 4,
     ).get(name, 0.0)
     return f, b
 

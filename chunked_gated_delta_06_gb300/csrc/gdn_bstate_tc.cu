@@ -3,9 +3,9 @@
 // section 2; the reverse recurrence of the GDN context-parallel dh scan in
 // "Qwen3.5-397B RL trainer on 128 v7x", maxtext #5799).
 //
-// As in the forward scan, the value columns never mix, so one CTA of 128
-// threads owns one (sequence, value head, value half) and walks the chunks in
-// reverse.  dh[k][v'] (v' = 64 vb .. 64 vb + 63) lives in TMEM as fp32 (lane
+// As in the forward scan, the value columns never mix, so one CTA (two
+// warpgroups that split the columns of every pass) owns one (sequence, value
+// head, value half) and walks the chunks in reverse.  dh[k][v'] (v' = 64 vb .. 64 vb + 63) lives in TMEM as fp32 (lane
 // k, 64 columns), seeded with d(final state).  Per chunk, with dh' the gradient
 // of the state after the chunk (= the current dh):
 //   1. thread k writes row k of dh' as bf16 to shared memory (copied to
@@ -17,10 +17,13 @@
 //   4. dh += Q^T (c dO) - w^T dv_new                  (two M=128 N=64 K=64
 //      products; Q and w are raw tiles read MN-major)
 // which is dh <- e^{G_L} dh' + Qtil^T dO - w^T dv_new and dv_new = dv_loc +
-// Ktil dh'.  dh0 = dh at the sequence start.  The tiles come in two single-
-// buffered groups so that two CTAs share an SM: X (K, this half of dO and of
-// dv_loc) is reloaded for the next chunk as soon as step 3 has read it, Y (Q, w)
-// as soon as step 4 has finished.  Waits are bounded.
+// Ktil dh'.  dh0 = dh at the sequence start.  The tiles are single-buffered so
+// that two CTAs share an SM, and each group is reloaded for the next chunk as
+// soon as it is free: K after step 2, the halves of dO and dv_loc after step 3,
+// Q and w after step 4; every tile of the chunk after that is prefetched into L2
+// a step ahead.  The next chunk's per-token scalars are loaded a step ahead and
+// published during the current epilogue; a chunk costs two block barriers.
+// Waits are bounded.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -32,7 +35,7 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThr = 128;
+constexpr int kThr = 256;
 constexpr uint32_t kBox = 64 * 128;       // one 64-row x 128-byte SW128 box
 constexpr uint32_t kXBytes = 4 * kBox;    // K (2 boxes), dO half, dv_loc half
 constexpr uint32_t kYBytes = 4 * kBox;    // Q (2 boxes), w (2 boxes)
@@ -43,25 +46,38 @@ struct BStateSmem {
     unsigned char a_dv[64 * 128];       // -dv_new bf16 [t][v']
     unsigned char x[kXBytes];
     unsigned char y[kYBytes];
-    float kc[64];                       // e^{G_L - G_t} / r_k,t (0 past L)
-    float qc[64];                       // e^{G_t} scale / r_q,t (0 past L)
-    float gt[64], rkt[64], rqt[64];     // this chunk's G, r_k, r_q (prefetched)
-    uint64_t x_bar, y_bar, mma_bar;
+    float kc[2][64];                    // e^{G_L - G_t} / r_k,t (0 past L), this and the next chunk
+    float qc[2][64];                    // e^{G_t} scale / r_q,t (0 past L)
+    uint64_t xk_bar, xd_bar, y_bar, mma_bar;   // X = K (xk) + dO, dv_loc halves (xd); Y = Q, w
     uint32_t tmem_base;
-    int error;
 };
 
 struct BStateMaps {
     CUtensorMap k, q, w, dO, dl, dhc;
 };
 
-__device__ __forceinline__ void issue_x(const BStateMaps &m, BStateSmem &sm, int t0, int h, int hv,
-                                        int vb) {
-    mbar_arrive_expect_tx(&sm.x_bar, kXBytes);
-    tma_load_3d(sm.x + 0 * kBox, &m.k, 0, h, t0, &sm.x_bar);
-    tma_load_3d(sm.x + 1 * kBox, &m.k, 64, h, t0, &sm.x_bar);
-    tma_load_3d(sm.x + 2 * kBox, &m.dO, 64 * vb, hv, t0, &sm.x_bar);
-    tma_load_3d(sm.x + 3 * kBox, &m.dl, 64 * vb, hv, t0, &sm.x_bar);
+__device__ __forceinline__ void issue_xk(const BStateMaps &m, BStateSmem &sm, int t0, int h) {
+    mbar_arrive_expect_tx(&sm.xk_bar, 2 * kBox);
+    tma_load_3d(sm.x + 0 * kBox, &m.k, 0, h, t0, &sm.xk_bar);
+    tma_load_3d(sm.x + 1 * kBox, &m.k, 64, h, t0, &sm.xk_bar);
+}
+
+__device__ __forceinline__ void issue_xd(const BStateMaps &m, BStateSmem &sm, int t0, int hv, int vb) {
+    mbar_arrive_expect_tx(&sm.xd_bar, 2 * kBox);
+    tma_load_3d(sm.x + 2 * kBox, &m.dO, 64 * vb, hv, t0, &sm.xd_bar);
+    tma_load_3d(sm.x + 3 * kBox, &m.dl, 64 * vb, hv, t0, &sm.xd_bar);
+}
+
+// L2 prefetch of every tile of one chunk (loaded a step later)
+__device__ __forceinline__ void prefetch_chunk(const BStateMaps &m, int t0, int h, int hv, int vb) {
+    tma_prefetch_3d(&m.k, 0, h, t0);
+    tma_prefetch_3d(&m.k, 64, h, t0);
+    tma_prefetch_3d(&m.dO, 64 * vb, hv, t0);
+    tma_prefetch_3d(&m.dl, 64 * vb, hv, t0);
+    tma_prefetch_3d(&m.q, 0, h, t0);
+    tma_prefetch_3d(&m.q, 64, h, t0);
+    tma_prefetch_3d(&m.w, 0, hv, t0);
+    tma_prefetch_3d(&m.w, 64, hv, t0);
 }
 
 __device__ __forceinline__ void issue_y(const BStateMaps &m, BStateSmem &sm, int t0, int h, int hv) {
@@ -89,38 +105,49 @@ __global__ void __launch_bounds__(kThr, 2)
     const int cb = a.seq_chunk_off[n];
     const int ce = min(a.seq_chunk_off[n + 1], a.num_chunks);
     const int nch = max(ce - cb, 0);
-    const int kr = tid;                 // the state row this thread owns (step 1)
-    const int tr = 16 * warp + lane;    // the token row it owns (lanes 0..15)
+    const int grp = warp >> 2, sub = warp & 3;
+    const int kr = sub * 32 + lane;     // state row (TMEM lane) of step 1
+    const int tr = sub * 16 + lane;     // token row of steps 2-3 (lanes 0..15)
     const bool trow = lane < 16;
+    const int c0 = 32 * grp;            // this warpgroup's 32 of the 64 columns
+    // the sequence's chunks are consecutive 64-token blocks of [ts0, ts1); the
+    // i-th step of the reverse walk handles block nch - 1 - i
+    const int ts0 = nch > 0 ? a.chunk_start[cb] : 0;
+    const int ts1 = nch > 0 ? a.chunk_start[ce - 1] + a.chunk_len[ce - 1] : 0;
+    auto step_t0 = [&](int i) { return ts0 + 64 * (nch - 1 - i); };
+    auto step_len = [&](int i) { return min(64, ts1 - step_t0(i)); };
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&sm.x_bar, 1);
+        mbar_init(&sm.xk_bar, 1);
+        mbar_init(&sm.xd_bar, 1);
         mbar_init(&sm.y_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
-        sm.error = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t t_row = sm.tmem_base + ((uint32_t)(warp * 32) << 16);
-    const uint32_t tS = t_row, tP = t_row + 64;
+    const uint32_t tbase = sm.tmem_base;
+    const uint32_t t_row = tbase + ((uint32_t)(sub * 32) << 16);
+    const uint32_t tS = t_row + c0, tP = t_row + 64 + c0;   // this warpgroup's columns
 
-    int x_issued = 0, y_issued = 0;  // loads issued (thread 0's count)
+    int xk_issued = 0, xd_issued = 0, y_issued = 0;  // thread 0's load counts
     if (tid == 0 && nch > 0) {
-        issue_x(maps, sm, a.chunk_start[ce - 1], h, hv, vb);
-        issue_y(maps, sm, a.chunk_start[ce - 1], h, hv);
-        x_issued = y_issued = 1;
+        issue_xk(maps, sm, step_t0(0), h);
+        issue_xd(maps, sm, step_t0(0), hv, vb);
+        issue_y(maps, sm, step_t0(0), h, hv);
+        if (nch > 1) prefetch_chunk(maps, step_t0(1), h, hv, vb);
+        xk_issued = xd_issued = y_issued = 1;
     }
-    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb;
-    for (int half = 0; half < 2; ++half) {
+    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb + c0;
+    {
         float r[32];
         if (a.d_ht) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.d_ht + sbase + 32 * half);
+            const float4 *src = reinterpret_cast<const float4 *>(a.d_ht + sbase);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 x = src[q];
@@ -130,101 +157,86 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0.f;
         }
-        tmem_st32(tS + 32 * half, r);
+        tmem_st32(tS, r);
+        tmem_st_wait();
     }
-    tmem_st_wait();
-
-    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // Pd = K dh'          (dh' MN-major)
-    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // dh += Q^T A + w^T B (all MN-major)
-    uint32_t mma_phase = 0;
-    bool ok = true;
-    // per-token scalars of the next chunk, loaded one chunk ahead
-    float pg = 0.f, prk = 1.f, prq = 1.f;
-    auto fetch = [&](int cc) {
-        const int tt0 = a.chunk_start[cc], LL = a.chunk_len[cc];
-        if (tid < LL) {
+    // per-chunk scalars: the raw values are loaded one step ahead (pgl: G_L; pg,
+    // prk, prq: G_t, r_k,t, r_q,t of thread t < 64) and turned into kc_t, qc_t and
+    // e^{G_L} only when they are published a step later, so no thread waits on the loads
+    float pgl = 0.f, pg = 0.f, prk = 1.f, prq = 1.f;
+    bool pin = false;
+    auto fetch = [&](int i) {
+        const int tt0 = step_t0(i), LL = step_len(i);
+        pgl = a.G[(size_t)(tt0 + LL - 1) * a.HV + hv];
+        pin = tid < LL;
+        if (pin) {
             const size_t t = (size_t)(tt0 + tid);
             pg = a.G[t * a.HV + hv];
             prk = a.rk[t * a.H + h];
             prq = a.rq[t * a.H + h];
-        } else {
-            pg = 0.f; prk = 1.f; prq = 1.f;
         }
     };
-    if (tid < 64 && nch > 0) fetch(ce - 1);
+    auto publish = [&](int buf) {  // returns e^{G_L}
+        if (tid < 64) {
+            sm.kc[buf][tid] = pin ? __expf(fminf(pgl - pg, 0.f)) / prk : 0.f;
+            sm.qc[buf][tid] = pin ? __expf(pg) * a.scale / prq : 0.f;
+        }
+        return __expf(pgl);
+    };
+    float egl = 1.f;
+    if (nch > 0) {
+        fetch(0);
+        egl = publish(0);
+        if (nch > 1) fetch(1);
+    }
+    __syncthreads();
+    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // Pd = K dh'          (dh' MN-major)
+    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // dh += Q^T A + w^T B (all MN-major)
+    uint32_t phase = 0;
+    bool ok = true;
     for (int i = 0; i < nch; ++i) {
         const int c = ce - 1 - i;
         const uint32_t par = i & 1;
-        const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-        if (tid < 64) {
-            sm.gt[tid] = pg;
-            sm.rkt[tid] = prk;
-            sm.rqt[tid] = prq;
-            if (i + 1 < nch) fetch(c - 1);
-        }
-        if (tid == 0) tma_store_wait_read();  // the previous chunk's dh_c store has read a_ds
-        __syncthreads();
-        const float Gl = L > 0 ? sm.gt[L - 1] : 0.f;
-        if (tid < 64) {
-            float kk = 0.f, qq = 0.f;
-            if (tid < L) {
-                const float Gt = sm.gt[tid];
-                kk = __expf(fminf(Gl - Gt, 0.f)) / sm.rkt[tid];
-                qq = __expf(Gt) * a.scale / sm.rqt[tid];
-            }
-            sm.kc[tid] = kk;
-            sm.qc[tid] = qq;
-        }
-        const float egl = __expf(Gl);
-        // 1. dh' -> bf16 operand row kr (copied to dh_c by TMA below), then dh <- e^{G_L} dh'
+        const int t0 = step_t0(i), L = step_len(i);
+        // 1. dh' -> bf16 operand (copied to dh_c by TMA below), then dh <- e^{G_L} dh'
         {
-            float r0[32], r1[32];
-            tmem_ld32(tS, r0);
-            tmem_ld32(tS + 32, r1);
+            float r[32];
+            tmem_ld32(tS, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                *reinterpret_cast<uint4 *>(sm.a_ds + sw128_off(kr, 8 * q)) =
-                    make_uint4(pack_bf2(r0[8 * q], r0[8 * q + 1]), pack_bf2(r0[8 * q + 2], r0[8 * q + 3]),
-                               pack_bf2(r0[8 * q + 4], r0[8 * q + 5]), pack_bf2(r0[8 * q + 6], r0[8 * q + 7]));
-                *reinterpret_cast<uint4 *>(sm.a_ds + sw128_off(kr, 32 + 8 * q)) =
-                    make_uint4(pack_bf2(r1[8 * q], r1[8 * q + 1]), pack_bf2(r1[8 * q + 2], r1[8 * q + 3]),
-                               pack_bf2(r1[8 * q + 4], r1[8 * q + 5]), pack_bf2(r1[8 * q + 6], r1[8 * q + 7]));
-            }
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(sm.a_ds + sw128_off(kr, c0 + 8 * q)) =
+                    make_uint4(pack_bf2(r[8 * q], r[8 * q + 1]), pack_bf2(r[8 * q + 2], r[8 * q + 3]),
+                               pack_bf2(r[8 * q + 4], r[8 * q + 5]), pack_bf2(r[8 * q + 6], r[8 * q + 7]));
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                r0[j] *= egl;
-                r1[j] *= egl;
-            }
-            tmem_st32(tS, r0);
-            tmem_st32(tS + 32, r1);
+            for (int j = 0; j < 32; ++j) r[j] *= egl;
+            tmem_st32(tS, r);
+            tmem_st_wait();
         }
-        tmem_st_wait();
-        if (!mbar_wait(&sm.x_bar, par)) sm.error = 1;
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (sm.error) { ok = false; break; }
+        const bool gx = mbar_wait(&sm.xk_bar, par) && mbar_wait(&sm.xd_bar, par);
+        ok = __syncthreads_and(ok && gx);
+        if (!ok) break;
         // 2. Pd = K dh'
         if (tid == 0) {
             tc_fence_after();
             const uint32_t as = smem_u32(sm.a_ds), ks = smem_u32(sm.x);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_bf16(tP, sdesc(ks + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
+                mma_bf16(tbase + 64, sdesc(ks + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
                          sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
             mma_commit(&sm.mma_bar);
-            const int hrow = (c * a.HV + hv) * 128;  // dh_c rows (k) of this chunk
-            tma_store_3d(&maps.dhc, 64 * vb, 0, hrow, sm.a_ds);
+            tma_store_3d(&maps.dhc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_ds);  // dh_c rows (k)
             tma_store_commit();
         }
-        // meanwhile: row tr of c_t dO
+        // meanwhile: row tr of c_t dO (this warpgroup's 32 columns)
         if (trow) {
-            const float qc = sm.qc[tr];
+            const float qc = sm.qc[i & 1][tr];
             const unsigned char *dos = sm.x + 2 * kBox;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 dx = *reinterpret_cast<const uint4 *>(dos + sw128_off(tr, 8 * q));
+            for (int q = 0; q < 4; ++q) {
+                const uint4 dx = *reinterpret_cast<const uint4 *>(dos + sw128_off(tr, c0 + 8 * q));
                 const __nv_bfloat162 *db = reinterpret_cast<const __nv_bfloat162 *>(&dx);
                 uint32_t pk[4];
 #pragma unroll
@@ -232,99 +244,105 @@ __global__ void __launch_bounds__(kThr, 2)
                     const float2 f = __bfloat1622float2(db[e]);
                     pk[e] = pack_bf2(f.x * qc, f.y * qc);
                 }
-                *reinterpret_cast<uint4 *>(sm.a_do + sw128_off(tr, 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(sm.a_do + sw128_off(tr, c0 + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
-        if (!mbar_wait(&sm.mma_bar, mma_phase)) sm.error = 1;
-        mma_phase ^= 1;
+        ok = mbar_wait(&sm.mma_bar, phase) && ok;
+        phase ^= 1;
         tc_fence_after();
+        if (tid == 0 && ok && i + 1 < nch) {  // K has been read by step 2
+            issue_xk(maps, sm, step_t0(i + 1), h);
+            ++xk_issued;
+        }
         // 3. dv_new = dv_loc + kc_t Pd, row tr
         {
-            float p0[32], p1[32];
-            tmem_ld32(tP, p0);
-            tmem_ld32(tP + 32, p1);
+            float p[32];
+            tmem_ld32(tP, p);
             tmem_ld_wait();
             if (trow) {
                 const bool live = tr < L;
-                const float kc = sm.kc[tr];
+                const float kc = sm.kc[i & 1][tr];
                 const unsigned char *dls = sm.x + 3 * kBox;
                 uint4 *dst = reinterpret_cast<uint4 *>(
-                    a.dvnew + ((size_t)(t0 + (live ? tr : 0)) * a.HV + hv) * kDim + 64 * vb);
+                    a.dvnew + ((size_t)(t0 + (live ? tr : 0)) * a.HV + hv) * kDim + 64 * vb + c0);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 lx = *reinterpret_cast<const uint4 *>(dls + sw128_off(tr, 8 * q));
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 lx = *reinterpret_cast<const uint4 *>(dls + sw128_off(tr, c0 + 8 * q));
                     const __nv_bfloat162 *lb = reinterpret_cast<const __nv_bfloat162 *>(&lx);
                     float dv[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 lf = __bfloat1622float2(lb[e]);
-                        const int j = 8 * q + 2 * e;
-                        const float pa = j < 32 ? p0[j & 31] : p1[j & 31];
-                        const float pb = j + 1 < 32 ? p0[(j + 1) & 31] : p1[(j + 1) & 31];
-                        dv[2 * e] = live ? lf.x + kc * pa : 0.f;
-                        dv[2 * e + 1] = live ? lf.y + kc * pb : 0.f;
+                        dv[2 * e] = live ? lf.x + kc * p[8 * q + 2 * e] : 0.f;
+                        dv[2 * e + 1] = live ? lf.y + kc * p[8 * q + 2 * e + 1] : 0.f;
                     }
                     if (live)
                         dst[q] = make_uint4(pack_bf2(dv[0], dv[1]), pack_bf2(dv[2], dv[3]),
                                             pack_bf2(dv[4], dv[5]), pack_bf2(dv[6], dv[7]));
-                    *reinterpret_cast<uint4 *>(sm.a_dv + sw128_off(tr, 8 * q)) =
+                    *reinterpret_cast<uint4 *>(sm.a_dv + sw128_off(tr, c0 + 8 * q)) =
                         make_uint4(pack_bf2(-dv[0], -dv[1]), pack_bf2(-dv[2], -dv[3]),
                                    pack_bf2(-dv[4], -dv[5]), pack_bf2(-dv[6], -dv[7]));
                 }
             }
         }
-        if (!mbar_wait(&sm.y_bar, par)) sm.error = 1;
+        float egl_next = egl;
+        if (i + 1 < nch) {  // publish the next step's scalars, and fetch one step further
+            egl_next = publish((i + 1) & 1);
+            if (i + 2 < nch) fetch(i + 2);
+        }
+        if (tid == 0) tma_store_wait_read();  // dh_c has been read out of a_ds
+        const bool gy = mbar_wait(&sm.y_bar, par);
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();  // X has been read by step 2 and 3
-        if (sm.error) { ok = false; break; }
-        // 4. dh += Q^T (c dO) - w^T dv_new; X is free for the next chunk
+        ok = __syncthreads_and(ok && gy);  // the dO / dv_loc halves have been read
+        if (!ok) break;
+        // 4. dh += Q^T (c dO) - w^T dv_new
         if (tid == 0) {
             tc_fence_after();
             const uint32_t ado = smem_u32(sm.a_do), adv = smem_u32(sm.a_dv);
             const uint32_t qs = smem_u32(sm.y), ws = smem_u32(sm.y + 2 * kBox);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tS, sdesc(qs + s * 2048, kBox, 1024), sdesc(ado + s * 2048, kBox, 1024), idS, true);
+                mma_bf16(tbase, sdesc(qs + s * 2048, kBox, 1024), sdesc(ado + s * 2048, kBox, 1024), idS, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tS, sdesc(ws + s * 2048, kBox, 1024), sdesc(adv + s * 2048, kBox, 1024), idS, true);
+                mma_bf16(tbase, sdesc(ws + s * 2048, kBox, 1024), sdesc(adv + s * 2048, kBox, 1024), idS, true);
             mma_commit(&sm.mma_bar);
             if (i + 1 < nch) {
-                issue_x(maps, sm, a.chunk_start[c - 1], h, hv, vb);
-                ++x_issued;
+                issue_xd(maps, sm, step_t0(i + 1), hv, vb);
+                ++xd_issued;
             }
+            if (i + 2 < nch) prefetch_chunk(maps, step_t0(i + 2), h, hv, vb);
         }
-        if (!mbar_wait(&sm.mma_bar, mma_phase)) sm.error = 1;
-        mma_phase ^= 1;
+        ok = mbar_wait(&sm.mma_bar, phase) && ok;
+        phase ^= 1;
         tc_fence_after();
-        __syncthreads();
-        if (sm.error) { ok = false; break; }
-        if (tid == 0 && i + 1 < nch) {  // Y is free once step 4 has finished
-            issue_y(maps, sm, a.chunk_start[c - 1], h, hv);
+        if (tid == 0 && ok && i + 1 < nch) {  // Q and w are free once step 4 has finished
+            issue_y(maps, sm, step_t0(i + 1), h, hv);
             ++y_issued;
         }
+        egl = egl_next;
     }
+    ok = __syncthreads_and(ok);
     if (ok && a.dh0) {
-        for (int half = 0; half < 2; ++half) {
-            float r[32];
-            tmem_ld32(tS + 32 * half, r);
-            tmem_ld_wait();
-            float4 *dst = reinterpret_cast<float4 *>(a.dh0 + sbase + 32 * half);
+        float r[32];
+        tmem_ld32(tS, r);
+        tmem_ld_wait();
+        float4 *dst = reinterpret_cast<float4 *>(a.dh0 + sbase);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-        }
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
     if (tid == 0) tma_store_wait_all();
     if (!ok && tid == 0) {
-        // drain the loads still in flight (bounded) before leaving
         if (a.status) atomicOr(a.status, 2);
-        if (x_issued > 0) mbar_wait(&sm.x_bar, (x_issued - 1) & 1, 1u << 20);
+        // drain the loads still in flight (bounded) before leaving
+        if (xk_issued > 0) mbar_wait(&sm.xk_bar, (xk_issued - 1) & 1, 1u << 20);
+        if (xd_issued > 0) mbar_wait(&sm.xd_bar, (xd_issued - 1) & 1, 1u << 20);
         if (y_issued > 0) mbar_wait(&sm.y_bar, (y_issued - 1) & 1, 1u << 20);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(sm.tmem_base, 128);
+    if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 }  // namespace

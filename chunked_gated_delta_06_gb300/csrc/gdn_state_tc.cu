@@ -3,9 +3,10 @@
 // The chunks of one sequence are walked in order ("cake_gdn: deterministic
 // chunked GDN training kernels", Summary: fp32 running state across chunks,
 // per-chunk h stored in bf16).  The value columns of the state never mix
-// (v_new[:, v] and h[:, v] depend only on column v), so one CTA of 128 threads
-// owns one (sequence, value head, value half): h[k][v'] for the 64 columns
-// v' = 64 vb .. 64 vb + 63, as an fp32 accumulator in TMEM (lane k, 64 columns).
+// (v_new[:, v] and h[:, v] depend only on column v), so one CTA owns one
+// (sequence, value head, value half): h[k][v'] for the 64 columns v' = 64 vb ..
+// 64 vb + 63, as an fp32 accumulator in TMEM (lane k, 64 columns); its 256
+// threads are two warpgroups that split the columns of every pass.
 // Per chunk (L <= 64 tokens from t0, G the chunk-local cumsum of g, G_L its last
 // value):
 //   1. thread k writes row k of h as bf16 to shared memory (MMA operand; one TMA
@@ -17,9 +18,11 @@
 //   4. h[k][v'] += sum_t K[t][k] A_V[t][v']        (tcgen05, M=128 N=64 K=64; the
 //      raw key tile is read MN-major)
 // which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with Khat =
-// diag(1 / r_k) K.  w, K and this half of u stream in by TMA two chunks ahead.
-// Two CTAs share an SM.  Every wait is bounded; a timeout sets status bit 2 and
-// the CTA unwinds.
+// diag(1 / r_k) K.  w, K and this half of u stream in by TMA two chunks ahead,
+// the next chunk's per-token scalars are loaded a chunk ahead and published
+// during the current epilogue, and a chunk costs two block barriers.  Two CTAs
+// share an SM.  Every wait is bounded; a timeout sets status bit 2 and the CTA
+// unwinds.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -31,7 +34,7 @@ namespace {
 
 using namespace umma;
 
-constexpr int kThr = 128;
+constexpr int kThr = 256;
 constexpr uint32_t kBox = 64 * 128;             // one 64-row x 128-byte SW128 box
 constexpr uint32_t kStageBytes = 5 * kBox;      // w (2 boxes), K (2), u half (1)
 
@@ -40,12 +43,10 @@ struct StateSmem {
     unsigned char a_s[128 * 128];       // h bf16 [k][v']: 128 rows x 128 B
     unsigned char a_v[64 * 128];        // A_V bf16 [t][v']: 64 rows x 128 B
     unsigned char stage[2][kStageBytes];
-    float coef[64];                     // e^{G_L - G_t} / r_k,t, 0 past L
-    float gt[64], rkt[64];              // this chunk's G and r_k (prefetched)
+    float coef[2][64];                  // e^{G_L - G_t} / r_k,t, 0 past L (this and the next chunk)
     uint64_t tma_bar[2];
     uint64_t mma_bar;
     uint32_t tmem_base;
-    int error;
 };
 
 struct StateMaps {
@@ -80,9 +81,16 @@ __global__ void __launch_bounds__(kThr, 2)
     const int cb = a.seq_chunk_off[n];
     const int ce = min(a.seq_chunk_off[n + 1], a.num_chunks);
     const int nch = max(ce - cb, 0);
-    const int kr = tid;                         // the state row this thread owns (S pass)
-    const int tr = 16 * warp + lane;            // the token row it owns (lanes 0..15)
+    const int grp = warp >> 2, sub = warp & 3;
+    const int kr = sub * 32 + lane;     // state row (TMEM lane) of the state pass
+    const int tr = sub * 16 + lane;     // token row of the epilogue (lanes 0..15)
     const bool trow = lane < 16;
+    const int c0 = 32 * grp;            // this warpgroup's 32 of the 64 columns
+    // the sequence's chunks are consecutive 64-token blocks of [ts0, ts1)
+    const int ts0 = nch > 0 ? a.chunk_start[cb] : 0;
+    const int ts1 = nch > 0 ? a.chunk_start[ce - 1] + a.chunk_len[ce - 1] : 0;
+    auto chunk_t0 = [&](int j) { return ts0 + 64 * j; };
+    auto chunk_len = [&](int j) { return min(64, ts1 - (ts0 + 64 * j)); };
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 128);
@@ -93,24 +101,22 @@ __global__ void __launch_bounds__(kThr, 2)
         mbar_init(&sm.tma_bar[1], 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
-        sm.error = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t t_row = sm.tmem_base + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
-    const uint32_t tH = t_row, tP = t_row + 64;
+    const uint32_t tbase = sm.tmem_base;
+    const uint32_t t_row = tbase + ((uint32_t)(sub * 32) << 16);  // this warp's lanes
+    const uint32_t tH = t_row + c0, tP = t_row + 64 + c0;          // this warpgroup's columns
 
-    if (tid == 0) {
-        for (int i = 0; i < 2 && i < nch; ++i)
-            issue_stage(maps, sm, i, a.chunk_start[cb + i], h, hv, vb);
-    }
-    // h <- h0[n][hv][k][v'] (row kr, this half's 64 columns)
-    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb;
-    for (int half = 0; half < 2; ++half) {
+    if (tid == 0)
+        for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, i, chunk_t0(i), h, hv, vb);
+    // h <- h0[n][hv][k][v'] (row kr, this warpgroup's 32 columns)
+    const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb + c0;
+    {
         float r[32];
         if (a.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.h0 + sbase + 32 * half);
+            const float4 *src = reinterpret_cast<const float4 *>(a.h0 + sbase);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 x = src[q];
@@ -120,166 +126,152 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0.f;
         }
-        tmem_st32(tH + 32 * half, r);
+        tmem_st32(tH, r);
+        tmem_st_wait();
     }
-    tmem_st_wait();
-
-    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // P = w h       (h MN-major)
-    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // h += K^T A_V  (both MN-major)
-    uint32_t mma_phase = 0;
-    bool ok = true;
-    // per-token scalars of the next chunk, loaded one chunk ahead
-    float pg = 0.f, prk = 1.f;
-    auto fetch = [&](int cc) {
-        const int tt0 = a.chunk_start[cc], LL = a.chunk_len[cc];
-        if (tid < LL) {
+    // per-chunk scalars: the raw values are loaded one chunk ahead (pgl: G_L; pg,
+    // prk: G_t and r_k,t of thread t < 64) and turned into coef_t and e^{G_L} only
+    // when they are published a chunk later, so no thread waits on the loads
+    float pgl = 0.f, pg = 0.f, prk = 1.f;
+    bool pin = false;
+    auto fetch = [&](int j) {
+        const int tt0 = chunk_t0(j), LL = chunk_len(j);
+        pgl = a.G[(size_t)(tt0 + LL - 1) * a.HV + hv];
+        pin = tid < LL;
+        if (pin) {
             const size_t t = (size_t)(tt0 + tid);
             pg = a.G[t * a.HV + hv];
             prk = a.rk[t * a.H + h];
-        } else {
-            pg = 0.f; prk = 1.f;
         }
     };
-    if (tid < 64 && nch > 0) fetch(cb);
-    for (int i = 0; i < nch && ok; ++i) {
+    auto publish = [&](int buf) {  // returns e^{G_L}
+        if (tid < 64) sm.coef[buf][tid] = pin ? __expf(fminf(pgl - pg, 0.f)) / prk : 0.f;
+        return __expf(pgl);
+    };
+    float egl = 1.f;
+    if (nch > 0) {
+        fetch(0);
+        egl = publish(0);
+        if (nch > 1) fetch(1);
+    }
+    __syncthreads();
+    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // P = w h       (h MN-major)
+    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // h += K^T A_V  (both MN-major)
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int i = 0; i < nch; ++i) {
         const int c = cb + i, st = i & 1;
-        const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-        if (tid < 64) {
-            sm.gt[tid] = pg;
-            sm.rkt[tid] = prk;
-            if (i + 1 < nch) fetch(c + 1);
-        }
-        if (tid == 0) tma_store_wait_read();  // the previous chunk's h_c store has read a_s
-        __syncthreads();
-        const float Gl = L > 0 ? sm.gt[L - 1] : 0.f;
-        if (tid < 64) sm.coef[tid] = tid < L ? __expf(fminf(Gl - sm.gt[tid], 0.f)) / sm.rkt[tid] : 0.f;
-        const float egl = __expf(Gl);
-        // 1. h -> bf16 operand row kr (copied to h_c by TMA below), then h <- e^{G_L} h
+        const int t0 = chunk_t0(i), L = chunk_len(i);
+        // 1. h -> bf16 operand (copied to h_c by TMA below), then h <- e^{G_L} h
         {
-            float r0[32], r1[32];
-            tmem_ld32(tH, r0);
-            tmem_ld32(tH + 32, r1);
+            float r[32];
+            tmem_ld32(tH, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                *reinterpret_cast<uint4 *>(sm.a_s + sw128_off(kr, 8 * q)) =
-                    make_uint4(pack_bf2(r0[8 * q], r0[8 * q + 1]), pack_bf2(r0[8 * q + 2], r0[8 * q + 3]),
-                               pack_bf2(r0[8 * q + 4], r0[8 * q + 5]), pack_bf2(r0[8 * q + 6], r0[8 * q + 7]));
-                *reinterpret_cast<uint4 *>(sm.a_s + sw128_off(kr, 32 + 8 * q)) =
-                    make_uint4(pack_bf2(r1[8 * q], r1[8 * q + 1]), pack_bf2(r1[8 * q + 2], r1[8 * q + 3]),
-                               pack_bf2(r1[8 * q + 4], r1[8 * q + 5]), pack_bf2(r1[8 * q + 6], r1[8 * q + 7]));
-            }
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(sm.a_s + sw128_off(kr, c0 + 8 * q)) =
+                    make_uint4(pack_bf2(r[8 * q], r[8 * q + 1]), pack_bf2(r[8 * q + 2], r[8 * q + 3]),
+                               pack_bf2(r[8 * q + 4], r[8 * q + 5]), pack_bf2(r[8 * q + 6], r[8 * q + 7]));
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                r0[j] *= egl;
-                r1[j] *= egl;
-            }
-            tmem_st32(tH, r0);
-            tmem_st32(tH + 32, r1);
+            for (int j = 0; j < 32; ++j) r[j] *= egl;
+            tmem_st32(tH, r);
+            tmem_st_wait();
         }
-        tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        // every thread waits for the chunk's tiles (u is read below)
-        if (!mbar_wait(&sm.tma_bar[st], (i >> 1) & 1)) sm.error = 1;
-        __syncthreads();
+        const bool got = mbar_wait(&sm.tma_bar[st], (i >> 1) & 1);  // u is read below by everyone
+        ok = __syncthreads_and(ok && got);
+        if (!ok) break;
         // 2. P = w h
         if (tid == 0) {
             tc_fence_after();
-            if (!sm.error) {
-                const uint32_t as = smem_u32(sm.a_s), ws = smem_u32(sm.stage[st]);
+            const uint32_t as = smem_u32(sm.a_s), ws = smem_u32(sm.stage[st]);
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_bf16(tP, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
-                             sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
-                mma_commit(&sm.mma_bar);
-                const int hrow = (c * a.HV + hv) * 128;  // h_c rows (k) of this chunk
-                tma_store_3d(&maps.hc, 64 * vb, 0, hrow, sm.a_s);
-                tma_store_commit();
-            }
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tbase + 64, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
+                         sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
+            mma_commit(&sm.mma_bar);
+            tma_store_3d(&maps.hc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_s);  // h_c rows (k)
+            tma_store_commit();
         }
-        __syncthreads();
-        if (sm.error) { ok = false; break; }
-        if (!mbar_wait(&sm.mma_bar, mma_phase)) sm.error = 1;
-        mma_phase ^= 1;
+        ok = mbar_wait(&sm.mma_bar, phase) && ok;
+        phase ^= 1;
         tc_fence_after();
-        // 3. v_new = u - P, row tr
+        // 3. v_new = u - P: row tr, this warpgroup's 32 columns
         {
-            float p0[32], p1[32];
-            tmem_ld32(tP, p0);
-            tmem_ld32(tP + 32, p1);
+            float p[32];
+            tmem_ld32(tP, p);
             tmem_ld_wait();
             if (trow) {
                 const bool live = tr < L;
-                const float cf = sm.coef[tr];
+                const float cf = sm.coef[i & 1][tr];
                 const unsigned char *us = sm.stage[st] + 4 * kBox;
                 uint4 *dst = reinterpret_cast<uint4 *>(
-                    a.vnew + ((size_t)(t0 + (live ? tr : 0)) * a.HV + hv) * kDim + 64 * vb);
+                    a.vnew + ((size_t)(t0 + (live ? tr : 0)) * a.HV + hv) * kDim + 64 * vb + c0);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 ux = *reinterpret_cast<const uint4 *>(us + sw128_off(tr, 8 * q));
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 ux = *reinterpret_cast<const uint4 *>(us + sw128_off(tr, c0 + 8 * q));
                     const __nv_bfloat162 *ub = reinterpret_cast<const __nv_bfloat162 *>(&ux);
                     float vn[8];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 uf = __bfloat1622float2(ub[e]);
-                        const int j = 8 * q + 2 * e;
-                        const float pa = j < 32 ? p0[j & 31] : p1[j & 31];
-                        const float pb = j + 1 < 32 ? p0[(j + 1) & 31] : p1[(j + 1) & 31];
-                        vn[2 * e] = live ? uf.x - pa : 0.f;
-                        vn[2 * e + 1] = live ? uf.y - pb : 0.f;
+                        vn[2 * e] = live ? uf.x - p[8 * q + 2 * e] : 0.f;
+                        vn[2 * e + 1] = live ? uf.y - p[8 * q + 2 * e + 1] : 0.f;
                     }
                     if (live)
                         dst[q] = make_uint4(pack_bf2(vn[0], vn[1]), pack_bf2(vn[2], vn[3]),
                                             pack_bf2(vn[4], vn[5]), pack_bf2(vn[6], vn[7]));
-                    *reinterpret_cast<uint4 *>(sm.a_v + sw128_off(tr, 8 * q)) =
+                    *reinterpret_cast<uint4 *>(sm.a_v + sw128_off(tr, c0 + 8 * q)) =
                         make_uint4(pack_bf2(vn[0] * cf, vn[1] * cf), pack_bf2(vn[2] * cf, vn[3] * cf),
                                    pack_bf2(vn[4] * cf, vn[5] * cf), pack_bf2(vn[6] * cf, vn[7] * cf));
                 }
             }
         }
+        float egl_next = egl;
+        if (i + 1 < nch) {  // publish the next chunk's scalars, and fetch one chunk further
+            egl_next = publish((i + 1) & 1);
+            if (i + 2 < nch) fetch(i + 2);
+        }
+        if (tid == 0) tma_store_wait_read();  // h_c has been read out of a_s
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
         // 4. h += K^T A_V
         if (tid == 0) {
             tc_fence_after();
             const uint32_t av = smem_u32(sm.a_v), ks = smem_u32(sm.stage[st] + 2 * kBox);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tH, sdesc(ks + s * 2048, kBox, 1024), sdesc(av + s * 2048, kBox, 1024), idS,
-                         true);
+                mma_bf16(tbase, sdesc(ks + s * 2048, kBox, 1024), sdesc(av + s * 2048, kBox, 1024), idS, true);
             mma_commit(&sm.mma_bar);
         }
-        if (!mbar_wait(&sm.mma_bar, mma_phase)) sm.error = 1;
-        mma_phase ^= 1;
+        ok = mbar_wait(&sm.mma_bar, phase) && ok;
+        phase ^= 1;
         tc_fence_after();
-        __syncthreads();
-        if (sm.error) { ok = false; break; }
-        if (tid == 0 && i + 2 < nch) issue_stage(maps, sm, st, a.chunk_start[c + 2], h, hv, vb);
+        if (tid == 0 && ok && i + 2 < nch) issue_stage(maps, sm, st, chunk_t0(i + 2), h, hv, vb);
+        egl = egl_next;
     }
+    ok = __syncthreads_and(ok);
     if (ok && a.ht) {
-        for (int half = 0; half < 2; ++half) {
-            float r[32];
-            tmem_ld32(tH + 32 * half, r);
-            tmem_ld_wait();
-            float4 *dst = reinterpret_cast<float4 *>(a.ht + sbase + 32 * half);
+        float r[32];
+        tmem_ld32(tH, r);
+        tmem_ld_wait();
+        float4 *dst = reinterpret_cast<float4 *>(a.ht + sbase);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-        }
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
     if (tid == 0) tma_store_wait_all();
-    if (!ok) {
+    if (!ok && tid == 0) {
         // drain outstanding TMA copies (bounded) before leaving
-        if (tid == 0) {
-            if (a.status) atomicOr(a.status, 2);
-            mbar_wait(&sm.tma_bar[0], 0, 1u << 20);
-            mbar_wait(&sm.tma_bar[1], 0, 1u << 20);
-        }
+        if (a.status) atomicOr(a.status, 2);
+        mbar_wait(&sm.tma_bar[0], 0, 1u << 20);
+        mbar_wait(&sm.tma_bar[1], 0, 1u << 20);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(sm.tmem_base, 128);
+    if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 }  // namespace

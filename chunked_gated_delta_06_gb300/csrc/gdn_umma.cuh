@@ -183,6 +183,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
         : "memory");
 }
 
+// Warm L2 with a tile that a later tma_load_3d of the same coordinates will read
+// (no shared memory, no barrier; out-of-range parts are ignored as in a load).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Tile store shared -> global (bulk async group of the issuing thread).  The
 // writing threads must have made the tile visible to the async proxy
 // (fence_proxy_async_smem + barrier) before one thread issues the store.

@@ -3,7 +3,7 @@
     python -m chunked_gated_delta_06_gb300.ncu_summary launches.csv [--skip-first N]
         per kernel of a launch list (--metrics gpu__time_duration.sum --csv):
         launches, total and mean device time, share of the total;
-    python -m chunked_gated_delta_06_gb300.ncu_summary --traffic prof.ncu-rep UNITS
+    python -m chunked_gated_delta_06_gb300.ncu_summary --traffic prof.ncu-rep UNITS [prof2 UNITS2 ...]
         JSON record of DRAM bytes per work unit (UNITS = chunk x value-head units,
         or active decode rows x value heads, of the captured launches) with the
         hash of each kernel's source file at capture time (bench.py reports the
@@ -87,6 +87,7 @@ KERNELS = {  # ncu kernel name -> (bench kernel name, source file)
     "k_out_tc<true>": ("out", "gdn_out_tc.cu"), "k_out_tc<false>": ("dvloc", "gdn_out_tc.cu"),
     "k_bstate_tc": ("bstate", "gdn_bstate_tc.cu"), "k_bintra_a_tc": ("bintra_a", "gdn_bintra_tc.cu"),
     "k_bintra_b_tc": ("bintra_b", "gdn_bintra_b_tc.cu"), "k_decode": ("decode", "gdn_decode.cu"),
+    "k_bnorm": ("bnorm", "gdn_chunk.cu"), "k_prep": ("prep", "gdn_chunk.cu"),
 }
 
 
@@ -120,8 +121,13 @@ def traffic(path, units):
 
 if __name__ == "__main__":
     if "--traffic" in sys.argv:
+        # --traffic REPORT UNITS [REPORT UNITS ...]: one merged record
+        import json
         i = sys.argv.index("--traffic")
-        print(traffic(sys.argv[i + 1], float(sys.argv[i + 2])))
+        args, rec = sys.argv[i + 1:], {}
+        for r, u in zip(args[0::2], args[1::2]):
+            rec.update(json.loads(traffic(r, float(u))))
+        print(json.dumps(rec, indent=1, sort_keys=True))
         sys.exit(0)
     if "--report" in sys.argv:
         print(report(sys.argv[sys.argv.index("--report") + 1]))

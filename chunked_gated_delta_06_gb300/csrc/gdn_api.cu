@@ -66,7 +66,7 @@ void carve_saved(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.hc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
     a.vnew = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.w = cv.take<bf16>((size_t)d.T * d.HV * D);
-    a.Tm = cv.take<float>((size_t)d.C * d.HV * gdn::kChunk * gdn::kChunk);
+    a.Tm = cv.take<bf16>((size_t)d.C * d.HV * gdn::kChunk * gdn::kChunk);
     a.rq = cv.take<float>((size_t)d.T * d.H);
     a.rk = cv.take<float>((size_t)d.T * d.H);
     a.G = cv.take<float>((size_t)d.T * d.HV);

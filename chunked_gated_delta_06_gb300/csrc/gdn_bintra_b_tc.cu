@@ -4,7 +4,7 @@
 //
 // One CTA of 256 threads per (chunk, value head), about 100 KB of shared memory
 // and 256 TMEM columns, so that two CTAs share an SM.  With Khat = diag(1/r_k) K,
-// Gamma_ij = exp(G_i - G_j), the WY inverse T (saved by the forward) and dW =
+// Gamma_ij = exp(G_i - G_j), the WY inverse T (saved in bf16 by the forward) and dW =
 // -dv_new h^T (from the h / dh' kernel):
 //   phase 1 (M=64 N=64 K=128, rows = tokens):  KK = K K^T, D1 = dW K^T, D2 = dv_new V^T
 //     dT_ij = beta_j (e^{G_j} D1_ij / r_k,j + D2_ij)          (j < i)
@@ -59,7 +59,7 @@ struct BwSmem {
 };
 
 struct BwMaps {
-    CUtensorMap k, v, dw, dvn;
+    CUtensorMap k, v, dw, dvn, t;
 };
 
 __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-        mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile);
+        mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile + kHalf);
+        tma_load_3d(sm.op_t, &maps.t, 0, 0, (c * a.HV + hv) * 64, &sm.tma_bar);  // T rows (bf16)
         const CUtensorMap *mk[4] = {&maps.k, &maps.v, &maps.dw, &maps.dvn};
         unsigned char *dst[4] = {sm.k, sm.v, sm.dw, sm.dvn};
 #pragma unroll
@@ -110,16 +111,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         sm.eg[tid] = in ? __expf(gg) : 0.f;
         sm.dG[tid] = in ? a.dGp[gi] : 0.f;
     }
-    {  // T (fp32, saved by the forward) -> bf16 rows
-        const float *Tsrc = a.Tm + ((size_t)c * a.HV + hv) * 64 * 64;
-        for (int idx = tid; idx < 64 * 16; idx += kThr) {
-            const int i = idx >> 4, j4 = (idx & 15) * 4;
-            const float4 t4 = __ldg(reinterpret_cast<const float4 *>(Tsrc + i * 64 + j4));
-            *reinterpret_cast<uint2 *>(sm.op_t + sw128_off(i, j4)) =
-                make_uint2(pack_bf2(t4.x, t4.y), pack_bf2(t4.z, t4.w));
-        }
-    }
-    fence_proxy_async_smem();
     bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(sub * 32) << 16);
@@ -364,7 +355,8 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
     if (!encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64))
+        !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BwSmem) + 1024;
     static_assert(2 * (sizeof(BwSmem) + 2048) <= 233472, "two CTAs per SM");

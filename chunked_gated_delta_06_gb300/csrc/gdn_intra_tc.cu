@@ -16,7 +16,7 @@
 //                                                (tcgen05, M=128 N=64 K=64; the K
 //                                                 and V tiles are read MN-major, so
 //                                                 row d of w^T / u^T is TMEM lane d)
-// w and u go to HBM in bf16, T in fp32 (kept for the backward).
+// w, u and T (kept for the backward) go to HBM in bf16.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -235,13 +235,13 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
     {  // operands T diag(c) as bf16 rows, and T to HBM: thread -> row tid / 2, 32 columns
         const int i = tid >> 1, j0 = 32 * (tid & 1);
         const float *Mi = sm.M + i * kS + j0;
-        float4 *Tdst = reinterpret_cast<float4 *>(a.Tm + (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0);
+        uint4 *Tdst = reinterpret_cast<uint4 *>(a.Tm + (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 t0v = *reinterpret_cast<const float4 *>(Mi + 8 * q);
             const float4 t1v = *reinterpret_cast<const float4 *>(Mi + 8 * q + 4);
-            Tdst[2 * q] = t0v;
-            Tdst[2 * q + 1] = t1v;
+            Tdst[q] = make_uint4(pack_bf2(t0v.x, t0v.y), pack_bf2(t0v.z, t0v.w), pack_bf2(t1v.x, t1v.y),
+                                 pack_bf2(t1v.z, t1v.w));
             const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
             const int jb = j0 + 8 * q;
             uint32_t pw[4], pu[4];

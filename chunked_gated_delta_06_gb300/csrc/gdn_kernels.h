@@ -27,7 +27,7 @@ struct ChunkArgs {
     bf16 *hc;               // [C_total,HV,K,V] state at each chunk start
     bf16 *vnew;             // [T,HV,V]
     bf16 *w;                // [T,HV,K]
-    float *Tm;              // [C_total,HV,64,64] (I + A)^-1
+    bf16 *Tm;               // [C_total,HV,64,64] (I + A)^-1
     float *rq, *rk;         // [T,H] sqrt(|x|^2 + eps)
     float *G;               // [T,HV] chunk-local cumulative log decay
     // chunk table (device, rebuilt by every call)

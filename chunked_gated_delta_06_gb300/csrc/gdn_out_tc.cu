@@ -28,11 +28,14 @@ constexpr int kThr = 128;
 constexpr uint32_t kBox = 64 * 128;    // 64 rows x 128 B
 constexpr uint32_t kBig = 128 * 128;   // 128 rows x 128 B
 
+// The backward mode needs no h_c tile and half the TMEM columns, so three of its
+// CTAs share an SM (two in the forward mode).
+template <bool kForward>
 struct OutSmem {
     unsigned char kq[2 * kBig];   // [K; Q] per k-half: K rows 0..63, Q rows 64..127
-    unsigned char hc[2 * kBig];   // h_c [k][v] per v-half (forward)
     unsigned char tv[2 * kBox];   // v_new (forward) or dO (backward) [t][v] per v-half
     unsigned char mm[kBox];       // M, row i at row i (bf16)
+    unsigned char hc[kForward ? 2 * kBig : 16];   // h_c [k][v] per v-half (forward only)
     float G[64], rq[64], rk[64];
     float qsc[64], rki[64], ct[64];  // scale / r_q, 1 / r_k, e^{G} scale / r_q
     uint64_t tma_bar, mma_bar;
@@ -49,11 +52,14 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
 }
 
 template <bool kForward>
-__global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
-                                                    const __grid_constant__ OutMaps maps) {
+constexpr uint32_t kTmemCols = kForward ? 256 : 128;
+
+template <bool kForward>
+__global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkArgs a,
+                                                                   const __grid_constant__ OutMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    OutSmem &sm = *reinterpret_cast<OutSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
+    OutSmem<kForward> &sm = *reinterpret_cast<OutSmem<kForward> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
     const int c = blockIdx.x, hv = blockIdx.y;
     const int h = hv / (a.HV / a.H);
@@ -61,7 +67,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
     if (L <= 0) return;
 
     if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 256);
+        tmem_alloc(&sm.tmem_base, kTmemCols<kForward>);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kThr, 1) k_out_tc(const ChunkArgs a,
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tb, 256);
+    if (warp == 0) tmem_dealloc(tb, kTmemCols<kForward>);
 }
 
 template <bool kForward>
@@ -207,7 +213,8 @@ cudaError_t launch_out_mode(const ChunkArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     if (kForward && !encode_rows_bf16(&m.h, a.hc, 1, hrows, rowb, rowb, 128))
         return cudaErrorInvalidValue;
-    const size_t smem = sizeof(OutSmem) + 1024;
+    const size_t smem = sizeof(OutSmem<kForward>) + 1024;
+    static_assert((kForward ? 2 : 3) * (sizeof(OutSmem<kForward>) + 2048) <= 233472, "CTAs per SM");
     cudaError_t e = cudaFuncSetAttribute(k_out_tc<kForward>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

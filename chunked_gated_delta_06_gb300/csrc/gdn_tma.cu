@@ -24,10 +24,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 bool encode_rows_bf16(CUtensorMap *map, const void *base, uint64_t d1, uint64_t d2,
-                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box2) {
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box2,
+                      uint64_t inner) {
     auto fn = encode_fn();
     if (!fn || !base) return false;
-    cuuint64_t dims[3] = {128, d1 > 0 ? d1 : 1, d2 > 0 ? d2 : 1};
+    cuuint64_t dims[3] = {inner, d1 > 0 ? d1 : 1, d2 > 0 ? d2 : 1};
     cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
     cuuint32_t box[3] = {64, 1, box2};
     cuuint32_t es[3] = {1, 1, 1};

@@ -43,7 +43,7 @@ def test_saved_and_workspace_sizes(lib):
     def al(x):
         return (x + 255) // 256 * 256
     saved = (al(C * HV * D * D * 2) + al(T * HV * D * 2) + al(T * HV * D * 2)
-             + al(C * HV * 64 * 64 * 4) + al(T * H * 4) + al(T * H * 4) + al(T * HV * 4))
+             + al(C * HV * 64 * 64 * 2) + al(T * H * 4) + al(T * H * 4) + al(T * HV * 4))
     assert gdn.gdn_chunk_saved_bytes(p) == saved
     fwd_ws = gdn.gdn_chunk_workspace_bytes(p, 0)
     assert fwd_ws >= saved + T * HV * D * 2

@@ -71,9 +71,9 @@ def kernel_work(name, T, H, HV, N, C_total):
         out=T * H * D * bf * 2 + TV * D * bf * 2 + C_total * HV * D * D * bf,
         dvloc=T * H * D * bf * 2 + TV * D * bf * 2,
         bstate=T * H * D * bf * 2 + TV * D * bf * 4 + C_total * HV * D * D * bf,
-        bintra_a=T * H * D * bf * 2 + TV * D * (bf * 4 + 4 * 2) + TV * 4 + C_total * HV * D * D * bf * 2,
-        bintra_b=T * H * D * bf + TV * D * (bf * 4 + 4) + TV * 12 + C_total * HV * C * C * 2,
-        bnorm=TV * D * 4 * 3 + T * H * D * bf * 4,
+        bintra_a=T * H * D * bf * 2 + TV * D * bf * 6 + TV * 4 + C_total * HV * D * D * bf * 2,
+        bintra_b=T * H * D * bf + TV * D * bf * 5 + TV * 12 + C_total * HV * C * C * 2,
+        bnorm=TV * D * bf * 3 + T * H * D * bf * 4,
     ).get(name, 0.0)
     return f, b
 

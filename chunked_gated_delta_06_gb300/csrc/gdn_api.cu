@@ -94,9 +94,9 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.dvnew = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dhc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
     a.dW = cv.take<bf16>((size_t)d.T * d.HV * D);
-    a.dqp = cv.take<float>((size_t)d.T * d.HV * D);
-    a.dkp = cv.take<float>((size_t)d.T * d.HV * D);
-    a.dkp2 = cv.take<float>((size_t)d.T * d.HV * D);
+    a.dqp = cv.take<bf16>((size_t)d.T * d.HV * D);
+    a.dkp = cv.take<bf16>((size_t)d.T * d.HV * D);
+    a.dkp2 = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dGp = cv.take<float>((size_t)d.T * d.HV);
 }
 

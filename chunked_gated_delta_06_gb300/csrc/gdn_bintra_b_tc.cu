@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
 #pragma unroll
             for (int mm = 0; mm < 32; ++mm) {
                 const int m = j0 + mm;
-                if (m < L) a.dkp2[base + (size_t)m * ts] = dk[mm] + sm.beta[m] * sm.eg[m] * wt[mm];
+                if (m < L) a.dkp2[base + (size_t)m * ts] = __float2bfloat16_rn(dk[mm] + sm.beta[m] * sm.eg[m] * wt[mm]);
             }
         }
         float ut[32];

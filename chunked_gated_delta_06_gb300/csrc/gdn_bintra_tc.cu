@@ -16,8 +16,8 @@
 //   M_ij = QK_ij scale / (r_q,i r_k,j) Gamma_ij,  dMG = dM (.) Gamma,  P1 = dM (.) M
 //   (j <= i);
 //   batch 2 (M=64, contraction 64): dMG Khat and dMG^T Qhat;
-//   dqhat_t = e^{G_t} Dq_t + (dMG Khat)_t                  -> HBM (fp32, per value head)
-//   dkhat_t = e^{G_L - G_t} Dk_t + (dMG^T Qhat)_t           -> HBM (fp32, the rest comes
+//   dqhat_t = e^{G_t} Dq_t + (dMG Khat)_t                  -> HBM (bf16, per value head)
+//   dkhat_t = e^{G_L - G_t} Dk_t + (dMG^T Qhat)_t           -> HBM (bf16, the rest comes
 //                                                              from the WY pullback)
 //   dG_t    = qhat_t . e^{G_t} Dq_t - xi_t + sum_j P1_tj - sum_i P1_it,
 //   xi_t = khat_t . e^{G_L - G_t} Dk_t,   dG_L += sum_t xi_t + e^{G_L} <h, dh'>.
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 tmem_ld32(t_row + cQI + cc * 32, qi);
                 tmem_ld_wait();
                 const unsigned char *qrow = sm.q + (cc >> 1) * kBox;
-                float4 *qp = reinterpret_cast<float4 *>(a.dqp + o + cc * 32);
+                uint4 *qp = reinterpret_cast<uint4 *>(a.dqp + o + cc * 32);
 #pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per step
                     const int col = (cc & 1) * 32 + q8 * 8;
@@ -325,10 +325,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                         v8[2 * e] = a0 + qi[q8 * 8 + 2 * e];
                         v8[2 * e + 1] = a1 + qi[q8 * 8 + 2 * e + 1];
                     }
-                    if (live) {
-                        qp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
-                        qp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
-                    }
+                    if (live)
+                        qp[q8] = make_uint4(pack_bf2(v8[0], v8[1]), pack_bf2(v8[2], v8[3]),
+                                            pack_bf2(v8[4], v8[5]), pack_bf2(v8[6], v8[7]));
                 }
             }
 #pragma unroll
@@ -338,7 +337,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 tmem_ld32(t_row + cKI + cc * 32, ki);
                 tmem_ld_wait();
                 const unsigned char *krow = sm.k + (cc >> 1) * kBox;
-                float4 *kp = reinterpret_cast<float4 *>(a.dkp + o + cc * 32);
+                uint4 *kp = reinterpret_cast<uint4 *>(a.dkp + o + cc * 32);
 #pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8) {
                     const int col = (cc & 1) * 32 + q8 * 8;
@@ -353,10 +352,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                         v8[2 * e] = a0 + ki[q8 * 8 + 2 * e];
                         v8[2 * e + 1] = a1 + ki[q8 * 8 + 2 * e + 1];
                     }
-                    if (live) {
-                        kp[q8 * 2] = make_float4(v8[0], v8[1], v8[2], v8[3]);
-                        kp[q8 * 2 + 1] = make_float4(v8[4], v8[5], v8[6], v8[7]);
-                    }
+                    if (live)
+                        kp[q8] = make_uint4(pack_bf2(v8[0], v8[1]), pack_bf2(v8[2], v8[3]),
+                                            pack_bf2(v8[4], v8[5]), pack_bf2(v8[6], v8[7]));
                 }
             }
             if (active) {

@@ -136,9 +136,15 @@ __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
     float dq[4] = {0, 0, 0, 0}, dk[4] = {0, 0, 0, 0}, xq[4], xk[4];
     for (int j = 0; j < r; ++j) {
         const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + lane * 4;
-        const float4 q1 = *reinterpret_cast<const float4 *>(a.dqp + o);
-        const float4 k1 = *reinterpret_cast<const float4 *>(a.dkp + o);
-        const float4 k2 = *reinterpret_cast<const float4 *>(a.dkp2 + o);
+        const uint2 q2 = *reinterpret_cast<const uint2 *>(a.dqp + o);
+        const uint2 k2a = *reinterpret_cast<const uint2 *>(a.dkp + o);
+        const uint2 k2b = *reinterpret_cast<const uint2 *>(a.dkp2 + o);
+        const float2 qa = bf2_to_f2(q2.x), qb = bf2_to_f2(q2.y);
+        const float2 ka = bf2_to_f2(k2a.x), kb = bf2_to_f2(k2a.y);
+        const float2 kc = bf2_to_f2(k2b.x), kd = bf2_to_f2(k2b.y);
+        const float4 q1 = make_float4(qa.x, qa.y, qb.x, qb.y);
+        const float4 k1 = make_float4(ka.x, ka.y, kb.x, kb.y);
+        const float4 k2 = make_float4(kc.x, kc.y, kd.x, kd.y);
         dq[0] += q1.x; dq[1] += q1.y; dq[2] += q1.z; dq[3] += q1.w;
         dk[0] += k1.x + k2.x; dk[1] += k1.y + k2.y; dk[2] += k1.z + k2.z; dk[3] += k1.w + k2.w;
     }

@@ -14,6 +14,10 @@ constexpr float kNormEps = 1e-6f;
 using bf16 = __nv_bfloat16;
 
 __device__ __forceinline__ float bf2f(bf16 x) { return __bfloat162float(x); }
+// two packed bf16 (the first in the low half) -> their float values (exact)
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t x) {
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
 __device__ __forceinline__ bf16 f2bf(float x) { return __float2bfloat16_rn(x); }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -45,9 +45,9 @@ struct ChunkArgs {
     bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
     bf16 *dhc;              // [C_total,HV,K,V] gradient of the state after each chunk
     bf16 *dW;               // [T,HV,K]
-    float *dqp, *dkp;       // [T,HV,K] per-value-head gradients of qhat (all terms) and
+    bf16 *dqp, *dkp;        // [T,HV,K] per-value-head gradients of qhat (all terms) and
                             // khat (h / dh' and Q K^T terms)
-    float *dkp2;            // [T,HV,K] the WY-pullback terms of the khat gradient
+    bf16 *dkp2;             // [T,HV,K] the WY-pullback terms of the khat gradient
     float *dGp;             // [T,HV]
     gdn_kernel_timer *timer;  // optional per-kernel events
 };

@@ -126,45 +126,73 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
 // ---------------------------------------------------------------------------
 // Backward, step 5: sum the per-value-head gradients of qhat / khat over the
 // HV / H value heads of each key head (fixed order) and apply the L2-norm
-// backward dx = (dn - n (n . dn)) / r.  One warp per (token, key head).
+// backward dx = (dn - n (n . dn)) / r.  Half a warp per (token, key head): each
+// lane moves 8 elements with 16-byte loads and stores.
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
+    const float2 a0 = bf2_to_f2(u.x), a1 = bf2_to_f2(u.y), a2 = bf2_to_f2(u.z), a3 = bf2_to_f2(u.w);
+    x[0] = a0.x; x[1] = a0.y; x[2] = a1.x; x[3] = a1.y; x[4] = a2.x; x[5] = a2.y; x[6] = a3.x; x[7] = a3.y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
 __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t item = (size_t)blockIdx.x * (kThreads / 32) + warp;
-    if (item >= (size_t)a.T * a.H) return;
-    const int t = (int)(item / a.H), h = (int)(item % a.H);
+    const int l16 = threadIdx.x & 15;
+    const size_t item = (size_t)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
+    const bool valid = item < (size_t)a.T * a.H;
+    const int t = valid ? (int)(item / a.H) : 0, h = valid ? (int)(item % a.H) : 0;
     const int r = a.HV / a.H;
-    float dq[4] = {0, 0, 0, 0}, dk[4] = {0, 0, 0, 0}, xq[4], xk[4];
-    for (int j = 0; j < r; ++j) {
-        const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + lane * 4;
-        const uint2 q2 = *reinterpret_cast<const uint2 *>(a.dqp + o);
-        const uint2 k2a = *reinterpret_cast<const uint2 *>(a.dkp + o);
-        const uint2 k2b = *reinterpret_cast<const uint2 *>(a.dkp2 + o);
-        const float2 qa = bf2_to_f2(q2.x), qb = bf2_to_f2(q2.y);
-        const float2 ka = bf2_to_f2(k2a.x), kb = bf2_to_f2(k2a.y);
-        const float2 kc = bf2_to_f2(k2b.x), kd = bf2_to_f2(k2b.y);
-        const float4 q1 = make_float4(qa.x, qa.y, qb.x, qb.y);
-        const float4 k1 = make_float4(ka.x, ka.y, kb.x, kb.y);
-        const float4 k2 = make_float4(kc.x, kc.y, kd.x, kd.y);
-        dq[0] += q1.x; dq[1] += q1.y; dq[2] += q1.z; dq[3] += q1.w;
-        dk[0] += k1.x + k2.x; dk[1] += k1.y + k2.y; dk[2] += k1.z + k2.z; dk[3] += k1.w + k2.w;
+    float dq[8], dk[8], xq[8], xk[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) dq[u] = dk[u] = 0.f;
+    if (valid) {
+        for (int j = 0; j < r; ++j) {
+            const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + l16 * 8;
+            float x1[8], x2[8], x3[8];
+            unpack8(*reinterpret_cast<const uint4 *>(a.dqp + o), x1);
+            unpack8(*reinterpret_cast<const uint4 *>(a.dkp + o), x2);
+            unpack8(*reinterpret_cast<const uint4 *>(a.dkp2 + o), x3);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                dq[u] += x1[u];
+                dk[u] += x2[u] + x3[u];
+            }
+        }
     }
-    const size_t row = ((size_t)t * a.H + h) * kDim + lane * 4;
-    const float rq = a.rq[(size_t)t * a.H + h], rk = a.rk[(size_t)t * a.H + h];
+    const size_t row = ((size_t)t * a.H + h) * kDim + l16 * 8;
+    const float rq = valid ? a.rq[(size_t)t * a.H + h] : 1.f, rk = valid ? a.rk[(size_t)t * a.H + h] : 1.f;
+    if (valid) {
+        unpack8(*reinterpret_cast<const uint4 *>(a.q + row), xq);
+        unpack8(*reinterpret_cast<const uint4 *>(a.k + row), xk);
+    } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) xq[u] = xk[u] = 0.f;
+    }
     float nq = 0.f, nk = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        xq[u] = bf2f(a.q[row + u]) / rq;
-        xk[u] = bf2f(a.k[row + u]) / rk;
+    for (int u = 0; u < 8; ++u) {
+        xq[u] /= rq;
+        xk[u] /= rk;
         dq[u] *= a.scale;
         nq += xq[u] * dq[u];
         nk += xk[u] * dk[u];
     }
-    nq = warp_sum(nq);
-    nk = warp_sum(nk);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        a.dq[row + u] = f2bf((dq[u] - xq[u] * nq) / rq);
-        a.dk[row + u] = f2bf((dk[u] - xk[u] * nk) / rk);
+    for (int o = 8; o; o >>= 1) {  // the 16 lanes of this item
+        nq += __shfl_xor_sync(0xffffffffu, nq, o);
+        nk += __shfl_xor_sync(0xffffffffu, nk, o);
+    }
+    if (valid) {
+        uint32_t pq[4], pk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            pq[u] = pack2((dq[2 * u] - xq[2 * u] * nq) / rq, (dq[2 * u + 1] - xq[2 * u + 1] * nq) / rq);
+            pk[u] = pack2((dk[2 * u] - xk[2 * u] * nk) / rk, (dk[2 * u + 1] - xk[2 * u + 1] * nk) / rk);
+        }
+        *reinterpret_cast<uint4 *>(a.dq + row) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
+        *reinterpret_cast<uint4 *>(a.dk + row) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
 }
 
@@ -202,7 +230,7 @@ cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     if ((e = launch_bintra_b_tc(a, s)) != cudaSuccess) return e;
     {
         const size_t items = (size_t)a.T * a.H;
-        const unsigned blocks = (unsigned)((items + kThreads / 32 - 1) / (kThreads / 32));
+        const unsigned blocks = (unsigned)((items + kThreads / 16 - 1) / (kThreads / 16));
         TimerScope ts(a.timer, GDN_KERNEL_BNORM, s);
         k_bnorm<<<blocks, kThreads, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

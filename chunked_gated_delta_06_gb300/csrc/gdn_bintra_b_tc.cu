@@ -13,10 +13,11 @@
 //   phase 2 (M=128 N=64 K=64, rows = features d, columns = tokens m):
 //     (B Khat + B^T Khat)^T,  dWt^T = (T^T dW)^T,  dUt^T = (T^T dv_new)^T
 //     dkhat_m += (B Khat + B^T Khat)_m + beta_m e^{G_m} dWt_m,  dv_m = beta_m dUt_m
-// The row dots khat_m . dWt_m = sum_i T_im D1_im / r_k,m and v_m . dUt_m =
-// sum_i T_im D2_im that dbeta and dG need are column sums of T (.) D1 and
-// T (.) D2 read off phase 1, taken with warp butterflies, as are the column sums
-// of beta_i P2:
+// The M=64 results are read as 16x256b fragments (two rows and eight columns per
+// lane, all 32 lanes busy).  The row dots khat_m . dWt_m = sum_i T_im D1_im / r_k,m
+// and v_m . dUt_m = sum_i T_im D2_im that dbeta and dG need are column sums of
+// T (.) D1 and T (.) D2 read off phase 1, taken with warp butterflies, as are the
+// column sums of beta_i P2:
 //   dbeta_m = sum_j P2_mj + e^{G_m}/r_k,m sum_i T_im D1_im + sum_i T_im D2_im
 //   dG_m   += beta_m sum_j P2_mj - sum_i beta_i P2_im + beta_m e^{G_m}/r_k,m sum_i T_im D1_im
 // and dg is the reverse cumulative sum of dG (which arrives holding the h / dh'
@@ -33,9 +34,13 @@ namespace gdn {
 namespace {
 
 using namespace umma;
-using epi::colsum16;
 using epi::pack_bf2;
-using epi::put_row32;
+using epi::colsum_frag;
+using epi::colsum_frag_col;
+using epi::get_pair;
+using epi::put_pair;
+using epi::quad_sum;
+using epi::tmem_ld16x256_x4;
 
 constexpr int kThr = 256;   // two warpgroups share the 128 TMEM lanes
 constexpr uint32_t kHalf = 64 * 128;      // 64 rows x 128 B
@@ -72,10 +77,8 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     const int h = hv / (a.HV / a.H);
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
     if (L <= 0) return;
-    const bool active = lane < 16;            // lane holds an M=64 result row
     const int grp = warp >> 2;                // warpgroup: which half of the columns
     const int sub = warp & 3;                 // TMEM lane quarter
-    const int row = sub * 16 + lane;          // M=64 row (valid when active)
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 256);
@@ -137,55 +140,39 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         mma_commit(&sm.mma_bar);
     }
     commit_wait(ok);
-    const int i = row;
-    const bool live = active && i < L;
-    const int j0 = 32 * grp;  // this warpgroup's columns
-    if (ok) {  // dT rows (bf16 operand) and the column sums of T (.) D1, T (.) D2
-        float d1[32], d2[32];
-        tmem_ld32(t_row + cD1 + j0, d1);
-        tmem_ld32(t_row + cD2 + j0, d2);
+    // M=64 epilogues read 16x256b fragments: lane t of warp (grp, sub) holds rows
+    // ra = 16 sub + t/4 and rb = ra + 8, columns j0 + 8k + 2 (t % 4) + {0, 1}.
+    const int j0 = 32 * grp;                  // this warpgroup's columns
+    const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+    const bool la = ra < L, lb = rb < L;
+    const int ccol = j0 + colsum_frag_col(lane);  // the column whose sums this lane keeps
+    if (ok) {  // dT rows (bf16 operand) and the column sums of T (.) D1, T (.) s
+        float d1[16], d2[16];
+        tmem_ld16x256_x4(t_row + cD1 + j0, d1);
+        tmem_ld16x256_x4(t_row + cD2 + j0, d2);
         tmem_ld_wait();
-        float t[32];
+        float z[8], y[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 x = *reinterpret_cast<const uint4 *>(sm.op_t + sw128_off(active ? i : 0, j0 + 8 * q));
-            const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&x);
+        for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(xb[e]);
-                t[8 * q + 2 * e] = f.x;
-                t[8 * q + 2 * e + 1] = f.y;
+            for (int p = 0; p < 2; ++p) {
+                const int j = j0 + 8 * k + cq + p;
+                const float f1 = sm.eg[j] * sm.rki[j], bj = sm.beta[j];
+                const float sa = f1 * d1[4 * k + p] + d2[4 * k + p];
+                const float sb = f1 * d1[4 * k + 2 + p] + d2[4 * k + 2 + p];
+                const float2 ta = get_pair(sm.op_t, ra, j0 + 8 * k + cq);   // T is zero above the diagonal
+                const float2 tb2 = get_pair(sm.op_t, rb, j0 + 8 * k + cq);
+                const float tva = la ? (p ? ta.y : ta.x) : 0.f, tvb = lb ? (p ? tb2.y : tb2.x) : 0.f;
+                z[2 * k + p] = tva * d1[4 * k + p] + tvb * d1[4 * k + 2 + p];
+                y[2 * k + p] = tva * sa + tvb * sb;
+                d2[4 * k + p] = (la && j < ra) ? bj * sa : 0.f;        // dT, in place
+                d2[4 * k + 2 + p] = (lb && j < rb) ? bj * sb : 0.f;
             }
+            put_pair(sm.op_dx, ra, j0 + 8 * k + cq, d2[4 * k], d2[4 * k + 1]);
+            put_pair(sm.op_dx, rb, j0 + 8 * k + cq, d2[4 * k + 2], d2[4 * k + 3]);
         }
-        // in place, to keep the register count low: d2 <- s = e^{G_j}/r_k,j D1 + D2,
-        // d1 <- T (.) D1, then T (.) s, then dT
-        const float lm = live ? 1.f : 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int j = j0 + jj;
-            t[jj] *= lm;                              // T is zero above the diagonal
-            d2[jj] = sm.eg[j] * sm.rki[j] * d1[jj] + d2[jj];
-            d1[jj] = t[jj] * d1[jj];
-        }
-        float s0, s1;
-        colsum16(d1, lane, s0, s1);
-        if (active) {
-            sm.cz[sub][j0 + 2 * lane] = s0;
-            sm.cz[sub][j0 + 2 * lane + 1] = s1;
-        }
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) d1[jj] = t[jj] * d2[jj];
-        colsum16(d1, lane, s0, s1);
-        if (active) {
-            sm.cy[sub][j0 + 2 * lane] = s0;
-            sm.cy[sub][j0 + 2 * lane + 1] = s1;
-        }
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int j = j0 + jj;
-            d1[jj] = (live && j < i) ? sm.beta[j] * d2[jj] : 0.f;
-        }
-        if (active) put_row32(sm.op_dx, i, j0, d1);
+        sm.cz[sub][ccol] = colsum_frag(z, lane);
+        sm.cy[sub][ccol] = colsum_frag(y, lane);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -202,10 +189,14 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     }
     commit_wait(ok);
     if (ok) {  // X rows -> bf16 over the dT rows (the product that read them is done)
-        float x[32];
-        tmem_ld32(t_row + cX + j0, x);
+        float x[16];
+        tmem_ld16x256_x4(t_row + cX + j0, x);
         tmem_ld_wait();
-        if (active) put_row32(sm.op_dx, i, j0, x);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            put_pair(sm.op_dx, ra, j0 + 8 * k + cq, x[4 * k], x[4 * k + 1]);
+            put_pair(sm.op_dx, rb, j0 + 8 * k + cq, x[4 * k + 2], x[4 * k + 3]);
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -222,37 +213,45 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     }
     commit_wait(ok);
     if (ok) {  // dA = -(T^T X): B and its operands, P2 row sums, column sums of beta_i P2
-        float ta[32], kk[32];
-        tmem_ld32(t_row + cA + j0, ta);
-        tmem_ld32(t_row + cKK + j0, kk);
+        float ta[16], kk[16];
+        tmem_ld16x256_x4(t_row + cA + j0, ta);
+        tmem_ld16x256_x4(t_row + cKK + j0, kk);
         tmem_ld_wait();
-        const float Gi = active ? sm.G[i] : 0.f;
-        const float bi = active ? sm.beta[i] : 0.f;
-        const float rkii = active ? sm.rki[i] : 1.f;
-        // in place: ta <- dA (.) Gamma, kk <- beta_i P2, then the two B operand rows
-        float rsp = 0.f;
+        const float Ga = sm.G[ra], Gb = sm.G[rb];
+        const float ba = sm.beta[ra], bb = sm.beta[rb];
+        const float rka = sm.rki[ra], rkb = sm.rki[rb];
+        float rsa = 0.f, rsb = 0.f, pb[8];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int j = j0 + jj;
-            const float msk = (live && j < i) ? 1.f : 0.f;
-            ta[jj] = -ta[jj] * msk * __expf(fminf(Gi - sm.G[j], 0.f));
-            const float p2 = ta[jj] * kk[jj] * rkii * sm.rki[j];
-            rsp += p2;
-            kk[jj] = bi * p2;
+        for (int k = 0; k < 4; ++k) {
+            float b1[4], b2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = j0 + 8 * k + cq + (e & 1);
+                const bool up = e & 2;                       // row rb
+                const int r = up ? rb : ra;
+                const float msk = ((up ? lb : la) && j < r) ? 1.f : 0.f;
+                const float dag = -ta[4 * k + e] * msk * __expf(fminf((up ? Gb : Ga) - sm.G[j], 0.f));
+                const float rkj = sm.rki[j], br = up ? bb : ba, rkr = up ? rkb : rka;
+                const float p2 = dag * kk[4 * k + e] * rkr * rkj;
+                if (up) rsb += p2; else rsa += p2;
+                b1[e] = dag * br * rkj;   // B_rj / r_k,j
+                b2[e] = dag * br * rkr;   // B_rj / r_k,r
+                kk[4 * k + e] = br * p2;  // beta_r P2_rj
+            }
+            pb[2 * k] = kk[4 * k] + kk[4 * k + 2];
+            pb[2 * k + 1] = kk[4 * k + 1] + kk[4 * k + 3];
+            put_pair(sm.op_b, ra, j0 + 8 * k + cq, b1[0], b1[1]);
+            put_pair(sm.op_b, rb, j0 + 8 * k + cq, b1[2], b1[3]);
+            put_pair(sm.op_bt, ra, j0 + 8 * k + cq, b2[0], b2[1]);
+            put_pair(sm.op_bt, rb, j0 + 8 * k + cq, b2[2], b2[3]);
         }
-        float s0, s1;
-        colsum16(kk, lane, s0, s1);
-        if (active) {
-            sm.cp[sub][j0 + 2 * lane] = s0;
-            sm.cp[sub][j0 + 2 * lane + 1] = s1;
-            sm.rs[grp][i] = rsp;
+        sm.cp[sub][ccol] = colsum_frag(pb, lane);
+        rsa = quad_sum(rsa);
+        rsb = quad_sum(rsb);
+        if ((lane & 3) == 0) {
+            sm.rs[grp][ra] = rsa;
+            sm.rs[grp][rb] = rsb;
         }
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) kk[jj] = ta[jj] * bi * sm.rki[j0 + jj];
-        if (active) put_row32(sm.op_b, i, j0, kk);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) kk[jj] = ta[jj] * bi * rkii;
-        if (active) put_row32(sm.op_bt, i, j0, kk);
     }
     fence_proxy_async_smem();
     tc_fence_before();

@@ -56,5 +56,66 @@ __device__ __forceinline__ void colsum16(const float (&x)[32], int lane, float &
     s1 = (b0 ? c[3] : c[1]) + r1;
 }
 
+// ---- M=64 results read as 16x256b fragments: all 32 lanes of a warp work.
+// For the 16 TMEM lanes (result rows) of warp w and 32 columns from column
+// address c, tcgen05.ld.16x256b.x4 gives lane t the registers
+//   x[4k + e] = D[16 w + t/4 + 8 (e >> 1)][c + 8k + 2 (t % 4) + (e & 1)],  k, e = 0..3
+// (checked on the GPU: two rows, eight columns per lane).
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float (&x)[16]) {
+    uint32_t u[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+        "[%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(u[i]);
+}
+
+// Column sums over the 16 rows of a 16x256b fragment: y[2k + p] is this lane's
+// two-row partial of column 8k + 2 (t % 4) + p.  Three butterfly steps over the
+// eight lanes that share t % 4 leave lane t with the sum of column
+// 8 (c8 >> 1) + 2 (t % 4) + (c8 & 1), c8 = t / 4.  Fixed order.
+__device__ __forceinline__ float colsum_frag(const float (&y)[8], int lane) {
+    float a[4], b[2];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = b4 ? y[j] : y[4 + j];
+        a[j] = (b4 ? y[4 + j] : y[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = b3 ? a[j] : a[2 + j];
+        b[j] = (b3 ? a[2 + j] : a[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? b[0] : b[1];
+    return (b2 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+}
+
+// The column that colsum_frag leaves in lane t, relative to the fragment's first column.
+__device__ __forceinline__ int colsum_frag_col(int lane) {
+    const int c8 = lane >> 2;
+    return 8 * (c8 >> 1) + 2 * (lane & 3) + (c8 & 1);
+}
+
+// Sum over the four lanes of a quad (the eight columns of one row that a fragment
+// spreads over lanes 4q .. 4q + 3).
+__device__ __forceinline__ float quad_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v;
+}
+
+// bf16 pair (columns col, col + 1 of row `row`) into a 64-wide SW128 tile.
+__device__ __forceinline__ void put_pair(unsigned char *tile, int row, int col, float a, float b) {
+    *reinterpret_cast<uint32_t *>(tile + umma::sw128_off(row, col)) = pack_bf2(a, b);
+}
+
+__device__ __forceinline__ float2 get_pair(const unsigned char *tile, int row, int col) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(tile + umma::sw128_off(row, col)));
+}
+
 }  // namespace epi
 }  // namespace gdn

@@ -37,7 +37,12 @@ namespace {
 using namespace umma;
 using epi::colsum16;
 using epi::pack_bf2;
-using epi::put_row32;
+using epi::colsum_frag;
+using epi::colsum_frag_col;
+using epi::get_pair;
+using epi::put_pair;
+using epi::quad_sum;
+using epi::tmem_ld16x256_x4;
 
 constexpr int kThr = 256;
 constexpr uint32_t kBox = 64 * 128;       // 64 rows x 128 B
@@ -232,37 +237,46 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             ++a_issued;
         }
         const bool live = active && t < L;
+        const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);  // fragment rows / column
+        const bool la = ra < L, lb = rb < L;
         {
-            // (a) QK, dM -> P1 (row and column sums) and the two dMG operand rows
+            // (a) QK, dM -> P1 (row and column sums) and the two dMG operand rows, read
+            // as 16x256b fragments: rows ra, rb = ra + 8, columns j0 + 8k + cq + {0, 1}
             const int j0 = 32 * grp;
-            float qk[32], dm[32];
-            tmem_ld32(t_row + cQK + j0, qk);
-            tmem_ld32(t_row + cDM + j0, dm);
+            float qk[16], dm[16];
+            tmem_ld16x256_x4(t_row + cQK + j0, qk);
+            tmem_ld16x256_x4(t_row + cDM + j0, dm);
             tmem_ld_wait();
-            const float Gi = active ? sm.G[t] : 0.f;
-            const float qsi = active ? sm.qsc[t] : 0.f;
-            float rsum = 0.f;
+            const float Ga = sm.G[ra], Gb = sm.G[rb], qsa = sm.qsc[ra], qsb = sm.qsc[rb];
+            float rsa = 0.f, rsb = 0.f, pc[8];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {  // in place: dm <- dMG, qk <- P1
-                const int j = j0 + jj;
-                const float msk = (live && j <= t) ? 1.f : 0.f;
-                dm[jj] *= msk * __expf(fminf(Gi - sm.G[j], 0.f));
-                qk[jj] = dm[jj] * qk[jj] * qsi * sm.rki[j];
-                rsum += qk[jj];
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {  // in place: dm <- dMG, qk <- P1
+                    const int j = j0 + 8 * k + cq + (e & 1);
+                    const bool up = e & 2;
+                    const int r = up ? rb : ra;
+                    const float msk = ((up ? lb : la) && j <= r) ? 1.f : 0.f;
+                    dm[4 * k + e] *= msk * __expf(fminf((up ? Gb : Ga) - sm.G[j], 0.f));
+                    qk[4 * k + e] = dm[4 * k + e] * qk[4 * k + e] * (up ? qsb : qsa) * sm.rki[j];
+                    if (up) rsb += qk[4 * k + e]; else rsa += qk[4 * k + e];
+                }
+                pc[2 * k] = qk[4 * k] + qk[4 * k + 2];
+                pc[2 * k + 1] = qk[4 * k + 1] + qk[4 * k + 3];
+                const int j = j0 + 8 * k + cq;
+                const float r0 = sm.rki[j], r1 = sm.rki[j + 1];
+                put_pair(sm.op_dmg, ra, j, dm[4 * k] * r0, dm[4 * k + 1] * r1);
+                put_pair(sm.op_dmg, rb, j, dm[4 * k + 2] * r0, dm[4 * k + 3] * r1);
+                put_pair(sm.op_dmgt, ra, j, dm[4 * k] * qsa, dm[4 * k + 1] * qsa);
+                put_pair(sm.op_dmgt, rb, j, dm[4 * k + 2] * qsb, dm[4 * k + 3] * qsb);
             }
-            float s0, s1;
-            colsum16(qk, lane, s0, s1);
-            if (active) {
-                sm.cp[sub][j0 + 2 * lane] = s0;
-                sm.cp[sub][j0 + 2 * lane + 1] = s1;
-                sm.rp[grp][t] = rsum;
+            sm.cp[sub][j0 + colsum_frag_col(lane)] = colsum_frag(pc, lane);
+            rsa = quad_sum(rsa);
+            rsb = quad_sum(rsb);
+            if ((lane & 3) == 0) {
+                sm.rp[grp][ra] = rsa;
+                sm.rp[grp][rb] = rsb;
             }
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * sm.rki[j0 + jj];
-            if (active) put_row32(sm.op_dmg, t, j0, qk);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) qk[jj] = dm[jj] * qsi;
-            if (active) put_row32(sm.op_dmgt, t, j0, qk);
             // (b) dW = -Dw rows, this warpgroup's 64 columns
             const size_t o = ((size_t)(x.t0 + (live ? t : 0)) * a.HV + x.hv) * kDim;
 #pragma unroll
@@ -299,67 +313,50 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         phase ^= 1;
         tc_fence_after();
         if (!done) { ok = false; break; }
-        {  // dqhat, dkhat rows (this warpgroup's 64 columns) and the inter-term row dots
-            const float eg = live ? sm.eg[t] : 0.f, el = live ? sm.egl_g[t] : 0.f;
-            const size_t o = ((size_t)(x.t0 + (live ? t : 0)) * a.HV + x.hv) * kDim;
-            float xq = 0.f, xk = 0.f;
+        {  // dqhat, dkhat rows (this warpgroup's 64 columns) and the inter-term row dots,
+           // on 16x256b fragments (rows ra, rb; columns c0 + 8k + cq + {0, 1})
+            const float ega = la ? sm.eg[ra] : 0.f, egb = lb ? sm.eg[rb] : 0.f;
+            const float ela = la ? sm.egl_g[ra] : 0.f, elb = lb ? sm.egl_g[rb] : 0.f;
+            const size_t oa = ((size_t)(x.t0 + (la ? ra : 0)) * a.HV + x.hv) * kDim;
+            const size_t ob = ((size_t)(x.t0 + (lb ? rb : 0)) * a.HV + x.hv) * kDim;
+            float xqa = 0.f, xqb = 0.f, xka = 0.f, xkb = 0.f;
 #pragma unroll
-            for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
-                float dq[32], qi[32];
-                tmem_ld32(t_row + cDQ + cc * 32, dq);
-                tmem_ld32(t_row + cQI + cc * 32, qi);
-                tmem_ld_wait();
-                const unsigned char *qrow = sm.q + (cc >> 1) * kBox;
-                uint4 *qp = reinterpret_cast<uint4 *>(a.dqp + o + cc * 32);
+            for (int m = 0; m < 2; ++m) {  // m = 0: dq with q; m = 1: dk with k
+                const uint32_t cA = m ? cDK : cDQ, cB = m ? cKI : cQI;
+                const unsigned char *tile = m ? sm.k : sm.q;
+                bf16 *dst = m ? a.dkp : a.dqp;
+                const float fa = m ? ela : ega, fb = m ? elb : egb;
+                float xa = 0.f, xb = 0.f;
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per step
-                    const int col = (cc & 1) * 32 + q8 * 8;
-                    const uint4 qx = *reinterpret_cast<const uint4 *>(qrow + sw128_off(t, col));
-                    const __nv_bfloat162 *qb = reinterpret_cast<const __nv_bfloat162 *>(&qx);
-                    float v8[8];
+                for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
+                    const int c0 = 32 * cc;
+                    float dd[16], ii[16];
+                    tmem_ld16x256_x4(t_row + cA + c0, dd);
+                    tmem_ld16x256_x4(t_row + cB + c0, ii);
+                    tmem_ld_wait();
+                    const unsigned char *half = tile + (c0 >> 6) * kBox;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 qf = __bfloat1622float2(qb[e]);
-                        const float a0 = eg * dq[q8 * 8 + 2 * e], a1 = eg * dq[q8 * 8 + 2 * e + 1];
-                        xq += qf.x * a0 + qf.y * a1;
-                        v8[2 * e] = a0 + qi[q8 * 8 + 2 * e];
-                        v8[2 * e + 1] = a1 + qi[q8 * 8 + 2 * e + 1];
+                    for (int k = 0; k < 4; ++k) {
+                        const int col = (c0 & 63) + 8 * k + cq;  // within the 64-column half
+                        const float2 qa = get_pair(half, ra, col), qb = get_pair(half, rb, col);
+                        const float a0 = fa * dd[4 * k], a1 = fa * dd[4 * k + 1];
+                        const float b0 = fb * dd[4 * k + 2], b1 = fb * dd[4 * k + 3];
+                        xa += qa.x * a0 + qa.y * a1;
+                        xb += qb.x * b0 + qb.y * b1;
+                        const int gcol = c0 + 8 * k + cq;
+                        if (la)
+                            *reinterpret_cast<uint32_t *>(dst + oa + gcol) = pack_bf2(a0 + ii[4 * k], a1 + ii[4 * k + 1]);
+                        if (lb)
+                            *reinterpret_cast<uint32_t *>(dst + ob + gcol) = pack_bf2(b0 + ii[4 * k + 2], b1 + ii[4 * k + 3]);
                     }
-                    if (live)
-                        qp[q8] = make_uint4(pack_bf2(v8[0], v8[1]), pack_bf2(v8[2], v8[3]),
-                                            pack_bf2(v8[4], v8[5]), pack_bf2(v8[6], v8[7]));
                 }
+                if (m) { xka = xa; xkb = xb; } else { xqa = xa; xqb = xb; }
             }
-#pragma unroll
-            for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
-                float dk[32], ki[32];
-                tmem_ld32(t_row + cDK + cc * 32, dk);
-                tmem_ld32(t_row + cKI + cc * 32, ki);
-                tmem_ld_wait();
-                const unsigned char *krow = sm.k + (cc >> 1) * kBox;
-                uint4 *kp = reinterpret_cast<uint4 *>(a.dkp + o + cc * 32);
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    const int col = (cc & 1) * 32 + q8 * 8;
-                    const uint4 kx = *reinterpret_cast<const uint4 *>(krow + sw128_off(t, col));
-                    const __nv_bfloat162 *kb = reinterpret_cast<const __nv_bfloat162 *>(&kx);
-                    float v8[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 kf = __bfloat1622float2(kb[e]);
-                        const float a0 = el * dk[q8 * 8 + 2 * e], a1 = el * dk[q8 * 8 + 2 * e + 1];
-                        xk += kf.x * a0 + kf.y * a1;
-                        v8[2 * e] = a0 + ki[q8 * 8 + 2 * e];
-                        v8[2 * e + 1] = a1 + ki[q8 * 8 + 2 * e + 1];
-                    }
-                    if (live)
-                        kp[q8] = make_uint4(pack_bf2(v8[0], v8[1]), pack_bf2(v8[2], v8[3]),
-                                            pack_bf2(v8[4], v8[5]), pack_bf2(v8[6], v8[7]));
-                }
-            }
-            if (active) {
-                sm.pq[grp][t] = xq;
-                sm.pk[grp][t] = xk;
+            xqa = quad_sum(xqa); xqb = quad_sum(xqb);
+            xka = quad_sum(xka); xkb = quad_sum(xkb);
+            if ((lane & 3) == 0) {
+                sm.pq[grp][ra] = xqa; sm.pq[grp][rb] = xqb;
+                sm.pk[grp][ra] = xka; sm.pk[grp][rb] = xkb;
             }
         }
         tc_fence_before();

@@ -4,9 +4,9 @@
 // One CTA of 128 threads per (chunk, value head).  Both modes start from the
 // intra-chunk attention matrix
 //   M[t][j] = (qhat_t . khat_j) exp(G_t - G_j),  j <= t < L   (else 0)
-// formed by one product D1 = [K; Q] K^T (M=128 N=64 K=128: rows 64..127 are
-// Q K^T; rows 0..63, K K^T, are not used here) and scaled by
-// scale / (r_q,t r_k,j) in the epilogue.
+// formed by one product Q K^T (M=64 N=64 K=128) and scaled by
+// scale / (r_q,t r_k,j) in an epilogue that reads it as 16x256b fragments
+// (all four warps, two rows and eight columns per lane).
 //   forward : o^T[v][t] = c_t (h^T Q^T)[v][t] + (v_new^T M^T)[v][t],
 //             c_t = e^{G_t} scale / r_q,t            (o = diag(e^G) Qhat h + M v_new)
 //   backward: dv_loc^T[v][t] = (dO^T M)[v][t]        (dv_loc = M^T dO)
@@ -16,6 +16,7 @@
 #include <string.h>
 
 #include "gdn_kernels.h"
+#include "gdn_epi.cuh"
 #include "gdn_tma.h"
 #include "gdn_umma.cuh"
 
@@ -32,7 +33,7 @@ constexpr uint32_t kBig = 128 * 128;   // 128 rows x 128 B
 // CTAs share an SM (two in the forward mode).
 template <bool kForward>
 struct OutSmem {
-    unsigned char kq[2 * kBig];   // [K; Q] per k-half: K rows 0..63, Q rows 64..127
+    unsigned char kq[2 * kBig];   // [K; Q] per k-half: K rows 0..63, Q rows 64..127 (one TMA box each)
     unsigned char tv[2 * kBox];   // v_new (forward) or dO (backward) [t][v] per v-half
     unsigned char mm[kBox];       // M, row i at row i (bf16)
     unsigned char hc[kForward ? 2 * kBig : 16];   // h_c [k][v] per v-half (forward only)
@@ -45,11 +46,6 @@ struct OutSmem {
 struct OutMaps {
     CUtensorMap q, k, h, tv;
 };
-
-__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&t);
-}
 
 template <bool kForward>
 constexpr uint32_t kTmemCols = kForward ? 256 : 128;
@@ -87,7 +83,7 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
         tma_load_3d(sm.kq + kBig + kBox, &maps.q, 64, h, t0, &sm.tma_bar);
         tma_load_3d(sm.tv, &maps.tv, 0, hv, t0, &sm.tma_bar);
         tma_load_3d(sm.tv + kBox, &maps.tv, 64, hv, t0, &sm.tma_bar);
-        if (kForward) {
+        if constexpr (kForward) {
             const int row = (c * a.HV + hv) * 128;
             tma_load_3d(sm.hc, &maps.h, 0, 0, row, &sm.tma_bar);
             tma_load_3d(sm.hc + kBig, &maps.h, 64, 0, row, &sm.tma_bar);
@@ -107,39 +103,49 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
     uint32_t phase = 0;
-    // D1 = [K; Q] K^T
+    // QK = Q K^T (M=64; Q rows sit at kBox inside each k-half of the [K; Q] tile)
     if (tid == 0 && ok) {
         tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+        const uint32_t id = idesc_bf16(64, 64, 0, 0);
         const uint32_t as = smem_u32(sm.kq);
-        for (int s = 0; s < 8; ++s)
-            mma_bf16(tb, sdesc(as + (s >> 2) * kBig + (s & 3) * 32, 16, 1024),
-                     sdesc(as + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id, s > 0);
+        for (int s = 0; s < 8; ++s) {
+            const uint32_t off = (s >> 2) * kBig + (s & 3) * 32;
+            mma_bf16(tb, sdesc(as + kBox + off, 16, 1024), sdesc(as + off, 16, 1024), id, s > 0);
+        }
         mma_commit(&sm.mma_bar);
     }
     ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
     phase ^= 1;
     tc_fence_after();
-    if (ok && tid >= 64) {  // thread 64 + t: row t of Q K^T  ->  M row t
-        const int t = tid - 64;
-        float r[32];
-        for (int half = 0; half < 2; ++half) {
-            tmem_ld32(t_row + half * 32, r);
+    if (ok) {  // M from 16x256b fragments of QK: rows ra, rb = ra + 8 of warp w's block,
+               // columns 32 c + 8k + cq + {0, 1}
+        const int lane = tid & 31;
+        const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+        const float qa = sm.qsc[ra], qb = sm.qsc[rb], Ga = sm.G[ra], Gb = sm.G[rb];
+        const bool la = ra < L, lb = rb < L;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float r[16];
+            epi::tmem_ld16x256_x4(t_row + 32 * c, r);
             tmem_ld_wait();
-            float m[32];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = half * 32 + jj;
-                const float msk = (j <= t && t < L) ? 1.f : 0.f;
-                m[jj] = msk * r[jj] * sm.qsc[t] * sm.rki[j] * __expf(fminf(sm.G[t] - sm.G[j], 0.f));
+            for (int k = 0; k < 4; ++k) {
+                const int j = 32 * c + 8 * k + cq;
+                float m[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = j + (e & 1);
+                    const bool up = e & 2;
+                    const int row = up ? rb : ra;
+                    const float msk = (jj <= row && (up ? lb : la)) ? 1.f : 0.f;
+                    m[e] = msk * r[4 * k + e] * (up ? qb : qa) * sm.rki[jj] *
+                           __expf(fminf((up ? Gb : Ga) - sm.G[jj], 0.f));
+                }
+                // row t of M at row t: the forward reads it as K-major [t][j] (B = M^T
+                // operand of v_new^T M^T), the backward as MN-major [j][t] (B = M of dO^T M)
+                epi::put_pair(sm.mm, ra, j, m[0], m[1]);
+                epi::put_pair(sm.mm, rb, j, m[2], m[3]);
             }
-            // row t of M at row t: the forward reads it as K-major [t][j] (B = M^T
-            // operand of v_new^T M^T), the backward as MN-major [j][t] (B = M of dO^T M)
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4 *>(sm.mm + sw128_off(t, half * 32 + q * 8)) =
-                    make_uint4(pack_bf2(m[q * 8 + 0], m[q * 8 + 1]), pack_bf2(m[q * 8 + 2], m[q * 8 + 3]),
-                               pack_bf2(m[q * 8 + 4], m[q * 8 + 5]), pack_bf2(m[q * 8 + 6], m[q * 8 + 7]));
         }
     }
     fence_proxy_async_smem();

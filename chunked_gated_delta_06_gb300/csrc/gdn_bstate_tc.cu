@@ -11,9 +11,9 @@
 //   1. thread k writes row k of dh' as bf16 to shared memory (copied to
 //      dh_c[chunk][hv][k][v'] by one TMA store), then dh <- e^{G_L} dh';
 //   2. Pd[t][v'] = sum_k K[t][k] dh'[k][v']          (M=64 N=64 K=128)
-//   3. thread t forms whole rows dv_new[t][v'] = dv_loc + e^{G_L-G_t}/r_k,t Pd
-//      (to HBM, bf16) and the operands c_t dO[t][v'] and -dv_new[t][v'],
-//      c_t = e^{G_t} scale / r_q,t;
+//   3. on 16x256b fragments of Pd (two token rows and eight columns per lane):
+//      dv_new[t][v'] = dv_loc + e^{G_L-G_t}/r_k,t Pd (to HBM, bf16) and the
+//      operands c_t dO[t][v'] and -dv_new[t][v'], c_t = e^{G_t} scale / r_q,t;
 //   4. dh += Q^T (c dO) - w^T dv_new                  (two M=128 N=64 K=64
 //      products; Q and w are raw tiles read MN-major)
 // which is dh <- e^{G_L} dh' + Qtil^T dO - w^T dv_new and dv_new = dv_loc +
@@ -26,6 +26,7 @@
 // Waits are bounded.
 #include <string.h>
 
+#include "gdn_epi.cuh"
 #include "gdn_kernels.h"
 #include "gdn_tma.h"
 #include "gdn_umma.cuh"
@@ -107,8 +108,6 @@ __global__ void __launch_bounds__(kThr, 2)
     const int nch = max(ce - cb, 0);
     const int grp = warp >> 2, sub = warp & 3;
     const int kr = sub * 32 + lane;     // state row (TMEM lane) of step 1
-    const int tr = sub * 16 + lane;     // token row of steps 2-3 (lanes 0..15)
-    const bool trow = lane < 16;
     const int c0 = 32 * grp;            // this warpgroup's 32 of the 64 columns
     // the sequence's chunks are consecutive 64-token blocks of [ts0, ts1); the
     // i-th step of the reverse walk handles block nch - 1 - i
@@ -230,21 +229,18 @@ __global__ void __launch_bounds__(kThr, 2)
             tma_store_3d(&maps.dhc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_ds);  // dh_c rows (k)
             tma_store_commit();
         }
-        // meanwhile: row tr of c_t dO (this warpgroup's 32 columns)
-        if (trow) {
-            const float qc = sm.qc[i & 1][tr];
+        // meanwhile: c_t dO on the fragment positions used below (rows ra, ra + 8,
+        // columns c0 + 8k + cq + {0, 1})
+        const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+        {
+            const float qa = sm.qc[i & 1][ra], qb = sm.qc[i & 1][rb];
             const unsigned char *dos = sm.x + 2 * kBox;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 dx = *reinterpret_cast<const uint4 *>(dos + sw128_off(tr, c0 + 8 * q));
-                const __nv_bfloat162 *db = reinterpret_cast<const __nv_bfloat162 *>(&dx);
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(db[e]);
-                    pk[e] = pack_bf2(f.x * qc, f.y * qc);
-                }
-                *reinterpret_cast<uint4 *>(sm.a_do + sw128_off(tr, c0 + 8 * q)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int k = 0; k < 4; ++k) {
+                const int col = c0 + 8 * k + cq;
+                const float2 fa = epi::get_pair(dos, ra, col), fb = epi::get_pair(dos, rb, col);
+                epi::put_pair(sm.a_do, ra, col, fa.x * qa, fa.y * qa);
+                epi::put_pair(sm.a_do, rb, col, fb.x * qb, fb.y * qb);
             }
         }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
@@ -254,35 +250,26 @@ __global__ void __launch_bounds__(kThr, 2)
             issue_xk(maps, sm, step_t0(i + 1), h);
             ++xk_issued;
         }
-        // 3. dv_new = dv_loc + kc_t Pd, row tr
+        // 3. dv_new = dv_loc + kc_t Pd on 16x256b fragments
         {
-            float p[32];
-            tmem_ld32(tP, p);
+            float p[16];
+            epi::tmem_ld16x256_x4(tP, p);
             tmem_ld_wait();
-            if (trow) {
-                const bool live = tr < L;
-                const float kc = sm.kc[i & 1][tr];
-                const unsigned char *dls = sm.x + 3 * kBox;
-                uint4 *dst = reinterpret_cast<uint4 *>(
-                    a.dvnew + ((size_t)(t0 + (live ? tr : 0)) * a.HV + hv) * kDim + 64 * vb + c0);
+            const bool la = ra < L, lb = rb < L;
+            const float ka = sm.kc[i & 1][ra], kb = sm.kc[i & 1][rb];
+            const unsigned char *dls = sm.x + 3 * kBox;
+            bf16 *da = a.dvnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
+            bf16 *db = a.dvnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 lx = *reinterpret_cast<const uint4 *>(dls + sw128_off(tr, c0 + 8 * q));
-                    const __nv_bfloat162 *lb = reinterpret_cast<const __nv_bfloat162 *>(&lx);
-                    float dv[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 lf = __bfloat1622float2(lb[e]);
-                        dv[2 * e] = live ? lf.x + kc * p[8 * q + 2 * e] : 0.f;
-                        dv[2 * e + 1] = live ? lf.y + kc * p[8 * q + 2 * e + 1] : 0.f;
-                    }
-                    if (live)
-                        dst[q] = make_uint4(pack_bf2(dv[0], dv[1]), pack_bf2(dv[2], dv[3]),
-                                            pack_bf2(dv[4], dv[5]), pack_bf2(dv[6], dv[7]));
-                    *reinterpret_cast<uint4 *>(sm.a_dv + sw128_off(tr, c0 + 8 * q)) =
-                        make_uint4(pack_bf2(-dv[0], -dv[1]), pack_bf2(-dv[2], -dv[3]),
-                                   pack_bf2(-dv[4], -dv[5]), pack_bf2(-dv[6], -dv[7]));
-                }
+            for (int k = 0; k < 4; ++k) {
+                const int col = c0 + 8 * k + cq;
+                const float2 la2 = epi::get_pair(dls, ra, col), lb2 = epi::get_pair(dls, rb, col);
+                const float va0 = la ? la2.x + ka * p[4 * k] : 0.f, va1 = la ? la2.y + ka * p[4 * k + 1] : 0.f;
+                const float vb0 = lb ? lb2.x + kb * p[4 * k + 2] : 0.f, vb1 = lb ? lb2.y + kb * p[4 * k + 3] : 0.f;
+                if (la) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                if (lb) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                epi::put_pair(sm.a_dv, ra, col, -va0, -va1);
+                epi::put_pair(sm.a_dv, rb, col, -vb0, -vb1);
             }
         }
         float egl_next = egl;

@@ -12,9 +12,9 @@
 //   1. thread k writes row k of h as bf16 to shared memory (MMA operand; one TMA
 //      store copies it to h_c[chunk][hv][k][v']), and e^{G_L} h back to TMEM;
 //   2. P[t][v'] = sum_k w[t][k] h[k][v']          (tcgen05, M=64 N=64 K=128)
-//   3. thread t (TMEM lane 32 (t / 16) + t % 16) forms v_new[t][v'] = u - P as
-//      whole rows: to HBM (bf16), and A_V[t][v'] = v_new e^{G_L - G_t} / r_k,t
-//      (bf16, shared memory);
+//   3. the result is read as 16x256b fragments (two token rows and eight columns
+//      per lane); v_new[t][v'] = u - P goes to HBM (bf16), and
+//      A_V[t][v'] = v_new e^{G_L - G_t} / r_k,t to shared memory (bf16);
 //   4. h[k][v'] += sum_t K[t][k] A_V[t][v']        (tcgen05, M=128 N=64 K=64; the
 //      raw key tile is read MN-major)
 // which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with Khat =
@@ -25,6 +25,7 @@
 // unwinds.
 #include <string.h>
 
+#include "gdn_epi.cuh"
 #include "gdn_kernels.h"
 #include "gdn_tma.h"
 #include "gdn_umma.cuh"
@@ -83,8 +84,6 @@ __global__ void __launch_bounds__(kThr, 2)
     const int nch = max(ce - cb, 0);
     const int grp = warp >> 2, sub = warp & 3;
     const int kr = sub * 32 + lane;     // state row (TMEM lane) of the state pass
-    const int tr = sub * 16 + lane;     // token row of the epilogue (lanes 0..15)
-    const bool trow = lane < 16;
     const int c0 = 32 * grp;            // this warpgroup's 32 of the 64 columns
     // the sequence's chunks are consecutive 64-token blocks of [ts0, ts1)
     const int ts0 = nch > 0 ? a.chunk_start[cb] : 0;
@@ -197,35 +196,28 @@ __global__ void __launch_bounds__(kThr, 2)
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
-        // 3. v_new = u - P: row tr, this warpgroup's 32 columns
+        // 3. v_new = u - P on 16x256b fragments: rows ra, ra + 8, this warpgroup's
+        //    columns c0 + 8k + cq + {0, 1}
         {
-            float p[32];
-            tmem_ld32(tP, p);
+            float p[16];
+            epi::tmem_ld16x256_x4(tP, p);
             tmem_ld_wait();
-            if (trow) {
-                const bool live = tr < L;
-                const float cf = sm.coef[i & 1][tr];
-                const unsigned char *us = sm.stage[st] + 4 * kBox;
-                uint4 *dst = reinterpret_cast<uint4 *>(
-                    a.vnew + ((size_t)(t0 + (live ? tr : 0)) * a.HV + hv) * kDim + 64 * vb + c0);
+            const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+            const bool la = ra < L, lb = rb < L;
+            const float cfa = sm.coef[i & 1][ra], cfb = sm.coef[i & 1][rb];
+            const unsigned char *us = sm.stage[st] + 4 * kBox;
+            bf16 *da = a.vnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
+            bf16 *db = a.vnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 ux = *reinterpret_cast<const uint4 *>(us + sw128_off(tr, c0 + 8 * q));
-                    const __nv_bfloat162 *ub = reinterpret_cast<const __nv_bfloat162 *>(&ux);
-                    float vn[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 uf = __bfloat1622float2(ub[e]);
-                        vn[2 * e] = live ? uf.x - p[8 * q + 2 * e] : 0.f;
-                        vn[2 * e + 1] = live ? uf.y - p[8 * q + 2 * e + 1] : 0.f;
-                    }
-                    if (live)
-                        dst[q] = make_uint4(pack_bf2(vn[0], vn[1]), pack_bf2(vn[2], vn[3]),
-                                            pack_bf2(vn[4], vn[5]), pack_bf2(vn[6], vn[7]));
-                    *reinterpret_cast<uint4 *>(sm.a_v + sw128_off(tr, c0 + 8 * q)) =
-                        make_uint4(pack_bf2(vn[0] * cf, vn[1] * cf), pack_bf2(vn[2] * cf, vn[3] * cf),
-                                   pack_bf2(vn[4] * cf, vn[5] * cf), pack_bf2(vn[6] * cf, vn[7] * cf));
-                }
+            for (int k = 0; k < 4; ++k) {
+                const int col = c0 + 8 * k + cq;
+                const float2 ua = epi::get_pair(us, ra, col), ub = epi::get_pair(us, rb, col);
+                const float va0 = la ? ua.x - p[4 * k] : 0.f, va1 = la ? ua.y - p[4 * k + 1] : 0.f;
+                const float vb0 = lb ? ub.x - p[4 * k + 2] : 0.f, vb1 = lb ? ub.y - p[4 * k + 3] : 0.f;
+                if (la) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                if (lb) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                epi::put_pair(sm.a_v, ra, col, va0 * cfa, va1 * cfa);
+                epi::put_pair(sm.a_v, rb, col, vb0 * cfb, vb1 * cfb);
             }
         }
         float egl_next = egl;

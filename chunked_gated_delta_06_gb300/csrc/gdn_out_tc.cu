@@ -7,12 +7,12 @@
 // formed by one product Q K^T (M=64 N=64 K=128) and scaled by
 // scale / (r_q,t r_k,j) in an epilogue that reads it as 16x256b fragments
 // (all four warps, two rows and eight columns per lane).
-//   forward : o^T[v][t] = c_t (h^T Q^T)[v][t] + (v_new^T M^T)[v][t],
+//   forward : o[t][v] = c_t (Q h)[t][v] + (M v_new)[t][v],
 //             c_t = e^{G_t} scale / r_q,t            (o = diag(e^G) Qhat h + M v_new)
-//   backward: dv_loc^T[v][t] = (dO^T M)[v][t]        (dv_loc = M^T dO)
-// h_c [k][v], v_new and dO are read as MN-major operands straight from their TMA
-// tiles; thread v owns row v of the results and writes o[t][hv][v] /
-// dv_loc[t][hv][v] with coalesced stores.
+//   backward: dv_loc[t][v] = (M^T dO)[t][v]
+// as token-row products (M=64, N=128); h_c [k][v], v_new and dO are read as
+// MN-major operands straight from their TMA tiles, and the results are read as
+// 16x256b fragments so that every lane writes bf16 pairs of two token rows.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -151,50 +151,57 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ok) {
+    if (tid == 0 && ok) {  // token-row products (M=64, N=128), rows t of the results
         tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 1, 0);    // A MN-major, B K-major
         const uint32_t tvs = smem_u32(sm.tv), mms = smem_u32(sm.mm);
-        if (kForward) {
-            // O1 = h^T Q^T : A = h_c [k][v] (MN-major, v halves 16 KB apart), B = Q [t][k] (K-major)
-            const uint32_t id1 = idesc_bf16(128, 64, 1, 0);
+        if constexpr (kForward) {
+            // O1 = Q h : A = Q [t][k] (K-major), B = h_c [k][v] (MN-major, v halves 16 KB apart)
+            const uint32_t id1 = idesc_bf16(64, 128, 0, 1);
             const uint32_t hs = smem_u32(sm.hc), qs = smem_u32(sm.kq + kBox);
             for (int s = 0; s < 8; ++s)
-                mma_bf16(tb + 64, sdesc(hs + s * 2048, kBig, 1024),
-                         sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), id1, s > 0);
-            // O2 = v_new^T M^T : A = v_new [j][v] (MN-major, v atoms 8 KB apart), B = M [t][j]
+                mma_bf16(tb, sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), sdesc(hs + s * 2048, kBig, 1024),
+                         id1, s > 0);
+            // O2 = M v_new : A = M [t][j] (K-major), B = v_new [j][v] (MN-major, v halves 8 KB apart)
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tb + 128, sdesc(tvs + s * 2048, kBox, 1024), sdesc(mms + s * 32, 16, 1024), id,
-                         s > 0);
+                mma_bf16(tb + 128, sdesc(mms + s * 32, 16, 1024), sdesc(tvs + s * 2048, kBox, 1024), id1, s > 0);
         } else {
-            // DL = dO^T M : A = dO [j][v] (MN-major), B = M [j][t] (MN-major)
-            const uint32_t id2 = idesc_bf16(128, 64, 1, 1);
+            // DL = M^T dO : A = M [j][t] (MN-major), B = dO [j][v] (MN-major)
+            const uint32_t id2 = idesc_bf16(64, 128, 1, 1);
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tb + 64, sdesc(tvs + s * 2048, kBox, 1024), sdesc(mms + s * 2048, kBox, 1024),
-                         id2, s > 0);
+                mma_bf16(tb, sdesc(mms + s * 2048, kBox, 1024), sdesc(tvs + s * 2048, kBox, 1024), id2, s > 0);
         }
         mma_commit(&sm.mma_bar);
     }
     ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
     tc_fence_after();
-    if (ok) {
-        const int v = tid;
-        for (int half = 0; half < 2; ++half) {
-            float r1[32], r2[32];
-            tmem_ld32(t_row + 64 + half * 32, r1);
-            if (kForward) tmem_ld32(t_row + 128 + half * 32, r2);
+    if (ok) {  // 16x256b fragments: rows ra, ra + 8, columns v = 32 c + 8k + cq + {0, 1}
+        const int lane = tid & 31;
+        const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+        const bool la = ra < L, lb = rb < L;
+        const float ca = sm.ct[ra], cb = sm.ct[rb];
+        bf16 *dst = kForward ? a.o : a.dvloc;
+        bf16 *da = dst + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim;
+        bf16 *db = dst + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float r1[16], r2[16];
+            epi::tmem_ld16x256_x4(t_row + 32 * c, r1);
+            if constexpr (kForward) epi::tmem_ld16x256_x4(t_row + 128 + 32 * c, r2);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = half * 32 + j;
-                if (t < L) {
-                    const size_t o = ((size_t)(t0 + t) * a.HV + hv) * kDim + v;
-                    if (kForward) {
-                        a.o[o] = f2bf(sm.ct[t] * r1[j] + r2[j]);
-                    } else {
-                        a.dvloc[o] = f2bf(r1[j]);
-                    }
+            for (int k = 0; k < 4; ++k) {
+                const int v = 32 * c + 8 * k + cq;
+                float x0, x1, y0, y1;
+                if constexpr (kForward) {
+                    x0 = ca * r1[4 * k] + r2[4 * k];
+                    x1 = ca * r1[4 * k + 1] + r2[4 * k + 1];
+                    y0 = cb * r1[4 * k + 2] + r2[4 * k + 2];
+                    y1 = cb * r1[4 * k + 3] + r2[4 * k + 3];
+                } else {
+                    x0 = r1[4 * k]; x1 = r1[4 * k + 1]; y0 = r1[4 * k + 2]; y1 = r1[4 * k + 3];
                 }
+                if (la) *reinterpret_cast<uint32_t *>(da + v) = epi::pack_bf2(x0, x1);
+                if (lb) *reinterpret_cast<uint32_t *>(db + v) = epi::pack_bf2(y0, y1);
             }
         }
     } else if (tid == 0 && a.status) {

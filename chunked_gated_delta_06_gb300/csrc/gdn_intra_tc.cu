@@ -8,6 +8,7 @@
 // chain of short dependent steps, and co-resident CTAs hide one another's
 // latencies.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
 //   KK = K K^T                                   (tcgen05, M=64 N=64 K=128)
+// The M=64 KK result is read as 16x256b fragments (two rows, eight columns per lane).
 //   A  = strict_tril(diag(beta) KKhat (.) Gamma) (CUDA cores, fp32)
 //   T  = (I + A)^-1                              (fp32, in place over A:
 //        16x16 diagonal blocks by substitution, then T21 = -T22 (A21 T11) at
@@ -19,6 +20,7 @@
 // w, u and T (kept for the backward) go to HBM in bf16.
 #include <string.h>
 
+#include "gdn_epi.cuh"
 #include "gdn_kernels.h"
 #include "gdn_tma.h"
 #include "gdn_umma.cuh"
@@ -196,36 +198,27 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
     }
     ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, 0));
     tc_fence_after();
-    if (ok) {  // A row i = 16 warp + lane (lanes 0..15): zeros on and above the diagonal
-        float k0[32], k1[32];
-        tmem_ld32(t_row, k0);
-        tmem_ld32(t_row + 32, k1);
-        tmem_ld_wait();
-        if (lane < 16) {
-            const int i = 16 * warp + lane;
-            const float Gi = sm.G[i], ai = sm.beta[i] * sm.rki[i];
-            float *Mi = sm.M + i * kS;
+    if (ok) {  // A from 16x256b fragments of KK: rows ra, ra + 8 of the warp's block, columns
+               // 32 c + 8k + cq + {0, 1}; zeros on and above the diagonal
+        const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+        const float Ga = sm.G[ra], Gb = sm.G[rb];
+        const float aa = sm.beta[ra] * sm.rki[ra], ab = sm.beta[rb] * sm.rki[rb];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float e[4];
+        for (int c = 0; c < 2; ++c) {
+            float kk[16];
+            epi::tmem_ld16x256_x4(t_row + 32 * c, kk);
+            tmem_ld_wait();
 #pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    const int j = 4 * q + z;
-                    const float msk = j < i ? 1.f : 0.f;
-                    e[z] = msk * ai * k0[j] * sm.rki[j] * __expf(fminf(Gi - sm.G[j], 0.f));
-                }
-                *reinterpret_cast<float4 *>(Mi + 4 * q) = make_float4(e[0], e[1], e[2], e[3]);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float e[4];
-#pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    const int j = 32 + 4 * q + z;
-                    const float msk = j < i ? 1.f : 0.f;
-                    e[z] = msk * ai * k1[4 * q + z] * sm.rki[j] * __expf(fminf(Gi - sm.G[j], 0.f));
-                }
-                *reinterpret_cast<float4 *>(Mi + 32 + 4 * q) = make_float4(e[0], e[1], e[2], e[3]);
+            for (int k = 0; k < 4; ++k) {
+                const int j = 32 * c + 8 * k + cq;
+                const float r0 = sm.rki[j], r1 = sm.rki[j + 1];
+                const float g0 = sm.G[j], g1 = sm.G[j + 1];
+                const float e0 = (j < ra ? aa : 0.f) * kk[4 * k] * r0 * __expf(fminf(Ga - g0, 0.f));
+                const float e1 = (j + 1 < ra ? aa : 0.f) * kk[4 * k + 1] * r1 * __expf(fminf(Ga - g1, 0.f));
+                const float f0 = (j < rb ? ab : 0.f) * kk[4 * k + 2] * r0 * __expf(fminf(Gb - g0, 0.f));
+                const float f1 = (j + 1 < rb ? ab : 0.f) * kk[4 * k + 3] * r1 * __expf(fminf(Gb - g1, 0.f));
+                *reinterpret_cast<float2 *>(sm.M + ra * kS + j) = make_float2(e0, e1);
+                *reinterpret_cast<float2 *>(sm.M + rb * kS + j) = make_float2(f0, f1);
             }
         }
     }

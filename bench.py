@@ -189,41 +189,61 @@ def _bf(torch, bits, dev):
     return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
 
 
-class ChunkRunner:
-    """Device buffers of one chunk workload and one fwd+bwd step through the C ABI."""
+# training-step variants ("[Cake 1/13] gdn: chunked gated delta rule, det and fast, with
+# KCP and FLA-CP", Performance (3/5): fwd+bwd = one training step; ckpt = forward,
+# recomputed forward and backward of a checkpointed step; the recompute-state option
+# of API and flags rebuilds w, u, h and v_new inside the backward)
+STEP_MODES = {
+    "saved": "gdn_chunk_fwd (saving for backward) + gdn_chunk_bwd",
+    "recompute": "gdn_chunk_fwd (no saved buffer) + gdn_chunk_bwd in recompute-state mode",
+    "ckpt": "gdn_chunk_fwd (no saved buffer) + gdn_chunk_fwd (saving) + gdn_chunk_bwd",
+}
 
-    def __init__(self, torch, wl, dev):
+
+class ChunkRunner:
+    """Device buffers of one chunk workload and one training step through the C ABI
+    (mode: a key of STEP_MODES; beta in fp32 when the workload carries fp32 beta)."""
+
+    def __init__(self, torch, wl, dev, mode="saved"):
         import chunked_gated_delta_06_gb300 as gdn
-        self.torch, self.gdn, self.wl, self.dev = torch, gdn, wl, dev
+        self.torch, self.gdn, self.wl, self.dev, self.mode = torch, gdn, wl, dev, mode
         T, H, HV, N = wl.T, wl.H, wl.HV, wl.N
         self.q, self.k, self.v = _bf(torch, wl.q_bits, dev), _bf(torch, wl.k_bits, dev), _bf(torch, wl.v_bits, dev)
         self.g = torch.from_numpy(wl.g).to(dev)
-        self.beta = _bf(torch, wl.beta_bits, dev)
+        f32 = wl.beta_f32 is not None
+        self.beta = torch.from_numpy(wl.beta_f32).to(dev) if f32 else _bf(torch, wl.beta_bits, dev)
         self.h0 = None if wl.h0 is None else torch.from_numpy(wl.h0).to(dev)
         self.d_o = _bf(torch, wl.do_bits, dev)
         self.d_ht = None if wl.d_ht is None else torch.from_numpy(wl.d_ht).to(dev)
         self.cu_dev = torch.from_numpy(wl.cu_seqlens).to(dev)
-        self.p, self._keep = gdn.make_problem(wl.cu_seqlens, H, HV, cu_dev_ptr=self.cu_dev.data_ptr())
+        self.p, self._keep = gdn.make_problem(wl.cu_seqlens, H, HV, cu_dev_ptr=self.cu_dev.data_ptr(),
+                                              beta_dtype=gdn.GDN_DTYPE_F32 if f32 else gdn.GDN_DTYPE_BF16)
         e = lambda *s, dt=torch.float32: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
         self.o = e(T, HV, D, dt=torch.bfloat16)
         self.ht = e(N, HV, D, D)
-        self.saved = e(gdn.gdn_chunk_saved_bytes(self.p), dt=torch.uint8)
+        self.saved = None if mode == "recompute" else e(gdn.gdn_chunk_saved_bytes(self.p), dt=torch.uint8)
         self.ws_f = e(gdn.gdn_chunk_workspace_bytes(self.p, 0), dt=torch.uint8)
-        self.ws_b = e(gdn.gdn_chunk_workspace_bytes(self.p, 1), dt=torch.uint8)
+        self.ws_b = e(gdn.gdn_chunk_workspace_bytes(self.p, 2 if mode == "recompute" else 1), dt=torch.uint8)
         self.dq, self.dk = torch.empty_like(self.q), torch.empty_like(self.k)
         self.dv = torch.empty_like(self.v)
         self.dg = e(T, HV)
-        self.dbeta = e(T, HV, dt=torch.bfloat16)
+        self.dbeta = e(T, HV, dt=torch.float32 if f32 else torch.bfloat16)
         self.dh0 = e(N, HV, D, D)
+
+    def _fwd(self, saved, s, timer):
+        gdn, P = self.gdn, lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        st = gdn.gdn_chunk_fwd(self.p, P(self.q), P(self.k), P(self.v), P(self.g), P(self.beta),
+                               P(self.h0), P(self.o), P(self.ht), P(saved), P(self.ws_f),
+                               self.ws_f.numel(), s, timer)
+        if st:
+            raise gdn.GdnError(st, "gdn_chunk_fwd")
 
     def step(self, timer=None, stream=None):
         gdn, P = self.gdn, lambda t: None if t is None else t.data_ptr()  # noqa: E731
         s = (stream or self.torch.cuda.current_stream()).cuda_stream
-        st = gdn.gdn_chunk_fwd(self.p, P(self.q), P(self.k), P(self.v), P(self.g), P(self.beta),
-                               P(self.h0), P(self.o), P(self.ht), P(self.saved), P(self.ws_f),
-                               self.ws_f.numel(), s, timer)
-        if st:
-            raise gdn.GdnError(st, "gdn_chunk_fwd")
+        if self.mode == "ckpt":
+            self._fwd(None, s, timer)  # the forward of the checkpointed step keeps nothing
+        self._fwd(self.saved, s, timer)
         st = gdn.gdn_chunk_bwd(self.p, P(self.q), P(self.k), P(self.v), P(self.g), P(self.beta),
                                P(self.h0), P(self.saved), P(self.d_o), P(self.d_ht), P(self.dq),
                                P(self.dk), P(self.dv), P(self.dg), P(self.dbeta), P(self.dh0),
@@ -414,6 +434,25 @@ def bench_ours(args):
             "roofline": roof, "kernels": ktab, "gpu_launches": launches_per_step * args.steps,
             "clocks": clk}
 
+    # the other training-step forms on the same workload: recompute-state mode,
+    # the checkpointed step, and fp32 beta (same kernels; device-timed like value)
+    if not args.no_variants:
+        vsteps = max(3, min(args.steps, 10))
+        variants = {}
+        for name, vwl, mode in (("recompute", wl, "recompute"), ("ckpt", wl, "ckpt"),
+                                ("beta_f32", W.with_fp32_beta(wl), "saved")):
+            vr = ChunkRunner(torch, vwl, dev, mode=mode)
+            for _ in range(max(2, min(args.warmup, 3))):
+                vr.step()
+            barrier()
+            vms, _ = aggregate_over_ranks(_time_loop(torch, vr.step, vsteps), T)
+            barrier()
+            variants[name] = {"value": total_tokens / (vms / 1e3), "unit": "tokens/s",
+                              "ms_per_step": vms, "steps": vsteps, "step": STEP_MODES[mode],
+                              "beta": "fp32" if vwl.beta_f32 is not None else "bf16"}
+            del vr
+        line["variants"] = variants
+
     # decode state bandwidth
     if not args.no_decode:
         dw = W.decode_workload(seed=rank)
@@ -533,6 +572,8 @@ def main():
                     help="chunk workload of the fwd+bwd step (the headline is fb_32k_varlen)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the recompute-state, checkpointed-step and fp32-beta timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=2048,
                     help="tokens of the workload the oracle runs per baseline sample")

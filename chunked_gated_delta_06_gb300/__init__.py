@@ -6,7 +6,8 @@ include/gdn.h) with a thin ctypes binding.
 The library is loaded on first use; it must have been built with
 ``python -m chunked_gated_delta_06_gb300.build``.
 """
-from .binding import (GdnError, GdnProblem, chunk_bwd, chunk_fwd, decode_step,  # noqa: F401
+from .binding import (GDN_DTYPE_BF16, GDN_DTYPE_F32, GdnError, GdnProblem,  # noqa: F401
+                      chunk_bwd, chunk_fwd, decode_step,
                       gdn_chunk_bwd, gdn_chunk_fwd, gdn_chunk_saved_bytes,
                       gdn_chunk_workspace_bytes, gdn_decode_step, lib, make_problem,
                       status_string)

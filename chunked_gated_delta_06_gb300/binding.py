@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libgdn.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "gdn.h")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE_TOO_SMALL, GDN_ERR_CUDA = range(5)
+GDN_DTYPE_BF16, GDN_DTYPE_F32 = 0, 1
 
 
 class GdnError(RuntimeError):
@@ -48,6 +49,7 @@ class GdnProblem(ctypes.Structure):
         ("head_dim_k", ctypes.c_int32),
         ("head_dim_v", ctypes.c_int32),
         ("scale", ctypes.c_float),
+        ("beta_dtype", ctypes.c_int32),
         ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
         ("cu_seqlens_dev", ctypes.c_void_p),
     ]
@@ -140,7 +142,7 @@ class KernelTimer:
 
 
 # ----------------------------------------------------------------------------- raw entry points
-def make_problem(cu_host, H, HV, K=128, V=128, scale=0.0, cu_dev_ptr=0):
+def make_problem(cu_host, H, HV, K=128, V=128, scale=0.0, cu_dev_ptr=0, beta_dtype=GDN_DTYPE_BF16):
     """Build a GdnProblem; returns (problem, keepalive) -- keep both alive during the call."""
     cu = np.ascontiguousarray(np.asarray(cu_host, dtype=np.int32))
     p = GdnProblem()
@@ -148,6 +150,7 @@ def make_problem(cu_host, H, HV, K=128, V=128, scale=0.0, cu_dev_ptr=0):
     p.total_tokens = int(cu[-1]) if len(cu) else 0
     p.num_k_heads, p.num_v_heads, p.head_dim_k, p.head_dim_v = H, HV, K, V
     p.scale = float(scale)
+    p.beta_dtype = int(beta_dtype)
     p.cu_seqlens_host = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if len(cu) else None
     p.cu_seqlens_dev = cu_dev_ptr or None
     return p, cu
@@ -213,15 +216,27 @@ def _check(st, where):
         raise GdnError(st, where)
 
 
-class ChunkContext:
-    """Problem description plus the saved buffer of one forward (for the backward)."""
+def beta_dtype_of(beta):
+    """GDN_DTYPE_* of a torch beta tensor (bf16 or fp32)."""
+    import torch
+    if beta.dtype == torch.bfloat16:
+        return GDN_DTYPE_BF16
+    if beta.dtype == torch.float32:
+        return GDN_DTYPE_F32
+    raise TypeError("beta must be bfloat16 or float32, not %s" % beta.dtype)
 
-    def __init__(self, cu_host, cu_dev, H, HV, scale):
+
+class ChunkContext:
+    """Problem description plus the saved buffer of one forward (for the backward);
+    saved stays None after a forward without for_backward, and the backward then
+    runs in recompute-state mode."""
+
+    def __init__(self, cu_host, cu_dev, H, HV, scale, beta_dtype=GDN_DTYPE_BF16):
         self.cu_host = np.ascontiguousarray(np.asarray(cu_host, dtype=np.int32))
         self.cu_dev = cu_dev
         self.H, self.HV, self.scale = H, HV, scale
         self.problem, self._keep = make_problem(self.cu_host, H, HV, scale=scale or 0.0,
-                                                cu_dev_ptr=cu_dev.data_ptr())
+                                                cu_dev_ptr=cu_dev.data_ptr(), beta_dtype=beta_dtype)
         self.saved = None
 
 
@@ -231,7 +246,7 @@ def chunk_fwd(q, k, v, g, beta, cu_host, cu_dev, scale=None, initial_state=None,
     import torch
     T, H, K = q.shape
     HV = v.shape[1]
-    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale)
+    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale, beta_dtype_of(beta))
     p = ctx.problem
     N = p.num_seqs
     dev = q.device
@@ -256,7 +271,9 @@ def chunk_fwd(q, k, v, g, beta, cu_host, cu_dev, scale=None, initial_state=None,
 
 def chunk_bwd(ctx, q, k, v, g, beta, d_o, d_final_state=None, initial_state=None,
               want_dh0=True, workspace=None):
-    """gdn_chunk_bwd on torch tensors.  Returns dict dq, dk, dv, dg, dbeta, dh0."""
+    """gdn_chunk_bwd on torch tensors.  Returns dict dq, dk, dv, dg, dbeta, dh0.
+    Without a saved buffer in ctx (forward run without for_backward) this is the
+    recompute-state mode: the call rebuilds the forward's tensors itself."""
     import torch
     T, H, K = q.shape
     HV = v.shape[1]
@@ -268,7 +285,7 @@ def chunk_bwd(ctx, q, k, v, g, beta, d_o, d_final_state=None, initial_state=None
     dg = torch.empty((T, HV), dtype=torch.float32, device=dev)
     dbeta = torch.empty((T, HV), dtype=beta.dtype, device=dev)
     dh0 = torch.empty((p.num_seqs, HV, K, v.shape[2]), dtype=torch.float32, device=dev) if want_dh0 else None
-    nws = gdn_chunk_workspace_bytes(p, 1)
+    nws = gdn_chunk_workspace_bytes(p, 1 if ctx.saved is not None else 2)
     if workspace is None or workspace.numel() < nws:
         workspace = torch.empty(nws, dtype=torch.uint8, device=dev)
     st = gdn_chunk_bwd(p, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),

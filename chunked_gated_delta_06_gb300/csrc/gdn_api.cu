@@ -30,9 +30,11 @@ struct Carver {
 struct Dims {
     int N, T, H, HV, C;  // C = chunk count
     float scale;
+    int beta_f32;        // beta / dbeta are fp32 (else bf16)
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
 gdn_status check_problem(const gdn_problem *p, Dims *d) {
     if (!p) return GDN_ERR_INVALID_ARG;
@@ -43,6 +45,7 @@ gdn_status check_problem(const gdn_problem *p, Dims *d) {
         return GDN_ERR_INVALID_ARG;
     if (p->head_dim_k != 128 || p->head_dim_v != 128) return GDN_ERR_UNSUPPORTED;
     if (p->num_v_heads % p->num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+    if (p->beta_dtype != GDN_DTYPE_BF16 && p->beta_dtype != GDN_DTYPE_F32) return GDN_ERR_INVALID_ARG;
     if (!p->cu_seqlens_host || !p->cu_seqlens_dev) return GDN_ERR_INVALID_ARG;
     const int32_t *cu = p->cu_seqlens_host;
     if (cu[0] != 0 || (int64_t)cu[p->num_seqs] != p->total_tokens) return GDN_ERR_INVALID_ARG;
@@ -57,6 +60,7 @@ gdn_status check_problem(const gdn_problem *p, Dims *d) {
     d->HV = p->num_v_heads;
     d->C = (int)chunks;
     d->scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->head_dim_k);
+    d->beta_f32 = p->beta_dtype == GDN_DTYPE_F32;
     return GDN_OK;
 }
 
@@ -107,11 +111,19 @@ size_t saved_bytes(const Dims &d) {
     return cv.used();
 }
 
-size_t ws_bytes(const Dims &d, int for_backward) {
+// Workspace of gdn_chunk_fwd (mode 0), gdn_chunk_bwd with a saved buffer (1) and
+// gdn_chunk_bwd in recompute-state mode (2: the saved tensors follow the backward
+// scratch; the forward's u lives in dv_loc, which the backward writes only after
+// the recomputed state scan has read u).
+size_t ws_bytes(const Dims &d, int mode) {
     Carver cv(nullptr);
     gdn::ChunkArgs a{};
-    if (for_backward) carve_bwd_ws(cv, d, a);
-    else carve_fwd_ws(cv, d, a, true);
+    if (mode == 0) {
+        carve_fwd_ws(cv, d, a, true);
+    } else {
+        carve_bwd_ws(cv, d, a);
+        if (mode == 2) carve_saved(cv, d, a);
+    }
     return cv.used();
 }
 
@@ -128,7 +140,8 @@ void fill_common(gdn::ChunkArgs &a, const Dims &d, const gdn_problem *p, const v
     a.k = static_cast<const bf16 *>(k);
     a.v = static_cast<const bf16 *>(v);
     a.g = g;
-    a.beta = static_cast<const bf16 *>(beta);
+    a.beta = beta;
+    a.beta_f32 = d.beta_f32;
     a.h0 = h0;
     a.cu_dev = p->cu_seqlens_dev;
 }
@@ -158,6 +171,7 @@ size_t gdn_chunk_saved_bytes(const gdn_problem *p) {
 
 size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward) {
     Dims d;
+    if (for_backward < 0 || for_backward > 2) return 0;
     if (check_problem(p, &d) != GDN_OK) return 0;
     return ws_bytes(d, for_backward);
 }
@@ -174,6 +188,7 @@ gdn_status gdn_chunk_fwd_timed(const gdn_problem *p, const void *q, const void *
     const void *ptrs[] = {q, k, v, initial_state, o, final_state, saved, workspace};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
+    if (!aligned_to(g, 4) || !aligned_to(beta, d.beta_f32 ? 4 : 2)) return GDN_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
         (saved && (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0))
         return GDN_ERR_INVALID_ARG;
@@ -207,36 +222,48 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem *p, const void *q, const void *
     Dims d;
     gdn_status st = check_problem(p, &d);
     if (st != GDN_OK) return st;
-    if (!saved && saved_bytes(d) > 0) return GDN_ERR_INVALID_ARG;  // T == 0 saves nothing
+    const bool recompute = !saved && saved_bytes(d) > 0;  // T == 0 saves nothing
     if (d.T > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta))
         return GDN_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, initial_state, saved, d_o, d_final_state, dq, dk, dv, dh0,
                           workspace};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
+    if (!aligned_to(g, 4) || !aligned_to(dg, 4) || !aligned_to(beta, d.beta_f32 ? 4 : 2) ||
+        !aligned_to(dbeta, d.beta_f32 ? 4 : 2))
+        return GDN_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
         (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0)
         return GDN_ERR_INVALID_ARG;
-    if (ws_size < ws_bytes(d, 1)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_size < ws_bytes(d, recompute ? 2 : 1)) return GDN_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     gdn::ChunkArgs a{};
     fill_common(a, d, p, q, k, v, g, beta, initial_state);
     a.timer = timer;
-    Carver sc(const_cast<void *>(saved));
-    carve_saved(sc, d, a);
     Carver wc(workspace);
     carve_bwd_ws(wc, d, a);
+    if (recompute) {
+        carve_saved(wc, d, a);
+        a.u = a.dvloc;  // read by the recomputed state scan before dv_loc is written
+    } else {
+        Carver sc(const_cast<void *>(saved));
+        carve_saved(sc, d, a);
+    }
     a.d_o = static_cast<const bf16 *>(d_o);
     a.d_ht = d_final_state;
     a.dq = static_cast<bf16 *>(dq);
     a.dk = static_cast<bf16 *>(dk);
     a.dv = static_cast<bf16 *>(dv);
-    a.dbeta = static_cast<bf16 *>(dbeta);
+    a.dbeta = dbeta;
     a.dg = dg;
     a.dh0 = dh0;
     cudaError_t e;
     if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
+    if (recompute) {  // the forward's saved tensors, rebuilt by the forward's own kernels
+        if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = gdn::launch_recompute_chunks(a, s)) != cudaSuccess) return cuda_status(e);
+    }
     if ((e = gdn::launch_bwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
     return GDN_OK;
 }

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
         const float gg = in ? a.G[gi] : 0.f;
         sm.G[tid] = gg;
-        sm.beta[tid] = in ? bf2f(a.beta[gi]) : 0.f;
+        sm.beta[tid] = in ? load_beta(a, gi) : 0.f;
         sm.rki[tid] = in ? 1.f / a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
         sm.eg[tid] = in ? __expf(gg) : 0.f;
         sm.dG[tid] = in ? a.dGp[gi] : 0.f;
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             if (m < L) {
                 const size_t gi = (size_t)(t0 + m) * a.HV + hv;
                 a.dg[gi] = (z == 0 ? dgv[0] + dgv[1] : dgv[1]) + after;
-                a.dbeta[gi] = f2bf(sm.db[m]);
+                store_dbeta(a, gi, sm.db[m]);
             }
         }
     }

@@ -221,6 +221,12 @@ cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     return cudaSuccess;
 }
 
+cudaError_t launch_recompute_chunks(const ChunkArgs &a, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = launch_intra_tc(a, s)) != cudaSuccess) return e;
+    return launch_state_tc(a, s);  // a.ht is null: no final state
+}
+
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e;
     if ((e = launch_dvloc_tc(a, s)) != cudaSuccess) return e;

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
     if (tid < 64) {  // per-token scalars; tokens past L get beta = 0 and 1 / r_k = 1
         const bool in = tid < L;
         const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
-        const float gg = in ? a.G[gi] : 0.f, bb = in ? bf2f(a.beta[gi]) : 0.f;
+        const float gg = in ? a.G[gi] : 0.f, bb = in ? load_beta(a, gi) : 0.f;
         const float ri = in ? 1.f / a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
         sm.G[tid] = gg;
         sm.beta[tid] = bb;

@@ -17,7 +17,8 @@ struct ChunkArgs {
     // inputs
     const bf16 *q, *k, *v;
     const float *g;
-    const bf16 *beta;
+    const void *beta;       // [T,HV] bf16, or fp32 when beta_f32
+    int beta_f32;           // the dtype of beta and dbeta
     const float *h0;        // [N,HV,K,V] or null
     const int *cu_dev;      // [N+1]
     // forward outputs
@@ -39,7 +40,8 @@ struct ChunkArgs {
     // backward
     const bf16 *d_o;
     const float *d_ht;      // or null
-    bf16 *dq, *dk, *dv, *dbeta;
+    bf16 *dq, *dk, *dv;
+    void *dbeta;            // [T,HV], beta's dtype
     float *dg, *dh0;        // dh0 may be null
     bf16 *dvloc;            // [T,HV,V]  tril(M)^T dO
     bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
@@ -51,6 +53,15 @@ struct ChunkArgs {
     float *dGp;             // [T,HV]
     gdn_kernel_timer *timer;  // optional per-kernel events
 };
+
+// beta_i and dbeta_i in the dtype the call names (a uniform branch per load).
+__device__ __forceinline__ float load_beta(const ChunkArgs &a, size_t i) {
+    return a.beta_f32 ? static_cast<const float *>(a.beta)[i] : bf2f(static_cast<const bf16 *>(a.beta)[i]);
+}
+__device__ __forceinline__ void store_dbeta(const ChunkArgs &a, size_t i, float x) {
+    if (a.beta_f32) static_cast<float *>(a.dbeta)[i] = x;
+    else static_cast<bf16 *>(a.dbeta)[i] = f2bf(x);
+}
 
 // Records the caller's event pair around one launch (no-op without a timer).
 struct TimerScope {
@@ -72,6 +83,7 @@ struct TimerScope {
 cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_recompute_chunks(const ChunkArgs &a, cudaStream_t s);  // WY pass + state scan
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s);

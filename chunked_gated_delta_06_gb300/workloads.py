@@ -96,6 +96,7 @@ class ChunkWorkload:
     backward: bool = True
     want_final: bool = True
     notes: dict = field(default_factory=dict)
+    beta_f32: np.ndarray | None = None  # float32 [T,HV]: fp32 beta (then beta_bits is unused)
 
     @property
     def T(self) -> int:
@@ -120,7 +121,7 @@ class ChunkWorkload:
 
     @property
     def beta(self):
-        return bf16_value(self.beta_bits)
+        return self.beta_f32 if self.beta_f32 is not None else bf16_value(self.beta_bits)
 
     @property
     def d_o(self):
@@ -174,13 +175,14 @@ def varlen_lengths(seed: int, total: int, lo: int, hi: int) -> list[int]:
 
 def chunk_workload(name: str, lengths, H: int, HV: int, *, seed: int = 0, K: int = 128,
                    V: int = 128, gate: str = "softplus", h0: bool = False, backward: bool = True,
-                   d_ht: bool = False, h0_std: float = 0.1) -> ChunkWorkload:
+                   d_ht: bool = False, h0_std: float = 0.1, beta_dtype: str = "bf16") -> ChunkWorkload:
     """General recipe.
 
     gate = "logsigmoid":  g = logsigmoid(N(0,1))                      (per token, head)
     gate = "softplus":    g = -softplus(N(0,1) + dt_bias) * exp(A_log),
                           A_log ~ U(0, 2.7) per value head, dt_bias = 0
-    beta = sigmoid(N(0,1)) rounded to bf16; q, k, v, dO ~ N(0,1) rounded to bf16;
+    beta = sigmoid(N(0,1)) rounded to bf16 (beta_dtype "bf16") or kept in fp32
+    (beta_dtype "f32"); q, k, v, dO ~ N(0,1) rounded to bf16;
     h0 ~ h0_std * N(0,1) fp32 per sequence; d(final state) ~ N(0,1) fp32.
     """
     lengths = [int(x) for x in lengths]
@@ -201,13 +203,27 @@ def chunk_workload(name: str, lengths, H: int, HV: int, *, seed: int = 0, K: int
             np.float32)
     else:
         raise ValueError(gate)
-    beta = bf16_bits(_sigmoid(_normal(seed, S_BETA, (T, HV))))
+    beta32 = _sigmoid(_normal(seed, S_BETA, (T, HV)))
+    beta = bf16_bits(beta32)
+    if beta_dtype not in ("bf16", "f32"):
+        raise ValueError(beta_dtype)
     h0a = _normal(seed, S_H0, (N, HV, K, V), h0_std) if h0 else None
     do = bf16_bits(_normal(seed, S_DO, (T, HV, V))) if backward else None
     dht = _normal(seed, S_DHT, (N, HV, K, V)) if (backward and d_ht) else None
     return ChunkWorkload(name=name, cu_seqlens=cu, H=H, HV=HV, K=K, V=V, q_bits=q, k_bits=k,
                          v_bits=v, g=g, beta_bits=beta, h0=h0a, do_bits=do, d_ht=dht,
-                         backward=backward, notes=dict(gate=gate, seed=seed))
+                         backward=backward, notes=dict(gate=gate, seed=seed, beta_dtype=beta_dtype),
+                         beta_f32=beta32 if beta_dtype == "f32" else None)
+
+
+def with_fp32_beta(wl: ChunkWorkload) -> ChunkWorkload:
+    """The same workload with beta kept in fp32: the draw that the bf16 beta is the
+    rounding of (same seed and stream)."""
+    import dataclasses
+    T, HV = wl.T, wl.HV
+    beta32 = _sigmoid(_normal(wl.notes.get("seed", 0), S_BETA, (T, HV)))
+    notes = dict(wl.notes, beta_dtype="f32")
+    return dataclasses.replace(wl, beta_f32=beta32, notes=notes)
 
 
 def fwd_t256(seed: int = 0) -> ChunkWorkload:

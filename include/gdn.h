@@ -60,6 +60,12 @@ typedef enum {
     GDN_ERR_CUDA = 4                  /* a CUDA launch or call failed */
 } gdn_status;
 
+/* Element types of beta / dbeta in the chunk calls ("[Cake 1/13] gdn: chunked
+ * gated delta rule, det and fast, with KCP and FLA-CP", Performance (3/5): the
+ * training kernels are timed with BF16 beta and with FP32 beta). */
+#define GDN_DTYPE_BF16 0
+#define GDN_DTYPE_F32 1
+
 /* A packed variable-length problem (B = 1).  Sequence n holds tokens
  * [cu[n], cu[n+1]) of the packed arrays.  Chunks of 64 tokens never span two
  * sequences; the last chunk of a sequence may be partial. */
@@ -71,6 +77,10 @@ typedef struct {
     int32_t head_dim_k;               /* K, must be 128 */
     int32_t head_dim_v;               /* V, must be 128 */
     float scale;                      /* > 0, or <= 0 to select 1/sqrt(K) */
+    int32_t beta_dtype;               /* GDN_DTYPE_BF16 (0, the default of a
+                                         zeroed struct) or GDN_DTYPE_F32: the
+                                         element type of beta and dbeta; any
+                                         other value is GDN_ERR_INVALID_ARG */
     const int32_t *cu_seqlens_host;   /* host [N+1]: 0 = c0 <= c1 <= ... <= cN = T */
     const int32_t *cu_seqlens_dev;    /* device [N+1], the same values */
 } gdn_problem;
@@ -82,14 +92,17 @@ size_t gdn_chunk_saved_bytes(const gdn_problem *p);
 
 /* Bytes of scratch the calls need.  for_backward = 0: gdn_chunk_fwd (this
  * includes room for the saved tensors, used when `saved` is NULL);
- * for_backward = 1: gdn_chunk_bwd.  Returns 0 for an invalid problem. */
+ * for_backward = 1: gdn_chunk_bwd with a `saved` buffer; for_backward = 2:
+ * gdn_chunk_bwd in recompute-state mode (`saved` NULL: the workspace also
+ * holds the recomputed forward tensors).  Returns 0 for an invalid problem or
+ * another for_backward value. */
 size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward);
 
 /* Forward of chunk_gated_delta_rule.
  *   q, k           bf16 [T, H, 128]
  *   v              bf16 [T, HV, 128]
  *   g              fp32 [T, HV]  log decay per token and value head
- *   beta           bf16 [T, HV]
+ *   beta           [T, HV], bf16 or fp32 as p->beta_dtype says
  *   initial_state  fp32 [N, HV, 128(K), 128(V)] K-major, or NULL for zeros
  *   o              bf16 [T, HV, 128]           (out)
  *   final_state    fp32 [N, HV, 128, 128] (out), or NULL
@@ -125,14 +138,22 @@ gdn_status gdn_chunk_fwd_noalloc(const gdn_problem *p, const void *q, const void
 
 /* Backward of chunk_gated_delta_rule.  q ... initial_state exactly as passed
  * to the gdn_chunk_fwd that filled `saved` (not modified since).
+ *   saved          the buffer gdn_chunk_fwd filled, or NULL for recompute-state
+ *                  mode ("[Cake 1/13] gdn: ...", API and flags: the recompute
+ *                  option rebuilds w, u, h and v_new in the backward): the call
+ *                  first reruns the forward's norm / gate pass, WY pass and
+ *                  state scan into the workspace (no o, no final state), then
+ *                  the backward; the results are bit-identical to those of the
+ *                  saved mode, since the same kernels run in the same order
  *   d_o            bf16 [T, HV, 128]
  *   d_final_state  fp32 [N, HV, 128, 128], or NULL for zeros
  *   dq, dk         bf16 [T, H, 128]   (out; summed over the HV/H value heads)
  *   dv             bf16 [T, HV, 128]  (out)
  *   dg             fp32 [T, HV]       (out)
- *   dbeta          bf16 [T, HV]       (out)
+ *   dbeta          [T, HV] (out), beta's dtype
  *   dh0            fp32 [N, HV, 128, 128] (out), or NULL
- *   workspace      ws_bytes >= gdn_chunk_workspace_bytes(p, 1), 256-byte aligned
+ *   workspace      ws_bytes >= gdn_chunk_workspace_bytes(p, 1) with `saved`,
+ *                  >= gdn_chunk_workspace_bytes(p, 2) without; 256-byte aligned
  * The reverse state recurrence follows "Qwen3.5-397B RL trainer on 128 v7x"
  * (maxtext #5799), GDN context-parallel dh-scan commit. */
 gdn_status gdn_chunk_bwd(const gdn_problem *p, const void *q, const void *k, const void *v,

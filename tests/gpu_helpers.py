@@ -32,8 +32,9 @@ def to_dev(wl, torch):
     def bf(bits):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
 
+    beta = bf(wl.beta_bits) if wl.beta_f32 is None else torch.from_numpy(wl.beta_f32).to(dev)
     d = dict(q=bf(wl.q_bits), k=bf(wl.k_bits), v=bf(wl.v_bits),
-             g=torch.from_numpy(wl.g).to(dev), beta=bf(wl.beta_bits),
+             g=torch.from_numpy(wl.g).to(dev), beta=beta,
              h0=None if wl.h0 is None else torch.from_numpy(wl.h0).to(dev),
              cu_dev=torch.from_numpy(wl.cu_seqlens).to(dev))
     d["d_o"] = None if wl.do_bits is None else bf(wl.do_bits)
@@ -41,31 +42,22 @@ def to_dev(wl, torch):
     return d
 
 
-def run_chunk(wl, torch, backward=None):
+def run_chunk(wl, torch, backward=None, recompute=False):
     """Run gdn_chunk_fwd (+ gdn_chunk_bwd) on a workload; returns numpy float64 results."""
-    import chunked_gated_delta_06_gb300 as gdn
-    backward = wl.backward if backward is None else backward
-    d = to_dev(wl, torch)
-    o, ht, ctx = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], wl.cu_seqlens, d["cu_dev"],
-                               initial_state=d["h0"], output_final_state=True,
-                               for_backward=backward)
-    out = dict(o=o, ht=ht)
-    if backward:
-        out.update(gdn.chunk_bwd(ctx, d["q"], d["k"], d["v"], d["g"], d["beta"], d["d_o"],
-                                 d_final_state=d["d_ht"], initial_state=d["h0"]))
-    torch.cuda.synchronize()
+    out = run_chunk_raw(wl, torch, backward=backward, recompute=recompute)
     return {k_: (None if v_ is None else v_.float().cpu().numpy().astype(np.float64))
             for k_, v_ in out.items()}
 
 
-def run_chunk_raw(wl, torch, backward=None):
-    """Like run_chunk but returns the device tensors (for bitwise comparisons)."""
+def run_chunk_raw(wl, torch, backward=None, recompute=False):
+    """Like run_chunk but returns the device tensors (for bitwise comparisons).
+    recompute: the forward keeps no saved buffer and the backward rebuilds it."""
     import chunked_gated_delta_06_gb300 as gdn
     backward = wl.backward if backward is None else backward
     d = to_dev(wl, torch)
     o, ht, ctx = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], wl.cu_seqlens, d["cu_dev"],
                                initial_state=d["h0"], output_final_state=True,
-                               for_backward=backward)
+                               for_backward=backward and not recompute)
     out = dict(o=o, ht=ht)
     if backward:
         out.update(gdn.chunk_bwd(ctx, d["q"], d["k"], d["v"], d["g"], d["beta"], d["d_o"],

@@ -30,8 +30,8 @@ def test_status_strings(lib):
     assert "unknown" in gdn.status_string(99)
 
 
-def _problem(cu, H=2, HV=4, K=128, V=128, scale=0.0, dev=0x1000):
-    return binding.make_problem(cu, H, HV, K, V, scale, cu_dev_ptr=dev)
+def _problem(cu, H=2, HV=4, K=128, V=128, scale=0.0, dev=0x1000, beta_dtype=0):
+    return binding.make_problem(cu, H, HV, K, V, scale, cu_dev_ptr=dev, beta_dtype=beta_dtype)
 
 
 def test_saved_and_workspace_sizes(lib):
@@ -50,6 +50,14 @@ def test_saved_and_workspace_sizes(lib):
     bwd_ws = gdn.gdn_chunk_workspace_bytes(p, 1)
     # dqhat, dkhat partials, dv_loc, dv_new, dW (bf16); per-chunk dh (bf16)
     assert bwd_ws >= 6 * T * HV * D * 2 + C * HV * D * D * 2
+    # recompute-state mode: the backward scratch followed by the saved tensors
+    assert gdn.gdn_chunk_workspace_bytes(p, 2) == bwd_ws + saved
+    assert gdn.gdn_chunk_workspace_bytes(p, 3) == 0
+    assert gdn.gdn_chunk_workspace_bytes(p, -1) == 0
+    # the beta dtype changes no buffer size (beta and dbeta are the caller's)
+    p32, keep32 = _problem(cu, beta_dtype=binding.GDN_DTYPE_F32)
+    assert gdn.gdn_chunk_saved_bytes(p32) == saved
+    assert gdn.gdn_chunk_workspace_bytes(p32, 2) == bwd_ws + saved
 
 
 @pytest.mark.parametrize("mut, status", [
@@ -59,6 +67,8 @@ def test_saved_and_workspace_sizes(lib):
     (dict(cu=[0, 5, 3]), binding.GDN_ERR_INVALID_ARG),
     (dict(cu=[1, 5]), binding.GDN_ERR_INVALID_ARG),
     (dict(dev=0), binding.GDN_ERR_INVALID_ARG),
+    (dict(beta_dtype=2), binding.GDN_ERR_INVALID_ARG),
+    (dict(beta_dtype=-1), binding.GDN_ERR_INVALID_ARG),
 ])
 def test_invalid_problems_are_rejected_before_any_launch(lib, mut, status):
     kw = dict(cu=[0, 5, 9], H=2, HV=4, K=128, V=128, dev=0x1000)
@@ -86,9 +96,17 @@ def test_missing_buffers_are_rejected(lib):
     # workspace too small
     assert gdn.gdn_chunk_fwd(p, fake, fake, fake, fake, fake, None, fake, None, None, fake, 1024,
                              None) == binding.GDN_ERR_WORKSPACE_TOO_SMALL
-    # backward without the saved buffer
+    # backward without the saved buffer is recompute-state mode: its workspace must also
+    # hold the forward's tensors (checked before any launch)
+    ws1 = gdn.gdn_chunk_workspace_bytes(p, 1)
     assert gdn.gdn_chunk_bwd(p, fake, fake, fake, fake, fake, None, None, fake, None, fake, fake,
-                             fake, fake, fake, None, fake, 1 << 40, None) == binding.GDN_ERR_INVALID_ARG
+                             fake, fake, fake, None, fake, ws1, None) == binding.GDN_ERR_WORKSPACE_TOO_SMALL
+    # fp32 beta must be 4-byte aligned, bf16 beta 2-byte aligned
+    p32, keep32 = _problem([0, 5], beta_dtype=binding.GDN_DTYPE_F32)
+    assert gdn.gdn_chunk_fwd(p32, fake, fake, fake, fake, fake + 2, None, fake, None, None, fake,
+                             1 << 40, None) == binding.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_chunk_fwd(p, fake, fake, fake, fake, fake + 1, None, fake, None, None, fake,
+                             1 << 40, None) == binding.GDN_ERR_INVALID_ARG
     # null problem
     assert lib.gdn_chunk_saved_bytes(None) == 0
 
@@ -112,9 +130,11 @@ def test_decode_argument_checks(lib):
 
 
 def test_problem_struct_layout_matches_the_header(lib):
-    # int32, int64, 4 x int32, float, 2 pointers: offsets as a C compiler lays them out
+    # int32, int64, 4 x int32, float, int32, 2 pointers: offsets as a C compiler lays them
+    # out (beta_dtype fills what was the padding before the pointers)
     P = binding.GdnProblem
     assert P.total_tokens.offset == 8
     assert P.scale.offset == 32
+    assert P.beta_dtype.offset == 36
     assert P.cu_seqlens_host.offset == 40
     assert ctypes.sizeof(P) == 56

@@ -47,3 +47,12 @@ def test_single_process_keeps_its_numbers():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.aggregate_over_ranks(3.5, 42) == (3.5, 42)
+
+
+def test_every_package_name_the_bench_calls_is_exported():
+    # the bench drives the library through the package namespace (gdn.<name>)
+    import re
+    import chunked_gated_delta_06_gb300 as gdn
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench.py")).read()
+    names = set(re.findall(r"\bgdn\.([A-Za-z_]\w*)", src))
+    assert names and not [n for n in sorted(names) if not hasattr(gdn, n)]

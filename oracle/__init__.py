@@ -59,6 +59,8 @@ def _load():
                                               + [_D] * 6 + [ctypes.c_int, _I, _D]
                                               + [ctypes.c_int] * 2)
             lib.gdn_oracle_decode.restype = ctypes.c_int
+            lib.gdn_oracle_gate_fwd.argtypes = [ctypes.c_int] * 2 + [_D] * 6
+            lib.gdn_oracle_gate_bwd.argtypes = [ctypes.c_int] * 2 + [_D] * 10
             _lib = lib
     return _lib
 
@@ -202,3 +204,30 @@ def decode(q, k, v, g, beta, pool, state_indices, scale=None, use_l2norm=True, t
     # rows of one slot must not run on two threads; repeated indices are a caller error
     _parallel(B * HV, run, threads)
     return o, pool, bad[0] // max(HV, 1)
+
+
+def gate_fwd(a, b, A_log, dt_bias):
+    """Fused gating: g = -exp(A_log) softplus(a + dt_bias) (threshold 20), beta = sigmoid(b).
+    a, b [..., HV]; A_log, dt_bias [HV].  Returns (g, beta) shaped like a."""
+    lib = _load()
+    a, b, A_log, dt_bias = map(_f64, (a, b, A_log, dt_bias))
+    HV = a.shape[-1]
+    n = a.size // HV if HV else 0
+    g = np.zeros(a.shape)
+    beta = np.zeros(a.shape)
+    lib.gdn_oracle_gate_fwd(n, HV, _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g), _ptr(beta))
+    return g, beta
+
+
+def gate_bwd(a, b, A_log, dt_bias, dg, dbeta):
+    """Backward of gate_fwd.  Returns dict da, db (shaped like a), dA_log, ddt_bias [HV]
+    (sums over every row in row order)."""
+    lib = _load()
+    a, b, A_log, dt_bias, dg, dbeta = map(_f64, (a, b, A_log, dt_bias, dg, dbeta))
+    HV = a.shape[-1]
+    n = a.size // HV if HV else 0
+    da, db = np.zeros(a.shape), np.zeros(a.shape)
+    dA, ddt = np.zeros(HV), np.zeros(HV)
+    lib.gdn_oracle_gate_bwd(n, HV, _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(dg), _ptr(dbeta),
+                            _ptr(da), _ptr(db), _ptr(dA), _ptr(ddt))
+    return dict(da=da, db=db, dA_log=dA, ddt_bias=ddt)

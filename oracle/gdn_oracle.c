@@ -24,6 +24,10 @@
  *    + beta_t v_t k_t^T, o_t = S_t q_t (S is V x K), written per token as
  *      S' = exp(g_t) S_{t-1};  p = S' k;  delta = beta_t (v_t - p);
  *      S_t = S' + delta k^T;    o_t = S_t q.
+ *  - Fused gating: "C6: GDN decode-step goldens and recurrent/conv state
+ *    contract" (RL-Kernel #469), "What" and "Provider": beta = sigmoid(b) and
+ *    g = -exp(A_log) softplus(a + dt_bias), computed in fp32 in the provider
+ *    (fp64 here) with the softplus threshold at 20 (softplus(x) = x above it).
  *  - The chunked (WY) form: "Qwen3.5-397B RL trainer on 128 v7x" (maxtext
  *    #5799), GDN context-parallel m-scan and dh-scan commits: the chunk
  *    transition M_c = g_last I - k_bwd^T (t_inv k_beta_g) and the reverse
@@ -468,4 +472,47 @@ int gdn_oracle_decode(int B, int H, int HV, int K, int V, double scale, int use_
     }
     free(qh); free(kh);
     return bad;
+}
+
+/* ---------------------------------------------------------------- fused gating
+ * a, b, g, beta, dg, dbeta, da, db: [n, HV] (n tokens or decode rows); A_log,
+ * dt_bias, dA_log, ddt_bias: [HV].  softplus(x) = x for x > 20, log(1 + e^x)
+ * otherwise, so its derivative is 1 above the threshold and sigmoid(x) below. */
+static double softplus_thr(double x) { return x > 20.0 ? x : log1p(exp(x)); }
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+void gdn_oracle_gate_fwd(int n, int HV, const double *a, const double *b, const double *A_log,
+                         const double *dt_bias, double *g, double *beta)
+{
+    for (int t = 0; t < n; ++t)
+        for (int h = 0; h < HV; ++h) {
+            const size_t i = (size_t)t * HV + h;
+            g[i] = -exp(A_log[h]) * softplus_thr(a[i] + dt_bias[h]);
+            beta[i] = sigmoid(b[i]);
+        }
+}
+
+/* Backward of gdn_oracle_gate_fwd for incoming dg, dbeta:
+ *   da = dg * (-e^{A_log}) * softplus'(a + dt_bias),   ddt_bias = sum_t da,
+ *   dA_log = sum_t dg * g,                             db = dbeta * beta (1 - beta). */
+void gdn_oracle_gate_bwd(int n, int HV, const double *a, const double *b, const double *A_log,
+                         const double *dt_bias, const double *dg, const double *dbeta,
+                         double *da, double *db, double *dA_log, double *ddt_bias)
+{
+    for (int h = 0; h < HV; ++h) {
+        dA_log[h] = 0.0;
+        ddt_bias[h] = 0.0;
+    }
+    for (int t = 0; t < n; ++t)
+        for (int h = 0; h < HV; ++h) {
+            const size_t i = (size_t)t * HV + h;
+            const double x = a[i] + dt_bias[h], e = exp(A_log[h]);
+            const double dsp = x > 20.0 ? 1.0 : sigmoid(x);
+            const double gi = -e * softplus_thr(x);
+            da[i] = dg[i] * -e * (g_mutation == 9 ? softplus_thr(x) : dsp);
+            dA_log[h] += dg[i] * gi;
+            ddt_bias[h] += da[i];
+            const double be = sigmoid(b[i]);
+            db[i] = dbeta[i] * (g_mutation == 8 ? be : be * (1.0 - be));
+        }
 }

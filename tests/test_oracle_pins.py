@@ -352,6 +352,113 @@ def test_decode_counts_out_of_range_slots_and_skips_them():
     np.testing.assert_array_equal(newpool[2:], pool[2:])
 
 
+# ----------------------------------------------------------------------------- fused gating
+def check_gate_closed_forms():
+    # softplus(0) = ln 2; above the threshold 20 softplus is the identity; far below it
+    # softplus(x) = e^x to within e^{2x}; sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4,
+    # sigmoid(x) + sigmoid(-x) = 1
+    A = np.array([0.0, 0.7, -1.3, 2.0])
+    dt = np.array([0.0, 0.5, 0.25, -1.0])
+    a = np.array([[0.0 - 0.0, 30.0 - 0.5, -40.0 - 0.25, 20.5 + 1.0]])
+    b = np.array([[0.0, np.log(3.0), 2.5, -2.5]])
+    g, beta = oracle.gate_fwd(a, b, A, dt)
+    assert g[0, 0] == pytest.approx(-np.log(2.0), rel=1e-15)
+    assert g[0, 1] == -np.exp(0.7) * 30.0
+    assert g[0, 2] == pytest.approx(-np.exp(-1.3) * np.exp(-40.0), rel=1e-12)
+    assert g[0, 3] == -np.exp(2.0) * 20.5
+    assert beta[0, 0] == 0.5
+    assert beta[0, 1] == pytest.approx(0.75, rel=1e-15)
+    assert beta[0, 2] + beta[0, 3] == pytest.approx(1.0, rel=1e-15)
+
+
+def check_gate_backward_matches_finite_differences():
+    r = np.random.default_rng(61)
+    n, HV = 5, 3
+    A = r.uniform(-1, 1.5, size=HV)
+    dt = r.uniform(-1, 1, size=HV)
+    a = r.uniform(-6, 6, size=(n, HV))
+    a[2, 1] = 26.0 - dt[1]  # above the softplus threshold: derivative exactly 1
+    b = r.uniform(-4, 4, size=(n, HV))
+    wg, wb = r.standard_normal((n, HV)), r.standard_normal((n, HV))
+
+    def loss(a_, b_, A_, dt_):
+        g, beta = oracle.gate_fwd(a_, b_, A_, dt_)
+        return float((wg * g).sum() + (wb * beta).sum())
+
+    gr = oracle.gate_bwd(a, b, A, dt, wg, wb)
+    eps = 1e-6
+    for name, x, ref in (("a", a, gr["da"]), ("b", b, gr["db"]), ("A_log", A, gr["dA_log"]),
+                         ("dt_bias", dt, gr["ddt_bias"])):
+        fd = np.zeros_like(x)
+        for i in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[i] += eps
+            xm[i] -= eps
+            args_p = dict(a_=a, b_=b, A_=A, dt_=dt)
+            args_m = dict(args_p)
+            key = {"a": "a_", "b": "b_", "A_log": "A_", "dt_bias": "dt_"}[name]
+            args_p[key], args_m[key] = xp, xm
+            fd[i] = (loss(**args_p) - loss(**args_m)) / (2 * eps)
+        np.testing.assert_allclose(ref, fd, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def check_gated_rule_gradients_through_the_gate():
+    # the composition the gated entry points compute: g, beta from a, b, then the rule;
+    # d loss / d (a, b, A_log, dt_bias) by the chain rule against central differences
+    r = np.random.default_rng(62)
+    lengths, H, HV, K, V = [5, 4], 1, 2, 4, 4
+    c = _rand_case(63, lengths, H, HV, K, V, h0=True)
+    T = sum(lengths)
+    A = r.uniform(-0.5, 1.0, size=HV)
+    dt = r.uniform(-0.5, 0.5, size=HV)
+    a = r.standard_normal((T, HV))
+    b = r.standard_normal((T, HV))
+    dO = r.standard_normal((T, HV, V))
+
+    def loss(a_, b_, A_, dt_):
+        g, beta = oracle.gate_fwd(a_, b_, A_, dt_)
+        o, _ = oracle.fwd(c["q"], c["k"], c["v"], g, beta, c["cu"], h0=c["h0"], threads=1)
+        return float((dO * o).sum())
+
+    g, beta = oracle.gate_fwd(a, b, A, dt)
+    gr = oracle.bwd(c["q"], c["k"], c["v"], g, beta, c["cu"], dO, h0=c["h0"], threads=1)
+    ch = oracle.gate_bwd(a, b, A, dt, gr["dg"], gr["dbeta"])
+    eps = 1e-6
+    for (t, h) in [(0, 0), (3, 1), (5, 0), (8, 1)]:
+        for name, x in (("a", a), ("b", b)):
+            xp, xm = x.copy(), x.copy()
+            xp[t, h] += eps
+            xm[t, h] -= eps
+            if name == "a":
+                fd = (loss(xp, b, A, dt) - loss(xm, b, A, dt)) / (2 * eps)
+            else:
+                fd = (loss(a, xp, A, dt) - loss(a, xm, A, dt)) / (2 * eps)
+            assert ch["d" + name][t, h] == pytest.approx(fd, rel=1e-5, abs=1e-8), (name, t, h)
+    for h in range(HV):
+        Ap, Am = A.copy(), A.copy()
+        Ap[h] += eps
+        Am[h] -= eps
+        fd = (loss(a, b, Ap, dt) - loss(a, b, Am, dt)) / (2 * eps)
+        assert ch["dA_log"][h] == pytest.approx(fd, rel=1e-5, abs=1e-8)
+        dp, dm = dt.copy(), dt.copy()
+        dp[h] += eps
+        dm[h] -= eps
+        fd = (loss(a, b, A, dp) - loss(a, b, A, dm)) / (2 * eps)
+        assert ch["ddt_bias"][h] == pytest.approx(fd, rel=1e-5, abs=1e-8)
+
+
+def test_gate_closed_forms():
+    check_gate_closed_forms()
+
+
+def test_gate_backward_matches_finite_differences():
+    check_gate_backward_matches_finite_differences()
+
+
+def test_gated_rule_gradients_through_the_gate():
+    check_gated_rule_gradients_through_the_gate()
+
+
 # ----------------------------------------------------------------------------- discrimination
 PINS = [
     lambda: check_golden("delta_rule_hand_worked.json"),
@@ -365,11 +472,14 @@ PINS = [
     check_split_call_equals_one_call,
     check_grouped_heads_equal_repeated_keys,
     check_decode_equals_one_token_chunk_call,
+    check_gate_closed_forms,
+    check_gate_backward_matches_finite_differences,
 ]
 
 # 1 decay after the write, 2 prediction from the undecayed state, 3 output before the write,
-# 4 scale on k too, 5 epsilon outside the sqrt, 6 sign of dp flipped (backward), 7 key head hv % H
-MUTATIONS = [1, 2, 3, 4, 5, 6, 7]
+# 4 scale on k too, 5 epsilon outside the sqrt, 6 sign of dp flipped (backward), 7 key head hv % H,
+# 8 dbeta -> db through beta instead of beta (1 - beta), 9 da through softplus instead of its slope
+MUTATIONS = [1, 2, 3, 4, 5, 6, 7, 8, 9]
 
 
 @pytest.mark.parametrize("m", MUTATIONS)

@@ -197,6 +197,7 @@ STEP_MODES = {
     "saved": "gdn_chunk_fwd (saving for backward) + gdn_chunk_bwd",
     "recompute": "gdn_chunk_fwd (no saved buffer) + gdn_chunk_bwd in recompute-state mode",
     "ckpt": "gdn_chunk_fwd (no saved buffer) + gdn_chunk_fwd (saving) + gdn_chunk_bwd",
+    "gated": "gdn_chunk_fwd_gated (saving) + gdn_chunk_bwd_gated: g, beta from the fused gate",
 }
 
 
@@ -229,6 +230,14 @@ class ChunkRunner:
         self.dg = e(T, HV)
         self.dbeta = e(T, HV, dt=torch.float32 if f32 else torch.bfloat16)
         self.dh0 = e(N, HV, D, D)
+        if mode == "gated":  # pre-activations and parameters of the fused gate
+            from chunked_gated_delta_06_gb300 import workloads as W
+            gi = W.gate_inputs(T, HV, seed=wl.notes.get("seed", 0))
+            self.ga, self.gb = _bf(torch, gi.a_bits, dev), _bf(torch, gi.b_bits, dev)
+            self.A_log = torch.from_numpy(gi.A_log).to(dev)
+            self.dt_bias = torch.from_numpy(gi.dt_bias).to(dev)
+            self.da, self.db = e(T, HV, dt=torch.bfloat16), e(T, HV, dt=torch.bfloat16)
+            self.dA_log, self.ddt_bias = e(HV), e(HV)
 
     def _fwd(self, saved, s, timer):
         gdn, P = self.gdn, lambda t: None if t is None else t.data_ptr()  # noqa: E731
@@ -238,9 +247,26 @@ class ChunkRunner:
         if st:
             raise gdn.GdnError(st, "gdn_chunk_fwd")
 
+    def _gated_step(self, s):
+        gdn, P = self.gdn, lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        gate = (P(self.ga), P(self.gb), P(self.A_log), P(self.dt_bias))
+        st = gdn.gdn_chunk_fwd_gated(self.p, P(self.q), P(self.k), P(self.v), *gate, P(self.h0),
+                                     P(self.o), P(self.ht), P(self.saved), P(self.ws_f),
+                                     self.ws_f.numel(), s)
+        if st:
+            raise gdn.GdnError(st, "gdn_chunk_fwd_gated")
+        st = gdn.gdn_chunk_bwd_gated(self.p, P(self.q), P(self.k), P(self.v), *gate, P(self.h0),
+                                     P(self.saved), P(self.d_o), P(self.d_ht), P(self.dq), P(self.dk),
+                                     P(self.dv), P(self.da), P(self.db), P(self.dA_log),
+                                     P(self.ddt_bias), P(self.dh0), P(self.ws_b), self.ws_b.numel(), s)
+        if st:
+            raise gdn.GdnError(st, "gdn_chunk_bwd_gated")
+
     def step(self, timer=None, stream=None):
         gdn, P = self.gdn, lambda t: None if t is None else t.data_ptr()  # noqa: E731
         s = (stream or self.torch.cuda.current_stream()).cuda_stream
+        if self.mode == "gated":
+            return self._gated_step(s)
         if self.mode == "ckpt":
             self._fwd(None, s, timer)  # the forward of the checkpointed step keeps nothing
         self._fwd(self.saved, s, timer)
@@ -440,7 +466,8 @@ def bench_ours(args):
         vsteps = max(3, min(args.steps, 10))
         variants = {}
         for name, vwl, mode in (("recompute", wl, "recompute"), ("ckpt", wl, "ckpt"),
-                                ("beta_f32", W.with_fp32_beta(wl), "saved")):
+                                ("beta_f32", W.with_fp32_beta(wl), "saved"),
+                                ("gated", wl, "gated")):
             vr = ChunkRunner(torch, vwl, dev, mode=mode)
             for _ in range(max(2, min(args.warmup, 3))):
                 vr.step()
@@ -449,7 +476,8 @@ def bench_ours(args):
             barrier()
             variants[name] = {"value": total_tokens / (vms / 1e3), "unit": "tokens/s",
                               "ms_per_step": vms, "steps": vsteps, "step": STEP_MODES[mode],
-                              "beta": "fp32" if vwl.beta_f32 is not None else "bf16"}
+                              "beta": ("sigmoid(b), b bf16" if mode == "gated" else
+                                       "fp32" if vwl.beta_f32 is not None else "bf16")}
             del vr
         line["variants"] = variants
 

@@ -91,6 +91,13 @@ def lib():
             L.gdn_chunk_bwd_timed.restype = ctypes.c_int
             L.gdn_decode_step_timed.argtypes = L.gdn_decode_step.argtypes + [T]
             L.gdn_decode_step_timed.restype = ctypes.c_int
+            L.gdn_chunk_fwd_gated.argtypes = [P] + [_vp] * 12 + [_sz, _vp]
+            L.gdn_chunk_fwd_gated.restype = ctypes.c_int
+            L.gdn_chunk_bwd_gated.argtypes = [P] + [_vp] * 20 + [_sz, _vp]
+            L.gdn_chunk_bwd_gated.restype = ctypes.c_int
+            L.gdn_decode_step_gated.argtypes = ([ctypes.c_int32] * 5 + [ctypes.c_float] + [_vp] * 8
+                                                + [ctypes.c_int32] + [_vp] * 3 + [_vp])
+            L.gdn_decode_step_gated.restype = ctypes.c_int
             L.gdn_chunk_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
             L.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
             L.gdn_kernel_name.argtypes = [ctypes.c_int32]
@@ -189,6 +196,28 @@ def gdn_chunk_bwd(p, q, k, v, g, beta, initial_state, saved, d_o, d_final_state,
     return int(lib().gdn_chunk_bwd(ctypes.byref(p), q, k, v, g, beta, initial_state, saved, d_o,
                                    d_final_state, dq, dk, dv, dg, dbeta, dh0, workspace, ws_bytes,
                                    stream))
+
+
+def gdn_chunk_fwd_gated(p, q, k, v, a, b, A_log, dt_bias, initial_state, o, final_state, saved,
+                        workspace, ws_bytes, stream) -> int:
+    return int(lib().gdn_chunk_fwd_gated(ctypes.byref(p), q, k, v, a, b, A_log, dt_bias,
+                                         initial_state, o, final_state, saved, workspace, ws_bytes,
+                                         stream))
+
+
+def gdn_chunk_bwd_gated(p, q, k, v, a, b, A_log, dt_bias, initial_state, saved, d_o, d_final_state,
+                        dq, dk, dv, da, db, dA_log, ddt_bias, dh0, workspace, ws_bytes,
+                        stream) -> int:
+    return int(lib().gdn_chunk_bwd_gated(ctypes.byref(p), q, k, v, a, b, A_log, dt_bias,
+                                         initial_state, saved, d_o, d_final_state, dq, dk, dv, da,
+                                         db, dA_log, ddt_bias, dh0, workspace, ws_bytes, stream))
+
+
+def gdn_decode_step_gated(batch, H, HV, K, V, scale, q, k, v, a, b, A_log, dt_bias, state_pool,
+                          num_slots, state_indices, o, device_status, stream) -> int:
+    return int(lib().gdn_decode_step_gated(batch, H, HV, K, V, scale, q, k, v, a, b, A_log,
+                                           dt_bias, state_pool, num_slots, state_indices, o,
+                                           device_status, stream))
 
 
 def gdn_decode_step(batch, H, HV, K, V, scale, q, k, v, g, beta, state_pool, num_slots,
@@ -306,4 +335,73 @@ def decode_step(q, k, v, g, beta, state_pool, state_indices, scale=None, device_
                          _ptr(beta), _ptr(state_pool), state_pool.shape[0], _ptr(state_indices),
                          _ptr(o), _ptr(device_status), _stream())
     _check(st, "gdn_decode_step")
+    return o
+
+
+def chunk_fwd_gated(q, k, v, a, b, A_log, dt_bias, cu_host, cu_dev, scale=None, initial_state=None,
+                    output_final_state=True, for_backward=False, workspace=None):
+    """gdn_chunk_fwd_gated on torch tensors (g and beta from the fused gate).
+    Returns (o, final_state or None, ctx); ctx feeds chunk_bwd_gated."""
+    import torch
+    T, H, K = q.shape
+    HV = v.shape[1]
+    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale)
+    p = ctx.problem
+    dev = q.device
+    o = torch.empty((T, HV, v.shape[2]), dtype=torch.bfloat16, device=dev)
+    ht = (torch.empty((p.num_seqs, HV, K, v.shape[2]), dtype=torch.float32, device=dev)
+          if output_final_state else None)
+    nws = gdn_chunk_workspace_bytes(p, 0)
+    if workspace is None or workspace.numel() < nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=dev)
+    saved = torch.empty(gdn_chunk_saved_bytes(p), dtype=torch.uint8, device=dev) if for_backward else None
+    st = gdn_chunk_fwd_gated(p, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                             _ptr(dt_bias), _ptr(initial_state), _ptr(o), _ptr(ht), _ptr(saved),
+                             _ptr(workspace), workspace.numel(), _stream())
+    _check(st, "gdn_chunk_fwd_gated")
+    ctx.saved = saved
+    ctx.workspace = workspace
+    return o, ht, ctx
+
+
+def chunk_bwd_gated(ctx, q, k, v, a, b, A_log, dt_bias, d_o, d_final_state=None,
+                    initial_state=None, want_dh0=True, workspace=None):
+    """gdn_chunk_bwd_gated on torch tensors.  Returns dict dq, dk, dv, da, db, dA_log,
+    ddt_bias, dh0 (recompute-state mode when ctx holds no saved buffer)."""
+    import torch
+    T, H, K = q.shape
+    HV = v.shape[1]
+    p = ctx.problem
+    dev = q.device
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    da = torch.empty((T, HV), dtype=torch.bfloat16, device=dev)
+    db = torch.empty((T, HV), dtype=torch.bfloat16, device=dev)
+    dA_log = torch.empty((HV,), dtype=torch.float32, device=dev)
+    ddt_bias = torch.empty((HV,), dtype=torch.float32, device=dev)
+    dh0 = (torch.empty((p.num_seqs, HV, K, v.shape[2]), dtype=torch.float32, device=dev)
+           if want_dh0 else None)
+    nws = gdn_chunk_workspace_bytes(p, 1 if ctx.saved is not None else 2)
+    if workspace is None or workspace.numel() < nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=dev)
+    st = gdn_chunk_bwd_gated(p, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                             _ptr(dt_bias), _ptr(initial_state), _ptr(ctx.saved), _ptr(d_o),
+                             _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(da), _ptr(db),
+                             _ptr(dA_log), _ptr(ddt_bias), _ptr(dh0), _ptr(workspace),
+                             workspace.numel(), _stream())
+    _check(st, "gdn_chunk_bwd_gated")
+    return dict(dq=dq, dk=dk, dv=dv, da=da, db=db, dA_log=dA_log, ddt_bias=ddt_bias, dh0=dh0)
+
+
+def decode_step_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, scale=None,
+                      device_status=None):
+    """gdn_decode_step_gated on torch tensors (state_pool updated in place).  Returns o."""
+    import torch
+    B, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    o = torch.empty((B, HV, V), dtype=torch.bfloat16, device=q.device)
+    st = gdn_decode_step_gated(B, H, HV, K, V, float(scale or 0.0), _ptr(q), _ptr(k), _ptr(v),
+                               _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(state_pool),
+                               state_pool.shape[0], _ptr(state_indices), _ptr(o),
+                               _ptr(device_status), _stream())
+    _check(st, "gdn_decode_step_gated")
     return o

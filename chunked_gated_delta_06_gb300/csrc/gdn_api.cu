@@ -30,7 +30,7 @@ struct Carver {
 struct Dims {
     int N, T, H, HV, C;  // C = chunk count
     float scale;
-    int beta_f32;        // beta / dbeta are fp32 (else bf16)
+    int beta_f32;        // beta / dbeta are fp32 (else bf16); fused-gating calls need bf16
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -102,6 +102,7 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.dkp = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dkp2 = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dGp = cv.take<float>((size_t)d.T * d.HV);
+    a.gpart = cv.take<float>((size_t)d.C * d.HV * 2);
 }
 
 size_t saved_bytes(const Dims &d) {
@@ -141,12 +142,193 @@ void fill_common(gdn::ChunkArgs &a, const Dims &d, const gdn_problem *p, const v
     a.v = static_cast<const bf16 *>(v);
     a.g = g;
     a.beta = beta;
-    a.beta_f32 = d.beta_f32;
+    a.beta_mode = d.beta_f32 ? 1 : 0;
     a.h0 = h0;
     a.cu_dev = p->cu_seqlens_dev;
 }
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// Fused-gating arguments of the *_gated entry points (all null otherwise).
+struct Gate {
+    const void *a, *b;             // bf16 [T, HV] (decode: [batch, HV])
+    const float *A_log, *dt_bias;  // fp32 [HV]
+    void *da, *db;                 // bf16 [T, HV] (backward)
+    float *dA_log, *ddt_bias;      // fp32 [HV] (backward)
+};
+
+// The gate / beta inputs of a chunk call: g and beta, or the fused gate's a, b,
+// A_log and dt_bias (2-byte aligned bf16, 4-byte aligned fp32).
+gdn_status check_gate_inputs(const Dims &d, const gdn_problem *p, const float *g, const void *beta,
+                             const Gate *gt) {
+    if (gt) {
+        if (p->beta_dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARG;  // a and b are bf16
+        if (d.T > 0 && (!gt->a || !gt->b)) return GDN_ERR_INVALID_ARG;
+        if (!gt->A_log || !gt->dt_bias) return GDN_ERR_INVALID_ARG;
+        if (!aligned_to(gt->a, 2) || !aligned_to(gt->b, 2) || !aligned_to(gt->A_log, 4) ||
+            !aligned_to(gt->dt_bias, 4))
+            return GDN_ERR_INVALID_ARG;
+        return GDN_OK;
+    }
+    if (d.T > 0 && (!g || !beta)) return GDN_ERR_INVALID_ARG;
+    if (!aligned_to(g, 4) || !aligned_to(beta, d.beta_f32 ? 4 : 2)) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+void fill_gate(gdn::ChunkArgs &a, const Gate *gt) {
+    if (!gt) return;
+    a.beta_mode = 2;
+    a.ga = static_cast<const bf16 *>(gt->a);
+    a.gb = static_cast<const bf16 *>(gt->b);
+    a.A_log = gt->A_log;
+    a.dt_bias = gt->dt_bias;
+}
+
+gdn_status chunk_fwd_impl(const gdn_problem *p, const void *q, const void *k, const void *v,
+                          const float *g, const void *beta, const Gate *gt,
+                          const float *initial_state, void *o, float *final_state, void *saved,
+                          void *workspace, size_t ws_size, gdn_stream_t stream,
+                          gdn_kernel_timer *timer) {
+    Dims d;
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    if (d.T > 0 && (!q || !k || !v || !o)) return GDN_ERR_INVALID_ARG;
+    if ((st = check_gate_inputs(d, p, g, beta, gt)) != GDN_OK) return st;
+    const void *ptrs[] = {q, k, v, initial_state, o, final_state, saved, workspace};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+        (saved && (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0))
+        return GDN_ERR_INVALID_ARG;
+    if (ws_size < ws_bytes(d, 0)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    gdn::ChunkArgs a{};
+    fill_common(a, d, p, q, k, v, g, beta, initial_state);
+    fill_gate(a, gt);
+    a.timer = timer;
+    a.o = static_cast<bf16 *>(o);
+    a.ht = final_state;
+    Carver wc(workspace);
+    carve_fwd_ws(wc, d, a, saved == nullptr);
+    if (saved) {
+        Carver sc(saved);
+        carve_saved(sc, d, a);
+    }
+    cudaError_t e;
+    if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = gdn::launch_fwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
+    return GDN_OK;
+}
+
+gdn_status chunk_bwd_impl(const gdn_problem *p, const void *q, const void *k, const void *v,
+                          const float *g, const void *beta, const Gate *gt,
+                          const float *initial_state, const void *saved, const void *d_o,
+                          const float *d_final_state, void *dq, void *dk, void *dv, float *dg,
+                          void *dbeta, float *dh0, void *workspace, size_t ws_size,
+                          gdn_stream_t stream, gdn_kernel_timer *timer) {
+    Dims d;
+    gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    const bool recompute = !saved && saved_bytes(d) > 0;  // T == 0 saves nothing
+    if (d.T > 0 && (!q || !k || !v || !d_o || !dq || !dk || !dv)) return GDN_ERR_INVALID_ARG;
+    if ((st = check_gate_inputs(d, p, g, beta, gt)) != GDN_OK) return st;
+    if (gt) {
+        if (d.T > 0 && (!gt->da || !gt->db)) return GDN_ERR_INVALID_ARG;
+        if (!gt->dA_log || !gt->ddt_bias) return GDN_ERR_INVALID_ARG;
+        if (!aligned_to(gt->da, 2) || !aligned_to(gt->db, 2) || !aligned_to(gt->dA_log, 4) ||
+            !aligned_to(gt->ddt_bias, 4))
+            return GDN_ERR_INVALID_ARG;
+    } else {
+        if (d.T > 0 && (!dg || !dbeta)) return GDN_ERR_INVALID_ARG;
+        if (!aligned_to(dg, 4) || !aligned_to(dbeta, d.beta_f32 ? 4 : 2)) return GDN_ERR_INVALID_ARG;
+    }
+    const void *ptrs[] = {q, k, v, initial_state, saved, d_o, d_final_state, dq, dk, dv, dh0,
+                          workspace};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+        (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0)
+        return GDN_ERR_INVALID_ARG;
+    if (ws_size < ws_bytes(d, recompute ? 2 : 1)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    gdn::ChunkArgs a{};
+    fill_common(a, d, p, q, k, v, g, beta, initial_state);
+    fill_gate(a, gt);
+    a.timer = timer;
+    Carver wc(workspace);
+    carve_bwd_ws(wc, d, a);
+    if (recompute) {
+        carve_saved(wc, d, a);
+        a.u = a.dvloc;  // read by the recomputed state scan before dv_loc is written
+    } else {
+        Carver sc(const_cast<void *>(saved));
+        carve_saved(sc, d, a);
+    }
+    a.d_o = static_cast<const bf16 *>(d_o);
+    a.d_ht = d_final_state;
+    a.dq = static_cast<bf16 *>(dq);
+    a.dk = static_cast<bf16 *>(dk);
+    a.dv = static_cast<bf16 *>(dv);
+    a.dh0 = dh0;
+    if (gt) {
+        a.dbeta = gt->db;
+        a.da = static_cast<bf16 *>(gt->da);
+        a.dA_log = gt->dA_log;
+        a.ddt_bias = gt->ddt_bias;
+    } else {
+        a.dbeta = dbeta;
+        a.dg = dg;
+    }
+    cudaError_t e;
+    if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
+    if (recompute) {  // the forward's saved tensors, rebuilt by the forward's own kernels
+        if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = gdn::launch_recompute_chunks(a, s)) != cudaSuccess) return cuda_status(e);
+    }
+    if ((e = gdn::launch_bwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
+    if (gt && (e = gdn::launch_gate_reduce(a, s)) != cudaSuccess) return cuda_status(e);
+    return GDN_OK;
+}
+
+gdn_status decode_impl(int32_t batch, int32_t num_k_heads, int32_t num_v_heads, int32_t head_dim_k,
+                       int32_t head_dim_v, float scale, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const Gate *gt, float *state_pool,
+                       int32_t num_slots, const int32_t *state_indices, void *o,
+                       int32_t *device_status, gdn_stream_t stream, gdn_kernel_timer *timer) {
+    if (batch < 0 || num_k_heads < 1 || num_v_heads < 1 || num_slots < 1)
+        return GDN_ERR_INVALID_ARG;
+    if (head_dim_k != 128 || head_dim_v != 128) return GDN_ERR_UNSUPPORTED;
+    if (num_v_heads % num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)batch * num_v_heads > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+    if (batch == 0) return GDN_OK;
+    if (!q || !k || !v || !state_pool || !state_indices || !o) return GDN_ERR_INVALID_ARG;
+    if (gt) {
+        if (!gt->a || !gt->b || !gt->A_log || !gt->dt_bias) return GDN_ERR_INVALID_ARG;
+        if (!aligned_to(gt->a, 2) || !aligned_to(gt->b, 2) || !aligned_to(gt->A_log, 4) ||
+            !aligned_to(gt->dt_bias, 4))
+            return GDN_ERR_INVALID_ARG;
+    } else {
+        if (!g || !beta || !aligned_to(g, 4) || !aligned_to(beta, 4)) return GDN_ERR_INVALID_ARG;
+    }
+    if (!aligned16(state_pool)) return GDN_ERR_INVALID_ARG;
+    const float s = scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim_k);
+    gdn::DecodeGate dg{};
+    if (gt) {
+        dg.a = static_cast<const bf16 *>(gt->a);
+        dg.b = static_cast<const bf16 *>(gt->b);
+        dg.A_log = gt->A_log;
+        dg.dt_bias = gt->dt_bias;
+    }
+    cudaError_t e = gdn::launch_decode(
+        batch, num_k_heads, num_v_heads, s, static_cast<const bf16 *>(q),
+        static_cast<const bf16 *>(k), static_cast<const bf16 *>(v), g, beta, dg, state_pool,
+        num_slots, state_indices, static_cast<bf16 *>(o), device_status,
+        reinterpret_cast<cudaStream_t>(stream), timer);
+    return cuda_status(e);
+}
 
 }  // namespace
 
@@ -176,41 +358,14 @@ size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward) {
     return ws_bytes(d, for_backward);
 }
 
+
 gdn_status gdn_chunk_fwd_timed(const gdn_problem *p, const void *q, const void *k,
                                const void *v, const float *g, const void *beta,
                                const float *initial_state, void *o, float *final_state,
                                void *saved, void *workspace, size_t ws_size,
                                gdn_stream_t stream, gdn_kernel_timer *timer) {
-    Dims d;
-    gdn_status st = check_problem(p, &d);
-    if (st != GDN_OK) return st;
-    if (d.T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, initial_state, o, final_state, saved, workspace};
-    for (const void *x : ptrs)
-        if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
-    if (!aligned_to(g, 4) || !aligned_to(beta, d.beta_f32 ? 4 : 2)) return GDN_ERR_INVALID_ARG;
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
-        (saved && (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0))
-        return GDN_ERR_INVALID_ARG;
-    if (ws_size < ws_bytes(d, 0)) return GDN_ERR_WORKSPACE_TOO_SMALL;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-    gdn::ChunkArgs a{};
-    fill_common(a, d, p, q, k, v, g, beta, initial_state);
-    a.timer = timer;
-    a.o = static_cast<bf16 *>(o);
-    a.ht = final_state;
-    Carver wc(workspace);
-    carve_fwd_ws(wc, d, a, saved == nullptr);
-    if (saved) {
-        Carver sc(saved);
-        carve_saved(sc, d, a);
-    }
-    cudaError_t e;
-    if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
-    if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
-    if ((e = gdn::launch_fwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
-    return GDN_OK;
+    return chunk_fwd_impl(p, q, k, v, g, beta, nullptr, initial_state, o, final_state, saved,
+                          workspace, ws_size, stream, timer);
 }
 
 gdn_status gdn_chunk_bwd_timed(const gdn_problem *p, const void *q, const void *k,
@@ -219,53 +374,44 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem *p, const void *q, const void *
                                const float *d_final_state, void *dq, void *dk, void *dv,
                                float *dg, void *dbeta, float *dh0, void *workspace,
                                size_t ws_size, gdn_stream_t stream, gdn_kernel_timer *timer) {
-    Dims d;
-    gdn_status st = check_problem(p, &d);
-    if (st != GDN_OK) return st;
-    const bool recompute = !saved && saved_bytes(d) > 0;  // T == 0 saves nothing
-    if (d.T > 0 && (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta))
-        return GDN_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, initial_state, saved, d_o, d_final_state, dq, dk, dv, dh0,
-                          workspace};
-    for (const void *x : ptrs)
-        if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
-    if (!aligned_to(g, 4) || !aligned_to(dg, 4) || !aligned_to(beta, d.beta_f32 ? 4 : 2) ||
-        !aligned_to(dbeta, d.beta_f32 ? 4 : 2))
-        return GDN_ERR_INVALID_ARG;
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
-        (reinterpret_cast<uintptr_t>(saved) % kAlign) != 0)
-        return GDN_ERR_INVALID_ARG;
-    if (ws_size < ws_bytes(d, recompute ? 2 : 1)) return GDN_ERR_WORKSPACE_TOO_SMALL;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return chunk_bwd_impl(p, q, k, v, g, beta, nullptr, initial_state, saved, d_o, d_final_state,
+                          dq, dk, dv, dg, dbeta, dh0, workspace, ws_size, stream, timer);
+}
 
-    gdn::ChunkArgs a{};
-    fill_common(a, d, p, q, k, v, g, beta, initial_state);
-    a.timer = timer;
-    Carver wc(workspace);
-    carve_bwd_ws(wc, d, a);
-    if (recompute) {
-        carve_saved(wc, d, a);
-        a.u = a.dvloc;  // read by the recomputed state scan before dv_loc is written
-    } else {
-        Carver sc(const_cast<void *>(saved));
-        carve_saved(sc, d, a);
-    }
-    a.d_o = static_cast<const bf16 *>(d_o);
-    a.d_ht = d_final_state;
-    a.dq = static_cast<bf16 *>(dq);
-    a.dk = static_cast<bf16 *>(dk);
-    a.dv = static_cast<bf16 *>(dv);
-    a.dbeta = dbeta;
-    a.dg = dg;
-    a.dh0 = dh0;
-    cudaError_t e;
-    if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
-    if (recompute) {  // the forward's saved tensors, rebuilt by the forward's own kernels
-        if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
-        if ((e = gdn::launch_recompute_chunks(a, s)) != cudaSuccess) return cuda_status(e);
-    }
-    if ((e = gdn::launch_bwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
-    return GDN_OK;
+gdn_status gdn_chunk_fwd_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
+                               const void *a, const void *b, const float *A_log,
+                               const float *dt_bias, const float *initial_state, void *o,
+                               float *final_state, void *saved, void *workspace, size_t ws_size,
+                               gdn_stream_t stream) {
+    const Gate gt{a, b, A_log, dt_bias, nullptr, nullptr, nullptr, nullptr};
+    return chunk_fwd_impl(p, q, k, v, nullptr, nullptr, &gt, initial_state, o, final_state, saved,
+                          workspace, ws_size, stream, nullptr);
+}
+
+gdn_status gdn_chunk_bwd_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
+                               const void *a, const void *b, const float *A_log,
+                               const float *dt_bias, const float *initial_state,
+                               const void *saved, const void *d_o, const float *d_final_state,
+                               void *dq, void *dk, void *dv, void *da, void *db, float *dA_log,
+                               float *ddt_bias, float *dh0, void *workspace, size_t ws_size,
+                               gdn_stream_t stream) {
+    const Gate gt{a, b, A_log, dt_bias, da, db, dA_log, ddt_bias};
+    return chunk_bwd_impl(p, q, k, v, nullptr, nullptr, &gt, initial_state, saved, d_o,
+                          d_final_state, dq, dk, dv, nullptr, nullptr, dh0, workspace, ws_size,
+                          stream, nullptr);
+}
+
+gdn_status gdn_decode_step_gated(int32_t batch, int32_t num_k_heads, int32_t num_v_heads,
+                                 int32_t head_dim_k, int32_t head_dim_v, float scale,
+                                 const void *q, const void *k, const void *v, const void *a,
+                                 const void *b, const float *A_log, const float *dt_bias,
+                                 float *state_pool, int32_t num_slots,
+                                 const int32_t *state_indices, void *o, int32_t *device_status,
+                                 gdn_stream_t stream) {
+    const Gate gt{a, b, A_log, dt_bias, nullptr, nullptr, nullptr, nullptr};
+    return decode_impl(batch, num_k_heads, num_v_heads, head_dim_k, head_dim_v, scale, q, k, v,
+                       nullptr, nullptr, &gt, state_pool, num_slots, state_indices, o,
+                       device_status, stream, nullptr);
 }
 
 gdn_status gdn_decode_step_timed(int32_t batch, int32_t num_k_heads, int32_t num_v_heads,
@@ -274,22 +420,9 @@ gdn_status gdn_decode_step_timed(int32_t batch, int32_t num_k_heads, int32_t num
                                  const float *beta, float *state_pool, int32_t num_slots,
                                  const int32_t *state_indices, void *o, int32_t *device_status,
                                  gdn_stream_t stream, gdn_kernel_timer *timer) {
-    if (batch < 0 || num_k_heads < 1 || num_v_heads < 1 || num_slots < 1)
-        return GDN_ERR_INVALID_ARG;
-    if (head_dim_k != 128 || head_dim_v != 128) return GDN_ERR_UNSUPPORTED;
-    if (num_v_heads % num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
-    if ((int64_t)batch * num_v_heads > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
-    if (batch == 0) return GDN_OK;
-    if (!q || !k || !v || !g || !beta || !state_pool || !state_indices || !o)
-        return GDN_ERR_INVALID_ARG;
-    if (!aligned16(state_pool)) return GDN_ERR_INVALID_ARG;
-    const float s = scale > 0.f ? scale : 1.0f / sqrtf((float)head_dim_k);
-    cudaError_t e = gdn::launch_decode(
-        batch, num_k_heads, num_v_heads, s, static_cast<const bf16 *>(q),
-        static_cast<const bf16 *>(k), static_cast<const bf16 *>(v), g, beta, state_pool, num_slots,
-        state_indices, static_cast<bf16 *>(o), device_status,
-        reinterpret_cast<cudaStream_t>(stream), timer);
-    return cuda_status(e);
+    return decode_impl(batch, num_k_heads, num_v_heads, head_dim_k, head_dim_v, scale, q, k, v, g,
+                       beta, nullptr, state_pool, num_slots, state_indices, o, device_status,
+                       stream, timer);
 }
 
 gdn_status gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,

@@ -329,14 +329,30 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             if (lane + off < 32) suf += y;
         }
         const float after = suf - pair;  // sum over elements 2*lane+2 ...
+        float pa = 0.f, pd = 0.f;        // fused gating: sums of dg g and of da over the chunk
 #pragma unroll
         for (int z = 0; z < 2; ++z) {
             const int m = 2 * lane + z;
             if (m < L) {
                 const size_t gi = (size_t)(t0 + m) * a.HV + hv;
-                a.dg[gi] = (z == 0 ? dgv[0] + dgv[1] : dgv[1]) + after;
-                store_dbeta(a, gi, sm.db[m]);
+                const float dgm = (z == 0 ? dgv[0] + dgv[1] : dgv[1]) + after;
+                store_dbeta(a, gi, sm.db[m], sm.beta[m]);
+                if (a.beta_mode == 2) {  // da = dg (-e^{A_log}) softplus'(a + dt_bias)
+                    const float x = bf2f(a.ga[gi]) + a.dt_bias[hv], nea = -expf(a.A_log[hv]);
+                    const float da = dgm * nea * gate_softplus_slope(x);
+                    a.da[gi] = f2bf(da);
+                    pa += dgm * (nea * gate_softplus(x));
+                    pd += da;
+                } else {
+                    a.dg[gi] = dgm;
+                }
             }
+        }
+        if (a.beta_mode == 2) {
+            pa = warp_sum(pa);
+            pd = warp_sum(pd);
+            if (lane == 0)
+                reinterpret_cast<float2 *>(a.gpart)[(size_t)c * a.HV + hv] = make_float2(pa, pd);
         }
     }
     tc_fence_before();

@@ -82,7 +82,8 @@ __global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunk
 }
 
 // ---------------------------------------------------------------------------
-// Norms of q and k rows and the chunk-local cumsum of g.  grid (chunks, H).
+// Norms of q and k rows and the chunk-local cumsum of g (g from the fused gate when
+// the call passes its pre-activations).  grid (chunks, H).
 __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
     const int c = blockIdx.x, h = blockIdx.y;
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
@@ -109,8 +110,8 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
     for (int j = warp; j < r; j += kThreads / 32) {
         const int hv = h * r + j;
         const int i0 = 2 * lane, i1 = 2 * lane + 1;
-        float x0 = i0 < L ? a.g[(size_t)(t0 + i0) * a.HV + hv] : 0.f;
-        float x1 = i1 < L ? a.g[(size_t)(t0 + i1) * a.HV + hv] : 0.f;
+        float x0 = i0 < L ? load_g(a, (size_t)(t0 + i0) * a.HV + hv, hv) : 0.f;
+        float x1 = i1 < L ? load_g(a, (size_t)(t0 + i1) * a.HV + hv, hv) : 0.f;
         float s = x0 + x1;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -225,6 +226,35 @@ cudaError_t launch_recompute_chunks(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e;
     if ((e = launch_intra_tc(a, s)) != cudaSuccess) return e;
     return launch_state_tc(a, s);  // a.ht is null: no final state
+}
+
+// Fused-gating backward, last step: dA_log[hv] and ddt_bias[hv] as sums of the
+// per-chunk partials of the WY-pullback kernel.  One warp per value head: lane l
+// adds the chunks c = l, l + 32, ... in order (fp64), then a fixed butterfly.
+__global__ void k_gate_reduce(ChunkArgs a) {
+    const int hv = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (hv >= a.HV) return;
+    const float2 *part = reinterpret_cast<const float2 *>(a.gpart);
+    double sa = 0.0, sd = 0.0;
+    for (int c = lane; c < a.num_chunks; c += 32) {
+        const float2 p = part[(size_t)c * a.HV + hv];
+        sa += p.x;
+        sd += p.y;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+        sd += __shfl_xor_sync(0xffffffffu, sd, o);
+    }
+    if (lane == 0) {
+        a.dA_log[hv] = (float)sa;
+        a.ddt_bias[hv] = (float)sd;
+    }
+}
+
+cudaError_t launch_gate_reduce(const ChunkArgs &a, cudaStream_t s) {
+    k_gate_reduce<<<(a.HV + 7) / 8, 256, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {

@@ -26,6 +26,15 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Fused gating ("C6: GDN decode-step goldens and recurrent/conv state contract",
+// Provider): beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias) in fp32, with
+// softplus(x) = x above the threshold 20 (its slope there is 1, sigmoid(x) below).
+__device__ __forceinline__ float gate_softplus(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+__device__ __forceinline__ float gate_softplus_slope(float x) {
+    return x > 20.f ? 1.f : 1.f / (1.f + expf(-x));
+}
+__device__ __forceinline__ float gate_sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
+
 // Chunk table built on the device from cu_seqlens (see k_plan).
 struct ChunkTable {
     const int *seq_chunk_off;  // [N+1] first chunk of each sequence

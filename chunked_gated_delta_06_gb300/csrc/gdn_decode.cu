@@ -6,6 +6,8 @@
 //   qhat = scale * q / sqrt(sum q^2 + 1e-6),  khat = k / sqrt(sum k^2 + 1e-6)
 //   key head = value head // (HV / H)
 //   S <- e^g S;  p = S khat;  S += beta (v - p) khat^T;  o = S qhat
+// with g and beta given, or computed in the kernel from the fused gate's
+// pre-activations (Provider: beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias)),
 // on the pool [num_slots, HV, V, K] (row v of S holds K contiguous floats),
 // indices <= 0 skipped with a zero output row.
 //
@@ -33,8 +35,9 @@ __device__ __forceinline__ void st_stream(float *p, float4 v) {
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     k_decode(int H, int HV, float scale, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
              const bf16 *__restrict__ v, const float *__restrict__ g,
-             const float *__restrict__ beta, float *__restrict__ pool, int num_slots,
-             const int32_t *__restrict__ idx, bf16 *__restrict__ o, int32_t *status) {
+             const float *__restrict__ beta, const DecodeGate gate, float *__restrict__ pool,
+             int num_slots, const int32_t *__restrict__ idx, bf16 *__restrict__ o,
+             int32_t *status) {
     const int b = blockIdx.x / HV, hv = blockIdx.x % HV;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slot = idx[b];
@@ -73,8 +76,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         kq += kv[u] * qv[u];
     }
     kq = warp_sum(kq);
-    const float a = expf(g[(size_t)b * HV + hv]);
-    const float bt = beta[(size_t)b * HV + hv];
+    // decay and beta: given, or from the fused gate (fp32, softplus threshold 20)
+    const size_t gi = (size_t)b * HV + hv;
+    const float gv = gate.a ? -expf(gate.A_log[hv]) * gate_softplus(bf2f(gate.a[gi]) + gate.dt_bias[hv])
+                            : g[gi];
+    const float a = expf(gv);
+    const float bt = gate.a ? gate_sigmoid(bf2f(gate.b[gi])) : beta[gi];
     const bf16 *vrow = v + ((size_t)b * HV + hv) * kDim;
     float my_o = 0.f;
 #pragma unroll
@@ -99,13 +106,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 }  // namespace
 
 cudaError_t launch_decode(int B, int H, int HV, float scale, const bf16 *q, const bf16 *k,
-                          const bf16 *v, const float *g, const float *beta, float *pool,
-                          int num_slots, const int32_t *idx, bf16 *o, int32_t *status,
+                          const bf16 *v, const float *g, const float *beta, const DecodeGate &gate,
+                          float *pool, int num_slots, const int32_t *idx, bf16 *o, int32_t *status,
                           cudaStream_t s, gdn_kernel_timer *timer) {
     if (B == 0) return cudaSuccess;
     TimerScope ts(timer, GDN_KERNEL_DECODE, s);
     k_decode<<<(unsigned)((size_t)B * HV), kDecodeWarps * 32, 0, s>>>(
-        H, HV, scale, q, k, v, g, beta, pool, num_slots, idx, o, status);
+        H, HV, scale, q, k, v, g, beta, gate, pool, num_slots, idx, o, status);
     return cudaGetLastError();
 }
 

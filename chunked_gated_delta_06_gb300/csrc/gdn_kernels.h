@@ -17,8 +17,11 @@ struct ChunkArgs {
     // inputs
     const bf16 *q, *k, *v;
     const float *g;
-    const void *beta;       // [T,HV] bf16, or fp32 when beta_f32
-    int beta_f32;           // the dtype of beta and dbeta
+    const void *beta;       // [T,HV] bf16 or fp32 (beta_mode 0 / 1)
+    int beta_mode;          // 0: bf16 beta; 1: fp32 beta; 2: fused gating (beta = sigmoid(gb))
+    // fused gating (beta_mode 2): g and beta come from these instead of g / beta
+    const bf16 *ga, *gb;    // [T,HV] pre-activations of the gate and of beta
+    const float *A_log, *dt_bias;  // [HV]
     const float *h0;        // [N,HV,K,V] or null
     const int *cu_dev;      // [N+1]
     // forward outputs
@@ -41,7 +44,10 @@ struct ChunkArgs {
     const bf16 *d_o;
     const float *d_ht;      // or null
     bf16 *dq, *dk, *dv;
-    void *dbeta;            // [T,HV], beta's dtype
+    void *dbeta;            // [T,HV], beta's dtype; with fused gating db (bf16)
+    bf16 *da;               // [T,HV] fused gating: gradient of the gate pre-activation
+    float *dA_log, *ddt_bias;  // [HV] fused gating: sums over all tokens
+    float *gpart;           // [C_total,HV,2] per-chunk sums of dg g and of da (fused gating)
     float *dg, *dh0;        // dh0 may be null
     bf16 *dvloc;            // [T,HV,V]  tril(M)^T dO
     bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
@@ -54,13 +60,20 @@ struct ChunkArgs {
     gdn_kernel_timer *timer;  // optional per-kernel events
 };
 
-// beta_i and dbeta_i in the dtype the call names (a uniform branch per load).
+// beta_i in the form the call gives it (a uniform branch per load).
 __device__ __forceinline__ float load_beta(const ChunkArgs &a, size_t i) {
-    return a.beta_f32 ? static_cast<const float *>(a.beta)[i] : bf2f(static_cast<const bf16 *>(a.beta)[i]);
+    if (a.beta_mode == 2) return gate_sigmoid(bf2f(a.gb[i]));
+    return a.beta_mode ? static_cast<const float *>(a.beta)[i] : bf2f(static_cast<const bf16 *>(a.beta)[i]);
 }
-__device__ __forceinline__ void store_dbeta(const ChunkArgs &a, size_t i, float x) {
-    if (a.beta_f32) static_cast<float *>(a.dbeta)[i] = x;
-    else static_cast<bf16 *>(a.dbeta)[i] = f2bf(x);
+// dbeta_i = x in beta's dtype; with fused gating db_i = x beta_i (1 - beta_i) (bf16).
+__device__ __forceinline__ void store_dbeta(const ChunkArgs &a, size_t i, float x, float beta) {
+    if (a.beta_mode == 1) static_cast<float *>(a.dbeta)[i] = x;
+    else static_cast<bf16 *>(a.dbeta)[i] = f2bf(a.beta_mode == 2 ? x * (beta * (1.f - beta)) : x);
+}
+// g_i: the input, or -exp(A_log) softplus(a + dt_bias) with fused gating.
+__device__ __forceinline__ float load_g(const ChunkArgs &a, size_t i, int hv) {
+    if (a.beta_mode != 2) return a.g[i];
+    return -expf(a.A_log[hv]) * gate_softplus(bf2f(a.ga[i]) + a.dt_bias[hv]);
 }
 
 // Records the caller's event pair around one launch (no-op without a timer).
@@ -84,6 +97,7 @@ cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_recompute_chunks(const ChunkArgs &a, cudaStream_t s);  // WY pass + state scan
+cudaError_t launch_gate_reduce(const ChunkArgs &a, cudaStream_t s);       // dA_log, ddt_bias
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s);
@@ -93,9 +107,14 @@ cudaError_t launch_dvloc_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_intra_tc(const ChunkArgs &a, cudaStream_t s);
 
+// Fused-gating inputs of the decode step (a null = g and beta are given).
+struct DecodeGate {
+    const bf16 *a, *b;             // [B,HV]
+    const float *A_log, *dt_bias;  // [HV]
+};
 cudaError_t launch_decode(int B, int H, int HV, float scale, const bf16 *q, const bf16 *k,
-                          const bf16 *v, const float *g, const float *beta, float *pool,
-                          int num_slots, const int32_t *idx, bf16 *o, int32_t *status,
+                          const bf16 *v, const float *g, const float *beta, const DecodeGate &gate,
+                          float *pool, int num_slots, const int32_t *idx, bf16 *o, int32_t *status,
                           cudaStream_t s, gdn_kernel_timer *timer);
 
 }  // namespace gdn

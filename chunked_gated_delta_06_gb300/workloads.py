@@ -30,7 +30,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 # stream numbers of default_rng([seed, stream])
-S_LEN, S_Q, S_K, S_V, S_G, S_BETA, S_ALOG, S_H0, S_DO, S_DHT, S_POOL, S_IDX = range(12)
+S_LEN, S_Q, S_K, S_V, S_G, S_BETA, S_ALOG, S_H0, S_DO, S_DHT, S_POOL, S_IDX, S_GATE = range(13)
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -224,6 +224,39 @@ def with_fp32_beta(wl: ChunkWorkload) -> ChunkWorkload:
     beta32 = _sigmoid(_normal(wl.notes.get("seed", 0), S_BETA, (T, HV)))
     notes = dict(wl.notes, beta_dtype="f32")
     return dataclasses.replace(wl, beta_f32=beta32, notes=notes)
+
+
+@dataclass
+class GateInputs:
+    """Pre-activations and parameters of the fused gate for n rows of HV heads."""
+    a_bits: np.ndarray               # uint16 [n,HV] bf16 gate pre-activation
+    b_bits: np.ndarray               # uint16 [n,HV] bf16 beta pre-activation
+    A_log: np.ndarray                # float32 [HV]
+    dt_bias: np.ndarray              # float32 [HV]
+
+    @property
+    def a(self):
+        return bf16_value(self.a_bits)
+
+    @property
+    def b(self):
+        return bf16_value(self.b_bits)
+
+
+def gate_inputs(n: int, HV: int, seed: int = 0, over_threshold: int = 3) -> GateInputs:
+    """a, b ~ N(0,1) rounded to bf16 with ``over_threshold`` entries of a set to 24 (past
+    the softplus threshold of 20 even after dt_bias), A_log ~ U(0, 2.7) and
+    dt_bias ~ U(-1, 1) per value head, fp32 (the gate recipe of the chunk workloads,
+    with the gate computed by the kernels)."""
+    r = _rng(seed, S_GATE)
+    a = r.standard_normal(size=(n, HV), dtype=np.float32)
+    b = r.standard_normal(size=(n, HV), dtype=np.float32)
+    if n * HV and over_threshold:
+        flat = r.choice(n * HV, size=min(over_threshold, n * HV), replace=False)
+        a.reshape(-1)[flat] = 24.0
+    A_log = r.uniform(0.0, 2.7, size=HV).astype(np.float32)
+    dt_bias = r.uniform(-1.0, 1.0, size=HV).astype(np.float32)
+    return GateInputs(a_bits=bf16_bits(a), b_bits=bf16_bits(b), A_log=A_log, dt_bias=dt_bias)
 
 
 def fwd_t256(seed: int = 0) -> ChunkWorkload:

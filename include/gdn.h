@@ -184,6 +184,46 @@ gdn_status gdn_decode_step(int32_t batch, int32_t num_k_heads, int32_t num_v_hea
                            const int32_t *state_indices, void *o, int32_t *device_status,
                            gdn_stream_t stream);
 
+/* Fused gating ("C6: GDN decode-step goldens and recurrent/conv state
+ * contract" (RL-Kernel #469), What and Provider): the decay and beta are
+ * computed inside the kernels, in fp32, from their pre-activations:
+ *     beta_t = sigmoid(b_t)
+ *     g_t    = -exp(A_log[hv]) * softplus(a_t + dt_bias[hv]),
+ *     softplus(x) = x for x > 20, log(1 + exp(x)) otherwise.
+ *   a, b           bf16 [T, HV] (decode: [batch, HV])
+ *   A_log, dt_bias fp32 [HV]
+ * The *_gated calls take these in place of g and beta; every other argument
+ * is as in the call without the suffix, and p->beta_dtype must be
+ * GDN_DTYPE_BF16.  The backward returns, in place of dg and dbeta:
+ *   da, db            bf16 [T, HV]: da = dg * (-exp(A_log)) * softplus'(a + dt_bias)
+ *                     with softplus' = 1 above the threshold and sigmoid below;
+ *                     db = dbeta * beta (1 - beta)
+ *   dA_log, ddt_bias  fp32 [HV] (out, required): sums over every token of the
+ *                     call of dg * g and of da, in a fixed order (zeros when
+ *                     T == 0)
+ * A backward after gdn_chunk_fwd_gated must be gdn_chunk_bwd_gated (the saved
+ * buffer holds the cumulative decay of the fused gate).  Recompute-state mode
+ * (saved NULL) works as in gdn_chunk_bwd. */
+gdn_status gdn_chunk_fwd_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
+                               const void *a, const void *b, const float *A_log,
+                               const float *dt_bias, const float *initial_state, void *o,
+                               float *final_state, void *saved, void *workspace,
+                               size_t ws_bytes, gdn_stream_t stream);
+gdn_status gdn_chunk_bwd_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
+                               const void *a, const void *b, const float *A_log,
+                               const float *dt_bias, const float *initial_state,
+                               const void *saved, const void *d_o, const float *d_final_state,
+                               void *dq, void *dk, void *dv, void *da, void *db, float *dA_log,
+                               float *ddt_bias, float *dh0, void *workspace, size_t ws_bytes,
+                               gdn_stream_t stream);
+gdn_status gdn_decode_step_gated(int32_t batch, int32_t num_k_heads, int32_t num_v_heads,
+                                 int32_t head_dim_k, int32_t head_dim_v, float scale,
+                                 const void *q, const void *k, const void *v, const void *a,
+                                 const void *b, const float *A_log, const float *dt_bias,
+                                 float *state_pool, int32_t num_slots,
+                                 const int32_t *state_indices, void *o, int32_t *device_status,
+                                 gdn_stream_t stream);
+
 /* Optional per-kernel timing, for profiling tools and benchmarks.  The caller
  * creates `capacity` pairs of CUDA events (cudaEvent_t, passed as void*) and
  * passes the struct to a *_timed entry point; the library records

@@ -138,3 +138,42 @@ def test_problem_struct_layout_matches_the_header(lib):
     assert P.beta_dtype.offset == 36
     assert P.cu_seqlens_host.offset == 40
     assert ctypes.sizeof(P) == 56
+
+
+def test_gated_calls_check_their_arguments_before_any_launch(lib):
+    fake = 0x10000
+    p, keep = _problem([0, 5])
+    big = 1 << 40
+
+    def fwd(pp=p, a=fake, b=fake, A=fake, dt=fake):
+        return gdn.gdn_chunk_fwd_gated(pp, fake, fake, fake, a, b, A, dt, None, fake, None, None,
+                                       fake, big, None)
+
+    def bwd(pp=p, a=fake, b=fake, A=fake, dt=fake, da=fake, db=fake, dA=fake, ddt=fake):
+        return gdn.gdn_chunk_bwd_gated(pp, fake, fake, fake, a, b, A, dt, None, fake, fake, None,
+                                       fake, fake, fake, da, db, dA, ddt, None, fake, big, None)
+
+    assert fwd(A=None) == binding.GDN_ERR_INVALID_ARG
+    assert fwd(a=None) == binding.GDN_ERR_INVALID_ARG
+    assert fwd(b=fake + 1) == binding.GDN_ERR_INVALID_ARG      # bf16 must be 2-byte aligned
+    assert fwd(dt=fake + 2) == binding.GDN_ERR_INVALID_ARG     # fp32 must be 4-byte aligned
+    p32, keep32 = _problem([0, 5], beta_dtype=binding.GDN_DTYPE_F32)
+    assert fwd(pp=p32) == binding.GDN_ERR_INVALID_ARG          # a and b are bf16
+    assert bwd(dA=None) == binding.GDN_ERR_INVALID_ARG
+    assert bwd(ddt=None) == binding.GDN_ERR_INVALID_ARG
+    assert bwd(da=None) == binding.GDN_ERR_INVALID_ARG
+    assert bwd(db=fake + 1) == binding.GDN_ERR_INVALID_ARG
+    # the workspace check still comes before any launch
+    assert gdn.gdn_chunk_bwd_gated(p, fake, fake, fake, fake, fake, fake, fake, None, fake, fake,
+                                   None, fake, fake, fake, fake, fake, fake, fake, None, fake, 1024,
+                                   None) == binding.GDN_ERR_WORKSPACE_TOO_SMALL
+
+    def dec(**over):
+        a = dict(batch=4, a=fake, b=fake, A=fake, dt=fake)
+        a.update(over)
+        return gdn.gdn_decode_step_gated(a["batch"], 2, 4, 128, 128, 0.0, fake, fake, fake, a["a"],
+                                         a["b"], a["A"], a["dt"], fake, 8, fake, fake, None, None)
+    assert dec(a=None) == binding.GDN_ERR_INVALID_ARG
+    assert dec(A=None) == binding.GDN_ERR_INVALID_ARG
+    assert dec(b=fake + 1) == binding.GDN_ERR_INVALID_ARG
+    assert dec(batch=0) == binding.GDN_OK

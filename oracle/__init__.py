@@ -231,3 +231,32 @@ def gate_bwd(a, b, A_log, dt_bias, dg, dbeta):
     lib.gdn_oracle_gate_bwd(n, HV, _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(dg), _ptr(dbeta),
                             _ptr(da), _ptr(db), _ptr(dA), _ptr(ddt))
     return dict(da=da, db=db, dA_log=dA, ddt_bias=ddt)
+
+
+def prefill_paged(q, k, v, g, beta, cu_seqlens, pool, state_indices, has_initial_state=None,
+                  scale=None, use_l2norm=True, threads=None):
+    """Paged chunk prefill ("Replace Qwen3.5 FLA paths with Attention Gym", GDN prefill
+    ablation and Paged-state continuity): the forward whose states live in a decode
+    pool [num_slots, HV, V, K] (S itself; the chunk call's state is its transpose).
+    Sequence n starts from the transpose of pool[idx[n]] when 0 < idx[n] < num_slots and
+    has_initial_state[n] is nonzero (or not given), else from zeros; its final state is
+    written back, transposed, to every slot 0 < idx[n] < num_slots.
+
+    Returns (o [T,HV,V], new_pool, number of indices >= num_slots)."""
+    pool = np.array(pool, dtype=np.float64, copy=True, order="C")
+    idx = np.asarray(state_indices, dtype=np.int64)
+    cu = np.asarray(cu_seqlens)
+    N = len(cu) - 1
+    slots, HV, V, K = pool.shape
+    transpose = _load().gdn_oracle_get_mutation() != 10
+    h0 = np.zeros((N, HV, K, V))
+    for n in range(N):
+        s = int(idx[n])
+        if 0 < s < slots and (has_initial_state is None or has_initial_state[n]):
+            h0[n] = pool[s].transpose(0, 2, 1) if transpose else pool[s]
+    o, ht = fwd(q, k, v, g, beta, cu, scale=scale, h0=h0, use_l2norm=use_l2norm, threads=threads)
+    for n in range(N):
+        s = int(idx[n])
+        if 0 < s < slots:
+            pool[s] = ht[n].transpose(0, 2, 1) if transpose else ht[n]
+    return o, pool, int((idx >= slots).sum())

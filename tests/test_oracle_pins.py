@@ -459,6 +459,76 @@ def test_gated_rule_gradients_through_the_gate():
     check_gated_rule_gradients_through_the_gate()
 
 
+# ----------------------------------------------------------------------------- paged prefill
+def check_paged_prefill_one_token_equals_decode():
+    # a one-token prefill that resumes a slot is the decode step on that slot: the two
+    # read the pool through different code (transpose + chunk call vs the decode rule)
+    r = np.random.default_rng(71)
+    B, H, HV, K, V, slots = 3, 1, 2, 4, 4, 6
+    pool = 0.5 * r.standard_normal((slots, HV, V, K))
+    q, k = r.standard_normal((B, H, K)), r.standard_normal((B, H, K))
+    v = r.standard_normal((B, HV, V))
+    g = -np.abs(r.standard_normal((B, HV)))
+    beta = 1 / (1 + np.exp(-r.standard_normal((B, HV))))
+    idx = np.array([4, 1, 5], dtype=np.int32)
+    cu = np.arange(B + 1, dtype=np.int32)
+    o, newpool, bad = oracle.prefill_paged(q, k, v, g, beta, cu, pool, idx, scale=0.7)
+    od, pool_d, bad_d = oracle.decode(q, k, v, g, beta, pool, idx, scale=0.7)
+    assert bad == bad_d == 0
+    np.testing.assert_allclose(o, od, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(newpool, pool_d, rtol=1e-12, atol=1e-12)
+
+
+def check_paged_prefill_continues_a_sequence():
+    # "Paged-state continuity": a sequence prefilled in two calls through its slot
+    # gives the outputs and final state of one call over the whole sequence
+    c = _rand_case(72, [23], 1, 2, 4, 4, h0=False)
+    slots = 3
+    pool = np.zeros((slots, 2, 4, 4))
+    idx = np.array([2], dtype=np.int32)
+    o_all, ht_all = oracle.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu"])
+    for cut in (1, 9, 22):
+        parts = [(0, cut), (cut, 23)]
+        p = pool.copy()
+        outs = []
+        for i, (a, b) in enumerate(parts):
+            sl = slice(a, b)
+            o, p, _ = oracle.prefill_paged(c["q"][sl], c["k"][sl], c["v"][sl], c["g"][sl],
+                                           c["beta"][sl], np.array([0, b - a], dtype=np.int32), p,
+                                           idx, has_initial_state=np.array([i > 0]))
+            outs.append(o)
+        np.testing.assert_allclose(np.concatenate(outs), o_all, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(p[2], ht_all[0].transpose(0, 2, 1), rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(p[[0, 1]], pool[[0, 1]])
+
+
+def check_paged_prefill_fresh_and_null_slots():
+    c = _rand_case(73, [5, 4, 6], 1, 2, 4, 4, h0=False)
+    r = np.random.default_rng(74)
+    slots = 5
+    pool = r.standard_normal((slots, 2, 4, 4))
+    idx = np.array([3, 0, 7], dtype=np.int32)        # fresh with a slot, none, out of range
+    o, newpool, bad = oracle.prefill_paged(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu"], pool,
+                                           idx, has_initial_state=np.array([0, 1, 1]))
+    o0, ht0 = oracle.fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu"])  # all from zeros
+    assert bad == 1
+    np.testing.assert_allclose(o, o0, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(newpool[3], ht0[0].transpose(0, 2, 1), rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(newpool[[0, 1, 2, 4]], pool[[0, 1, 2, 4]])
+
+
+def test_paged_prefill_one_token_equals_decode():
+    check_paged_prefill_one_token_equals_decode()
+
+
+def test_paged_prefill_continues_a_sequence():
+    check_paged_prefill_continues_a_sequence()
+
+
+def test_paged_prefill_fresh_and_null_slots():
+    check_paged_prefill_fresh_and_null_slots()
+
+
 # ----------------------------------------------------------------------------- discrimination
 PINS = [
     lambda: check_golden("delta_rule_hand_worked.json"),
@@ -474,12 +544,15 @@ PINS = [
     check_decode_equals_one_token_chunk_call,
     check_gate_closed_forms,
     check_gate_backward_matches_finite_differences,
+    check_paged_prefill_one_token_equals_decode,
+    check_paged_prefill_continues_a_sequence,
 ]
 
 # 1 decay after the write, 2 prediction from the undecayed state, 3 output before the write,
 # 4 scale on k too, 5 epsilon outside the sqrt, 6 sign of dp flipped (backward), 7 key head hv % H,
-# 8 dbeta -> db through beta instead of beta (1 - beta), 9 da through softplus instead of its slope
-MUTATIONS = [1, 2, 3, 4, 5, 6, 7, 8, 9]
+# 8 dbeta -> db through beta instead of beta (1 - beta), 9 da through softplus instead of its slope,
+# 10 paged prefill reads and writes the slots without transposing
+MUTATIONS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10]
 
 
 @pytest.mark.parametrize("m", MUTATIONS)

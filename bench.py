@@ -481,6 +481,45 @@ def bench_ours(args):
             del vr
         line["variants"] = variants
 
+    # paged chunk prefill at the largest case of the pages' GDN prefill ablation
+    # ("Replace Qwen3.5 FLA paths with Attention Gym": N = 64 sequences, T = 8192 packed
+    # tokens, 8 key / 16 value heads, states resumed from and written back to pool
+    # slots in place; warm cache, repeated calls on fixed pointers, as there)
+    if not args.no_prefill:
+        import chunked_gated_delta_06_gb300 as gdn
+        pw = W.chunk_workload("prefill_64x128", [128] * 64, 8, 16, seed=rank, backward=False)
+        pr = np.random.default_rng([rank, 99])
+        slots = 2 * pw.N + 1
+        ppool = torch.from_numpy((0.1 * pr.standard_normal((slots, pw.HV, D, D))).astype(np.float32)).to(dev)
+        pidx = torch.from_numpy(pr.choice(np.arange(1, slots), size=pw.N, replace=False).astype(np.int32)).to(dev)
+        pq, pk, pv = _bf(torch, pw.q_bits, dev), _bf(torch, pw.k_bits, dev), _bf(torch, pw.v_bits, dev)
+        pg_, pb = torch.from_numpy(pw.g).to(dev), _bf(torch, pw.beta_bits, dev)
+        pcu = torch.from_numpy(pw.cu_seqlens).to(dev)
+        pp, pkeep = gdn.make_problem(pw.cu_seqlens, pw.H, pw.HV, cu_dev_ptr=pcu.data_ptr())
+        po = torch.empty((pw.T, pw.HV, D), dtype=torch.bfloat16, device=dev)
+        pws = torch.empty(gdn.gdn_chunk_workspace_bytes(pp, 0), dtype=torch.uint8, device=dev)
+
+        def pstep():
+            st = gdn.gdn_chunk_prefill_paged(pp, pq.data_ptr(), pk.data_ptr(), pv.data_ptr(),
+                                             pg_.data_ptr(), pb.data_ptr(), ppool.data_ptr(), slots,
+                                             pidx.data_ptr(), None, po.data_ptr(), None,
+                                             pws.data_ptr(), pws.numel(),
+                                             torch.cuda.current_stream().cuda_stream)
+            if st:
+                raise gdn.GdnError(st, "gdn_chunk_prefill_paged")
+
+        for _ in range(max(3, args.warmup)):
+            pstep()
+        psteps = max(args.steps, 20)
+        pms = _time_loop(torch, pstep, psteps)
+        line["prefill_paged"] = {
+            "metric": "paged chunk prefill us per call", "value": pms * 1e3, "unit": "us",
+            "higher_is_better": False, "tokens_per_s": pw.T / (pms / 1e3), "steps": psteps,
+            "config": {"workload": "prefill_64x128", "N": pw.N, "T": pw.T, "H": pw.H, "HV": pw.HV,
+                       "slots": slots, "cache": "warm (repeated calls on fixed pointers)",
+                       "step": "gdn_chunk_prefill_paged, every sequence resumed from its slot"}}
+        del ppool, pws
+
     # decode state bandwidth
     if not args.no_decode:
         dw = W.decode_workload(seed=rank)
@@ -600,6 +639,7 @@ def main():
                     help="chunk workload of the fwd+bwd step (the headline is fb_32k_varlen)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the paged-prefill timing")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the recompute-state, checkpointed-step and fp32-beta timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")

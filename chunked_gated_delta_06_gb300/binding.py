@@ -98,6 +98,8 @@ def lib():
             L.gdn_decode_step_gated.argtypes = ([ctypes.c_int32] * 5 + [ctypes.c_float] + [_vp] * 8
                                                 + [ctypes.c_int32] + [_vp] * 3 + [_vp])
             L.gdn_decode_step_gated.restype = ctypes.c_int
+            L.gdn_chunk_prefill_paged.argtypes = [P] + [_vp] * 6 + [ctypes.c_int32] + [_vp] * 5 + [_sz, _vp]
+            L.gdn_chunk_prefill_paged.restype = ctypes.c_int
             L.gdn_chunk_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
             L.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
             L.gdn_kernel_name.argtypes = [ctypes.c_int32]
@@ -196,6 +198,13 @@ def gdn_chunk_bwd(p, q, k, v, g, beta, initial_state, saved, d_o, d_final_state,
     return int(lib().gdn_chunk_bwd(ctypes.byref(p), q, k, v, g, beta, initial_state, saved, d_o,
                                    d_final_state, dq, dk, dv, dg, dbeta, dh0, workspace, ws_bytes,
                                    stream))
+
+
+def gdn_chunk_prefill_paged(p, q, k, v, g, beta, state_pool, num_slots, state_indices,
+                            has_initial_state, o, device_status, workspace, ws_bytes, stream) -> int:
+    return int(lib().gdn_chunk_prefill_paged(ctypes.byref(p), q, k, v, g, beta, state_pool,
+                                             num_slots, state_indices, has_initial_state, o,
+                                             device_status, workspace, ws_bytes, stream))
 
 
 def gdn_chunk_fwd_gated(p, q, k, v, a, b, A_log, dt_bias, initial_state, o, final_state, saved,
@@ -404,4 +413,26 @@ def decode_step_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, 
                                state_pool.shape[0], _ptr(state_indices), _ptr(o),
                                _ptr(device_status), _stream())
     _check(st, "gdn_decode_step_gated")
+    return o
+
+
+def chunk_prefill_paged(q, k, v, g, beta, cu_host, cu_dev, state_pool, state_indices,
+                        has_initial_state=None, scale=None, device_status=None, workspace=None):
+    """gdn_chunk_prefill_paged on torch tensors: sequence n starts from pool slot
+    state_indices[n] (zeros when the slot is <= 0 or has_initial_state[n] == 0) and its
+    final state is written back to that slot in place.  Returns o."""
+    import torch
+    T, H, K = q.shape
+    HV = v.shape[1]
+    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale, beta_dtype_of(beta))
+    p = ctx.problem
+    o = torch.empty((T, HV, v.shape[2]), dtype=torch.bfloat16, device=q.device)
+    nws = gdn_chunk_workspace_bytes(p, 0)
+    if workspace is None or workspace.numel() < nws:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
+    st = gdn_chunk_prefill_paged(p, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool),
+                                 state_pool.shape[0], _ptr(state_indices), _ptr(has_initial_state),
+                                 _ptr(o), _ptr(device_status), _ptr(workspace), workspace.numel(),
+                                 _stream())
+    _check(st, "gdn_chunk_prefill_paged")
     return o

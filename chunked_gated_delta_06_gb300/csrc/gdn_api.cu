@@ -184,16 +184,31 @@ void fill_gate(gdn::ChunkArgs &a, const Gate *gt) {
     a.dt_bias = gt->dt_bias;
 }
 
+// Paged-prefill arguments (the initial and final states live in decode-pool slots).
+struct Paged {
+    float *pool;                 // [num_slots, HV, V, K]
+    int32_t num_slots;
+    const int32_t *indices;      // device [N]
+    const int32_t *resume;       // device [N] or null
+    int32_t *status;             // device or null
+};
+
 gdn_status chunk_fwd_impl(const gdn_problem *p, const void *q, const void *k, const void *v,
                           const float *g, const void *beta, const Gate *gt,
                           const float *initial_state, void *o, float *final_state, void *saved,
                           void *workspace, size_t ws_size, gdn_stream_t stream,
-                          gdn_kernel_timer *timer) {
+                          gdn_kernel_timer *timer, const Paged *pg = nullptr) {
     Dims d;
     gdn_status st = check_problem(p, &d);
     if (st != GDN_OK) return st;
     if (d.T > 0 && (!q || !k || !v || !o)) return GDN_ERR_INVALID_ARG;
     if ((st = check_gate_inputs(d, p, g, beta, gt)) != GDN_OK) return st;
+    if (pg) {
+        if (!pg->pool || pg->num_slots < 1 || !pg->indices || !aligned16(pg->pool) ||
+            !aligned_to(pg->indices, 4) || !aligned_to(pg->resume, 4) || !aligned_to(pg->status, 4))
+            return GDN_ERR_INVALID_ARG;
+        if ((int64_t)pg->num_slots * d.HV > (int64_t)1 << 40) return GDN_ERR_INVALID_ARG;
+    }
     const void *ptrs[] = {q, k, v, initial_state, o, final_state, saved, workspace};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDN_ERR_INVALID_ARG;
@@ -209,6 +224,13 @@ gdn_status chunk_fwd_impl(const gdn_problem *p, const void *q, const void *k, co
     a.timer = timer;
     a.o = static_cast<bf16 *>(o);
     a.ht = final_state;
+    if (pg) {
+        a.pool = pg->pool;
+        a.num_slots = pg->num_slots;
+        a.pool_idx = pg->indices;
+        a.pool_resume = pg->resume;
+        a.pool_status = pg->status;
+    }
     Carver wc(workspace);
     carve_fwd_ws(wc, d, a, saved == nullptr);
     if (saved) {
@@ -376,6 +398,17 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem *p, const void *q, const void *
                                size_t ws_size, gdn_stream_t stream, gdn_kernel_timer *timer) {
     return chunk_bwd_impl(p, q, k, v, g, beta, nullptr, initial_state, saved, d_o, d_final_state,
                           dq, dk, dv, dg, dbeta, dh0, workspace, ws_size, stream, timer);
+}
+
+gdn_status gdn_chunk_prefill_paged(const gdn_problem *p, const void *q, const void *k,
+                                   const void *v, const float *g, const void *beta,
+                                   float *state_pool, int32_t num_slots,
+                                   const int32_t *state_indices, const int32_t *has_initial_state,
+                                   void *o, int32_t *device_status, void *workspace,
+                                   size_t ws_size, gdn_stream_t stream) {
+    const Paged pg{state_pool, num_slots, state_indices, has_initial_state, device_status};
+    return chunk_fwd_impl(p, q, k, v, g, beta, nullptr, nullptr, o, nullptr, nullptr, workspace,
+                          ws_size, stream, nullptr, &pg);
 }
 
 gdn_status gdn_chunk_fwd_gated(const gdn_problem *p, const void *q, const void *k, const void *v,

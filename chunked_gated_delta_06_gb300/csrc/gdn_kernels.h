@@ -27,6 +27,13 @@ struct ChunkArgs {
     // forward outputs
     bf16 *o;
     float *ht;              // or null
+    // paged prefill: the initial state of sequence n is read from, and its final state
+    // written to, pool slot pool_idx[n] ([num_slots,HV,V,K], V-major) in place
+    float *pool;            // null = h0 / ht above
+    int num_slots;
+    const int *pool_idx;    // [N] device; <= 0: no slot (zero start, final state dropped)
+    const int *pool_resume; // [N] device or null: 0 = fresh (zero start) although a slot is named
+    int *pool_status;       // device or null: set to 1 when an index >= num_slots was skipped
     // saved by the forward, read by the backward
     bf16 *hc;               // [C_total,HV,K,V] state at each chunk start
     bf16 *vnew;             // [T,HV,V]

@@ -22,7 +22,10 @@
 // the next chunk's per-token scalars are loaded a chunk ahead and published
 // during the current epilogue, and a chunk costs two block barriers.  Two CTAs
 // share an SM.  Every wait is bounded; a timeout sets status bit 2 and the CTA
-// unwinds.
+// unwinds.  In paged-prefill mode the initial state comes from, and the final
+// state goes back to, a slot of the decode state pool [slots, HV, V, K] (the
+// layout "Replace Qwen3.5 FLA paths with Attention Gym" keeps shared between
+// prefill and decode), read and written transposed in place.
 #include <string.h>
 
 #include "gdn_epi.cuh"
@@ -110,11 +113,28 @@ __global__ void __launch_bounds__(kThr, 2)
 
     if (tid == 0)
         for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, i, chunk_t0(i), h, hv, vb);
-    // h <- h0[n][hv][k][v'] (row kr, this warpgroup's 32 columns)
+    // h <- h0[n][hv][k][v'] (row kr, this warpgroup's 32 columns), or in paged mode
+    // the transpose of pool slot S[v'][k] (lanes are consecutive k: coalesced per v')
     const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb + c0;
+    int slot = 0;
+    bool resume = false;
+    if (a.pool) {
+        slot = a.pool_idx[n];
+        if (slot >= a.num_slots) {
+            if (a.pool_status && tid == 0) *a.pool_status = 1;
+            slot = 0;
+        }
+        if (slot < 0) slot = 0;
+        resume = slot > 0 && (!a.pool_resume || a.pool_resume[n] != 0);
+    }
+    float *pslot = a.pool ? a.pool + (((size_t)slot * a.HV + hv) * kDim + 64 * vb + c0) * kDim + kr
+                          : nullptr;  // S[v'][kr] of this thread's first column
     {
         float r[32];
-        if (a.h0) {
+        if (a.pool) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = resume ? pslot[(size_t)j * kDim] : 0.f;
+        } else if (a.h0) {
             const float4 *src = reinterpret_cast<const float4 *>(a.h0 + sbase);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -253,6 +273,13 @@ __global__ void __launch_bounds__(kThr, 2)
         float4 *dst = reinterpret_cast<float4 *>(a.ht + sbase);
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+    }
+    if (ok && a.pool && slot > 0) {  // final state back into the slot, transposed
+        float r[32];
+        tmem_ld32(tH, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pslot[(size_t)j * kDim] = r[j];
     }
     if (tid == 0) tma_store_wait_all();
     if (!ok && tid == 0) {

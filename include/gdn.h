@@ -136,6 +136,33 @@ gdn_status gdn_chunk_fwd_noalloc(const gdn_problem *p, const void *q, const void
                                  const float *initial_state, void *o, float *final_state,
                                  gdn_stream_t stream);
 
+/* Paged chunk prefill ("Replace Qwen3.5 FLA paths with Attention Gym"
+ * (torchtitan #4389), GDN prefill ablation and Paged-state continuity): the
+ * forward of gdn_chunk_fwd whose states live in the decode state pool, so a
+ * prefill advances the slots in place with no gather / scatter copies.
+ *   q, k, v, g, beta, o   as in gdn_chunk_fwd (forward only: nothing saved)
+ *   state_pool            fp32 [num_slots, HV, V, K] (V-major, the layout of
+ *                         gdn_decode_step), updated in place
+ *   state_indices         int32 [N] on the device: the slot of sequence n; a
+ *                         slot <= 0 is none: the sequence starts from zeros
+ *                         and its final state is dropped; a slot >= num_slots
+ *                         is skipped the same way and flagged in device_status
+ *   has_initial_state     int32 [N] on the device, or NULL (= all nonzero):
+ *                         nonzero resumes from the slot's state, 0 starts the
+ *                         sequence fresh from zeros; the final state of every
+ *                         sequence with a slot is written to that slot
+ *   device_status         int32 on the device, or NULL
+ *   workspace             ws_bytes >= gdn_chunk_workspace_bytes(p, 0)
+ * Two sequences naming the same slot race (a caller error).  The results are
+ * the bits of gdn_chunk_fwd with initial_state[n] = the transpose of the slot
+ * (or zeros) and final_state[n] copied back transposed. */
+gdn_status gdn_chunk_prefill_paged(const gdn_problem *p, const void *q, const void *k,
+                                   const void *v, const float *g, const void *beta,
+                                   float *state_pool, int32_t num_slots,
+                                   const int32_t *state_indices, const int32_t *has_initial_state,
+                                   void *o, int32_t *device_status, void *workspace,
+                                   size_t ws_bytes, gdn_stream_t stream);
+
 /* Backward of chunk_gated_delta_rule.  q ... initial_state exactly as passed
  * to the gdn_chunk_fwd that filled `saved` (not modified since).
  *   saved          the buffer gdn_chunk_fwd filled, or NULL for recompute-state

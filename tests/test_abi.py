@@ -177,3 +177,19 @@ def test_gated_calls_check_their_arguments_before_any_launch(lib):
     assert dec(A=None) == binding.GDN_ERR_INVALID_ARG
     assert dec(b=fake + 1) == binding.GDN_ERR_INVALID_ARG
     assert dec(batch=0) == binding.GDN_OK
+
+
+def test_paged_prefill_checks_its_arguments_before_any_launch(lib):
+    fake = 0x10000
+    p, keep = _problem([0, 5, 9])
+
+    def call(pool=fake, slots=8, idx=fake, resume=None, status=None, ws=1 << 40):
+        return gdn.gdn_chunk_prefill_paged(p, fake, fake, fake, fake, fake, pool, slots, idx, resume,
+                                           fake, status, fake, ws, None)
+    assert call(pool=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(pool=fake + 4) == binding.GDN_ERR_INVALID_ARG
+    assert call(slots=0) == binding.GDN_ERR_INVALID_ARG
+    assert call(idx=None) == binding.GDN_ERR_INVALID_ARG
+    assert call(idx=fake + 2) == binding.GDN_ERR_INVALID_ARG
+    assert call(resume=fake + 1) == binding.GDN_ERR_INVALID_ARG
+    assert call(ws=1024) == binding.GDN_ERR_WORKSPACE_TOO_SMALL

@@ -75,6 +75,8 @@ def lib():
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_chunk_saved_bytes.argtypes = [P]
             L.gdn_chunk_saved_bytes.restype = _sz
+            L.gdn_chunk_scan_plan.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+            L.gdn_chunk_scan_plan.restype = ctypes.c_int
             L.gdn_chunk_workspace_bytes.argtypes = [P, ctypes.c_int]
             L.gdn_chunk_workspace_bytes.restype = _sz
             L.gdn_chunk_fwd.argtypes = [P] + [_vp] * 10 + [_sz, _vp]
@@ -167,6 +169,13 @@ def make_problem(cu_host, H, HV, K=128, V=128, scale=0.0, cu_dev_ptr=0, beta_dty
 
 def gdn_chunk_saved_bytes(p: GdnProblem) -> int:
     return int(lib().gdn_chunk_saved_bytes(ctypes.byref(p)))
+
+
+def gdn_chunk_scan_plan(p: GdnProblem):
+    """(status, seg_len, num_segments) of the forward state scan of a problem."""
+    sl, ns = ctypes.c_int32(), ctypes.c_int32()
+    st = int(lib().gdn_chunk_scan_plan(ctypes.byref(p), ctypes.byref(sl), ctypes.byref(ns)))
+    return st, int(sl.value), int(ns.value)
 
 
 def gdn_chunk_workspace_bytes(p: GdnProblem, for_backward: int) -> int:

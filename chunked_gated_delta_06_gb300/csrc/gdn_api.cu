@@ -2,6 +2,7 @@
 // validation (before any launch), carving of the caller's saved / workspace
 // buffers, and the launch order of the chunk and decode kernels.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/gdn.h"
@@ -31,7 +32,73 @@ struct Dims {
     int N, T, H, HV, C;  // C = chunk count
     float scale;
     int beta_f32;        // beta / dbeta are fp32 (else bf16); fused-gating calls need bf16
+    int seg_len, seg_max;  // segment-parallel forward scan (seg_len 0: not split)
 };
+
+// Plan of the forward state scan.  A scan CTA walks the chunks of one (sequence,
+// value head, value half) one after another, so a few long sequences leave most of
+// the GPU idle.  Cutting every sequence into segments of L chunks lets segment 0
+// and the pre-scans of segments 1 .. S-2 run at once (pass 1; a pre-scan carries
+// the 128 transition columns as well, so it is two CTAs more per value head), then
+// segments 1 .. S-1 re-scan from their stitched start states (pass 2).  The model
+// counts scan steps: a pass takes max(its longest CTA, its CTA-steps / the number of
+// resident scan CTAs), with 2 per SM on 152 SMs; the stitch costs half a step per
+// segment plus three steps for the extra launches.  The plan is a pure function of
+// the problem (the same bits on every device): a split is taken only when the model
+// gains at least 20 % and its buffers stay under 1 GiB.
+// GDN_SCAN_SEGMENT_CHUNKS in the environment overrides the model: 0 never splits, L > 0
+// cuts every sequence into segments of L chunks whenever that gives 3 or more.
+void plan_segments(const gdn_problem *p, Dims *d) {
+    d->seg_len = 0;
+    d->seg_max = 1;
+    const double slots = 2.0 * 152.0;
+    const int N = d->N, HV = d->HV;
+    int longest = 0;
+    double total = 0.0;
+    for (int n = 0; n < N; ++n) {
+        const int c = (p->cu_seqlens_host[n + 1] - p->cu_seqlens_host[n] + gdn::kChunk - 1) / gdn::kChunk;
+        longest = c > longest ? c : longest;
+        total += c;
+    }
+    if (const char *ov = getenv("GDN_SCAN_SEGMENT_CHUNKS")) {
+        const int L = atoi(ov);
+        const int smax = L > 0 ? (longest + L - 1) / L : 0;
+        if (L > 0 && smax >= 3 && smax <= 4096) {
+            d->seg_len = L;
+            d->seg_max = smax;
+        }
+        return;
+    }
+    if (longest < 24) return;
+    const double t0 = fmax((double)longest, 2.0 * HV * total / slots);
+    double best = 0.8 * t0;
+    static const int cand[] = {8, 12, 16, 24, 32, 48, 64, 96, 128, 192, 256, 384, 512};
+    for (int L : cand) {
+        int smax = 1;
+        double w1 = 0.0, w2 = 0.0;
+        for (int n = 0; n < N; ++n) {
+            const int c = (p->cu_seqlens_host[n + 1] - p->cu_seqlens_host[n] + gdn::kChunk - 1) / gdn::kChunk;
+            const int S = c > 0 ? (c + L - 1) / L : 1;
+            smax = S > smax ? S : smax;
+            if (S == 1) {
+                w1 += 2.0 * HV * c;
+            } else {
+                w1 += 2.0 * HV * L + 4.0 * HV * L * (S - 2);
+                w2 += 2.0 * HV * (c - L);
+            }
+        }
+        if (smax < 3 || smax > 64) continue;
+        const double bytes = (double)N * (smax - 1) * HV * (3.0 * gdn::kDim * gdn::kDim * 4.0);
+        if (bytes > 1073741824.0) continue;
+        const double chain1 = fmin((double)L, (double)longest);
+        const double t = fmax(chain1, w1 / slots) + fmax((double)L, w2 / slots) + 0.5 * (smax - 2) + 3.0;
+        if (t < best) {
+            best = t;
+            d->seg_len = L;
+            d->seg_max = smax;
+        }
+    }
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_to(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -61,6 +128,7 @@ gdn_status check_problem(const gdn_problem *p, Dims *d) {
     d->C = (int)chunks;
     d->scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->head_dim_k);
     d->beta_f32 = p->beta_dtype == GDN_DTYPE_F32;
+    plan_segments(p, d);
     return GDN_OK;
 }
 
@@ -85,9 +153,20 @@ void carve_table(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.status = cv.take<int>(1);
 }
 
+// Segment buffers of a split forward scan (none when the scan is not split).
+void carve_segments(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
+    a.seg_len = d.seg_len;
+    a.seg_max = d.seg_max;
+    if (d.seg_len == 0) return;
+    const size_t recs = (size_t)d.N * (d.seg_max - 1) * d.HV;
+    a.seg_end = cv.take<float>(recs * gdn::kDim * 2 * gdn::kDim);
+    a.seg_start = cv.take<float>(recs * gdn::kDim * gdn::kDim);
+}
+
 void carve_fwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a, bool with_saved) {
     carve_table(cv, d, a);
     a.u = cv.take<bf16>((size_t)d.T * d.HV * gdn::kDim);
+    carve_segments(cv, d, a);
     if (with_saved) carve_saved(cv, d, a);
 }
 
@@ -123,7 +202,10 @@ size_t ws_bytes(const Dims &d, int mode) {
         carve_fwd_ws(cv, d, a, true);
     } else {
         carve_bwd_ws(cv, d, a);
-        if (mode == 2) carve_saved(cv, d, a);
+        if (mode == 2) {
+            carve_saved(cv, d, a);
+            carve_segments(cv, d, a);
+        }
     }
     return cv.used();
 }
@@ -284,6 +366,7 @@ gdn_status chunk_bwd_impl(const gdn_problem *p, const void *q, const void *k, co
     carve_bwd_ws(wc, d, a);
     if (recompute) {
         carve_saved(wc, d, a);
+        carve_segments(wc, d, a);
         a.u = a.dvloc;  // read by the recomputed state scan before dv_loc is written
     } else {
         Carver sc(const_cast<void *>(saved));
@@ -371,6 +454,16 @@ size_t gdn_chunk_saved_bytes(const gdn_problem *p) {
     Dims d;
     if (check_problem(p, &d) != GDN_OK) return 0;
     return saved_bytes(d);
+}
+
+gdn_status gdn_chunk_scan_plan(const gdn_problem *p, int32_t *seg_len, int32_t *num_segments) {
+    Dims d;
+    const gdn_status st = check_problem(p, &d);
+    if (st != GDN_OK) return st;
+    if (!seg_len || !num_segments) return GDN_ERR_INVALID_ARG;
+    *seg_len = d.seg_len;
+    *num_segments = d.seg_len ? d.seg_max : 1;
+    return GDN_OK;
 }
 
 size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward) {
@@ -488,7 +581,7 @@ gdn_status gdn_decode_step(int32_t batch, int32_t num_k_heads, int32_t num_v_hea
 const char *gdn_kernel_name(int32_t id) {
     static const char *names[GDN_KERNEL_COUNT] = {
         "plan", "prep", "intra", "state", "out", "dvloc", "bstate", "bintra_a", "bintra_b",
-        "bnorm", "decode"};
+        "bnorm", "decode", "seg_stitch"};
     return (id >= 0 && id < GDN_KERNEL_COUNT) ? names[id] : "unknown";
 }
 

@@ -45,6 +45,11 @@ struct ChunkArgs {
     int *seq_chunk_off, *chunk_seq, *chunk_start, *chunk_len;
     int *seq_order;         // [N] sequences by decreasing length (scans start the longest first)
     int *status;            // device int, nonzero = inconsistent device cu_seqlens
+    // segment-parallel forward state scan (seg_len = 0: one piece per sequence)
+    int seg_len;            // chunks per segment
+    int seg_max;            // largest segment count of any sequence (>= 3 when seg_len > 0)
+    float *seg_end;         // [N,seg_max-1,HV,K,2K] end states of segment 0 and the pre-scans: [h | Phi]
+    float *seg_start;       // [N,seg_max-1,HV,K,V] start states of segments 1 .. S-1
     // forward scratch
     bf16 *u;                // [T,HV,V]
     // backward

@@ -57,15 +57,16 @@ struct StateMaps {
     CUtensorMap w, k, u, hc;
 };
 
+// w, K and (unless the columns are a transition's, whose u is zero) this half of u
 __device__ __forceinline__ void issue_stage(const StateMaps &m, StateSmem &sm, int st, int t0, int h,
-                                            int hv, int vb) {
+                                            int hv, int vb, bool with_u) {
     unsigned char *b = sm.stage[st];
-    mbar_arrive_expect_tx(&sm.tma_bar[st], kStageBytes);
+    mbar_arrive_expect_tx(&sm.tma_bar[st], with_u ? kStageBytes : kStageBytes - kBox);
     tma_load_3d(b + 0 * kBox, &m.w, 0, hv, t0, &sm.tma_bar[st]);
     tma_load_3d(b + 1 * kBox, &m.w, 64, hv, t0, &sm.tma_bar[st]);
     tma_load_3d(b + 2 * kBox, &m.k, 0, h, t0, &sm.tma_bar[st]);
     tma_load_3d(b + 3 * kBox, &m.k, 64, h, t0, &sm.tma_bar[st]);
-    tma_load_3d(b + 4 * kBox, &m.u, 64 * vb, hv, t0, &sm.tma_bar[st]);
+    if (with_u) tma_load_3d(b + 4 * kBox, &m.u, 64 * vb, hv, t0, &sm.tma_bar[st]);
 }
 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -73,26 +74,46 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&t);
 }
 
+// pass 0: every sequence in one piece.  Segment-parallel scan (sequences cut into
+// segments of a.seg_len chunks, S segments): pass 1 runs segment 0 from the
+// initial state (all outputs, end state to seg_end) beside the pre-scans of
+// segments 1 .. S-2, which start from h = 0 with the transition columns
+// [h | Phi] (Phi from the identity, u = 0 there) and store only their end state;
+// k_seg_stitch turns those into the start states of segments 1 .. S-1; pass 2
+// re-scans those segments from them with every output.
 __global__ void __launch_bounds__(kThr, 2)
-    k_state_tc(const ChunkArgs a, const __grid_constant__ StateMaps maps) {
+    k_state_tc(const ChunkArgs a, const __grid_constant__ StateMaps maps, int pass) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     StateSmem &sm = *reinterpret_cast<StateSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hv = blockIdx.x >> 1, vb = blockIdx.x & 1;
-    const int n = a.seq_order[blockIdx.y];  // longest sequences first
+    const int ncol = pass == 1 ? 4 : 2;            // column blocks of 64 per value head
+    const int hv = blockIdx.x / ncol, cbk = blockIdx.x % ncol;
+    const bool phi = cbk >= 2;                     // transition columns (pass 1 only)
+    const int vb = cbk & 1;
+    const int nsy = pass ? a.seg_max - 1 : 1;
+    const int n = a.seq_order[blockIdx.y / nsy];   // longest sequences first
     const int h = hv / (a.HV / a.H);
     const int cb = a.seq_chunk_off[n];
     const int ce = min(a.seq_chunk_off[n + 1], a.num_chunks);
-    const int nch = max(ce - cb, 0);
+    const int nseq = max(ce - cb, 0);              // chunks of the sequence
+    const int S = pass ? max(1, (nseq + a.seg_len - 1) / a.seg_len) : 1;
+    const int sg = pass == 2 ? blockIdx.y % nsy + 1 : (pass ? blockIdx.y % nsy : 0);
+    if (pass == 1 && !(S == 1 ? (sg == 0 && !phi) : (sg == 0 ? !phi : sg <= S - 2))) return;
+    if (pass == 2 && !(S >= 2 && sg <= S - 1)) return;
+    const bool from_input = sg == 0;               // h0 / pool slot (else zero or seg_start)
+    const bool pre = pass == 1 && sg >= 1;         // pre-scan: no per-chunk outputs
+    const bool to_final = pass == 0 || (pass == 1 && S == 1) || (pass == 2 && sg == S - 1);
+    const int jb = pass ? sg * a.seg_len : 0;      // first chunk of the segment
+    const int nch = pass ? max(0, min(a.seg_len, nseq - jb)) : nseq;
     const int grp = warp >> 2, sub = warp & 3;
     const int kr = sub * 32 + lane;     // state row (TMEM lane) of the state pass
     const int c0 = 32 * grp;            // this warpgroup's 32 of the 64 columns
     // the sequence's chunks are consecutive 64-token blocks of [ts0, ts1)
-    const int ts0 = nch > 0 ? a.chunk_start[cb] : 0;
-    const int ts1 = nch > 0 ? a.chunk_start[ce - 1] + a.chunk_len[ce - 1] : 0;
-    auto chunk_t0 = [&](int j) { return ts0 + 64 * j; };
-    auto chunk_len = [&](int j) { return min(64, ts1 - (ts0 + 64 * j)); };
+    const int ts0 = nseq > 0 ? a.chunk_start[cb] : 0;
+    const int ts1 = nseq > 0 ? a.chunk_start[ce - 1] + a.chunk_len[ce - 1] : 0;
+    auto chunk_t0 = [&](int j) { return ts0 + 64 * (jb + j); };
+    auto chunk_len = [&](int j) { return min(64, ts1 - chunk_t0(j)); };
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 128);
@@ -112,7 +133,7 @@ __global__ void __launch_bounds__(kThr, 2)
     const uint32_t tH = t_row + c0, tP = t_row + 64 + c0;          // this warpgroup's columns
 
     if (tid == 0)
-        for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, i, chunk_t0(i), h, hv, vb);
+        for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, i, chunk_t0(i), h, hv, vb, !phi);
     // h <- h0[n][hv][k][v'] (row kr, this warpgroup's 32 columns), or in paged mode
     // the transpose of pool slot S[v'][k] (lanes are consecutive k: coalesced per v')
     const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb + c0;
@@ -129,9 +150,26 @@ __global__ void __launch_bounds__(kThr, 2)
     }
     float *pslot = a.pool ? a.pool + (((size_t)slot * a.HV + hv) * kDim + 64 * vb + c0) * kDim + kr
                           : nullptr;  // S[v'][kr] of this thread's first column
+    // segment buffers: seg_end[n][s][hv][k][256] (h | Phi), seg_start[n][s-1][hv][k][128]
+    const size_t seg_row = (size_t)kr * (2 * kDim) + (phi ? kDim : 0) + 64 * vb + c0;
+    float *send = pass == 1 ? a.seg_end + (((size_t)n * (a.seg_max - 1) + sg) * a.HV + hv) * kDim * 2 * kDim +
+                                  seg_row
+                            : nullptr;
     {
         float r[32];
-        if (a.pool) {
+        if (pre) {  // h from zero; Phi from the identity (row k, column k' = 64 vb + c0 + j)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = (phi && kr == 64 * vb + c0 + j) ? 1.f : 0.f;
+        } else if (!from_input) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                a.seg_start + (((size_t)n * (a.seg_max - 1) + sg - 1) * a.HV + hv) * kDim * kDim +
+                (size_t)kr * kDim + 64 * vb + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = src[q];
+                r[4 * q] = x.x; r[4 * q + 1] = x.y; r[4 * q + 2] = x.z; r[4 * q + 3] = x.w;
+            }
+        } else if (a.pool) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = resume ? pslot[(size_t)j * kDim] : 0.f;
         } else if (a.h0) {
@@ -179,7 +217,7 @@ __global__ void __launch_bounds__(kThr, 2)
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0; i < nch; ++i) {
-        const int c = cb + i, st = i & 1;
+        const int c = cb + jb + i, st = i & 1;
         const int t0 = chunk_t0(i), L = chunk_len(i);
         // 1. h -> bf16 operand (copied to h_c by TMA below), then h <- e^{G_L} h
         {
@@ -210,8 +248,10 @@ __global__ void __launch_bounds__(kThr, 2)
                 mma_bf16(tbase + 64, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
                          sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
             mma_commit(&sm.mma_bar);
-            tma_store_3d(&maps.hc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_s);  // h_c rows (k)
-            tma_store_commit();
+            if (!pre) {
+                tma_store_3d(&maps.hc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_s);  // h_c rows (k)
+                tma_store_commit();
+            }
         }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
@@ -231,11 +271,12 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int col = c0 + 8 * k + cq;
-                const float2 ua = epi::get_pair(us, ra, col), ub = epi::get_pair(us, rb, col);
+                const float2 ua = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, ra, col);
+                const float2 ub = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, rb, col);
                 const float va0 = la ? ua.x - p[4 * k] : 0.f, va1 = la ? ua.y - p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? ub.x - p[4 * k + 2] : 0.f, vb1 = lb ? ub.y - p[4 * k + 3] : 0.f;
-                if (la) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
-                if (lb) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                if (la && !pre) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                if (lb && !pre) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
                 epi::put_pair(sm.a_v, ra, col, va0 * cfa, va1 * cfa);
                 epi::put_pair(sm.a_v, rb, col, vb0 * cfb, vb1 * cfb);
             }
@@ -262,11 +303,11 @@ __global__ void __launch_bounds__(kThr, 2)
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
-        if (tid == 0 && ok && i + 2 < nch) issue_stage(maps, sm, st, chunk_t0(i + 2), h, hv, vb);
+        if (tid == 0 && ok && i + 2 < nch) issue_stage(maps, sm, st, chunk_t0(i + 2), h, hv, vb, !phi);
         egl = egl_next;
     }
     ok = __syncthreads_and(ok);
-    if (ok && a.ht) {
+    if (ok && to_final && a.ht) {
         float r[32];
         tmem_ld32(tH, r);
         tmem_ld_wait();
@@ -274,12 +315,20 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
-    if (ok && a.pool && slot > 0) {  // final state back into the slot, transposed
+    if (ok && to_final && a.pool && slot > 0) {  // final state back into the slot, transposed
         float r[32];
         tmem_ld32(tH, r);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) pslot[(size_t)j * kDim] = r[j];
+    }
+    if (ok && pass == 1 && !to_final) {  // a segment's end state (h columns, and Phi in a pre-scan)
+        float r[32];
+        tmem_ld32(tH, r);
+        tmem_ld_wait();
+        float4 *dst = reinterpret_cast<float4 *>(send);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
     if (tid == 0) tma_store_wait_all();
     if (!ok && tid == 0) {
@@ -291,6 +340,50 @@ __global__ void __launch_bounds__(kThr, 2)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 128);
+}
+
+// Start states of segments 1 .. S-1 of every split sequence: H_1 = end of segment 0,
+// H_{s+1} = Phi_s H_s + beta_s (Phi_s, beta_s from the pre-scan of segment s).
+// grid (8 HV, N): 16 value columns of one (sequence, value head) per CTA; thread t
+// owns row k = t / 2 and 8 columns; sums run over k' in order (fp32).
+__global__ void __launch_bounds__(256) k_seg_stitch(const ChunkArgs a) {
+    const int hv = blockIdx.x >> 3, v0 = 16 * (blockIdx.x & 7), n = blockIdx.y;
+    const int nseq = max(0, min(a.seq_chunk_off[n + 1], a.num_chunks) - a.seq_chunk_off[n]);
+    const int S = max(1, (nseq + a.seg_len - 1) / a.seg_len);
+    if (S < 2) return;
+    __shared__ float H[kDim][16];
+    const int t = threadIdx.x, k = t >> 1, cc = 8 * (t & 1);
+    const size_t eh = (size_t)kDim * 2 * kDim;  // floats of one (segment, head) end record
+    auto end_rec = [&](int sg) { return a.seg_end + (((size_t)n * (a.seg_max - 1) + sg) * a.HV + hv) * eh; };
+    {
+        const float *e0 = end_rec(0) + (size_t)k * 2 * kDim + v0 + cc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) H[k][cc + j] = e0[j];
+    }
+    __syncthreads();
+    for (int sg = 1; sg <= S - 1; ++sg) {
+        float *dst = a.seg_start + (((size_t)n * (a.seg_max - 1) + sg - 1) * a.HV + hv) * kDim * kDim +
+                     (size_t)k * kDim + v0 + cc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = H[k][cc + j];
+        if (sg == S - 1) break;
+        const float *rec = end_rec(sg) + (size_t)k * 2 * kDim;  // row k: beta_s [0, K), Phi_s [K, 2K)
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        for (int k2 = 0; k2 < kDim; k2 += 4) {
+            const float4 ph = *reinterpret_cast<const float4 *>(rec + kDim + k2);
+            const float pv[4] = {ph.x, ph.y, ph.z, ph.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] += pv[u] * H[k2 + u][cc + j];
+        }
+        __syncthreads();  // every thread has read H
+#pragma unroll
+        for (int j = 0; j < 8; ++j) H[k][cc + j] = acc[j] + rec[v0 + cc + j];
+        __syncthreads();
+    }
 }
 
 }  // namespace
@@ -309,8 +402,24 @@ cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
+    if (a.seg_len == 0) {
+        TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
+        k_state_tc<<<dim3(2 * a.HV, a.N), kThr, smem, s>>>(a, m, 0);
+        return cudaGetLastError();
+    }
+    const unsigned ny = (unsigned)a.N * (unsigned)(a.seg_max - 1);
+    {
+        TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
+        k_state_tc<<<dim3(4 * a.HV, ny), kThr, smem, s>>>(a, m, 1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    {
+        TimerScope ts(a.timer, GDN_KERNEL_SEG_STITCH, s);
+        k_seg_stitch<<<dim3(8 * a.HV, a.N), 256, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
-    k_state_tc<<<dim3(2 * a.HV, a.N), kThr, smem, s>>>(a, m);
+    k_state_tc<<<dim3(2 * a.HV, ny), kThr, smem, s>>>(a, m, 2);
     return cudaGetLastError();
 }
 

@@ -98,6 +98,23 @@ size_t gdn_chunk_saved_bytes(const gdn_problem *p);
  * another for_backward value. */
 size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward);
 
+/* How the forward state scan of this problem is run (a pure host function of
+ * the problem; the same plan on every device, so the same bits).  A scan walks
+ * the chunks of a sequence one after another; when a few long sequences would
+ * leave the GPU idle, every sequence is cut into segments of *seg_len chunks
+ * (segment-parallel scan: the transitions of the segments are scanned at once,
+ * stitched, and the segments re-scanned from their start states, as the
+ * pre-scan + stitch of the context-parallel state scans in "[Cake 1/13] gdn:
+ * ...", Review items, and the GDN context-parallel m-scan of "Qwen3.5-397B RL
+ * trainer on 128 v7x").  *seg_len = 0 and *num_segments = 1 when the scan is
+ * not split; otherwise *num_segments is the largest segment count of any
+ * sequence.  The split changes the rounding of the states (not their values
+ * beyond it) and adds its buffers to both workspace queries.  The environment
+ * variable GDN_SCAN_SEGMENT_CHUNKS, read by every host call, overrides the
+ * plan: 0 never splits, L > 0 cuts every sequence into segments of L chunks
+ * whenever some sequence then has 3 or more. */
+gdn_status gdn_chunk_scan_plan(const gdn_problem *p, int32_t *seg_len, int32_t *num_segments);
+
 /* Forward of chunk_gated_delta_rule.
  *   q, k           bf16 [T, H, 128]
  *   v              bf16 [T, HV, 128]
@@ -278,6 +295,7 @@ enum {
     GDN_KERNEL_BINTRA_B,     /* backward: intra-chunk terms, WY pullback, dg */
     GDN_KERNEL_BNORM,        /* backward: sum over value heads, L2-norm backward */
     GDN_KERNEL_DECODE,       /* decode step */
+    GDN_KERNEL_SEG_STITCH,   /* segment-parallel state scan: start states of the segments */
     GDN_KERNEL_COUNT
 };
 

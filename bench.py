@@ -520,48 +520,33 @@ def bench_ours(args):
                        "step": "gdn_chunk_prefill_paged, every sequence resumed from its slot"}}
         del ppool, pws
 
-    # segment-parallel forward state scan: one long sequence with few value heads (the
-    # case the plain scan leaves the GPU idle in), forward with the planned split and
-    # with the split turned off (GDN_SCAN_SEGMENT_CHUNKS=0), device-timed
+    # segment-parallel state scans: one long sequence with few value heads (the case
+    # the plain scans leave the GPU idle in), fwd+bwd with the planned split and with
+    # the split turned off (GDN_SCAN_SEGMENT_CHUNKS=0), device-timed
     if not args.no_segscan:
         import chunked_gated_delta_06_gb300 as gdn
-        sw = W.chunk_workload("fwd_1x65536_hv16", [65536], 8, 16, seed=rank, h0=True, backward=False)
-        sq, sk, sv = _bf(torch, sw.q_bits, dev), _bf(torch, sw.k_bits, dev), _bf(torch, sw.v_bits, dev)
-        sg, sb = torch.from_numpy(sw.g).to(dev), _bf(torch, sw.beta_bits, dev)
-        sh0 = torch.from_numpy(sw.h0).to(dev)
-        scu = torch.from_numpy(sw.cu_seqlens).to(dev)
+        sw = W.chunk_workload("fb_1x65536_hv16", [65536], 8, 16, seed=rank, h0=True, backward=True,
+                              d_ht=True)
         seg = {}
         for label, env in (("split", None), ("plain", "0")):
             if env is not None:
                 os.environ["GDN_SCAN_SEGMENT_CHUNKS"] = env
             try:
-                sp, skeep = gdn.make_problem(sw.cu_seqlens, sw.H, sw.HV, cu_dev_ptr=scu.data_ptr())
-                _, seg_len, nseg = gdn.gdn_chunk_scan_plan(sp)
-                so = torch.empty((sw.T, sw.HV, D), dtype=torch.bfloat16, device=dev)
-                sht = torch.empty((1, sw.HV, D, D), dtype=torch.float32, device=dev)
-                sws = torch.empty(gdn.gdn_chunk_workspace_bytes(sp, 0), dtype=torch.uint8, device=dev)
-
-                def sstep(timer=None):
-                    st = gdn.gdn_chunk_fwd(sp, sq.data_ptr(), sk.data_ptr(), sv.data_ptr(), sg.data_ptr(),
-                                           sb.data_ptr(), sh0.data_ptr(), so.data_ptr(), sht.data_ptr(),
-                                           None, sws.data_ptr(), sws.numel(),
-                                           torch.cuda.current_stream().cuda_stream, timer)
-                    if st:
-                        raise gdn.GdnError(st, "gdn_chunk_fwd")
-
+                sr = ChunkRunner(torch, sw, dev)
+                _, seg_len, nseg = gdn.gdn_chunk_scan_plan(sr.p)
                 for _ in range(3):
-                    sstep()
-                sms = _time_loop(torch, sstep, 5)
-                sper = _kernel_table(torch, sstep, 3, 16)
-                seg[label] = {"ms_per_call": sms, "tokens_per_s": sw.T / (sms / 1e3), "seg_len": seg_len,
-                              "segments": nseg,
-                              "scan_ms": sum(statistics.mean(v) * (len(v) // 3) for k_, v in sper.items()
-                                             if k_ in ("state", "seg_stitch"))}
-                del sws
+                    sr.step()
+                sms = _time_loop(torch, sr.step, 5)
+                sper = _kernel_table(torch, sr.step, 3, 32)
+                scan = {k_: statistics.mean(v) * (len(v) // 3) for k_, v in sper.items()
+                        if k_ in ("state", "bstate", "seg_stitch")}
+                seg[label] = {"ms_per_step": sms, "tokens_per_s": sw.T / (sms / 1e3), "seg_len": seg_len,
+                              "segments": nseg, "scan_ms": scan}
+                del sr
             finally:
                 os.environ.pop("GDN_SCAN_SEGMENT_CHUNKS", None)
-        line["segscan"] = {"config": {"workload": "fwd_1x65536_hv16", "T": sw.T, "N": 1, "H": sw.H,
-                                      "HV": sw.HV, "step": "gdn_chunk_fwd (no saved buffer)"}, **seg}
+        line["segscan"] = {"config": {"workload": "fb_1x65536_hv16", "T": sw.T, "N": 1, "H": sw.H,
+                                      "HV": sw.HV, "step": STEP_MODES["saved"]}, **seg}
 
     # decode state bandwidth
     if not args.no_decode:

@@ -182,6 +182,7 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.dkp2 = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dGp = cv.take<float>((size_t)d.T * d.HV);
     a.gpart = cv.take<float>((size_t)d.C * d.HV * 2);
+    carve_segments(cv, d, a);  // the reverse scan's segments (shared with a recomputed forward)
 }
 
 size_t saved_bytes(const Dims &d) {
@@ -202,10 +203,7 @@ size_t ws_bytes(const Dims &d, int mode) {
         carve_fwd_ws(cv, d, a, true);
     } else {
         carve_bwd_ws(cv, d, a);
-        if (mode == 2) {
-            carve_saved(cv, d, a);
-            carve_segments(cv, d, a);
-        }
+        if (mode == 2) carve_saved(cv, d, a);
     }
     return cv.used();
 }
@@ -366,7 +364,6 @@ gdn_status chunk_bwd_impl(const gdn_problem *p, const void *q, const void *k, co
     carve_bwd_ws(wc, d, a);
     if (recompute) {
         carve_saved(wc, d, a);
-        carve_segments(wc, d, a);
         a.u = a.dvloc;  // read by the recomputed state scan before dv_loc is written
     } else {
         Carver sc(const_cast<void *>(saved));

@@ -23,7 +23,8 @@
 // Q and w after step 4; every tile of the chunk after that is prefetched into L2
 // a step ahead.  The next chunk's per-token scalars are loaded a step ahead and
 // published during the current epilogue; a chunk costs two block barriers.
-// Waits are bounded.
+// Waits are bounded.  Long sequences with few heads can be scanned segment-
+// parallel (the plan of the forward scan; see k_bstate_tc).
 #include <string.h>
 
 #include "gdn_epi.cuh"
@@ -69,12 +70,16 @@ __device__ __forceinline__ void issue_xd(const BStateMaps &m, BStateSmem &sm, in
     tma_load_3d(sm.x + 3 * kBox, &m.dl, 64 * vb, hv, t0, &sm.xd_bar);
 }
 
-// L2 prefetch of every tile of one chunk (loaded a step later)
-__device__ __forceinline__ void prefetch_chunk(const BStateMaps &m, int t0, int h, int hv, int vb) {
+// L2 prefetch of every tile of one chunk (loaded a step later); transition columns
+// read no dO / dv_loc
+__device__ __forceinline__ void prefetch_chunk(const BStateMaps &m, int t0, int h, int hv, int vb,
+                                               bool with_d) {
     tma_prefetch_3d(&m.k, 0, h, t0);
     tma_prefetch_3d(&m.k, 64, h, t0);
-    tma_prefetch_3d(&m.dO, 64 * vb, hv, t0);
-    tma_prefetch_3d(&m.dl, 64 * vb, hv, t0);
+    if (with_d) {
+        tma_prefetch_3d(&m.dO, 64 * vb, hv, t0);
+        tma_prefetch_3d(&m.dl, 64 * vb, hv, t0);
+    }
     tma_prefetch_3d(&m.q, 0, h, t0);
     tma_prefetch_3d(&m.q, 64, h, t0);
     tma_prefetch_3d(&m.w, 0, hv, t0);
@@ -94,26 +99,49 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&t);
 }
 
+// pass 0: every sequence in one piece.  Segment-parallel reverse scan (the forward
+// scan's segments of a.seg_len chunks, walked from the last): pass 1 scans the last
+// segment from d(final state) (all outputs, end state to seg_end) beside the
+// pre-scans of segments S-2 .. 1, which start from dh = 0 with the transition
+// columns [dh | Psi] (Psi from the identity, dO = dv_loc = 0 there) and store only
+// their end state; k_seg_stitch turns those into the start states (the gradient
+// after each segment's last chunk) of segments S-2 .. 0; pass 2 re-scans them.
+// Segment records are indexed by rho = S - 1 - segment.
+template <int pass>
 __global__ void __launch_bounds__(kThr, 2)
     k_bstate_tc(const ChunkArgs a, const __grid_constant__ BStateMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BStateSmem &sm = *reinterpret_cast<BStateSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hv = blockIdx.x >> 1, vb = blockIdx.x & 1;
-    const int n = a.seq_order[blockIdx.y];  // longest sequences first
+    const int ncol = pass == 1 ? 4 : 2;            // column blocks of 64 per value head
+    const int hv = blockIdx.x / ncol, cbk = blockIdx.x % ncol;
+    const bool phi = pass == 1 && cbk >= 2;        // transition columns (pass 1 only)
+    const int vb = cbk & 1;
+    const int nsy = pass ? a.seg_max - 1 : 1;
+    const int n = a.seq_order[blockIdx.y / nsy];   // longest sequences first
     const int h = hv / (a.HV / a.H);
     const int cb = a.seq_chunk_off[n];
     const int ce = min(a.seq_chunk_off[n + 1], a.num_chunks);
-    const int nch = max(ce - cb, 0);
+    const int nseq = max(ce - cb, 0);
+    const int S = pass ? max(1, (nseq + a.seg_len - 1) / a.seg_len) : 1;
+    const int rho = pass == 2 ? blockIdx.y % nsy + 1 : (pass ? blockIdx.y % nsy : 0);
+    if (pass == 1 && !(S == 1 ? (rho == 0 && !phi) : (rho == 0 ? !phi : rho <= S - 2))) return;
+    if (pass == 2 && !(S >= 2 && rho <= S - 1)) return;
+    const bool from_input = rho == 0;              // d(final state) (else zero or seg_start)
+    const bool pre = pass == 1 && rho >= 1;        // pre-scan: no per-chunk outputs
+    const bool to_final = pass == 0 || (pass == 1 && S == 1) || (pass == 2 && rho == S - 1);
+    const int sgm = S - 1 - rho;                   // the segment, in chunk order
+    const int jend = pass ? min(nseq, (sgm + 1) * a.seg_len) : nseq;  // one past its last chunk
+    const int nch = pass ? max(0, jend - sgm * a.seg_len) : nseq;
     const int grp = warp >> 2, sub = warp & 3;
     const int kr = sub * 32 + lane;     // state row (TMEM lane) of step 1
     const int c0 = 32 * grp;            // this warpgroup's 32 of the 64 columns
     // the sequence's chunks are consecutive 64-token blocks of [ts0, ts1); the
-    // i-th step of the reverse walk handles block nch - 1 - i
-    const int ts0 = nch > 0 ? a.chunk_start[cb] : 0;
-    const int ts1 = nch > 0 ? a.chunk_start[ce - 1] + a.chunk_len[ce - 1] : 0;
-    auto step_t0 = [&](int i) { return ts0 + 64 * (nch - 1 - i); };
+    // i-th step of the reverse walk handles block jend - 1 - i
+    const int ts0 = nseq > 0 ? a.chunk_start[cb] : 0;
+    const int ts1 = nseq > 0 ? a.chunk_start[ce - 1] + a.chunk_len[ce - 1] : 0;
+    auto step_t0 = [&](int i) { return ts0 + 64 * (jend - 1 - i); };
     auto step_len = [&](int i) { return min(64, ts1 - step_t0(i)); };
 
     if (warp == 0) {
@@ -137,15 +165,32 @@ __global__ void __launch_bounds__(kThr, 2)
     int xk_issued = 0, xd_issued = 0, y_issued = 0;  // thread 0's load counts
     if (tid == 0 && nch > 0) {
         issue_xk(maps, sm, step_t0(0), h);
-        issue_xd(maps, sm, step_t0(0), hv, vb);
+        if (!phi) issue_xd(maps, sm, step_t0(0), hv, vb);
         issue_y(maps, sm, step_t0(0), h, hv);
-        if (nch > 1) prefetch_chunk(maps, step_t0(1), h, hv, vb);
-        xk_issued = xd_issued = y_issued = 1;
+        if (nch > 1) prefetch_chunk(maps, step_t0(1), h, hv, vb, !phi);
+        xk_issued = y_issued = 1;
+        xd_issued = phi ? 0 : 1;
     }
     const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb + c0;
+    // segment buffers: seg_end[n][rho][hv][k][256] (dh | Psi), seg_start[n][rho-1][hv][k][128]
+    float *send = pass == 1 ? a.seg_end + (((size_t)n * (a.seg_max - 1) + rho) * a.HV + hv) * kDim * 2 * kDim +
+                                  (size_t)kr * (2 * kDim) + (phi ? kDim : 0) + 64 * vb + c0
+                            : nullptr;
     {
         float r[32];
-        if (a.d_ht) {
+        if (pre) {  // dh from zero; Psi from the identity (row k, column k' = 64 vb + c0 + j)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = (phi && kr == 64 * vb + c0 + j) ? 1.f : 0.f;
+        } else if (!from_input) {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                a.seg_start + (((size_t)n * (a.seg_max - 1) + rho - 1) * a.HV + hv) * kDim * kDim +
+                (size_t)kr * kDim + 64 * vb + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = src[q];
+                r[4 * q] = x.x; r[4 * q + 1] = x.y; r[4 * q + 2] = x.z; r[4 * q + 3] = x.w;
+            }
+        } else if (a.d_ht) {
             const float4 *src = reinterpret_cast<const float4 *>(a.d_ht + sbase);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -194,7 +239,7 @@ __global__ void __launch_bounds__(kThr, 2)
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0; i < nch; ++i) {
-        const int c = ce - 1 - i;
+        const int c = cb + jend - 1 - i;
         const uint32_t par = i & 1;
         const int t0 = step_t0(i), L = step_len(i);
         // 1. dh' -> bf16 operand (copied to dh_c by TMA below), then dh <- e^{G_L} dh'
@@ -214,7 +259,7 @@ __global__ void __launch_bounds__(kThr, 2)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        const bool gx = mbar_wait(&sm.xk_bar, par) && mbar_wait(&sm.xd_bar, par);
+        const bool gx = mbar_wait(&sm.xk_bar, par) && (phi || mbar_wait(&sm.xd_bar, par));
         ok = __syncthreads_and(ok && gx);
         if (!ok) break;
         // 2. Pd = K dh'
@@ -226,13 +271,15 @@ __global__ void __launch_bounds__(kThr, 2)
                 mma_bf16(tbase + 64, sdesc(ks + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
                          sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
             mma_commit(&sm.mma_bar);
-            tma_store_3d(&maps.dhc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_ds);  // dh_c rows (k)
-            tma_store_commit();
+            if (!pre) {
+                tma_store_3d(&maps.dhc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_ds);  // dh_c rows (k)
+                tma_store_commit();
+            }
         }
         // meanwhile: c_t dO on the fragment positions used below (rows ra, ra + 8,
-        // columns c0 + 8k + cq + {0, 1})
+        // columns c0 + 8k + cq + {0, 1}); transition columns have no dO term
         const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
-        {
+        if (!phi) {
             const float qa = sm.qc[i & 1][ra], qb = sm.qc[i & 1][rb];
             const unsigned char *dos = sm.x + 2 * kBox;
 #pragma unroll
@@ -263,11 +310,12 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int col = c0 + 8 * k + cq;
-                const float2 la2 = epi::get_pair(dls, ra, col), lb2 = epi::get_pair(dls, rb, col);
+                const float2 la2 = phi ? make_float2(0.f, 0.f) : epi::get_pair(dls, ra, col);
+                const float2 lb2 = phi ? make_float2(0.f, 0.f) : epi::get_pair(dls, rb, col);
                 const float va0 = la ? la2.x + ka * p[4 * k] : 0.f, va1 = la ? la2.y + ka * p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? lb2.x + kb * p[4 * k + 2] : 0.f, vb1 = lb ? lb2.y + kb * p[4 * k + 3] : 0.f;
-                if (la) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
-                if (lb) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                if (la && !pre) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                if (lb && !pre) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
                 epi::put_pair(sm.a_dv, ra, col, -va0, -va1);
                 epi::put_pair(sm.a_dv, rb, col, -vb0, -vb1);
             }
@@ -288,18 +336,19 @@ __global__ void __launch_bounds__(kThr, 2)
             tc_fence_after();
             const uint32_t ado = smem_u32(sm.a_do), adv = smem_u32(sm.a_dv);
             const uint32_t qs = smem_u32(sm.y), ws = smem_u32(sm.y + 2 * kBox);
+            if (!phi)
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase, sdesc(qs + s * 2048, kBox, 1024), sdesc(ado + s * 2048, kBox, 1024), idS, true);
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tbase, sdesc(qs + s * 2048, kBox, 1024), sdesc(ado + s * 2048, kBox, 1024), idS, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase, sdesc(ws + s * 2048, kBox, 1024), sdesc(adv + s * 2048, kBox, 1024), idS, true);
             mma_commit(&sm.mma_bar);
-            if (i + 1 < nch) {
+            if (i + 1 < nch && !phi) {
                 issue_xd(maps, sm, step_t0(i + 1), hv, vb);
                 ++xd_issued;
             }
-            if (i + 2 < nch) prefetch_chunk(maps, step_t0(i + 2), h, hv, vb);
+            if (i + 2 < nch) prefetch_chunk(maps, step_t0(i + 2), h, hv, vb, !phi);
         }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
@@ -311,11 +360,19 @@ __global__ void __launch_bounds__(kThr, 2)
         egl = egl_next;
     }
     ok = __syncthreads_and(ok);
-    if (ok && a.dh0) {
+    if (ok && to_final && a.dh0) {
         float r[32];
         tmem_ld32(tS, r);
         tmem_ld_wait();
         float4 *dst = reinterpret_cast<float4 *>(a.dh0 + sbase);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+    }
+    if (ok && pass == 1 && !to_final) {  // a segment's end state (dh columns, and Psi in a pre-scan)
+        float r[32];
+        tmem_ld32(tS, r);
+        tmem_ld_wait();
+        float4 *dst = reinterpret_cast<float4 *>(send);
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
@@ -348,11 +405,25 @@ cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BStateSmem) + 1024;
     static_assert(2 * (sizeof(BStateSmem) + 2048) <= 233472, "two CTAs per SM");
-    cudaError_t e = cudaFuncSetAttribute(k_bstate_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    for (const void *f : {(const void *)k_bstate_tc<0>, (const void *)k_bstate_tc<1>, (const void *)k_bstate_tc<2>})
+        if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+            return e;
+    if (a.seg_len == 0) {
+        TimerScope ts(a.timer, GDN_KERNEL_BSTATE, s);
+        k_bstate_tc<0><<<dim3(2 * a.HV, a.N), kThr, smem, s>>>(a, m);
+        return cudaGetLastError();
+    }
+    const unsigned ny = (unsigned)a.N * (unsigned)(a.seg_max - 1);
+    {
+        TimerScope ts(a.timer, GDN_KERNEL_BSTATE, s);
+        k_bstate_tc<1><<<dim3(4 * a.HV, ny), kThr, smem, s>>>(a, m);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if ((e = launch_seg_stitch(a, s)) != cudaSuccess) return e;
     TimerScope ts(a.timer, GDN_KERNEL_BSTATE, s);
-    k_bstate_tc<<<dim3(2 * a.HV, a.N), kThr, smem, s>>>(a, m);
+    k_bstate_tc<2><<<dim3(2 * a.HV, ny), kThr, smem, s>>>(a, m);
     return cudaGetLastError();
 }
 

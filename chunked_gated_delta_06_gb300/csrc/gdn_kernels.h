@@ -113,6 +113,7 @@ cudaError_t launch_gate_reduce(const ChunkArgs &a, cudaStream_t s);       // dA_
 cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s);
+cudaError_t launch_seg_stitch(const ChunkArgs &a, cudaStream_t s);  // segment start states
 cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_out_tc(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_dvloc_tc(const ChunkArgs &a, cudaStream_t s);

@@ -81,15 +81,16 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
 // [h | Phi] (Phi from the identity, u = 0 there) and store only their end state;
 // k_seg_stitch turns those into the start states of segments 1 .. S-1; pass 2
 // re-scans those segments from them with every output.
+template <int pass>
 __global__ void __launch_bounds__(kThr, 2)
-    k_state_tc(const ChunkArgs a, const __grid_constant__ StateMaps maps, int pass) {
+    k_state_tc(const ChunkArgs a, const __grid_constant__ StateMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     StateSmem &sm = *reinterpret_cast<StateSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ncol = pass == 1 ? 4 : 2;            // column blocks of 64 per value head
     const int hv = blockIdx.x / ncol, cbk = blockIdx.x % ncol;
-    const bool phi = cbk >= 2;                     // transition columns (pass 1 only)
+    const bool phi = pass == 1 && cbk >= 2;        // transition columns (pass 1 only)
     const int vb = cbk & 1;
     const int nsy = pass ? a.seg_max - 1 : 1;
     const int n = a.seq_order[blockIdx.y / nsy];   // longest sequences first
@@ -343,7 +344,8 @@ __global__ void __launch_bounds__(kThr, 2)
 }
 
 // Start states of segments 1 .. S-1 of every split sequence: H_1 = end of segment 0,
-// H_{s+1} = Phi_s H_s + beta_s (Phi_s, beta_s from the pre-scan of segment s).
+// H_{s+1} = Phi_s H_s + beta_s (Phi_s, beta_s from the pre-scan of segment s).  The
+// reverse scan uses the same records in reverse segment order (Psi_rho, beta'_rho).
 // grid (8 HV, N): 16 value columns of one (sequence, value head) per CTA; thread t
 // owns row k = t / 2 and 8 columns; sums run over k' in order (fp32).
 __global__ void __launch_bounds__(256) k_seg_stitch(const ChunkArgs a) {
@@ -388,6 +390,12 @@ __global__ void __launch_bounds__(256) k_seg_stitch(const ChunkArgs a) {
 
 }  // namespace
 
+cudaError_t launch_seg_stitch(const ChunkArgs &a, cudaStream_t s) {
+    TimerScope ts(a.timer, GDN_KERNEL_SEG_STITCH, s);
+    k_seg_stitch<<<dim3(8 * a.HV, a.N), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
     StateMaps m;
     memset(&m, 0, sizeof(m));
@@ -399,27 +407,25 @@ cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(StateSmem) + 1024;
     static_assert(2 * (sizeof(StateSmem) + 2048) <= 233472, "two CTAs per SM");
-    cudaError_t e = cudaFuncSetAttribute(k_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    for (const void *f : {(const void *)k_state_tc<0>, (const void *)k_state_tc<1>, (const void *)k_state_tc<2>})
+        if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+            return e;
     if (a.seg_len == 0) {
         TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
-        k_state_tc<<<dim3(2 * a.HV, a.N), kThr, smem, s>>>(a, m, 0);
+        k_state_tc<0><<<dim3(2 * a.HV, a.N), kThr, smem, s>>>(a, m);
         return cudaGetLastError();
     }
     const unsigned ny = (unsigned)a.N * (unsigned)(a.seg_max - 1);
     {
         TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
-        k_state_tc<<<dim3(4 * a.HV, ny), kThr, smem, s>>>(a, m, 1);
+        k_state_tc<1><<<dim3(4 * a.HV, ny), kThr, smem, s>>>(a, m);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    {
-        TimerScope ts(a.timer, GDN_KERNEL_SEG_STITCH, s);
-        k_seg_stitch<<<dim3(8 * a.HV, a.N), 256, 0, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    if ((e = launch_seg_stitch(a, s)) != cudaSuccess) return e;
     TimerScope ts(a.timer, GDN_KERNEL_STATE, s);
-    k_state_tc<<<dim3(2 * a.HV, ny), kThr, smem, s>>>(a, m, 2);
+    k_state_tc<2><<<dim3(2 * a.HV, ny), kThr, smem, s>>>(a, m);
     return cudaGetLastError();
 }
 

@@ -86,6 +86,7 @@ KERNELS = {  # ncu kernel name -> (bench kernel name, source file)
     "k_out_tc<1>": ("out", "gdn_out_tc.cu"), "k_out_tc<0>": ("dvloc", "gdn_out_tc.cu"),
     "k_out_tc<true>": ("out", "gdn_out_tc.cu"), "k_out_tc<false>": ("dvloc", "gdn_out_tc.cu"),
     "k_bstate_tc": ("bstate", "gdn_bstate_tc.cu"), "k_bintra_a_tc": ("bintra_a", "gdn_bintra_tc.cu"),
+    "k_state_tc<0>": ("state", "gdn_state_tc.cu"), "k_bstate_tc<0>": ("bstate", "gdn_bstate_tc.cu"),
     "k_bintra_b_tc": ("bintra_b", "gdn_bintra_b_tc.cu"), "k_decode": ("decode", "gdn_decode.cu"),
     "k_bnorm": ("bnorm", "gdn_chunk.cu"), "k_prep": ("prep", "gdn_chunk.cu"),
 }

@@ -1,7 +1,7 @@
-"""GPU parity of the segment-parallel forward state scan (a long sequence cut into
-segments: pass 1 scans segment 0 beside the pre-scans of the transitions of
-segments 1 .. S-2, k_seg_stitch forms the segments' start states, pass 2 re-scans
-them; "[Cake 1/13] gdn: ...", Review items: pre-scan + stitch; "Qwen3.5-397B RL
+"""GPU parity of the segment-parallel state scans (a long sequence cut into
+segments: pass 1 scans the first segment -- the last one in the reverse scan --
+beside the pre-scans of the transitions of the inner segments, k_seg_stitch forms
+the segments' start states, pass 2 re-scans them; "[Cake 1/13] gdn: ...", Review items: pre-scan + stitch; "Qwen3.5-397B RL
 trainer on 128 v7x", GDN context-parallel m-scan).  Each case asserts that the
 plan really splits, then compares with the fp64 oracle, whose per-token forward
 has no segments at all.  Tolerance: |x - ref| <= 1e-2 max|ref| + 1e-2 |ref|.
@@ -82,10 +82,11 @@ def test_split_paged_prefill_matches_the_oracle():
 
 
 def test_split_and_plain_scans_agree(monkeypatch):
-    wl = W.chunk_workload("seg_vs_plain", [8192, 700], 2, 4, seed=46, h0=True, backward=False)
+    wl = W.chunk_workload("seg_vs_plain", [8192, 700], 2, 4, seed=46, h0=True, backward=True,
+                          d_ht=True)
     split = run_chunk(wl, torch)
     monkeypatch.setenv("GDN_SCAN_SEGMENT_CHUNKS", "0")
     assert _plan(wl) == (0, 1)
     plain = run_chunk(wl, torch)
-    close("o", split["o"], plain["o"])
-    close("final_state", split["ht"], plain["ht"])
+    for key in ("o", "ht", "dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        close(key, split[key], plain[key])

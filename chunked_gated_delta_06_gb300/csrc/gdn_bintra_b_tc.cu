@@ -2,8 +2,8 @@
 // pullback" of "cake_gdn: deterministic chunked GDN training kernels",
 // section 2).
 //
-// One CTA of 256 threads per (chunk, value head), about 100 KB of shared memory
-// and 256 TMEM columns, so that two CTAs share an SM.  With Khat = diag(1/r_k) K,
+// Persistent CTAs of 256 threads, two per SM (about 100 KB of shared memory and
+// 256 TMEM columns each), each walking a run of (chunk, value head) units.  With Khat = diag(1/r_k) K,
 // Gamma_ij = exp(G_i - G_j), the WY inverse T (saved in bf16 by the forward) and dW =
 // -dv_new h^T (from the h / dh' kernel):
 //   phase 1 (M=64 N=64 K=128, rows = tokens):  KK = K K^T, D1 = dW K^T, D2 = dv_new V^T
@@ -59,7 +59,7 @@ struct BwSmem {
     float G[64], beta[64], rki[64], eg[64], dG[64], db[64];
     float rs[2][64];               // per-warpgroup partial row sums of P2
     float cy[4][64], cz[4][64], cp[4][64];  // per-row-block column sums
-    uint64_t tma_bar, mma_bar;
+    uint64_t a_bar, v_bar, mma_bar;
     uint32_t tmem_base;
 };
 
@@ -67,16 +67,51 @@ struct BwMaps {
     CUtensorMap k, v, dw, dvn, t;
 };
 
+struct BwUnit {
+    int c, hv, h, t0, L;
+};
+
+__device__ __forceinline__ BwUnit bw_unit(const ChunkArgs &a, int u) {
+    BwUnit x;
+    x.c = u / a.HV;
+    x.hv = u - x.c * a.HV;
+    x.h = x.hv / (a.HV / a.H);
+    x.t0 = a.chunk_start[x.c];
+    x.L = a.chunk_len[x.c];
+    return x;
+}
+
+// group A: K, dW, dv_new and T (free once phase 2 has run); group V: V (free after phase 1)
+__device__ __forceinline__ void issue_a(const BwMaps &m, BwSmem &sm, const ChunkArgs &a, const BwUnit &x) {
+    mbar_arrive_expect_tx(&sm.a_bar, 3 * kTile + kHalf);
+    tma_load_3d(sm.op_t, &m.t, 0, 0, (x.c * a.HV + x.hv) * 64, &sm.a_bar);  // T rows (bf16)
+    tma_load_3d(sm.k, &m.k, 0, x.h, x.t0, &sm.a_bar);
+    tma_load_3d(sm.k + kHalf, &m.k, 64, x.h, x.t0, &sm.a_bar);
+    tma_load_3d(sm.dw, &m.dw, 0, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.dw + kHalf, &m.dw, 64, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.dvn, &m.dvn, 0, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.dvn + kHalf, &m.dvn, 64, x.hv, x.t0, &sm.a_bar);
+}
+
+__device__ __forceinline__ void issue_v(const BwMaps &m, BwSmem &sm, const BwUnit &x) {
+    mbar_arrive_expect_tx(&sm.v_bar, kTile);
+    tma_load_3d(sm.v, &m.v, 0, x.hv, x.t0, &sm.v_bar);
+    tma_load_3d(sm.v + kHalf, &m.v, 64, x.hv, x.t0, &sm.v_bar);
+}
+
+// Persistent: CTA b walks the units [b per, (b + 1) per) (unit u = chunk u / HV, value
+// head u % HV), two CTAs per SM.  The next unit's V loads as soon as phase 1 has read
+// this one's, its K, dW, dv_new and T as soon as phase 2 has, and its per-token scalars
+// a unit ahead, so the loads run under the epilogues.
 __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
-                                                         const __grid_constant__ BwMaps maps) {
+                                                         const __grid_constant__ BwMaps maps, int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     BwSmem &sm = *reinterpret_cast<BwSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hv = blockIdx.y;
-    const int h = hv / (a.HV / a.H);
-    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-    if (L <= 0) return;
+    const int nunits = a.num_chunks * a.HV;
+    const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
+    if (ub >= ue) return;
     const int grp = warp >> 2;                // warpgroup: which half of the columns
     const int sub = warp & 3;                 // TMEM lane quarter
 
@@ -85,275 +120,307 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&sm.tma_bar, 1);
+        mbar_init(&sm.a_bar, 1);
+        mbar_init(&sm.v_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    BwUnit x = bw_unit(a, ub);
     if (tid == 0) {
-        mbar_arrive_expect_tx(&sm.tma_bar, 4 * kTile + kHalf);
-        tma_load_3d(sm.op_t, &maps.t, 0, 0, (c * a.HV + hv) * 64, &sm.tma_bar);  // T rows (bf16)
-        const CUtensorMap *mk[4] = {&maps.k, &maps.v, &maps.dw, &maps.dvn};
-        unsigned char *dst[4] = {sm.k, sm.v, sm.dw, sm.dvn};
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-            const int hh = x == 0 ? h : hv;
-            tma_load_3d(dst[x], mk[x], 0, hh, t0, &sm.tma_bar);
-            tma_load_3d(dst[x] + kHalf, mk[x], 64, hh, t0, &sm.tma_bar);
+        issue_a(maps, sm, a, x);
+        issue_v(maps, sm, x);
+    }
+    int a_issued = 1, v_issued = 1, waited = 0;  // same on every thread
+    // per-token scalars of thread tid < 64, fetched one unit ahead
+    float pG = 0.f, pB = 0.f, pR = 1.f, pD = 0.f;
+    auto fetch = [&](const BwUnit &y) {
+        if (tid < 64 && tid < y.L) {
+            const size_t gi = (size_t)(y.t0 + tid) * a.HV + y.hv;
+            pG = a.G[gi];
+            pB = load_beta(a, gi);
+            pR = a.rk[(size_t)(y.t0 + tid) * a.H + y.h];
+            pD = a.dGp[gi];
+        } else {
+            pG = 0.f; pB = 0.f; pR = 1.f; pD = 0.f;
         }
-    }
-    if (tid < 64) {
-        const bool in = tid < L;
-        const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
-        const float gg = in ? a.G[gi] : 0.f;
-        sm.G[tid] = gg;
-        sm.beta[tid] = in ? load_beta(a, gi) : 0.f;
-        sm.rki[tid] = in ? 1.f / a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
-        sm.eg[tid] = in ? __expf(gg) : 0.f;
-        sm.dG[tid] = in ? a.dGp[gi] : 0.f;
-    }
-    bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
+    };
+    fetch(x);
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(sub * 32) << 16);
     uint32_t phase = 0;
-    auto commit_wait = [&](bool &okr) {
-        okr = __syncthreads_and(okr && mbar_wait(&sm.mma_bar, phase));
-        phase ^= 1;
-        tc_fence_after();
-    };
-    // ---- phase 1: KK, D1, D2 (64 x 64, contraction 128)
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 64, 0, 0);
-        const uint32_t A[3] = {smem_u32(sm.k), smem_u32(sm.dw), smem_u32(sm.dvn)};
-        const uint32_t B[3] = {smem_u32(sm.k), smem_u32(sm.k), smem_u32(sm.v)};
-        const uint32_t col[3] = {cKK, cD1, cD2};
-#pragma unroll
-        for (int p = 0; p < 3; ++p)
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-                mma_bf16(tb + col[p], sdesc(A[p] + off, 16, 1024), sdesc(B[p] + off, 16, 1024), id, s > 0);
-            }
-        mma_commit(&sm.mma_bar);
-    }
-    commit_wait(ok);
-    // M=64 epilogues read 16x256b fragments: lane t of warp (grp, sub) holds rows
-    // ra = 16 sub + t/4 and rb = ra + 8, columns j0 + 8k + 2 (t % 4) + {0, 1}.
-    const int j0 = 32 * grp;                  // this warpgroup's columns
-    const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
-    const bool la = ra < L, lb = rb < L;
-    const int ccol = j0 + colsum_frag_col(lane);  // the column whose sums this lane keeps
-    if (ok) {  // dT rows (bf16 operand) and the column sums of T (.) D1, T (.) s
-        float d1[16], d2[16];
-        tmem_ld16x256_x4(t_row + cD1 + j0, d1);
-        tmem_ld16x256_x4(t_row + cD2 + j0, d2);
-        tmem_ld_wait();
-        float z[8], y[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int j = j0 + 8 * k + cq + p;
-                const float f1 = sm.eg[j] * sm.rki[j], bj = sm.beta[j];
-                const float sa = f1 * d1[4 * k + p] + d2[4 * k + p];
-                const float sb = f1 * d1[4 * k + 2 + p] + d2[4 * k + 2 + p];
-                const float2 ta = get_pair(sm.op_t, ra, j0 + 8 * k + cq);   // T is zero above the diagonal
-                const float2 tb2 = get_pair(sm.op_t, rb, j0 + 8 * k + cq);
-                const float tva = la ? (p ? ta.y : ta.x) : 0.f, tvb = lb ? (p ? tb2.y : tb2.x) : 0.f;
-                z[2 * k + p] = tva * d1[4 * k + p] + tvb * d1[4 * k + 2 + p];
-                y[2 * k + p] = tva * sa + tvb * sb;
-                d2[4 * k + p] = (la && j < ra) ? bj * sa : 0.f;        // dT, in place
-                d2[4 * k + 2 + p] = (lb && j < rb) ? bj * sb : 0.f;
-            }
-            put_pair(sm.op_dx, ra, j0 + 8 * k + cq, d2[4 * k], d2[4 * k + 1]);
-            put_pair(sm.op_dx, rb, j0 + 8 * k + cq, d2[4 * k + 2], d2[4 * k + 3]);
+    bool ok = true;
+    for (int u = ub; u < ue; ++u) {
+        const bool has_next = u + 1 < ue;
+        const BwUnit nx = has_next ? bw_unit(a, u + 1) : x;
+        const int c = x.c, hv = x.hv, t0 = x.t0, L = x.L;
+        if (tid < 64) {
+            const bool in = tid < L;
+            sm.G[tid] = pG;
+            sm.beta[tid] = pB;
+            sm.rki[tid] = in ? 1.f / pR : 1.f;
+            sm.eg[tid] = in ? __expf(pG) : 0.f;
+            sm.dG[tid] = pD;
         }
-        sm.cz[sub][ccol] = colsum_frag(z, lane);
-        sm.cy[sub][ccol] = colsum_frag(y, lane);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- phase 1b: X = dT T^T  (A = dT rows, B = T rows as [N][K])
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 64, 0, 0);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_bf16(tb + cX, sdesc(smem_u32(sm.op_dx) + s * 32, 16, 1024),
-                     sdesc(smem_u32(sm.op_t) + s * 32, 16, 1024), id, s > 0);
-        mma_commit(&sm.mma_bar);
-    }
-    commit_wait(ok);
-    if (ok) {  // X rows -> bf16 over the dT rows (the product that read them is done)
-        float x[16];
-        tmem_ld16x256_x4(t_row + cX + j0, x);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            put_pair(sm.op_dx, ra, j0 + 8 * k + cq, x[4 * k], x[4 * k + 1]);
-            put_pair(sm.op_dx, rb, j0 + 8 * k + cq, x[4 * k + 2], x[4 * k + 3]);
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- phase 1c: T^T X  (A = T rows read MN-major, B = X rows read MN-major)
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 64, 1, 1);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_bf16(tb + cA, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024),
-                     sdesc(smem_u32(sm.op_dx) + s * 2048, kHalf, 1024), id, s > 0);
-        mma_commit(&sm.mma_bar);
-    }
-    commit_wait(ok);
-    if (ok) {  // dA = -(T^T X): B and its operands, P2 row sums, column sums of beta_i P2
-        float ta[16], kk[16];
-        tmem_ld16x256_x4(t_row + cA + j0, ta);
-        tmem_ld16x256_x4(t_row + cKK + j0, kk);
-        tmem_ld_wait();
-        const float Ga = sm.G[ra], Gb = sm.G[rb];
-        const float ba = sm.beta[ra], bb = sm.beta[rb];
-        const float rka = sm.rki[ra], rkb = sm.rki[rb];
-        float rsa = 0.f, rsb = 0.f, pb[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float b1[4], b2[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j = j0 + 8 * k + cq + (e & 1);
-                const bool up = e & 2;                       // row rb
-                const int r = up ? rb : ra;
-                const float msk = ((up ? lb : la) && j < r) ? 1.f : 0.f;
-                const float dag = -ta[4 * k + e] * msk * __expf(fminf((up ? Gb : Ga) - sm.G[j], 0.f));
-                const float rkj = sm.rki[j], br = up ? bb : ba, rkr = up ? rkb : rka;
-                const float p2 = dag * kk[4 * k + e] * rkr * rkj;
-                if (up) rsb += p2; else rsa += p2;
-                b1[e] = dag * br * rkj;   // B_rj / r_k,j
-                b2[e] = dag * br * rkr;   // B_rj / r_k,r
-                kk[4 * k + e] = br * p2;  // beta_r P2_rj
-            }
-            pb[2 * k] = kk[4 * k] + kk[4 * k + 2];
-            pb[2 * k + 1] = kk[4 * k + 1] + kk[4 * k + 3];
-            put_pair(sm.op_b, ra, j0 + 8 * k + cq, b1[0], b1[1]);
-            put_pair(sm.op_b, rb, j0 + 8 * k + cq, b1[2], b1[3]);
-            put_pair(sm.op_bt, ra, j0 + 8 * k + cq, b2[0], b2[1]);
-            put_pair(sm.op_bt, rb, j0 + 8 * k + cq, b2[2], b2[3]);
-        }
-        sm.cp[sub][ccol] = colsum_frag(pb, lane);
-        rsa = quad_sum(rsa);
-        rsb = quad_sum(rsb);
-        if ((lane & 3) == 0) {
-            sm.rs[grp][ra] = rsa;
-            sm.rs[grp][rb] = rsb;
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // ---- phase 2 (M=128: row d of each product is TMEM lane d, column m is a token)
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        const uint32_t kA = smem_u32(sm.k), wA = smem_u32(sm.dw), vA = smem_u32(sm.dvn);
-        const uint32_t tB = smem_u32(sm.op_t), bB = smem_u32(sm.op_b), btB = smem_u32(sm.op_bt);
-        const uint32_t id_mk = idesc_bf16(128, 64, 1, 0);  // A MN-major, B K-major
-        const uint32_t id_mm = idesc_bf16(128, 64, 1, 1);  // A MN-major, B MN-major
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const uint64_t aK = sdesc(kA + s * 2048, kHalf, 1024);
-            mma_bf16(tb + cDK, aK, sdesc(bB + s * 32, 16, 1024), id_mk, s > 0);
-            mma_bf16(tb + cDK, aK, sdesc(btB + s * 2048, kHalf, 1024), id_mm, true);
-            mma_bf16(tb + cWT, sdesc(wA + s * 2048, kHalf, 1024), sdesc(tB + s * 2048, kHalf, 1024), id_mm,
-                     s > 0);
-            mma_bf16(tb + cUT, sdesc(vA + s * 2048, kHalf, 1024), sdesc(tB + s * 2048, kHalf, 1024), id_mm,
-                     s > 0);
-        }
-        mma_commit(&sm.mma_bar);
-    }
-    // meanwhile: dbeta and this kernel's dG terms per token m (fixed order)
-    if (ok && tid < 64) {
-        const int m = tid;
-        const float r2 = sm.rs[0][m] + sm.rs[1][m];
-        const float cy = ((sm.cy[0][m] + sm.cy[1][m]) + sm.cy[2][m]) + sm.cy[3][m];
-        const float cz = ((sm.cz[0][m] + sm.cz[1][m]) + sm.cz[2][m]) + sm.cz[3][m];
-        const float cp = ((sm.cp[0][m] + sm.cp[1][m]) + sm.cp[2][m]) + sm.cp[3][m];
-        const float bm = sm.beta[m];
-        sm.db[m] = r2 + cy;
-        sm.dG[m] += bm * r2 - cp + bm * sm.eg[m] * sm.rki[m] * cz;
-    }
-    commit_wait(ok);
-    if (ok) {  // thread d: element d of the token rows m in [32 grp, 32 grp + 32)
-        const int d = sub * 32 + lane;
-        const size_t base = ((size_t)t0 * a.HV + hv) * kDim + d;
-        const size_t ts = (size_t)a.HV * kDim;
+        if (has_next) fetch(nx);
         {
-            float dk[32], wt[32];
-            tmem_ld32(t_row + cDK + j0, dk);
-            tmem_ld32(t_row + cWT + j0, wt);
+            const bool got = mbar_wait(&sm.a_bar, waited & 1) && mbar_wait(&sm.v_bar, waited & 1);
+            ok = __syncthreads_and(ok && got);
+            ++waited;
+            if (!ok) break;
+        }
+        auto commit_wait = [&](bool &okr) {
+            okr = __syncthreads_and(okr && mbar_wait(&sm.mma_bar, phase));
+            phase ^= 1;
+            tc_fence_after();
+        };
+        // ---- phase 1: KK, D1, D2 (64 x 64, contraction 128)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(64, 64, 0, 0);
+            const uint32_t A[3] = {smem_u32(sm.k), smem_u32(sm.dw), smem_u32(sm.dvn)};
+            const uint32_t B[3] = {smem_u32(sm.k), smem_u32(sm.k), smem_u32(sm.v)};
+            const uint32_t col[3] = {cKK, cD1, cD2};
+    #pragma unroll
+            for (int p = 0; p < 3; ++p)
+    #pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
+                    mma_bf16(tb + col[p], sdesc(A[p] + off, 16, 1024), sdesc(B[p] + off, 16, 1024), id, s > 0);
+                }
+            mma_commit(&sm.mma_bar);
+        }
+        commit_wait(ok);
+        if (tid == 0 && ok && has_next) issue_v(maps, sm, nx);  // V has been read by phase 1
+        if (ok && has_next) ++v_issued;
+        // M=64 epilogues read 16x256b fragments: lane t of warp (grp, sub) holds rows
+        // ra = 16 sub + t/4 and rb = ra + 8, columns j0 + 8k + 2 (t % 4) + {0, 1}.
+        const int j0 = 32 * grp;                  // this warpgroup's columns
+        const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+        const bool la = ra < L, lb = rb < L;
+        const int ccol = j0 + colsum_frag_col(lane);  // the column whose sums this lane keeps
+        if (ok) {  // dT rows (bf16 operand) and the column sums of T (.) D1, T (.) s
+            float d1[16], d2[16];
+            tmem_ld16x256_x4(t_row + cD1 + j0, d1);
+            tmem_ld16x256_x4(t_row + cD2 + j0, d2);
             tmem_ld_wait();
-#pragma unroll
-            for (int mm = 0; mm < 32; ++mm) {
-                const int m = j0 + mm;
-                if (m < L) a.dkp2[base + (size_t)m * ts] = __float2bfloat16_rn(dk[mm] + sm.beta[m] * sm.eg[m] * wt[mm]);
+            float z[8], y[8];
+    #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+    #pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int j = j0 + 8 * k + cq + p;
+                    const float f1 = sm.eg[j] * sm.rki[j], bj = sm.beta[j];
+                    const float sa = f1 * d1[4 * k + p] + d2[4 * k + p];
+                    const float sb = f1 * d1[4 * k + 2 + p] + d2[4 * k + 2 + p];
+                    const float2 ta = get_pair(sm.op_t, ra, j0 + 8 * k + cq);   // T is zero above the diagonal
+                    const float2 tb2 = get_pair(sm.op_t, rb, j0 + 8 * k + cq);
+                    const float tva = la ? (p ? ta.y : ta.x) : 0.f, tvb = lb ? (p ? tb2.y : tb2.x) : 0.f;
+                    z[2 * k + p] = tva * d1[4 * k + p] + tvb * d1[4 * k + 2 + p];
+                    y[2 * k + p] = tva * sa + tvb * sb;
+                    d2[4 * k + p] = (la && j < ra) ? bj * sa : 0.f;        // dT, in place
+                    d2[4 * k + 2 + p] = (lb && j < rb) ? bj * sb : 0.f;
+                }
+                put_pair(sm.op_dx, ra, j0 + 8 * k + cq, d2[4 * k], d2[4 * k + 1]);
+                put_pair(sm.op_dx, rb, j0 + 8 * k + cq, d2[4 * k + 2], d2[4 * k + 3]);
+            }
+            sm.cz[sub][ccol] = colsum_frag(z, lane);
+            sm.cy[sub][ccol] = colsum_frag(y, lane);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- phase 1b: X = dT T^T  (A = dT rows, B = T rows as [N][K])
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(64, 64, 0, 0);
+    #pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tb + cX, sdesc(smem_u32(sm.op_dx) + s * 32, 16, 1024),
+                         sdesc(smem_u32(sm.op_t) + s * 32, 16, 1024), id, s > 0);
+            mma_commit(&sm.mma_bar);
+        }
+        commit_wait(ok);
+        if (ok) {  // X rows -> bf16 over the dT rows (the product that read them is done)
+            float x[16];
+            tmem_ld16x256_x4(t_row + cX + j0, x);
+            tmem_ld_wait();
+    #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                put_pair(sm.op_dx, ra, j0 + 8 * k + cq, x[4 * k], x[4 * k + 1]);
+                put_pair(sm.op_dx, rb, j0 + 8 * k + cq, x[4 * k + 2], x[4 * k + 3]);
             }
         }
-        float ut[32];
-        tmem_ld32(t_row + cUT + j0, ut);
-        tmem_ld_wait();
-#pragma unroll
-        for (int mm = 0; mm < 32; ++mm) {
-            const int m = j0 + mm;
-            if (m < L) a.dv[base + (size_t)m * ts] = __float2bfloat16_rn(sm.beta[m] * ut[mm]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- phase 1c: T^T X  (A = T rows read MN-major, B = X rows read MN-major)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(64, 64, 1, 1);
+    #pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tb + cA, sdesc(smem_u32(sm.op_t) + s * 2048, kHalf, 1024),
+                         sdesc(smem_u32(sm.op_dx) + s * 2048, kHalf, 1024), id, s > 0);
+            mma_commit(&sm.mma_bar);
         }
-    } else if (tid == 0 && a.status) {
-        atomicOr(a.status, 2);
-    }
-    __syncthreads();
-    if (ok && warp == 0) {  // dg = reverse cumulative sum of dG (warp scan), dbeta
-        float dgv[2];
-#pragma unroll
-        for (int z = 0; z < 2; ++z) {
-            const int m = 2 * lane + z;
-            dgv[z] = m < L ? sm.dG[m] : 0.f;
+        commit_wait(ok);
+        if (ok) {  // dA = -(T^T X): B and its operands, P2 row sums, column sums of beta_i P2
+            float ta[16], kk[16];
+            tmem_ld16x256_x4(t_row + cA + j0, ta);
+            tmem_ld16x256_x4(t_row + cKK + j0, kk);
+            tmem_ld_wait();
+            const float Ga = sm.G[ra], Gb = sm.G[rb];
+            const float ba = sm.beta[ra], bb = sm.beta[rb];
+            const float rka = sm.rki[ra], rkb = sm.rki[rb];
+            float rsa = 0.f, rsb = 0.f, pb[8];
+    #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float b1[4], b2[4];
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = j0 + 8 * k + cq + (e & 1);
+                    const bool up = e & 2;                       // row rb
+                    const int r = up ? rb : ra;
+                    const float msk = ((up ? lb : la) && j < r) ? 1.f : 0.f;
+                    const float dag = -ta[4 * k + e] * msk * __expf(fminf((up ? Gb : Ga) - sm.G[j], 0.f));
+                    const float rkj = sm.rki[j], br = up ? bb : ba, rkr = up ? rkb : rka;
+                    const float p2 = dag * kk[4 * k + e] * rkr * rkj;
+                    if (up) rsb += p2; else rsa += p2;
+                    b1[e] = dag * br * rkj;   // B_rj / r_k,j
+                    b2[e] = dag * br * rkr;   // B_rj / r_k,r
+                    kk[4 * k + e] = br * p2;  // beta_r P2_rj
+                }
+                pb[2 * k] = kk[4 * k] + kk[4 * k + 2];
+                pb[2 * k + 1] = kk[4 * k + 1] + kk[4 * k + 3];
+                put_pair(sm.op_b, ra, j0 + 8 * k + cq, b1[0], b1[1]);
+                put_pair(sm.op_b, rb, j0 + 8 * k + cq, b1[2], b1[3]);
+                put_pair(sm.op_bt, ra, j0 + 8 * k + cq, b2[0], b2[1]);
+                put_pair(sm.op_bt, rb, j0 + 8 * k + cq, b2[2], b2[3]);
+            }
+            sm.cp[sub][ccol] = colsum_frag(pb, lane);
+            rsa = quad_sum(rsa);
+            rsb = quad_sum(rsb);
+            if ((lane & 3) == 0) {
+                sm.rs[grp][ra] = rsa;
+                sm.rs[grp][rb] = rsb;
+            }
         }
-        const float pair = dgv[0] + dgv[1];
-        float suf = pair;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_down_sync(0xffffffffu, suf, off);
-            if (lane + off < 32) suf += y;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- phase 2 (M=128: row d of each product is TMEM lane d, column m is a token)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t kA = smem_u32(sm.k), wA = smem_u32(sm.dw), vA = smem_u32(sm.dvn);
+            const uint32_t tB = smem_u32(sm.op_t), bB = smem_u32(sm.op_b), btB = smem_u32(sm.op_bt);
+            const uint32_t id_mk = idesc_bf16(128, 64, 1, 0);  // A MN-major, B K-major
+            const uint32_t id_mm = idesc_bf16(128, 64, 1, 1);  // A MN-major, B MN-major
+    #pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t aK = sdesc(kA + s * 2048, kHalf, 1024);
+                mma_bf16(tb + cDK, aK, sdesc(bB + s * 32, 16, 1024), id_mk, s > 0);
+                mma_bf16(tb + cDK, aK, sdesc(btB + s * 2048, kHalf, 1024), id_mm, true);
+                mma_bf16(tb + cWT, sdesc(wA + s * 2048, kHalf, 1024), sdesc(tB + s * 2048, kHalf, 1024), id_mm,
+                         s > 0);
+                mma_bf16(tb + cUT, sdesc(vA + s * 2048, kHalf, 1024), sdesc(tB + s * 2048, kHalf, 1024), id_mm,
+                         s > 0);
+            }
+            mma_commit(&sm.mma_bar);
         }
-        const float after = suf - pair;  // sum over elements 2*lane+2 ...
-        float pa = 0.f, pd = 0.f;        // fused gating: sums of dg g and of da over the chunk
-#pragma unroll
-        for (int z = 0; z < 2; ++z) {
-            const int m = 2 * lane + z;
-            if (m < L) {
-                const size_t gi = (size_t)(t0 + m) * a.HV + hv;
-                const float dgm = (z == 0 ? dgv[0] + dgv[1] : dgv[1]) + after;
-                store_dbeta(a, gi, sm.db[m], sm.beta[m]);
-                if (a.beta_mode == 2) {  // da = dg (-e^{A_log}) softplus'(a + dt_bias)
-                    const float x = bf2f(a.ga[gi]) + a.dt_bias[hv], nea = -expf(a.A_log[hv]);
-                    const float da = dgm * nea * gate_softplus_slope(x);
-                    a.da[gi] = f2bf(da);
-                    pa += dgm * (nea * gate_softplus(x));
-                    pd += da;
-                } else {
-                    a.dg[gi] = dgm;
+        // meanwhile: dbeta and this kernel's dG terms per token m (fixed order)
+        if (ok && tid < 64) {
+            const int m = tid;
+            const float r2 = sm.rs[0][m] + sm.rs[1][m];
+            const float cy = ((sm.cy[0][m] + sm.cy[1][m]) + sm.cy[2][m]) + sm.cy[3][m];
+            const float cz = ((sm.cz[0][m] + sm.cz[1][m]) + sm.cz[2][m]) + sm.cz[3][m];
+            const float cp = ((sm.cp[0][m] + sm.cp[1][m]) + sm.cp[2][m]) + sm.cp[3][m];
+            const float bm = sm.beta[m];
+            sm.db[m] = r2 + cy;
+            sm.dG[m] += bm * r2 - cp + bm * sm.eg[m] * sm.rki[m] * cz;
+        }
+        commit_wait(ok);
+        if (tid == 0 && ok && has_next) issue_a(maps, sm, a, nx);  // K, dW, dv_new, T read by phase 2
+        if (ok && has_next) ++a_issued;
+        if (ok) {  // thread d: element d of the token rows m in [32 grp, 32 grp + 32)
+            const int d = sub * 32 + lane;
+            const size_t base = ((size_t)t0 * a.HV + hv) * kDim + d;
+            const size_t ts = (size_t)a.HV * kDim;
+    #pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {  // 16 token columns at a time
+                const int m0 = j0 + 16 * hh;
+                float dk[16], wt[16], ut[16];
+                tmem_ld16(t_row + cDK + m0, dk);
+                tmem_ld16(t_row + cWT + m0, wt);
+                tmem_ld16(t_row + cUT + m0, ut);
+                tmem_ld_wait();
+    #pragma unroll
+                for (int mm = 0; mm < 16; ++mm) {
+                    const int m = m0 + mm;
+                    if (m < L) {
+                        const float bm = sm.beta[m];
+                        a.dkp2[base + (size_t)m * ts] = __float2bfloat16_rn(dk[mm] + bm * sm.eg[m] * wt[mm]);
+                        a.dv[base + (size_t)m * ts] = __float2bfloat16_rn(bm * ut[mm]);
+                    }
                 }
             }
+        } else if (tid == 0 && a.status) {
+            atomicOr(a.status, 2);
         }
-        if (a.beta_mode == 2) {
-            pa = warp_sum(pa);
-            pd = warp_sum(pd);
-            if (lane == 0)
-                reinterpret_cast<float2 *>(a.gpart)[(size_t)c * a.HV + hv] = make_float2(pa, pd);
+        __syncthreads();
+        if (ok && warp == 0) {  // dg = reverse cumulative sum of dG (warp scan), dbeta
+            float dgv[2];
+    #pragma unroll
+            for (int z = 0; z < 2; ++z) {
+                const int m = 2 * lane + z;
+                dgv[z] = m < L ? sm.dG[m] : 0.f;
+            }
+            const float pair = dgv[0] + dgv[1];
+            float suf = pair;
+    #pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, suf, off);
+                if (lane + off < 32) suf += y;
+            }
+            const float after = suf - pair;  // sum over elements 2*lane+2 ...
+            float pa = 0.f, pd = 0.f;        // fused gating: sums of dg g and of da over the chunk
+    #pragma unroll
+            for (int z = 0; z < 2; ++z) {
+                const int m = 2 * lane + z;
+                if (m < L) {
+                    const size_t gi = (size_t)(t0 + m) * a.HV + hv;
+                    const float dgm = (z == 0 ? dgv[0] + dgv[1] : dgv[1]) + after;
+                    store_dbeta(a, gi, sm.db[m], sm.beta[m]);
+                    if (a.beta_mode == 2) {  // da = dg (-e^{A_log}) softplus'(a + dt_bias)
+                        const float x = bf2f(a.ga[gi]) + a.dt_bias[hv], nea = -expf(a.A_log[hv]);
+                        const float da = dgm * nea * gate_softplus_slope(x);
+                        a.da[gi] = f2bf(da);
+                        pa += dgm * (nea * gate_softplus(x));
+                        pd += da;
+                    } else {
+                        a.dg[gi] = dgm;
+                    }
+                }
+            }
+            if (a.beta_mode == 2) {
+                pa = warp_sum(pa);
+                pd = warp_sum(pd);
+                if (lane == 0)
+                    reinterpret_cast<float2 *>(a.gpart)[(size_t)c * a.HV + hv] = make_float2(pa, pd);
+            }
         }
+        tc_fence_before();
+        ok = __syncthreads_and(ok);  // the unit's scalars, operand tiles and TMEM are free
+        if (!ok) break;
+        x = nx;
+    }
+    if (!ok && tid == 0) {
+        if (a.status) atomicOr(a.status, 2);
+        // drain the loads still in flight (bounded) before leaving
+        if (a_issued > waited) mbar_wait(&sm.a_bar, (a_issued - 1) & 1, 1u << 20);
+        if (v_issued > waited) mbar_wait(&sm.v_bar, (v_issued - 1) & 1, 1u << 20);
     }
     tc_fence_before();
     __syncthreads();
@@ -378,8 +445,13 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_bintra_b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = sm_count(&sms)) != cudaSuccess) return e;
+    const int nunits = a.num_chunks * a.HV;
+    const int slots = 2 * sms;
+    const int per = (nunits + slots - 1) / slots;
     TimerScope ts(a.timer, GDN_KERNEL_BINTRA_B, s);
-    k_bintra_b_tc<<<dim3(a.num_chunks, a.HV), kThr, smem, s>>>(a, m);
+    k_bintra_b_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
     return cudaGetLastError();
 }
 

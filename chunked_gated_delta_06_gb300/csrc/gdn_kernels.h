@@ -105,6 +105,14 @@ struct TimerScope {
     }
 };
 
+// Number of SMs of the current device (grid sizing of the persistent kernels).
+inline cudaError_t sm_count(int *n) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+}
+
 cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s);
 cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s);

@@ -135,16 +135,17 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     }
     int a_issued = 1, v_issued = 1, waited = 0;  // same on every thread
     // per-token scalars of thread tid < 64, fetched one unit ahead
-    float pG = 0.f, pB = 0.f, pR = 1.f, pD = 0.f;
+    float pG = 0.f, pR = 1.f, pD = 0.f;
+    uint32_t pB = 0;   // raw beta bits, converted when published
+    bool pin = false;
     auto fetch = [&](const BwUnit &y) {
-        if (tid < 64 && tid < y.L) {
+        pin = tid < 64 && tid < y.L;
+        if (pin) {
             const size_t gi = (size_t)(y.t0 + tid) * a.HV + y.hv;
             pG = a.G[gi];
-            pB = load_beta(a, gi);
+            pB = load_beta_raw(a, gi);
             pR = a.rk[(size_t)(y.t0 + tid) * a.H + y.h];
             pD = a.dGp[gi];
-        } else {
-            pG = 0.f; pB = 0.f; pR = 1.f; pD = 0.f;
         }
     };
     fetch(x);
@@ -154,17 +155,14 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     bool ok = true;
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
-        const BwUnit nx = has_next ? bw_unit(a, u + 1) : x;
         const int c = x.c, hv = x.hv, t0 = x.t0, L = x.L;
-        if (tid < 64) {
-            const bool in = tid < L;
-            sm.G[tid] = pG;
-            sm.beta[tid] = pB;
-            sm.rki[tid] = in ? 1.f / pR : 1.f;
-            sm.eg[tid] = in ? __expf(pG) : 0.f;
-            sm.dG[tid] = pD;
+        if (tid < 64) {  // tokens past L get zeros and 1 / r_k = 1
+            sm.G[tid] = pin ? pG : 0.f;
+            sm.beta[tid] = pin ? beta_from_raw(a, pB) : 0.f;
+            sm.rki[tid] = pin ? 1.f / pR : 1.f;
+            sm.eg[tid] = pin ? __expf(pG) : 0.f;
+            sm.dG[tid] = pin ? pD : 0.f;
         }
-        if (has_next) fetch(nx);
         {
             const bool got = mbar_wait(&sm.a_bar, waited & 1) && mbar_wait(&sm.v_bar, waited & 1);
             ok = __syncthreads_and(ok && got);
@@ -192,6 +190,9 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                 }
             mma_commit(&sm.mma_bar);
         }
+        // the next unit (its table entries are a dependent load: after the MMA issue)
+        const BwUnit nx = has_next ? bw_unit(a, u + 1) : x;
+        if (has_next) fetch(nx);
         commit_wait(ok);
         if (tid == 0 && ok && has_next) issue_v(maps, sm, nx);  // V has been read by phase 1
         if (ok && has_next) ++v_issued;

@@ -167,7 +167,6 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     uint32_t phase = 0;
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
-        const Unit nx = has_next ? unit_of(a, u + 1) : x;
         const int L = x.L;
         if (tid < 64) {
             const bool in = tid < L;
@@ -175,7 +174,6 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             sm.qsc[tid] = in ? a.scale / pRq : 0.f;
             sm.rki[tid] = in ? 1.f / pRk : 0.f;
         }
-        if (has_next) fetch(nx);
         bool got = mbar_wait(&sm.a_bar, a_waited & 1);
         if (need_b) got = mbar_wait(&sm.b_bar, b_waited & 1) && got;
         got = __syncthreads_and(got);
@@ -206,6 +204,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             }
             mma_commit(&sm.mma_bar);
         }
+        // the next unit (its table entries are a dependent load: after the MMA issue)
+        const Unit nx = has_next ? unit_of(a, u + 1) : x;
+        if (has_next) fetch(nx);
         // <h, dh'> while the products run: thread tid takes half a row of h and dh'
         float hdh = 0.f;
         {

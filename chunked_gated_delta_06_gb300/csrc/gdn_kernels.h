@@ -77,6 +77,18 @@ __device__ __forceinline__ float load_beta(const ChunkArgs &a, size_t i) {
     if (a.beta_mode == 2) return gate_sigmoid(bf2f(a.gb[i]));
     return a.beta_mode ? static_cast<const float *>(a.beta)[i] : bf2f(static_cast<const bf16 *>(a.beta)[i]);
 }
+// The same in two steps, so that a prefetch does not wait for its load: the raw bits
+// (fp32, or bf16 in the low half) now, the value when it is used.
+__device__ __forceinline__ uint32_t load_beta_raw(const ChunkArgs &a, size_t i) {
+    if (a.beta_mode == 1) return __float_as_uint(static_cast<const float *>(a.beta)[i]);
+    const bf16 *p = a.beta_mode == 2 ? a.gb : static_cast<const bf16 *>(a.beta);
+    return (uint32_t)__bfloat16_as_ushort(p[i]);
+}
+__device__ __forceinline__ float beta_from_raw(const ChunkArgs &a, uint32_t bits) {
+    if (a.beta_mode == 1) return __uint_as_float(bits);
+    const float x = __uint_as_float(bits << 16);
+    return a.beta_mode == 2 ? gate_sigmoid(x) : x;
+}
 // dbeta_i = x in beta's dtype; with fused gating db_i = x beta_i (1 - beta_i) (bf16).
 __device__ __forceinline__ void store_dbeta(const ChunkArgs &a, size_t i, float x, float beta) {
     if (a.beta_mode == 1) static_cast<float *>(a.dbeta)[i] = x;

@@ -80,6 +80,17 @@ __device__ __forceinline__ BwUnit bw_unit(const ChunkArgs &a, int u) {
     x.L = a.chunk_len[x.c];
     return x;
 }
+// Unit u + 1 after unit x = u: the chunk table is read only when the chunk changes
+// (once every HV units), so the lookup rarely waits on a load.
+__device__ __forceinline__ BwUnit bw_next(const ChunkArgs &a, const BwUnit &x) {
+    if (x.hv + 1 < a.HV) {
+        BwUnit y = x;
+        y.hv = x.hv + 1;
+        y.h = y.hv / (a.HV / a.H);
+        return y;
+    }
+    return bw_unit(a, (x.c + 1) * a.HV);
+}
 
 // group A: K, dW, dv_new and T (free once phase 2 has run); group V: V (free after phase 1)
 __device__ __forceinline__ void issue_a(const BwMaps &m, BwSmem &sm, const ChunkArgs &a, const BwUnit &x) {
@@ -191,7 +202,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             mma_commit(&sm.mma_bar);
         }
         // the next unit (its table entries are a dependent load: after the MMA issue)
-        const BwUnit nx = has_next ? bw_unit(a, u + 1) : x;
+        const BwUnit nx = has_next ? bw_next(a, x) : x;
         if (has_next) fetch(nx);
         commit_wait(ok);
         if (tid == 0 && ok && has_next) issue_v(maps, sm, nx);  // V has been read by phase 1
@@ -345,10 +356,12 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         commit_wait(ok);
         if (tid == 0 && ok && has_next) issue_a(maps, sm, a, nx);  // K, dW, dv_new, T read by phase 2
         if (ok && has_next) ++a_issued;
-        if (ok) {  // thread d: element d of the token rows m in [32 grp, 32 grp + 32)
-            const int d = sub * 32 + lane;
-            const size_t base = ((size_t)t0 * a.HV + hv) * kDim + d;
+        if (ok) {  // thread d holds element d of the token rows m in [32 grp, 32 grp + 32);
+                   // lanes 2i and 2i + 1 swap halves so that each stores bf16 pairs (d even,
+                   // d + 1) of alternate tokens: even lanes tokens 2j, odd lanes 2j + 1
+            const int d = sub * 32 + lane, odd = lane & 1;
             const size_t ts = (size_t)a.HV * kDim;
+            const size_t base = ((size_t)t0 * a.HV + hv) * kDim + (d & ~1) + (size_t)odd * ts;
     #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {  // 16 token columns at a time
                 const int m0 = j0 + 16 * hh;
@@ -358,12 +371,18 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                 tmem_ld16(t_row + cUT + m0, ut);
                 tmem_ld_wait();
     #pragma unroll
-                for (int mm = 0; mm < 16; ++mm) {
-                    const int m = m0 + mm;
-                    if (m < L) {
-                        const float bm = sm.beta[m];
-                        a.dkp2[base + (size_t)m * ts] = __float2bfloat16_rn(dk[mm] + bm * sm.eg[m] * wt[mm]);
-                        a.dv[base + (size_t)m * ts] = __float2bfloat16_rn(bm * ut[mm]);
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int me = m0 + 2 * jj;  // the even token of the pair
+                    const float b0 = sm.beta[me], b1 = sm.beta[me + 1];
+                    const float k0 = dk[2 * jj] + b0 * sm.eg[me] * wt[2 * jj];
+                    const float k1 = dk[2 * jj + 1] + b1 * sm.eg[me + 1] * wt[2 * jj + 1];
+                    const float v0 = b0 * ut[2 * jj], v1 = b1 * ut[2 * jj + 1];
+                    const float rk = __shfl_xor_sync(0xffffffffu, odd ? k0 : k1, 1);
+                    const float rv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                    if (me + odd < L) {
+                        const size_t o = base + (size_t)me * ts;
+                        *reinterpret_cast<uint32_t *>(a.dkp2 + o) = odd ? pack_bf2(rk, k1) : pack_bf2(k0, rk);
+                        *reinterpret_cast<uint32_t *>(a.dv + o) = odd ? pack_bf2(rv, v1) : pack_bf2(v0, rv);
                     }
                 }
             }

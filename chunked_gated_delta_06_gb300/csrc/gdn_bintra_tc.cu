@@ -89,6 +89,17 @@ __device__ __forceinline__ Unit unit_of(const ChunkArgs &a, int u) {
     x.L = a.chunk_len[x.c];
     return x;
 }
+// Unit u + 1 after unit x = u: the chunk table is read only when the chunk changes
+// (once every HV units), so the lookup rarely waits on a load.
+__device__ __forceinline__ Unit next_unit(const ChunkArgs &a, const Unit &x) {
+    if (x.hv + 1 < a.HV) {
+        Unit y = x;
+        y.hv = x.hv + 1;
+        y.h = y.hv / (a.HV / a.H);
+        return y;
+    }
+    return unit_of(a, (x.c + 1) * a.HV);
+}
 
 __device__ __forceinline__ void issue_a(const BaMaps &m, BaSmem &sm, const ChunkArgs &a, const Unit &x) {
     const int row = (x.c * a.HV + x.hv) * 128;
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             mma_commit(&sm.mma_bar);
         }
         // the next unit (its table entries are a dependent load: after the MMA issue)
-        const Unit nx = has_next ? unit_of(a, u + 1) : x;
+        const Unit nx = has_next ? next_unit(a, x) : x;
         if (has_next) fetch(nx);
         // <h, dh'> while the products run: thread tid takes half a row of h and dh'
         float hdh = 0.f;

@@ -134,10 +134,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
     if (ub >= ue) return;
-    const bool active = lane < 16;
     const int grp = warp >> 2;
     const int sub = warp & 3;
-    const int t = sub * 16 + lane;  // the token row this lane owns (valid when active)
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -248,7 +246,6 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             if (tid == 0) issue_a(maps, sm, a, nx);
             ++a_issued;
         }
-        const bool live = active && t < L;
         const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);  // fragment rows / column
         const bool la = ra < L, lb = rb < L;
         {
@@ -289,21 +286,22 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 sm.rp[grp][ra] = rsa;
                 sm.rp[grp][rb] = rsb;
             }
-            // (b) dW = -Dw rows, this warpgroup's 64 columns
-            const size_t o = ((size_t)(x.t0 + (live ? t : 0)) * a.HV + x.hv) * kDim;
+            // (b) dW = -Dw rows on 16x256b fragments: rows ra, rb, this warpgroup's 64
+            // columns 64 grp + 32 cc + 8k + cq + {0, 1}
+            const size_t oa = ((size_t)(x.t0 + (la ? ra : 0)) * a.HV + x.hv) * kDim;
+            const size_t ob = ((size_t)(x.t0 + (lb ? rb : 0)) * a.HV + x.hv) * kDim;
+            float dw[2][16];
+            tmem_ld16x256_x4(t_row + cDW + 64 * grp, dw[0]);
+            tmem_ld16x256_x4(t_row + cDW + 64 * grp + 32, dw[1]);
+            tmem_ld_wait();
 #pragma unroll
-            for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
-                float dw[32];
-                tmem_ld32(t_row + cDW + cc * 32, dw);
-                tmem_ld_wait();
-                if (live) {
-                    uint4 *wp = reinterpret_cast<uint4 *>(a.dW + o + cc * 32);
+            for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        wp[q8] = make_uint4(pack_bf2(-dw[q8 * 8], -dw[q8 * 8 + 1]), pack_bf2(-dw[q8 * 8 + 2], -dw[q8 * 8 + 3]),
-                                            pack_bf2(-dw[q8 * 8 + 4], -dw[q8 * 8 + 5]), pack_bf2(-dw[q8 * 8 + 6], -dw[q8 * 8 + 7]));
+                for (int k = 0; k < 4; ++k) {
+                    const int col = 64 * grp + 32 * cc + 8 * k + cq;
+                    if (la) *reinterpret_cast<uint32_t *>(a.dW + oa + col) = pack_bf2(-dw[cc][4 * k], -dw[cc][4 * k + 1]);
+                    if (lb) *reinterpret_cast<uint32_t *>(a.dW + ob + col) = pack_bf2(-dw[cc][4 * k + 2], -dw[cc][4 * k + 3]);
                 }
-            }
         }
         fence_proxy_async_smem();
         tc_fence_before();

@@ -50,17 +50,62 @@ struct OutMaps {
 template <bool kForward>
 constexpr uint32_t kTmemCols = kForward ? 256 : 128;
 
+struct OutUnit {
+    int c, hv, h, t0, L;
+};
+
+__device__ __forceinline__ OutUnit out_unit(const ChunkArgs &a, int u) {
+    OutUnit x;
+    x.c = u / a.HV;
+    x.hv = u - x.c * a.HV;
+    x.h = x.hv / (a.HV / a.H);
+    x.t0 = a.chunk_start[x.c];
+    x.L = a.chunk_len[x.c];
+    return x;
+}
+// Unit u + 1 after unit x = u; the chunk table is read only when the chunk changes.
+__device__ __forceinline__ OutUnit out_next(const ChunkArgs &a, const OutUnit &x) {
+    if (x.hv + 1 < a.HV) {
+        OutUnit y = x;
+        y.hv = x.hv + 1;
+        y.h = y.hv / (a.HV / a.H);
+        return y;
+    }
+    return out_unit(a, (x.c + 1) * a.HV);
+}
+
+template <bool kForward>
+__device__ __forceinline__ void out_issue(const OutMaps &m, OutSmem<kForward> &sm, const ChunkArgs &a,
+                                          const OutUnit &x) {
+    const uint32_t bytes = 2 * kBig + 2 * kBox + (kForward ? 2 * kBig : 0);
+    mbar_arrive_expect_tx(&sm.tma_bar, bytes);
+    tma_load_3d(sm.kq, &m.k, 0, x.h, x.t0, &sm.tma_bar);
+    tma_load_3d(sm.kq + kBox, &m.q, 0, x.h, x.t0, &sm.tma_bar);
+    tma_load_3d(sm.kq + kBig, &m.k, 64, x.h, x.t0, &sm.tma_bar);
+    tma_load_3d(sm.kq + kBig + kBox, &m.q, 64, x.h, x.t0, &sm.tma_bar);
+    tma_load_3d(sm.tv, &m.tv, 0, x.hv, x.t0, &sm.tma_bar);
+    tma_load_3d(sm.tv + kBox, &m.tv, 64, x.hv, x.t0, &sm.tma_bar);
+    if constexpr (kForward) {
+        const int row = (x.c * a.HV + x.hv) * 128;
+        tma_load_3d(sm.hc, &m.h, 0, 0, row, &sm.tma_bar);
+        tma_load_3d(sm.hc + kBig, &m.h, 64, 0, row, &sm.tma_bar);
+    }
+}
+
+// Persistent: CTA b walks the units [b per, (b + 1) per) (unit u = chunk u / HV, value
+// head u % HV); the next unit's tiles load as soon as the second product has read
+// this unit's, and its per-token scalars a unit ahead.
 template <bool kForward>
 __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkArgs a,
-                                                                   const __grid_constant__ OutMaps maps) {
+                                                                   const __grid_constant__ OutMaps maps,
+                                                                   int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     OutSmem<kForward> &sm = *reinterpret_cast<OutSmem<kForward> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int c = blockIdx.x, hv = blockIdx.y;
-    const int h = hv / (a.HV / a.H);
-    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-    if (L <= 0) return;
+    const int nunits = a.num_chunks * a.HV;
+    const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
+    if (ub >= ue) return;
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, kTmemCols<kForward>);
@@ -74,138 +119,156 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {
-        const uint32_t bytes = 2 * kBig + 2 * kBox + (kForward ? 2 * kBig : 0);
-        mbar_arrive_expect_tx(&sm.tma_bar, bytes);
-        tma_load_3d(sm.kq, &maps.k, 0, h, t0, &sm.tma_bar);
-        tma_load_3d(sm.kq + kBox, &maps.q, 0, h, t0, &sm.tma_bar);
-        tma_load_3d(sm.kq + kBig, &maps.k, 64, h, t0, &sm.tma_bar);
-        tma_load_3d(sm.kq + kBig + kBox, &maps.q, 64, h, t0, &sm.tma_bar);
-        tma_load_3d(sm.tv, &maps.tv, 0, hv, t0, &sm.tma_bar);
-        tma_load_3d(sm.tv + kBox, &maps.tv, 64, hv, t0, &sm.tma_bar);
-        if constexpr (kForward) {
-            const int row = (c * a.HV + hv) * 128;
-            tma_load_3d(sm.hc, &maps.h, 0, 0, row, &sm.tma_bar);
-            tma_load_3d(sm.hc + kBig, &maps.h, 64, 0, row, &sm.tma_bar);
+    OutUnit x = out_unit(a, ub);
+    if (tid == 0) out_issue<kForward>(maps, sm, a, x);
+    // per-token scalars of thread tid < 64 (raw), fetched one unit ahead
+    float pG = 0.f, pRq = 1.f, pRk = 1.f;
+    bool pin = false;
+    auto fetch = [&](const OutUnit &y) {
+        pin = tid < 64 && tid < y.L;
+        if (pin) {
+            const size_t r = (size_t)(y.t0 + tid) * a.H + y.h;
+            pG = a.G[(size_t)(y.t0 + tid) * a.HV + y.hv];
+            pRq = a.rq[r];
+            pRk = a.rk[r];
         }
-    }
-    if (tid < 64) {
-        const bool in = tid < L;
-        const size_t r = (size_t)(t0 + tid) * a.H + h;
-        sm.G[tid] = in ? a.G[(size_t)(t0 + tid) * a.HV + hv] : 0.f;
-        sm.rq[tid] = in ? a.rq[r] : 1.f;
-        sm.rk[tid] = in ? a.rk[r] : 1.f;
-        sm.qsc[tid] = a.scale / sm.rq[tid];
-        sm.rki[tid] = 1.f / sm.rk[tid];
-        sm.ct[tid] = in ? __expf(sm.G[tid]) * sm.qsc[tid] : 0.f;
-    }
-    bool ok = __syncthreads_and(mbar_wait(&sm.tma_bar, 0));
+    };
+    fetch(x);
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
     uint32_t phase = 0;
-    // QK = Q K^T (M=64; Q rows sit at kBox inside each k-half of the [K; Q] tile)
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 64, 0, 0);
-        const uint32_t as = smem_u32(sm.kq);
-        for (int s = 0; s < 8; ++s) {
-            const uint32_t off = (s >> 2) * kBig + (s & 3) * 32;
-            mma_bf16(tb, sdesc(as + kBox + off, 16, 1024), sdesc(as + off, 16, 1024), id, s > 0);
+    int issued = 1, waited = 0;
+    bool ok = true;
+    for (int u = ub; u < ue; ++u) {
+        const bool has_next = u + 1 < ue;
+        const int hv = x.hv, t0 = x.t0, L = x.L;
+        if (tid < 64) {  // tokens past L: G = 0, r = 1, e^G term 0
+            const float rq = pin ? pRq : 1.f, rk = pin ? pRk : 1.f, gg = pin ? pG : 0.f;
+            sm.G[tid] = gg;
+            sm.rq[tid] = rq;
+            sm.rk[tid] = rk;
+            sm.qsc[tid] = a.scale / rq;
+            sm.rki[tid] = 1.f / rk;
+            sm.ct[tid] = pin ? __expf(gg) * (a.scale / rq) : 0.f;
         }
-        mma_commit(&sm.mma_bar);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
-    phase ^= 1;
-    tc_fence_after();
-    if (ok) {  // M from 16x256b fragments of QK: rows ra, rb = ra + 8 of warp w's block,
-               // columns 32 c + 8k + cq + {0, 1}
-        const int lane = tid & 31;
-        const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
-        const float qa = sm.qsc[ra], qb = sm.qsc[rb], Ga = sm.G[ra], Gb = sm.G[rb];
-        const bool la = ra < L, lb = rb < L;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            float r[16];
-            epi::tmem_ld16x256_x4(t_row + 32 * c, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int j = 32 * c + 8 * k + cq;
-                float m[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int jj = j + (e & 1);
-                    const bool up = e & 2;
-                    const int row = up ? rb : ra;
-                    const float msk = (jj <= row && (up ? lb : la)) ? 1.f : 0.f;
-                    m[e] = msk * r[4 * k + e] * (up ? qb : qa) * sm.rki[jj] *
-                           __expf(fminf((up ? Gb : Ga) - sm.G[jj], 0.f));
+        ok = __syncthreads_and(ok && mbar_wait(&sm.tma_bar, waited & 1));
+        ++waited;
+        if (!ok) break;
+        // QK = Q K^T (M=64; Q rows sit at kBox inside each k-half of the [K; Q] tile)
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(64, 64, 0, 0);
+            const uint32_t as = smem_u32(sm.kq);
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = (s >> 2) * kBig + (s & 3) * 32;
+                mma_bf16(tb, sdesc(as + kBox + off, 16, 1024), sdesc(as + off, 16, 1024), id, s > 0);
+            }
+            mma_commit(&sm.mma_bar);
+        }
+        const OutUnit nx = has_next ? out_next(a, x) : x;
+        if (has_next) fetch(nx);
+        ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
+        phase ^= 1;
+        tc_fence_after();
+        if (ok) {  // M from 16x256b fragments of QK: rows ra, rb = ra + 8 of warp w's block,
+                   // columns 32 c + 8k + cq + {0, 1}
+            const int lane = tid & 31;
+            const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+            const float qa = sm.qsc[ra], qb = sm.qsc[rb], Ga = sm.G[ra], Gb = sm.G[rb];
+            const bool la = ra < L, lb = rb < L;
+    #pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float r[16];
+                epi::tmem_ld16x256_x4(t_row + 32 * c, r);
+                tmem_ld_wait();
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = 32 * c + 8 * k + cq;
+                    float m[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int jj = j + (e & 1);
+                        const bool up = e & 2;
+                        const int row = up ? rb : ra;
+                        const float msk = (jj <= row && (up ? lb : la)) ? 1.f : 0.f;
+                        m[e] = msk * r[4 * k + e] * (up ? qb : qa) * sm.rki[jj] *
+                               __expf(fminf((up ? Gb : Ga) - sm.G[jj], 0.f));
+                    }
+                    // row t of M at row t: the forward reads it as K-major [t][j] (B = M^T
+                    // operand of v_new^T M^T), the backward as MN-major [j][t] (B = M of dO^T M)
+                    epi::put_pair(sm.mm, ra, j, m[0], m[1]);
+                    epi::put_pair(sm.mm, rb, j, m[2], m[3]);
                 }
-                // row t of M at row t: the forward reads it as K-major [t][j] (B = M^T
-                // operand of v_new^T M^T), the backward as MN-major [j][t] (B = M of dO^T M)
-                epi::put_pair(sm.mm, ra, j, m[0], m[1]);
-                epi::put_pair(sm.mm, rb, j, m[2], m[3]);
             }
         }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok) {  // token-row products (M=64, N=128), rows t of the results
-        tc_fence_after();
-        const uint32_t tvs = smem_u32(sm.tv), mms = smem_u32(sm.mm);
-        if constexpr (kForward) {
-            // O1 = Q h : A = Q [t][k] (K-major), B = h_c [k][v] (MN-major, v halves 16 KB apart)
-            const uint32_t id1 = idesc_bf16(64, 128, 0, 1);
-            const uint32_t hs = smem_u32(sm.hc), qs = smem_u32(sm.kq + kBox);
-            for (int s = 0; s < 8; ++s)
-                mma_bf16(tb, sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), sdesc(hs + s * 2048, kBig, 1024),
-                         id1, s > 0);
-            // O2 = M v_new : A = M [t][j] (K-major), B = v_new [j][v] (MN-major, v halves 8 KB apart)
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tb + 128, sdesc(mms + s * 32, 16, 1024), sdesc(tvs + s * 2048, kBox, 1024), id1, s > 0);
-        } else {
-            // DL = M^T dO : A = M [j][t] (MN-major), B = dO [j][v] (MN-major)
-            const uint32_t id2 = idesc_bf16(64, 128, 1, 1);
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tb, sdesc(mms + s * 2048, kBox, 1024), sdesc(tvs + s * 2048, kBox, 1024), id2, s > 0);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && ok) {  // token-row products (M=64, N=128), rows t of the results
+            tc_fence_after();
+            const uint32_t tvs = smem_u32(sm.tv), mms = smem_u32(sm.mm);
+            if constexpr (kForward) {
+                // O1 = Q h : A = Q [t][k] (K-major), B = h_c [k][v] (MN-major, v halves 16 KB apart)
+                const uint32_t id1 = idesc_bf16(64, 128, 0, 1);
+                const uint32_t hs = smem_u32(sm.hc), qs = smem_u32(sm.kq + kBox);
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16(tb, sdesc(qs + (s >> 2) * kBig + (s & 3) * 32, 16, 1024), sdesc(hs + s * 2048, kBig, 1024),
+                             id1, s > 0);
+                // O2 = M v_new : A = M [t][j] (K-major), B = v_new [j][v] (MN-major, v halves 8 KB apart)
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tb + 128, sdesc(mms + s * 32, 16, 1024), sdesc(tvs + s * 2048, kBox, 1024), id1, s > 0);
+            } else {
+                // DL = M^T dO : A = M [j][t] (MN-major), B = dO [j][v] (MN-major)
+                const uint32_t id2 = idesc_bf16(64, 128, 1, 1);
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tb, sdesc(mms + s * 2048, kBox, 1024), sdesc(tvs + s * 2048, kBox, 1024), id2, s > 0);
+            }
+            mma_commit(&sm.mma_bar);
         }
-        mma_commit(&sm.mma_bar);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
-    tc_fence_after();
-    if (ok) {  // 16x256b fragments: rows ra, ra + 8, columns v = 32 c + 8k + cq + {0, 1}
-        const int lane = tid & 31;
-        const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
-        const bool la = ra < L, lb = rb < L;
-        const float ca = sm.ct[ra], cb = sm.ct[rb];
-        bf16 *dst = kForward ? a.o : a.dvloc;
-        bf16 *da = dst + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim;
-        bf16 *db = dst + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float r1[16], r2[16];
-            epi::tmem_ld16x256_x4(t_row + 32 * c, r1);
-            if constexpr (kForward) epi::tmem_ld16x256_x4(t_row + 128 + 32 * c, r2);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int v = 32 * c + 8 * k + cq;
-                float x0, x1, y0, y1;
-                if constexpr (kForward) {
-                    x0 = ca * r1[4 * k] + r2[4 * k];
-                    x1 = ca * r1[4 * k + 1] + r2[4 * k + 1];
-                    y0 = cb * r1[4 * k + 2] + r2[4 * k + 2];
-                    y1 = cb * r1[4 * k + 3] + r2[4 * k + 3];
-                } else {
-                    x0 = r1[4 * k]; x1 = r1[4 * k + 1]; y0 = r1[4 * k + 2]; y1 = r1[4 * k + 3];
+        ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
+        phase ^= 1;
+        tc_fence_after();
+        if (tid == 0 && ok && has_next) out_issue<kForward>(maps, sm, a, nx);  // the tiles have been read
+        if (ok && has_next) ++issued;
+        if (ok) {  // 16x256b fragments: rows ra, ra + 8, columns v = 32 c + 8k + cq + {0, 1}
+            const int lane = tid & 31;
+            const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+            const bool la = ra < L, lb = rb < L;
+            const float ca = sm.ct[ra], cb = sm.ct[rb];
+            bf16 *dst = kForward ? a.o : a.dvloc;
+            bf16 *da = dst + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim;
+            bf16 *db = dst + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim;
+    #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float r1[16], r2[16];
+                epi::tmem_ld16x256_x4(t_row + 32 * c, r1);
+                if constexpr (kForward) epi::tmem_ld16x256_x4(t_row + 128 + 32 * c, r2);
+                tmem_ld_wait();
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int v = 32 * c + 8 * k + cq;
+                    float x0, x1, y0, y1;
+                    if constexpr (kForward) {
+                        x0 = ca * r1[4 * k] + r2[4 * k];
+                        x1 = ca * r1[4 * k + 1] + r2[4 * k + 1];
+                        y0 = cb * r1[4 * k + 2] + r2[4 * k + 2];
+                        y1 = cb * r1[4 * k + 3] + r2[4 * k + 3];
+                    } else {
+                        x0 = r1[4 * k]; x1 = r1[4 * k + 1]; y0 = r1[4 * k + 2]; y1 = r1[4 * k + 3];
+                    }
+                    if (la) *reinterpret_cast<uint32_t *>(da + v) = epi::pack_bf2(x0, x1);
+                    if (lb) *reinterpret_cast<uint32_t *>(db + v) = epi::pack_bf2(y0, y1);
                 }
-                if (la) *reinterpret_cast<uint32_t *>(da + v) = epi::pack_bf2(x0, x1);
-                if (lb) *reinterpret_cast<uint32_t *>(db + v) = epi::pack_bf2(y0, y1);
             }
         }
-    } else if (tid == 0 && a.status) {
-        atomicOr(a.status, 2);
+        tc_fence_before();
+        ok = __syncthreads_and(ok);  // the unit's scalars, M operand and TMEM are free
+        if (!ok) break;
+        x = nx;
+    }
+    if (!ok && tid == 0) {
+        if (a.status) atomicOr(a.status, 2);
+        if (issued > waited) mbar_wait(&sm.tma_bar, (issued - 1) & 1, 1u << 20);  // drain (bounded)
     }
     tc_fence_before();
     __syncthreads();
@@ -231,8 +294,13 @@ cudaError_t launch_out_mode(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_out_tc<kForward>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = sm_count(&sms)) != cudaSuccess) return e;
+    const int nunits = a.num_chunks * a.HV;
+    const int slots = (kForward ? 2 : 3) * sms;
+    const int per = (nunits + slots - 1) / slots;
     TimerScope ts(a.timer, kForward ? GDN_KERNEL_OUT : GDN_KERNEL_DVLOC, s);
-    k_out_tc<kForward><<<dim3(a.num_chunks, a.HV), kThr, smem, s>>>(a, m);
+    k_out_tc<kForward><<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
     return cudaGetLastError();
 }
 

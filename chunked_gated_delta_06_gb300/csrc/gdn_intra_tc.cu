@@ -3,10 +3,10 @@
 // chunk form of the GDN context-parallel scans in "Qwen3.5-397B RL trainer on
 // 128 v7x", maxtext #5799).
 //
-// One CTA of 128 threads per (chunk, value head), sized so that three CTAs share
-// an SM (about 72 KB of shared memory and 128 TMEM columns each): the pass is a
-// chain of short dependent steps, and co-resident CTAs hide one another's
-// latencies.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
+// Persistent CTAs of 128 threads walking runs of (chunk, value head) units, sized
+// so that three share an SM (about 72 KB of shared memory and 128 TMEM columns
+// each): the pass is a chain of short dependent steps, and co-resident CTAs hide
+// one another's latencies, while each CTA loads its next unit under its epilogue.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
 //   KK = K K^T                                   (tcgen05, M=64 N=64 K=128)
 // The M=64 KK result is read as 16x256b fragments (two rows, eight columns per lane).
 //   A  = strict_tril(diag(beta) KKhat (.) Gamma) (CUDA cores, fp32)
@@ -146,141 +146,207 @@ __device__ __forceinline__ void tri_inverse(float *M, float *X, int tid) {
     }
 }
 
+struct IntraUnit {
+    int c, hv, h, t0, L;
+};
+
+__device__ __forceinline__ IntraUnit intra_unit(const ChunkArgs &a, int u) {
+    IntraUnit x;
+    x.c = u / a.HV;
+    x.hv = u - x.c * a.HV;
+    x.h = x.hv / (a.HV / a.H);
+    x.t0 = a.chunk_start[x.c];
+    x.L = a.chunk_len[x.c];
+    return x;
+}
+
+// Unit u + 1 after unit x = u; the chunk table is read only when the chunk changes.
+__device__ __forceinline__ IntraUnit intra_next(const ChunkArgs &a, const IntraUnit &x) {
+    if (x.hv + 1 < a.HV) {
+        IntraUnit y = x;
+        y.hv = x.hv + 1;
+        y.h = y.hv / (a.HV / a.H);
+        return y;
+    }
+    return intra_unit(a, (x.c + 1) * a.HV);
+}
+
+__device__ __forceinline__ void issue_kv(const IntraMaps &m, IntraSmem &sm, const IntraUnit &x) {
+    mbar_arrive_expect_tx(&sm.ld_bar, 2 * kTile);
+    tma_load_3d(sm.k, &m.k, 0, x.h, x.t0, &sm.ld_bar);
+    tma_load_3d(sm.k + kHalf, &m.k, 64, x.h, x.t0, &sm.ld_bar);
+    tma_load_3d(sm.v, &m.v, 0, x.hv, x.t0, &sm.ld_bar);
+    tma_load_3d(sm.v + kHalf, &m.v, 64, x.hv, x.t0, &sm.ld_bar);
+}
+
+// Persistent: CTA b walks the units [b per, (b + 1) per) (unit u = chunk u / HV, value
+// head u % HV), three CTAs per SM; the next unit's K and V tiles load as soon as the
+// w / u products have read this unit's, and its per-token scalars a unit ahead.
 __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
-                                                      const __grid_constant__ IntraMaps maps) {
+                                                      const __grid_constant__ IntraMaps maps, int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     IntraSmem &sm = *reinterpret_cast<IntraSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                    ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hv = blockIdx.y;
-    const int h = hv / (a.HV / a.H);
-    const int t0 = a.chunk_start[c], L = a.chunk_len[c];
-    if (L <= 0) return;
+    const int nunits = a.num_chunks * a.HV;
+    const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
+    if (ub >= ue) return;
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
+    IntraUnit x = intra_unit(a, ub);
     if (tid == 0) {
         mbar_init(&sm.ld_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&sm.ld_bar, 2 * kTile);
-        tma_load_3d(sm.k, &maps.k, 0, h, t0, &sm.ld_bar);
-        tma_load_3d(sm.k + kHalf, &maps.k, 64, h, t0, &sm.ld_bar);
-        tma_load_3d(sm.v, &maps.v, 0, hv, t0, &sm.ld_bar);
-        tma_load_3d(sm.v + kHalf, &maps.v, 64, hv, t0, &sm.ld_bar);
+        issue_kv(maps, sm, x);
     }
-    if (tid < 64) {  // per-token scalars; tokens past L get beta = 0 and 1 / r_k = 1
-        const bool in = tid < L;
-        const size_t gi = (size_t)(t0 + tid) * a.HV + hv;
-        const float gg = in ? a.G[gi] : 0.f, bb = in ? load_beta(a, gi) : 0.f;
-        const float ri = in ? 1.f / a.rk[(size_t)(t0 + tid) * a.H + h] : 1.f;
-        sm.G[tid] = gg;
-        sm.beta[tid] = bb;
-        sm.rki[tid] = ri;
-        sm.wc[tid] = bb * __expf(gg) * ri;
-    }
+    // per-token scalars of thread tid < 64, fetched one unit ahead
+    float pG = 0.f, pR = 1.f;
+    uint32_t pB = 0;   // raw beta bits, converted when published
+    bool pin = false;
+    auto fetch = [&](const IntraUnit &y) {
+        pin = tid < 64 && tid < y.L;
+        if (pin) {
+            const size_t gi = (size_t)(y.t0 + tid) * a.HV + y.hv;
+            pG = a.G[gi];
+            pB = load_beta_raw(a, gi);
+            pR = a.rk[(size_t)(y.t0 + tid) * a.H + y.h];
+        }
+    };
+    fetch(x);
     tc_fence_before();
     __syncthreads();  // the barriers are initialised before anyone waits on them
-    bool ok = __syncthreads_and(mbar_wait(&sm.ld_bar, 0));
-    tc_fence_after();
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
-    if (tid == 0 && ok) {  // KK = K K^T into columns 0..63 (M=64: row m at lane 32 (m / 16) + m % 16)
-        const uint32_t ks = smem_u32(sm.k);
-        const uint32_t id = idesc_bf16(64, 64, 0, 0);
-        for (int s = 0; s < 8; ++s) {
-            const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
-            mma_bf16(tb, sdesc(ks + off, 16, 1024), sdesc(ks + off, 16, 1024), id, s > 0);
+    int issued = 1, waited = 0;
+    uint32_t mphase = 0;
+    bool ok = true;
+    for (int u = ub; u < ue; ++u) {
+        const bool has_next = u + 1 < ue;
+        const int c = x.c, hv = x.hv, t0 = x.t0, L = x.L;
+        if (tid < 64) {  // tokens past L get G = 0, beta = 0 and 1 / r_k = 1
+            const float ri = pin ? 1.f / pR : 1.f, bb = pin ? beta_from_raw(a, pB) : 0.f;
+            const float gg = pin ? pG : 0.f;
+            sm.G[tid] = gg;
+            sm.beta[tid] = bb;
+            sm.rki[tid] = ri;
+            sm.wc[tid] = bb * __expf(gg) * ri;
         }
-        mma_commit(&sm.mma_bar);
-    }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, 0));
-    tc_fence_after();
-    if (ok) {  // A from 16x256b fragments of KK: rows ra, ra + 8 of the warp's block, columns
-               // 32 c + 8k + cq + {0, 1}; zeros on and above the diagonal
-        const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
-        const float Ga = sm.G[ra], Gb = sm.G[rb];
-        const float aa = sm.beta[ra] * sm.rki[ra], ab = sm.beta[rb] * sm.rki[rb];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            float kk[16];
-            epi::tmem_ld16x256_x4(t_row + 32 * c, kk);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int j = 32 * c + 8 * k + cq;
-                const float r0 = sm.rki[j], r1 = sm.rki[j + 1];
-                const float g0 = sm.G[j], g1 = sm.G[j + 1];
-                const float e0 = (j < ra ? aa : 0.f) * kk[4 * k] * r0 * __expf(fminf(Ga - g0, 0.f));
-                const float e1 = (j + 1 < ra ? aa : 0.f) * kk[4 * k + 1] * r1 * __expf(fminf(Ga - g1, 0.f));
-                const float f0 = (j < rb ? ab : 0.f) * kk[4 * k + 2] * r0 * __expf(fminf(Gb - g0, 0.f));
-                const float f1 = (j + 1 < rb ? ab : 0.f) * kk[4 * k + 3] * r1 * __expf(fminf(Gb - g1, 0.f));
-                *reinterpret_cast<float2 *>(sm.M + ra * kS + j) = make_float2(e0, e1);
-                *reinterpret_cast<float2 *>(sm.M + rb * kS + j) = make_float2(f0, f1);
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();  // KK has been read: its TMEM columns are free
-    tri_inverse(sm.M, sm.X, tid);
-    {  // operands T diag(c) as bf16 rows, and T to HBM: thread -> row tid / 2, 32 columns
-        const int i = tid >> 1, j0 = 32 * (tid & 1);
-        const float *Mi = sm.M + i * kS + j0;
-        uint4 *Tdst = reinterpret_cast<uint4 *>(a.Tm + (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 t0v = *reinterpret_cast<const float4 *>(Mi + 8 * q);
-            const float4 t1v = *reinterpret_cast<const float4 *>(Mi + 8 * q + 4);
-            Tdst[q] = make_uint4(pack_bf2(t0v.x, t0v.y), pack_bf2(t0v.z, t0v.w), pack_bf2(t1v.x, t1v.y),
-                                 pack_bf2(t1v.z, t1v.w));
-            const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
-            const int jb = j0 + 8 * q;
-            uint32_t pw[4], pu[4];
-#pragma unroll
-            for (int z = 0; z < 4; ++z) {
-                pw[z] = pack_bf2(tv[2 * z] * sm.wc[jb + 2 * z], tv[2 * z + 1] * sm.wc[jb + 2 * z + 1]);
-                pu[z] = pack_bf2(tv[2 * z] * sm.beta[jb + 2 * z], tv[2 * z + 1] * sm.beta[jb + 2 * z + 1]);
-            }
-            *reinterpret_cast<uint4 *>(sm.op_w + sw128_off(i, jb)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-            *reinterpret_cast<uint4 *>(sm.op_u + sw128_off(i, jb)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok) {  // w^T -> columns 0..63, u^T -> 64..127 (lane d, column i)
+        ok = __syncthreads_and(ok && mbar_wait(&sm.ld_bar, waited & 1));
+        ++waited;
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 1, 0);
-        const uint32_t ks = smem_u32(sm.k), vs = smem_u32(sm.v);
-        const uint32_t ws = smem_u32(sm.op_w), us = smem_u32(sm.op_u);
-        for (int s = 0; s < 4; ++s) {
-            mma_bf16(tb, sdesc(ks + s * 2048, kHalf, 1024), sdesc(ws + s * 32, 16, 1024), id, s > 0);
-            mma_bf16(tb + 64, sdesc(vs + s * 2048, kHalf, 1024), sdesc(us + s * 32, 16, 1024), id, s > 0);
+        if (tid == 0 && ok) {  // KK = K K^T into columns 0..63 (M=64: row m at lane 32 (m / 16) + m % 16)
+            const uint32_t ks = smem_u32(sm.k);
+            const uint32_t id = idesc_bf16(64, 64, 0, 0);
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t off = (s >> 2) * kHalf + (s & 3) * 32;
+                mma_bf16(tb, sdesc(ks + off, 16, 1024), sdesc(ks + off, 16, 1024), id, s > 0);
+            }
+            mma_commit(&sm.mma_bar);
         }
-        mma_commit(&sm.mma_bar);
+        // the next unit (its table entries are a dependent load: after the MMA issue)
+        const IntraUnit nx = has_next ? intra_next(a, x) : x;
+        if (has_next) fetch(nx);
+        ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
+        mphase ^= 1;
+        tc_fence_after();
+        if (ok) {  // A from 16x256b fragments of KK: rows ra, ra + 8 of the warp's block, columns
+                   // 32 c + 8k + cq + {0, 1}; zeros on and above the diagonal
+            const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+            const float Ga = sm.G[ra], Gb = sm.G[rb];
+            const float aa = sm.beta[ra] * sm.rki[ra], ab = sm.beta[rb] * sm.rki[rb];
+    #pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float kk[16];
+                epi::tmem_ld16x256_x4(t_row + 32 * c, kk);
+                tmem_ld_wait();
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = 32 * c + 8 * k + cq;
+                    const float r0 = sm.rki[j], r1 = sm.rki[j + 1];
+                    const float g0 = sm.G[j], g1 = sm.G[j + 1];
+                    const float e0 = (j < ra ? aa : 0.f) * kk[4 * k] * r0 * __expf(fminf(Ga - g0, 0.f));
+                    const float e1 = (j + 1 < ra ? aa : 0.f) * kk[4 * k + 1] * r1 * __expf(fminf(Ga - g1, 0.f));
+                    const float f0 = (j < rb ? ab : 0.f) * kk[4 * k + 2] * r0 * __expf(fminf(Gb - g0, 0.f));
+                    const float f1 = (j + 1 < rb ? ab : 0.f) * kk[4 * k + 3] * r1 * __expf(fminf(Gb - g1, 0.f));
+                    *reinterpret_cast<float2 *>(sm.M + ra * kS + j) = make_float2(e0, e1);
+                    *reinterpret_cast<float2 *>(sm.M + rb * kS + j) = make_float2(f0, f1);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // KK has been read: its TMEM columns are free
+        tri_inverse(sm.M, sm.X, tid);
+        {  // operands T diag(c) as bf16 rows, and T to HBM: thread -> row tid / 2, 32 columns
+            const int i = tid >> 1, j0 = 32 * (tid & 1);
+            const float *Mi = sm.M + i * kS + j0;
+            uint4 *Tdst = reinterpret_cast<uint4 *>(a.Tm + (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0);
+    #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 t0v = *reinterpret_cast<const float4 *>(Mi + 8 * q);
+                const float4 t1v = *reinterpret_cast<const float4 *>(Mi + 8 * q + 4);
+                Tdst[q] = make_uint4(pack_bf2(t0v.x, t0v.y), pack_bf2(t0v.z, t0v.w), pack_bf2(t1v.x, t1v.y),
+                                     pack_bf2(t1v.z, t1v.w));
+                const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+                const int jb = j0 + 8 * q;
+                uint32_t pw[4], pu[4];
+    #pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    pw[z] = pack_bf2(tv[2 * z] * sm.wc[jb + 2 * z], tv[2 * z + 1] * sm.wc[jb + 2 * z + 1]);
+                    pu[z] = pack_bf2(tv[2 * z] * sm.beta[jb + 2 * z], tv[2 * z + 1] * sm.beta[jb + 2 * z + 1]);
+                }
+                *reinterpret_cast<uint4 *>(sm.op_w + sw128_off(i, jb)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                *reinterpret_cast<uint4 *>(sm.op_u + sw128_off(i, jb)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && ok) {  // w^T -> columns 0..63, u^T -> 64..127 (lane d, column i)
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 64, 1, 0);
+            const uint32_t ks = smem_u32(sm.k), vs = smem_u32(sm.v);
+            const uint32_t ws = smem_u32(sm.op_w), us = smem_u32(sm.op_u);
+            for (int s = 0; s < 4; ++s) {
+                mma_bf16(tb, sdesc(ks + s * 2048, kHalf, 1024), sdesc(ws + s * 32, 16, 1024), id, s > 0);
+                mma_bf16(tb + 64, sdesc(vs + s * 2048, kHalf, 1024), sdesc(us + s * 32, 16, 1024), id, s > 0);
+            }
+            mma_commit(&sm.mma_bar);
+        }
+        ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
+        mphase ^= 1;
+        tc_fence_after();
+        if (tid == 0 && ok && has_next) issue_kv(maps, sm, nx);  // K and V have been read
+        if (ok && has_next) ++issued;
+        if (ok) {  // thread d writes element d of every live token row of w and u
+            const size_t base = ((size_t)t0 * a.HV + hv) * kDim + tid;
+            const size_t tstride = (size_t)a.HV * kDim;
+            for (int part = 0; part < 2; ++part) {
+                bf16 *dst = (part == 0 ? a.w : a.u) + base;
+                float x0[32], x1[32];
+                tmem_ld32(t_row + 64 * part, x0);
+                tmem_ld32(t_row + 64 * part + 32, x1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < L) dst[(size_t)i * tstride] = __float2bfloat16_rn(x0[i]);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (32 + i < L) dst[(size_t)(32 + i) * tstride] = __float2bfloat16_rn(x1[i]);
+            }
+        }
+        tc_fence_before();
+        ok = __syncthreads_and(ok);  // the unit's scalars, operands and TMEM are free
+        if (!ok) break;
+        x = nx;
     }
-    ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, 1));
-    tc_fence_after();
-    if (ok) {  // thread d writes element d of every live token row of w and u
-        const size_t base = ((size_t)t0 * a.HV + hv) * kDim + tid;
-        const size_t tstride = (size_t)a.HV * kDim;
-        for (int part = 0; part < 2; ++part) {
-            bf16 *dst = (part == 0 ? a.w : a.u) + base;
-            float x0[32], x1[32];
-            tmem_ld32(t_row + 64 * part, x0);
-            tmem_ld32(t_row + 64 * part + 32, x1);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < L) dst[(size_t)i * tstride] = __float2bfloat16_rn(x0[i]);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (32 + i < L) dst[(size_t)(32 + i) * tstride] = __float2bfloat16_rn(x1[i]);
-        }
-    } else if (tid == 0 && a.status) {
-        atomicOr(a.status, 2);
+    if (!ok && tid == 0) {
+        if (a.status) atomicOr(a.status, 2);
+        if (issued > waited) mbar_wait(&sm.ld_bar, (issued - 1) & 1, 1u << 20);  // drain (bounded)
     }
     tc_fence_before();
     __syncthreads();
@@ -302,8 +368,12 @@ cudaError_t launch_intra_tc(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = sm_count(&sms)) != cudaSuccess) return e;
+    const int nunits = a.num_chunks * a.HV;
+    const int per = (nunits + 3 * sms - 1) / (3 * sms);
     TimerScope ts(a.timer, GDN_KERNEL_INTRA, s);
-    k_intra_tc<<<dim3(a.num_chunks, a.HV), kThr, smem, s>>>(a, m);
+    k_intra_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
     return cudaGetLastError();
 }
 

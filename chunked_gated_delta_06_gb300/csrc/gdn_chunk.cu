@@ -89,19 +89,30 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
     if (L <= 0) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = warp; i < L; i += kThreads / 32) {
-        const size_t row = ((size_t)(t0 + i) * a.H + h) * kDim;
-        float sq = 0.f, sk = 0.f;
+    // warp w takes rows w, w + 8, ..., w + 56: all 16 row slices (8 bytes a lane) are
+    // loaded before the first sum
+    constexpr int kRows = kChunk / (kThreads / 32);
+    uint2 xq[kRows], xk[kRows];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float x = bf2f(a.q[row + lane * 4 + e]);
-            float y = bf2f(a.k[row + lane * 4 + e]);
-            sq += x * x;
-            sk += y * y;
+    for (int m = 0; m < kRows; ++m) {
+        const int i = warp + 8 * m;
+        xq[m] = xk[m] = make_uint2(0u, 0u);
+        if (i < L) {
+            const size_t row = ((size_t)(t0 + i) * a.H + h) * kDim + lane * 4;
+            xq[m] = *reinterpret_cast<const uint2 *>(a.q + row);
+            xk[m] = *reinterpret_cast<const uint2 *>(a.k + row);
         }
+    }
+#pragma unroll
+    for (int m = 0; m < kRows; ++m) {
+        const int i = warp + 8 * m;
+        const float2 q0 = bf2_to_f2(xq[m].x), q1 = bf2_to_f2(xq[m].y);
+        const float2 k0 = bf2_to_f2(xk[m].x), k1 = bf2_to_f2(xk[m].y);
+        float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+        float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
         sq = warp_sum(sq);
         sk = warp_sum(sk);
-        if (lane == 0) {
+        if (lane == 0 && i < L) {
             a.rq[(size_t)(t0 + i) * a.H + h] = sqrtf(sq + kNormEps);
             a.rk[(size_t)(t0 + i) * a.H + h] = sqrtf(sk + kNormEps);
         }

@@ -5,8 +5,9 @@
 //
 // Persistent: one CTA of 256 threads per SM walks a contiguous run of (chunk,
 // value head) units, and the next unit's h, dh', dO, dv_new and v_new tiles load
-// as soon as batch 1 has consumed the current ones (q and k only when the key
-// head changes), so the loads run under the epilogues.  With h_c, dh_c [k][v] (bf16,
+// as soon as batch 1 has consumed the current ones; q and k (only when the key head
+// changes) load into a second buffer at the start of the unit before, so the loads
+// run under the epilogues.  With h_c, dh_c [k][v] (bf16,
 // from the forward and reverse scans), dO, dv_new, v_new [t][v], Qhat =
 // diag(scale / r_q) Q, Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
 //   batch 1 (M=64, rows = tokens, contraction 128):
@@ -58,8 +59,8 @@ struct BaSmem {
     unsigned char dO[2 * kBox];   // [t][v]
     unsigned char dvn[2 * kBox];
     unsigned char vn[2 * kBox];
-    unsigned char q[2 * kBox];    // [t][k]
-    unsigned char k[2 * kBox];
+    unsigned char q[2][2 * kBox];  // [t][k], two buffers (the next key head loads into the other)
+    unsigned char k[2][2 * kBox];
     unsigned char op_dmg[kBox];   // dMG_tj / r_k,j        [t][j]  K-major A of dMG Khat
     unsigned char op_dmgt[kBox];  // dMG_it scale / r_q,i  [i][t]  MN-major A of dMG^T Qhat
     float pq[2][64], pk[2][64];   // per-warpgroup partial row dots
@@ -68,7 +69,7 @@ struct BaSmem {
     float hdh[kThr / 32];
     float G[64], eg[64], egl_g[64];  // G, e^{G_t}, e^{G_L - G_t} (0 past L)
     float qsc[64], rki[64];       // scale / r_q, 1 / r_k
-    uint64_t a_bar, b_bar, mma_bar;   // group A (h, dh, dO, dv_new, v_new), group B (q, k)
+    uint64_t a_bar, b_bar[2], mma_bar;   // group A (h, dh, dO, dv_new, v_new), group B (q, k) per buffer
     uint32_t tmem_base;
 };
 
@@ -116,12 +117,12 @@ __device__ __forceinline__ void issue_a(const BaMaps &m, BaSmem &sm, const Chunk
     tma_load_3d(sm.vn + kBox, &m.vn, 64, x.hv, x.t0, &sm.a_bar);
 }
 
-__device__ __forceinline__ void issue_b(const BaMaps &m, BaSmem &sm, const Unit &x) {
-    mbar_arrive_expect_tx(&sm.b_bar, 4 * kBox);
-    tma_load_3d(sm.q, &m.q, 0, x.h, x.t0, &sm.b_bar);
-    tma_load_3d(sm.q + kBox, &m.q, 64, x.h, x.t0, &sm.b_bar);
-    tma_load_3d(sm.k, &m.k, 0, x.h, x.t0, &sm.b_bar);
-    tma_load_3d(sm.k + kBox, &m.k, 64, x.h, x.t0, &sm.b_bar);
+__device__ __forceinline__ void issue_b(const BaMaps &m, BaSmem &sm, const Unit &x, int bf) {
+    mbar_arrive_expect_tx(&sm.b_bar[bf], 4 * kBox);
+    tma_load_3d(sm.q[bf], &m.q, 0, x.h, x.t0, &sm.b_bar[bf]);
+    tma_load_3d(sm.q[bf] + kBox, &m.q, 64, x.h, x.t0, &sm.b_bar[bf]);
+    tma_load_3d(sm.k[bf], &m.k, 0, x.h, x.t0, &sm.b_bar[bf]);
+    tma_load_3d(sm.k[bf] + kBox, &m.k, 64, x.h, x.t0, &sm.b_bar[bf]);
 }
 
 
@@ -143,7 +144,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     }
     if (tid == 0) {
         mbar_init(&sm.a_bar, 1);
-        mbar_init(&sm.b_bar, 1);
+        mbar_init(&sm.b_bar[0], 1);
+        mbar_init(&sm.b_bar[1], 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
     }
@@ -155,10 +157,12 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     Unit x = unit_of(a, ub);
     if (tid == 0) {
         issue_a(maps, sm, a, x);
-        issue_b(maps, sm, x);
+        issue_b(maps, sm, x, 0);
     }
-    int a_issued = 1, a_waited = 0, b_issued = 1, b_waited = 0;  // same on every thread
-    bool need_b = true;  // the current unit waits for a q / k load
+    int a_issued = 1, a_waited = 0;           // same on every thread
+    uint32_t bpar = 0, bpend = 1;  // per q / k buffer (bit i): parity of its next wait, a load in flight
+    int bcur = 0;         // the q / k buffer of the current unit
+    bool need_b = true;   // the current unit waits for a q / k load
     // per-token scalars, fetched one unit ahead (threads 0..63)
     float pG = 0.f, pRq = 1.f, pRk = 1.f;
     auto fetch = [&](const Unit &y) {
@@ -184,10 +188,13 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             sm.rki[tid] = in ? 1.f / pRk : 0.f;
         }
         bool got = mbar_wait(&sm.a_bar, a_waited & 1);
-        if (need_b) got = mbar_wait(&sm.b_bar, b_waited & 1) && got;
+        if (need_b) got = mbar_wait(&sm.b_bar[bcur], (bpar >> bcur) & 1) && got;
         got = __syncthreads_and(got);
         ++a_waited;
-        if (need_b) ++b_waited;
+        if (need_b) {
+            bpar ^= 1u << bcur;
+            bpend &= ~(1u << bcur);
+        }
         if (!got) { ok = false; break; }
         const float Gl = L > 0 ? sm.G[L - 1] : 0.f;
         if (tid < 64) {
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             const uint32_t id128 = idesc_bf16(64, 128, 0, 0), id64 = idesc_bf16(64, 64, 0, 0);
             const uint32_t hs = smem_u32(sm.h), dhs = smem_u32(sm.dh);
             const uint32_t os = smem_u32(sm.dO), ds = smem_u32(sm.dvn), vs = smem_u32(sm.vn);
-            const uint32_t qs = smem_u32(sm.q), ks = smem_u32(sm.k);
+            const uint32_t qs = smem_u32(sm.q[bcur]), ks = smem_u32(sm.k[bcur]);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t ao = (s >> 2) * kBox + (s & 3) * 32, bo = (s >> 2) * kBig + (s & 3) * 32;
@@ -216,6 +223,13 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         // the next unit (its table entries are a dependent load: after the MMA issue)
         const Unit nx = has_next ? next_unit(a, x) : x;
         if (has_next) fetch(nx);
+        // a new key head for the next unit: its q / k load into the other buffer now (that
+        // buffer's last reader, an earlier unit, has finished)
+        const bool need_next_b = has_next && (nx.c != x.c || nx.h != x.h);
+        if (need_next_b) {
+            if (tid == 0) issue_b(maps, sm, nx, bcur ^ 1);
+            bpend |= 1u << (bcur ^ 1);
+        }
         // <h, dh'> while the products run: thread tid takes half a row of h and dh'
         float hdh = 0.f;
         {
@@ -310,7 +324,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             tc_fence_after();
             const uint32_t id_km = idesc_bf16(64, 128, 0, 1);  // A K-major, B MN-major
             const uint32_t id_mm = idesc_bf16(64, 128, 1, 1);  // A MN-major, B MN-major
-            const uint32_t ks = smem_u32(sm.k), qs = smem_u32(sm.q);
+            const uint32_t ks = smem_u32(sm.k[bcur]), qs = smem_u32(sm.q[bcur]);
             const uint32_t g1 = smem_u32(sm.op_dmg), g2 = smem_u32(sm.op_dmgt);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
@@ -333,7 +347,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
 #pragma unroll
             for (int m = 0; m < 2; ++m) {  // m = 0: dq with q; m = 1: dk with k
                 const uint32_t cA = m ? cDK : cDQ, cB = m ? cKI : cQI;
-                const unsigned char *tile = m ? sm.k : sm.q;
+                const unsigned char *tile = m ? sm.k[bcur] : sm.q[bcur];
                 bf16 *dst = m ? a.dkp : a.dqp;
                 const float fa = m ? ela : ega, fb = m ? elb : egb;
                 float xa = 0.f, xb = 0.f;
@@ -371,11 +385,6 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         }
         tc_fence_before();
         __syncthreads();  // q / k tiles, TMEM and the row sums are all read or written
-        need_b = has_next && (nx.c != x.c || nx.h != x.h);
-        if (need_b) {
-            if (tid == 0) issue_b(maps, sm, nx);
-            ++b_issued;
-        }
         if (warp == 0) {  // dG_t, and the G_L terms summed in a fixed order
             float dgz[2], sx = 0.f;
 #pragma unroll
@@ -404,13 +413,16 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             }
         }
         __syncthreads();  // the per-unit scalars are free for the next unit
+        if (need_next_b) bcur ^= 1;
+        need_b = need_next_b;
         x = nx;
     }
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving
         if (a_issued > a_waited) mbar_wait(&sm.a_bar, a_waited & 1, 1u << 20);
-        if (b_issued > b_waited) mbar_wait(&sm.b_bar, b_waited & 1, 1u << 20);
+        for (int bf = 0; bf < 2; ++bf)
+            if ((bpend >> bf) & 1) mbar_wait(&sm.b_bar[bf], (bpar >> bf) & 1, 1u << 20);
     }
     tc_fence_before();
     __syncthreads();

@@ -34,6 +34,15 @@ SMALL = [
 ]
 
 
+def test_many_short_sequences_match_oracle():
+    # 400 sequences of 1 .. 80 tokens: a chunk table and scan grid far wider than the
+    # small cases, with a partial chunk at the end of almost every sequence
+    lengths = np.random.default_rng(6).integers(1, 81, size=400).tolist()
+    wl = W.chunk_workload("many_short", lengths, 1, 2, seed=7, gate="softplus", h0=True,
+                          backward=True, d_ht=True)
+    compare_units(run_chunk(wl, torch), oracle_chunk(wl), wl)
+
+
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 def test_small_fwd_bwd_matches_oracle(case):
     name, lengths, H, HV, gate, h0, dht = case

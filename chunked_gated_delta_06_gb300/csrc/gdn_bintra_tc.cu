@@ -63,6 +63,8 @@ struct BaSmem {
     unsigned char k[2][2 * kBox];
     unsigned char op_dmg[kBox];   // dMG_tj / r_k,j        [t][j]  K-major A of dMG Khat
     unsigned char op_dmgt[kBox];  // dMG_it scale / r_q,i  [i][t]  MN-major A of dMG^T Qhat
+                                  // (after batch 2, with op_dmg: the dqhat rows of a full chunk)
+    unsigned char stg[2 * kBox];  // rows of a full chunk staged for TMA stores: dW, then dkhat
     float pq[2][64], pk[2][64];   // per-warpgroup partial row dots
     float rp[2][64];              // per-warpgroup partial row sums of P1
     float cp[4][64];              // per-row-block column sums of P1
@@ -75,6 +77,7 @@ struct BaSmem {
 
 struct BaMaps {
     CUtensorMap h, dh, dO, dvn, vn, q, k;
+    CUtensorMap dw, dqp, dkp;   // outputs, stored by TMA from a full chunk's staged rows
 };
 
 struct Unit {
@@ -251,6 +254,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         }
         hdh = warp_sum(hdh);
         if (lane == 0) sm.hdh[warp] = hdh;
+        if (tid == 0) tma_store_wait_read();  // the last unit's staged rows have been read
         bool done = __syncthreads_and(mbar_wait(&sm.mma_bar, phase));
         phase ^= 1;
         tc_fence_after();
@@ -301,7 +305,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 sm.rp[grp][rb] = rsb;
             }
             // (b) dW = -Dw rows on 16x256b fragments: rows ra, rb, this warpgroup's 64
-            // columns 64 grp + 32 cc + 8k + cq + {0, 1}
+            // columns 64 grp + 32 cc + 8k + cq + {0, 1}; a full chunk's rows are staged
+            // (this warpgroup's 64-column half of stg) for one TMA store
             const size_t oa = ((size_t)(x.t0 + (la ? ra : 0)) * a.HV + x.hv) * kDim;
             const size_t ob = ((size_t)(x.t0 + (lb ? rb : 0)) * a.HV + x.hv) * kDim;
             float dw[2][16];
@@ -312,9 +317,14 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int col = 64 * grp + 32 * cc + 8 * k + cq;
-                    if (la) *reinterpret_cast<uint32_t *>(a.dW + oa + col) = pack_bf2(-dw[cc][4 * k], -dw[cc][4 * k + 1]);
-                    if (lb) *reinterpret_cast<uint32_t *>(a.dW + ob + col) = pack_bf2(-dw[cc][4 * k + 2], -dw[cc][4 * k + 3]);
+                    const int cl = 32 * cc + 8 * k + cq, col = 64 * grp + cl;
+                    if (L == 64) {
+                        put_pair(sm.stg + grp * kBox, ra, cl, -dw[cc][4 * k], -dw[cc][4 * k + 1]);
+                        put_pair(sm.stg + grp * kBox, rb, cl, -dw[cc][4 * k + 2], -dw[cc][4 * k + 3]);
+                    } else {
+                        if (la) *reinterpret_cast<uint32_t *>(a.dW + oa + col) = pack_bf2(-dw[cc][4 * k], -dw[cc][4 * k + 1]);
+                        if (lb) *reinterpret_cast<uint32_t *>(a.dW + ob + col) = pack_bf2(-dw[cc][4 * k + 2], -dw[cc][4 * k + 3]);
+                    }
                 }
         }
         fence_proxy_async_smem();
@@ -332,11 +342,18 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 mma_bf16(tb + cKI, sdesc(g2 + s * 2048, kBox, 1024), sdesc(qs + s * 2048, kBox, 1024), id_mm, s > 0);
             }
             mma_commit(&sm.mma_bar);
+            if (L == 64) {  // the staged dW rows
+                tma_store_3d(&maps.dw, 0, x.hv, x.t0, sm.stg);
+                tma_store_3d(&maps.dw, 64, x.hv, x.t0, sm.stg + kBox);
+                tma_store_commit();
+            }
         }
         done = __syncthreads_and(mbar_wait(&sm.mma_bar, phase));
         phase ^= 1;
         tc_fence_after();
         if (!done) { ok = false; break; }
+        if (tid == 0) tma_store_wait_read();  // stg is rewritten below
+        __syncthreads();
         {  // dqhat, dkhat rows (this warpgroup's 64 columns) and the inter-term row dots,
            // on 16x256b fragments (rows ra, rb; columns c0 + 8k + cq + {0, 1})
             const float ega = la ? sm.eg[ra] : 0.f, egb = lb ? sm.eg[rb] : 0.f;
@@ -349,6 +366,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 const uint32_t cA = m ? cDK : cDQ, cB = m ? cKI : cQI;
                 const unsigned char *tile = m ? sm.k[bcur] : sm.q[bcur];
                 bf16 *dst = m ? a.dkp : a.dqp;
+                unsigned char *stage = m ? sm.stg : sm.op_dmg;  // two 64-column halves each
                 const float fa = m ? ela : ega, fb = m ? elb : egb;
                 float xa = 0.f, xb = 0.f;
 #pragma unroll
@@ -368,10 +386,15 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                         xa += qa.x * a0 + qa.y * a1;
                         xb += qb.x * b0 + qb.y * b1;
                         const int gcol = c0 + 8 * k + cq;
-                        if (la)
-                            *reinterpret_cast<uint32_t *>(dst + oa + gcol) = pack_bf2(a0 + ii[4 * k], a1 + ii[4 * k + 1]);
-                        if (lb)
-                            *reinterpret_cast<uint32_t *>(dst + ob + gcol) = pack_bf2(b0 + ii[4 * k + 2], b1 + ii[4 * k + 3]);
+                        if (L == 64) {
+                            put_pair(stage + (c0 >> 6) * kBox, ra, col, a0 + ii[4 * k], a1 + ii[4 * k + 1]);
+                            put_pair(stage + (c0 >> 6) * kBox, rb, col, b0 + ii[4 * k + 2], b1 + ii[4 * k + 3]);
+                        } else {
+                            if (la)
+                                *reinterpret_cast<uint32_t *>(dst + oa + gcol) = pack_bf2(a0 + ii[4 * k], a1 + ii[4 * k + 1]);
+                            if (lb)
+                                *reinterpret_cast<uint32_t *>(dst + ob + gcol) = pack_bf2(b0 + ii[4 * k + 2], b1 + ii[4 * k + 3]);
+                        }
                     }
                 }
                 if (m) { xka = xa; xkb = xb; } else { xqa = xa; xqb = xb; }
@@ -383,8 +406,16 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 sm.pk[grp][ra] = xka; sm.pk[grp][rb] = xkb;
             }
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();  // q / k tiles, TMEM and the row sums are all read or written
+        if (tid == 0 && L == 64) {  // the staged dqhat and dkhat rows
+            tma_store_3d(&maps.dqp, 0, x.hv, x.t0, sm.op_dmg);
+            tma_store_3d(&maps.dqp, 64, x.hv, x.t0, sm.op_dmg + kBox);
+            tma_store_3d(&maps.dkp, 0, x.hv, x.t0, sm.stg);
+            tma_store_3d(&maps.dkp, 64, x.hv, x.t0, sm.stg + kBox);
+            tma_store_commit();
+        }
         if (warp == 0) {  // dG_t, and the G_L terms summed in a fixed order
             float dgz[2], sx = 0.f;
 #pragma unroll
@@ -424,6 +455,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         for (int bf = 0; bf < 2; ++bf)
             if ((bpend >> bf) & 1) mbar_wait(&sm.b_bar[bf], (bpar >> bf) & 1, 1u << 20);
     }
+    if (tid == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
@@ -444,7 +476,10 @@ cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.vn, a.vnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
-        !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64))
+        !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
+        !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.dqp, a.dqp, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.dkp, a.dkp, a.HV, a.T, rowb, rowb * a.HV, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BaSmem) + 1024;
     static_assert(sizeof(BaSmem) + 1024 <= 232448, "shared memory budget");

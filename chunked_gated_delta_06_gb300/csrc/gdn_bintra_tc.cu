@@ -25,6 +25,7 @@
 // h / dh' are read as [N=k][K=v], i.e. their [k][v] tiles K-major; all tiles
 // come by TMA.  An M=64 result row t sits in TMEM lane 32 (t / 16) + t % 16; the
 // two warpgroups split the columns.  Column sums are warp butterflies.
+#include <stddef.h>
 #include <string.h>
 
 #include "gdn_epi.cuh"
@@ -74,6 +75,14 @@ struct BaSmem {
     uint64_t a_bar, b_bar[2], mma_bar;   // group A (h, dh, dO, dv_new, v_new), group B (q, k) per buffer
     uint32_t tmem_base;
 };
+
+// Every TMA / SW128 tile starts on a 1024-byte boundary of the (1024-aligned) struct.
+static_assert(offsetof(BaSmem, dh) % 1024 == 0 && offsetof(BaSmem, dO) % 1024 == 0 &&
+                  offsetof(BaSmem, dvn) % 1024 == 0 && offsetof(BaSmem, vn) % 1024 == 0 &&
+                  offsetof(BaSmem, q) % 1024 == 0 && offsetof(BaSmem, k) % 1024 == 0 &&
+                  offsetof(BaSmem, op_dmg) % 1024 == 0 && offsetof(BaSmem, op_dmgt) % 1024 == 0 &&
+                  offsetof(BaSmem, stg) % 1024 == 0,
+              "SW128 tiles on 1024-byte boundaries");
 
 struct BaMaps {
     CUtensorMap h, dh, dO, dvn, vn, q, k;

@@ -13,6 +13,7 @@
 // as token-row products (M=64, N=128); h_c [k][v], v_new and dO are read as
 // MN-major operands straight from their TMA tiles, and the results are read as
 // 16x256b fragments so that every lane writes bf16 pairs of two token rows.
+#include <stddef.h>
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -36,6 +37,7 @@ struct OutSmem {
     unsigned char kq[2 * kBig];   // [K; Q] per k-half: K rows 0..63, Q rows 64..127 (one TMA box each)
     unsigned char tv[2 * kBox];   // v_new (forward) or dO (backward) [t][v] per v-half
     unsigned char mm[kBox];       // M, row i at row i (bf16)
+    unsigned char stg[2 * kBox];  // a full chunk's output rows per v-half, for two TMA stores
     unsigned char hc[kForward ? 2 * kBig : 16];   // h_c [k][v] per v-half (forward only)
     float G[64], rq[64], rk[64];
     float qsc[64], rki[64], ct[64];  // scale / r_q, 1 / r_k, e^{G} scale / r_q
@@ -43,8 +45,14 @@ struct OutSmem {
     uint32_t tmem_base;
 };
 
+// Every TMA / SW128 tile starts on a 1024-byte boundary of the (1024-aligned) struct.
+static_assert(offsetof(OutSmem<true>, tv) % 1024 == 0 && offsetof(OutSmem<true>, mm) % 1024 == 0 &&
+                  offsetof(OutSmem<true>, stg) % 1024 == 0 && offsetof(OutSmem<true>, hc) % 1024 == 0 &&
+                  offsetof(OutSmem<false>, stg) % 1024 == 0,
+              "SW128 tiles on 1024-byte boundaries");
+
 struct OutMaps {
-    CUtensorMap q, k, h, tv;
+    CUtensorMap q, k, h, tv, out;   // out: o (forward) or dv_loc (backward)
 };
 
 template <bool kForward>
@@ -225,6 +233,7 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
             }
             mma_commit(&sm.mma_bar);
         }
+        if (tid == 0) tma_store_wait_read();  // the last unit's staged rows have been read
         ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, phase));
         phase ^= 1;
         tc_fence_after();
@@ -256,20 +265,32 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
                     } else {
                         x0 = r1[4 * k]; x1 = r1[4 * k + 1]; y0 = r1[4 * k + 2]; y1 = r1[4 * k + 3];
                     }
-                    if (la) *reinterpret_cast<uint32_t *>(da + v) = epi::pack_bf2(x0, x1);
-                    if (lb) *reinterpret_cast<uint32_t *>(db + v) = epi::pack_bf2(y0, y1);
+                    if (L == 64) {  // staged for the TMA store
+                        epi::put_pair(sm.stg + (c >> 1) * kBox, ra, v & 63, x0, x1);
+                        epi::put_pair(sm.stg + (c >> 1) * kBox, rb, v & 63, y0, y1);
+                    } else {
+                        if (la) *reinterpret_cast<uint32_t *>(da + v) = epi::pack_bf2(x0, x1);
+                        if (lb) *reinterpret_cast<uint32_t *>(db + v) = epi::pack_bf2(y0, y1);
+                    }
                 }
             }
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         ok = __syncthreads_and(ok);  // the unit's scalars, M operand and TMEM are free
         if (!ok) break;
+        if (tid == 0 && L == 64) {
+            tma_store_3d(&maps.out, 0, hv, t0, sm.stg);
+            tma_store_3d(&maps.out, 64, hv, t0, sm.stg + kBox);
+            tma_store_commit();
+        }
         x = nx;
     }
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         if (issued > waited) mbar_wait(&sm.tma_bar, (issued - 1) & 1, 1u << 20);  // drain (bounded)
     }
+    if (tid == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, kTmemCols<kForward>);
@@ -285,6 +306,8 @@ cudaError_t launch_out_mode(const ChunkArgs &a, cudaStream_t s) {
     if (!encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
         !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
         !encode_rows_bf16(&m.tv, kForward ? (const void *)a.vnew : (const void *)a.d_o, a.HV, a.T,
+                          rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.out, kForward ? (const void *)a.o : (const void *)a.dvloc, a.HV, a.T,
                           rowb, rowb * a.HV, 64))
         return cudaErrorInvalidValue;
     if (kForward && !encode_rows_bf16(&m.h, a.hc, 1, hrows, rowb, rowb, 128))

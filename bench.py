@@ -375,21 +375,21 @@ def bench_reference(args):
     from chunked_gated_delta_06_gb300 import workloads as W
     import oracle
     oracle.build()
-    wl = W.fb_32k_varlen(seed=0)
+    wl = W.CHUNK_CONFIGS[args.workload](seed=0)
     vals = []
     for i in range(args.warmup + args.steps):
         tok, dt, thr, used = run_oracle_sample(wl, args.ref_tokens)
         if i >= args.warmup:
             vals.append(tok / dt)
     v = statistics.median(vals)
-    sample = ("first %d tokens of the packed fb_32k_varlen workload (whole sequences in packing "
-              "order, last cut), all 32 value heads, fwd+bwd per step" % args.ref_tokens)
+    sample = ("first %d tokens of the packed %s workload (whole sequences in packing "
+              "order, last cut), all %d value heads, fwd+bwd per step" % (args.ref_tokens, args.workload, wl.HV))
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 32768 / v * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.T / v * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": "fb_32k_varlen", "T": 32768, "H": 16, "HV": 32, "K": 128,
-                       "V": 128, "chunk": 64, "parallelism": "replicas"},
+            "config": {"workload": args.workload, "T": wl.T, "num_seqs": wl.N, "H": wl.H, "HV": wl.HV,
+                       "K": wl.K, "V": wl.V, "chunk": C, "parallelism": "replicas"},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,

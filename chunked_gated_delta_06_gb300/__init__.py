@@ -15,3 +15,4 @@ from .binding import (GDN_DTYPE_BF16, GDN_DTYPE_F32, GdnError, GdnProblem,  # no
                       gdn_chunk_bwd, gdn_chunk_fwd, gdn_chunk_saved_bytes,
                       gdn_chunk_workspace_bytes, gdn_decode_step, lib, make_problem,
                       status_string)
+from .autograd import chunk_gated_delta_rule  # noqa: E402,F401

@@ -193,3 +193,12 @@ def test_paged_prefill_checks_its_arguments_before_any_launch(lib):
     assert call(idx=fake + 2) == binding.GDN_ERR_INVALID_ARG
     assert call(resume=fake + 1) == binding.GDN_ERR_INVALID_ARG
     assert call(ws=1024) == binding.GDN_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_differentiable_call_takes_packed_batches_only():
+    torch = pytest.importorskip("torch")
+    assert callable(gdn.chunk_gated_delta_rule)
+    x = torch.zeros((2, 4, 1, 128), dtype=torch.bfloat16)
+    gb = torch.zeros((2, 4, 1))
+    with pytest.raises(ValueError, match="B must be 1"):
+        gdn.chunk_gated_delta_rule(x, x, x, gb, gb)

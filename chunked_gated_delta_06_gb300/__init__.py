@@ -8,7 +8,8 @@ The library is loaded on first use; it must have been built with
 """
 from .binding import (GDN_DTYPE_BF16, GDN_DTYPE_F32, GdnError, GdnProblem,  # noqa: F401
                       chunk_bwd, chunk_bwd_gated, chunk_fwd, chunk_fwd_gated,
-                      chunk_prefill_paged, decode_step, gdn_chunk_prefill_paged,
+                      check_indices, chunk_prefill_paged, decode_step,
+                      gdn_check_indices, gdn_chunk_prefill_paged,
                       gdn_chunk_scan_plan,
                       decode_step_gated, gdn_chunk_bwd_gated, gdn_chunk_fwd_gated,
                       gdn_decode_step_gated,

@@ -104,6 +104,8 @@ def lib():
             L.gdn_chunk_prefill_paged.restype = ctypes.c_int
             L.gdn_chunk_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
             L.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
+            L.gdn_check_indices.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, _vp]
+            L.gdn_check_indices.restype = ctypes.c_int
             L.gdn_kernel_name.argtypes = [ctypes.c_int32]
             L.gdn_kernel_name.restype = ctypes.c_char_p
             _lib = L
@@ -246,6 +248,24 @@ def gdn_decode_step(batch, H, HV, K, V, scale, q, k, v, g, beta, state_pool, num
                                                device_status, stream, ctypes.byref(timer.struct)))
     return int(lib().gdn_decode_step(batch, H, HV, K, V, scale, q, k, v, g, beta, state_pool,
                                      num_slots, state_indices, o, device_status, stream))
+
+
+def gdn_check_indices(state_indices, batch, num_slots, bad_row) -> int:
+    return int(lib().gdn_check_indices(state_indices, batch, num_slots, bad_row))
+
+
+def check_indices(state_indices, num_slots):
+    """gdn_check_indices on a host array (numpy, list or CPU tensor) of decode slot
+    indices.  Returns -1 when every active (> 0) index is < num_slots and unique,
+    else the first offending row."""
+    idx = np.ascontiguousarray(
+        state_indices.numpy() if hasattr(state_indices, "numpy") else state_indices, dtype=np.int32)
+    bad = ctypes.c_int32(-1)
+    st = gdn_check_indices(idx.ctypes.data if idx.size else None, idx.size, int(num_slots),
+                           ctypes.byref(bad))
+    if st != GDN_OK and bad.value < 0:
+        raise GdnError(st, "gdn_check_indices")
+    return bad.value
 
 
 # ----------------------------------------------------------------------------- torch helpers

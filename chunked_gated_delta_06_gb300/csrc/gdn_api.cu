@@ -575,6 +575,29 @@ gdn_status gdn_decode_step(int32_t batch, int32_t num_k_heads, int32_t num_v_hea
                                  device_status, stream, nullptr);
 }
 
+gdn_status gdn_check_indices(const int32_t *state_indices, int32_t batch, int32_t num_slots,
+                             int32_t *bad_row) {
+    if (bad_row) *bad_row = -1;
+    if (batch < 0 || num_slots < 1 || (batch > 0 && !state_indices)) return GDN_ERR_INVALID_ARG;
+    // one bit per slot: O(batch + num_slots) and no ordering of the rows
+    uint64_t *seen = static_cast<uint64_t *>(calloc((static_cast<size_t>(num_slots) + 63) / 64, 8));
+    if (!seen) return GDN_ERR_INVALID_ARG;
+    gdn_status st = GDN_OK;
+    for (int32_t i = 0; i < batch; ++i) {
+        const int32_t s = state_indices[i];
+        if (s <= 0) continue;
+        const uint64_t bit = uint64_t(1) << (s & 63);
+        if (s >= num_slots || (seen[s >> 6] & bit)) {
+            if (bad_row) *bad_row = i;
+            st = GDN_ERR_INVALID_ARG;
+            break;
+        }
+        seen[s >> 6] |= bit;
+    }
+    free(seen);
+    return st;
+}
+
 const char *gdn_kernel_name(int32_t id) {
     static const char *names[GDN_KERNEL_COUNT] = {
         "plan", "prep", "intra", "state", "out", "dvloc", "bstate", "bintra_a", "bintra_b",

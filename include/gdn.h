@@ -228,6 +228,22 @@ gdn_status gdn_decode_step(int32_t batch, int32_t num_k_heads, int32_t num_v_hea
                            const int32_t *state_indices, void *o, int32_t *device_status,
                            gdn_stream_t stream);
 
+/* Host-side check of a decode batch's slot indices ("C6: GDN decode-step goldens
+ * and recurrent/conv state contract", State contract: one slot per active row).
+ * gdn_decode_step cannot see a repeated slot without a device-to-host copy, so
+ * it races on one instead; callers that want the rule enforced run this on the
+ * host copy of the indices before the step.  Reads only host memory, launches
+ * nothing, needs no GPU.
+ *   state_indices  int32 [batch] on the HOST
+ *   num_slots      pool size (>= 1)
+ *   bad_row        out, or NULL: the first row that breaks the rule, -1 if none
+ * Rows with an index <= 0 are null and may repeat.  Returns GDN_OK when every
+ * active index is < num_slots and no active index repeats; GDN_ERR_INVALID_ARG
+ * otherwise (also for batch < 0, num_slots < 1 or a NULL array with batch > 0).
+ * A repeat is reported at the later of the two rows. */
+gdn_status gdn_check_indices(const int32_t *state_indices, int32_t batch, int32_t num_slots,
+                             int32_t *bad_row);
+
 /* Fused gating ("C6: GDN decode-step goldens and recurrent/conv state
  * contract" (RL-Kernel #469), What and Provider): the decay and beta are
  * computed inside the kernels, in fp32, from their pre-activations:

@@ -202,3 +202,21 @@ def test_differentiable_call_takes_packed_batches_only():
     gb = torch.zeros((2, 4, 1))
     with pytest.raises(ValueError, match="B must be 1"):
         gdn.chunk_gated_delta_rule(x, x, x, gb, gb)
+
+
+def test_index_check_finds_repeats_and_out_of_range_slots(lib):
+    assert gdn.check_indices(np.array([3, 0, -1, 0, 5, 1], np.int32), 6) == -1
+    assert gdn.check_indices([], 1) == -1
+    assert gdn.check_indices([0, 0, -7], 1) == -1          # null rows may repeat
+    assert gdn.check_indices([4, 2, 9, 2, 2], 10) == 3     # later row of the first repeat
+    assert gdn.check_indices([4, 2, 10, 2], 10) == 2       # index == num_slots
+    assert gdn.check_indices(np.array([63, 64, 127, 128, 64]), 200) == 4  # across bit words
+    # the bench's decode batch: 256 draws without repeat from 1..511, some set to 0
+    from chunked_gated_delta_06_gb300 import workloads as W
+    dw = W.decode_workload(B=256, H=1, HV=1, num_slots=512, seed=3)
+    assert gdn.check_indices(dw.state_indices, 512) == -1
+    bad = ctypes.c_int32(7)
+    assert binding.gdn_check_indices(None, 3, 8, ctypes.byref(bad)) == binding.GDN_ERR_INVALID_ARG
+    assert binding.gdn_check_indices(None, 0, 0, None) == binding.GDN_ERR_INVALID_ARG
+    assert binding.gdn_check_indices(None, 0, 8, ctypes.byref(bad)) == binding.GDN_OK
+    assert bad.value == -1

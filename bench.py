@@ -78,6 +78,35 @@ def kernel_work(name, T, H, HV, N, C_total):
     return f, b
 
 
+def step_work(T, H, HV, N, backward=True, h0=True, final_state=True, d_final_state=False):
+    """Algorithmic (flops, minimum bytes) of a whole call on a problem.
+
+    Flops: per (token, value head) the forward's contractions of the chunked form,
+    4CK/r (K K^T and Q K^T once per key head) + 2C(K + 2V) (w, u, the intra part of o)
+    + 6KV (v_new, the state update, the inter part of o) + 2C^2/3 (the triangular
+    inverse); the backward counts twice the forward.  Bytes: the call's own inputs
+    and outputs, each moved once (q, k, v, g, beta, o; then dO, dq, dk, dv, dg,
+    dbeta; the fp32 states), none of the per-chunk intermediates."""
+    r = HV // H
+    f_fwd = (4 * C * D / r + 2 * C * (D + 2 * D) + 6 * D * D + 2 * C * C / 3) * T * HV
+    st = N * HV * D * D * 4
+    io = 2 * T * H * D * 2 + T * HV * D * 2 + T * HV * 6          # q, k, v, g, beta
+    fwd_b = io + T * HV * D * 2 + st * (h0 + final_state)          # + o, h0, final state
+    if not backward:
+        return f_fwd, fwd_b
+    bwd_b = (io + T * HV * D * 2 + 2 * T * H * D * 2 + T * HV * D * 2 + T * HV * 6
+             + st * (h0 + h0 + d_final_state))                      # dO; dq, dk, dv, dg, dbeta; h0, dh0, dht
+    return 3 * f_fwd, fwd_b + bwd_b
+
+
+def step_fractions(flops, nbytes, seconds, peaks):
+    """A call against both measured peaks: tensor (sustained bf16) and HBM (copy)."""
+    return {"tflops": flops / seconds / 1e12, "gbs": nbytes / seconds / 1e9,
+            "tensor_frac": flops / seconds / 1e12 / peaks["bf16_sustained"],
+            "hbm_frac": nbytes / seconds / 1e9 / peaks["hbm"],
+            "algorithmic_flops": flops, "min_bytes": nbytes}
+
+
 # kernel name -> source file (the DRAM-traffic record is valid only for the source it was taken on)
 KERNEL_SOURCE = {
     "intra": "gdn_intra_tc.cu", "state": "gdn_state_tc.cu", "out": "gdn_out_tc.cu",
@@ -198,6 +227,7 @@ STEP_MODES = {
     "recompute": "gdn_chunk_fwd (no saved buffer) + gdn_chunk_bwd in recompute-state mode",
     "ckpt": "gdn_chunk_fwd (no saved buffer) + gdn_chunk_fwd (saving) + gdn_chunk_bwd",
     "gated": "gdn_chunk_fwd_gated (saving) + gdn_chunk_bwd_gated: g, beta from the fused gate",
+    "fwd": "gdn_chunk_fwd (o and the final state; no backward follows)",
 }
 
 
@@ -214,7 +244,7 @@ class ChunkRunner:
         f32 = wl.beta_f32 is not None
         self.beta = torch.from_numpy(wl.beta_f32).to(dev) if f32 else _bf(torch, wl.beta_bits, dev)
         self.h0 = None if wl.h0 is None else torch.from_numpy(wl.h0).to(dev)
-        self.d_o = _bf(torch, wl.do_bits, dev)
+        self.d_o = None if mode == "fwd" else _bf(torch, wl.do_bits, dev)
         self.d_ht = None if wl.d_ht is None else torch.from_numpy(wl.d_ht).to(dev)
         self.cu_dev = torch.from_numpy(wl.cu_seqlens).to(dev)
         self.p, self._keep = gdn.make_problem(wl.cu_seqlens, H, HV, cu_dev_ptr=self.cu_dev.data_ptr(),
@@ -222,8 +252,11 @@ class ChunkRunner:
         e = lambda *s, dt=torch.float32: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
         self.o = e(T, HV, D, dt=torch.bfloat16)
         self.ht = e(N, HV, D, D)
-        self.saved = None if mode == "recompute" else e(gdn.gdn_chunk_saved_bytes(self.p), dt=torch.uint8)
+        self.saved = (None if mode in ("recompute", "fwd") else
+                      e(gdn.gdn_chunk_saved_bytes(self.p), dt=torch.uint8))
         self.ws_f = e(gdn.gdn_chunk_workspace_bytes(self.p, 0), dt=torch.uint8)
+        if mode == "fwd":
+            return
         self.ws_b = e(gdn.gdn_chunk_workspace_bytes(self.p, 2 if mode == "recompute" else 1), dt=torch.uint8)
         self.dq, self.dk = torch.empty_like(self.q), torch.empty_like(self.k)
         self.dv = torch.empty_like(self.v)
@@ -267,6 +300,8 @@ class ChunkRunner:
         s = (stream or self.torch.cuda.current_stream()).cuda_stream
         if self.mode == "gated":
             return self._gated_step(s)
+        if self.mode == "fwd":
+            return self._fwd(None, s, timer)
         if self.mode == "ckpt":
             self._fwd(None, s, timer)  # the forward of the checkpointed step keeps nothing
         self._fwd(self.saved, s, timer)
@@ -282,6 +317,8 @@ class ChunkRunner:
                 if x is not None]
 
     def outputs(self):
+        if self.mode == "fwd":
+            return [self.o, self.ht]
         return [self.o, self.ht, self.dq, self.dk, self.dv, self.dg, self.dbeta, self.dh0]
 
 
@@ -459,6 +496,37 @@ def bench_ours(args):
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roof, "kernels": ktab, "gpu_launches": launches_per_step * args.steps,
             "clocks": clk}
+    sf, sb = step_work(T, H, HV, N, True, wl.h0 is not None, True, wl.d_ht is not None)
+    line["step_roofline"] = step_fractions(sf, sb, ms / 1e3, peaks)
+
+    # the other chunk workloads of the method's configurations, each timed the same
+    # way (device-timed steps on resident inputs larger than L2, but for the
+    # 256-token forward, which fits in L2 and runs warm), with the whole call
+    # against both peaks
+    if not args.no_workloads:
+        others = {}
+        for name in ("fwd_t256", "fb_4x4096", "fb_65536_long"):
+            if name == args.workload:
+                continue
+            owl = W.CHUNK_CONFIGS[name](seed=rank)
+            mode = "saved" if owl.backward else "fwd"
+            orun = ChunkRunner(torch, owl, dev, mode=mode)
+            for _ in range(max(3, args.warmup)):
+                orun.step()
+            barrier()
+            osteps = max(3, min(args.steps, 10))
+            oms, otok = aggregate_over_ranks(_time_loop(torch, orun.step, osteps), owl.T)
+            barrier()
+            of, ob = step_work(owl.T, owl.H, owl.HV, owl.N, owl.backward, owl.h0 is not None, True,
+                               owl.d_ht is not None)
+            others[name] = {"value": otok / (oms / 1e3), "unit": "tokens/s", "ms_per_step": oms,
+                            "steps": osteps, "step": STEP_MODES[mode],
+                            "config": {"T": owl.T, "num_seqs": owl.N, "H": owl.H, "HV": owl.HV,
+                                       "initial_state": owl.h0 is not None,
+                                       "d_final_state": owl.d_ht is not None},
+                            **step_fractions(of, ob, oms / 1e3, peaks)}
+            del orun, owl
+        line["workloads"] = others
 
     # the other training-step forms on the same workload: recompute-state mode,
     # the checkpointed step, and fp32 beta (same kernels; device-timed like value)
@@ -693,6 +761,9 @@ def main():
     ap.add_argument("--no-segscan", action="store_true", help="skip the segment-parallel scan timing")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the recompute-state, checkpointed-step and fp32-beta timings")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the timings of the other chunk workloads (256-token forward, "
+                         "4x4096, 1x65536 with 64 value heads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=2048,
                     help="tokens of the workload the oracle runs per baseline sample")

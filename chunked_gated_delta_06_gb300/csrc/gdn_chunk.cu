@@ -150,16 +150,50 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&t);
 }
 
+// R = HV / H when it is a compile-time case (1, 2, 4), else 0 (read from a): with R
+// known, every load of the item (q, k, the norms and the 3 R partials) is issued
+// before the first is used.  The sums run in the same order either way.
+template <int R>
 __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
     const int l16 = threadIdx.x & 15;
     const size_t item = (size_t)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
     const bool valid = item < (size_t)a.T * a.H;
     const int t = valid ? (int)(item / a.H) : 0, h = valid ? (int)(item % a.H) : 0;
-    const int r = a.HV / a.H;
+    const int r = R > 0 ? R : a.HV / a.H;
+    const size_t row = ((size_t)t * a.H + h) * kDim + l16 * 8;
+    uint4 lq = make_uint4(0u, 0u, 0u, 0u), lk = lq;
+    float rq = 1.f, rk = 1.f;
+    if (valid) {
+        lq = *reinterpret_cast<const uint4 *>(a.q + row);
+        lk = *reinterpret_cast<const uint4 *>(a.k + row);
+        rq = a.rq[(size_t)t * a.H + h];
+        rk = a.rk[(size_t)t * a.H + h];
+    }
     float dq[8], dk[8], xq[8], xk[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) dq[u] = dk[u] = 0.f;
-    if (valid) {
+    if constexpr (R > 0) {
+        uint4 p1[R], p2[R], p3[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const size_t o = ((size_t)t * a.HV + h * R + j) * kDim + l16 * 8;
+            p1[j] = valid ? *reinterpret_cast<const uint4 *>(a.dqp + o) : make_uint4(0u, 0u, 0u, 0u);
+            p2[j] = valid ? *reinterpret_cast<const uint4 *>(a.dkp + o) : make_uint4(0u, 0u, 0u, 0u);
+            p3[j] = valid ? *reinterpret_cast<const uint4 *>(a.dkp2 + o) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            float x1[8], x2[8], x3[8];
+            unpack8(p1[j], x1);
+            unpack8(p2[j], x2);
+            unpack8(p3[j], x3);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                dq[u] += x1[u];
+                dk[u] += x2[u] + x3[u];
+            }
+        }
+    } else if (valid) {
         for (int j = 0; j < r; ++j) {
             const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + l16 * 8;
             float x1[8], x2[8], x3[8];
@@ -173,15 +207,8 @@ __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
             }
         }
     }
-    const size_t row = ((size_t)t * a.H + h) * kDim + l16 * 8;
-    const float rq = valid ? a.rq[(size_t)t * a.H + h] : 1.f, rk = valid ? a.rk[(size_t)t * a.H + h] : 1.f;
-    if (valid) {
-        unpack8(*reinterpret_cast<const uint4 *>(a.q + row), xq);
-        unpack8(*reinterpret_cast<const uint4 *>(a.k + row), xk);
-    } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) xq[u] = xk[u] = 0.f;
-    }
+    unpack8(lq, xq);
+    unpack8(lk, xk);
     float nq = 0.f, nk = 0.f;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -279,7 +306,11 @@ cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
         const size_t items = (size_t)a.T * a.H;
         const unsigned blocks = (unsigned)((items + kThreads / 16 - 1) / (kThreads / 16));
         TimerScope ts(a.timer, GDN_KERNEL_BNORM, s);
-        k_bnorm<<<blocks, kThreads, 0, s>>>(a);
+        const int r = a.HV / a.H;
+        if (r == 1) k_bnorm<1><<<blocks, kThreads, 0, s>>>(a);
+        else if (r == 2) k_bnorm<2><<<blocks, kThreads, 0, s>>>(a);
+        else if (r == 4) k_bnorm<4><<<blocks, kThreads, 0, s>>>(a);
+        else k_bnorm<0><<<blocks, kThreads, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

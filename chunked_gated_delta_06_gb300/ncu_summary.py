@@ -89,6 +89,8 @@ KERNELS = {  # ncu kernel name -> (bench kernel name, source file)
     "k_state_tc<0>": ("state", "gdn_state_tc.cu"), "k_bstate_tc<0>": ("bstate", "gdn_bstate_tc.cu"),
     "k_bintra_b_tc": ("bintra_b", "gdn_bintra_b_tc.cu"), "k_decode": ("decode", "gdn_decode.cu"),
     "k_bnorm": ("bnorm", "gdn_chunk.cu"), "k_prep": ("prep", "gdn_chunk.cu"),
+    "k_bnorm<1>": ("bnorm", "gdn_chunk.cu"), "k_bnorm<2>": ("bnorm", "gdn_chunk.cu"),
+    "k_bnorm<4>": ("bnorm", "gdn_chunk.cu"), "k_bnorm<0>": ("bnorm", "gdn_chunk.cu"),
 }
 
 

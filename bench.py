@@ -426,7 +426,8 @@ def bench_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "T": wl.T, "num_seqs": wl.N, "H": wl.H, "HV": wl.HV,
-                       "K": wl.K, "V": wl.V, "chunk": C, "parallelism": "replicas"},
+                       "K": wl.K, "V": wl.V, "chunk": C,
+                       "parallelism": "single" if world == 1 else "rank 0 alone (host cores)"},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,

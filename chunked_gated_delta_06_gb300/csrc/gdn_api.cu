@@ -56,7 +56,8 @@ void plan_segments(const gdn_problem *p, Dims *d) {
     int longest = 0;
     double total = 0.0;
     for (int n = 0; n < N; ++n) {
-        const int c = (p->cu_seqlens_host[n + 1] - p->cu_seqlens_host[n] + gdn::kChunk - 1) / gdn::kChunk;
+        const int c = (int)(((int64_t)p->cu_seqlens_host[n + 1] - p->cu_seqlens_host[n] + gdn::kChunk - 1) /
+                            gdn::kChunk);
         longest = c > longest ? c : longest;
         total += c;
     }
@@ -77,7 +78,8 @@ void plan_segments(const gdn_problem *p, Dims *d) {
         int smax = 1;
         double w1 = 0.0, w2 = 0.0;
         for (int n = 0; n < N; ++n) {
-            const int c = (p->cu_seqlens_host[n + 1] - p->cu_seqlens_host[n] + gdn::kChunk - 1) / gdn::kChunk;
+            const int c = (int)(((int64_t)p->cu_seqlens_host[n + 1] - p->cu_seqlens_host[n] + gdn::kChunk - 1) /
+                                gdn::kChunk);
             const int S = c > 0 ? (c + L - 1) / L : 1;
             smax = S > smax ? S : smax;
             if (S == 1) {
@@ -119,7 +121,7 @@ gdn_status check_problem(const gdn_problem *p, Dims *d) {
     int64_t chunks = 0;
     for (int n = 0; n < p->num_seqs; ++n) {
         if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARG;
-        chunks += (cu[n + 1] - cu[n] + gdn::kChunk - 1) / gdn::kChunk;
+        chunks += ((int64_t)cu[n + 1] - cu[n] + gdn::kChunk - 1) / gdn::kChunk;
     }
     d->N = p->num_seqs;
     d->T = (int)p->total_tokens;

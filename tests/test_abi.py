@@ -220,3 +220,20 @@ def test_index_check_finds_repeats_and_out_of_range_slots(lib):
     assert binding.gdn_check_indices(None, 0, 0, None) == binding.GDN_ERR_INVALID_ARG
     assert binding.gdn_check_indices(None, 0, 8, ctypes.byref(bad)) == binding.GDN_OK
     assert bad.value == -1
+
+
+def test_sizes_at_the_largest_token_count(lib):
+    """T = 2^31 - 1 in one sequence: the chunk count and every size are computed
+    without overflow (no launch: size queries and the scan plan only)."""
+    T = 2**31 - 1
+    p, keep = _problem([0, T], H=1, HV=1)
+    C = (T + 63) // 64
+    saved = gdn.gdn_chunk_saved_bytes(p)
+    # h_c (bf16 per chunk), v_new and w rows (bf16), T per chunk (bf16), r_q, r_k, G (fp32),
+    # each rounded up to 256 bytes
+    need = C * 128 * 128 * 2 + 2 * T * 128 * 2 + C * 64 * 64 * 2 + 3 * T * 4
+    assert need <= saved <= need + 7 * 256
+    for mode in (0, 1, 2):
+        assert gdn.gdn_chunk_workspace_bytes(p, mode) > 0
+    st, seg_len, nseg = gdn.gdn_chunk_scan_plan(p)
+    assert st == binding.GDN_OK and nseg >= 1

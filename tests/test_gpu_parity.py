@@ -110,3 +110,33 @@ def test_fb_32k_varlen_repeats_bit_for_bit():
     for key in a:
         if a[key] is not None:
             assert torch.equal(a[key], b[key]), key
+
+
+def test_hundred_repeats_of_the_32k_varlen_step_are_bit_identical():
+    """fwd + bwd of the 32K varlen pack 100 times (every tenth on a side stream):
+    every output of every run equals the first run's bit for bit."""
+    import chunked_gated_delta_06_gb300 as gdn
+    from gpu_helpers import to_dev
+    wl = W.fb_32k_varlen()
+    d = to_dev(wl, torch)
+    side = torch.cuda.Stream()
+
+    def step():
+        o, ht, ctx = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], wl.cu_seqlens, d["cu_dev"],
+                                   initial_state=d["h0"], output_final_state=True, for_backward=True)
+        gr = gdn.chunk_bwd(ctx, d["q"], d["k"], d["v"], d["g"], d["beta"], d["d_o"],
+                           d_final_state=d["d_ht"], initial_state=d["h0"])
+        return dict(o=o, ht=ht, **gr)
+
+    first = step()
+    for i in range(1, 100):
+        if i % 10 == 0:
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                out = step()
+            torch.cuda.current_stream().wait_stream(side)
+        else:
+            out = step()
+        for key, ref in first.items():
+            if ref is not None:
+                assert torch.equal(out[key], ref), (i, key)

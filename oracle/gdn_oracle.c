@@ -367,7 +367,7 @@ void gdn_oracle_fwd_chunked(int N, const int *cu, int H, int HV, int K, int V,
                     if (j < i) {
                         double kk = 0.0;
                         for (int c = 0; c < K; ++c) kk += Kh[(size_t)i * K + c] * Kh[(size_t)j * K + c];
-                        a = bi * kk * exp(G[i] - G[j]);
+                        a = bi * kk * (g_mutation == 11 ? exp(G[j] - G[i]) : exp(G[i] - G[j]));  /* 11: flipped */
                     }
                     A[(size_t)i * C + j] = a;
                 }
@@ -427,7 +427,7 @@ void gdn_oracle_fwd_chunked(int N, const int *cu, int H, int HV, int K, int V,
             double GL = G[L - 1], egl = exp(GL);
             for (size_t i = 0; i < SZ; ++i) hs[i] *= egl;
             for (int j = 0; j < L; ++j) {
-                double f = exp(GL - G[j]);
+                double f = g_mutation == 12 ? exp(G[j] - GL) : exp(GL - G[j]);  /* 12: flipped */
                 for (int a = 0; a < K; ++a) {
                     double ka = f * Kh[(size_t)j * K + a];
                     for (int c = 0; c < V; ++c) hs[(size_t)a * V + c] += ka * vn[(size_t)j * V + c];
@@ -468,7 +468,8 @@ int gdn_oracle_decode(int B, int H, int HV, int K, int V, double scale, int use_
         l2_normalise(q + ((size_t)b * H + h) * K, K, use_l2norm, scale, qh, NULL);
         l2_normalise(k + ((size_t)b * H + h) * K, K, use_l2norm, 1.0, kh, NULL);
         token_step(S, K, V, kh, qh, v + ((size_t)b * HV + hv) * V,
-                   exp(g[(size_t)b * HV + hv]), beta[(size_t)b * HV + hv], orow, NULL, NULL);
+                   g_mutation == 13 ? 1.0 : exp(g[(size_t)b * HV + hv]),  /* 13: decay left out */
+                   beta[(size_t)b * HV + hv], orow, NULL, NULL);
     }
     free(qh); free(kh);
     return bad;

@@ -551,8 +551,10 @@ PINS = [
 # 1 decay after the write, 2 prediction from the undecayed state, 3 output before the write,
 # 4 scale on k too, 5 epsilon outside the sqrt, 6 sign of dp flipped (backward), 7 key head hv % H,
 # 8 dbeta -> db through beta instead of beta (1 - beta), 9 da through softplus instead of its slope,
-# 10 paged prefill reads and writes the slots without transposing
-MUTATIONS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10]
+# 10 paged prefill reads and writes the slots without transposing, 11 chunked form: the
+# decay in A as e^{G_j - G_i}, 12 chunked form: the state update's decay factor e^{G_j - G_L},
+# 13 decode step without the decay
+MUTATIONS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13]
 
 
 @pytest.mark.parametrize("m", MUTATIONS)

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from chunked_gated_delta_06_gb300 import workloads as W
-from gpu_helpers import close, compare_units, oracle_chunk, run_chunk, run_chunk_raw
+from gpu_helpers import compare_units, oracle_chunk, run_chunk, run_chunk_raw
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu

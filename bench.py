@@ -235,7 +235,7 @@ class ChunkRunner:
     """Device buffers of one chunk workload and one training step through the C ABI
     (mode: a key of STEP_MODES; beta in fp32 when the workload carries fp32 beta)."""
 
-    def __init__(self, torch, wl, dev, mode="saved"):
+    def __init__(self, torch, wl, dev, mode="saved", scan_segment_chunks=0):
         import chunked_gated_delta_06_gb300 as gdn
         self.torch, self.gdn, self.wl, self.dev, self.mode = torch, gdn, wl, dev, mode
         T, H, HV, N = wl.T, wl.H, wl.HV, wl.N
@@ -247,8 +247,11 @@ class ChunkRunner:
         self.d_o = None if mode == "fwd" else _bf(torch, wl.do_bits, dev)
         self.d_ht = None if wl.d_ht is None else torch.from_numpy(wl.d_ht).to(dev)
         self.cu_dev = torch.from_numpy(wl.cu_seqlens).to(dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.p, self._keep = gdn.make_problem(wl.cu_seqlens, H, HV, cu_dev_ptr=self.cu_dev.data_ptr(),
-                                              beta_dtype=gdn.GDN_DTYPE_F32 if f32 else gdn.GDN_DTYPE_BF16)
+                                              beta_dtype=gdn.GDN_DTYPE_F32 if f32 else gdn.GDN_DTYPE_BF16,
+                                              device_status_ptr=self.status.data_ptr(),
+                                              scan_segment_chunks=scan_segment_chunks)
         e = lambda *s, dt=torch.float32: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
         self.o = e(T, HV, D, dt=torch.bfloat16)
         self.ht = e(N, HV, D, D)
@@ -312,6 +315,12 @@ class ChunkRunner:
         if st:
             raise gdn.GdnError(st, "gdn_chunk_bwd")
 
+    def check_status(self):
+        """The kernels' status word after the steps so far (must stay 0)."""
+        st = int(self.status.item())
+        if st:
+            raise RuntimeError("device status %d after the timed steps" % st)
+
     def inputs(self):
         return [x for x in (self.q, self.k, self.v, self.g, self.beta, self.h0, self.d_o, self.d_ht)
                 if x is not None]
@@ -322,28 +331,70 @@ class ChunkRunner:
         return [self.o, self.ht, self.dq, self.dk, self.dv, self.dg, self.dbeta, self.dh0]
 
 
-def _time_loop(torch, fn, steps):
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _time_steps(torch, fn, steps, flush=True):
+    """Per-step device times in ms ("cake_gdn: deterministic chunked GDN training
+    kernels", section 2, Operator level, Method): before every step a 512 MiB memset
+    evicts L2 (outside the timed region), then CUDA events on the launching stream
+    bracket the step alone.  Returns the list of per-step times."""
+    buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda") if flush else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize()
-    a.record()
-    for _ in range(steps):
+    for i in range(steps):
+        if buf is not None:
+            buf.zero_()
+        starts[i].record()
         fn()
-    b.record()
+        stops[i].record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps
+    del buf
+    return [a.elapsed_time(b) for a, b in zip(starts, stops)]
 
 
-def _kernel_table(torch, runner_step, steps, capacity):
+def _time_loop(torch, fn, steps, flush=True):
+    """Median per-step time (ms) under the protocol of _time_steps."""
+    return statistics.median(_time_steps(torch, fn, steps, flush))
+
+
+def _kernel_table(torch, runner_step, steps, capacity, flush=True):
+    """Per-kernel device times (ms) of `steps` steps, each after an L2 flush:
+    {kernel name: [duration of each launch]}."""
     from chunked_gated_delta_06_gb300.binding import KernelTimer
     timer = KernelTimer(capacity)
+    buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda") if flush else None
     per = {}
     for _ in range(steps):
+        if buf is not None:
+            buf.zero_()
         timer.reset()
         runner_step(timer)
         for name, ms in timer.records():
             per.setdefault(name, []).append(ms)
+    del buf
     return per
+
+
+def _cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 # ---------------------------------------------------------------------------- CPU oracle
@@ -405,7 +456,10 @@ def _dist():
 
 
 def bench_reference(args):
-    """The oracle (fp64 CPU) on the same workload, metric and unit."""
+    """The oracle (fp64 CPU) on the same workload, metric and unit: every step runs
+    fwd+bwd on a bounded sample of the workload (its first --ref-tokens tokens, whole
+    sequences in packing order, every value head); value and ms_per_step are those of
+    the sample actually run."""
     rank, world, _ = _dist()
     if rank != 0:
         return
@@ -413,23 +467,26 @@ def bench_reference(args):
     import oracle
     oracle.build()
     wl = W.CHUNK_CONFIGS[args.workload](seed=0)
-    vals = []
+    vals, secs = [], []
+    tok = used = 0
     for i in range(args.warmup + args.steps):
         tok, dt, thr, used = run_oracle_sample(wl, args.ref_tokens)
         if i >= args.warmup:
             vals.append(tok / dt)
+            secs.append(dt)
     v = statistics.median(vals)
     sample = ("first %d tokens of the packed %s workload (whole sequences in packing "
-              "order, last cut), all %d value heads, fwd+bwd per step" % (args.ref_tokens, args.workload, wl.HV))
+              "order, last cut), all %d value heads, fwd+bwd per step" % (tok, args.workload, wl.HV))
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.T / v * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "T": wl.T, "num_seqs": wl.N, "H": wl.H, "HV": wl.HV,
                        "K": wl.K, "V": wl.V, "chunk": C,
+                       "sample_tokens_per_step": tok,
                        "parallelism": "single" if world == 1 else "rank 0 alone (host cores)"},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                             "cpu_model": _cpu_model(), "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -464,45 +521,65 @@ def bench_ours(args):
     barrier()
     clocks = ClockSampler(local)
     clocks.start()
-    ms = _time_loop(torch, run.step, args.steps)
+    step_ms = _time_steps(torch, run.step, args.steps)
     clk = clocks.stop()
     barrier()
-    ms, total_tokens = aggregate_over_ranks(ms, T)
+    run.check_status()
+    ms, total_tokens = aggregate_over_ranks(statistics.median(step_ms), T)
     value = total_tokens / (ms / 1e3)
 
-    # per-kernel durations (same steps with the kernel timer), launches per step
-    per = _kernel_table(torch, run.step, max(3, min(args.steps, 10)), 64)
-    launches_per_step = sum(len(v) for v in per.values()) // max(3, min(args.steps, 10))
-    ktab = {k: {"ms": statistics.mean(v), "launches_per_step": len(v) // max(3, min(args.steps, 10))}
+    # per-kernel durations (the same steps with the kernel timer, each after an L2
+    # flush; median per kernel), launches per step
+    ksteps = max(3, min(args.steps, 10))
+    per = _kernel_table(torch, run.step, ksteps, 64)
+    launches_per_step = sum(len(v) for v in per.values()) // ksteps
+    ktab = {k: {"ms": statistics.median(v), "launches_per_step": len(v) // ksteps}
             for k, v in per.items()}
     dom = max(ktab, key=lambda k: ktab[k]["ms"] * ktab[k]["launches_per_step"])
     fl, by = kernel_work(dom, T, H, HV, N, C_total)
-    roof = roofline(dom, fl, by, ktab[dom]["ms"] / 1e3, peaks, C_total * HV)
+    dom_roof = roofline(dom, fl, by, ktab[dom]["ms"] / 1e3, peaks, C_total * HV)
+    step_bytes = 0
     for k in ktab:
         f_, b_ = kernel_work(k, T, H, HV, N, C_total)
+        step_bytes += b_ * ktab[k]["launches_per_step"]
         ktab[k]["tflops"] = f_ / (ktab[k]["ms"] / 1e3) / 1e12 if f_ else None
         ktab[k]["gbs"] = b_ / (ktab[k]["ms"] / 1e3) / 1e9 if b_ else None
         ktab[k]["tensor_frac"] = (ktab[k]["tflops"] / peaks["bf16_sustained"]) if f_ else None
         ktab[k]["hbm_frac"] = (ktab[k]["gbs"] / peaks["hbm"]) if b_ else None
+        ktab[k]["algorithmic_bytes"] = b_
+
+    sf, sb = step_work(T, H, HV, N, True, wl.h0 is not None, True, wl.d_ht is not None)
+    srf = step_fractions(sf, sb, ms / 1e3, peaks)
+    # the headline roofline is the whole step on the tensor cores (the target is half of
+    # the sustained bf16 peak); the kernel with the largest share of the step follows
+    # with its own bound and its ncu DRAM traffic
+    traffic = [measured_traffic(k, C_total * HV) for k in ktab if k not in ("plan",)]
+    roof = {"scope": "whole fwd+bwd step (every kernel of gdn_chunk_fwd + gdn_chunk_bwd)",
+            "bound": "tensor", "achieved": srf["tflops"], "peak": peaks["bf16_sustained"],
+            "unit": "TFLOP/s", "frac": srf["tensor_frac"], "target_frac": 0.5,
+            "peak_source": "bf16_tflops_sustained (%s)" % peaks["source"],
+            "algorithmic_flops": sf,
+            "traffic": (sum(traffic) if traffic and all(t is not None for t in traffic) else None),
+            "kernel_bytes_per_step": step_bytes,
+            "dominant_kernel": dom_roof}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_per_step_mean": statistics.mean(step_ms),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": args.workload, "T": T, "num_seqs": N, "H": H, "HV": HV,
                        "K": D, "V": D, "chunk": C, "chunks": C_total,
                        "step": "gdn_chunk_fwd (saving for backward) + gdn_chunk_bwd",
-                       "l2": "inputs larger than L2 (q,k,v,dO = %.0f MB)" % (
-                           (2 * T * H + 2 * T * HV) * D * 2 / 1e6),
+                       "l2": "512 MiB memset before every timed step (outside the timed region); "
+                             "the median of the per-step CUDA-event times",
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roof, "kernels": ktab, "gpu_launches": launches_per_step * args.steps,
             "clocks": clk}
-    sf, sb = step_work(T, H, HV, N, True, wl.h0 is not None, True, wl.d_ht is not None)
-    line["step_roofline"] = step_fractions(sf, sb, ms / 1e3, peaks)
+    line["step_roofline"] = srf
 
     # the other chunk workloads of the method's configurations, each timed the same
-    # way (device-timed steps on resident inputs larger than L2, but for the
-    # 256-token forward, which fits in L2 and runs warm), with the whole call
+    # way (per-step CUDA events after an L2 flush, the median), with the whole call
     # against both peaks
     if not args.no_workloads:
         others = {}
@@ -580,7 +657,7 @@ def bench_ours(args):
         for _ in range(max(3, args.warmup)):
             pstep()
         psteps = max(args.steps, 20)
-        pms = _time_loop(torch, pstep, psteps)
+        pms = _time_loop(torch, pstep, psteps, flush=False)  # warm, as the pages' ablation
         line["prefill_paged"] = {
             "metric": "paged chunk prefill us per call", "value": pms * 1e3, "unit": "us",
             "higher_is_better": False, "tokens_per_s": pw.T / (pms / 1e3), "steps": psteps,
@@ -591,29 +668,25 @@ def bench_ours(args):
 
     # segment-parallel state scans: one long sequence with few value heads (the case
     # the plain scans leave the GPU idle in), fwd+bwd with the planned split and with
-    # the split turned off (GDN_SCAN_SEGMENT_CHUNKS=0), device-timed
+    # the split turned off (scan_segment_chunks = -1), device-timed
     if not args.no_segscan:
         import chunked_gated_delta_06_gb300 as gdn
         sw = W.chunk_workload("fb_1x65536_hv16", [65536], 8, 16, seed=rank, h0=True, backward=True,
                               d_ht=True)
         seg = {}
-        for label, env in (("split", None), ("plain", "0")):
-            if env is not None:
-                os.environ["GDN_SCAN_SEGMENT_CHUNKS"] = env
-            try:
-                sr = ChunkRunner(torch, sw, dev)
-                _, seg_len, nseg = gdn.gdn_chunk_scan_plan(sr.p)
-                for _ in range(3):
-                    sr.step()
-                sms = _time_loop(torch, sr.step, 5)
-                sper = _kernel_table(torch, sr.step, 3, 32)
-                scan = {k_: statistics.mean(v) * (len(v) // 3) for k_, v in sper.items()
-                        if k_ in ("state", "bstate", "seg_stitch")}
-                seg[label] = {"ms_per_step": sms, "tokens_per_s": sw.T / (sms / 1e3), "seg_len": seg_len,
-                              "segments": nseg, "scan_ms": scan}
-                del sr
-            finally:
-                os.environ.pop("GDN_SCAN_SEGMENT_CHUNKS", None)
+        for label, field in (("split", 0), ("plain", -1)):
+            sr = ChunkRunner(torch, sw, dev, scan_segment_chunks=field)
+            _, seg_len, nseg = gdn.gdn_chunk_scan_plan(sr.p)
+            for _ in range(3):
+                sr.step()
+            sms = _time_loop(torch, sr.step, 5)
+            sper = _kernel_table(torch, sr.step, 3, 32)
+            scan = {k_: statistics.median(v) * (len(v) // 3) for k_, v in sper.items()
+                    if k_ in ("state", "bstate", "seg_stitch")}
+            sr.check_status()
+            seg[label] = {"ms_per_step": sms, "tokens_per_s": sw.T / (sms / 1e3), "seg_len": seg_len,
+                          "segments": nseg, "scan_ms": scan}
+            del sr
         line["segscan"] = {"config": {"workload": "fb_1x65536_hv16", "T": sw.T, "N": 1, "H": sw.H,
                                       "HV": sw.HV, "step": STEP_MODES["saved"]}, **seg}
 
@@ -642,7 +715,7 @@ def bench_ours(args):
         n_active = int((dw.state_indices > 0).sum())
         nb = decode_bytes(n_active, dw.B, dw.H, dw.HV)
         dper = _kernel_table(torch, dstep, 10, 4)
-        kms = statistics.mean(dper["decode"])
+        kms = statistics.median(dper["decode"])
         line["decode"] = {
             "metric": "decode state GB/s", "value": nb / (dms / 1e3) / 1e9, "unit": "GB/s",
             "ms_per_step": dms, "steps": dsteps,
@@ -739,6 +812,7 @@ def bench_ours(args):
         tok, dt, thr, used = run_oracle_sample(wl, args.ref_tokens)
         line["cpu_baseline"] = {
             "value": tok / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "cpu_model": _cpu_model(),
             "sample": "first %d tokens of the workload (whole sequences in packing order), all "
                       "32 value heads, fwd+bwd, %.1f s on %d threads" % (tok, dt, used)}
     if world > 1:

@@ -22,6 +22,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "gdn.h")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE_TOO_SMALL, GDN_ERR_CUDA = range(5)
 GDN_DTYPE_BF16, GDN_DTYPE_F32 = 0, 1
+GDN_DEVICE_CU_SEQLENS_MISMATCH, GDN_DEVICE_WAIT_TIMEOUT, GDN_DEVICE_INDEX_OUT_OF_RANGE = 1, 2, 4
 
 
 class GdnError(RuntimeError):
@@ -52,6 +53,8 @@ class GdnProblem(ctypes.Structure):
         ("beta_dtype", ctypes.c_int32),
         ("cu_seqlens_host", ctypes.POINTER(ctypes.c_int32)),
         ("cu_seqlens_dev", ctypes.c_void_p),
+        ("device_status", ctypes.c_void_p),
+        ("scan_segment_chunks", ctypes.c_int32),
     ]
 
 
@@ -106,6 +109,8 @@ def lib():
             L.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
             L.gdn_check_indices.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, _vp]
             L.gdn_check_indices.restype = ctypes.c_int
+            L.gdn_selftest_bounded_wait.argtypes = [_vp, ctypes.c_uint64, _vp]
+            L.gdn_selftest_bounded_wait.restype = ctypes.c_int
             L.gdn_kernel_name.argtypes = [ctypes.c_int32]
             L.gdn_kernel_name.restype = ctypes.c_char_p
             _lib = L
@@ -155,8 +160,11 @@ class KernelTimer:
 
 
 # ----------------------------------------------------------------------------- raw entry points
-def make_problem(cu_host, H, HV, K=128, V=128, scale=0.0, cu_dev_ptr=0, beta_dtype=GDN_DTYPE_BF16):
-    """Build a GdnProblem; returns (problem, keepalive) -- keep both alive during the call."""
+def make_problem(cu_host, H, HV, K=128, V=128, scale=0.0, cu_dev_ptr=0, beta_dtype=GDN_DTYPE_BF16,
+                 device_status_ptr=0, scan_segment_chunks=0):
+    """Build a GdnProblem; returns (problem, keepalive) -- keep both alive during the call.
+    device_status_ptr: a device int32 the kernels OR GDN_DEVICE_* bits into (0: none);
+    scan_segment_chunks: 0 = the library's scan plan, -1 = never split, L > 0 = force L."""
     cu = np.ascontiguousarray(np.asarray(cu_host, dtype=np.int32))
     p = GdnProblem()
     p.num_seqs = len(cu) - 1
@@ -166,6 +174,8 @@ def make_problem(cu_host, H, HV, K=128, V=128, scale=0.0, cu_dev_ptr=0, beta_dty
     p.beta_dtype = int(beta_dtype)
     p.cu_seqlens_host = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if len(cu) else None
     p.cu_seqlens_dev = cu_dev_ptr or None
+    p.device_status = device_status_ptr or None
+    p.scan_segment_chunks = int(scan_segment_chunks)
     return p, cu
 
 
@@ -250,6 +260,10 @@ def gdn_decode_step(batch, H, HV, K, V, scale, q, k, v, g, beta, state_pool, num
                                      num_slots, state_indices, o, device_status, stream))
 
 
+def gdn_selftest_bounded_wait(device_status, limit_ns, stream) -> int:
+    return int(lib().gdn_selftest_bounded_wait(device_status, int(limit_ns), stream))
+
+
 def gdn_check_indices(state_indices, batch, num_slots, bad_row) -> int:
     return int(lib().gdn_check_indices(state_indices, batch, num_slots, bad_row))
 
@@ -298,22 +312,30 @@ class ChunkContext:
     saved stays None after a forward without for_backward, and the backward then
     runs in recompute-state mode."""
 
-    def __init__(self, cu_host, cu_dev, H, HV, scale, beta_dtype=GDN_DTYPE_BF16):
+    def __init__(self, cu_host, cu_dev, H, HV, scale, beta_dtype=GDN_DTYPE_BF16, device_status=None,
+                 scan_segment_chunks=0):
         self.cu_host = np.ascontiguousarray(np.asarray(cu_host, dtype=np.int32))
         self.cu_dev = cu_dev
         self.H, self.HV, self.scale = H, HV, scale
+        self.device_status = device_status
         self.problem, self._keep = make_problem(self.cu_host, H, HV, scale=scale or 0.0,
-                                                cu_dev_ptr=cu_dev.data_ptr(), beta_dtype=beta_dtype)
+                                                cu_dev_ptr=cu_dev.data_ptr(), beta_dtype=beta_dtype,
+                                                device_status_ptr=_ptr(device_status) or 0,
+                                                scan_segment_chunks=scan_segment_chunks)
         self.saved = None
 
 
 def chunk_fwd(q, k, v, g, beta, cu_host, cu_dev, scale=None, initial_state=None,
-              output_final_state=True, for_backward=False, workspace=None):
-    """gdn_chunk_fwd on torch tensors.  Returns (o, final_state or None, ctx)."""
+              output_final_state=True, for_backward=False, workspace=None, device_status=None,
+              scan_segment_chunks=0):
+    """gdn_chunk_fwd on torch tensors.  Returns (o, final_state or None, ctx).
+    device_status: an int32 device tensor the kernels OR GDN_DEVICE_* bits into (the
+    backward of ctx uses it too); scan_segment_chunks: the problem field of that name."""
     import torch
     T, H, K = q.shape
     HV = v.shape[1]
-    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale, beta_dtype_of(beta))
+    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale, beta_dtype_of(beta), device_status,
+                       scan_segment_chunks)
     p = ctx.problem
     N = p.num_seqs
     dev = q.device

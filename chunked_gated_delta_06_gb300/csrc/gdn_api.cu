@@ -30,6 +30,7 @@ struct Carver {
 
 struct Dims {
     int N, T, H, HV, C;  // C = chunk count
+    int longest;         // chunks of the longest sequence
     float scale;
     int beta_f32;        // beta / dbeta are fp32 (else bf16); fused-gating calls need bf16
     int seg_len, seg_max;  // segment-parallel forward scan (seg_len 0: not split)
@@ -46,7 +47,7 @@ struct Dims {
 // segment plus three steps for the extra launches.  The plan is a pure function of
 // the problem (the same bits on every device): a split is taken only when the model
 // gains at least 20 % and its buffers stay under 1 GiB.
-// GDN_SCAN_SEGMENT_CHUNKS in the environment overrides the model: 0 never splits, L > 0
+// The problem's scan_segment_chunks overrides the model: -1 never splits, L > 0
 // cuts every sequence into segments of L chunks whenever that gives 3 or more.
 void plan_segments(const gdn_problem *p, Dims *d) {
     d->seg_len = 0;
@@ -61,10 +62,11 @@ void plan_segments(const gdn_problem *p, Dims *d) {
         longest = c > longest ? c : longest;
         total += c;
     }
-    if (const char *ov = getenv("GDN_SCAN_SEGMENT_CHUNKS")) {
-        const int L = atoi(ov);
-        const int smax = L > 0 ? (longest + L - 1) / L : 0;
-        if (L > 0 && smax >= 3 && smax <= 4096) {
+    if (p->scan_segment_chunks < 0) return;
+    if (p->scan_segment_chunks > 0) {
+        const int L = p->scan_segment_chunks;
+        const int smax = (longest + L - 1) / L;
+        if (smax >= 3 && smax <= 4096) {
             d->seg_len = L;
             d->seg_max = smax;
         }
@@ -115,14 +117,19 @@ gdn_status check_problem(const gdn_problem *p, Dims *d) {
     if (p->head_dim_k != 128 || p->head_dim_v != 128) return GDN_ERR_UNSUPPORTED;
     if (p->num_v_heads % p->num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
     if (p->beta_dtype != GDN_DTYPE_BF16 && p->beta_dtype != GDN_DTYPE_F32) return GDN_ERR_INVALID_ARG;
+    if (p->scan_segment_chunks < -1) return GDN_ERR_INVALID_ARG;
+    if (!aligned_to(p->device_status, 4)) return GDN_ERR_INVALID_ARG;
     if (!p->cu_seqlens_host || !p->cu_seqlens_dev) return GDN_ERR_INVALID_ARG;
     const int32_t *cu = p->cu_seqlens_host;
     if (cu[0] != 0 || (int64_t)cu[p->num_seqs] != p->total_tokens) return GDN_ERR_INVALID_ARG;
-    int64_t chunks = 0;
+    int64_t chunks = 0, longest = 0;
     for (int n = 0; n < p->num_seqs; ++n) {
         if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARG;
-        chunks += ((int64_t)cu[n + 1] - cu[n] + gdn::kChunk - 1) / gdn::kChunk;
+        const int64_t c = ((int64_t)cu[n + 1] - cu[n] + gdn::kChunk - 1) / gdn::kChunk;
+        chunks += c;
+        longest = c > longest ? c : longest;
     }
+    d->longest = (int)longest;
     d->N = p->num_seqs;
     d->T = (int)p->total_tokens;
     d->H = p->num_k_heads;
@@ -148,11 +155,9 @@ void carve_saved(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
 
 void carve_table(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.seq_chunk_off = cv.take<int>((size_t)d.N + 1);
-    a.chunk_seq = cv.take<int>((size_t)d.C);
     a.chunk_start = cv.take<int>((size_t)d.C);
     a.chunk_len = cv.take<int>((size_t)d.C);
     a.seq_order = cv.take<int>((size_t)d.N);
-    a.status = cv.take<int>(1);
 }
 
 // Segment buffers of a split forward scan (none when the scan is not split).
@@ -218,6 +223,7 @@ void fill_common(gdn::ChunkArgs &a, const Dims &d, const gdn_problem *p, const v
     a.H = d.H;
     a.HV = d.HV;
     a.num_chunks = d.C;
+    a.max_seq_chunks = d.longest;
     a.scale = d.scale;
     a.q = static_cast<const bf16 *>(q);
     a.k = static_cast<const bf16 *>(k);
@@ -227,6 +233,7 @@ void fill_common(gdn::ChunkArgs &a, const Dims &d, const gdn_problem *p, const v
     a.beta_mode = d.beta_f32 ? 1 : 0;
     a.h0 = h0;
     a.cu_dev = p->cu_seqlens_dev;
+    a.status = p->device_status;
 }
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }

@@ -439,8 +439,8 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving
-        if (a_issued > waited) mbar_wait(&sm.a_bar, (a_issued - 1) & 1, 1u << 20);
-        if (v_issued > waited) mbar_wait(&sm.v_bar, (v_issued - 1) & 1, 1u << 20);
+        if (a_issued > waited) mbar_wait(&sm.a_bar, (a_issued - 1) & 1, kDrainLimitNs);
+        if (v_issued > waited) mbar_wait(&sm.v_bar, (v_issued - 1) & 1, kDrainLimitNs);
     }
     tc_fence_before();
     __syncthreads();

@@ -460,9 +460,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving
-        if (a_issued > a_waited) mbar_wait(&sm.a_bar, a_waited & 1, 1u << 20);
+        if (a_issued > a_waited) mbar_wait(&sm.a_bar, a_waited & 1, kDrainLimitNs);
         for (int bf = 0; bf < 2; ++bf)
-            if ((bpend >> bf) & 1) mbar_wait(&sm.b_bar[bf], (bpar >> bf) & 1, 1u << 20);
+            if ((bpend >> bf) & 1) mbar_wait(&sm.b_bar[bf], (bpar >> bf) & 1, kDrainLimitNs);
     }
     if (tid == 0) tma_store_wait_all();
     tc_fence_before();

@@ -380,9 +380,9 @@ __global__ void __launch_bounds__(kThr, 2)
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving
-        if (xk_issued > 0) mbar_wait(&sm.xk_bar, (xk_issued - 1) & 1, 1u << 20);
-        if (xd_issued > 0) mbar_wait(&sm.xd_bar, (xd_issued - 1) & 1, 1u << 20);
-        if (y_issued > 0) mbar_wait(&sm.y_bar, (y_issued - 1) & 1, 1u << 20);
+        if (xk_issued > 0) mbar_wait(&sm.xk_bar, (xk_issued - 1) & 1, kDrainLimitNs);
+        if (xd_issued > 0) mbar_wait(&sm.xd_bar, (xd_issued - 1) & 1, kDrainLimitNs);
+        if (y_issued > 0) mbar_wait(&sm.y_bar, (y_issued - 1) & 1, kDrainLimitNs);
     }
     tc_fence_before();
     __syncthreads();

@@ -21,17 +21,28 @@ namespace {
 constexpr int kThreads = 256;
 
 // ---------------------------------------------------------------------------
-// Chunk table from the device cu_seqlens (one block).  Host code computed the
-// chunk count from the host copy; a mismatch sets *status.
-__global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunks, int *seq_off,
-                       int *chunk_seq, int *chunk_start, int *chunk_len, int *seq_order,
-                       int *status) {
+// Chunk table from the device cu_seqlens (one block).  The host sized every buffer
+// from its own copy of cu_seqlens (total_chunks chunks, at most max_seq_chunks in one
+// sequence, T tokens).  The device copy is accepted only when it fits those extents:
+// cu[0] = 0, cu[N] = T, non-decreasing, total_chunks chunks in all and no sequence
+// longer than max_seq_chunks.  Otherwise bit 1 is ORed into the caller's status word
+// (when there is one) and the table written is empty (every sequence without chunks,
+// every chunk of length 0), which every kernel turns into no work, so a bad device
+// copy never leads to an access outside the buffers.
+__global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunks, int max_seq_chunks,
+                       int *seq_off, int *chunk_start, int *chunk_len, int *seq_order, int *status) {
     __shared__ int sums[1024];
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (N + nt - 1) / nt;
     const int b = min(N, tid * per), e = min(N, b + per);
     int cnt = 0;
-    for (int n = b; n < e; ++n) cnt += (max(cu[n + 1] - cu[n], 0) + kChunk - 1) / kChunk;
+    bool bad = tid == 0 && (cu[0] != 0 || cu[N] != T);
+    for (int n = b; n < e; ++n) {
+        const int L = cu[n + 1] - cu[n];
+        const int ch = (max(L, 0) + kChunk - 1) / kChunk;
+        bad = bad || L < 0 || ch > max_seq_chunks;
+        cnt += ch;
+    }
     sums[tid] = cnt;
     __syncthreads();
     for (int off = 1; off < nt; off <<= 1) {
@@ -40,40 +51,39 @@ __global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunk
         sums[tid] += x;
         __syncthreads();
     }
+    bad = __syncthreads_or(bad || sums[nt - 1] != total_chunks);
+    if (bad) {
+        if (tid == 0 && status) atomicOr(status, 1);
+        for (int c = tid; c < total_chunks; c += nt) {
+            chunk_start[c] = 0;
+            chunk_len[c] = 0;
+        }
+        for (int n = tid; n <= N; n += nt) seq_off[n] = 0;
+        for (int n = tid; n < N; n += nt) seq_order[n] = n;
+        return;
+    }
+    // the table: chunk c of sequence n starts at cu[n] + 64 j (consecutive 64-token
+    // blocks inside [0, T), the last one partial)
     int base = sums[tid] - cnt;
     for (int n = b; n < e; ++n) {
         seq_off[n] = base;
-        int L = max(cu[n + 1] - cu[n], 0);
+        const int L = cu[n + 1] - cu[n];
         for (int j = 0; j * kChunk < L; ++j) {
-            int c = base + j;
-            if (c < total_chunks) {
-                // clamp to [0, T): a device copy of cu_seqlens that disagrees with
-                // the host copy yields empty chunks and a status flag, never an
-                // out-of-bounds access
-                const int st = min(max(cu[n] + j * kChunk, 0), T);
-                chunk_seq[c] = n;
-                chunk_start[c] = st;
-                chunk_len[c] = max(0, min(min(kChunk, L - j * kChunk), T - st));
-            }
+            chunk_start[base + j] = cu[n] + j * kChunk;
+            chunk_len[base + j] = min(kChunk, L - j * kChunk);
         }
         base += (L + kChunk - 1) / kChunk;
     }
-    __syncthreads();
-    if (tid == nt - 1) {
-        seq_off[N] = min(sums[tid], total_chunks);
-        if (status) *status = (sums[tid] != total_chunks || cu[N] != T) ? 1 : 0;
-    }
-    // keep every sequence's chunk range inside [0, total_chunks]
-    for (int n = b; n < e; ++n) seq_off[n] = min(seq_off[n], total_chunks);
+    if (tid == nt - 1) seq_off[N] = total_chunks;
     // longest sequences first (ties by index), so the scans start the longest
     // chunk chains first; identity order beyond 4096 sequences
     for (int n = b; n < e; ++n) {
         int rank = n;
         if (N <= 4096) {
-            const int Ln = max(cu[n + 1] - cu[n], 0);
+            const int Ln = cu[n + 1] - cu[n];
             rank = 0;
             for (int m = 0; m < N; ++m) {
-                const int Lm = max(cu[m + 1] - cu[m], 0);
+                const int Lm = cu[m + 1] - cu[m];
                 rank += (Lm > Ln || (Lm == Ln && m < n)) ? 1 : 0;
             }
         }
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
 
 cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s) {
     TimerScope ts(a.timer, GDN_KERNEL_PLAN, s);
-    k_plan<<<1, 1024, 0, s>>>(a.cu_dev, a.N, a.T, a.num_chunks, a.seq_chunk_off, a.chunk_seq,
+    k_plan<<<1, 1024, 0, s>>>(a.cu_dev, a.N, a.T, a.num_chunks, a.max_seq_chunks, a.seq_chunk_off,
                               a.chunk_start, a.chunk_len, a.seq_order, a.status);
     return cudaGetLastError();
 }

@@ -35,12 +35,5 @@ __device__ __forceinline__ float gate_softplus_slope(float x) {
 }
 __device__ __forceinline__ float gate_sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
 
-// Chunk table built on the device from cu_seqlens (see k_plan).
-struct ChunkTable {
-    const int *seq_chunk_off;  // [N+1] first chunk of each sequence
-    const int *chunk_seq;      // [C_total] sequence of each chunk
-    const int *chunk_start;    // [C_total] first token (packed index)
-    const int *chunk_len;      // [C_total] 1..64
-};
 
 }  // namespace gdn

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
     }
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
-        if (issued > waited) mbar_wait(&sm.ld_bar, (issued - 1) & 1, 1u << 20);  // drain (bounded)
+        if (issued > waited) mbar_wait(&sm.ld_bar, (issued - 1) & 1, kDrainLimitNs);  // drain (bounded)
     }
     tc_fence_before();
     __syncthreads();

@@ -42,9 +42,11 @@ struct ChunkArgs {
     float *rq, *rk;         // [T,H] sqrt(|x|^2 + eps)
     float *G;               // [T,HV] chunk-local cumulative log decay
     // chunk table (device, rebuilt by every call)
-    int *seq_chunk_off, *chunk_seq, *chunk_start, *chunk_len;
+    int *seq_chunk_off, *chunk_start, *chunk_len;
+    int max_seq_chunks;     // chunks of the longest sequence (host copy of cu_seqlens)
     int *seq_order;         // [N] sequences by decreasing length (scans start the longest first)
-    int *status;            // device int, nonzero = inconsistent device cu_seqlens
+    int *status;            // the caller's device status word or null: bit 1 = inconsistent
+                            // device cu_seqlens, bit 2 = a bounded wait ran out
     // segment-parallel forward state scan (seg_len = 0: one piece per sequence)
     int seg_len;            // chunks per segment
     int seg_max;            // largest segment count of any sequence (>= 3 when seg_len > 0)

@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
     }
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
-        if (issued > waited) mbar_wait(&sm.tma_bar, (issued - 1) & 1, 1u << 20);  // drain (bounded)
+        if (issued > waited) mbar_wait(&sm.tma_bar, (issued - 1) & 1, kDrainLimitNs);  // drain (bounded)
     }
     if (tid == 0) tma_store_wait_all();
     tc_fence_before();

@@ -335,8 +335,8 @@ __global__ void __launch_bounds__(kThr, 2)
     if (!ok && tid == 0) {
         // drain outstanding TMA copies (bounded) before leaving
         if (a.status) atomicOr(a.status, 2);
-        mbar_wait(&sm.tma_bar[0], 0, 1u << 20);
-        mbar_wait(&sm.tma_bar[1], 0, 1u << 20);
+        mbar_wait(&sm.tma_bar[0], 0, kDrainLimitNs);
+        mbar_wait(&sm.tma_bar[1], 0, kDrainLimitNs);
     }
     tc_fence_before();
     __syncthreads();

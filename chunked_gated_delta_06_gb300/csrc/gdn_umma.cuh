@@ -51,12 +51,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: false after `limit` polls (the caller records an error and
-// unwinds instead of hanging).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = 1u << 26) {
-    for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+// Nanoseconds since an arbitrary origin (the GPU's global timer).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Time limits of the bounded waits: a wait for an MMA or a TMA copy takes
+// microseconds, so one that has not finished after a second never will; the
+// drains on the error path (copies already in flight) get a tenth of that.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+// Bounded wait: false once `limit_ns` nanoseconds have passed without the phase
+// completing (the caller records an error and unwinds instead of hanging).  The
+// timer is read only after the first poll fails.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
 }
 
 // ---------------------------------------------------------------- fences

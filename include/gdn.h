@@ -83,7 +83,35 @@ typedef struct {
                                          other value is GDN_ERR_INVALID_ARG */
     const int32_t *cu_seqlens_host;   /* host [N+1]: 0 = c0 <= c1 <= ... <= cN = T */
     const int32_t *cu_seqlens_dev;    /* device [N+1], the same values */
+    int32_t *device_status;           /* device int32, or NULL: the chunk calls OR
+                                         GDN_DEVICE_* bits into it when a kernel
+                                         finds something wrong (see below); the
+                                         library never clears it */
+    int32_t scan_segment_chunks;      /* plan of the state scans (see
+                                         gdn_chunk_scan_plan): 0 (the default of a
+                                         zeroed struct) = the library's plan, -1 =
+                                         never split, L > 0 = segments of L chunks;
+                                         other values are GDN_ERR_INVALID_ARG */
 } gdn_problem;
+
+/* Bits of gdn_problem.device_status ("[Cake 1/13] gdn: chunked gated delta rule,
+ * det and fast, with KCP and FLA-CP", API and flags: failures are reported, not
+ * silent).  The word is written by the kernels, so it is valid once the call's
+ * work on `stream` has finished; a set bit means the outputs of that call are
+ * not to be trusted.
+ *   GDN_DEVICE_CU_SEQLENS_MISMATCH  cu_seqlens_dev disagrees with the host copy
+ *                                   (the chunk table is clamped to the host's
+ *                                   extents, so no access leaves the buffers)
+ *   GDN_DEVICE_WAIT_TIMEOUT         a bounded wait for a tensor-core product or
+ *                                   a TMA copy ran out (one second); the kernel
+ *                                   drained its copies, freed its tensor memory
+ *                                   and returned early
+ *   GDN_DEVICE_INDEX_OUT_OF_RANGE   (builds with GDN_CHECKED only) a global
+ *                                   index fell outside its buffer; the access
+ *                                   was skipped */
+#define GDN_DEVICE_CU_SEQLENS_MISMATCH 1
+#define GDN_DEVICE_WAIT_TIMEOUT 2
+#define GDN_DEVICE_INDEX_OUT_OF_RANGE 4
 
 /* Bytes of the `saved` buffer gdn_chunk_fwd fills for gdn_chunk_bwd (per-chunk
  * states in bf16, the WY matrices, v_new and the norm / gate prefix sums).
@@ -109,10 +137,10 @@ size_t gdn_chunk_workspace_bytes(const gdn_problem *p, int for_backward);
  * trainer on 128 v7x").  *seg_len = 0 and *num_segments = 1 when the scan is
  * not split; otherwise *num_segments is the largest segment count of any
  * sequence.  The split changes the rounding of the states (not their values
- * beyond it) and adds its buffers to both workspace queries.  The environment
- * variable GDN_SCAN_SEGMENT_CHUNKS, read by every host call, overrides the
- * plan: 0 never splits, L > 0 cuts every sequence into segments of L chunks
- * whenever some sequence then has 3 or more. */
+ * beyond it) and adds its buffers to both workspace queries.  The problem's
+ * scan_segment_chunks field overrides the plan: -1 never splits, L > 0 cuts
+ * every sequence into segments of L chunks whenever some sequence then has 3 or
+ * more (and the segment count stays within 4096). */
 gdn_status gdn_chunk_scan_plan(const gdn_problem *p, int32_t *seg_len, int32_t *num_segments);
 
 /* Forward of chunk_gated_delta_rule.
@@ -337,6 +365,17 @@ gdn_status gdn_decode_step_timed(int32_t batch, int32_t num_k_heads, int32_t num
                                  const float *beta, float *state_pool, int32_t num_slots,
                                  const int32_t *state_indices, void *o, int32_t *device_status,
                                  gdn_stream_t stream, gdn_kernel_timer *timer);
+
+/* Diagnostic: runs one kernel that waits, with the same bounded mbarrier wait
+ * the chunk kernels use, on a barrier that nothing ever arrives on.  After
+ * limit_ns nanoseconds (1e3 .. 1e9) the wait gives up and the kernel ORs
+ * GDN_DEVICE_WAIT_TIMEOUT into *device_status (device int32, required), as a
+ * chunk kernel does when one of its waits runs out; the context stays usable.
+ * Returns GDN_ERR_INVALID_ARG for a NULL or misaligned word or a limit outside
+ * the range.  The pages have no counterpart: it exists so that the failure path
+ * of the bounded waits can be tested without faulting or hanging a GPU. */
+gdn_status gdn_selftest_bounded_wait(int32_t *device_status, uint64_t limit_ns,
+                                     gdn_stream_t stream);
 
 /* A static, human-readable name of a status code. */
 const char *gdn_status_string(gdn_status s);

@@ -42,27 +42,32 @@ def to_dev(wl, torch):
     return d
 
 
-def run_chunk(wl, torch, backward=None, recompute=False):
+def run_chunk(wl, torch, backward=None, recompute=False, scan_segment_chunks=0):
     """Run gdn_chunk_fwd (+ gdn_chunk_bwd) on a workload; returns numpy float64 results."""
-    out = run_chunk_raw(wl, torch, backward=backward, recompute=recompute)
+    out = run_chunk_raw(wl, torch, backward=backward, recompute=recompute,
+                        scan_segment_chunks=scan_segment_chunks)
     return {k_: (None if v_ is None else v_.float().cpu().numpy().astype(np.float64))
             for k_, v_ in out.items()}
 
 
-def run_chunk_raw(wl, torch, backward=None, recompute=False):
+def run_chunk_raw(wl, torch, backward=None, recompute=False, scan_segment_chunks=0):
     """Like run_chunk but returns the device tensors (for bitwise comparisons).
-    recompute: the forward keeps no saved buffer and the backward rebuilds it."""
+    recompute: the forward keeps no saved buffer and the backward rebuilds it.
+    Every call passes a device status word and asserts that the kernels left it 0."""
     import chunked_gated_delta_06_gb300 as gdn
     backward = wl.backward if backward is None else backward
     d = to_dev(wl, torch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, ht, ctx = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], wl.cu_seqlens, d["cu_dev"],
                                initial_state=d["h0"], output_final_state=True,
-                               for_backward=backward and not recompute)
+                               for_backward=backward and not recompute, device_status=status,
+                               scan_segment_chunks=scan_segment_chunks)
     out = dict(o=o, ht=ht)
     if backward:
         out.update(gdn.chunk_bwd(ctx, d["q"], d["k"], d["v"], d["g"], d["beta"], d["d_o"],
                                  d_final_state=d["d_ht"], initial_state=d["h0"]))
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %d after a valid call" % int(status.item())
     return out
 
 

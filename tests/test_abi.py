@@ -137,7 +137,10 @@ def test_problem_struct_layout_matches_the_header(lib):
     assert P.scale.offset == 32
     assert P.beta_dtype.offset == 36
     assert P.cu_seqlens_host.offset == 40
-    assert ctypes.sizeof(P) == 56
+    assert P.cu_seqlens_dev.offset == 48
+    assert P.device_status.offset == 56
+    assert P.scan_segment_chunks.offset == 64
+    assert ctypes.sizeof(P) == 72
 
 
 def test_gated_calls_check_their_arguments_before_any_launch(lib):

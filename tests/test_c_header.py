@@ -13,6 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PKG = os.path.join(ROOT, "chunked_gated_delta_06_gb300")
 
 PROGRAM = textwrap.dedent(r"""
+    #include <stddef.h>
     #include <stdio.h>
     #include <string.h>
     #include "gdn.h"
@@ -36,7 +37,16 @@ PROGRAM = textwrap.dedent(r"""
             != GDN_ERR_INVALID_ARG) return 5;
         p.head_dim_v = 64;
         if (gdn_chunk_saved_bytes(&p) != 0) return 6;
-        printf("ok %zu\n", sizeof(gdn_problem));
+        /* a zeroed struct is the library's plan; -1 never splits; -2 is rejected */
+        p.head_dim_v = 128;
+        p.scan_segment_chunks = -2;
+        if (gdn_chunk_scan_plan(&p, &seg_len, &nseg) != GDN_ERR_INVALID_ARG) return 7;
+        p.scan_segment_chunks = -1;
+        if (gdn_chunk_scan_plan(&p, &seg_len, &nseg) != GDN_OK || seg_len != 0) return 8;
+        p.device_status = (int32_t *)(uintptr_t)0x1002;   /* misaligned: rejected */
+        if (gdn_chunk_workspace_bytes(&p, 0) != 0) return 9;
+        printf("ok %zu %zu %zu\n", sizeof(gdn_problem), offsetof(gdn_problem, device_status),
+               offsetof(gdn_problem, scan_segment_chunks));
         return 0;
     }
 """)
@@ -55,4 +65,5 @@ def test_header_compiles_as_c99_and_host_calls_work(tmp_path):
                     str(src), "-L", PKG, "-lgdn", "-Wl,-rpath," + PKG, "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, (out.returncode, out.stdout, out.stderr)
-    assert out.stdout.strip() == "ok 56"
+    # the same layout the ctypes binding declares
+    assert out.stdout.strip() == "ok 72 56 64"

@@ -97,10 +97,12 @@ def test_fb_32k_varlen_sampled_units():
     _sampled(wl, seqs=seqs, key_heads=[7])
 
 
-def test_fb_65536_long_sampled_unit():
+def test_fb_65536_long_sampled_key_head():
     wl = W.fb_65536_long()
-    # one value head of the single long sequence: o, final state, dv, dg, dbeta, dh0
-    _sampled(wl, seqs=[0], value_heads=[37], skip=("dqdk",))
+    # all four value heads (36 .. 39) of key head 9 of the single 65536-token sequence:
+    # o, final state, dv, dg, dbeta, dh0 per value head, and dq, dk of the key head
+    # (its sum over the four value heads) over all 1024 chunks
+    _sampled(wl, seqs=[0], key_heads=[9])
 
 
 def test_fb_32k_varlen_repeats_bit_for_bit():

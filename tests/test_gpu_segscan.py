@@ -26,8 +26,9 @@ def _built():
     build.build()
 
 
-def _plan(wl):
-    p, keep = binding.make_problem(wl.cu_seqlens, wl.H, wl.HV, cu_dev_ptr=0x1000)
+def _plan(wl, scan_segment_chunks=0):
+    p, keep = binding.make_problem(wl.cu_seqlens, wl.H, wl.HV, cu_dev_ptr=0x1000,
+                                   scan_segment_chunks=scan_segment_chunks)
     st, seg_len, nseg = gdn_pkg.gdn_chunk_scan_plan(p)
     assert st == 0
     return seg_len, nseg
@@ -81,12 +82,13 @@ def test_split_paged_prefill_matches_the_oracle():
     close("pool", pool.cpu().numpy()[[1, 3]], pool_ref[[1, 3]])
 
 
-def test_split_and_plain_scans_agree(monkeypatch):
+def test_split_and_plain_scans_agree():
+    # the split is driven through the ABI: scan_segment_chunks = -1 never splits
     wl = W.chunk_workload("seg_vs_plain", [8192, 700], 2, 4, seed=46, h0=True, backward=True,
                           d_ht=True)
+    assert _plan(wl)[0] > 0
     split = run_chunk(wl, torch)
-    monkeypatch.setenv("GDN_SCAN_SEGMENT_CHUNKS", "0")
-    assert _plan(wl) == (0, 1)
-    plain = run_chunk(wl, torch)
+    assert _plan(wl, scan_segment_chunks=-1) == (0, 1)
+    plain = run_chunk(wl, torch, scan_segment_chunks=-1)
     for key in ("o", "ht", "dq", "dk", "dv", "dg", "dbeta", "dh0"):
         close(key, split[key], plain[key])

@@ -7,10 +7,10 @@ import chunked_gated_delta_06_gb300 as gdn
 from chunked_gated_delta_06_gb300 import binding, build, workloads as W
 
 
-def _plan(lengths, H, HV):
+def _plan(lengths, H, HV, scan_segment_chunks=0):
     build.build()
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
-    p, keep = binding.make_problem(cu, H, HV, cu_dev_ptr=0x1000)
+    p, keep = binding.make_problem(cu, H, HV, cu_dev_ptr=0x1000, scan_segment_chunks=scan_segment_chunks)
     st, seg_len, nseg = gdn.gdn_chunk_scan_plan(p)
     assert st == binding.GDN_OK
     return seg_len, nseg, gdn.gdn_chunk_workspace_bytes(p, 0)
@@ -55,11 +55,22 @@ def test_the_plan_query_rejects_an_invalid_problem():
     assert st == binding.GDN_ERR_INVALID_ARG
 
 
-def test_the_environment_overrides_the_plan(monkeypatch):
+def test_the_problem_field_overrides_the_plan():
+    assert _plan([8192], 2, 4, scan_segment_chunks=-1)[:2] == (0, 1)
+    assert _plan([8192], 2, 4, scan_segment_chunks=16)[:2] == (16, 8)
+    assert _plan(W.varlen_lengths(0, 32768, 1, 8192), 16, 32, scan_segment_chunks=16)[0] == 16
+    assert _plan([8192], 2, 4, scan_segment_chunks=64)[:2] == (0, 1)  # two segments: nothing to gain
+
+
+def test_the_environment_no_longer_changes_the_plan(monkeypatch):
+    # the plan (and so the bits) depends on the call's arguments only
+    before = _plan([8192], 2, 4)
     monkeypatch.setenv("GDN_SCAN_SEGMENT_CHUNKS", "0")
-    assert _plan([8192], 2, 4)[:2] == (0, 1)
-    monkeypatch.setenv("GDN_SCAN_SEGMENT_CHUNKS", "16")
-    assert _plan([8192], 2, 4)[:2] == (16, 8)
-    assert _plan(W.varlen_lengths(0, 32768, 1, 8192), 16, 32)[0] == 16
-    monkeypatch.setenv("GDN_SCAN_SEGMENT_CHUNKS", "64")
-    assert _plan([8192], 2, 4)[:2] == (0, 1)  # two segments: nothing to gain
+    assert _plan([8192], 2, 4) == before
+
+
+def test_an_invalid_scan_field_is_rejected():
+    cu = np.array([0, 8192], dtype=np.int32)
+    p, keep = binding.make_problem(cu, 2, 4, cu_dev_ptr=0x1000, scan_segment_chunks=-2)
+    assert gdn.gdn_chunk_scan_plan(p)[0] == binding.GDN_ERR_INVALID_ARG
+    assert gdn.gdn_chunk_workspace_bytes(p, 0) == 0

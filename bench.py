@@ -71,9 +71,10 @@ def kernel_work(name, T, H, HV, N, C_total):
         out=T * H * D * bf * 2 + TV * D * bf * 2 + C_total * HV * D * D * bf,
         dvloc=T * H * D * bf * 2 + TV * D * bf * 2,
         bstate=T * H * D * bf * 2 + TV * D * bf * 4 + C_total * HV * D * D * bf,
-        bintra_a=T * H * D * bf * 2 + TV * D * bf * 6 + TV * 4 + C_total * HV * D * D * bf * 2,
-        bintra_b=T * H * D * bf + TV * D * bf * 5 + TV * 12 + C_total * HV * C * C * 2,
-        bnorm=TV * D * bf * 3 + T * H * D * bf * 4,
+        # q, k; dO, dv_new, v_new in and dW out; dG; h_c, dh_c; dq and the summed dkhat out
+        bintra_a=T * H * D * bf * 4 + TV * D * bf * 4 + TV * 4 + C_total * HV * D * D * bf * 2,
+        # k; v, dW, dv_new in and dv out; beta, G, dG, dg / dbeta; T; summed dkhat in, dk out
+        bintra_b=T * H * D * bf * 3 + TV * D * bf * 4 + TV * 12 + C_total * HV * C * C * 2,
     ).get(name, 0.0)
     return f, b
 
@@ -112,7 +113,7 @@ KERNEL_SOURCE = {
     "intra": "gdn_intra_tc.cu", "state": "gdn_state_tc.cu", "out": "gdn_out_tc.cu",
     "dvloc": "gdn_out_tc.cu", "bstate": "gdn_bstate_tc.cu", "bintra_a": "gdn_bintra_tc.cu",
     "bintra_b": "gdn_bintra_b_tc.cu", "decode": "gdn_decode.cu", "prep": "gdn_chunk.cu",
-    "bnorm": "gdn_chunk.cu", "plan": "gdn_chunk.cu",
+    "plan": "gdn_chunk.cu",
 }
 
 

@@ -21,8 +21,12 @@
 //   dbeta_m = sum_j P2_mj + e^{G_m}/r_k,m sum_i T_im D1_im + sum_i T_im D2_im
 //   dG_m   += beta_m sum_j P2_mj - sum_i beta_i P2_im + beta_m e^{G_m}/r_k,m sum_i T_im D1_im
 // and dg is the reverse cumulative sum of dG (which arrives holding the h / dh'
-// and Q K^T terms).  The dkhat terms go to their own buffer; the head-sum kernel
-// adds them to the rest and applies the L2-norm backward.
+// and Q K^T terms).  A CTA walks whole groups of the r = HV / H value heads of one
+// key head and sums their dkhat terms in registers (fp32, value heads in order);
+// after the group's last value head it adds the key head's h / dh' and Q K^T terms
+// (summed the same way by the previous kernel) and writes dk with the L2-norm
+// backward applied, dk = (dkhat - khat (khat . dkhat)) / r_k, the row dot taken
+// over the 128 features by lane butterflies and a fixed-order sum of four warps.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -59,6 +63,8 @@ struct BwSmem {
     float G[64], beta[64], rki[64], eg[64], dG[64], db[64];
     float rs[2][64];               // per-warpgroup partial row sums of P2
     float cy[4][64], cz[4][64], cp[4][64];  // per-row-block column sums
+    float dotp[2][4][32];          // khat . dkhat of token 32 grp + l over the d of warp (grp, sub)
+    float dot[64];                 // k . dkhat per token (all 128 features)
     uint64_t a_bar, v_bar, mma_bar;
     uint32_t tmem_base;
 };
@@ -164,6 +170,9 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     const uint32_t t_row = tb + ((uint32_t)(sub * 32) << 16);
     uint32_t phase = 0;
     bool ok = true;
+    // the key head's dkhat sums over its value heads: feature d = 32 sub + lane of
+    // tokens 32 grp .. 32 grp + 31
+    float acc_dk[32];
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int c = x.c, hv = x.hv, t0 = x.t0, L = x.L;
@@ -356,9 +365,13 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         commit_wait(ok);
         if (tid == 0 && ok && has_next) issue_a(maps, sm, a, nx);  // K, dW, dv_new, T read by phase 2
         if (ok && has_next) ++a_issued;
+        const int r = a.HV / a.H;
+        const bool first = hv % r == 0, last = hv % r == r - 1;  // of the key head's value heads
         if (ok) {  // thread d holds element d of the token rows m in [32 grp, 32 grp + 32);
                    // lanes 2i and 2i + 1 swap halves so that each stores bf16 pairs (d even,
-                   // d + 1) of alternate tokens: even lanes tokens 2j, odd lanes 2j + 1
+                   // d + 1) of alternate tokens: even lanes tokens 2j, odd lanes 2j + 1.
+                   // The dkhat terms are added to the key head's sums (fp32, value heads
+                   // in order); dv is this value head's own.
             const int d = sub * 32 + lane, odd = lane & 1;
             const size_t ts = (size_t)a.HV * kDim;
             const size_t base = ((size_t)t0 * a.HV + hv) * kDim + (d & ~1) + (size_t)odd * ts;
@@ -376,12 +389,12 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                     const float b0 = sm.beta[me], b1 = sm.beta[me + 1];
                     const float k0 = dk[2 * jj] + b0 * sm.eg[me] * wt[2 * jj];
                     const float k1 = dk[2 * jj + 1] + b1 * sm.eg[me + 1] * wt[2 * jj + 1];
+                    acc_dk[16 * hh + 2 * jj] = (first ? 0.f : acc_dk[16 * hh + 2 * jj]) + k0;
+                    acc_dk[16 * hh + 2 * jj + 1] = (first ? 0.f : acc_dk[16 * hh + 2 * jj + 1]) + k1;
                     const float v0 = b0 * ut[2 * jj], v1 = b1 * ut[2 * jj + 1];
-                    const float rk = __shfl_xor_sync(0xffffffffu, odd ? k0 : k1, 1);
                     const float rv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
                     if (me + odd < L) {
                         const size_t o = base + (size_t)me * ts;
-                        *reinterpret_cast<uint32_t *>(a.dkp2 + o) = odd ? pack_bf2(rk, k1) : pack_bf2(k0, rk);
                         *reinterpret_cast<uint32_t *>(a.dv + o) = odd ? pack_bf2(rv, v1) : pack_bf2(v0, rv);
                     }
                 }
@@ -390,6 +403,42 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             atomicOr(a.status, 2);
         }
         __syncthreads();
+        if (ok && last) {  // the key head's dk: its dkhat (these sums plus the h / dh' and
+                           // Q K^T terms the previous kernel summed), then the L2-norm
+                           // backward dk = (dkhat - khat (khat . dkhat)) / r_k
+            const int d = sub * 32 + lane, odd = lane & 1;
+            const size_t hs = (size_t)a.H * kDim;
+            const size_t pbase = ((size_t)t0 * a.H + x.h) * kDim + d;
+            const unsigned char *kcol = sm.k + (d >> 6) * kHalf;
+            float kv[32];
+    #pragma unroll
+            for (int i = 0; i < 32; ++i) {  // dkhat and k of token j0 + i, feature d
+                const int m = j0 + i;
+                acc_dk[i] += m < L ? bf2f(a.dkpart[pbase + (size_t)m * hs]) : 0.f;
+                kv[i] = bf2f(*reinterpret_cast<const bf16 *>(kcol + sw128_off(m, d & 63)));
+            }
+            float prod[32];
+    #pragma unroll
+            for (int i = 0; i < 32; ++i) prod[i] = kv[i] * acc_dk[i];
+            sm.dotp[grp][sub][lane] = epi::lanesum32(prod, lane);  // token j0 + lane, this warp's d
+            __syncthreads();
+            if (tid < 64)
+                sm.dot[tid] = ((sm.dotp[tid >> 5][0][tid & 31] + sm.dotp[tid >> 5][1][tid & 31]) +
+                               sm.dotp[tid >> 5][2][tid & 31]) + sm.dotp[tid >> 5][3][tid & 31];
+            __syncthreads();
+            const size_t obase = ((size_t)t0 * a.H + x.h) * kDim + (d & ~1) + (size_t)odd * hs;
+    #pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int i0 = 2 * jj, me = j0 + i0;
+                const float r0 = sm.rki[me], r1 = sm.rki[me + 1];
+                const float k0 = r0 * (acc_dk[i0] - kv[i0] * (r0 * r0 * sm.dot[me]));
+                const float k1 = r1 * (acc_dk[i0 + 1] - kv[i0 + 1] * (r1 * r1 * sm.dot[me + 1]));
+                const float rk = __shfl_xor_sync(0xffffffffu, odd ? k0 : k1, 1);
+                if (me + odd < L)
+                    *reinterpret_cast<uint32_t *>(a.dk + obase + (size_t)me * hs) =
+                        odd ? pack_bf2(rk, k1) : pack_bf2(k0, rk);
+            }
+        }
         if (ok && warp == 0) {  // dg = reverse cumulative sum of dG (warp scan), dbeta
             float dgv[2];
     #pragma unroll
@@ -467,9 +516,11 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     int sms = 0;
     if ((e = sm_count(&sms)) != cudaSuccess) return e;
-    const int nunits = a.num_chunks * a.HV;
+    // whole groups of the r value heads of a key head per CTA (their dk sums)
+    const int r = a.HV / a.H;
+    const int nunits = a.num_chunks * a.HV, ngroups = nunits / r;
     const int slots = 2 * sms;
-    const int per = (nunits + slots - 1) / slots;
+    const int per = (ngroups + slots - 1) / slots * r;
     TimerScope ts(a.timer, GDN_KERNEL_BINTRA_B, s);
     k_bintra_b_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
     return cudaGetLastError();

@@ -17,9 +17,15 @@
 //   M_ij = QK_ij scale / (r_q,i r_k,j) Gamma_ij,  dMG = dM (.) Gamma,  P1 = dM (.) M
 //   (j <= i);
 //   batch 2 (M=64, contraction 64): dMG Khat and dMG^T Qhat;
-//   dqhat_t = e^{G_t} Dq_t + (dMG Khat)_t                  -> HBM (bf16, per value head)
-//   dkhat_t = e^{G_L - G_t} Dk_t + (dMG^T Qhat)_t           -> HBM (bf16, the rest comes
-//                                                              from the WY pullback)
+//   dqhat_t = e^{G_t} Dq_t + (dMG Khat)_t
+//   dkhat_t = e^{G_L - G_t} Dk_t + (dMG^T Qhat)_t           (the rest comes from the WY
+//                                                              pullback)
+// A CTA walks whole groups of the r = HV / H value heads of one key head, which
+// share q and k, and sums dqhat and dkhat over them in registers (fp32, value heads
+// in order).  After the group's last value head it writes the key head's dq with the
+// L2-norm backward applied, dq = (scale dqhat - nq (nq . scale dqhat)) / r_q with
+// nq = q / r_q, and the summed dkhat terms (bf16 [T, H, 128]) that the WY pullback
+// completes;
 //   dG_t    = qhat_t . e^{G_t} Dq_t - xi_t + sum_j P1_tj - sum_i P1_it,
 //   xi_t = khat_t . e^{G_L - G_t} Dk_t,   dG_L += sum_t xi_t + e^{G_L} <h, dh'>.
 // h / dh' are read as [N=k][K=v], i.e. their [k][v] tiles K-major; all tiles
@@ -67,6 +73,8 @@ struct BaSmem {
                                   // (after batch 2, with op_dmg: the dqhat rows of a full chunk)
     unsigned char stg[2 * kBox];  // rows of a full chunk staged for TMA stores: dW, then dkhat
     float pq[2][64], pk[2][64];   // per-warpgroup partial row dots
+    float pn[2][64];              // per-warpgroup partial row dots q . (summed dqhat)
+    float iq[64];                 // 1 / r_q (0 past L)
     float rp[2][64];              // per-warpgroup partial row sums of P1
     float cp[4][64];              // per-row-block column sums of P1
     float hdh[kThr / 32];
@@ -86,7 +94,7 @@ static_assert(offsetof(BaSmem, dh) % 1024 == 0 && offsetof(BaSmem, dO) % 1024 ==
 
 struct BaMaps {
     CUtensorMap h, dh, dO, dvn, vn, q, k;
-    CUtensorMap dw, dqp, dkp;   // outputs, stored by TMA from a full chunk's staged rows
+    CUtensorMap dw, dq, dkp;    // outputs, stored by TMA from a full chunk's staged rows
 };
 
 struct Unit {
@@ -190,6 +198,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     fetch(x);
     bool ok = true;
     uint32_t phase = 0;
+    // the key head's sums of dqhat ([0]) and dkhat ([1]) over its value heads: this
+    // lane's 16x256b fragment positions in the warpgroup's two 32-column blocks
+    float acc_dk[2][2][16];
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int L = x.L;
@@ -198,6 +209,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             sm.G[tid] = pG;
             sm.qsc[tid] = in ? a.scale / pRq : 0.f;
             sm.rki[tid] = in ? 1.f / pRk : 0.f;
+            sm.iq[tid] = in ? 1.f / pRq : 0.f;
         }
         bool got = mbar_wait(&sm.a_bar, a_waited & 1);
         if (need_b) got = mbar_wait(&sm.b_bar[bcur], (bpar >> bcur) & 1) && got;
@@ -363,29 +375,29 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         if (!done) { ok = false; break; }
         if (tid == 0) tma_store_wait_read();  // stg is rewritten below
         __syncthreads();
-        {  // dqhat, dkhat rows (this warpgroup's 64 columns) and the inter-term row dots,
-           // on 16x256b fragments (rows ra, rb; columns c0 + 8k + cq + {0, 1})
+        const int r = a.HV / a.H;
+        const bool first = x.hv % r == 0, last = x.hv % r == r - 1;  // of the key head's value heads
+        {  // dqhat, dkhat rows (this warpgroup's 64 columns) added to the key head's sums,
+           // and the inter-term row dots, on 16x256b fragments (rows ra, rb; columns
+           // c0 + 8k + cq + {0, 1})
             const float ega = la ? sm.eg[ra] : 0.f, egb = lb ? sm.eg[rb] : 0.f;
             const float ela = la ? sm.egl_g[ra] : 0.f, elb = lb ? sm.egl_g[rb] : 0.f;
-            const size_t oa = ((size_t)(x.t0 + (la ? ra : 0)) * a.HV + x.hv) * kDim;
-            const size_t ob = ((size_t)(x.t0 + (lb ? rb : 0)) * a.HV + x.hv) * kDim;
-            float xqa = 0.f, xqb = 0.f, xka = 0.f, xkb = 0.f;
+            float xqa = 0.f, xqb = 0.f, xka = 0.f, xkb = 0.f, pna = 0.f, pnb = 0.f;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {  // m = 0: dq with q; m = 1: dk with k
                 const uint32_t cA = m ? cDK : cDQ, cB = m ? cKI : cQI;
                 const unsigned char *tile = m ? sm.k[bcur] : sm.q[bcur];
-                bf16 *dst = m ? a.dkp : a.dqp;
-                unsigned char *stage = m ? sm.stg : sm.op_dmg;  // two 64-column halves each
                 const float fa = m ? ela : ega, fb = m ? elb : egb;
                 float xa = 0.f, xb = 0.f;
 #pragma unroll
-                for (int cc = 2 * grp; cc < 2 * grp + 2; ++cc) {
-                    const int c0 = 32 * cc;
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c0 = 32 * (2 * grp + h2);
                     float dd[16], ii[16];
                     tmem_ld16x256_x4(t_row + cA + c0, dd);
                     tmem_ld16x256_x4(t_row + cB + c0, ii);
                     tmem_ld_wait();
                     const unsigned char *half = tile + (c0 >> 6) * kBox;
+                    float *acc = acc_dk[m][h2];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int col = (c0 & 63) + 8 * k + cq;  // within the 64-column half
@@ -394,15 +406,13 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                         const float b0 = fb * dd[4 * k + 2], b1 = fb * dd[4 * k + 3];
                         xa += qa.x * a0 + qa.y * a1;
                         xb += qb.x * b0 + qb.y * b1;
-                        const int gcol = c0 + 8 * k + cq;
-                        if (L == 64) {
-                            put_pair(stage + (c0 >> 6) * kBox, ra, col, a0 + ii[4 * k], a1 + ii[4 * k + 1]);
-                            put_pair(stage + (c0 >> 6) * kBox, rb, col, b0 + ii[4 * k + 2], b1 + ii[4 * k + 3]);
-                        } else {
-                            if (la)
-                                *reinterpret_cast<uint32_t *>(dst + oa + gcol) = pack_bf2(a0 + ii[4 * k], a1 + ii[4 * k + 1]);
-                            if (lb)
-                                *reinterpret_cast<uint32_t *>(dst + ob + gcol) = pack_bf2(b0 + ii[4 * k + 2], b1 + ii[4 * k + 3]);
+                        const float v[4] = {a0 + ii[4 * k], a1 + ii[4 * k + 1], b0 + ii[4 * k + 2],
+                                            b1 + ii[4 * k + 3]};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[4 * k + e] = (first ? 0.f : acc[4 * k + e]) + v[e];
+                        if (m == 0 && last) {
+                            pna += qa.x * acc[4 * k] + qa.y * acc[4 * k + 1];
+                            pnb += qb.x * acc[4 * k + 2] + qb.y * acc[4 * k + 3];
                         }
                     }
                 }
@@ -410,21 +420,61 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             }
             xqa = quad_sum(xqa); xqb = quad_sum(xqb);
             xka = quad_sum(xka); xkb = quad_sum(xkb);
+            if (last) { pna = quad_sum(pna); pnb = quad_sum(pnb); }
             if ((lane & 3) == 0) {
                 sm.pq[grp][ra] = xqa; sm.pq[grp][rb] = xqb;
                 sm.pk[grp][ra] = xka; sm.pk[grp][rb] = xkb;
+                if (last) { sm.pn[grp][ra] = pna; sm.pn[grp][rb] = pnb; }
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
         __syncthreads();  // q / k tiles, TMEM and the row sums are all read or written
-        if (tid == 0 && L == 64) {  // the staged dqhat and dkhat rows
-            tma_store_3d(&maps.dqp, 0, x.hv, x.t0, sm.op_dmg);
-            tma_store_3d(&maps.dqp, 64, x.hv, x.t0, sm.op_dmg + kBox);
-            tma_store_3d(&maps.dkp, 0, x.hv, x.t0, sm.stg);
-            tma_store_3d(&maps.dkp, 64, x.hv, x.t0, sm.stg + kBox);
-            tma_store_commit();
+        if (last) {  // the key head's dq (L2-norm backward applied) and summed dkhat terms:
+                     // full chunks staged for TMA stores, ragged ones stored directly
+            const float sa = la ? sm.qsc[ra] : 0.f, sb = lb ? sm.qsc[rb] : 0.f;
+            const float ia = la ? sm.iq[ra] : 0.f, ib = lb ? sm.iq[rb] : 0.f;
+            const float Pa = (sm.pn[0][ra] + sm.pn[1][ra]) * ia * ia;
+            const float Pb = (sm.pn[0][rb] + sm.pn[1][rb]) * ib * ib;
+            const size_t oa = ((size_t)(x.t0 + (la ? ra : 0)) * a.H + x.h) * kDim;
+            const size_t ob = ((size_t)(x.t0 + (lb ? rb : 0)) * a.H + x.h) * kDim;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int c0 = 32 * (2 * grp + h2);
+                const unsigned char *half = sm.q[bcur] + (c0 >> 6) * kBox;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int col = (c0 & 63) + 8 * k + cq, gcol = c0 + 8 * k + cq;
+                    const float2 qa = get_pair(half, ra, col), qb = get_pair(half, rb, col);
+                    const float *aq = acc_dk[0][h2], *ak = acc_dk[1][h2];
+                    const float q0 = sa * (aq[4 * k] - qa.x * Pa), q1 = sa * (aq[4 * k + 1] - qa.y * Pa);
+                    const float q2 = sb * (aq[4 * k + 2] - qb.x * Pb), q3 = sb * (aq[4 * k + 3] - qb.y * Pb);
+                    if (L == 64) {
+                        put_pair(sm.op_dmg + (c0 >> 6) * kBox, ra, col, q0, q1);
+                        put_pair(sm.op_dmg + (c0 >> 6) * kBox, rb, col, q2, q3);
+                        put_pair(sm.stg + (c0 >> 6) * kBox, ra, col, ak[4 * k], ak[4 * k + 1]);
+                        put_pair(sm.stg + (c0 >> 6) * kBox, rb, col, ak[4 * k + 2], ak[4 * k + 3]);
+                    } else {
+                        if (la) {
+                            *reinterpret_cast<uint32_t *>(a.dq + oa + gcol) = pack_bf2(q0, q1);
+                            *reinterpret_cast<uint32_t *>(a.dkpart + oa + gcol) = pack_bf2(ak[4 * k], ak[4 * k + 1]);
+                        }
+                        if (lb) {
+                            *reinterpret_cast<uint32_t *>(a.dq + ob + gcol) = pack_bf2(q2, q3);
+                            *reinterpret_cast<uint32_t *>(a.dkpart + ob + gcol) = pack_bf2(ak[4 * k + 2], ak[4 * k + 3]);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0 && L == 64) {  // the staged dq and dkhat rows of key head h
+                tma_store_3d(&maps.dq, 0, x.h, x.t0, sm.op_dmg);
+                tma_store_3d(&maps.dq, 64, x.h, x.t0, sm.op_dmg + kBox);
+                tma_store_3d(&maps.dkp, 0, x.h, x.t0, sm.stg);
+                tma_store_3d(&maps.dkp, 64, x.h, x.t0, sm.stg + kBox);
+                tma_store_commit();
+            }
         }
+        tc_fence_before();
         if (warp == 0) {  // dG_t, and the G_L terms summed in a fixed order
             float dgz[2], sx = 0.f;
 #pragma unroll
@@ -487,8 +537,8 @@ cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
         !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
         !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.dqp, a.dqp, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.dkp, a.dkp, a.HV, a.T, rowb, rowb * a.HV, 64))
+        !encode_rows_bf16(&m.dq, a.dq, a.H, a.T, rowb, rowb * a.H, 64) ||
+        !encode_rows_bf16(&m.dkp, a.dkpart, a.H, a.T, rowb, rowb * a.H, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BaSmem) + 1024;
     static_assert(sizeof(BaSmem) + 1024 <= 232448, "shared memory budget");
@@ -498,9 +548,11 @@ cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int nunits = a.num_chunks * a.HV;
-    const int grid = nunits < sms ? nunits : sms;
-    const int per = (nunits + grid - 1) / grid;
+    // whole groups of the r value heads of a key head per CTA (their dq / dk sums)
+    const int r = a.HV / a.H;
+    const int nunits = a.num_chunks * a.HV, ngroups = nunits / r;
+    const int grid = ngroups < sms ? ngroups : sms;
+    const int per = (ngroups + grid - 1) / grid * r;
     TimerScope ts(a.timer, GDN_KERNEL_BINTRA_A, s);
     k_bintra_a_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
     return cudaGetLastError();

@@ -7,9 +7,6 @@
 //   k_prep   q / k norms r = sqrt(sum x^2 + 1e-6) ("C6: GDN decode-step
 //            goldens ...", Provider: divide by the sqrt) and the chunk-local
 //            cumulative sum G of g;
-//   k_bnorm  fixed-order sum of the per-value-head gradients of qhat / khat
-//            over the HV / H value heads of each key head, then the L2-norm
-//            backward dx = (dn - n (n . dn)) / r.
 // The tensor-core kernels of the chunked (WY) form live in gdn_*_tc.cu.
 // Every reduction runs in a fixed order and no kernel uses atomics, so results
 // are bit-identical from run to run.
@@ -145,107 +142,6 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// Backward, step 5: sum the per-value-head gradients of qhat / khat over the
-// HV / H value heads of each key head (fixed order) and apply the L2-norm
-// backward dx = (dn - n (n . dn)) / r.  Half a warp per (token, key head): each
-// lane moves 8 elements with 16-byte loads and stores.
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
-    const float2 a0 = bf2_to_f2(u.x), a1 = bf2_to_f2(u.y), a2 = bf2_to_f2(u.z), a3 = bf2_to_f2(u.w);
-    x[0] = a0.x; x[1] = a0.y; x[2] = a1.x; x[3] = a1.y; x[4] = a2.x; x[5] = a2.y; x[6] = a3.x; x[7] = a3.y;
-}
-
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&t);
-}
-
-// R = HV / H when it is a compile-time case (1, 2, 4), else 0 (read from a): with R
-// known, every load of the item (q, k, the norms and the 3 R partials) is issued
-// before the first is used.  The sums run in the same order either way.
-template <int R>
-__global__ void __launch_bounds__(kThreads) k_bnorm(ChunkArgs a) {
-    const int l16 = threadIdx.x & 15;
-    const size_t item = (size_t)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
-    const bool valid = item < (size_t)a.T * a.H;
-    const int t = valid ? (int)(item / a.H) : 0, h = valid ? (int)(item % a.H) : 0;
-    const int r = R > 0 ? R : a.HV / a.H;
-    const size_t row = ((size_t)t * a.H + h) * kDim + l16 * 8;
-    uint4 lq = make_uint4(0u, 0u, 0u, 0u), lk = lq;
-    float rq = 1.f, rk = 1.f;
-    if (valid) {
-        lq = *reinterpret_cast<const uint4 *>(a.q + row);
-        lk = *reinterpret_cast<const uint4 *>(a.k + row);
-        rq = a.rq[(size_t)t * a.H + h];
-        rk = a.rk[(size_t)t * a.H + h];
-    }
-    float dq[8], dk[8], xq[8], xk[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) dq[u] = dk[u] = 0.f;
-    if constexpr (R > 0) {
-        uint4 p1[R], p2[R], p3[R];
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const size_t o = ((size_t)t * a.HV + h * R + j) * kDim + l16 * 8;
-            p1[j] = valid ? *reinterpret_cast<const uint4 *>(a.dqp + o) : make_uint4(0u, 0u, 0u, 0u);
-            p2[j] = valid ? *reinterpret_cast<const uint4 *>(a.dkp + o) : make_uint4(0u, 0u, 0u, 0u);
-            p3[j] = valid ? *reinterpret_cast<const uint4 *>(a.dkp2 + o) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            float x1[8], x2[8], x3[8];
-            unpack8(p1[j], x1);
-            unpack8(p2[j], x2);
-            unpack8(p3[j], x3);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                dq[u] += x1[u];
-                dk[u] += x2[u] + x3[u];
-            }
-        }
-    } else if (valid) {
-        for (int j = 0; j < r; ++j) {
-            const size_t o = ((size_t)t * a.HV + h * r + j) * kDim + l16 * 8;
-            float x1[8], x2[8], x3[8];
-            unpack8(*reinterpret_cast<const uint4 *>(a.dqp + o), x1);
-            unpack8(*reinterpret_cast<const uint4 *>(a.dkp + o), x2);
-            unpack8(*reinterpret_cast<const uint4 *>(a.dkp2 + o), x3);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                dq[u] += x1[u];
-                dk[u] += x2[u] + x3[u];
-            }
-        }
-    }
-    unpack8(lq, xq);
-    unpack8(lk, xk);
-    float nq = 0.f, nk = 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        xq[u] /= rq;
-        xk[u] /= rk;
-        dq[u] *= a.scale;
-        nq += xq[u] * dq[u];
-        nk += xk[u] * dk[u];
-    }
-#pragma unroll
-    for (int o = 8; o; o >>= 1) {  // the 16 lanes of this item
-        nq += __shfl_xor_sync(0xffffffffu, nq, o);
-        nk += __shfl_xor_sync(0xffffffffu, nk, o);
-    }
-    if (valid) {
-        uint32_t pq[4], pk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            pq[u] = pack2((dq[2 * u] - xq[2 * u] * nq) / rq, (dq[2 * u + 1] - xq[2 * u + 1] * nq) / rq);
-            pk[u] = pack2((dk[2 * u] - xk[2 * u] * nk) / rk, (dk[2 * u + 1] - xk[2 * u + 1] * nk) / rk);
-        }
-        *reinterpret_cast<uint4 *>(a.dq + row) = make_uint4(pq[0], pq[1], pq[2], pq[3]);
-        *reinterpret_cast<uint4 *>(a.dk + row) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-}
-
-
 }  // namespace
 
 cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s) {
@@ -312,17 +208,6 @@ cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     if (a.num_chunks == 0) return cudaSuccess;
     if ((e = launch_bintra_a_tc(a, s)) != cudaSuccess) return e;
     if ((e = launch_bintra_b_tc(a, s)) != cudaSuccess) return e;
-    {
-        const size_t items = (size_t)a.T * a.H;
-        const unsigned blocks = (unsigned)((items + kThreads / 16 - 1) / (kThreads / 16));
-        TimerScope ts(a.timer, GDN_KERNEL_BNORM, s);
-        const int r = a.HV / a.H;
-        if (r == 1) k_bnorm<1><<<blocks, kThreads, 0, s>>>(a);
-        else if (r == 2) k_bnorm<2><<<blocks, kThreads, 0, s>>>(a);
-        else if (r == 4) k_bnorm<4><<<blocks, kThreads, 0, s>>>(a);
-        else k_bnorm<0><<<blocks, kThreads, 0, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
     return cudaSuccess;
 }
 

@@ -108,6 +108,40 @@ __device__ __forceinline__ float quad_sum(float v) {
     return v;
 }
 
+// Sums over the 32 lanes of a warp of 32 values per lane, transposed: lane l ends with
+// the sum over all lanes of x[l].  Five butterfly steps (16 + 8 + 4 + 2 + 1 shuffles):
+// at the step of offset o a lane keeps the half of its values whose index has bit o
+// equal to its own lane bit o, and adds the partner's copy of that half.  Fixed order.
+__device__ __forceinline__ float lanesum32(const float (&x)[32], int lane) {
+    float a[16], b[8], c[4], d[2];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const bool hi = lane & 16;
+        const float send = hi ? x[j] : x[16 + j];
+        a[j] = (hi ? x[16 + j] : x[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const bool hi = lane & 8;
+        const float send = hi ? a[j] : a[8 + j];
+        b[j] = (hi ? a[8 + j] : a[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const bool hi = lane & 4;
+        const float send = hi ? b[j] : b[4 + j];
+        c[j] = (hi ? b[4 + j] : b[j]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const bool hi = lane & 2;
+        const float send = hi ? c[j] : c[2 + j];
+        d[j] = (hi ? c[2 + j] : c[j]) + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const bool hi = lane & 1;
+    return (hi ? d[1] : d[0]) + __shfl_xor_sync(0xffffffffu, hi ? d[0] : d[1], 1);
+}
+
 // bf16 pair (columns col, col + 1 of row `row`) into a 64-wide SW128 tile.
 __device__ __forceinline__ void put_pair(unsigned char *tile, int row, int col, float a, float b) {
     *reinterpret_cast<uint32_t *>(tile + umma::sw128_off(row, col)) = pack_bf2(a, b);

@@ -67,9 +67,8 @@ struct ChunkArgs {
     bf16 *dvnew;            // [T,HV,V]  full gradient of v_new
     bf16 *dhc;              // [C_total,HV,K,V] gradient of the state after each chunk
     bf16 *dW;               // [T,HV,K]
-    bf16 *dqp, *dkp;        // [T,HV,K] per-value-head gradients of qhat (all terms) and
-                            // khat (h / dh' and Q K^T terms)
-    bf16 *dkp2;             // [T,HV,K] the WY-pullback terms of the khat gradient
+    bf16 *dkpart;           // [T,H,K] the h / dh' and Q K^T terms of the khat gradient,
+                            // summed over the value heads of each key head
     float *dGp;             // [T,HV]
     gdn_kernel_timer *timer;  // optional per-kernel events
 };

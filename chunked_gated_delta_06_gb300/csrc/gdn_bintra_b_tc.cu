@@ -363,10 +363,12 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             sm.dG[m] += bm * r2 - cp + bm * sm.eg[m] * sm.rki[m] * cz;
         }
         commit_wait(ok);
-        if (tid == 0 && ok && has_next) issue_a(maps, sm, a, nx);  // K, dW, dv_new, T read by phase 2
-        if (ok && has_next) ++a_issued;
         const int r = a.HV / a.H;
         const bool first = hv % r == 0, last = hv % r == r - 1;  // of the key head's value heads
+        // K, dW, dv_new and T have been read by phase 2; after a key head's last value
+        // head the K tile is read once more (dk below), so the next load waits for that
+        if (tid == 0 && ok && has_next && !last) issue_a(maps, sm, a, nx);
+        if (ok && has_next && !last) ++a_issued;
         if (ok) {  // thread d holds element d of the token rows m in [32 grp, 32 grp + 32);
                    // lanes 2i and 2i + 1 swap halves so that each stores bf16 pairs (d even,
                    // d + 1) of alternate tokens: even lanes tokens 2j, odd lanes 2j + 1.
@@ -421,7 +423,9 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     #pragma unroll
             for (int i = 0; i < 32; ++i) prod[i] = kv[i] * acc_dk[i];
             sm.dotp[grp][sub][lane] = epi::lanesum32(prod, lane);  // token j0 + lane, this warp's d
-            __syncthreads();
+            __syncthreads();  // every k value is in registers: the next unit's tiles may load
+            if (tid == 0 && has_next) issue_a(maps, sm, a, nx);
+            if (has_next) ++a_issued;
             if (tid < 64)
                 sm.dot[tid] = ((sm.dotp[tid >> 5][0][tid & 31] + sm.dotp[tid >> 5][1][tid & 31]) +
                                sm.dotp[tid >> 5][2][tid & 31]) + sm.dotp[tid >> 5][3][tid & 31];

@@ -50,27 +50,31 @@ constexpr int kThr = 256;   // two warpgroups share the 128 TMEM lanes
 constexpr uint32_t kHalf = 64 * 128;      // 64 rows x 128 B
 constexpr uint32_t kTile = 2 * kHalf;     // 64 rows x 128 bf16: two 8 KB halves
 
-// TMEM columns (256 allocated)
-constexpr uint32_t cKK = 0, cD1 = 64, cD2 = 128, cX = 192, cA = 64;   // phase 1
+// TMEM columns (256 allocated).  X reuses D2's columns and T^T X D1's (both read
+// before), so that columns 192 .. 255 hold, for the whole kernel, the key head's
+// dkhat sums (lane d = feature, column 192 + token).
+constexpr uint32_t cKK = 0, cD1 = 64, cD2 = 128, cX = 128, cA = 64;   // phase 1
 constexpr uint32_t cDK = 0, cWT = 64, cUT = 128;                       // phase 2
+constexpr uint32_t cACC = 192;                                         // dkhat sums
 
 struct BwSmem {
     unsigned char k[kTile], v[kTile], dw[kTile], dvn[kTile];
     unsigned char op_t[kHalf];     // T_ij [i][j]: K-major B of X, MN-major A of T^T X, MN-major B of phase 2
     unsigned char op_dx[kHalf];    // dT rows (K-major A of X = dT T^T), then X rows (MN-major B of T^T X)
-    unsigned char op_b[kHalf];     // B_tj / r_k,j  [t][j]  K-major B
-    unsigned char op_bt[kHalf];    // B_it / r_k,i  [i][t]  MN-major B
+    unsigned char op_b[kHalf];     // B_tj / r_k,j  [t][j]  K-major B; after phase 2 of a key
+                                   // head's last value head: its summed dkhat terms, columns 0..63
+    unsigned char op_bt[kHalf];    // B_it / r_k,i  [i][t]  MN-major B; then columns 64..127
     float G[64], beta[64], rki[64], eg[64], dG[64], db[64];
     float rs[2][64];               // per-warpgroup partial row sums of P2
     float cy[4][64], cz[4][64], cp[4][64];  // per-row-block column sums
     float dotp[2][4][32];          // khat . dkhat of token 32 grp + l over the d of warp (grp, sub)
     float dot[64];                 // k . dkhat per token (all 128 features)
-    uint64_t a_bar, v_bar, mma_bar;
+    uint64_t a_bar, v_bar, mma_bar, p_bar;
     uint32_t tmem_base;
 };
 
 struct BwMaps {
-    CUtensorMap k, v, dw, dvn, t;
+    CUtensorMap k, v, dw, dvn, t, dkp;
 };
 
 struct BwUnit {
@@ -140,6 +144,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         mbar_init(&sm.a_bar, 1);
         mbar_init(&sm.v_bar, 1);
         mbar_init(&sm.mma_bar, 1);
+        mbar_init(&sm.p_bar, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -151,6 +156,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         issue_v(maps, sm, x);
     }
     int a_issued = 1, v_issued = 1, waited = 0;  // same on every thread
+    int p_issued = 0, p_waited = 0;              // loads of the summed dkhat terms
     // per-token scalars of thread tid < 64, fetched one unit ahead
     float pG = 0.f, pR = 1.f, pD = 0.f;
     uint32_t pB = 0;   // raw beta bits, converted when published
@@ -170,9 +176,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     const uint32_t t_row = tb + ((uint32_t)(sub * 32) << 16);
     uint32_t phase = 0;
     bool ok = true;
-    // the key head's dkhat sums over its value heads: feature d = 32 sub + lane of
-    // tokens 32 grp .. 32 grp + 31
-    float acc_dk[32];
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int c = x.c, hv = x.hv, t0 = x.t0, L = x.L;
@@ -369,6 +372,14 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         // head the K tile is read once more (dk below), so the next load waits for that
         if (tid == 0 && ok && has_next && !last) issue_a(maps, sm, a, nx);
         if (ok && has_next && !last) ++a_issued;
+        if (ok && last) {  // the key head's summed dkhat terms over the free phase-2 operands
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&sm.p_bar, 2 * kHalf);
+                tma_load_3d(sm.op_b, &maps.dkp, 0, x.h, t0, &sm.p_bar);
+                tma_load_3d(sm.op_bt, &maps.dkp, 64, x.h, t0, &sm.p_bar);
+            }
+            ++p_issued;
+        }
         if (ok) {  // thread d holds element d of the token rows m in [32 grp, 32 grp + 32);
                    // lanes 2i and 2i + 1 swap halves so that each stores bf16 pairs (d even,
                    // d + 1) of alternate tokens: even lanes tokens 2j, odd lanes 2j + 1.
@@ -380,10 +391,11 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {  // 16 token columns at a time
                 const int m0 = j0 + 16 * hh;
-                float dk[16], wt[16], ut[16];
+                float dk[16], wt[16], ut[16], acc[16];
                 tmem_ld16(t_row + cDK + m0, dk);
                 tmem_ld16(t_row + cWT + m0, wt);
                 tmem_ld16(t_row + cUT + m0, ut);
+                if (!first) tmem_ld16(t_row + cACC + m0, acc);
                 tmem_ld_wait();
     #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
@@ -391,8 +403,8 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                     const float b0 = sm.beta[me], b1 = sm.beta[me + 1];
                     const float k0 = dk[2 * jj] + b0 * sm.eg[me] * wt[2 * jj];
                     const float k1 = dk[2 * jj + 1] + b1 * sm.eg[me + 1] * wt[2 * jj + 1];
-                    acc_dk[16 * hh + 2 * jj] = (first ? 0.f : acc_dk[16 * hh + 2 * jj]) + k0;
-                    acc_dk[16 * hh + 2 * jj + 1] = (first ? 0.f : acc_dk[16 * hh + 2 * jj + 1]) + k1;
+                    acc[2 * jj] = (first ? 0.f : acc[2 * jj]) + k0;
+                    acc[2 * jj + 1] = (first ? 0.f : acc[2 * jj + 1]) + k1;
                     const float v0 = b0 * ut[2 * jj], v1 = b1 * ut[2 * jj + 1];
                     const float rv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
                     if (me + odd < L) {
@@ -400,29 +412,46 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                         *reinterpret_cast<uint32_t *>(a.dv + o) = odd ? pack_bf2(rv, v1) : pack_bf2(v0, rv);
                     }
                 }
+                tmem_st16(t_row + cACC + m0, acc);
             }
+            tmem_st_wait();
         } else if (tid == 0 && a.status) {
             atomicOr(a.status, 2);
         }
         __syncthreads();
+        if (ok && last) {
+            const bool got = mbar_wait(&sm.p_bar, p_waited & 1);
+            ++p_waited;
+            ok = __syncthreads_and(got);
+        }
         if (ok && last) {  // the key head's dk: its dkhat (these sums plus the h / dh' and
                            // Q K^T terms the previous kernel summed), then the L2-norm
                            // backward dk = (dkhat - khat (khat . dkhat)) / r_k
             const int d = sub * 32 + lane, odd = lane & 1;
             const size_t hs = (size_t)a.H * kDim;
-            const size_t pbase = ((size_t)t0 * a.H + x.h) * kDim + d;
             const unsigned char *kcol = sm.k + (d >> 6) * kHalf;
-            float kv[32];
+            const unsigned char *pcol = d >> 6 ? sm.op_bt : sm.op_b;
+            auto kval = [&](int m) {  // raw k of token m, feature d (bf16 K tile)
+                return bf2f(*reinterpret_cast<const bf16 *>(kcol + sw128_off(m, d & 63)));
+            };
+            float acc_dk[32];
+            tmem_ld32(t_row + cACC + j0, acc_dk);
+            tmem_ld_wait();
     #pragma unroll
-            for (int i = 0; i < 32; ++i) {  // dkhat and k of token j0 + i, feature d
-                const int m = j0 + i;
-                acc_dk[i] += m < L ? bf2f(a.dkpart[pbase + (size_t)m * hs]) : 0.f;
-                kv[i] = bf2f(*reinterpret_cast<const bf16 *>(kcol + sw128_off(m, d & 63)));
+            for (int i = 0; i < 32; ++i)  // dkhat of token j0 + i, feature d
+                acc_dk[i] += j0 + i < L ? bf2f(*reinterpret_cast<const bf16 *>(pcol + sw128_off(j0 + i, d & 63))) : 0.f;
+            // k . dkhat of token j0 + lane over this warp's 32 features: the first step of the
+            // transposed lane sum (epi::lanesum32) is taken here, on products formed as needed
+            float half16[16];
+            {
+                const bool hi = lane & 16;
+    #pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float lo_p = kval(j0 + j) * acc_dk[j], hi_p = kval(j0 + 16 + j) * acc_dk[16 + j];
+                    half16[j] = (hi ? hi_p : lo_p) + __shfl_xor_sync(0xffffffffu, hi ? lo_p : hi_p, 16);
+                }
             }
-            float prod[32];
-    #pragma unroll
-            for (int i = 0; i < 32; ++i) prod[i] = kv[i] * acc_dk[i];
-            sm.dotp[grp][sub][lane] = epi::lanesum32(prod, lane);  // token j0 + lane, this warp's d
+            sm.dotp[grp][sub][lane] = epi::lanesum16(half16, lane);  // token j0 + lane, this warp's d
             __syncthreads();  // every k value is in registers: the next unit's tiles may load
             if (tid == 0 && has_next) issue_a(maps, sm, a, nx);
             if (has_next) ++a_issued;
@@ -435,8 +464,8 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             for (int jj = 0; jj < 16; ++jj) {
                 const int i0 = 2 * jj, me = j0 + i0;
                 const float r0 = sm.rki[me], r1 = sm.rki[me + 1];
-                const float k0 = r0 * (acc_dk[i0] - kv[i0] * (r0 * r0 * sm.dot[me]));
-                const float k1 = r1 * (acc_dk[i0 + 1] - kv[i0 + 1] * (r1 * r1 * sm.dot[me + 1]));
+                const float k0 = r0 * (acc_dk[i0] - kval(me) * (r0 * r0 * sm.dot[me]));
+                const float k1 = r1 * (acc_dk[i0 + 1] - kval(me + 1) * (r1 * r1 * sm.dot[me + 1]));
                 const float rk = __shfl_xor_sync(0xffffffffu, odd ? k0 : k1, 1);
                 if (me + odd < L)
                     *reinterpret_cast<uint32_t *>(a.dk + obase + (size_t)me * hs) =
@@ -493,6 +522,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving
         if (a_issued > waited) mbar_wait(&sm.a_bar, (a_issued - 1) & 1, kDrainLimitNs);
+        if (p_issued > 0) mbar_wait(&sm.p_bar, (p_issued - 1) & 1, kDrainLimitNs);
         if (v_issued > waited) mbar_wait(&sm.v_bar, (v_issued - 1) & 1, kDrainLimitNs);
     }
     tc_fence_before();
@@ -511,7 +541,8 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64))
+        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64) ||
+        !encode_rows_bf16(&m.dkp, a.dkpart, a.H, a.T, rowb, rowb * a.H, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BwSmem) + 1024;
     static_assert(2 * (sizeof(BwSmem) + 2048) <= 233472, "two CTAs per SM");

@@ -59,6 +59,10 @@ constexpr uint32_t kBig = 128 * 128;      // 128 rows x 128 B
 // TMEM columns (512 allocated)
 constexpr uint32_t cDQ = 0, cDW = 128, cDK = 256, cQK = 384, cDM = 448;   // batch 1
 constexpr uint32_t cQI = 384, cKI = 128;                                   // batch 2
+// Every product here is M = 64, which fills lanes 0..15 of each 32-lane quarter; the
+// key head's dqhat / dkhat sums live in lanes 16..31 of the Dq / Dk columns, in the
+// 16x256b fragment layout of the epilogue (the MMAs never write those lanes).
+constexpr uint32_t kAccLanes = 16u << 16;
 
 struct BaSmem {
     unsigned char h[2 * kBig];    // h_c [k][v]: two v-halves of 128 rows
@@ -198,9 +202,6 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     fetch(x);
     bool ok = true;
     uint32_t phase = 0;
-    // the key head's sums of dqhat ([0]) and dkhat ([1]) over its value heads: this
-    // lane's 16x256b fragment positions in the warpgroup's two 32-column blocks
-    float acc_dk[2][2][16];
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int L = x.L;
@@ -397,7 +398,11 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                     tmem_ld16x256_x4(t_row + cB + c0, ii);
                     tmem_ld_wait();
                     const unsigned char *half = tile + (c0 >> 6) * kBox;
-                    float *acc = acc_dk[m][h2];
+                    float acc[16];
+                    if (!first) {
+                        tmem_ld16x256_x4(t_row + kAccLanes + cA + c0, acc);
+                        tmem_ld_wait();
+                    }
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int col = (c0 & 63) + 8 * k + cq;  // within the 64-column half
@@ -415,11 +420,13 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                             pnb += qb.x * acc[4 * k + 2] + qb.y * acc[4 * k + 3];
                         }
                     }
+                    epi::tmem_st16x256_x4(t_row + kAccLanes + cA + c0, acc);
                 }
                 if (m) { xka = xa; xkb = xb; } else { xqa = xa; xqb = xb; }
             }
             xqa = quad_sum(xqa); xqb = quad_sum(xqb);
             xka = quad_sum(xka); xkb = quad_sum(xkb);
+            tmem_st_wait();
             if (last) { pna = quad_sum(pna); pnb = quad_sum(pnb); }
             if ((lane & 3) == 0) {
                 sm.pq[grp][ra] = xqa; sm.pq[grp][rb] = xqb;
@@ -440,11 +447,14 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int c0 = 32 * (2 * grp + h2);
                 const unsigned char *half = sm.q[bcur] + (c0 >> 6) * kBox;
+                float aq[16], ak[16];
+                tmem_ld16x256_x4(t_row + kAccLanes + cDQ + c0, aq);
+                tmem_ld16x256_x4(t_row + kAccLanes + cDK + c0, ak);
+                tmem_ld_wait();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int col = (c0 & 63) + 8 * k + cq, gcol = c0 + 8 * k + cq;
                     const float2 qa = get_pair(half, ra, col), qb = get_pair(half, rb, col);
-                    const float *aq = acc_dk[0][h2], *ak = acc_dk[1][h2];
                     const float q0 = sa * (aq[4 * k] - qa.x * Pa), q1 = sa * (aq[4 * k + 1] - qa.y * Pa);
                     const float q2 = sb * (aq[4 * k + 2] - qb.x * Pb), q3 = sb * (aq[4 * k + 3] - qb.y * Pb);
                     if (L == 64) {

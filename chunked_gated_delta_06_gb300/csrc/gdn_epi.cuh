@@ -73,6 +73,19 @@ __device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float (&x)[16])
     for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(u[i]);
 }
 
+// Store of the same fragment layout (16 lanes from the address's lane, 32 columns).
+__device__ __forceinline__ void tmem_st16x256_x4(uint32_t taddr, const float (&x)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(__float_as_uint(x[0])), "r"(__float_as_uint(x[1])), "r"(__float_as_uint(x[2])),
+          "r"(__float_as_uint(x[3])), "r"(__float_as_uint(x[4])), "r"(__float_as_uint(x[5])),
+          "r"(__float_as_uint(x[6])), "r"(__float_as_uint(x[7])), "r"(__float_as_uint(x[8])),
+          "r"(__float_as_uint(x[9])), "r"(__float_as_uint(x[10])), "r"(__float_as_uint(x[11])),
+          "r"(__float_as_uint(x[12])), "r"(__float_as_uint(x[13])), "r"(__float_as_uint(x[14])),
+          "r"(__float_as_uint(x[15]))
+        : "memory");
+}
+
 // Column sums over the 16 rows of a 16x256b fragment: y[2k + p] is this lane's
 // two-row partial of column 8k + 2 (t % 4) + p.  Three butterfly steps over the
 // eight lanes that share t % 4 leave lane t with the sum of column
@@ -112,14 +125,23 @@ __device__ __forceinline__ float quad_sum(float v) {
 // the sum over all lanes of x[l].  Five butterfly steps (16 + 8 + 4 + 2 + 1 shuffles):
 // at the step of offset o a lane keeps the half of its values whose index has bit o
 // equal to its own lane bit o, and adds the partner's copy of that half.  Fixed order.
+__device__ __forceinline__ float lanesum16(const float (&a)[16], int lane);
 __device__ __forceinline__ float lanesum32(const float (&x)[32], int lane) {
-    float a[16], b[8], c[4], d[2];
+    float a[16];
+    const bool hi = lane & 16;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const bool hi = lane & 16;
         const float send = hi ? x[j] : x[16 + j];
         a[j] = (hi ? x[16 + j] : x[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
     }
+    return lanesum16(a, lane);
+}
+
+// The last four steps of lanesum32, for values already halved by the offset-16 step:
+// lane l holds, for j < 16, a partial of index (l & 16) + j; it ends with the sum
+// over all lanes of index l.
+__device__ __forceinline__ float lanesum16(const float (&a)[16], int lane) {
+    float b[8], c[4], d[2];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const bool hi = lane & 8;

@@ -452,9 +452,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                 }
             }
             sm.dotp[grp][sub][lane] = epi::lanesum16(half16, lane);  // token j0 + lane, this warp's d
-            __syncthreads();  // every k value is in registers: the next unit's tiles may load
-            if (tid == 0 && has_next) issue_a(maps, sm, a, nx);
-            if (has_next) ++a_issued;
+            __syncthreads();
             if (tid < 64)
                 sm.dot[tid] = ((sm.dotp[tid >> 5][0][tid & 31] + sm.dotp[tid >> 5][1][tid & 31]) +
                                sm.dotp[tid >> 5][2][tid & 31]) + sm.dotp[tid >> 5][3][tid & 31];
@@ -471,6 +469,9 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                     *reinterpret_cast<uint32_t *>(a.dk + obase + (size_t)me * hs) =
                         odd ? pack_bf2(rk, k1) : pack_bf2(k0, rk);
             }
+            __syncthreads();  // every read of the K tile is done: the next unit's tiles may load
+            if (tid == 0 && has_next) issue_a(maps, sm, a, nx);
+            if (has_next) ++a_issued;
         }
         if (ok && warp == 0) {  // dg = reverse cumulative sum of dG (warp scan), dbeta
             float dgv[2];

@@ -216,6 +216,16 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         // the next unit (its table entries are a dependent load: after the MMA issue)
         const BwUnit nx = has_next ? bw_next(a, x) : x;
         if (has_next) fetch(nx);
+        if (tid == 0 && hv % (a.HV / a.H) == a.HV / a.H - 1) {
+            // a key head's last value head: its summed dkhat terms and the next unit's K
+            // (both loaded only after phase 2) are warmed in L2 now
+            tma_prefetch_3d(&maps.dkp, 0, x.h, t0);
+            tma_prefetch_3d(&maps.dkp, 64, x.h, t0);
+            if (has_next) {
+                tma_prefetch_3d(&maps.k, 0, nx.h, nx.t0);
+                tma_prefetch_3d(&maps.k, 64, nx.h, nx.t0);
+            }
+        }
         commit_wait(ok);
         if (tid == 0 && ok && has_next) issue_v(maps, sm, nx);  // V has been read by phase 1
         if (ok && has_next) ++v_issued;

@@ -393,16 +393,12 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int c0 = 32 * (2 * grp + h2);
-                    float dd[16], ii[16];
+                    float dd[16], ii[16], acc[16];
                     tmem_ld16x256_x4(t_row + cA + c0, dd);
                     tmem_ld16x256_x4(t_row + cB + c0, ii);
+                    if (!first) tmem_ld16x256_x4(t_row + kAccLanes + cA + c0, acc);
                     tmem_ld_wait();
                     const unsigned char *half = tile + (c0 >> 6) * kBox;
-                    float acc[16];
-                    if (!first) {
-                        tmem_ld16x256_x4(t_row + kAccLanes + cA + c0, acc);
-                        tmem_ld_wait();
-                    }
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int col = (c0 & 63) + 8 * k + cq;  // within the 64-column half

@@ -73,8 +73,10 @@ def kernel_work(name, T, H, HV, N, C_total):
         bstate=T * H * D * bf * 2 + TV * D * bf * 4 + C_total * HV * D * D * bf,
         # q, k; dO, dv_new, v_new in and dW out; dG; h_c, dh_c; dq and the summed dkhat out
         bintra_a=T * H * D * bf * 4 + TV * D * bf * 4 + TV * 4 + C_total * HV * D * D * bf * 2,
-        # k; v, dW, dv_new in and dv out; beta, G, dG, dg / dbeta; T; summed dkhat in, dk out
-        bintra_b=T * H * D * bf * 3 + TV * D * bf * 4 + TV * 12 + C_total * HV * C * C * 2,
+        # k; v, dW, dv_new in and dv out; beta, G, dG, dg / dbeta; T; summed dkhat terms out
+        bintra_b=T * H * D * bf * 2 + TV * D * bf * 4 + TV * 12 + C_total * HV * C * C * 2,
+        # the two summed dkhat terms and k in, dk out; r_k
+        dknorm=T * H * D * bf * 4 + T * H * 4,
     ).get(name, 0.0)
     return f, b
 
@@ -113,7 +115,7 @@ KERNEL_SOURCE = {
     "intra": "gdn_intra_tc.cu", "state": "gdn_state_tc.cu", "out": "gdn_out_tc.cu",
     "dvloc": "gdn_out_tc.cu", "bstate": "gdn_bstate_tc.cu", "bintra_a": "gdn_bintra_tc.cu",
     "bintra_b": "gdn_bintra_b_tc.cu", "decode": "gdn_decode.cu", "prep": "gdn_chunk.cu",
-    "plan": "gdn_chunk.cu",
+    "plan": "gdn_chunk.cu", "dknorm": "gdn_chunk.cu",
 }
 
 

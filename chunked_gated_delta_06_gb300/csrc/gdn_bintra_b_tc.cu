@@ -22,11 +22,10 @@
 //   dG_m   += beta_m sum_j P2_mj - sum_i beta_i P2_im + beta_m e^{G_m}/r_k,m sum_i T_im D1_im
 // and dg is the reverse cumulative sum of dG (which arrives holding the h / dh'
 // and Q K^T terms).  A CTA walks whole groups of the r = HV / H value heads of one
-// key head and sums their dkhat terms in registers (fp32, value heads in order);
-// after the group's last value head it adds the key head's h / dh' and Q K^T terms
-// (summed the same way by the previous kernel) and writes dk with the L2-norm
-// backward applied, dk = (dkhat - khat (khat . dkhat)) / r_k, the row dot taken
-// over the 128 features by lane butterflies and a fixed-order sum of four warps.
+// key head and sums their dkhat terms in fp32 in spare TMEM columns (value heads in
+// order); after the group's last value head it writes the key head's sums (bf16
+// [T, H, 128]), which k_dknorm adds to the h / dh' and Q K^T terms before the L2-norm
+// backward.
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -61,20 +60,17 @@ struct BwSmem {
     unsigned char k[kTile], v[kTile], dw[kTile], dvn[kTile];
     unsigned char op_t[kHalf];     // T_ij [i][j]: K-major B of X, MN-major A of T^T X, MN-major B of phase 2
     unsigned char op_dx[kHalf];    // dT rows (K-major A of X = dT T^T), then X rows (MN-major B of T^T X)
-    unsigned char op_b[kHalf];     // B_tj / r_k,j  [t][j]  K-major B; after phase 2 of a key
-                                   // head's last value head: its summed dkhat terms, columns 0..63
-    unsigned char op_bt[kHalf];    // B_it / r_k,i  [i][t]  MN-major B; then columns 64..127
+    unsigned char op_b[kHalf];     // B_tj / r_k,j  [t][j]  K-major B
+    unsigned char op_bt[kHalf];    // B_it / r_k,i  [i][t]  MN-major B
     float G[64], beta[64], rki[64], eg[64], dG[64], db[64];
     float rs[2][64];               // per-warpgroup partial row sums of P2
     float cy[4][64], cz[4][64], cp[4][64];  // per-row-block column sums
-    float dotp[2][4][32];          // khat . dkhat of token 32 grp + l over the d of warp (grp, sub)
-    float dot[64];                 // k . dkhat per token (all 128 features)
-    uint64_t a_bar, v_bar, mma_bar, p_bar;
+    uint64_t a_bar, v_bar, mma_bar;
     uint32_t tmem_base;
 };
 
 struct BwMaps {
-    CUtensorMap k, v, dw, dvn, t, dkp;
+    CUtensorMap k, v, dw, dvn, t;
 };
 
 struct BwUnit {
@@ -144,7 +140,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         mbar_init(&sm.a_bar, 1);
         mbar_init(&sm.v_bar, 1);
         mbar_init(&sm.mma_bar, 1);
-        mbar_init(&sm.p_bar, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -156,7 +151,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         issue_v(maps, sm, x);
     }
     int a_issued = 1, v_issued = 1, waited = 0;  // same on every thread
-    int p_issued = 0, p_waited = 0;              // loads of the summed dkhat terms
     // per-token scalars of thread tid < 64, fetched one unit ahead
     float pG = 0.f, pR = 1.f, pD = 0.f;
     uint32_t pB = 0;   // raw beta bits, converted when published
@@ -216,16 +210,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         // the next unit (its table entries are a dependent load: after the MMA issue)
         const BwUnit nx = has_next ? bw_next(a, x) : x;
         if (has_next) fetch(nx);
-        if (tid == 0 && hv % (a.HV / a.H) == a.HV / a.H - 1) {
-            // a key head's last value head: its summed dkhat terms and the next unit's K
-            // (both loaded only after phase 2) are warmed in L2 now
-            tma_prefetch_3d(&maps.dkp, 0, x.h, t0);
-            tma_prefetch_3d(&maps.dkp, 64, x.h, t0);
-            if (has_next) {
-                tma_prefetch_3d(&maps.k, 0, nx.h, nx.t0);
-                tma_prefetch_3d(&maps.k, 64, nx.h, nx.t0);
-            }
-        }
         commit_wait(ok);
         if (tid == 0 && ok && has_next) issue_v(maps, sm, nx);  // V has been read by phase 1
         if (ok && has_next) ++v_issued;
@@ -376,20 +360,10 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             sm.dG[m] += bm * r2 - cp + bm * sm.eg[m] * sm.rki[m] * cz;
         }
         commit_wait(ok);
+        if (tid == 0 && ok && has_next) issue_a(maps, sm, a, nx);  // K, dW, dv_new, T read by phase 2
+        if (ok && has_next) ++a_issued;
         const int r = a.HV / a.H;
         const bool first = hv % r == 0, last = hv % r == r - 1;  // of the key head's value heads
-        // K, dW, dv_new and T have been read by phase 2; after a key head's last value
-        // head the K tile is read once more (dk below), so the next load waits for that
-        if (tid == 0 && ok && has_next && !last) issue_a(maps, sm, a, nx);
-        if (ok && has_next && !last) ++a_issued;
-        if (ok && last) {  // the key head's summed dkhat terms over the free phase-2 operands
-            if (tid == 0) {
-                mbar_arrive_expect_tx(&sm.p_bar, 2 * kHalf);
-                tma_load_3d(sm.op_b, &maps.dkp, 0, x.h, t0, &sm.p_bar);
-                tma_load_3d(sm.op_bt, &maps.dkp, 64, x.h, t0, &sm.p_bar);
-            }
-            ++p_issued;
-        }
         if (ok) {  // thread d holds element d of the token rows m in [32 grp, 32 grp + 32);
                    // lanes 2i and 2i + 1 swap halves so that each stores bf16 pairs (d even,
                    // d + 1) of alternate tokens: even lanes tokens 2j, odd lanes 2j + 1.
@@ -398,6 +372,8 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             const int d = sub * 32 + lane, odd = lane & 1;
             const size_t ts = (size_t)a.HV * kDim;
             const size_t base = ((size_t)t0 * a.HV + hv) * kDim + (d & ~1) + (size_t)odd * ts;
+            const size_t hs = (size_t)a.H * kDim;
+            const size_t kbase = ((size_t)t0 * a.H + x.h) * kDim + (d & ~1) + (size_t)odd * hs;
     #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {  // 16 token columns at a time
                 const int m0 = j0 + 16 * hh;
@@ -421,68 +397,20 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                         const size_t o = base + (size_t)me * ts;
                         *reinterpret_cast<uint32_t *>(a.dv + o) = odd ? pack_bf2(rv, v1) : pack_bf2(v0, rv);
                     }
+                    if (last) {  // the key head's summed terms, bf16 pairs as dv
+                        const float rk = __shfl_xor_sync(0xffffffffu, odd ? acc[2 * jj] : acc[2 * jj + 1], 1);
+                        if (me + odd < L)
+                            *reinterpret_cast<uint32_t *>(a.dkpart2 + kbase + (size_t)me * hs) =
+                                odd ? pack_bf2(rk, acc[2 * jj + 1]) : pack_bf2(acc[2 * jj], rk);
+                    }
                 }
-                tmem_st16(t_row + cACC + m0, acc);
+                if (!last) tmem_st16(t_row + cACC + m0, acc);
             }
             tmem_st_wait();
         } else if (tid == 0 && a.status) {
             atomicOr(a.status, 2);
         }
         __syncthreads();
-        if (ok && last) {
-            const bool got = mbar_wait(&sm.p_bar, p_waited & 1);
-            ++p_waited;
-            ok = __syncthreads_and(got);
-        }
-        if (ok && last) {  // the key head's dk: its dkhat (these sums plus the h / dh' and
-                           // Q K^T terms the previous kernel summed), then the L2-norm
-                           // backward dk = (dkhat - khat (khat . dkhat)) / r_k
-            const int d = sub * 32 + lane, odd = lane & 1;
-            const size_t hs = (size_t)a.H * kDim;
-            const unsigned char *kcol = sm.k + (d >> 6) * kHalf;
-            const unsigned char *pcol = d >> 6 ? sm.op_bt : sm.op_b;
-            auto kval = [&](int m) {  // raw k of token m, feature d (bf16 K tile)
-                return bf2f(*reinterpret_cast<const bf16 *>(kcol + sw128_off(m, d & 63)));
-            };
-            float acc_dk[32];
-            tmem_ld32(t_row + cACC + j0, acc_dk);
-            tmem_ld_wait();
-    #pragma unroll
-            for (int i = 0; i < 32; ++i)  // dkhat of token j0 + i, feature d
-                acc_dk[i] += j0 + i < L ? bf2f(*reinterpret_cast<const bf16 *>(pcol + sw128_off(j0 + i, d & 63))) : 0.f;
-            // k . dkhat of token j0 + lane over this warp's 32 features: the first step of the
-            // transposed lane sum (epi::lanesum32) is taken here, on products formed as needed
-            float half16[16];
-            {
-                const bool hi = lane & 16;
-    #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float lo_p = kval(j0 + j) * acc_dk[j], hi_p = kval(j0 + 16 + j) * acc_dk[16 + j];
-                    half16[j] = (hi ? hi_p : lo_p) + __shfl_xor_sync(0xffffffffu, hi ? lo_p : hi_p, 16);
-                }
-            }
-            sm.dotp[grp][sub][lane] = epi::lanesum16(half16, lane);  // token j0 + lane, this warp's d
-            __syncthreads();
-            if (tid < 64)
-                sm.dot[tid] = ((sm.dotp[tid >> 5][0][tid & 31] + sm.dotp[tid >> 5][1][tid & 31]) +
-                               sm.dotp[tid >> 5][2][tid & 31]) + sm.dotp[tid >> 5][3][tid & 31];
-            __syncthreads();
-            const size_t obase = ((size_t)t0 * a.H + x.h) * kDim + (d & ~1) + (size_t)odd * hs;
-    #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                const int i0 = 2 * jj, me = j0 + i0;
-                const float r0 = sm.rki[me], r1 = sm.rki[me + 1];
-                const float k0 = r0 * (acc_dk[i0] - kval(me) * (r0 * r0 * sm.dot[me]));
-                const float k1 = r1 * (acc_dk[i0 + 1] - kval(me + 1) * (r1 * r1 * sm.dot[me + 1]));
-                const float rk = __shfl_xor_sync(0xffffffffu, odd ? k0 : k1, 1);
-                if (me + odd < L)
-                    *reinterpret_cast<uint32_t *>(a.dk + obase + (size_t)me * hs) =
-                        odd ? pack_bf2(rk, k1) : pack_bf2(k0, rk);
-            }
-            __syncthreads();  // every read of the K tile is done: the next unit's tiles may load
-            if (tid == 0 && has_next) issue_a(maps, sm, a, nx);
-            if (has_next) ++a_issued;
-        }
         if (ok && warp == 0) {  // dg = reverse cumulative sum of dG (warp scan), dbeta
             float dgv[2];
     #pragma unroll
@@ -533,7 +461,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving
         if (a_issued > waited) mbar_wait(&sm.a_bar, (a_issued - 1) & 1, kDrainLimitNs);
-        if (p_issued > 0) mbar_wait(&sm.p_bar, (p_issued - 1) & 1, kDrainLimitNs);
         if (v_issued > waited) mbar_wait(&sm.v_bar, (v_issued - 1) & 1, kDrainLimitNs);
     }
     tc_fence_before();
@@ -552,8 +479,7 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64) ||
-        !encode_rows_bf16(&m.dkp, a.dkpart, a.H, a.T, rowb, rowb * a.H, 64))
+        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BwSmem) + 1024;
     static_assert(2 * (sizeof(BwSmem) + 2048) <= 233472, "two CTAs per SM");

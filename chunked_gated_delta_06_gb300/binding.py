@@ -9,6 +9,7 @@ first call raises, telling the user to build it.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -72,49 +73,69 @@ def lib():
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError("libgdn.so not found at %s: build it with "
                                    "`python -m chunked_gated_delta_06_gb300.build`" % LIB_PATH)
-            L = ctypes.CDLL(LIB_PATH)
-            P = ctypes.POINTER(GdnProblem)
-            L.gdn_status_string.argtypes = [ctypes.c_int]
-            L.gdn_status_string.restype = ctypes.c_char_p
-            L.gdn_chunk_saved_bytes.argtypes = [P]
-            L.gdn_chunk_saved_bytes.restype = _sz
-            L.gdn_chunk_scan_plan.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
-            L.gdn_chunk_scan_plan.restype = ctypes.c_int
-            L.gdn_chunk_workspace_bytes.argtypes = [P, ctypes.c_int]
-            L.gdn_chunk_workspace_bytes.restype = _sz
-            L.gdn_chunk_fwd.argtypes = [P] + [_vp] * 10 + [_sz, _vp]
-            L.gdn_chunk_fwd.restype = ctypes.c_int
-            L.gdn_chunk_bwd.argtypes = [P] + [_vp] * 16 + [_sz, _vp]
-            L.gdn_chunk_bwd.restype = ctypes.c_int
-            L.gdn_decode_step.argtypes = ([ctypes.c_int32] * 5 + [ctypes.c_float] + [_vp] * 6
-                                          + [ctypes.c_int32] + [_vp] * 3 + [_vp])
-            L.gdn_decode_step.restype = ctypes.c_int
-            T = ctypes.POINTER(GdnKernelTimer)
-            L.gdn_chunk_fwd_timed.argtypes = [P] + [_vp] * 10 + [_sz, _vp, T]
-            L.gdn_chunk_fwd_timed.restype = ctypes.c_int
-            L.gdn_chunk_bwd_timed.argtypes = [P] + [_vp] * 16 + [_sz, _vp, T]
-            L.gdn_chunk_bwd_timed.restype = ctypes.c_int
-            L.gdn_decode_step_timed.argtypes = L.gdn_decode_step.argtypes + [T]
-            L.gdn_decode_step_timed.restype = ctypes.c_int
-            L.gdn_chunk_fwd_gated.argtypes = [P] + [_vp] * 12 + [_sz, _vp]
-            L.gdn_chunk_fwd_gated.restype = ctypes.c_int
-            L.gdn_chunk_bwd_gated.argtypes = [P] + [_vp] * 20 + [_sz, _vp]
-            L.gdn_chunk_bwd_gated.restype = ctypes.c_int
-            L.gdn_decode_step_gated.argtypes = ([ctypes.c_int32] * 5 + [ctypes.c_float] + [_vp] * 8
-                                                + [ctypes.c_int32] + [_vp] * 3 + [_vp])
-            L.gdn_decode_step_gated.restype = ctypes.c_int
-            L.gdn_chunk_prefill_paged.argtypes = [P] + [_vp] * 6 + [ctypes.c_int32] + [_vp] * 5 + [_sz, _vp]
-            L.gdn_chunk_prefill_paged.restype = ctypes.c_int
-            L.gdn_chunk_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
-            L.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
-            L.gdn_check_indices.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, _vp]
-            L.gdn_check_indices.restype = ctypes.c_int
-            L.gdn_selftest_bounded_wait.argtypes = [_vp, ctypes.c_uint64, _vp]
-            L.gdn_selftest_bounded_wait.restype = ctypes.c_int
-            L.gdn_kernel_name.argtypes = [ctypes.c_int32]
-            L.gdn_kernel_name.restype = ctypes.c_char_p
-            _lib = L
+            _lib = load_library(LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def use_library(path):
+    """Route every call of this module through another build of the library (the
+    bounds-checked libgdn_checked.so, say) inside the `with` block."""
+    global _lib
+    other = load_library(path)
+    with _lock:
+        saved, _lib = _lib, other
+    try:
+        yield other
+    finally:
+        with _lock:
+            _lib = saved
+
+
+def load_library(path):
+    """ctypes handle of a build of libgdn with every entry point's signature set."""
+    L = ctypes.CDLL(path)
+    P = ctypes.POINTER(GdnProblem)
+    L.gdn_status_string.argtypes = [ctypes.c_int]
+    L.gdn_status_string.restype = ctypes.c_char_p
+    L.gdn_chunk_saved_bytes.argtypes = [P]
+    L.gdn_chunk_saved_bytes.restype = _sz
+    L.gdn_chunk_scan_plan.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+    L.gdn_chunk_scan_plan.restype = ctypes.c_int
+    L.gdn_chunk_workspace_bytes.argtypes = [P, ctypes.c_int]
+    L.gdn_chunk_workspace_bytes.restype = _sz
+    L.gdn_chunk_fwd.argtypes = [P] + [_vp] * 10 + [_sz, _vp]
+    L.gdn_chunk_fwd.restype = ctypes.c_int
+    L.gdn_chunk_bwd.argtypes = [P] + [_vp] * 16 + [_sz, _vp]
+    L.gdn_chunk_bwd.restype = ctypes.c_int
+    L.gdn_decode_step.argtypes = ([ctypes.c_int32] * 5 + [ctypes.c_float] + [_vp] * 6
+                                  + [ctypes.c_int32] + [_vp] * 3 + [_vp])
+    L.gdn_decode_step.restype = ctypes.c_int
+    T = ctypes.POINTER(GdnKernelTimer)
+    L.gdn_chunk_fwd_timed.argtypes = [P] + [_vp] * 10 + [_sz, _vp, T]
+    L.gdn_chunk_fwd_timed.restype = ctypes.c_int
+    L.gdn_chunk_bwd_timed.argtypes = [P] + [_vp] * 16 + [_sz, _vp, T]
+    L.gdn_chunk_bwd_timed.restype = ctypes.c_int
+    L.gdn_decode_step_timed.argtypes = L.gdn_decode_step.argtypes + [T]
+    L.gdn_decode_step_timed.restype = ctypes.c_int
+    L.gdn_chunk_fwd_gated.argtypes = [P] + [_vp] * 12 + [_sz, _vp]
+    L.gdn_chunk_fwd_gated.restype = ctypes.c_int
+    L.gdn_chunk_bwd_gated.argtypes = [P] + [_vp] * 20 + [_sz, _vp]
+    L.gdn_chunk_bwd_gated.restype = ctypes.c_int
+    L.gdn_decode_step_gated.argtypes = ([ctypes.c_int32] * 5 + [ctypes.c_float] + [_vp] * 8
+                                        + [ctypes.c_int32] + [_vp] * 3 + [_vp])
+    L.gdn_decode_step_gated.restype = ctypes.c_int
+    L.gdn_chunk_prefill_paged.argtypes = [P] + [_vp] * 6 + [ctypes.c_int32] + [_vp] * 5 + [_sz, _vp]
+    L.gdn_chunk_prefill_paged.restype = ctypes.c_int
+    L.gdn_chunk_fwd_noalloc.argtypes = [P] + [_vp] * 8 + [_vp]
+    L.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
+    L.gdn_check_indices.argtypes = [_vp, ctypes.c_int32, ctypes.c_int32, _vp]
+    L.gdn_check_indices.restype = ctypes.c_int
+    L.gdn_selftest_bounded_wait.argtypes = [_vp, ctypes.c_uint64, _vp]
+    L.gdn_selftest_bounded_wait.restype = ctypes.c_int
+    L.gdn_kernel_name.argtypes = [ctypes.c_int32]
+    L.gdn_kernel_name.restype = ctypes.c_char_p
+    return L
 
 
 def header_functions() -> list[str]:
@@ -399,13 +420,13 @@ def decode_step(q, k, v, g, beta, state_pool, state_indices, scale=None, device_
 
 
 def chunk_fwd_gated(q, k, v, a, b, A_log, dt_bias, cu_host, cu_dev, scale=None, initial_state=None,
-                    output_final_state=True, for_backward=False, workspace=None):
+                    output_final_state=True, for_backward=False, workspace=None, device_status=None):
     """gdn_chunk_fwd_gated on torch tensors (g and beta from the fused gate).
     Returns (o, final_state or None, ctx); ctx feeds chunk_bwd_gated."""
     import torch
     T, H, K = q.shape
     HV = v.shape[1]
-    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale)
+    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale, device_status=device_status)
     p = ctx.problem
     dev = q.device
     o = torch.empty((T, HV, v.shape[2]), dtype=torch.bfloat16, device=dev)
@@ -468,14 +489,16 @@ def decode_step_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, 
 
 
 def chunk_prefill_paged(q, k, v, g, beta, cu_host, cu_dev, state_pool, state_indices,
-                        has_initial_state=None, scale=None, device_status=None, workspace=None):
+                        has_initial_state=None, scale=None, device_status=None, workspace=None,
+                        problem_status=None):
     """gdn_chunk_prefill_paged on torch tensors: sequence n starts from pool slot
     state_indices[n] (zeros when the slot is <= 0 or has_initial_state[n] == 0) and its
-    final state is written back to that slot in place.  Returns o."""
+    final state is written back to that slot in place.  Returns o.  device_status is the
+    call's slot-status word; problem_status the kernels' status word of gdn_problem."""
     import torch
     T, H, K = q.shape
     HV = v.shape[1]
-    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale, beta_dtype_of(beta))
+    ctx = ChunkContext(cu_host, cu_dev, H, HV, scale, beta_dtype_of(beta), device_status=problem_status)
     p = ctx.problem
     o = torch.empty((T, HV, v.shape[2]), dtype=torch.bfloat16, device=q.device)
     nws = gdn_chunk_workspace_bytes(p, 0)

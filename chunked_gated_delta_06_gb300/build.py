@@ -17,6 +17,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
+# the bounds-checked variant (-DGDN_CHECKED): every direct global access of the kernels
+# is range-checked; a violation sets bit 4 of the caller's status word and is skipped
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libgdn_checked.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,15 +45,18 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link; returns the path of libgdn.so.  Incremental on mtimes."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          checked: bool = False) -> str:
+    """Compile and link; returns the path of libgdn.so (or, with checked=True, of the
+    bounds-checked libgdn_checked.so).  Incremental on mtimes."""
+    bdir, lib_path = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     hdr = _headers_mtime()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + (["-DGDN_CHECKED"] if checked else []) + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         if (not force and os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(src)
                 and os.path.getmtime(obj) >= hdr):
             return obj, False
@@ -66,15 +73,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         results = list(ex.map(compile_one, srcs))
     objs = [o for o, _ in results]
     rebuilt = any(b for _, b in results)
-    if force or rebuilt or not os.path.exists(LIB):
-        tmp = LIB + ".tmp.%d" % os.getpid()
+    if force or rebuilt or not os.path.exists(lib_path):
+        tmp = lib_path + ".tmp.%d" % os.getpid()
         cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -82,8 +82,9 @@ __device__ __forceinline__ BwUnit bw_unit(const ChunkArgs &a, int u) {
     x.c = u / a.HV;
     x.hv = u - x.c * a.HV;
     x.h = x.hv / (a.HV / a.H);
-    x.t0 = a.chunk_start[x.c];
-    x.L = a.chunk_len[x.c];
+    const bool in = in_range(x.c, 1, a.num_chunks, a.status);
+    x.t0 = in ? a.chunk_start[x.c] : 0;
+    x.L = in ? a.chunk_len[x.c] : 0;
     return x;
 }
 // Unit u + 1 after unit x = u: the chunk table is read only when the chunk changes
@@ -156,7 +157,8 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     uint32_t pB = 0;   // raw beta bits, converted when published
     bool pin = false;
     auto fetch = [&](const BwUnit &y) {
-        pin = tid < 64 && tid < y.L;
+        pin = tid < 64 && tid < y.L &&
+              in_range((size_t)(y.t0 + tid) * a.HV + y.hv, 1, n_tok_hv(a), a.status);
         if (pin) {
             const size_t gi = (size_t)(y.t0 + tid) * a.HV + y.hv;
             pG = a.G[gi];
@@ -393,13 +395,13 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                     acc[2 * jj + 1] = (first ? 0.f : acc[2 * jj + 1]) + k1;
                     const float v0 = b0 * ut[2 * jj], v1 = b1 * ut[2 * jj + 1];
                     const float rv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-                    if (me + odd < L) {
+                    if (me + odd < L && in_range(base + (size_t)me * ts, 2, n_rows_hv(a), a.status)) {
                         const size_t o = base + (size_t)me * ts;
                         *reinterpret_cast<uint32_t *>(a.dv + o) = odd ? pack_bf2(rv, v1) : pack_bf2(v0, rv);
                     }
                     if (last) {  // the key head's summed terms, bf16 pairs as dv
                         const float rk = __shfl_xor_sync(0xffffffffu, odd ? acc[2 * jj] : acc[2 * jj + 1], 1);
-                        if (me + odd < L)
+                        if (me + odd < L && in_range(kbase + (size_t)me * hs, 2, n_rows_h(a), a.status))
                             *reinterpret_cast<uint32_t *>(a.dkpart2 + kbase + (size_t)me * hs) =
                                 odd ? pack_bf2(rk, acc[2 * jj + 1]) : pack_bf2(acc[2 * jj], rk);
                     }
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     #pragma unroll
             for (int z = 0; z < 2; ++z) {
                 const int m = 2 * lane + z;
-                if (m < L) {
+                if (m < L && in_range((size_t)(t0 + m) * a.HV + hv, 1, n_tok_hv(a), a.status)) {
                     const size_t gi = (size_t)(t0 + m) * a.HV + hv;
                     const float dgm = (z == 0 ? dgv[0] + dgv[1] : dgv[1]) + after;
                     store_dbeta(a, gi, sm.db[m], sm.beta[m]);
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             if (a.beta_mode == 2) {
                 pa = warp_sum(pa);
                 pd = warp_sum(pd);
-                if (lane == 0)
+                if (lane == 0 && in_range((size_t)c * a.HV + hv, 1, (long long)a.num_chunks * a.HV, a.status))
                     reinterpret_cast<float2 *>(a.gpart)[(size_t)c * a.HV + hv] = make_float2(pa, pd);
             }
         }

@@ -110,8 +110,9 @@ __device__ __forceinline__ Unit unit_of(const ChunkArgs &a, int u) {
     x.c = u / a.HV;
     x.hv = u - x.c * a.HV;
     x.h = x.hv / (a.HV / a.H);
-    x.t0 = a.chunk_start[x.c];
-    x.L = a.chunk_len[x.c];
+    const bool in = in_range(x.c, 1, a.num_chunks, a.status);
+    x.t0 = in ? a.chunk_start[x.c] : 0;
+    x.L = in ? a.chunk_len[x.c] : 0;
     return x;
 }
 // Unit u + 1 after unit x = u: the chunk table is read only when the chunk changes
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     // per-token scalars, fetched one unit ahead (threads 0..63)
     float pG = 0.f, pRq = 1.f, pRk = 1.f;
     auto fetch = [&](const Unit &y) {
-        if (tid < y.L && tid < 64) {
+        if (tid < y.L && tid < 64 && in_range((size_t)(y.t0 + tid) * a.HV + y.hv, 1, n_tok_hv(a), a.status)) {
             const size_t r = (size_t)(y.t0 + tid) * a.H + y.h;
             pG = a.G[(size_t)(y.t0 + tid) * a.HV + y.hv];
             pRq = a.rq[r];
@@ -344,8 +345,10 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                         put_pair(sm.stg + grp * kBox, ra, cl, -dw[cc][4 * k], -dw[cc][4 * k + 1]);
                         put_pair(sm.stg + grp * kBox, rb, cl, -dw[cc][4 * k + 2], -dw[cc][4 * k + 3]);
                     } else {
-                        if (la) *reinterpret_cast<uint32_t *>(a.dW + oa + col) = pack_bf2(-dw[cc][4 * k], -dw[cc][4 * k + 1]);
-                        if (lb) *reinterpret_cast<uint32_t *>(a.dW + ob + col) = pack_bf2(-dw[cc][4 * k + 2], -dw[cc][4 * k + 3]);
+                        if (la && in_range(oa + col, 2, n_rows_hv(a), a.status))
+                            *reinterpret_cast<uint32_t *>(a.dW + oa + col) = pack_bf2(-dw[cc][4 * k], -dw[cc][4 * k + 1]);
+                        if (lb && in_range(ob + col, 2, n_rows_hv(a), a.status))
+                            *reinterpret_cast<uint32_t *>(a.dW + ob + col) = pack_bf2(-dw[cc][4 * k + 2], -dw[cc][4 * k + 3]);
                     }
                 }
         }
@@ -459,11 +462,11 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                         put_pair(sm.stg + (c0 >> 6) * kBox, ra, col, ak[4 * k], ak[4 * k + 1]);
                         put_pair(sm.stg + (c0 >> 6) * kBox, rb, col, ak[4 * k + 2], ak[4 * k + 3]);
                     } else {
-                        if (la) {
+                        if (la && in_range(oa + gcol, 2, n_rows_h(a), a.status)) {
                             *reinterpret_cast<uint32_t *>(a.dq + oa + gcol) = pack_bf2(q0, q1);
                             *reinterpret_cast<uint32_t *>(a.dkpart + oa + gcol) = pack_bf2(ak[4 * k], ak[4 * k + 1]);
                         }
-                        if (lb) {
+                        if (lb && in_range(ob + gcol, 2, n_rows_h(a), a.status)) {
                             *reinterpret_cast<uint32_t *>(a.dq + ob + gcol) = pack_bf2(q2, q3);
                             *reinterpret_cast<uint32_t *>(a.dkpart + ob + gcol) = pack_bf2(ak[4 * k + 2], ak[4 * k + 3]);
                         }
@@ -502,7 +505,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
 #pragma unroll
             for (int z = 0; z < 2; ++z) {
                 const int tt = 2 * lane + z;
-                if (tt < L) {
+                if (tt < L && in_range((size_t)(x.t0 + tt) * a.HV + x.hv, 1, n_tok_hv(a), a.status)) {
                     const float extra = (tt == L - 1) ? sx + __expf(Gl) * hd : 0.f;
                     a.dGp[(size_t)(x.t0 + tt) * a.HV + x.hv] = dgz[z] + extra;
                 }

@@ -119,10 +119,13 @@ __global__ void __launch_bounds__(kThr, 2)
     const bool phi = pass == 1 && cbk >= 2;        // transition columns (pass 1 only)
     const int vb = cbk & 1;
     const int nsy = pass ? a.seg_max - 1 : 1;
+    if (!in_range(blockIdx.y / nsy, 1, a.N, a.status)) return;
     const int n = a.seq_order[blockIdx.y / nsy];   // longest sequences first
+    if (!in_range(n, 2, a.N + 1, a.status)) return;
     const int h = hv / (a.HV / a.H);
     const int cb = a.seq_chunk_off[n];
     const int ce = min(a.seq_chunk_off[n + 1], a.num_chunks);
+    if (ce > cb && !in_range(cb, ce - cb, a.num_chunks, a.status)) return;
     const int nseq = max(ce - cb, 0);
     const int S = pass ? max(1, (nseq + a.seg_len - 1) / a.seg_len) : 1;
     const int rho = pass == 2 ? blockIdx.y % nsy + 1 : (pass ? blockIdx.y % nsy : 0);
@@ -182,15 +185,16 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = (phi && kr == 64 * vb + c0 + j) ? 1.f : 0.f;
         } else if (!from_input) {
-            const float4 *src = reinterpret_cast<const float4 *>(
-                a.seg_start + (((size_t)n * (a.seg_max - 1) + rho - 1) * a.HV + hv) * kDim * kDim +
-                (size_t)kr * kDim + 64 * vb + c0);
+            const size_t off = (((size_t)n * (a.seg_max - 1) + rho - 1) * a.HV + hv) * kDim * kDim +
+                               (size_t)kr * kDim + 64 * vb + c0;
+            const float4 *src = reinterpret_cast<const float4 *>(a.seg_start + off);
+            const bool in = in_range(off, 32, (long long)a.N * (a.seg_max - 1) * a.HV * kDim * kDim, a.status);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const float4 x = src[q];
+                const float4 x = in ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
                 r[4 * q] = x.x; r[4 * q + 1] = x.y; r[4 * q + 2] = x.z; r[4 * q + 3] = x.w;
             }
-        } else if (a.d_ht) {
+        } else if (a.d_ht && in_range(sbase, 32, n_states(a), a.status)) {
             const float4 *src = reinterpret_cast<const float4 *>(a.d_ht + sbase);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -211,8 +215,9 @@ __global__ void __launch_bounds__(kThr, 2)
     bool pin = false;
     auto fetch = [&](int i) {
         const int tt0 = step_t0(i), LL = step_len(i);
-        pgl = a.G[(size_t)(tt0 + LL - 1) * a.HV + hv];
-        pin = tid < LL;
+        const size_t gl = (size_t)(tt0 + LL - 1) * a.HV + hv;
+        pgl = in_range(gl, 1, n_tok_hv(a), a.status) ? a.G[gl] : 0.f;
+        pin = tid < LL && in_range((size_t)(tt0 + tid) * a.HV + hv, 1, n_tok_hv(a), a.status);
         if (pin) {
             const size_t t = (size_t)(tt0 + tid);
             pg = a.G[t * a.HV + hv];
@@ -314,8 +319,10 @@ __global__ void __launch_bounds__(kThr, 2)
                 const float2 lb2 = phi ? make_float2(0.f, 0.f) : epi::get_pair(dls, rb, col);
                 const float va0 = la ? la2.x + ka * p[4 * k] : 0.f, va1 = la ? la2.y + ka * p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? lb2.x + kb * p[4 * k + 2] : 0.f, vb1 = lb ? lb2.y + kb * p[4 * k + 3] : 0.f;
-                if (la && !pre) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
-                if (lb && !pre) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                if (la && !pre && in_range(da + col - a.dvnew, 2, n_rows_hv(a), a.status))
+                    *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                if (lb && !pre && in_range(db + col - a.dvnew, 2, n_rows_hv(a), a.status))
+                    *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
                 epi::put_pair(sm.a_dv, ra, col, -va0, -va1);
                 epi::put_pair(sm.a_dv, rb, col, -vb0, -vb1);
             }
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(kThr, 2)
         egl = egl_next;
     }
     ok = __syncthreads_and(ok);
-    if (ok && to_final && a.dh0) {
+    if (ok && to_final && a.dh0 && in_range(sbase, 32, n_states(a), a.status)) {
         float r[32];
         tmem_ld32(tS, r);
         tmem_ld_wait();
@@ -368,7 +375,9 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
-    if (ok && pass == 1 && !to_final) {  // a segment's end state (dh columns, and Psi in a pre-scan)
+    if (ok && pass == 1 && !to_final &&
+        in_range(send - a.seg_end, 32, (long long)a.N * (a.seg_max - 1) * a.HV * kDim * 2 * kDim, a.status)) {
+        // a segment's end state (dh columns, and Psi in a pre-scan)
         float r[32];
         tmem_ld32(tS, r);
         tmem_ld_wait();

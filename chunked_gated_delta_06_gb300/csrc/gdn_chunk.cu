@@ -67,6 +67,7 @@ __global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunk
         seq_off[n] = base;
         const int L = cu[n + 1] - cu[n];
         for (int j = 0; j * kChunk < L; ++j) {
+            if (!in_range(base + j, 1, total_chunks, status)) break;
             chunk_start[base + j] = cu[n] + j * kChunk;
             chunk_len[base + j] = min(kChunk, L - j * kChunk);
         }
@@ -85,7 +86,7 @@ __global__ void k_plan(const int *__restrict__ cu, int N, int T, int total_chunk
                 rank += (Lm > Ln || (Lm == Ln && m < n)) ? 1 : 0;
             }
         }
-        seq_order[rank] = n;
+        if (in_range(rank, 1, N, status)) seq_order[rank] = n;
     }
 }
 
@@ -107,8 +108,10 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
         xq[m] = xk[m] = make_uint2(0u, 0u);
         if (i < L) {
             const size_t row = ((size_t)(t0 + i) * a.H + h) * kDim + lane * 4;
-            xq[m] = *reinterpret_cast<const uint2 *>(a.q + row);
-            xk[m] = *reinterpret_cast<const uint2 *>(a.k + row);
+            if (in_range(row, 4, n_rows_h(a), a.status)) {
+                xq[m] = *reinterpret_cast<const uint2 *>(a.q + row);
+                xk[m] = *reinterpret_cast<const uint2 *>(a.k + row);
+            }
         }
     }
 #pragma unroll
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
         float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
         sq = warp_sum(sq);
         sk = warp_sum(sk);
-        if (lane == 0 && i < L) {
+        if (lane == 0 && i < L && in_range((size_t)(t0 + i) * a.H + h, 1, n_tok_h(a), a.status)) {
             a.rq[(size_t)(t0 + i) * a.H + h] = sqrtf(sq + kNormEps);
             a.rk[(size_t)(t0 + i) * a.H + h] = sqrtf(sk + kNormEps);
         }
@@ -138,8 +141,10 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
             if (lane >= off) s += y;
         }
         float excl = s - (x0 + x1);
-        if (i0 < L) a.G[(size_t)(t0 + i0) * a.HV + hv] = excl + x0;
-        if (i1 < L) a.G[(size_t)(t0 + i1) * a.HV + hv] = excl + x0 + x1;
+        if (i0 < L && in_range((size_t)(t0 + i0) * a.HV + hv, 1, n_tok_hv(a), a.status))
+            a.G[(size_t)(t0 + i0) * a.HV + hv] = excl + x0;
+        if (i1 < L && in_range((size_t)(t0 + i1) * a.HV + hv, 1, n_tok_hv(a), a.status))
+            a.G[(size_t)(t0 + i1) * a.HV + hv] = excl + x0 + x1;
     }
 }
 
@@ -162,8 +167,9 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 __global__ void __launch_bounds__(kThreads) k_dknorm(ChunkArgs a) {
     const int l16 = threadIdx.x & 15;
     const size_t item = (size_t)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
-    const bool valid = item < (size_t)a.T * a.H;
-    const size_t row = (valid ? item : 0) * kDim + l16 * 8;  // item = t H + h
+    const size_t row0 = item * kDim + l16 * 8;  // item = t H + h
+    const bool valid = item < (size_t)a.T * a.H && in_range(row0, 8, n_rows_h(a), a.status);
+    const size_t row = valid ? row0 : 0;
     uint4 lk = make_uint4(0u, 0u, 0u, 0u), l1 = lk, l2 = lk;
     float rk = 1.f;
     if (valid) {
@@ -233,6 +239,7 @@ __global__ void k_gate_reduce(ChunkArgs a) {
     const float2 *part = reinterpret_cast<const float2 *>(a.gpart);
     double sa = 0.0, sd = 0.0;
     for (int c = lane; c < a.num_chunks; c += 32) {
+        if (!in_range(((size_t)c * a.HV + hv) * 2, 2, (long long)a.num_chunks * a.HV * 2, a.status)) break;
         const float2 p = part[(size_t)c * a.HV + hv];
         sa += p.x;
         sd += p.y;

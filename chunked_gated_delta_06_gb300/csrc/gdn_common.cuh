@@ -20,6 +20,23 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t x) {
 }
 __device__ __forceinline__ bf16 f2bf(float x) { return __float2bfloat16_rn(x); }
 
+// Bounds-checked builds (nvcc -DGDN_CHECKED): every direct global access of the
+// kernels first passes its element index range [i, i + w) and its buffer's extent n
+// to in_range().  A range outside [0, n) ORs GDN_DEVICE_INDEX_OUT_OF_RANGE (4) into
+// the caller's status word and the access is skipped (a load gives 0); nothing traps.
+// In the normal build in_range() is the constant true and the checks compile away.
+#ifdef GDN_CHECKED
+constexpr bool kChecked = true;
+__device__ __forceinline__ bool in_range(long long i, long long w, long long n, int *status) {
+    if (i >= 0 && w >= 0 && i + w <= n) return true;
+    if (status) atomicOr(status, 4);
+    return false;
+}
+#else
+constexpr bool kChecked = false;
+__device__ __forceinline__ bool in_range(long long, long long, long long, int *) { return true; }
+#endif
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

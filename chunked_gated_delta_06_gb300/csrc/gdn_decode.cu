@@ -48,6 +48,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         return;
     }
     const int h = hv / (HV / H);
+    if (!in_range(((size_t)slot * HV + hv) * kDim * kDim, kDim * kDim, (long long)num_slots * HV * kDim * kDim,
+                  status) ||
+        !in_range(((size_t)b * H + h) * kDim, kDim, (long long)(gridDim.x / HV) * H * kDim, status))
+        return;
     float *S = pool + ((size_t)slot * HV + hv) * kDim * kDim;
     const int r0 = warp * kRowsPerWarp;
     // issue the state loads first: 16 rows x float4 per lane

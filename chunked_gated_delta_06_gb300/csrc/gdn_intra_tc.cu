@@ -155,8 +155,9 @@ __device__ __forceinline__ IntraUnit intra_unit(const ChunkArgs &a, int u) {
     x.c = u / a.HV;
     x.hv = u - x.c * a.HV;
     x.h = x.hv / (a.HV / a.H);
-    x.t0 = a.chunk_start[x.c];
-    x.L = a.chunk_len[x.c];
+    const bool in = in_range(x.c, 1, a.num_chunks, a.status);
+    x.t0 = in ? a.chunk_start[x.c] : 0;
+    x.L = in ? a.chunk_len[x.c] : 0;
     return x;
 }
 
@@ -211,9 +212,14 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
         pin = tid < 64 && tid < y.L;
         if (pin) {
             const size_t gi = (size_t)(y.t0 + tid) * a.HV + y.hv;
-            pG = a.G[gi];
-            pB = load_beta_raw(a, gi);
-            pR = a.rk[(size_t)(y.t0 + tid) * a.H + y.h];
+            const size_t ri = (size_t)(y.t0 + tid) * a.H + y.h;
+            if (kChecked && !(in_range(gi, 1, n_tok_hv(a), a.status) && in_range(ri, 1, n_tok_h(a), a.status)))
+                pin = false;
+            else {
+                pG = a.G[gi];
+                pB = load_beta_raw(a, gi);
+                pR = a.rk[ri];
+            }
         }
     };
     fetch(x);
@@ -284,12 +290,14 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
         {  // operands T diag(c) as bf16 rows, and T to HBM: thread -> row tid / 2, 32 columns
             const int i = tid >> 1, j0 = 32 * (tid & 1);
             const float *Mi = sm.M + i * kS + j0;
-            uint4 *Tdst = reinterpret_cast<uint4 *>(a.Tm + (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0);
+            const size_t toff = (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0;
+            const bool t_in = in_range(toff, 32, (long long)a.num_chunks * a.HV * 64 * 64, a.status);
+            uint4 *Tdst = reinterpret_cast<uint4 *>(a.Tm + toff);
     #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float4 t0v = *reinterpret_cast<const float4 *>(Mi + 8 * q);
                 const float4 t1v = *reinterpret_cast<const float4 *>(Mi + 8 * q + 4);
-                Tdst[q] = make_uint4(pack_bf2(t0v.x, t0v.y), pack_bf2(t0v.z, t0v.w), pack_bf2(t1v.x, t1v.y),
+                if (t_in) Tdst[q] = make_uint4(pack_bf2(t0v.x, t0v.y), pack_bf2(t0v.z, t0v.w), pack_bf2(t1v.x, t1v.y),
                                      pack_bf2(t1v.z, t1v.w));
                 const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
                 const int jb = j0 + 8 * q;
@@ -333,10 +341,12 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    if (i < L) dst[(size_t)i * tstride] = __float2bfloat16_rn(x0[i]);
+                    if (i < L && in_range(base + (size_t)i * tstride, 1, n_rows_hv(a), a.status))
+                        dst[(size_t)i * tstride] = __float2bfloat16_rn(x0[i]);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    if (32 + i < L) dst[(size_t)(32 + i) * tstride] = __float2bfloat16_rn(x1[i]);
+                    if (32 + i < L && in_range(base + (size_t)(32 + i) * tstride, 1, n_rows_hv(a), a.status))
+                        dst[(size_t)(32 + i) * tstride] = __float2bfloat16_rn(x1[i]);
             }
         }
         tc_fence_before();

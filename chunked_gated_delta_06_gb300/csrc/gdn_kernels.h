@@ -75,14 +75,25 @@ struct ChunkArgs {
     gdn_kernel_timer *timer;  // optional per-kernel events
 };
 
+// Element extents of the buffers a chunk call touches (for in_range()).
+__device__ __forceinline__ long long n_tok_h(const ChunkArgs &a) { return (long long)a.T * a.H; }
+__device__ __forceinline__ long long n_tok_hv(const ChunkArgs &a) { return (long long)a.T * a.HV; }
+__device__ __forceinline__ long long n_rows_h(const ChunkArgs &a) { return (long long)a.T * a.H * kDim; }
+__device__ __forceinline__ long long n_rows_hv(const ChunkArgs &a) { return (long long)a.T * a.HV * kDim; }
+__device__ __forceinline__ long long n_states(const ChunkArgs &a) {
+    return (long long)a.N * a.HV * kDim * kDim;
+}
+
 // beta_i in the form the call gives it (a uniform branch per load).
 __device__ __forceinline__ float load_beta(const ChunkArgs &a, size_t i) {
+    if (!in_range(i, 1, n_tok_hv(a), a.status)) return 0.f;
     if (a.beta_mode == 2) return gate_sigmoid(bf2f(a.gb[i]));
     return a.beta_mode ? static_cast<const float *>(a.beta)[i] : bf2f(static_cast<const bf16 *>(a.beta)[i]);
 }
 // The same in two steps, so that a prefetch does not wait for its load: the raw bits
 // (fp32, or bf16 in the low half) now, the value when it is used.
 __device__ __forceinline__ uint32_t load_beta_raw(const ChunkArgs &a, size_t i) {
+    if (!in_range(i, 1, n_tok_hv(a), a.status)) return 0u;
     if (a.beta_mode == 1) return __float_as_uint(static_cast<const float *>(a.beta)[i]);
     const bf16 *p = a.beta_mode == 2 ? a.gb : static_cast<const bf16 *>(a.beta);
     return (uint32_t)__bfloat16_as_ushort(p[i]);
@@ -94,11 +105,13 @@ __device__ __forceinline__ float beta_from_raw(const ChunkArgs &a, uint32_t bits
 }
 // dbeta_i = x in beta's dtype; with fused gating db_i = x beta_i (1 - beta_i) (bf16).
 __device__ __forceinline__ void store_dbeta(const ChunkArgs &a, size_t i, float x, float beta) {
+    if (!in_range(i, 1, n_tok_hv(a), a.status)) return;
     if (a.beta_mode == 1) static_cast<float *>(a.dbeta)[i] = x;
     else static_cast<bf16 *>(a.dbeta)[i] = f2bf(a.beta_mode == 2 ? x * (beta * (1.f - beta)) : x);
 }
 // g_i: the input, or -exp(A_log) softplus(a + dt_bias) with fused gating.
 __device__ __forceinline__ float load_g(const ChunkArgs &a, size_t i, int hv) {
+    if (!in_range(i, 1, n_tok_hv(a), a.status) || !in_range(hv, 1, a.HV, a.status)) return 0.f;
     if (a.beta_mode != 2) return a.g[i];
     return -expf(a.A_log[hv]) * gate_softplus(bf2f(a.ga[i]) + a.dt_bias[hv]);
 }

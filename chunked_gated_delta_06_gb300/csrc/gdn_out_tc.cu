@@ -67,8 +67,9 @@ __device__ __forceinline__ OutUnit out_unit(const ChunkArgs &a, int u) {
     x.c = u / a.HV;
     x.hv = u - x.c * a.HV;
     x.h = x.hv / (a.HV / a.H);
-    x.t0 = a.chunk_start[x.c];
-    x.L = a.chunk_len[x.c];
+    const bool in = in_range(x.c, 1, a.num_chunks, a.status);
+    x.t0 = in ? a.chunk_start[x.c] : 0;
+    x.L = in ? a.chunk_len[x.c] : 0;
     return x;
 }
 // Unit u + 1 after unit x = u; the chunk table is read only when the chunk changes.
@@ -133,7 +134,8 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
     float pG = 0.f, pRq = 1.f, pRk = 1.f;
     bool pin = false;
     auto fetch = [&](const OutUnit &y) {
-        pin = tid < 64 && tid < y.L;
+        pin = tid < 64 && tid < y.L &&
+              in_range((size_t)(y.t0 + tid) * a.HV + y.hv, 1, n_tok_hv(a), a.status);
         if (pin) {
             const size_t r = (size_t)(y.t0 + tid) * a.H + y.h;
             pG = a.G[(size_t)(y.t0 + tid) * a.HV + y.hv];
@@ -269,8 +271,10 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
                         epi::put_pair(sm.stg + (c >> 1) * kBox, ra, v & 63, x0, x1);
                         epi::put_pair(sm.stg + (c >> 1) * kBox, rb, v & 63, y0, y1);
                     } else {
-                        if (la) *reinterpret_cast<uint32_t *>(da + v) = epi::pack_bf2(x0, x1);
-                        if (lb) *reinterpret_cast<uint32_t *>(db + v) = epi::pack_bf2(y0, y1);
+                        if (la && in_range(da + v - dst, 2, n_rows_hv(a), a.status))
+                            *reinterpret_cast<uint32_t *>(da + v) = epi::pack_bf2(x0, x1);
+                        if (lb && in_range(db + v - dst, 2, n_rows_hv(a), a.status))
+                            *reinterpret_cast<uint32_t *>(db + v) = epi::pack_bf2(y0, y1);
                     }
                 }
             }

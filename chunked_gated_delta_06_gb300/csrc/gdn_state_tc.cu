@@ -93,10 +93,13 @@ __global__ void __launch_bounds__(kThr, 2)
     const bool phi = pass == 1 && cbk >= 2;        // transition columns (pass 1 only)
     const int vb = cbk & 1;
     const int nsy = pass ? a.seg_max - 1 : 1;
+    if (!in_range(blockIdx.y / nsy, 1, a.N, a.status)) return;
     const int n = a.seq_order[blockIdx.y / nsy];   // longest sequences first
+    if (!in_range(n, 2, a.N + 1, a.status)) return;
     const int h = hv / (a.HV / a.H);
     const int cb = a.seq_chunk_off[n];
     const int ce = min(a.seq_chunk_off[n + 1], a.num_chunks);
+    if (ce > cb && !in_range(cb, ce - cb, a.num_chunks, a.status)) return;
     const int nseq = max(ce - cb, 0);              // chunks of the sequence
     const int S = pass ? max(1, (nseq + a.seg_len - 1) / a.seg_len) : 1;
     const int sg = pass == 2 ? blockIdx.y % nsy + 1 : (pass ? blockIdx.y % nsy : 0);
@@ -151,6 +154,9 @@ __global__ void __launch_bounds__(kThr, 2)
     }
     float *pslot = a.pool ? a.pool + (((size_t)slot * a.HV + hv) * kDim + 64 * vb + c0) * kDim + kr
                           : nullptr;  // S[v'][kr] of this thread's first column
+    auto pool_in = [&](const float *ps) {  // the 32 columns of S[.][kr] this thread reads / writes
+        return in_range(ps - a.pool, 31 * kDim + 1, (long long)a.num_slots * a.HV * kDim * kDim, a.status);
+    };
     // segment buffers: seg_end[n][s][hv][k][256] (h | Phi), seg_start[n][s-1][hv][k][128]
     const size_t seg_row = (size_t)kr * (2 * kDim) + (phi ? kDim : 0) + 64 * vb + c0;
     float *send = pass == 1 ? a.seg_end + (((size_t)n * (a.seg_max - 1) + sg) * a.HV + hv) * kDim * 2 * kDim +
@@ -162,18 +168,20 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = (phi && kr == 64 * vb + c0 + j) ? 1.f : 0.f;
         } else if (!from_input) {
-            const float4 *src = reinterpret_cast<const float4 *>(
-                a.seg_start + (((size_t)n * (a.seg_max - 1) + sg - 1) * a.HV + hv) * kDim * kDim +
-                (size_t)kr * kDim + 64 * vb + c0);
+            const size_t off = (((size_t)n * (a.seg_max - 1) + sg - 1) * a.HV + hv) * kDim * kDim +
+                               (size_t)kr * kDim + 64 * vb + c0;
+            const float4 *src = reinterpret_cast<const float4 *>(a.seg_start + off);
+            const bool in = in_range(off, 32, (long long)a.N * (a.seg_max - 1) * a.HV * kDim * kDim, a.status);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const float4 x = src[q];
+                const float4 x = in ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
                 r[4 * q] = x.x; r[4 * q + 1] = x.y; r[4 * q + 2] = x.z; r[4 * q + 3] = x.w;
             }
         } else if (a.pool) {
+            const bool in = !resume || pool_in(pslot);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = resume ? pslot[(size_t)j * kDim] : 0.f;
-        } else if (a.h0) {
+            for (int j = 0; j < 32; ++j) r[j] = resume && in ? pslot[(size_t)j * kDim] : 0.f;
+        } else if (a.h0 && in_range(sbase, 32, n_states(a), a.status)) {
             const float4 *src = reinterpret_cast<const float4 *>(a.h0 + sbase);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -194,8 +202,9 @@ __global__ void __launch_bounds__(kThr, 2)
     bool pin = false;
     auto fetch = [&](int j) {
         const int tt0 = chunk_t0(j), LL = chunk_len(j);
-        pgl = a.G[(size_t)(tt0 + LL - 1) * a.HV + hv];
-        pin = tid < LL;
+        const size_t gl = (size_t)(tt0 + LL - 1) * a.HV + hv;
+        pgl = in_range(gl, 1, n_tok_hv(a), a.status) ? a.G[gl] : 0.f;
+        pin = tid < LL && in_range((size_t)(tt0 + tid) * a.HV + hv, 1, n_tok_hv(a), a.status);
         if (pin) {
             const size_t t = (size_t)(tt0 + tid);
             pg = a.G[t * a.HV + hv];
@@ -276,8 +285,10 @@ __global__ void __launch_bounds__(kThr, 2)
                 const float2 ub = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, rb, col);
                 const float va0 = la ? ua.x - p[4 * k] : 0.f, va1 = la ? ua.y - p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? ub.x - p[4 * k + 2] : 0.f, vb1 = lb ? ub.y - p[4 * k + 3] : 0.f;
-                if (la && !pre) *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
-                if (lb && !pre) *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                if (la && !pre && in_range(da + col - a.vnew, 2, n_rows_hv(a), a.status))
+                    *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                if (lb && !pre && in_range(db + col - a.vnew, 2, n_rows_hv(a), a.status))
+                    *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
                 epi::put_pair(sm.a_v, ra, col, va0 * cfa, va1 * cfa);
                 epi::put_pair(sm.a_v, rb, col, vb0 * cfb, vb1 * cfb);
             }
@@ -308,7 +319,7 @@ __global__ void __launch_bounds__(kThr, 2)
         egl = egl_next;
     }
     ok = __syncthreads_and(ok);
-    if (ok && to_final && a.ht) {
+    if (ok && to_final && a.ht && in_range(sbase, 32, n_states(a), a.status)) {
         float r[32];
         tmem_ld32(tH, r);
         tmem_ld_wait();
@@ -316,14 +327,16 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
-    if (ok && to_final && a.pool && slot > 0) {  // final state back into the slot, transposed
+    if (ok && to_final && a.pool && slot > 0 && pool_in(pslot)) {  // final state back into the slot, transposed
         float r[32];
         tmem_ld32(tH, r);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) pslot[(size_t)j * kDim] = r[j];
     }
-    if (ok && pass == 1 && !to_final) {  // a segment's end state (h columns, and Phi in a pre-scan)
+    if (ok && pass == 1 && !to_final &&
+        in_range(send - a.seg_end, 32, (long long)a.N * (a.seg_max - 1) * a.HV * kDim * 2 * kDim, a.status)) {
+        // a segment's end state (h columns, and Phi in a pre-scan)
         float r[32];
         tmem_ld32(tH, r);
         tmem_ld_wait();
@@ -352,7 +365,7 @@ __global__ void __launch_bounds__(256) k_seg_stitch(const ChunkArgs a) {
     const int hv = blockIdx.x >> 3, v0 = 16 * (blockIdx.x & 7), n = blockIdx.y;
     const int nseq = max(0, min(a.seq_chunk_off[n + 1], a.num_chunks) - a.seq_chunk_off[n]);
     const int S = max(1, (nseq + a.seg_len - 1) / a.seg_len);
-    if (S < 2) return;
+    if (S < 2 || !in_range(S - 1, 1, a.seg_max, a.status)) return;
     __shared__ float H[kDim][16];
     const int t = threadIdx.x, k = t >> 1, cc = 8 * (t & 1);
     const size_t eh = (size_t)kDim * 2 * kDim;  // floats of one (segment, head) end record

@@ -24,6 +24,17 @@ def test_library_exports_every_declared_function(lib):
         assert hasattr(lib, n), n
 
 
+def test_bounds_checked_build_exports_the_same_functions():
+    # nvcc -DGDN_CHECKED: the same entry points; its kernels only add range checks
+    path = build.build(checked=True)
+    checked = binding.load_library(path)
+    for n in binding.header_functions():
+        assert hasattr(checked, n), n
+    p, keep = _problem([0, 5])
+    assert checked.gdn_chunk_workspace_bytes(ctypes.byref(p), 1) == binding.lib().gdn_chunk_workspace_bytes(
+        ctypes.byref(p), 1)
+
+
 def test_status_strings(lib):
     for s in range(5):
         assert gdn.status_string(s).startswith("GDN_")

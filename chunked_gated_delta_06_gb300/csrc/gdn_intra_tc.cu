@@ -4,8 +4,9 @@
 // 128 v7x", maxtext #5799).
 //
 // Persistent CTAs of 128 threads walking runs of (chunk, value head) units, sized
-// so that three share an SM (about 72 KB of shared memory and 128 TMEM columns
-// each): the pass is a chain of short dependent steps, and co-resident CTAs hide
+// so that four share an SM (about 55 KB of shared memory, the w / u operands
+// taking the bytes of the fp32 inverse once it is in registers, and 128 TMEM
+// columns each): the pass is a chain of short dependent steps, and co-resident CTAs hide
 // one another's latencies, while each CTA loads its next unit under its epilogue.  With Khat = diag(1 / r_k) K and Gamma_ij = exp(G_i - G_j):
 //   KK = K K^T                                   (tcgen05, M=64 N=64 K=128)
 // The M=64 KK result is read as 16x256b fragments (two rows, eight columns per lane).
@@ -18,6 +19,7 @@
 //                                                 and V tiles are read MN-major, so
 //                                                 row d of w^T / u^T is TMEM lane d)
 // w, u and T (kept for the backward) go to HBM in bf16.
+#include <stddef.h>
 #include <string.h>
 
 #include "gdn_epi.cuh"
@@ -39,9 +41,9 @@ constexpr int kXs = 36;                // fp32 row stride of the X scratch
 struct IntraSmem {
     unsigned char k[kTile];     // K rows [t][d] (TMA, SW128, two 64-column halves)
     unsigned char v[kTile];     // V rows [t][d]
-    unsigned char op_w[kHalf];  // T_ij beta_j e^{G_j} / r_k,j  [i][j] K-major
-    unsigned char op_u[kHalf];  // T_ij beta_j                  [i][j] K-major
-    float M[64 * kS];           // A (strictly lower, zeros elsewhere), then T in place
+    float M[64 * kS];           // A (strictly lower, zeros elsewhere), then T in place; once
+                                // every thread holds its slice of T, the same bytes hold the
+                                // w / u operands (op_w, op_u below)
     float X[32 * kXs];          // A21 T11 of the current merge level
     float G[64], beta[64], wc[64], rki[64];
     uint64_t ld_bar, mma_bar;
@@ -181,9 +183,9 @@ __device__ __forceinline__ void issue_kv(const IntraMaps &m, IntraSmem &sm, cons
 }
 
 // Persistent: CTA b walks the units [b per, (b + 1) per) (unit u = chunk u / HV, value
-// head u % HV), three CTAs per SM; the next unit's K and V tiles load as soon as the
+// head u % HV), four CTAs per SM; the next unit's K and V tiles load as soon as the
 // w / u products have read this unit's, and its per-token scalars a unit ahead.
-__global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
+__global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
                                                       const __grid_constant__ IntraMaps maps, int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     IntraSmem &sm = *reinterpret_cast<IntraSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -293,22 +295,28 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
             const size_t toff = (((size_t)c * a.HV + hv) * 64 + i) * 64 + j0;
             const bool t_in = in_range(toff, 32, (long long)a.num_chunks * a.HV * 64 * 64, a.status);
             uint4 *Tdst = reinterpret_cast<uint4 *>(a.Tm + toff);
+            float tv[32];
+    #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = *reinterpret_cast<const float4 *>(Mi + 4 * q);
+                tv[4 * q] = x.x; tv[4 * q + 1] = x.y; tv[4 * q + 2] = x.z; tv[4 * q + 3] = x.w;
+            }
+            __syncthreads();  // T is in registers: its bytes become the operands
+            unsigned char *op_w = reinterpret_cast<unsigned char *>(sm.M), *op_u = op_w + kHalf;
     #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 t0v = *reinterpret_cast<const float4 *>(Mi + 8 * q);
-                const float4 t1v = *reinterpret_cast<const float4 *>(Mi + 8 * q + 4);
-                if (t_in) Tdst[q] = make_uint4(pack_bf2(t0v.x, t0v.y), pack_bf2(t0v.z, t0v.w), pack_bf2(t1v.x, t1v.y),
-                                     pack_bf2(t1v.z, t1v.w));
-                const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+                const float *t8 = tv + 8 * q;
+                if (t_in) Tdst[q] = make_uint4(pack_bf2(t8[0], t8[1]), pack_bf2(t8[2], t8[3]), pack_bf2(t8[4], t8[5]),
+                                               pack_bf2(t8[6], t8[7]));
                 const int jb = j0 + 8 * q;
                 uint32_t pw[4], pu[4];
     #pragma unroll
                 for (int z = 0; z < 4; ++z) {
-                    pw[z] = pack_bf2(tv[2 * z] * sm.wc[jb + 2 * z], tv[2 * z + 1] * sm.wc[jb + 2 * z + 1]);
-                    pu[z] = pack_bf2(tv[2 * z] * sm.beta[jb + 2 * z], tv[2 * z + 1] * sm.beta[jb + 2 * z + 1]);
+                    pw[z] = pack_bf2(t8[2 * z] * sm.wc[jb + 2 * z], t8[2 * z + 1] * sm.wc[jb + 2 * z + 1]);
+                    pu[z] = pack_bf2(t8[2 * z] * sm.beta[jb + 2 * z], t8[2 * z + 1] * sm.beta[jb + 2 * z + 1]);
                 }
-                *reinterpret_cast<uint4 *>(sm.op_w + sw128_off(i, jb)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                *reinterpret_cast<uint4 *>(sm.op_u + sw128_off(i, jb)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+                *reinterpret_cast<uint4 *>(op_w + sw128_off(i, jb)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                *reinterpret_cast<uint4 *>(op_u + sw128_off(i, jb)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
             }
         }
         fence_proxy_async_smem();
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(kThr, 3) k_intra_tc(const ChunkArgs a,
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64, 1, 0);
             const uint32_t ks = smem_u32(sm.k), vs = smem_u32(sm.v);
-            const uint32_t ws = smem_u32(sm.op_w), us = smem_u32(sm.op_u);
+            const uint32_t ws = smem_u32(sm.M), us = ws + kHalf;  // op_w, op_u
             for (int s = 0; s < 4; ++s) {
                 mma_bf16(tb, sdesc(ks + s * 2048, kHalf, 1024), sdesc(ws + s * 32, 16, 1024), id, s > 0);
                 mma_bf16(tb + 64, sdesc(vs + s * 2048, kHalf, 1024), sdesc(us + s * 32, 16, 1024), id, s > 0);
@@ -374,14 +382,16 @@ cudaError_t launch_intra_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(IntraSmem) + 1024;
-    static_assert(3 * (sizeof(IntraSmem) + 2048) <= 233472, "three CTAs per SM");
+    static_assert(4 * (sizeof(IntraSmem) + 2048) <= 233472, "four CTAs per SM");
+    static_assert(offsetof(IntraSmem, M) % 1024 == 0 && sizeof(IntraSmem::M) >= 2 * kHalf,
+                  "the w / u operands fit, 1024-aligned, in the bytes of T");
     cudaError_t e = cudaFuncSetAttribute(k_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     int sms = 0;
     if ((e = sm_count(&sms)) != cudaSuccess) return e;
     const int nunits = a.num_chunks * a.HV;
-    const int per = (nunits + 3 * sms - 1) / (3 * sms);
+    const int per = (nunits + 4 * sms - 1) / (4 * sms);
     TimerScope ts(a.timer, GDN_KERNEL_INTRA, s);
     k_intra_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
     return cudaGetLastError();

@@ -512,7 +512,7 @@ def bench_ours(args):
     wl = W.CHUNK_CONFIGS[args.workload](seed=rank)
     T, H, HV, N = wl.T, wl.H, wl.HV, wl.N
     C_total = int(sum((int(wl.cu_seqlens[i + 1] - wl.cu_seqlens[i]) + C - 1) // C for i in range(N)))
-    run = ChunkRunner(torch, wl, dev)
+    run = ChunkRunner(torch, wl, dev, scan_segment_chunks=args.scan_segment_chunks)
 
     def barrier():
         if world > 1:
@@ -843,6 +843,9 @@ def main():
                     help="skip the timings of the other chunk workloads (256-token forward, "
                          "4x4096, 1x65536 with 64 value heads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scan-segment-chunks", type=int, default=0,
+                    help="gdn_problem.scan_segment_chunks of the timed workload: 0 = the library's "
+                         "plan, -1 = never split, L > 0 = segments of L chunks")
     ap.add_argument("--ref-tokens", type=int, default=2048,
                     help="tokens of the workload the oracle runs per baseline sample")
     args = ap.parse_args()

@@ -278,8 +278,26 @@ __global__ void __launch_bounds__(kThr, 2)
             mma_bf16(tbase + cY, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
                      sdesc(as_addr + s * 2048, kBox, 1024), idP, s > 0);
     };
+    // Z_j = w_j K_{j-1}^T into cZR (thread 0)
+    auto issue_z = [&](int j) {
+        const uint32_t ws = smem_u32(sm.wb[j & 1]), ks = smem_u32(sm.kb[(j - 1) & 1]);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint32_t off = (s >> 2) * kBox + (s & 3) * 32;
+            mma_bf16(tbase + cZR, sdesc(ws + off, 16, 1024), sdesc(ks + off, 16, 1024), idZ, s > 0);
+        }
+    };
     uint32_t phase = 0, zphase = 0;
     bool ok = true;
+    // thread 0 waits for K_j / w_j (loaded in chunk order) before the first product that
+    // reads them
+    int k_done = 0, w_done = 0;
+    auto need_k = [&](int j) {
+        for (; k_done <= j && ok; ++k_done) ok = mbar_wait(&sm.k_bar[k_done & 1], (k_done >> 1) & 1);
+    };
+    auto need_w = [&](int j) {
+        for (; w_done <= j && ok; ++w_done) ok = mbar_wait(&sm.w_bar[w_done & 1], (w_done >> 1) & 1);
+    };
     if (nch > 0) {  // prologue: Y_0 = w_0 bf16(h_0), so that P_0 = Y_0
         float r[32];
         h_to_bf16(r);
@@ -288,11 +306,18 @@ __global__ void __launch_bounds__(kThr, 2)
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            if (mbar_wait(&sm.w_bar[0], 0)) {
+            need_w(0);
+            if (ok) {
                 issue_y(0);
                 mma_commit(&sm.mma_bar);
-            } else {
-                ok = false;
+            }
+            if (nch > 1) {  // Z_1 = w_1 K_0^T
+                need_k(0);
+                need_w(1);
+                if (ok) {
+                    issue_z(1);
+                    mma_commit(&sm.z_bar);
+                }
             }
         }
     }
@@ -314,18 +339,6 @@ __global__ void __launch_bounds__(kThr, 2)
             if (i + 2 < nch) {
                 issue_w(maps, sm, i & 1, chunk_t0(i + 2), hv);
                 ++w_issued;
-            }
-            // K_i (for the update and Z_{i+1}) and w_{i+1}
-            ok = mbar_wait(&sm.k_bar[i & 1], (i >> 1) & 1);
-            if (ok && has_next) ok = mbar_wait(&sm.w_bar[(i + 1) & 1], ((i + 1) >> 1) & 1);
-            if (ok && has_next) {  // Z_{i+1} = w_{i+1} K_i^T into cZR
-                const uint32_t ws = smem_u32(sm.wb[(i + 1) & 1]), ks = smem_u32(sm.kb[i & 1]);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = (s >> 2) * kBox + (s & 3) * 32;
-                    mma_bf16(tbase + cZR, sdesc(ws + off, 16, 1024), sdesc(ks + off, 16, 1024), idZ, s > 0);
-                }
-                mma_commit(&sm.z_bar);
             }
         }
         if (has_next && !phi) ++u_issued;
@@ -399,6 +412,8 @@ __global__ void __launch_bounds__(kThr, 2)
         // (D) the group: h += K_i^T A_V_i; Y_{i+1} = w_{i+1} bf16(h_i); ZA_{i+1} = Z_{i+1} A_V_i
         if (tid == 0) {
             tc_fence_after();
+            need_k(i);
+            if (has_next) need_w(i + 1);
             const uint32_t av = smem_u32(sm.ub[i & 1]), ks = smem_u32(sm.kb[i & 1]);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
@@ -415,6 +430,14 @@ __global__ void __launch_bounds__(kThr, 2)
             if (!pre) {
                 tma_store_3d(&maps.hc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_s);  // h_c rows (k)
                 tma_store_commit();
+            }
+            if (i + 2 < nch) {  // Z_{i+2} = w_{i+2} K_{i+1}^T, needed a step later (own barrier)
+                need_k(i + 1);
+                need_w(i + 2);
+                if (ok) {
+                    issue_z(i + 2);
+                    mma_commit(&sm.z_bar);
+                }
             }
             tma_store_wait_read();  // a_s may be rewritten once the store has read it
             mbar_arrive(&sm.as_bar);

@@ -7,36 +7,25 @@
 // (sequence, value head, value half): h[k][v'] for the 64 columns v' = 64 vb ..
 // 64 vb + 63, as an fp32 accumulator in TMEM (lane k, 64 columns); its 256
 // threads are two warpgroups that split the columns of every pass.
-// Per chunk j (L <= 64 tokens from t0, G the chunk-local cumsum of g, G_L its last
-// value), with Khat = diag(1 / r_k) K:
-//   P_j = w_j h_j,  v_new_j = u_j - P_j,  A_V_j = v_new_j e^{G_L - G_t} / r_k,t,
-//   h_{j+1} = e^{G_L,j} h_j + K_j^T A_V_j      (= e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new)
-// P_{j+1} is formed without waiting for h_{j+1}: since
-//   P_{j+1} = w_{j+1} h_{j+1} = e^{G_L,j} (w_{j+1} h_j) + (w_{j+1} K_j^T) A_V_j,
-// the products Y_{j+1} = w_{j+1} bf16(h_j) and ZA_{j+1} = bf16(w_{j+1} K_j^T) A_V_j are
-// issued together with the state update, in one group of tensor-core products per
-// chunk, and the small matrix Z_{j+1} = w_{j+1} K_j^T (64 x 64, inputs only) is formed
-// a step ahead.  A chunk step is then:
-//   (A) wait for the previous group; load K_{j+1}, w_{j+2}, u_{j+1} by TMA; issue
-//       Z_{j+1} (tcgen05, M=64 N=64 K=128);
-//   (B) thread k writes row k of h_j as bf16 to shared memory (the B operand of
-//       Y_{j+1}; one TMA store copies it to h_c[chunk][hv][k][v']) and e^{G_L} h_j back
-//       to TMEM; on 16x256b fragments (two token rows, eight columns per lane)
-//       P_j = e^{G_L,j-1} Y_j + ZA_j, v_new_j = u_j - P_j goes to HBM (bf16) and A_V_j
-//       to shared memory (over u_j's tile); Z_{j+1} goes to shared memory as bf16;
-//   (C) one block barrier;
-//   (D) one thread issues h += K_j^T A_V_j (M=128 N=64 K=64, the raw key tile read
-//       MN-major), Y_{j+1} (M=64 N=64 K=128) and ZA_{j+1} (M=64 N=64 K=64), and the
-//       TMA store of h_c.
-// So a chunk costs one round trip through the tensor cores and one block barrier.
-// K is loaded a chunk ahead and w two chunks ahead (both double-buffered), the
-// next chunk's per-token scalars a chunk ahead; two CTAs share an SM (about 105 KB
-// of shared memory and 256 TMEM columns each).  Every wait is bounded; a timeout
-// sets status bit 2 and the CTA unwinds.  In paged-prefill mode the initial state
-// comes from, and the final state goes back to, a slot of the decode state pool
-// [slots, HV, V, K] (the layout "Replace Qwen3.5 FLA paths with Attention Gym"
-// keeps shared between prefill and decode), read and written transposed in place.
-#include <stddef.h>
+// Per chunk (L <= 64 tokens from t0, G the chunk-local cumsum of g, G_L its last
+// value):
+//   1. thread k writes row k of h as bf16 to shared memory (MMA operand; one TMA
+//      store copies it to h_c[chunk][hv][k][v']), and e^{G_L} h back to TMEM;
+//   2. P[t][v'] = sum_k w[t][k] h[k][v']          (tcgen05, M=64 N=64 K=128)
+//   3. the result is read as 16x256b fragments (two token rows and eight columns
+//      per lane); v_new[t][v'] = u - P goes to HBM (bf16), and
+//      A_V[t][v'] = v_new e^{G_L - G_t} / r_k,t to shared memory (bf16);
+//   4. h[k][v'] += sum_t K[t][k] A_V[t][v']        (tcgen05, M=128 N=64 K=64; the
+//      raw key tile is read MN-major)
+// which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with Khat =
+// diag(1 / r_k) K.  w, K and this half of u stream in by TMA two chunks ahead,
+// the next chunk's per-token scalars are loaded a chunk ahead and published
+// during the current epilogue, and a chunk costs two block barriers.  Two CTAs
+// share an SM.  Every wait is bounded; a timeout sets status bit 2 and the CTA
+// unwinds.  In paged-prefill mode the initial state comes from, and the final
+// state goes back to, a slot of the decode state pool [slots, HV, V, K] (the
+// layout "Replace Qwen3.5 FLA paths with Attention Gym" keeps shared between
+// prefill and decode), read and written transposed in place.
 #include <string.h>
 
 #include "gdn_epi.cuh"
@@ -51,20 +40,16 @@ using namespace umma;
 
 constexpr int kThr = 256;
 constexpr uint32_t kBox = 64 * 128;             // one 64-row x 128-byte SW128 box
-
-// TMEM columns (256 allocated): the state (M = 128, lane k) and three M = 64 results
-constexpr uint32_t cH = 0, cY = 64, cZA = 128, cZR = 192;
+constexpr uint32_t kStageBytes = 5 * kBox;      // w (2 boxes), K (2), u half (1)
 
 struct StateSmem {
     // 1024-byte aligned operand tiles first
-    unsigned char a_s[128 * 128];       // bf16 h_j [k][v']: 128 rows x 128 B
-    unsigned char kb[2][2 * kBox];      // K_j [t][k] (two 64-column boxes), j = chunk & 1
-    unsigned char wb[2][2 * kBox];      // w_j [t][k]
-    unsigned char ub[2][kBox];          // this half of u_j [t][v'], then A_V_j in place
-    unsigned char z_s[kBox];            // bf16 Z_{j+1} = w_{j+1} K_j^T [t][t']
+    unsigned char a_s[128 * 128];       // h bf16 [k][v']: 128 rows x 128 B
+    unsigned char a_v[64 * 128];        // A_V bf16 [t][v']: 64 rows x 128 B
+    unsigned char stage[2][kStageBytes];
     float coef[2][64];                  // e^{G_L - G_t} / r_k,t, 0 past L (this and the next chunk)
-    uint64_t k_bar[2], w_bar[2], u_bar[2];
-    uint64_t mma_bar, z_bar, as_bar;    // product group; Z product; a_s read by the h_c store
+    uint64_t tma_bar[2];
+    uint64_t mma_bar;
     uint32_t tmem_base;
 };
 
@@ -72,19 +57,16 @@ struct StateMaps {
     CUtensorMap w, k, u, hc;
 };
 
-__device__ __forceinline__ void issue_k(const StateMaps &m, StateSmem &sm, int b, int t0, int h) {
-    mbar_arrive_expect_tx(&sm.k_bar[b], 2 * kBox);
-    tma_load_3d(sm.kb[b], &m.k, 0, h, t0, &sm.k_bar[b]);
-    tma_load_3d(sm.kb[b] + kBox, &m.k, 64, h, t0, &sm.k_bar[b]);
-}
-__device__ __forceinline__ void issue_w(const StateMaps &m, StateSmem &sm, int b, int t0, int hv) {
-    mbar_arrive_expect_tx(&sm.w_bar[b], 2 * kBox);
-    tma_load_3d(sm.wb[b], &m.w, 0, hv, t0, &sm.w_bar[b]);
-    tma_load_3d(sm.wb[b] + kBox, &m.w, 64, hv, t0, &sm.w_bar[b]);
-}
-__device__ __forceinline__ void issue_u(const StateMaps &m, StateSmem &sm, int b, int t0, int hv, int vb) {
-    mbar_arrive_expect_tx(&sm.u_bar[b], kBox);
-    tma_load_3d(sm.ub[b], &m.u, 64 * vb, hv, t0, &sm.u_bar[b]);
+// w, K and (unless the columns are a transition's, whose u is zero) this half of u
+__device__ __forceinline__ void issue_stage(const StateMaps &m, StateSmem &sm, int st, int t0, int h,
+                                            int hv, int vb, bool with_u) {
+    unsigned char *b = sm.stage[st];
+    mbar_arrive_expect_tx(&sm.tma_bar[st], with_u ? kStageBytes : kStageBytes - kBox);
+    tma_load_3d(b + 0 * kBox, &m.w, 0, hv, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 1 * kBox, &m.w, 64, hv, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 2 * kBox, &m.k, 0, h, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 3 * kBox, &m.k, 64, h, t0, &sm.tma_bar[st]);
+    if (with_u) tma_load_3d(b + 4 * kBox, &m.u, 64 * vb, hv, t0, &sm.tma_bar[st]);
 }
 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -138,18 +120,13 @@ __global__ void __launch_bounds__(kThr, 2)
     auto chunk_len = [&](int j) { return min(64, ts1 - chunk_t0(j)); };
 
     if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 256);
+        tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.k_bar[b], 1);
-            mbar_init(&sm.w_bar[b], 1);
-            mbar_init(&sm.u_bar[b], 1);
-        }
+        mbar_init(&sm.tma_bar[0], 1);
+        mbar_init(&sm.tma_bar[1], 1);
         mbar_init(&sm.mma_bar, 1);
-        mbar_init(&sm.z_bar, 1);
-        mbar_init(&sm.as_bar, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -157,22 +134,10 @@ __global__ void __launch_bounds__(kThr, 2)
     tc_fence_after();
     const uint32_t tbase = sm.tmem_base;
     const uint32_t t_row = tbase + ((uint32_t)(sub * 32) << 16);  // this warp's lanes
-    const uint32_t tH = t_row + cH + c0;                           // this warpgroup's columns
-    const uint32_t tY = t_row + cY + c0, tZA = t_row + cZA + c0, tZR = t_row + cZR + c0;
+    const uint32_t tH = t_row + c0, tP = t_row + 64 + c0;          // this warpgroup's columns
 
-    // loads in flight, counted by thread 0 (K, w) and by everyone (u)
-    int k_issued = 0, w_issued = 0, u_issued = 0;
-    if (tid == 0 && nch > 0) {  // K_0, w_0, w_1 and u_0
-        issue_k(maps, sm, 0, chunk_t0(0), h);
-        issue_w(maps, sm, 0, chunk_t0(0), hv);
-        k_issued = w_issued = 1;
-        if (nch > 1) {
-            issue_w(maps, sm, 1, chunk_t0(1), hv);
-            w_issued = 2;
-        }
-        if (!phi) issue_u(maps, sm, 0, chunk_t0(0), hv, vb);
-    }
-    if (nch > 0 && !phi) u_issued = 1;
+    if (tid == 0)
+        for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, i, chunk_t0(i), h, hv, vb, !phi);
     // h <- h0[n][hv][k][v'] (row kr, this warpgroup's 32 columns), or in paged mode
     // the transpose of pool slot S[v'][k] (lanes are consecutive k: coalesced per v')
     const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb + c0;
@@ -250,205 +215,108 @@ __global__ void __launch_bounds__(kThr, 2)
         if (tid < 64) sm.coef[buf][tid] = pin ? __expf(fminf(pgl - pg, 0.f)) / prk : 0.f;
         return __expf(pgl);
     };
-    float egl = 1.f;   // e^{G_L} of the current chunk
+    float egl = 1.f;
     if (nch > 0) {
         fetch(0);
         egl = publish(0);
         if (nch > 1) fetch(1);
     }
-    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // Y = w h_bf16, ZA = Z A_V (B MN-major)
-    const uint32_t idZ = idesc_bf16(64, 64, 0, 0);    // Z = w K^T           (both K-major)
-    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // h += K^T A_V        (both MN-major)
-    const uint32_t as_addr = smem_u32(sm.a_s);
-    // row kr of h as bf16 into a_s (this warpgroup's 32 columns); returns the values
-    auto h_to_bf16 = [&](float (&r)[32]) {
-        tmem_ld32(tH, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4 *>(sm.a_s + sw128_off(kr, c0 + 8 * q)) =
-                make_uint4(pack_bf2(r[8 * q], r[8 * q + 1]), pack_bf2(r[8 * q + 2], r[8 * q + 3]),
-                           pack_bf2(r[8 * q + 4], r[8 * q + 5]), pack_bf2(r[8 * q + 6], r[8 * q + 7]));
-    };
-    // Y = w_j a_s into cY (thread 0)
-    auto issue_y = [&](int j) {
-        const uint32_t ws = smem_u32(sm.wb[j & 1]);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-            mma_bf16(tbase + cY, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
-                     sdesc(as_addr + s * 2048, kBox, 1024), idP, s > 0);
-    };
-    // Z_j = w_j K_{j-1}^T into cZR (thread 0)
-    auto issue_z = [&](int j) {
-        const uint32_t ws = smem_u32(sm.wb[j & 1]), ks = smem_u32(sm.kb[(j - 1) & 1]);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint32_t off = (s >> 2) * kBox + (s & 3) * 32;
-            mma_bf16(tbase + cZR, sdesc(ws + off, 16, 1024), sdesc(ks + off, 16, 1024), idZ, s > 0);
-        }
-    };
-    uint32_t phase = 0, zphase = 0;
+    __syncthreads();
+    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // P = w h       (h MN-major)
+    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // h += K^T A_V  (both MN-major)
+    uint32_t phase = 0;
     bool ok = true;
-    // thread 0 waits for K_j / w_j (loaded in chunk order) before the first product that
-    // reads them
-    int k_done = 0, w_done = 0;
-    auto need_k = [&](int j) {
-        for (; k_done <= j && ok; ++k_done) ok = mbar_wait(&sm.k_bar[k_done & 1], (k_done >> 1) & 1);
-    };
-    auto need_w = [&](int j) {
-        for (; w_done <= j && ok; ++w_done) ok = mbar_wait(&sm.w_bar[w_done & 1], (w_done >> 1) & 1);
-    };
-    if (nch > 0) {  // prologue: Y_0 = w_0 bf16(h_0), so that P_0 = Y_0
-        float r[32];
-        h_to_bf16(r);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            need_w(0);
-            if (ok) {
-                issue_y(0);
-                mma_commit(&sm.mma_bar);
-            }
-            if (nch > 1) {  // Z_1 = w_1 K_0^T
-                need_k(0);
-                need_w(1);
-                if (ok) {
-                    issue_z(1);
-                    mma_commit(&sm.z_bar);
-                }
-            }
-        }
-    }
-    float eprev = 1.f;  // e^{G_L} of the chunk before (P_j = eprev Y_j + ZA_j)
     for (int i = 0; i < nch; ++i) {
-        const int c = cb + jb + i;
+        const int c = cb + jb + i, st = i & 1;
         const int t0 = chunk_t0(i), L = chunk_len(i);
-        const bool has_next = i + 1 < nch;
-        // (A) the previous group: h_i, Y_i, ZA_i are in TMEM and its operands are free
-        ok = mbar_wait(&sm.mma_bar, phase) && ok;
-        phase ^= 1;
-        tc_fence_after();
-        if (tid == 0 && ok) {
-            if (has_next) {
-                issue_k(maps, sm, (i + 1) & 1, chunk_t0(i + 1), h);
-                ++k_issued;
-                if (!phi) issue_u(maps, sm, (i + 1) & 1, chunk_t0(i + 1), hv, vb);
-            }
-            if (i + 2 < nch) {
-                issue_w(maps, sm, i & 1, chunk_t0(i + 2), hv);
-                ++w_issued;
-            }
-        }
-        if (has_next && !phi) ++u_issued;
-        // (B) h_i -> bf16 operand (once the h_c store of the chunk before has read a_s),
-        //     then h <- e^{G_L} h_i
-        if (i > 0) ok = mbar_wait(&sm.as_bar, (i - 1) & 1) && ok;
+        // 1. h -> bf16 operand (copied to h_c by TMA below), then h <- e^{G_L} h
         {
             float r[32];
-            h_to_bf16(r);
+            tmem_ld32(tH, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(sm.a_s + sw128_off(kr, c0 + 8 * q)) =
+                    make_uint4(pack_bf2(r[8 * q], r[8 * q + 1]), pack_bf2(r[8 * q + 2], r[8 * q + 3]),
+                               pack_bf2(r[8 * q + 4], r[8 * q + 5]), pack_bf2(r[8 * q + 6], r[8 * q + 7]));
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] *= egl;
             tmem_st32(tH, r);
+            tmem_st_wait();
         }
-        //     P_i = eprev Y_i + ZA_i on 16x256b fragments: rows ra, ra + 8, this
-        //     warpgroup's columns c0 + 8k + cq + {0, 1}; v_new = u - P to HBM, A_V over u
-        if (!phi) ok = mbar_wait(&sm.u_bar[i & 1], (i >> 1) & 1) && ok;
-        {
-            float yv[16], zv[16];
-            epi::tmem_ld16x256_x4(tY, yv);
-            if (i > 0) epi::tmem_ld16x256_x4(tZA, zv);
-            tmem_ld_wait();
-            const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
-            const bool la = ra < L, lb = rb < L;
-            const float cfa = sm.coef[i & 1][ra], cfb = sm.coef[i & 1][rb];
-            unsigned char *us = sm.ub[i & 1];
-            bf16 *da = a.vnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
-            bf16 *db = a.vnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int col = c0 + 8 * k + cq;
-                float p[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) p[e] = i > 0 ? eprev * yv[4 * k + e] + zv[4 * k + e] : yv[4 * k + e];
-                const float2 ua = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, ra, col);
-                const float2 ub = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, rb, col);
-                const float va0 = la ? ua.x - p[0] : 0.f, va1 = la ? ua.y - p[1] : 0.f;
-                const float vb0 = lb ? ub.x - p[2] : 0.f, vb1 = lb ? ub.y - p[3] : 0.f;
-                if (la && !pre && in_range(da + col - a.vnew, 2, n_rows_hv(a), a.status))
-                    *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
-                if (lb && !pre && in_range(db + col - a.vnew, 2, n_rows_hv(a), a.status))
-                    *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
-                epi::put_pair(us, ra, col, va0 * cfa, va1 * cfa);
-                epi::put_pair(us, rb, col, vb0 * cfb, vb1 * cfb);
-            }
-        }
-        float egl_next = egl;
-        if (has_next) {  // publish the next chunk's scalars, and fetch one chunk further
-            egl_next = publish((i + 1) & 1);
-            if (i + 2 < nch) fetch(i + 2);
-            //  Z_{i+1} -> bf16 operand [t][t'] (same fragment positions)
-            ok = mbar_wait(&sm.z_bar, zphase) && ok;
-            zphase ^= 1;
-            tc_fence_after();
-            float zr[16];
-            epi::tmem_ld16x256_x4(tZR, zr);
-            tmem_ld_wait();
-            const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int col = c0 + 8 * k + cq;
-                epi::put_pair(sm.z_s, ra, col, zr[4 * k], zr[4 * k + 1]);
-                epi::put_pair(sm.z_s, rb, col, zr[4 * k + 2], zr[4 * k + 3]);
-            }
-        }
-        tmem_st_wait();
-        // (C) one barrier: a_s, A_V, Z and the rescaled state are in place
         fence_proxy_async_smem();
         tc_fence_before();
-        ok = __syncthreads_and(ok);
+        const bool got = mbar_wait(&sm.tma_bar[st], (i >> 1) & 1);  // u is read below by everyone
+        ok = __syncthreads_and(ok && got);
         if (!ok) break;
-        // (D) the group: h += K_i^T A_V_i; Y_{i+1} = w_{i+1} bf16(h_i); ZA_{i+1} = Z_{i+1} A_V_i
+        // 2. P = w h
         if (tid == 0) {
             tc_fence_after();
-            need_k(i);
-            if (has_next) need_w(i + 1);
-            const uint32_t av = smem_u32(sm.ub[i & 1]), ks = smem_u32(sm.kb[i & 1]);
+            const uint32_t as = smem_u32(sm.a_s), ws = smem_u32(sm.stage[st]);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase + cH, sdesc(ks + s * 2048, kBox, 1024), sdesc(av + s * 2048, kBox, 1024), idS, true);
-            if (has_next) {
-                issue_y(i + 1);
-                const uint32_t zs = smem_u32(sm.z_s);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tbase + cZA, sdesc(zs + s * 32, 16, 1024), sdesc(av + s * 2048, kBox, 1024), idP,
-                             s > 0);
-            }
+            for (int s = 0; s < 8; ++s)
+                mma_bf16(tbase + 64, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
+                         sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
             mma_commit(&sm.mma_bar);
             if (!pre) {
                 tma_store_3d(&maps.hc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_s);  // h_c rows (k)
                 tma_store_commit();
             }
-            if (i + 2 < nch) {  // Z_{i+2} = w_{i+2} K_{i+1}^T, needed a step later (own barrier)
-                need_k(i + 1);
-                need_w(i + 2);
-                if (ok) {
-                    issue_z(i + 2);
-                    mma_commit(&sm.z_bar);
-                }
-            }
-            tma_store_wait_read();  // a_s may be rewritten once the store has read it
-            mbar_arrive(&sm.as_bar);
         }
-        eprev = egl;
-        egl = egl_next;
-    }
-    if (ok && nch > 0) {  // the last update
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
+        // 3. v_new = u - P on 16x256b fragments: rows ra, ra + 8, this warpgroup's
+        //    columns c0 + 8k + cq + {0, 1}
+        {
+            float p[16];
+            epi::tmem_ld16x256_x4(tP, p);
+            tmem_ld_wait();
+            const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+            const bool la = ra < L, lb = rb < L;
+            const float cfa = sm.coef[i & 1][ra], cfb = sm.coef[i & 1][rb];
+            const unsigned char *us = sm.stage[st] + 4 * kBox;
+            bf16 *da = a.vnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
+            bf16 *db = a.vnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int col = c0 + 8 * k + cq;
+                const float2 ua = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, ra, col);
+                const float2 ub = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, rb, col);
+                const float va0 = la ? ua.x - p[4 * k] : 0.f, va1 = la ? ua.y - p[4 * k + 1] : 0.f;
+                const float vb0 = lb ? ub.x - p[4 * k + 2] : 0.f, vb1 = lb ? ub.y - p[4 * k + 3] : 0.f;
+                if (la && !pre && in_range(da + col - a.vnew, 2, n_rows_hv(a), a.status))
+                    *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                if (lb && !pre && in_range(db + col - a.vnew, 2, n_rows_hv(a), a.status))
+                    *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                epi::put_pair(sm.a_v, ra, col, va0 * cfa, va1 * cfa);
+                epi::put_pair(sm.a_v, rb, col, vb0 * cfb, vb1 * cfb);
+            }
+        }
+        float egl_next = egl;
+        if (i + 1 < nch) {  // publish the next chunk's scalars, and fetch one chunk further
+            egl_next = publish((i + 1) & 1);
+            if (i + 2 < nch) fetch(i + 2);
+        }
+        if (tid == 0) tma_store_wait_read();  // h_c has been read out of a_s
+        fence_proxy_async_smem();
+        tc_fence_before();
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        // 4. h += K^T A_V
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t av = smem_u32(sm.a_v), ks = smem_u32(sm.stage[st] + 2 * kBox);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tbase, sdesc(ks + s * 2048, kBox, 1024), sdesc(av + s * 2048, kBox, 1024), idS, true);
+            mma_commit(&sm.mma_bar);
+        }
+        ok = mbar_wait(&sm.mma_bar, phase) && ok;
+        phase ^= 1;
+        tc_fence_after();
+        if (tid == 0 && ok && i + 2 < nch) issue_stage(maps, sm, st, chunk_t0(i + 2), h, hv, vb, !phi);
+        egl = egl_next;
     }
     ok = __syncthreads_and(ok);
     if (ok && to_final && a.ht && in_range(sbase, 32, n_states(a), a.status)) {
@@ -478,21 +346,14 @@ __global__ void __launch_bounds__(kThr, 2)
     }
     if (tid == 0) tma_store_wait_all();
     if (!ok && tid == 0) {
-        // drain the copies and products still in flight (bounded) before leaving: the
-        // last load into each buffer, the last product group and Z product
+        // drain outstanding TMA copies (bounded) before leaving
         if (a.status) atomicOr(a.status, 2);
-        for (int b = 0; b < 2; ++b) {
-            const int kn = k_issued - 1 - b, wn = w_issued - 1 - b, un = u_issued - 1 - b;
-            if (kn >= 0) mbar_wait(&sm.k_bar[kn & 1], (kn >> 1) & 1, kDrainLimitNs);
-            if (wn >= 0) mbar_wait(&sm.w_bar[wn & 1], (wn >> 1) & 1, kDrainLimitNs);
-            if (un >= 0) mbar_wait(&sm.u_bar[un & 1], (un >> 1) & 1, kDrainLimitNs);
-        }
-        mbar_wait(&sm.mma_bar, phase ^ 1, kDrainLimitNs);
-        mbar_wait(&sm.z_bar, zphase ^ 1, kDrainLimitNs);
+        mbar_wait(&sm.tma_bar[0], 0, kDrainLimitNs);
+        mbar_wait(&sm.tma_bar[1], 0, kDrainLimitNs);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 // Start states of segments 1 .. S-1 of every split sequence: H_1 = end of segment 0,
@@ -559,9 +420,6 @@ cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(StateSmem) + 1024;
     static_assert(2 * (sizeof(StateSmem) + 2048) <= 233472, "two CTAs per SM");
-    static_assert(offsetof(StateSmem, kb) % 1024 == 0 && offsetof(StateSmem, wb) % 1024 == 0 &&
-                      offsetof(StateSmem, ub) % 1024 == 0 && offsetof(StateSmem, z_s) % 1024 == 0,
-                  "SW128 tiles on 1024-byte boundaries");
     cudaError_t e = cudaSuccess;
     for (const void *f : {(const void *)k_state_tc<0>, (const void *)k_state_tc<1>, (const void *)k_state_tc<2>})
         if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=

@@ -60,10 +60,8 @@ struct BwSmem {
     unsigned char k[kTile], v[kTile], dw[kTile], dvn[kTile];
     unsigned char op_t[kHalf];     // T_ij [i][j]: K-major B of X, MN-major A of T^T X, MN-major B of phase 2
     unsigned char op_dx[kHalf];    // dT rows (K-major A of X = dT T^T), then X rows (MN-major B of T^T X)
-    unsigned char op_b[kHalf];     // B_tj / r_k,j  [t][j]  K-major B; after phase 2: dv rows
-                                   // [t][d < 64] of a full chunk, for a TMA store
-    unsigned char op_bt[kHalf];    // B_it / r_k,i  [i][t]  MN-major B; after phase 2: dv rows
-                                   // [t][d >= 64]
+    unsigned char op_b[kHalf];     // B_tj / r_k,j  [t][j]  K-major B
+    unsigned char op_bt[kHalf];    // B_it / r_k,i  [i][t]  MN-major B
     float G[64], beta[64], rki[64], eg[64], dG[64], db[64];
     float rs[2][64];               // per-warpgroup partial row sums of P2
     float cy[4][64], cz[4][64], cp[4][64];  // per-row-block column sums
@@ -73,7 +71,6 @@ struct BwSmem {
 
 struct BwMaps {
     CUtensorMap k, v, dw, dvn, t;
-    CUtensorMap dv;   // output: a full chunk's dv rows, staged over the phase-2 operands
 };
 
 struct BwUnit {
@@ -289,7 +286,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                          sdesc(smem_u32(sm.op_dx) + s * 2048, kHalf, 1024), id, s > 0);
             mma_commit(&sm.mma_bar);
         }
-        if (tid == 0) tma_store_wait_read();  // the last unit's staged dv rows have been read
         commit_wait(ok);
         if (ok) {  // dA = -(T^T X): B and its operands, P2 row sums, column sums of beta_i P2
             float ta[16], kk[16];
@@ -399,10 +395,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                     acc[2 * jj + 1] = (first ? 0.f : acc[2 * jj + 1]) + k1;
                     const float v0 = b0 * ut[2 * jj], v1 = b1 * ut[2 * jj + 1];
                     const float rv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-                    if (L == 64) {  // staged: row me + odd, features (d & ~1, + 1)
-                        epi::put_pair(d >> 6 ? sm.op_bt : sm.op_b, me + odd, (d & 63) & ~1, odd ? rv : v0,
-                                      odd ? v1 : rv);
-                    } else if (me + odd < L && in_range(base + (size_t)me * ts, 2, n_rows_hv(a), a.status)) {
+                    if (me + odd < L && in_range(base + (size_t)me * ts, 2, n_rows_hv(a), a.status)) {
                         const size_t o = base + (size_t)me * ts;
                         *reinterpret_cast<uint32_t *>(a.dv + o) = odd ? pack_bf2(rv, v1) : pack_bf2(v0, rv);
                     }
@@ -419,13 +412,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         } else if (tid == 0 && a.status) {
             atomicOr(a.status, 2);
         }
-        fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0 && ok && L == 64) {  // the staged dv rows
-            tma_store_3d(&maps.dv, 0, hv, t0, sm.op_b);
-            tma_store_3d(&maps.dv, 64, hv, t0, sm.op_bt);
-            tma_store_commit();
-        }
         if (ok && warp == 0) {  // dg = reverse cumulative sum of dG (warp scan), dbeta
             float dgv[2];
     #pragma unroll
@@ -478,7 +465,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         if (a_issued > waited) mbar_wait(&sm.a_bar, (a_issued - 1) & 1, kDrainLimitNs);
         if (v_issued > waited) mbar_wait(&sm.v_bar, (v_issued - 1) & 1, kDrainLimitNs);
     }
-    if (tid == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 256);
@@ -495,8 +481,7 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64) ||
-        !encode_rows_bf16(&m.dv, a.dv, a.HV, a.T, rowb, rowb * a.HV, 64))
+        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BwSmem) + 1024;
     static_assert(2 * (sizeof(BwSmem) + 2048) <= 233472, "two CTAs per SM");

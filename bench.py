@@ -17,13 +17,17 @@ over ranks and `value` counts every rank's tokens.
 from __future__ import annotations
 
 import argparse
+import csv
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
 import tempfile
 import time
+
+from collections import defaultdict
 
 import numpy as np
 
@@ -495,6 +499,109 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------- ncu summaries
+# (profiles/ holds what these print for the committed captures)
+def ncu_launches(path, skip_first=0):
+    """Per kernel of an ncu launch list (--metrics gpu__time_duration.sum --csv): launches,
+    total and mean device time, share of the total."""
+    rows = []
+    with open(path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for r in csv.DictReader(lines):
+        if r.get("Metric Name") != "gpu__time_duration.sum":
+            continue
+        rows.append(r)
+    rows = rows[skip_first:]
+    agg = defaultdict(lambda: [0, 0.0])
+    for r in rows:
+        name = r["Kernel Name"].replace("(anonymous namespace)", "anon")
+        if "FillFunctor" in name:  # torch's memset: the L2 flush between timed steps
+            name = "torch fill (L2 flush)"
+        else:
+            name = re.sub(r"\(.*", "", name).split("::")[-1].strip()
+        scale = {"ns": 1e-6, "us": 1e-3, "usecond": 1e-3, "nsecond": 1e-6, "ms": 1.0,
+                 "msecond": 1.0}.get(r["Metric Unit"], 1e-6)
+        agg[name][0] += 1
+        agg[name][1] += float(r["Metric Value"].replace(",", "")) * scale
+    total = sum(v[1] for v in agg.values())
+    out = ["%-28s %8s %12s %10s %7s" % ("kernel", "launches", "total ms", "mean ms", "share")]
+    for name, (n, ms) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        out.append("%-28s %8d %12.3f %10.4f %6.1f%%" % (name, n, ms, ms / n, 100 * ms / total))
+    out.append("%-28s %8d %12.3f" % ("total", sum(v[0] for v in agg.values()), total))
+    return "\n".join(out)
+
+
+def ncu_report(path):
+    """Per captured launch of a --set full report: duration, DRAM bytes, DRAM throughput,
+    tensor-pipe activity, warps active, registers, grid and the largest warp stalls."""
+    out = subprocess.run(["ncu", "-i", path, "--page", "raw", "--csv"], capture_output=True,
+                         text=True, check=True).stdout
+    rows = list(csv.reader(out.splitlines()))
+    hdr, units, data = rows[0], rows[1], rows[2:]
+
+    def get(r, m):
+        return r[hdr.index(m)] if m in hdr else ""
+
+    def unit(r, m):
+        return units[hdr.index(m)] if m in hdr else ""
+
+    stall = [c for c in hdr if c.startswith("smsp__average_warps_issue_stalled_")
+             and c.endswith("_per_issue_active.ratio")]
+    lines = []
+    for r in data:
+        name = re.sub(r"\(.*", "", r[hdr.index("Kernel Name")].replace("(anonymous namespace)", "anon"))
+        name = name.split("::")[-1].strip()
+        tops = sorted(((float(get(r, c) or 0), c[len("smsp__average_warps_issue_stalled_"):-len(
+            "_per_issue_active.ratio")]) for c in stall), reverse=True)[:4]
+        lines.append(
+            "%s: %s %s; DRAM read %s %s, write %s %s (%s %% of peak); tensor pipe %s %% of active; "
+            "warps active %s %%; %s regs/thread; grid %s block %s; stalls (cycles/issue): %s" % (
+                name, get(r, "gpu__time_duration.sum"), unit(r, "gpu__time_duration.sum"),
+                get(r, "dram__bytes_read.sum"), unit(r, "dram__bytes_read.sum"),
+                get(r, "dram__bytes_write.sum"), unit(r, "dram__bytes_write.sum"),
+                get(r, "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed"),
+                get(r, "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"),
+                get(r, "sm__warps_active.avg.pct_of_peak_sustained_active"),
+                get(r, "launch__registers_per_thread"), get(r, "launch__grid_size"),
+                get(r, "launch__block_size"),
+                ", ".join("%s %.2f" % (n, v) for v, n in tops)))
+    return "\n".join(lines)
+
+
+NCU_KERNELS = {  # ncu kernel name -> bench kernel name (its source: KERNEL_SOURCE)
+    "k_intra_tc": "intra", "k_state_tc": "state", "k_state_tc<0>": "state",
+    "k_out_tc<1>": "out", "k_out_tc<true>": "out", "k_out_tc<0>": "dvloc", "k_out_tc<false>": "dvloc",
+    "k_bstate_tc": "bstate", "k_bstate_tc<0>": "bstate", "k_bintra_a_tc": "bintra_a",
+    "k_bintra_b_tc": "bintra_b", "k_decode": "decode", "k_prep": "prep", "k_dknorm": "dknorm",
+    "k_plan": "plan",
+}
+
+
+def ncu_traffic(path, units):
+    """JSON record of DRAM bytes (read + write) per work unit of every known kernel in a
+    --set full (or dram-metric) report, with the hash of its source at capture time."""
+    out = subprocess.run(["ncu", "-i", path, "--page", "raw", "--csv"], capture_output=True,
+                         text=True, check=True).stdout
+    rows = list(csv.reader(out.splitlines()))
+    hdr, data = rows[0], rows[2:]
+    units_row = rows[1]
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    rec = {}
+    for r in data:
+        name = re.sub(r"\(.*", "", r[hdr.index("Kernel Name")].replace("(anonymous namespace)", "anon"))
+        name = name.split("::")[-1].strip()
+        if name not in NCU_KERNELS:
+            continue
+        kname = NCU_KERNELS[name]
+        rd = float(r[hdr.index("dram__bytes_read.sum")]) * scale[units_row[hdr.index("dram__bytes_read.sum")]]
+        wr = float(r[hdr.index("dram__bytes_write.sum")]) * scale[units_row[hdr.index("dram__bytes_write.sum")]]
+        sha = _source_hash(kname)
+        rec[kname] = {"bytes_per_unit": (rd + wr) / units, "captured_units": units,
+                      "capture": os.path.basename(path), "source_sha256_16": sha}
+    return json.dumps(rec, indent=1, sort_keys=True)
+
+
+
 # ---------------------------------------------------------------------------- main bench
 def bench_ours(args):
     import torch
@@ -848,7 +955,26 @@ def main():
                          "plan, -1 = never split, L > 0 = segments of L chunks")
     ap.add_argument("--ref-tokens", type=int, default=2048,
                     help="tokens of the workload the oracle runs per baseline sample")
+    ap.add_argument("--ncu-launches", metavar="CSV", help="print the per-kernel summary of an ncu launch "
+                    "list (--metrics gpu__time_duration.sum --csv) and exit")
+    ap.add_argument("--ncu-report", metavar="REP", help="print a per-launch summary of an ncu report and exit")
+    ap.add_argument("--ncu-traffic", nargs="+", metavar="REP UNITS",
+                    help="print the DRAM-bytes-per-unit record of ncu reports (pairs of report and the "
+                         "work units of its captured launches) and exit")
+    ap.add_argument("--skip-first", type=int, default=0, help="launches to skip in --ncu-launches")
     args = ap.parse_args()
+    if args.ncu_launches:
+        print(ncu_launches(args.ncu_launches, args.skip_first))
+        return
+    if args.ncu_report:
+        print(ncu_report(args.ncu_report))
+        return
+    if args.ncu_traffic:
+        rec = {}
+        for r, u in zip(args.ncu_traffic[0::2], args.ncu_traffic[1::2]):
+            rec.update(json.loads(ncu_traffic(r, float(u))))
+        print(json.dumps(rec, indent=1, sort_keys=True))
+        return
     if args.impl == "reference":
         bench_reference(args)
     else:

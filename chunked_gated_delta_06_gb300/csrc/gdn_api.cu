@@ -327,8 +327,7 @@ gdn_status chunk_fwd_impl(const gdn_problem *p, const void *q, const void *k, co
     }
     cudaError_t e;
     if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
-    if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
-    if ((e = gdn::launch_fwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = gdn::launch_fwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);  // G, norms inside
     return GDN_OK;
 }
 

@@ -70,8 +70,7 @@ def kernel_work(name, T, H, HV, N, C_total):
     b = dict(
         plan=4 * (N + 1 + 3 * C_total),
         prep=T * H * D * bf * 2 + TV * 4 * 2 + T * H * 8,
-        # k, v; g, beta in and G out, r_k out; w, u, T out
-        intra=T * H * D * bf + TV * D * bf + TV * 10 + T * H * 4 + TV * D * bf * 2 + C_total * HV * C * C * 2,
+        intra=T * H * D * bf + TV * D * bf + TV * 6 + TV * D * bf * 2 + C_total * HV * C * C * 2,
         state=TV * D * bf * 3 + T * H * D * bf + C_total * HV * D * D * bf + N * HV * D * D * 8,
         out=T * H * D * bf * 2 + TV * D * bf * 2 + C_total * HV * D * D * bf,
         dvloc=T * H * D * bf * 2 + TV * D * bf * 2,

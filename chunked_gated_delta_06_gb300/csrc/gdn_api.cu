@@ -327,7 +327,8 @@ gdn_status chunk_fwd_impl(const gdn_problem *p, const void *q, const void *k, co
     }
     cudaError_t e;
     if ((e = gdn::launch_plan(a, s)) != cudaSuccess) return cuda_status(e);
-    if ((e = gdn::launch_fwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);  // G, norms inside
+    if ((e = gdn::launch_prep(a, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = gdn::launch_fwd_chunks(a, s)) != cudaSuccess) return cuda_status(e);
     return GDN_OK;
 }
 

@@ -6,9 +6,7 @@
 //            partial), "[Cake 1/13] gdn: chunked gated delta rule ...", API;
 //   k_prep   q / k norms r = sqrt(sum x^2 + 1e-6) ("C6: GDN decode-step
 //            goldens ...", Provider: divide by the sqrt) and the chunk-local
-//            cumulative sum G of g, for the recompute-state backward (a forward
-//            forms them inside the WY pass and the output kernel, with the same
-//            operations);
+//            cumulative sum G of g;
 //   k_dknorm the last step of the backward: dk through the L2-norm backward.
 // The tensor-core kernels of the chunked (WY) form live in gdn_*_tc.cu.
 // Every reduction runs in a fixed order and no kernel uses atomics, so results
@@ -119,23 +117,34 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
 #pragma unroll
     for (int m = 0; m < kRows; ++m) {
         const int i = warp + 8 * m;
-        const float rq = row_norm4(xq[m]), rk = row_norm4(xk[m]);
+        const float2 q0 = bf2_to_f2(xq[m].x), q1 = bf2_to_f2(xq[m].y);
+        const float2 k0 = bf2_to_f2(xk[m].x), k1 = bf2_to_f2(xk[m].y);
+        float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+        float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
         if (lane == 0 && i < L && in_range((size_t)(t0 + i) * a.H + h, 1, n_tok_h(a), a.status)) {
-            a.rq[(size_t)(t0 + i) * a.H + h] = rq;
-            a.rk[(size_t)(t0 + i) * a.H + h] = rk;
+            a.rq[(size_t)(t0 + i) * a.H + h] = sqrtf(sq + kNormEps);
+            a.rk[(size_t)(t0 + i) * a.H + h] = sqrtf(sk + kNormEps);
         }
     }
     const int r = a.HV / a.H;
     for (int j = warp; j < r; j += kThreads / 32) {
         const int hv = h * r + j;
         const int i0 = 2 * lane, i1 = 2 * lane + 1;
-        const float x0 = i0 < L ? load_g(a, (size_t)(t0 + i0) * a.HV + hv, hv) : 0.f;
-        const float x1 = i1 < L ? load_g(a, (size_t)(t0 + i1) * a.HV + hv, hv) : 0.f;
-        const float2 G = chunk_cumsum64(x0, x1, lane);
+        float x0 = i0 < L ? load_g(a, (size_t)(t0 + i0) * a.HV + hv, hv) : 0.f;
+        float x1 = i1 < L ? load_g(a, (size_t)(t0 + i1) * a.HV + hv, hv) : 0.f;
+        float s = x0 + x1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            float y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        float excl = s - (x0 + x1);
         if (i0 < L && in_range((size_t)(t0 + i0) * a.HV + hv, 1, n_tok_hv(a), a.status))
-            a.G[(size_t)(t0 + i0) * a.HV + hv] = G.x;
+            a.G[(size_t)(t0 + i0) * a.HV + hv] = excl + x0;
         if (i1 < L && in_range((size_t)(t0 + i1) * a.HV + hv, 1, n_tok_hv(a), a.status))
-            a.G[(size_t)(t0 + i1) * a.HV + hv] = G.y;
+            a.G[(size_t)(t0 + i1) * a.HV + hv] = excl + x0 + x1;
     }
 }
 
@@ -209,9 +218,9 @@ cudaError_t launch_prep(const ChunkArgs &a, cudaStream_t s) {
 
 cudaError_t launch_fwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     cudaError_t e;
-    if ((e = launch_intra_tc(a, s)) != cudaSuccess) return e;  // also G and r_k
+    if ((e = launch_intra_tc(a, s)) != cudaSuccess) return e;
     if ((e = launch_state_tc(a, s)) != cudaSuccess) return e;
-    if ((e = launch_out_tc(a, s)) != cudaSuccess) return e;    // also r_q
+    if ((e = launch_out_tc(a, s)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 

@@ -43,35 +43,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Row norm sqrt(sum x^2 + 1e-6) of a 128-wide bf16 row held four elements per lane by
-// a full warp (lane l: elements 4l .. 4l + 3, as two packed pairs): the same operations
-// in the same order wherever a norm is formed (k_prep, the WY pass, the output kernel),
-// so every kernel gets the same bits.
-__device__ __forceinline__ float row_norm4(uint2 x) {
-    const float2 a = bf2_to_f2(x.x), b = bf2_to_f2(x.y);
-    float s = __fmul_rn(a.x, a.x);
-    s = __fmaf_rn(a.y, a.y, s);
-    s = __fmaf_rn(b.x, b.x, s);
-    s = __fmaf_rn(b.y, b.y, s);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
-    return sqrtf(__fadd_rn(s, kNormEps));
-}
-
-// Chunk-local inclusive cumulative sum of g over 64 tokens by one warp (lane l holds
-// tokens 2l and 2l + 1; zeros past the chunk): G of tokens 2l, 2l + 1.  Shared by k_prep
-// and the WY pass, so both give the same bits.
-__device__ __forceinline__ float2 chunk_cumsum64(float x0, float x1, int lane) {
-    float s = __fadd_rn(x0, x1);
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, s, off);
-        if (lane >= off) s = __fadd_rn(s, y);
-    }
-    const float excl = __fsub_rn(s, __fadd_rn(x0, x1));
-    return make_float2(__fadd_rn(excl, x0), __fadd_rn(__fadd_rn(excl, x0), x1));
-}
-
 // Fused gating ("C6: GDN decode-step goldens and recurrent/conv state contract",
 // Provider): beta = sigmoid(b), g = -exp(A_log) softplus(a + dt_bias) in fp32, with
 // softplus(x) = x above the threshold 20 (its slope there is 1, sigmoid(x) below).

@@ -206,18 +206,22 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         fence_mbar_init();
         issue_kv(maps, sm, x);
     }
-    // per-token inputs, fetched one unit ahead: g of tokens 2 lane, 2 lane + 1 (warp 0;
-    // zeros past the chunk) and the raw beta bits of token tid (tid < 64)
-    float pg0 = 0.f, pg1 = 0.f;
+    // per-token scalars of thread tid < 64, fetched one unit ahead
+    float pG = 0.f, pR = 1.f;
     uint32_t pB = 0;   // raw beta bits, converted when published
     bool pin = false;
     auto fetch = [&](const IntraUnit &y) {
-        pin = tid < 64 && tid < y.L && in_range((size_t)(y.t0 + tid) * a.HV + y.hv, 1, n_tok_hv(a), a.status);
-        if (pin) pB = load_beta_raw(a, (size_t)(y.t0 + tid) * a.HV + y.hv);
-        if (warp == 0) {
-            const int i0 = 2 * lane, i1 = 2 * lane + 1;
-            pg0 = i0 < y.L ? load_g(a, (size_t)(y.t0 + i0) * a.HV + y.hv, y.hv) : 0.f;
-            pg1 = i1 < y.L ? load_g(a, (size_t)(y.t0 + i1) * a.HV + y.hv, y.hv) : 0.f;
+        pin = tid < 64 && tid < y.L;
+        if (pin) {
+            const size_t gi = (size_t)(y.t0 + tid) * a.HV + y.hv;
+            const size_t ri = (size_t)(y.t0 + tid) * a.H + y.h;
+            if (kChecked && !(in_range(gi, 1, n_tok_hv(a), a.status) && in_range(ri, 1, n_tok_h(a), a.status)))
+                pin = false;
+            else {
+                pG = a.G[gi];
+                pB = load_beta_raw(a, gi);
+                pR = a.rk[ri];
+            }
         }
     };
     fetch(x);
@@ -231,14 +235,13 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int c = x.c, hv = x.hv, t0 = x.t0, L = x.L;
-        if (tid < 64) sm.beta[tid] = pin ? beta_from_raw(a, pB) : 0.f;  // beta = 0 past L
-        if (warp == 0) {  // G: the chunk-local cumulative sum of g (also kept for later kernels)
-            const float2 G2 = chunk_cumsum64(pg0, pg1, lane);
-            sm.G[2 * lane] = G2.x;
-            sm.G[2 * lane + 1] = G2.y;
-            const size_t gi = (size_t)(t0 + 2 * lane) * a.HV + hv;
-            if (2 * lane < L && in_range(gi, 1, n_tok_hv(a), a.status)) a.G[gi] = G2.x;
-            if (2 * lane + 1 < L && in_range(gi + a.HV, 1, n_tok_hv(a), a.status)) a.G[gi + a.HV] = G2.y;
+        if (tid < 64) {  // tokens past L get G = 0, beta = 0 and 1 / r_k = 1
+            const float ri = pin ? 1.f / pR : 1.f, bb = pin ? beta_from_raw(a, pB) : 0.f;
+            const float gg = pin ? pG : 0.f;
+            sm.G[tid] = gg;
+            sm.beta[tid] = bb;
+            sm.rki[tid] = ri;
+            sm.wc[tid] = bb * __expf(gg) * ri;
         }
         ok = __syncthreads_and(ok && mbar_wait(&sm.ld_bar, waited & 1));
         ++waited;
@@ -252,27 +255,6 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
                 mma_bf16(tb, sdesc(ks + off, 16, 1024), sdesc(ks + off, 16, 1024), id, s > 0);
             }
             mma_commit(&sm.mma_bar);
-        }
-        // the key norms r_k of the chunk's rows from the K tile (warp w: rows w, w + 4, ...;
-        // the first value head of a key head keeps them for later kernels), and the
-        // per-token factors 1 / r_k and beta e^G / r_k (1 and 0 past L)
-        {
-            const bool keep = hv % (a.HV / a.H) == 0;
-#pragma unroll 4
-            for (int m = 0; m < 16; ++m) {
-                const int i = warp + 4 * m;
-                const uint2 kx = *reinterpret_cast<const uint2 *>(sm.k + ((lane * 4) >> 6) * kHalf +
-                                                                  sw128_off(i, (lane * 4) & 63));
-                const float rk = row_norm4(kx);
-                if (lane == 0) {
-                    const bool in = i < L;
-                    const float ri = in ? 1.f / rk : 1.f;
-                    sm.rki[i] = ri;
-                    sm.wc[i] = in ? sm.beta[i] * __expf(sm.G[i]) * ri : 0.f;
-                    const size_t ki = (size_t)(t0 + i) * a.H + x.h;
-                    if (in && keep && in_range(ki, 1, n_tok_h(a), a.status)) a.rk[ki] = rk;
-                }
-            }
         }
         // the next unit (its table entries are a dependent load: after the MMA issue)
         const IntraUnit nx = has_next ? intra_next(a, x) : x;

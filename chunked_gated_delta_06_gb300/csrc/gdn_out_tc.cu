@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
         if (pin) {
             const size_t r = (size_t)(y.t0 + tid) * a.H + y.h;
             pG = a.G[(size_t)(y.t0 + tid) * a.HV + y.hv];
-            if (!kForward) pRq = a.rq[r];  // the forward forms r_q from its Q tile
+            pRq = a.rq[r];
             pRk = a.rk[r];
         }
     };
@@ -157,35 +157,13 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
             sm.G[tid] = gg;
             sm.rq[tid] = rq;
             sm.rk[tid] = rk;
+            sm.qsc[tid] = a.scale / rq;
             sm.rki[tid] = 1.f / rk;
-            if (!kForward) {
-                sm.qsc[tid] = a.scale / rq;
-                sm.ct[tid] = pin ? __expf(gg) * (a.scale / rq) : 0.f;
-            }
+            sm.ct[tid] = pin ? __expf(gg) * (a.scale / rq) : 0.f;
         }
         ok = __syncthreads_and(ok && mbar_wait(&sm.tma_bar, waited & 1));
         ++waited;
         if (!ok) break;
-        if constexpr (kForward) {  // r_q of the chunk's rows from the Q tile (warp w: rows
-                                   // w, w + 4, ...; kept for the backward by the first value
-                                   // head of a key head), then scale / r_q and e^G scale / r_q
-            const int lane = tid & 31;
-            const bool keep = hv % (a.HV / a.H) == 0;
-#pragma unroll 4
-            for (int m = 0; m < 16; ++m) {
-                const int i = warp + 4 * m;
-                const uint2 qx = *reinterpret_cast<const uint2 *>(sm.kq + ((lane * 4) >> 6) * kBig + kBox +
-                                                                  sw128_off(i, (lane * 4) & 63));
-                const float rq = row_norm4(qx);
-                if (lane == 0) {
-                    const bool in = i < L;
-                    sm.qsc[i] = a.scale / (in ? rq : 1.f);
-                    sm.ct[i] = in ? __expf(sm.G[i]) * (a.scale / rq) : 0.f;
-                    const size_t qi = (size_t)(t0 + i) * a.H + x.h;
-                    if (in && keep && in_range(qi, 1, n_tok_h(a), a.status)) a.rq[qi] = rq;
-                }
-            }
-        }
         // QK = Q K^T (M=64; Q rows sit at kBox inside each k-half of the [K; Q] tile)
         if (tid == 0 && ok) {
             tc_fence_after();

@@ -124,8 +124,7 @@ __device__ __forceinline__ void issue_v(const BwMaps &m, BwSmem &sm, const BwUni
 __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                                                          const __grid_constant__ BwMaps maps, int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    BwSmem &sm = *reinterpret_cast<BwSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+    BwSmem &sm = smem_struct<BwSmem>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);

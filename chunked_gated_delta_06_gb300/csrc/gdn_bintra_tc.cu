@@ -154,8 +154,7 @@ __device__ __forceinline__ void issue_b(const BaMaps &m, BaSmem &sm, const Unit 
 __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                                                          const __grid_constant__ BaMaps maps, int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    BaSmem &sm = *reinterpret_cast<BaSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+    BaSmem &sm = smem_struct<BaSmem>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);

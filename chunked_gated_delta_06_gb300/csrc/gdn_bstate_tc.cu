@@ -111,8 +111,7 @@ template <int pass>
 __global__ void __launch_bounds__(kThr, 2)
     k_bstate_tc(const ChunkArgs a, const __grid_constant__ BStateMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    BStateSmem &sm = *reinterpret_cast<BStateSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    BStateSmem &sm = smem_struct<BStateSmem>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ncol = pass == 1 ? 4 : 2;            // column blocks of 64 per value head
     const int hv = blockIdx.x / ncol, cbk = blockIdx.x % ncol;

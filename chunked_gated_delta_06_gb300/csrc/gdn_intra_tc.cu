@@ -188,8 +188,7 @@ __device__ __forceinline__ void issue_kv(const IntraMaps &m, IntraSmem &sm, cons
 __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
                                                       const __grid_constant__ IntraMaps maps, int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    IntraSmem &sm = *reinterpret_cast<IntraSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                   ~uintptr_t(1023));
+    IntraSmem &sm = smem_struct<IntraSmem>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);

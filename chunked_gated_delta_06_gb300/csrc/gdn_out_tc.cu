@@ -109,8 +109,7 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
                                                                    const __grid_constant__ OutMaps maps,
                                                                    int per) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    OutSmem<kForward> &sm = *reinterpret_cast<OutSmem<kForward> *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    OutSmem<kForward> &sm = smem_struct<OutSmem<kForward>>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);

@@ -85,8 +85,7 @@ template <int pass>
 __global__ void __launch_bounds__(kThr, 2)
     k_state_tc(const ChunkArgs a, const __grid_constant__ StateMaps maps) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    StateSmem &sm = *reinterpret_cast<StateSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    StateSmem &sm = smem_struct<StateSmem>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ncol = pass == 1 ? 4 : 2;            // column blocks of 64 per value head
     const int hv = blockIdx.x / ncol, cbk = blockIdx.x % ncol;

@@ -20,6 +20,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory block rounded up to a 1024-byte boundary (the SW128 tiles
+// need it).  Derived from the __shared__ array by pointer arithmetic, so the compiler
+// keeps knowing that every access through it is a shared-memory access.
+template <class T>
+__device__ __forceinline__ T &smem_struct(unsigned char *raw) {
+    const uint32_t pad = (1024u - (smem_u32(raw) & 1023u)) & 1023u;
+    return *reinterpret_cast<T *>(raw + pad);
+}
+
 // Byte offset of element (row, col) of a 64-wide bf16 SW128 tile.
 __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
     const uint32_t chunk = (uint32_t)(col >> 3) ^ (uint32_t)(row & 7);

@@ -146,7 +146,7 @@ void carve_saved(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     const size_t D = gdn::kDim;
     a.hc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
     a.vnew = cv.take<bf16>((size_t)d.T * d.HV * D);
-    a.w = cv.take<bf16>((size_t)d.T * d.HV * D);
+    a.w = cv.take<bf16>((size_t)d.C * d.HV * D * gdn::kChunk);
     a.Tm = cv.take<bf16>((size_t)d.C * d.HV * gdn::kChunk * gdn::kChunk);
     a.rq = cv.take<float>((size_t)d.T * d.H);
     a.rk = cv.take<float>((size_t)d.T * d.H);
@@ -172,7 +172,7 @@ void carve_segments(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
 
 void carve_fwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a, bool with_saved) {
     carve_table(cv, d, a);
-    a.u = cv.take<bf16>((size_t)d.T * d.HV * gdn::kDim);
+    a.u = cv.take<bf16>((size_t)d.C * d.HV * gdn::kDim * gdn::kChunk);
     carve_segments(cv, d, a);
     if (with_saved) carve_saved(cv, d, a);
 }

@@ -81,7 +81,7 @@ struct BaSmem {
     float iq[64];                 // 1 / r_q (0 past L)
     float rp[2][64];              // per-warpgroup partial row sums of P1
     float cp[4][64];              // per-row-block column sums of P1
-    float hdh[kThr / 32];
+    float hdh[4];                 // per-warp partial <h, dh'> (warps 4..7)
     float G[64], eg[64], egl_g[64];  // G, e^{G_t}, e^{G_L - G_t} (0 past L)
     float qsc[64], rki[64];       // scale / r_q, 1 / r_k
     uint64_t a_bar, b_bar[2], mma_bar;   // group A (h, dh, dO, dv_new, v_new), group B (q, k) per buffer
@@ -187,12 +187,17 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     uint32_t bpar = 0, bpend = 1;  // per q / k buffer (bit i): parity of its next wait, a load in flight
     int bcur = 0;         // the q / k buffer of the current unit
     bool need_b = true;   // the current unit waits for a q / k load
-    // per-token scalars, fetched one unit ahead (threads 0..63)
+    // Warp 0 issues the products and does nothing else while they run (its issuing
+    // thread stalls for as long as the tensor pipe is full); warps 2 and 3 own the
+    // per-token scalars (token ft = tid - 64), fetched one unit ahead, and warps 4..7
+    // the <h, dh'> dot.
+    const int ft = tid - 64;
+    const bool scal = ft >= 0 && ft < 64;
     float pG = 0.f, pRq = 1.f, pRk = 1.f;
     auto fetch = [&](const Unit &y) {
-        if (tid < y.L && tid < 64 && in_range((size_t)(y.t0 + tid) * a.HV + y.hv, 1, n_tok_hv(a), a.status)) {
-            const size_t r = (size_t)(y.t0 + tid) * a.H + y.h;
-            pG = a.G[(size_t)(y.t0 + tid) * a.HV + y.hv];
+        if (scal && ft < y.L && in_range((size_t)(y.t0 + ft) * a.HV + y.hv, 1, n_tok_hv(a), a.status)) {
+            const size_t r = (size_t)(y.t0 + ft) * a.H + y.h;
+            pG = a.G[(size_t)(y.t0 + ft) * a.HV + y.hv];
             pRq = a.rq[r];
             pRk = a.rk[r];
         } else {
@@ -205,12 +210,12 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int L = x.L;
-        if (tid < 64) {
-            const bool in = tid < L;
-            sm.G[tid] = pG;
-            sm.qsc[tid] = in ? a.scale / pRq : 0.f;
-            sm.rki[tid] = in ? 1.f / pRk : 0.f;
-            sm.iq[tid] = in ? 1.f / pRq : 0.f;
+        if (scal) {
+            const bool in = ft < L;
+            sm.G[ft] = pG;
+            sm.qsc[ft] = in ? a.scale / pRq : 0.f;
+            sm.rki[ft] = in ? 1.f / pRk : 0.f;
+            sm.iq[ft] = in ? 1.f / pRq : 0.f;
         }
         bool got = mbar_wait(&sm.a_bar, a_waited & 1);
         if (need_b) got = mbar_wait(&sm.b_bar[bcur], (bpar >> bcur) & 1) && got;
@@ -222,11 +227,11 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         }
         if (!got) { ok = false; break; }
         const float Gl = L > 0 ? sm.G[L - 1] : 0.f;
-        if (tid < 64) {
-            const bool in = tid < L;
-            const float Gt = sm.G[tid];
-            sm.eg[tid] = in ? __expf(Gt) : 0.f;
-            sm.egl_g[tid] = in ? __expf(fminf(Gl - Gt, 0.f)) : 0.f;
+        if (scal) {
+            const bool in = ft < L;
+            const float Gt = sm.G[ft];
+            sm.eg[ft] = in ? __expf(Gt) : 0.f;
+            sm.egl_g[ft] = in ? __expf(fminf(Gl - Gt, 0.f)) : 0.f;
         }
         if (tid == 0) {  // batch 1
             tc_fence_after();
@@ -255,27 +260,29 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             if (tid == 0) issue_b(maps, sm, nx, bcur ^ 1);
             bpend |= 1u << (bcur ^ 1);
         }
-        // <h, dh'> while the products run: thread tid takes half a row of h and dh'
-        float hdh = 0.f;
-        {
-            const int kr = tid >> 1, half = tid & 1;
-            const unsigned char *hr = sm.h + half * kBig, *dr = sm.dh + half * kBig;
+        // <h, dh'> while the products run: thread tid - 128 of warps 4..7 takes a row
+        // of h and dh'
+        if (warp >= 4) {
+            const int kr = tid - 128;
+            float hdh = 0.f;
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {
-                const uint32_t off = sw128_off(kr, q8 * 8);
-                const uint4 xx = *reinterpret_cast<const uint4 *>(hr + off);
-                const uint4 yy = *reinterpret_cast<const uint4 *>(dr + off);
-                const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xx);
-                const __nv_bfloat162 *yb = reinterpret_cast<const __nv_bfloat162 *>(&yy);
+            for (int half = 0; half < 2; ++half)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xf = __bfloat1622float2(xb[e]), yf = __bfloat1622float2(yb[e]);
-                    hdh += xf.x * yf.x + xf.y * yf.y;
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    const uint32_t off = half * kBig + sw128_off(kr, q8 * 8);
+                    const uint4 xx = *reinterpret_cast<const uint4 *>(sm.h + off);
+                    const uint4 yy = *reinterpret_cast<const uint4 *>(sm.dh + off);
+                    const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xx);
+                    const __nv_bfloat162 *yb = reinterpret_cast<const __nv_bfloat162 *>(&yy);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 xf = __bfloat1622float2(xb[e]), yf = __bfloat1622float2(yb[e]);
+                        hdh += xf.x * yf.x + xf.y * yf.y;
+                    }
                 }
-            }
+            hdh = warp_sum(hdh);
+            if (lane == 0) sm.hdh[warp - 4] = hdh;
         }
-        hdh = warp_sum(hdh);
-        if (lane == 0) sm.hdh[warp] = hdh;
         if (tid == 0) tma_store_wait_read();  // the last unit's staged rows have been read
         bool done = __syncthreads_and(mbar_wait(&sm.mma_bar, phase));
         phase ^= 1;
@@ -500,7 +507,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             sx = warp_sum(sx);
             float hd = 0.f;
 #pragma unroll
-            for (int w = 0; w < kThr / 32; ++w) hd += sm.hdh[w];
+            for (int w = 0; w < 4; ++w) hd += sm.hdh[w];
 #pragma unroll
             for (int z = 0; z < 2; ++z) {
                 const int tt = 2 * lane + z;

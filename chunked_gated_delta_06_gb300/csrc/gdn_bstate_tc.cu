@@ -15,7 +15,8 @@
 //      dv_new[t][v'] = dv_loc + e^{G_L-G_t}/r_k,t Pd (to HBM, bf16) and the
 //      operands c_t dO[t][v'] and -dv_new[t][v'], c_t = e^{G_t} scale / r_q,t;
 //   4. dh += Q^T (c dO) - w^T dv_new                  (two M=128 N=64 K=64
-//      products; Q and w are raw tiles read MN-major)
+//      products; Q is the raw tile read MN-major, w^T the chunk's [k][t] tile
+//      read K-major)
 // which is dh <- e^{G_L} dh' + Qtil^T dO - w^T dv_new and dv_new = dv_loc +
 // Ktil dh'.  dh0 = dh at the sequence start.  The tiles are single-buffered so
 // that two CTAs share an SM, and each group is reloaded for the next chunk as
@@ -40,7 +41,7 @@ using namespace umma;
 constexpr int kThr = 256;
 constexpr uint32_t kBox = 64 * 128;       // one 64-row x 128-byte SW128 box
 constexpr uint32_t kXBytes = 4 * kBox;    // K (2 boxes), dO half, dv_loc half
-constexpr uint32_t kYBytes = 4 * kBox;    // Q (2 boxes), w (2 boxes)
+constexpr uint32_t kYBytes = 4 * kBox;    // Q (2 boxes), w^T (128 rows: 2 boxes)
 
 struct BStateSmem {
     unsigned char a_ds[128 * 128];      // dh' bf16 [k][v']
@@ -70,10 +71,10 @@ __device__ __forceinline__ void issue_xd(const BStateMaps &m, BStateSmem &sm, in
     tma_load_3d(sm.x + 3 * kBox, &m.dl, 64 * vb, hv, t0, &sm.xd_bar);
 }
 
-// L2 prefetch of every tile of one chunk (loaded a step later); transition columns
-// read no dO / dv_loc
-__device__ __forceinline__ void prefetch_chunk(const BStateMaps &m, int t0, int h, int hv, int vb,
-                                               bool with_d) {
+// L2 prefetch of every tile of chunk c (tokens from t0; loaded a step later);
+// transition columns read no dO / dv_loc
+__device__ __forceinline__ void prefetch_chunk(const BStateMaps &m, const ChunkArgs &a, int c, int t0, int h,
+                                               int hv, int vb, bool with_d) {
     tma_prefetch_3d(&m.k, 0, h, t0);
     tma_prefetch_3d(&m.k, 64, h, t0);
     if (with_d) {
@@ -82,16 +83,15 @@ __device__ __forceinline__ void prefetch_chunk(const BStateMaps &m, int t0, int 
     }
     tma_prefetch_3d(&m.q, 0, h, t0);
     tma_prefetch_3d(&m.q, 64, h, t0);
-    tma_prefetch_3d(&m.w, 0, hv, t0);
-    tma_prefetch_3d(&m.w, 64, hv, t0);
+    tma_prefetch_3d(&m.w, 0, 0, (c * a.HV + hv) * kDim);
 }
 
-__device__ __forceinline__ void issue_y(const BStateMaps &m, BStateSmem &sm, int t0, int h, int hv) {
+__device__ __forceinline__ void issue_y(const BStateMaps &m, BStateSmem &sm, const ChunkArgs &a, int c, int t0,
+                                        int h, int hv) {
     mbar_arrive_expect_tx(&sm.y_bar, kYBytes);
     tma_load_3d(sm.y + 0 * kBox, &m.q, 0, h, t0, &sm.y_bar);
     tma_load_3d(sm.y + 1 * kBox, &m.q, 64, h, t0, &sm.y_bar);
-    tma_load_3d(sm.y + 2 * kBox, &m.w, 0, hv, t0, &sm.y_bar);
-    tma_load_3d(sm.y + 3 * kBox, &m.w, 64, hv, t0, &sm.y_bar);
+    tma_load_3d(sm.y + 2 * kBox, &m.w, 0, 0, (c * a.HV + hv) * kDim, &sm.y_bar);
 }
 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThr, 2)
     const int ts1 = nseq > 0 ? a.chunk_start[ce - 1] + a.chunk_len[ce - 1] : 0;
     auto step_t0 = [&](int i) { return ts0 + 64 * (jend - 1 - i); };
     auto step_len = [&](int i) { return min(64, ts1 - step_t0(i)); };
+    auto step_c = [&](int i) { return cb + jend - 1 - i; };  // its chunk
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 128);
@@ -168,8 +169,8 @@ __global__ void __launch_bounds__(kThr, 2)
     if (tid == 0 && nch > 0) {
         issue_xk(maps, sm, step_t0(0), h);
         if (!phi) issue_xd(maps, sm, step_t0(0), hv, vb);
-        issue_y(maps, sm, step_t0(0), h, hv);
-        if (nch > 1) prefetch_chunk(maps, step_t0(1), h, hv, vb, !phi);
+        issue_y(maps, sm, a, step_c(0), step_t0(0), h, hv);
+        if (nch > 1) prefetch_chunk(maps, a, step_c(1), step_t0(1), h, hv, vb, !phi);
         xk_issued = y_issued = 1;
         xd_issued = phi ? 0 : 1;
     }
@@ -239,11 +240,12 @@ __global__ void __launch_bounds__(kThr, 2)
     }
     __syncthreads();
     const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // Pd = K dh'          (dh' MN-major)
-    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // dh += Q^T A + w^T B (all MN-major)
+    const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // dh += Q^T A       (both MN-major)
+    const uint32_t idW = idesc_bf16(128, 64, 0, 1);   // dh += w^T B       (w^T K-major, B MN-major)
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0; i < nch; ++i) {
-        const int c = cb + jend - 1 - i;
+        const int c = step_c(i);
         const uint32_t par = i & 1;
         const int t0 = step_t0(i), L = step_len(i);
         // 1. dh' -> bf16 operand (copied to dh_c by TMA below), then dh <- e^{G_L} dh'
@@ -348,19 +350,19 @@ __global__ void __launch_bounds__(kThr, 2)
                     mma_bf16(tbase, sdesc(qs + s * 2048, kBox, 1024), sdesc(ado + s * 2048, kBox, 1024), idS, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tbase, sdesc(ws + s * 2048, kBox, 1024), sdesc(adv + s * 2048, kBox, 1024), idS, true);
+                mma_bf16(tbase, sdesc(ws + s * 32, 16, 1024), sdesc(adv + s * 2048, kBox, 1024), idW, true);
             mma_commit(&sm.mma_bar);
             if (i + 1 < nch && !phi) {
                 issue_xd(maps, sm, step_t0(i + 1), hv, vb);
                 ++xd_issued;
             }
-            if (i + 2 < nch) prefetch_chunk(maps, step_t0(i + 2), h, hv, vb, !phi);
+            if (i + 2 < nch) prefetch_chunk(maps, a, step_c(i + 2), step_t0(i + 2), h, hv, vb, !phi);
         }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
         if (tid == 0 && ok && i + 1 < nch) {  // Q and w are free once step 4 has finished
-            issue_y(maps, sm, step_t0(i + 1), h, hv);
+            issue_y(maps, sm, a, step_c(i + 1), step_t0(i + 1), h, hv);
             ++y_issued;
         }
         egl = egl_next;
@@ -405,7 +407,8 @@ cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s) {
     const uint64_t rowb = 128 * 2;
     if (a.T > 0 && (!encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
                     !encode_rows_bf16(&m.q, a.q, a.H, a.T, rowb, rowb * a.H, 64) ||
-                    !encode_rows_bf16(&m.w, a.w, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+                    !encode_rows_bf16(&m.w, a.w, 1, (uint64_t)a.num_chunks * a.HV * kDim, 128, 128, 128,
+                                      kChunk) ||
                     !encode_rows_bf16(&m.dO, a.d_o, a.HV, a.T, rowb, rowb * a.HV, 64) ||
                     !encode_rows_bf16(&m.dl, a.dvloc, a.HV, a.T, rowb, rowb * a.HV, 64) ||
                     !encode_rows_bf16(&m.dhc, a.dhc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb,

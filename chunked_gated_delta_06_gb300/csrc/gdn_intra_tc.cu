@@ -18,7 +18,12 @@
 //                                                (tcgen05, M=128 N=64 K=64; the K
 //                                                 and V tiles are read MN-major, so
 //                                                 row d of w^T / u^T is TMEM lane d)
-// w, u and T (kept for the backward) go to HBM in bf16.
+// w^T, u^T and T (kept for the backward) go to HBM in bf16, w^T and u^T per chunk
+// as [C][HV][128][64]: thread d holds row d of both (the chunk's 64 tokens) and
+// stages it in the bytes of T (swizzled as the tile map expects); one TMA store per
+// tile copies the 128 rows out.  Columns past L come out zero
+// (beta is zero there, so those rows of T diag(c) are), and the scans that read
+// the tiles rely on that.
 #include <stddef.h>
 #include <string.h>
 
@@ -52,6 +57,7 @@ struct IntraSmem {
 
 struct IntraMaps {
     CUtensorMap k, v;
+    CUtensorMap w, u;   // outputs: [C][HV][128] rows of 64 tokens, 128-row boxes
 };
 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -258,6 +264,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         // the next unit (its table entries are a dependent load: after the MMA issue)
         const IntraUnit nx = has_next ? intra_next(a, x) : x;
         if (has_next) fetch(nx);
+        if (tid == 0) tma_store_wait_read();  // the last unit's u^T rows have left M
         ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
         mphase ^= 1;
         tc_fence_after();
@@ -337,23 +344,31 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         tc_fence_after();
         if (tid == 0 && ok && has_next) issue_kv(maps, sm, nx);  // K and V have been read
         if (ok && has_next) ++issued;
-        if (ok) {  // thread d writes element d of every live token row of w and u
-            const size_t base = ((size_t)t0 * a.HV + hv) * kDim + tid;
-            const size_t tstride = (size_t)a.HV * kDim;
+        if (ok) {  // w^T, then u^T: thread d stages row d (64 tokens) in M, one TMA store each
+            unsigned char *stg = reinterpret_cast<unsigned char *>(sm.M);
+            const int row = (c * a.HV + hv) * kDim;
             for (int part = 0; part < 2; ++part) {
-                bf16 *dst = (part == 0 ? a.w : a.u) + base;
-                float x0[32], x1[32];
-                tmem_ld32(t_row + 64 * part, x0);
-                tmem_ld32(t_row + 64 * part + 32, x1);
+                float x[2][32];
+                tmem_ld32(t_row + 64 * part, x[0]);
+                tmem_ld32(t_row + 64 * part + 32, x[1]);
                 tmem_ld_wait();
+                if (part == 1) {  // the w^T store has read the staged rows
+                    if (tid == 0) tma_store_wait_read();
+                    __syncthreads();
+                }
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i < L && in_range(base + (size_t)i * tstride, 1, n_rows_hv(a), a.status))
-                        dst[(size_t)i * tstride] = __float2bfloat16_rn(x0[i]);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (32 + i < L && in_range(base + (size_t)(32 + i) * tstride, 1, n_rows_hv(a), a.status))
-                        dst[(size_t)(32 + i) * tstride] = __float2bfloat16_rn(x1[i]);
+                for (int q = 0; q < 8; ++q) {
+                    const float *y = x[q >> 2] + 8 * (q & 3);
+                    *reinterpret_cast<uint4 *>(stg + sw128_off(tid, 8 * q)) =
+                        make_uint4(pack_bf2(y[0], y[1]), pack_bf2(y[2], y[3]), pack_bf2(y[4], y[5]),
+                                   pack_bf2(y[6], y[7]));
+                }
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tma_store_3d(part == 0 ? &maps.w : &maps.u, 0, 0, row, stg);
+                    tma_store_commit();
+                }
             }
         }
         tc_fence_before();
@@ -365,6 +380,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         if (a.status) atomicOr(a.status, 2);
         if (issued > waited) mbar_wait(&sm.ld_bar, (issued - 1) & 1, kDrainLimitNs);  // drain (bounded)
     }
+    if (tid == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 128);
@@ -377,8 +393,11 @@ cudaError_t launch_intra_tc(const ChunkArgs &a, cudaStream_t s) {
     IntraMaps m;
     memset(&m, 0, sizeof(m));
     const uint64_t rowb = 256;
+    const uint64_t wrows = (uint64_t)a.num_chunks * a.HV * kDim;
     if (!encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
-        !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64))
+        !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.w, a.w, 1, wrows, 128, 128, 128, kChunk) ||
+        !encode_rows_bf16(&m.u, a.u, 1, wrows, 128, 128, 128, kChunk))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(IntraSmem) + 1024;
     static_assert(4 * (sizeof(IntraSmem) + 2048) <= 233472, "four CTAs per SM");

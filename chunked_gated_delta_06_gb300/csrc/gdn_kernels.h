@@ -37,7 +37,7 @@ struct ChunkArgs {
     // saved by the forward, read by the backward
     bf16 *hc;               // [C_total,HV,K,V] state at each chunk start
     bf16 *vnew;             // [T,HV,V]
-    bf16 *w;                // [T,HV,K]
+    bf16 *w;                // w^T per chunk: [C,HV,K,64] (row k holds the chunk's 64 tokens; zero past L)
     bf16 *Tm;               // [C_total,HV,64,64] (I + A)^-1
     float *rq, *rk;         // [T,H] sqrt(|x|^2 + eps)
     float *G;               // [T,HV] chunk-local cumulative log decay
@@ -53,7 +53,7 @@ struct ChunkArgs {
     float *seg_end;         // [N,seg_max-1,HV,K,2K] end states of segment 0 and the pre-scans: [h | Phi]
     float *seg_start;       // [N,seg_max-1,HV,K,V] start states of segments 1 .. S-1
     // forward scratch
-    bf16 *u;                // [T,HV,V]
+    bf16 *u;                // u^T per chunk: [C,HV,V,64] (as w)
     // backward
     const bf16 *d_o;
     const float *d_ht;      // or null

@@ -11,14 +11,15 @@
 // value):
 //   1. thread k writes row k of h as bf16 to shared memory (MMA operand; one TMA
 //      store copies it to h_c[chunk][hv][k][v']), and e^{G_L} h back to TMEM;
-//   2. P[t][v'] = sum_k w[t][k] h[k][v']          (tcgen05, M=64 N=64 K=128)
+//   2. P[t][v'] = sum_k w[t][k] h[k][v']          (tcgen05, M=64 N=64 K=128; w
+//      comes as the chunk's w^T tile [k][t] and is read MN-major)
 //   3. the result is read as 16x256b fragments (two token rows and eight columns
 //      per lane); v_new[t][v'] = u - P goes to HBM (bf16), and
 //      A_V[t][v'] = v_new e^{G_L - G_t} / r_k,t to shared memory (bf16);
 //   4. h[k][v'] += sum_t K[t][k] A_V[t][v']        (tcgen05, M=128 N=64 K=64; the
 //      raw key tile is read MN-major)
 // which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with Khat =
-// diag(1 / r_k) K.  w, K and this half of u stream in by TMA two chunks ahead,
+// diag(1 / r_k) K.  w^T, K and this half of u^T stream in by TMA two chunks ahead,
 // the next chunk's per-token scalars are loaded a chunk ahead and published
 // during the current epilogue, and a chunk costs two block barriers.  Two CTAs
 // share an SM.  Every wait is bounded; a timeout sets status bit 2 and the CTA
@@ -40,7 +41,7 @@ using namespace umma;
 
 constexpr int kThr = 256;
 constexpr uint32_t kBox = 64 * 128;             // one 64-row x 128-byte SW128 box
-constexpr uint32_t kStageBytes = 5 * kBox;      // w (2 boxes), K (2), u half (1)
+constexpr uint32_t kStageBytes = 5 * kBox;      // w^T (128 rows: 2 boxes), K (2), u^T half (1)
 
 struct StateSmem {
     // 1024-byte aligned operand tiles first
@@ -57,16 +58,17 @@ struct StateMaps {
     CUtensorMap w, k, u, hc;
 };
 
-// w, K and (unless the columns are a transition's, whose u is zero) this half of u
-__device__ __forceinline__ void issue_stage(const StateMaps &m, StateSmem &sm, int st, int t0, int h,
-                                            int hv, int vb, bool with_u) {
+// Chunk c (tokens from t0): its w^T tile [k][t] (128 rows), K, and (unless the columns
+// are a transition's, whose u is zero) this half of its u^T tile [v'][t] (64 rows)
+__device__ __forceinline__ void issue_stage(const StateMaps &m, StateSmem &sm, const ChunkArgs &a, int st,
+                                            int c, int t0, int h, int hv, int vb, bool with_u) {
     unsigned char *b = sm.stage[st];
+    const int row = (c * a.HV + hv) * kDim;
     mbar_arrive_expect_tx(&sm.tma_bar[st], with_u ? kStageBytes : kStageBytes - kBox);
-    tma_load_3d(b + 0 * kBox, &m.w, 0, hv, t0, &sm.tma_bar[st]);
-    tma_load_3d(b + 1 * kBox, &m.w, 64, hv, t0, &sm.tma_bar[st]);
+    tma_load_3d(b + 0 * kBox, &m.w, 0, 0, row, &sm.tma_bar[st]);
     tma_load_3d(b + 2 * kBox, &m.k, 0, h, t0, &sm.tma_bar[st]);
     tma_load_3d(b + 3 * kBox, &m.k, 64, h, t0, &sm.tma_bar[st]);
-    if (with_u) tma_load_3d(b + 4 * kBox, &m.u, 64 * vb, hv, t0, &sm.tma_bar[st]);
+    if (with_u) tma_load_3d(b + 4 * kBox, &m.u, 0, 0, row + 64 * vb, &sm.tma_bar[st]);
 }
 
 __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kThr, 2)
     const uint32_t tH = t_row + c0, tP = t_row + 64 + c0;          // this warpgroup's columns
 
     if (tid == 0)
-        for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, i, chunk_t0(i), h, hv, vb, !phi);
+        for (int i = 0; i < 2 && i < nch; ++i) issue_stage(maps, sm, a, i, cb + jb + i, chunk_t0(i), h, hv, vb, !phi);
     // h <- h0[n][hv][k][v'] (row kr, this warpgroup's 32 columns), or in paged mode
     // the transpose of pool slot S[v'][k] (lanes are consecutive k: coalesced per v')
     const size_t sbase = ((size_t)n * a.HV + hv) * kDim * kDim + (size_t)kr * kDim + 64 * vb + c0;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThr, 2)
         if (nch > 1) fetch(1);
     }
     __syncthreads();
-    const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // P = w h       (h MN-major)
+    const uint32_t idP = idesc_bf16(64, 64, 1, 1);    // P = w h       (w^T and h MN-major)
     const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // h += K^T A_V  (both MN-major)
     uint32_t phase = 0;
     bool ok = true;
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(kThr, 2)
             const uint32_t as = smem_u32(sm.a_s), ws = smem_u32(sm.stage[st]);
 #pragma unroll
             for (int s = 0; s < 8; ++s)
-                mma_bf16(tbase + 64, sdesc(ws + (s >> 2) * kBox + (s & 3) * 32, 16, 1024),
-                         sdesc(as + s * 2048, kBox, 1024), idP, s > 0);
+                mma_bf16(tbase + 64, sdesc(ws + s * 2048, kBox, 1024), sdesc(as + s * 2048, kBox, 1024), idP,
+                         s > 0);
             mma_commit(&sm.mma_bar);
             if (!pre) {
                 tma_store_3d(&maps.hc, 64 * vb, 0, (c * a.HV + hv) * 128, sm.a_s);  // h_c rows (k)
@@ -274,14 +276,19 @@ __global__ void __launch_bounds__(kThr, 2)
             const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
             const bool la = ra < L, lb = rb < L;
             const float cfa = sm.coef[i & 1][ra], cfb = sm.coef[i & 1][rb];
-            const unsigned char *us = sm.stage[st] + 4 * kBox;
+            const unsigned char *us = sm.stage[st] + 4 * kBox;   // u^T [v'][t]
+            auto u2 = [&](int t, int v) {  // u[t][v], u[t][v + 1]
+                const bf16 *e0 = reinterpret_cast<const bf16 *>(us + sw128_off(v, t));
+                const bf16 *e1 = reinterpret_cast<const bf16 *>(us + sw128_off(v + 1, t));
+                return make_float2(__bfloat162float(*e0), __bfloat162float(*e1));
+            };
             bf16 *da = a.vnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
             bf16 *db = a.vnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int col = c0 + 8 * k + cq;
-                const float2 ua = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, ra, col);
-                const float2 ub = phi ? make_float2(0.f, 0.f) : epi::get_pair(us, rb, col);
+                const float2 ua = phi ? make_float2(0.f, 0.f) : u2(ra, col);
+                const float2 ub = phi ? make_float2(0.f, 0.f) : u2(rb, col);
                 const float va0 = la ? ua.x - p[4 * k] : 0.f, va1 = la ? ua.y - p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? ub.x - p[4 * k + 2] : 0.f, vb1 = lb ? ub.y - p[4 * k + 3] : 0.f;
                 if (la && !pre && in_range(da + col - a.vnew, 2, n_rows_hv(a), a.status))
@@ -314,7 +321,8 @@ __global__ void __launch_bounds__(kThr, 2)
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
-        if (tid == 0 && ok && i + 2 < nch) issue_stage(maps, sm, st, chunk_t0(i + 2), h, hv, vb, !phi);
+        if (tid == 0 && ok && i + 2 < nch)
+            issue_stage(maps, sm, a, st, c + 2, chunk_t0(i + 2), h, hv, vb, !phi);
         egl = egl_next;
     }
     ok = __syncthreads_and(ok);
@@ -412,9 +420,11 @@ cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
     StateMaps m;
     memset(&m, 0, sizeof(m));
     const uint64_t rowb = 128 * 2;
-    if (a.T > 0 && (!encode_rows_bf16(&m.w, a.w, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+    // w^T / u^T: rows of one chunk's 64 tokens (128 bytes), [C][HV][128] of them
+    const uint64_t wrows = (uint64_t)a.num_chunks * a.HV * kDim;
+    if (a.T > 0 && (!encode_rows_bf16(&m.w, a.w, 1, wrows, 128, 128, 128, kChunk) ||
         !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
-        !encode_rows_bf16(&m.u, a.u, a.HV, a.T, rowb, rowb * a.HV, 64) ||
+        !encode_rows_bf16(&m.u, a.u, 1, wrows, 128, 128, 64, kChunk) ||
         !encode_rows_bf16(&m.hc, a.hc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb, rowb, 128)))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(StateSmem) + 1024;

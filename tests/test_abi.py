@@ -53,11 +53,13 @@ def test_saved_and_workspace_sizes(lib):
 
     def al(x):
         return (x + 255) // 256 * 256
-    saved = (al(C * HV * D * D * 2) + al(T * HV * D * 2) + al(T * HV * D * 2)
+    # per-chunk h (bf16), v_new (bf16 per token), w^T per chunk (bf16 [C, HV, 128, 64]),
+    # the WY inverses (bf16 [C, HV, 64, 64]), r_q, r_k (per key head), G (per value head)
+    saved = (al(C * HV * D * D * 2) + al(T * HV * D * 2) + al(C * HV * D * 64 * 2)
              + al(C * HV * 64 * 64 * 2) + al(T * H * 4) + al(T * H * 4) + al(T * HV * 4))
     assert gdn.gdn_chunk_saved_bytes(p) == saved
     fwd_ws = gdn.gdn_chunk_workspace_bytes(p, 0)
-    assert fwd_ws >= saved + T * HV * D * 2
+    assert fwd_ws >= saved + C * HV * D * 64 * 2  # and u^T per chunk
     bwd_ws = gdn.gdn_chunk_workspace_bytes(p, 1)
     # dv_loc, dv_new, dW (bf16 per value head); the key heads' summed dkhat terms (bf16);
     # per-chunk dh (bf16)

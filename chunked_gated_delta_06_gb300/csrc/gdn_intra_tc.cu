@@ -71,15 +71,22 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
 // block ranges.  All 128 threads call it; X is scratch.
 __device__ __forceinline__ void tri_inverse(float *M, float *X, int tid) {
     // 16x16 diagonal blocks: thread (b, c) forward-substitutes column c of block b.
-    // t[m] stays 0 for m < c, so the fixed-range sums need no masks.
+    // t[m] stays 0 for m < c, so the fixed-range sums need no masks; a row of the
+    // block comes in as four 16-byte loads.
     float t[16];
     if (tid < 64) {
         const int base = (tid >> 4) * 16, c = tid & 15;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
+            float arow[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(&M[(base + r) * kS + base + 4 * q]);
+                arow[4 * q] = v.x; arow[4 * q + 1] = v.y; arow[4 * q + 2] = v.z; arow[4 * q + 3] = v.w;
+            }
             float x = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) x -= M[(base + r) * kS + base + m] * t[m];
+            for (int m = 0; m < r; ++m) x -= arow[m] * t[m];
             t[r] = x;
         }
     }
@@ -90,40 +97,47 @@ __device__ __forceinline__ void tri_inverse(float *M, float *X, int tid) {
         for (int r = 0; r < 16; ++r) M[(base + r) * kS + base + c] = t[r];
     }
     __syncthreads();
-    // block size 16: pairs p = 0, 1 (rows 32p+16.., columns 32p..); 2x2 outputs a thread
+    // block size 16: pairs p = 0, 1 (rows 32p+16.., columns 32p..); 2x2 outputs a
+    // thread; the A rows come four elements at a time, the right factor in pairs
     {
         const int p = tid >> 6, tt = tid & 63;
         const int r0 = 32 * p + 16, c0 = 32 * p;
         const int rr = 2 * (tt >> 3), cc = 2 * (tt & 7);
         float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float a0 = M[(r0 + rr) * kS + c0 + m], a1 = M[(r0 + rr + 1) * kS + c0 + m];
-            const float b0 = M[(c0 + m) * kS + c0 + cc], b1 = M[(c0 + m) * kS + c0 + cc + 1];
-            x00 += a0 * b0;
-            x01 += a0 * b1;
-            x10 += a1 * b0;
-            x11 += a1 * b1;
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&M[(r0 + rr) * kS + c0 + 4 * m4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&M[(r0 + rr + 1) * kS + c0 + 4 * m4]);
+            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 b = *reinterpret_cast<const float2 *>(&M[(c0 + 4 * m4 + e) * kS + c0 + cc]);
+                x00 += av0[e] * b.x;
+                x01 += av0[e] * b.y;
+                x10 += av1[e] * b.x;
+                x11 += av1[e] * b.y;
+            }
         }
-        X[(16 * p + rr) * kXs + cc] = x00;
-        X[(16 * p + rr) * kXs + cc + 1] = x01;
-        X[(16 * p + rr + 1) * kXs + cc] = x10;
-        X[(16 * p + rr + 1) * kXs + cc + 1] = x11;
+        *reinterpret_cast<float2 *>(&X[(16 * p + rr) * kXs + cc]) = make_float2(x00, x01);
+        *reinterpret_cast<float2 *>(&X[(16 * p + rr + 1) * kXs + cc]) = make_float2(x10, x11);
         __syncthreads();
         float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float a0 = M[(r0 + rr) * kS + r0 + m], a1 = M[(r0 + rr + 1) * kS + r0 + m];
-            const float b0 = X[(16 * p + m) * kXs + cc], b1 = X[(16 * p + m) * kXs + cc + 1];
-            y00 += a0 * b0;
-            y01 += a0 * b1;
-            y10 += a1 * b0;
-            y11 += a1 * b1;
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&M[(r0 + rr) * kS + r0 + 4 * m4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&M[(r0 + rr + 1) * kS + r0 + 4 * m4]);
+            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 b = *reinterpret_cast<const float2 *>(&X[(16 * p + 4 * m4 + e) * kXs + cc]);
+                y00 += av0[e] * b.x;
+                y01 += av0[e] * b.y;
+                y10 += av1[e] * b.x;
+                y11 += av1[e] * b.y;
+            }
         }
-        M[(r0 + rr) * kS + c0 + cc] = -y00;
-        M[(r0 + rr) * kS + c0 + cc + 1] = -y01;
-        M[(r0 + rr + 1) * kS + c0 + cc] = -y10;
-        M[(r0 + rr + 1) * kS + c0 + cc + 1] = -y11;
+        *reinterpret_cast<float2 *>(&M[(r0 + rr) * kS + c0 + cc]) = make_float2(-y00, -y01);
+        *reinterpret_cast<float2 *>(&M[(r0 + rr + 1) * kS + c0 + cc]) = make_float2(-y10, -y11);
         __syncthreads();
     }
     // block size 32: rows 32.., columns 0..; 2x4 outputs a thread
@@ -131,22 +145,32 @@ __device__ __forceinline__ void tri_inverse(float *M, float *X, int tid) {
         const int rr = 2 * (tid >> 3), cc = 4 * (tid & 7);
         float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            const float a0 = M[(32 + rr) * kS + m], a1 = M[(32 + rr + 1) * kS + m];
-            const float4 b = *reinterpret_cast<const float4 *>(&M[m * kS + cc]);
-            x0.x += a0 * b.x; x0.y += a0 * b.y; x0.z += a0 * b.z; x0.w += a0 * b.w;
-            x1.x += a1 * b.x; x1.y += a1 * b.y; x1.z += a1 * b.z; x1.w += a1 * b.w;
+        for (int m4 = 0; m4 < 8; ++m4) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&M[(32 + rr) * kS + 4 * m4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&M[(32 + rr + 1) * kS + 4 * m4]);
+            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 b = *reinterpret_cast<const float4 *>(&M[(4 * m4 + e) * kS + cc]);
+                x0.x += av0[e] * b.x; x0.y += av0[e] * b.y; x0.z += av0[e] * b.z; x0.w += av0[e] * b.w;
+                x1.x += av1[e] * b.x; x1.y += av1[e] * b.y; x1.z += av1[e] * b.z; x1.w += av1[e] * b.w;
+            }
         }
         *reinterpret_cast<float4 *>(&X[rr * kXs + cc]) = x0;
         *reinterpret_cast<float4 *>(&X[(rr + 1) * kXs + cc]) = x1;
         __syncthreads();
         float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            const float a0 = M[(32 + rr) * kS + 32 + m], a1 = M[(32 + rr + 1) * kS + 32 + m];
-            const float4 b = *reinterpret_cast<const float4 *>(&X[m * kXs + cc]);
-            y0.x += a0 * b.x; y0.y += a0 * b.y; y0.z += a0 * b.z; y0.w += a0 * b.w;
-            y1.x += a1 * b.x; y1.y += a1 * b.y; y1.z += a1 * b.z; y1.w += a1 * b.w;
+        for (int m4 = 0; m4 < 8; ++m4) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&M[(32 + rr) * kS + 32 + 4 * m4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&M[(32 + rr + 1) * kS + 32 + 4 * m4]);
+            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 b = *reinterpret_cast<const float4 *>(&X[(4 * m4 + e) * kXs + cc]);
+                y0.x += av0[e] * b.x; y0.y += av0[e] * b.y; y0.z += av0[e] * b.z; y0.w += av0[e] * b.w;
+                y1.x += av1[e] * b.x; y1.y += av1[e] * b.y; y1.z += av1[e] * b.z; y1.w += av1[e] * b.w;
+            }
         }
         *reinterpret_cast<float4 *>(&M[(32 + rr) * kS + cc]) = make_float4(-y0.x, -y0.y, -y0.z, -y0.w);
         *reinterpret_cast<float4 *>(&M[(32 + rr + 1) * kS + cc]) = make_float4(-y1.x, -y1.y, -y1.z, -y1.w);
@@ -315,11 +339,16 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
                 if (t_in) Tdst[q] = make_uint4(pack_bf2(t8[0], t8[1]), pack_bf2(t8[2], t8[3]), pack_bf2(t8[4], t8[5]),
                                                pack_bf2(t8[6], t8[7]));
                 const int jb = j0 + 8 * q;
+                float wc[8], bt[8];  // the column scales of the eight columns, 16 bytes at a time
+                *reinterpret_cast<float4 *>(wc) = *reinterpret_cast<const float4 *>(&sm.wc[jb]);
+                *reinterpret_cast<float4 *>(wc + 4) = *reinterpret_cast<const float4 *>(&sm.wc[jb + 4]);
+                *reinterpret_cast<float4 *>(bt) = *reinterpret_cast<const float4 *>(&sm.beta[jb]);
+                *reinterpret_cast<float4 *>(bt + 4) = *reinterpret_cast<const float4 *>(&sm.beta[jb + 4]);
                 uint32_t pw[4], pu[4];
     #pragma unroll
                 for (int z = 0; z < 4; ++z) {
-                    pw[z] = pack_bf2(t8[2 * z] * sm.wc[jb + 2 * z], t8[2 * z + 1] * sm.wc[jb + 2 * z + 1]);
-                    pu[z] = pack_bf2(t8[2 * z] * sm.beta[jb + 2 * z], t8[2 * z + 1] * sm.beta[jb + 2 * z + 1]);
+                    pw[z] = pack_bf2(t8[2 * z] * wc[2 * z], t8[2 * z + 1] * wc[2 * z + 1]);
+                    pu[z] = pack_bf2(t8[2 * z] * bt[2 * z], t8[2 * z + 1] * bt[2 * z + 1]);
                 }
                 *reinterpret_cast<uint4 *>(op_w + sw128_off(i, jb)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 *reinterpret_cast<uint4 *>(op_u + sw128_off(i, jb)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);

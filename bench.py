@@ -77,10 +77,9 @@ def kernel_work(name, T, H, HV, N, C_total):
         bstate=T * H * D * bf * 2 + TV * D * bf * 4 + C_total * HV * D * D * bf,
         # q, k; dO, dv_new, v_new in and dW out; dG; h_c, dh_c; dq and the summed dkhat out
         bintra_a=T * H * D * bf * 4 + TV * D * bf * 4 + TV * 4 + C_total * HV * D * D * bf * 2,
-        # k; v, dW, dv_new in and dv out; beta, G, dG, dg / dbeta; T; summed dkhat terms out
-        bintra_b=T * H * D * bf * 2 + TV * D * bf * 4 + TV * 12 + C_total * HV * C * C * 2,
-        # the two summed dkhat terms and k in, dk out; r_k
-        dknorm=T * H * D * bf * 4 + T * H * 4,
+        # k and the h / dh' dkhat terms in, dk out; v, dW, dv_new in and dv out; beta, G, dG,
+        # dg / dbeta; r_k; T
+        bintra_b=T * H * D * bf * 3 + TV * D * bf * 4 + TV * 12 + T * H * 4 + C_total * HV * C * C * 2,
     ).get(name, 0.0)
     return f, b
 
@@ -119,7 +118,7 @@ KERNEL_SOURCE = {
     "intra": "gdn_intra_tc.cu", "state": "gdn_state_tc.cu", "out": "gdn_out_tc.cu",
     "dvloc": "gdn_out_tc.cu", "bstate": "gdn_bstate_tc.cu", "bintra_a": "gdn_bintra_tc.cu",
     "bintra_b": "gdn_bintra_b_tc.cu", "decode": "gdn_decode.cu", "prep": "gdn_chunk.cu",
-    "plan": "gdn_chunk.cu", "dknorm": "gdn_chunk.cu",
+    "plan": "gdn_chunk.cu",
 }
 
 
@@ -572,7 +571,7 @@ NCU_KERNELS = {  # ncu kernel name -> bench kernel name (its source: KERNEL_SOUR
     "k_intra_tc": "intra", "k_state_tc": "state", "k_state_tc<0>": "state",
     "k_out_tc<1>": "out", "k_out_tc<true>": "out", "k_out_tc<0>": "dvloc", "k_out_tc<false>": "dvloc",
     "k_bstate_tc": "bstate", "k_bstate_tc<0>": "bstate", "k_bintra_a_tc": "bintra_a",
-    "k_bintra_b_tc": "bintra_b", "k_decode": "decode", "k_prep": "prep", "k_dknorm": "dknorm",
+    "k_bintra_b_tc": "bintra_b", "k_decode": "decode", "k_prep": "prep",
     "k_plan": "plan",
 }
 

@@ -185,7 +185,6 @@ void carve_bwd_ws(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.dhc = cv.take<bf16>((size_t)d.C * d.HV * D * D);
     a.dW = cv.take<bf16>((size_t)d.T * d.HV * D);
     a.dkpart = cv.take<bf16>((size_t)d.T * d.H * D);
-    a.dkpart2 = cv.take<bf16>((size_t)d.T * d.H * D);
     a.dGp = cv.take<float>((size_t)d.T * d.HV);
     a.gpart = cv.take<float>((size_t)d.C * d.HV * 2);
     carve_segments(cv, d, a);  // the reverse scan's segments (shared with a recomputed forward)
@@ -609,7 +608,7 @@ gdn_status gdn_check_indices(const int32_t *state_indices, int32_t batch, int32_
 const char *gdn_kernel_name(int32_t id) {
     static const char *names[GDN_KERNEL_COUNT] = {
         "plan", "prep", "intra", "state", "out", "dvloc", "bstate", "bintra_a", "bintra_b",
-        "dknorm", "decode", "seg_stitch"};
+        "decode", "seg_stitch"};
     return (id >= 0 && id < GDN_KERNEL_COUNT) ? names[id] : "unknown";
 }
 

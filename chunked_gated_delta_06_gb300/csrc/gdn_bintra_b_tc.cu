@@ -23,9 +23,12 @@
 // and dg is the reverse cumulative sum of dG (which arrives holding the h / dh'
 // and Q K^T terms).  A CTA walks whole groups of the r = HV / H value heads of one
 // key head and sums their dkhat terms in fp32 in spare TMEM columns (value heads in
-// order); after the group's last value head it writes the key head's sums (bf16
-// [T, H, 128]), which k_dknorm adds to the h / dh' and Q K^T terms before the L2-norm
-// backward.
+// order).  After the group's last value head it finishes dk for the key head: the
+// sums (staged as bf16 rows in shared memory) plus the h / dh' and Q K^T terms that
+// k_bintra_a_tc left (bf16 [T, H, 128]) give dkhat_t, and the L2-norm backward
+//   dk_t = (dkhat_t - k_t (k_t . dkhat_t) / r_k,t^2) / r_k,t
+// runs token-major, half a warp per token.
+#include <stddef.h>
 #include <string.h>
 
 #include "gdn_kernels.h"
@@ -65,12 +68,17 @@ struct BwSmem {
     float G[64], beta[64], rki[64], eg[64], dG[64], db[64];
     float rs[2][64];               // per-warpgroup partial row sums of P2
     float cy[4][64], cz[4][64], cp[4][64];  // per-row-block column sums
+    // (op_b and op_bt, adjacent, also hold a last value head's summed dkhat rows: bf16
+    // [t][128], 256-byte rows, once phase 2 has read them)
     uint64_t a_bar, v_bar, mma_bar;
     uint32_t tmem_base;
 };
 
+static_assert(offsetof(BwSmem, op_bt) == offsetof(BwSmem, op_b) + kHalf, "op_b, op_bt: one 16 KB tile");
+
 struct BwMaps {
     CUtensorMap k, v, dw, dvn, t;
+    CUtensorMap dkp;   // the h / dh' dkhat terms [T][H][128]: L2 prefetch for the dk pass
 };
 
 struct BwUnit {
@@ -167,6 +175,60 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         }
     };
     fetch(x);
+    // dk of a key head (after its last value head): half a warp per token, eight features
+    // a lane, four tokens a warp.  Every global load of the pass (k and the h / dh' dkhat
+    // terms, L2-warm from the prefetch at the unit's start) goes out before any is used;
+    // the staged WY sums (op_b / op_bt) are added, the L2-norm backward applied and dk
+    // stored.
+    const int l16 = lane & 15;
+    auto dk_pass = [&](int ut0, int uh, int uL) {
+        const size_t base = ((size_t)ut0 * a.H + uh) * kDim + 8 * l16;
+        uint4 lks[4], l1s[4];
+        uint32_t live = 0;
+    #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = 8 * warp + 2 * i + (lane >> 4);
+            const size_t row = base + (size_t)m * a.H * kDim;
+            lks[i] = make_uint4(0u, 0u, 0u, 0u);
+            l1s[i] = lks[i];
+            if (m < uL && in_range(row, 8, n_rows_h(a), a.status)) {
+                live |= 1u << i;
+                lks[i] = __ldg(reinterpret_cast<const uint4 *>(a.k + row));
+                l1s[i] = __ldg(reinterpret_cast<const uint4 *>(a.dkpart + row));
+            }
+        }
+        const bf16 *stg = reinterpret_cast<const bf16 *>(sm.op_b);
+    #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = 8 * warp + 2 * i + (lane >> 4);
+            const uint4 lk = lks[i], l1 = l1s[i];
+            const uint4 l2 = *reinterpret_cast<const uint4 *>(stg + m * kDim + 8 * l16);
+            const uint32_t wk[4] = {lk.x, lk.y, lk.z, lk.w}, w1[4] = {l1.x, l1.y, l1.z, l1.w},
+                           w2[4] = {l2.x, l2.y, l2.z, l2.w};
+            float xk[8], dd[8];
+    #pragma unroll
+            for (int u2 = 0; u2 < 4; ++u2) {
+                const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wk[u2]));
+                const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w1[u2]));
+                const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w2[u2]));
+                xk[2 * u2] = kk.x; xk[2 * u2 + 1] = kk.y;
+                dd[2 * u2] = p1.x + p2.x; dd[2 * u2 + 1] = p1.y + p2.y;
+            }
+            float dot = 0.f;
+    #pragma unroll
+            for (int u2 = 0; u2 < 8; ++u2) dot += xk[u2] * dd[u2];
+    #pragma unroll
+            for (int o = 8; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);  // the token's 16 lanes
+            const float ri = sm.rki[m], cdot = dot * ri * ri;
+            if ((live >> i) & 1u) {
+                uint32_t pk[4];
+    #pragma unroll
+                for (int u2 = 0; u2 < 4; ++u2)
+                    pk[u2] = pack_bf2((dd[2 * u2] - xk[2 * u2] * cdot) * ri, (dd[2 * u2 + 1] - xk[2 * u2 + 1] * cdot) * ri);
+                *reinterpret_cast<uint4 *>(a.dk + base + (size_t)m * a.H * kDim) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+    };
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(sub * 32) << 16);
     uint32_t phase = 0;
@@ -194,6 +256,10 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         };
         // ---- phase 1: KK, D1, D2 (64 x 64, contraction 128)
         if (tid == 0 && ok) {
+            if (hv % (a.HV / a.H) == a.HV / a.H - 1) {  // a last value head: warm L2 for its dk pass
+                tma_prefetch_3d(&maps.dkp, 0, x.h, t0);
+                tma_prefetch_3d(&maps.dkp, 64, x.h, t0);
+            }
             tc_fence_after();
             const uint32_t id = idesc_bf16(64, 64, 0, 0);
             const uint32_t A[3] = {smem_u32(sm.k), smem_u32(sm.dw), smem_u32(sm.dvn)};
@@ -373,8 +439,6 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             const int d = sub * 32 + lane, odd = lane & 1;
             const size_t ts = (size_t)a.HV * kDim;
             const size_t base = ((size_t)t0 * a.HV + hv) * kDim + (d & ~1) + (size_t)odd * ts;
-            const size_t hs = (size_t)a.H * kDim;
-            const size_t kbase = ((size_t)t0 * a.H + x.h) * kDim + (d & ~1) + (size_t)odd * hs;
     #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {  // 16 token columns at a time
                 const int m0 = j0 + 16 * hh;
@@ -398,11 +462,10 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
                         const size_t o = base + (size_t)me * ts;
                         *reinterpret_cast<uint32_t *>(a.dv + o) = odd ? pack_bf2(rv, v1) : pack_bf2(v0, rv);
                     }
-                    if (last) {  // the key head's summed terms, bf16 pairs as dv
-                        const float rk = __shfl_xor_sync(0xffffffffu, odd ? acc[2 * jj] : acc[2 * jj + 1], 1);
-                        if (me + odd < L && in_range(kbase + (size_t)me * hs, 2, n_rows_h(a), a.status))
-                            *reinterpret_cast<uint32_t *>(a.dkpart2 + kbase + (size_t)me * hs) =
-                                odd ? pack_bf2(rk, acc[2 * jj + 1]) : pack_bf2(acc[2 * jj], rk);
+                    if (last) {  // the key head's summed terms, staged as bf16 rows [t][d]
+                        bf16 *stg = reinterpret_cast<bf16 *>(sm.op_b);
+                        stg[me * kDim + d] = __float2bfloat16_rn(acc[2 * jj]);
+                        stg[(me + 1) * kDim + d] = __float2bfloat16_rn(acc[2 * jj + 1]);
                     }
                 }
                 if (!last) tmem_st16(t_row + cACC + m0, acc);
@@ -412,6 +475,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             atomicOr(a.status, 2);
         }
         __syncthreads();
+        if (ok && last) dk_pass(t0, x.h, L);
         if (ok && warp == 0) {  // dg = reverse cumulative sum of dG (warp scan), dbeta
             float dgv[2];
     #pragma unroll
@@ -480,7 +544,8 @@ cudaError_t launch_bintra_b_tc(const ChunkArgs &a, cudaStream_t s) {
         !encode_rows_bf16(&m.v, a.v, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dw, a.dW, a.HV, a.T, rowb, rowb * a.HV, 64) ||
         !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64) ||
-        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64))
+        !encode_rows_bf16(&m.t, a.Tm, 1, (uint64_t)a.num_chunks * a.HV * 64, 128, 128, 64, 64) ||
+        !encode_rows_bf16(&m.dkp, a.dkpart, a.H, a.T, rowb, rowb * a.H, 64))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BwSmem) + 1024;
     static_assert(2 * (sizeof(BwSmem) + 2048) <= 233472, "two CTAs per SM");

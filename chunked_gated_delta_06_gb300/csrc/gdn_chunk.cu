@@ -6,8 +6,7 @@
 //            partial), "[Cake 1/13] gdn: chunked gated delta rule ...", API;
 //   k_prep   q / k norms r = sqrt(sum x^2 + 1e-6) ("C6: GDN decode-step
 //            goldens ...", Provider: divide by the sqrt) and the chunk-local
-//            cumulative sum G of g;
-//   k_dknorm the last step of the backward: dk through the L2-norm backward.
+//            cumulative sum G of g.
 // The tensor-core kernels of the chunked (WY) form live in gdn_*_tc.cu.
 // Every reduction runs in a fixed order and no kernel uses atomics, so results
 // are bit-identical from run to run.
@@ -148,58 +147,6 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// Backward, last step: dk of each (token, key head) from its khat gradient, the sum of
-// the two kernels' terms (each already summed over the value heads of the key head),
-// through the L2-norm backward dk = (dkhat - khat (khat . dkhat)) / r_k with
-// khat = k / r_k ("C6: GDN decode-step goldens ...", Provider: the norm divides by the
-// sqrt).  Half a warp per item: each lane moves 8 elements with 16-byte loads and stores.
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
-    const float2 a0 = bf2_to_f2(u.x), a1 = bf2_to_f2(u.y), a2 = bf2_to_f2(u.z), a3 = bf2_to_f2(u.w);
-    x[0] = a0.x; x[1] = a0.y; x[2] = a1.x; x[3] = a1.y; x[4] = a2.x; x[5] = a2.y; x[6] = a3.x; x[7] = a3.y;
-}
-
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&t);
-}
-
-__global__ void __launch_bounds__(kThreads) k_dknorm(ChunkArgs a) {
-    const int l16 = threadIdx.x & 15;
-    const size_t item = (size_t)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
-    const size_t row0 = item * kDim + l16 * 8;  // item = t H + h
-    const bool valid = item < (size_t)a.T * a.H && in_range(row0, 8, n_rows_h(a), a.status);
-    const size_t row = valid ? row0 : 0;
-    uint4 lk = make_uint4(0u, 0u, 0u, 0u), l1 = lk, l2 = lk;
-    float rk = 1.f;
-    if (valid) {
-        lk = *reinterpret_cast<const uint4 *>(a.k + row);
-        l1 = *reinterpret_cast<const uint4 *>(a.dkpart + row);
-        l2 = *reinterpret_cast<const uint4 *>(a.dkpart2 + row);
-        rk = a.rk[item];
-    }
-    float xk[8], d1[8], d2[8];
-    unpack8(lk, xk);
-    unpack8(l1, d1);
-    unpack8(l2, d2);
-    float dot = 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        d1[u] += d2[u];
-        dot += xk[u] * d1[u];
-    }
-#pragma unroll
-    for (int o = 8; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);  // the 16 lanes of the item
-    const float ri = 1.f / rk, c = dot * ri * ri;
-    if (valid) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            pk[u] = pack2((d1[2 * u] - xk[2 * u] * c) * ri, (d1[2 * u + 1] - xk[2 * u + 1] * c) * ri);
-        *reinterpret_cast<uint4 *>(a.dk + row) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_plan(const ChunkArgs &a, cudaStream_t s) {
@@ -266,15 +213,7 @@ cudaError_t launch_bwd_chunks(const ChunkArgs &a, cudaStream_t s) {
     if ((e = launch_bstate_tc(a, s)) != cudaSuccess) return e;
     if (a.num_chunks == 0) return cudaSuccess;
     if ((e = launch_bintra_a_tc(a, s)) != cudaSuccess) return e;
-    if ((e = launch_bintra_b_tc(a, s)) != cudaSuccess) return e;
-    {
-        const size_t items = (size_t)a.T * a.H;
-        const unsigned blocks = (unsigned)((items + kThreads / 16 - 1) / (kThreads / 16));
-        TimerScope ts(a.timer, GDN_KERNEL_DKNORM, s);
-        k_dknorm<<<blocks, kThreads, 0, s>>>(a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    return launch_bintra_b_tc(a, s);  // ends with dk (the L2-norm backward of khat)
 }
 
 }  // namespace gdn

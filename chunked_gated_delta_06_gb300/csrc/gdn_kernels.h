@@ -69,7 +69,6 @@ struct ChunkArgs {
     bf16 *dW;               // [T,HV,K]
     bf16 *dkpart;           // [T,H,K] the h / dh' and Q K^T terms of the khat gradient,
                             // summed over the value heads of each key head
-    bf16 *dkpart2;          // [T,H,K] the WY-pullback terms of the khat gradient, summed
                             // the same way
     float *dGp;             // [T,HV]
     gdn_kernel_timer *timer;  // optional per-kernel events

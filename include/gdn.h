@@ -337,9 +337,9 @@ enum {
     GDN_KERNEL_BSTATE,       /* backward reverse state scan: dh, dv_new, dh0 */
     GDN_KERNEL_BINTRA_A,     /* backward: terms through h and dh; dq (summed over the
                                 value heads of a key head, L2-norm backward applied) */
-    GDN_KERNEL_BINTRA_B,     /* backward: intra-chunk terms, WY pullback, dg */
-    GDN_KERNEL_DKNORM,       /* backward: dk (the khat gradient summed over the value
-                                heads, through the L2-norm backward) */
+    GDN_KERNEL_BINTRA_B,     /* backward: intra-chunk terms, WY pullback, dg, and dk
+                                (the khat gradient summed over the value heads of a
+                                key head, L2-norm backward applied) */
     GDN_KERNEL_DECODE,       /* decode step */
     GDN_KERNEL_SEG_STITCH,   /* segment-parallel state scan: start states of the segments */
     GDN_KERNEL_COUNT

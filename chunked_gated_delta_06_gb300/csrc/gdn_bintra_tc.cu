@@ -3,9 +3,11 @@
 // through the intra-chunk attention matrix, on the tensor cores ("dqkwg" of
 // "cake_gdn: deterministic chunked GDN training kernels", section 2).
 //
-// Persistent: one CTA of 256 threads per SM walks a contiguous run of (chunk,
-// value head) units, and the next unit's h, dh', dO, dv_new and v_new tiles load
-// as soon as batch 1 has consumed the current ones; q and k (only when the key head
+// Persistent: one CTA of 512 threads per SM walks a contiguous run of (chunk,
+// value head) units.  Its two halves of two warpgroups split every epilogue by
+// side: the first takes the Q K^T / dM terms and the dq terms, the second dW and
+// the dk terms.  The next unit's h, dh', dO, dv_new and v_new tiles load as soon
+// as batch 1 has consumed the current ones; q and k (only when the key head
 // changes) load into a second buffer at the start of the unit before, so the loads
 // run under the epilogues.  With h_c, dh_c [k][v] (bf16,
 // from the forward and reverse scans), dO, dv_new, v_new [t][v], Qhat =
@@ -52,7 +54,7 @@ using epi::put_pair;
 using epi::quad_sum;
 using epi::tmem_ld16x256_x4;
 
-constexpr int kThr = 256;
+constexpr int kThr = 512;   // two halves of two warpgroups: the dq side and the dk side
 constexpr uint32_t kBox = 64 * 128;       // 64 rows x 128 B
 constexpr uint32_t kBig = 128 * 128;      // 128 rows x 128 B
 
@@ -159,8 +161,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
     if (ub >= ue) return;
-    const int grp = warp >> 2;
-    const int sub = warp & 3;
+    const int side = warp >> 3;        // 0: (a) and the dq terms; 1: (b) and the dk terms
+    const int grp = (warp >> 2) & 1;   // warpgroup within the side: which column half
+    const int sub = warp & 3;          // TMEM lane quarter
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     bool need_b = true;   // the current unit waits for a q / k load
     // Warp 0 issues the products and does nothing else while they run (its issuing
     // thread stalls for as long as the tensor pipe is full); warps 2 and 3 own the
-    // per-token scalars (token ft = tid - 64), fetched one unit ahead, and warps 4..7
+    // per-token scalars (token ft = tid - 64), fetched one unit ahead, and warps 8..11
     // the <h, dh'> dot.
     const int ft = tid - 64;
     const bool scal = ft >= 0 && ft < 64;
@@ -260,10 +263,10 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             if (tid == 0) issue_b(maps, sm, nx, bcur ^ 1);
             bpend |= 1u << (bcur ^ 1);
         }
-        // <h, dh'> while the products run: thread tid - 128 of warps 4..7 takes a row
+        // <h, dh'> while the products run: thread tid - 256 of warps 8..11 takes a row
         // of h and dh'
-        if (warp >= 4) {
-            const int kr = tid - 128;
+        if (warp >= 8 && warp < 12) {
+            const int kr = tid - 256;
             float hdh = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half)
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                     }
                 }
             hdh = warp_sum(hdh);
-            if (lane == 0) sm.hdh[warp - 4] = hdh;
+            if (lane == 0) sm.hdh[warp - 8] = hdh;
         }
         if (tid == 0) tma_store_wait_read();  // the last unit's staged rows have been read
         bool done = __syncthreads_and(mbar_wait(&sm.mma_bar, phase));
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         }
         const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);  // fragment rows / column
         const bool la = ra < L, lb = rb < L;
-        {
+        if (side == 0) {
             // (a) QK, dM -> P1 (row and column sums) and the two dMG operand rows, read
             // as 16x256b fragments: rows ra, rb = ra + 8, columns j0 + 8k + cq + {0, 1}
             const int j0 = 32 * grp;
@@ -333,6 +336,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 sm.rp[grp][ra] = rsa;
                 sm.rp[grp][rb] = rsb;
             }
+        } else {
             // (b) dW = -Dw rows on 16x256b fragments: rows ra, rb, this warpgroup's 64
             // columns 64 grp + 32 cc + 8k + cq + {0, 1}; a full chunk's rows are staged
             // (this warpgroup's 64-column half of stg) for one TMA store
@@ -392,9 +396,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
            // c0 + 8k + cq + {0, 1})
             const float ega = la ? sm.eg[ra] : 0.f, egb = lb ? sm.eg[rb] : 0.f;
             const float ela = la ? sm.egl_g[ra] : 0.f, elb = lb ? sm.egl_g[rb] : 0.f;
-            float xqa = 0.f, xqb = 0.f, xka = 0.f, xkb = 0.f, pna = 0.f, pnb = 0.f;
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {  // m = 0: dq with q; m = 1: dk with k
+            float pna = 0.f, pnb = 0.f;
+            {
+                const int m = side;  // 0: dq with q; 1: dk with k
                 const uint32_t cA = m ? cDK : cDQ, cB = m ? cKI : cQI;
                 const unsigned char *tile = m ? sm.k[bcur] : sm.q[bcur];
                 const float fa = m ? ela : ega, fb = m ? elb : egb;
@@ -427,16 +431,16 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                     }
                     epi::tmem_st16x256_x4(t_row + kAccLanes + cA + c0, acc);
                 }
-                if (m) { xka = xa; xkb = xb; } else { xqa = xa; xqb = xb; }
+                xa = quad_sum(xa); xb = quad_sum(xb);
+                tmem_st_wait();
+                if ((lane & 3) == 0) {
+                    float (*dst)[64] = m ? sm.pk : sm.pq;
+                    dst[grp][ra] = xa; dst[grp][rb] = xb;
+                }
             }
-            xqa = quad_sum(xqa); xqb = quad_sum(xqb);
-            xka = quad_sum(xka); xkb = quad_sum(xkb);
-            tmem_st_wait();
-            if (last) { pna = quad_sum(pna); pnb = quad_sum(pnb); }
-            if ((lane & 3) == 0) {
-                sm.pq[grp][ra] = xqa; sm.pq[grp][rb] = xqb;
-                sm.pk[grp][ra] = xka; sm.pk[grp][rb] = xkb;
-                if (last) { sm.pn[grp][ra] = pna; sm.pn[grp][rb] = pnb; }
+            if (side == 0 && last) {
+                pna = quad_sum(pna); pnb = quad_sum(pnb);
+                if ((lane & 3) == 0) { sm.pn[grp][ra] = pna; sm.pn[grp][rb] = pnb; }
             }
         }
         __syncthreads();  // q / k tiles, TMEM and the row sums are all read or written
@@ -448,34 +452,33 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             const float Pb = (sm.pn[0][rb] + sm.pn[1][rb]) * ib * ib;
             const size_t oa = ((size_t)(x.t0 + (la ? ra : 0)) * a.H + x.h) * kDim;
             const size_t ob = ((size_t)(x.t0 + (lb ? rb : 0)) * a.H + x.h) * kDim;
+            // side 0: dq (staged in op_dmg); side 1: the summed dkhat terms (staged in stg)
+            bf16 *gout = side ? a.dkpart : a.dq;
+            unsigned char *st = side ? sm.stg : sm.op_dmg;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int c0 = 32 * (2 * grp + h2);
                 const unsigned char *half = sm.q[bcur] + (c0 >> 6) * kBox;
-                float aq[16], ak[16];
-                tmem_ld16x256_x4(t_row + kAccLanes + cDQ + c0, aq);
-                tmem_ld16x256_x4(t_row + kAccLanes + cDK + c0, ak);
+                float av[16];
+                tmem_ld16x256_x4(t_row + kAccLanes + (side ? cDK : cDQ) + c0, av);
                 tmem_ld_wait();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int col = (c0 & 63) + 8 * k + cq, gcol = c0 + 8 * k + cq;
-                    const float2 qa = get_pair(half, ra, col), qb = get_pair(half, rb, col);
-                    const float q0 = sa * (aq[4 * k] - qa.x * Pa), q1 = sa * (aq[4 * k + 1] - qa.y * Pa);
-                    const float q2 = sb * (aq[4 * k + 2] - qb.x * Pb), q3 = sb * (aq[4 * k + 3] - qb.y * Pb);
+                    float v0 = av[4 * k], v1 = av[4 * k + 1], v2 = av[4 * k + 2], v3 = av[4 * k + 3];
+                    if (side == 0) {
+                        const float2 qa = get_pair(half, ra, col), qb = get_pair(half, rb, col);
+                        v0 = sa * (v0 - qa.x * Pa); v1 = sa * (v1 - qa.y * Pa);
+                        v2 = sb * (v2 - qb.x * Pb); v3 = sb * (v3 - qb.y * Pb);
+                    }
                     if (L == 64) {
-                        put_pair(sm.op_dmg + (c0 >> 6) * kBox, ra, col, q0, q1);
-                        put_pair(sm.op_dmg + (c0 >> 6) * kBox, rb, col, q2, q3);
-                        put_pair(sm.stg + (c0 >> 6) * kBox, ra, col, ak[4 * k], ak[4 * k + 1]);
-                        put_pair(sm.stg + (c0 >> 6) * kBox, rb, col, ak[4 * k + 2], ak[4 * k + 3]);
+                        put_pair(st + (c0 >> 6) * kBox, ra, col, v0, v1);
+                        put_pair(st + (c0 >> 6) * kBox, rb, col, v2, v3);
                     } else {
-                        if (la && in_range(oa + gcol, 2, n_rows_h(a), a.status)) {
-                            *reinterpret_cast<uint32_t *>(a.dq + oa + gcol) = pack_bf2(q0, q1);
-                            *reinterpret_cast<uint32_t *>(a.dkpart + oa + gcol) = pack_bf2(ak[4 * k], ak[4 * k + 1]);
-                        }
-                        if (lb && in_range(ob + gcol, 2, n_rows_h(a), a.status)) {
-                            *reinterpret_cast<uint32_t *>(a.dq + ob + gcol) = pack_bf2(q2, q3);
-                            *reinterpret_cast<uint32_t *>(a.dkpart + ob + gcol) = pack_bf2(ak[4 * k + 2], ak[4 * k + 3]);
-                        }
+                        if (la && in_range(oa + gcol, 2, n_rows_h(a), a.status))
+                            *reinterpret_cast<uint32_t *>(gout + oa + gcol) = pack_bf2(v0, v1);
+                        if (lb && in_range(ob + gcol, 2, n_rows_h(a), a.status))
+                            *reinterpret_cast<uint32_t *>(gout + ob + gcol) = pack_bf2(v2, v3);
                     }
                 }
             }
@@ -569,7 +572,7 @@ cudaError_t launch_bintra_a_tc(const ChunkArgs &a, cudaStream_t s) {
     const int grid = ngroups < sms ? ngroups : sms;
     const int per = (ngroups + grid - 1) / grid * r;
     TimerScope ts(a.timer, GDN_KERNEL_BINTRA_A, s);
-    k_bintra_a_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);
+    k_bintra_a_tc<<<(nunits + per - 1) / per, kThr, smem, s>>>(a, m, per);  // 16 warps
     return cudaGetLastError();
 }
 

@@ -296,6 +296,13 @@ __global__ void __launch_bounds__(kThr, 2)
                 epi::put_pair(sm.a_do, rb, col, fb.x * qb, fb.y * qb);
             }
         }
+        // while the product runs: publish the next step's scalars (their buffer is not
+        // this one's), and fetch one step further, ahead of this step's global stores
+        float egl_next = egl;
+        if (i + 1 < nch) {
+            egl_next = publish((i + 1) & 1);
+            if (i + 2 < nch) fetch(i + 2);
+        }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
@@ -327,11 +334,6 @@ __global__ void __launch_bounds__(kThr, 2)
                 epi::put_pair(sm.a_dv, ra, col, -va0, -va1);
                 epi::put_pair(sm.a_dv, rb, col, -vb0, -vb1);
             }
-        }
-        float egl_next = egl;
-        if (i + 1 < nch) {  // publish the next step's scalars, and fetch one step further
-            egl_next = publish((i + 1) & 1);
-            if (i + 2 < nch) fetch(i + 2);
         }
         if (tid == 0) tma_store_wait_read();  // dh_c has been read out of a_ds
         const bool gy = mbar_wait(&sm.y_bar, par);

@@ -264,6 +264,13 @@ __global__ void __launch_bounds__(kThr, 2)
                 tma_store_commit();
             }
         }
+        // while the product runs: publish the next chunk's scalars (their buffer is not
+        // this one's), and fetch one chunk further, ahead of this chunk's global stores
+        float egl_next = egl;
+        if (i + 1 < nch) {
+            egl_next = publish((i + 1) & 1);
+            if (i + 2 < nch) fetch(i + 2);
+        }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
@@ -298,11 +305,6 @@ __global__ void __launch_bounds__(kThr, 2)
                 epi::put_pair(sm.a_v, ra, col, va0 * cfa, va1 * cfa);
                 epi::put_pair(sm.a_v, rb, col, vb0 * cfb, vb1 * cfb);
             }
-        }
-        float egl_next = egl;
-        if (i + 1 < nch) {  // publish the next chunk's scalars, and fetch one chunk further
-            egl_next = publish((i + 1) & 1);
-            if (i + 2 < nch) fetch(i + 2);
         }
         if (tid == 0) tma_store_wait_read();  // h_c has been read out of a_s
         fence_proxy_async_smem();

@@ -69,12 +69,14 @@ def kernel_work(name, T, H, HV, N, C_total):
     bf = 2
     b = dict(
         plan=4 * (N + 1 + 3 * C_total),
-        prep=T * H * D * bf * 2 + TV * 4 * 2 + T * H * 8,
+        # q, k in; g in and G out; r_q, r_k out; the scans' scalar records out
+        prep=T * H * D * bf * 2 + TV * 4 * 2 + T * H * 8 + C_total * HV * 132 * 4,
         intra=T * H * D * bf + TV * D * bf + TV * 6 + TV * D * bf * 2 + C_total * HV * C * C * 2,
-        state=TV * D * bf * 3 + T * H * D * bf + C_total * HV * D * D * bf + N * HV * D * D * 8,
+        state=TV * D * bf * 3 + T * H * D * bf + C_total * HV * D * D * bf + N * HV * D * D * 8
+        + C_total * HV * 132 * 4,
         out=T * H * D * bf * 2 + TV * D * bf * 2 + C_total * HV * D * D * bf,
         dvloc=T * H * D * bf * 2 + TV * D * bf * 2,
-        bstate=T * H * D * bf * 2 + TV * D * bf * 4 + C_total * HV * D * D * bf,
+        bstate=T * H * D * bf * 2 + TV * D * bf * 4 + C_total * HV * D * D * bf + C_total * HV * 132 * 4,
         # q, k; dO, dv_new, v_new in and dW out; dG; h_c, dh_c; dq and the summed dkhat out
         bintra_a=T * H * D * bf * 4 + TV * D * bf * 4 + TV * 4 + C_total * HV * D * D * bf * 2,
         # k and the h / dh' dkhat terms in, dk out; v, dW, dv_new in and dv out; beta, G, dG,

@@ -151,6 +151,7 @@ void carve_saved(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {
     a.rq = cv.take<float>((size_t)d.T * d.H);
     a.rk = cv.take<float>((size_t)d.T * d.H);
     a.G = cv.take<float>((size_t)d.T * d.HV);
+    a.sc = cv.take<float>((size_t)d.C * d.HV * gdn::kScRec);
 }
 
 void carve_table(Carver &cv, const Dims &d, gdn::ChunkArgs &a) {

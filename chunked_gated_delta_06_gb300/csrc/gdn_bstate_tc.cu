@@ -22,8 +22,9 @@
 // that two CTAs share an SM, and each group is reloaded for the next chunk as
 // soon as it is free: K after step 2, the halves of dO and dv_loc after step 3,
 // Q and w after step 4; every tile of the chunk after that is prefetched into L2
-// a step ahead.  The next chunk's per-token scalars are loaded a step ahead and
-// published during the current epilogue; a chunk costs two block barriers.
+// a step ahead.  The chunk's scalar record (kc_t = e^{G_L - G_t} / r_k,t, qc_t =
+// e^{G_t} scale / r_q,t and e^{G_L}, written by k_prep) comes with K, into one of two
+// buffers by the parity of the step; a chunk costs two block barriers.
 // Waits are bounded.  Long sequences with few heads can be scanned segment-
 // parallel (the plan of the forward scan; see k_bstate_tc).
 #include <string.h>
@@ -49,8 +50,7 @@ struct BStateSmem {
     unsigned char a_dv[64 * 128];       // -dv_new bf16 [t][v']
     unsigned char x[kXBytes];
     unsigned char y[kYBytes];
-    float kc[2][64];                    // e^{G_L - G_t} / r_k,t (0 past L), this and the next chunk
-    float qc[2][64];                    // e^{G_t} scale / r_q,t (0 past L)
+    ScRec sc[2];                        // the scalar records of this and the next step
     uint64_t xk_bar, xd_bar, y_bar, mma_bar;   // X = K (xk) + dO, dv_loc halves (xd); Y = Q, w
     uint32_t tmem_base;
 };
@@ -59,8 +59,11 @@ struct BStateMaps {
     CUtensorMap k, q, w, dO, dl, dhc;
 };
 
-__device__ __forceinline__ void issue_xk(const BStateMaps &m, BStateSmem &sm, int t0, int h) {
-    mbar_arrive_expect_tx(&sm.xk_bar, 2 * kBox);
+// K of chunk c (tokens from t0) and its scalar record, into record buffer rb
+__device__ __forceinline__ void issue_xk(const BStateMaps &m, BStateSmem &sm, const ChunkArgs &a, int c, int t0,
+                                         int h, int hv, int rb) {
+    mbar_arrive_expect_tx(&sm.xk_bar, 2 * kBox + (uint32_t)sizeof(ScRec));
+    bulk_load(&sm.sc[rb], a.sc + ((size_t)c * a.HV + hv) * kScRec, sizeof(ScRec), &sm.xk_bar);
     tma_load_3d(sm.x + 0 * kBox, &m.k, 0, h, t0, &sm.xk_bar);
     tma_load_3d(sm.x + 1 * kBox, &m.k, 64, h, t0, &sm.xk_bar);
 }
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kThr, 2)
 
     int xk_issued = 0, xd_issued = 0, y_issued = 0;  // thread 0's load counts
     if (tid == 0 && nch > 0) {
-        issue_xk(maps, sm, step_t0(0), h);
+        issue_xk(maps, sm, a, step_c(0), step_t0(0), h, hv, 0);
         if (!phi) issue_xd(maps, sm, step_t0(0), hv, vb);
         issue_y(maps, sm, a, step_c(0), step_t0(0), h, hv);
         if (nch > 1) prefetch_chunk(maps, a, step_c(1), step_t0(1), h, hv, vb, !phi);
@@ -208,36 +211,6 @@ __global__ void __launch_bounds__(kThr, 2)
         tmem_st32(tS, r);
         tmem_st_wait();
     }
-    // per-chunk scalars: the raw values are loaded one step ahead (pgl: G_L; pg,
-    // prk, prq: G_t, r_k,t, r_q,t of thread t < 64) and turned into kc_t, qc_t and
-    // e^{G_L} only when they are published a step later, so no thread waits on the loads
-    float pgl = 0.f, pg = 0.f, prk = 1.f, prq = 1.f;
-    bool pin = false;
-    auto fetch = [&](int i) {
-        const int tt0 = step_t0(i), LL = step_len(i);
-        const size_t gl = (size_t)(tt0 + LL - 1) * a.HV + hv;
-        pgl = in_range(gl, 1, n_tok_hv(a), a.status) ? a.G[gl] : 0.f;
-        pin = tid < LL && in_range((size_t)(tt0 + tid) * a.HV + hv, 1, n_tok_hv(a), a.status);
-        if (pin) {
-            const size_t t = (size_t)(tt0 + tid);
-            pg = a.G[t * a.HV + hv];
-            prk = a.rk[t * a.H + h];
-            prq = a.rq[t * a.H + h];
-        }
-    };
-    auto publish = [&](int buf) {  // returns e^{G_L}
-        if (tid < 64) {
-            sm.kc[buf][tid] = pin ? __expf(fminf(pgl - pg, 0.f)) / prk : 0.f;
-            sm.qc[buf][tid] = pin ? __expf(pg) * a.scale / prq : 0.f;
-        }
-        return __expf(pgl);
-    };
-    float egl = 1.f;
-    if (nch > 0) {
-        fetch(0);
-        egl = publish(0);
-        if (nch > 1) fetch(1);
-    }
     __syncthreads();
     const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // Pd = K dh'          (dh' MN-major)
     const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // dh += Q^T A       (both MN-major)
@@ -248,6 +221,10 @@ __global__ void __launch_bounds__(kThr, 2)
         const int c = step_c(i);
         const uint32_t par = i & 1;
         const int t0 = step_t0(i), L = step_len(i);
+        const ScRec &rec = sm.sc[par];
+        // K and the scalar record (e^{G_L} is needed right below)
+        const bool gk = mbar_wait(&sm.xk_bar, par);
+        const float egl = rec.egl;
         // 1. dh' -> bf16 operand (copied to dh_c by TMA below), then dh <- e^{G_L} dh'
         {
             float r[32];
@@ -265,7 +242,7 @@ __global__ void __launch_bounds__(kThr, 2)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        const bool gx = mbar_wait(&sm.xk_bar, par) && (phi || mbar_wait(&sm.xd_bar, par));
+        const bool gx = gk && (phi || mbar_wait(&sm.xd_bar, par));
         ok = __syncthreads_and(ok && gx);
         if (!ok) break;
         // 2. Pd = K dh'
@@ -286,7 +263,7 @@ __global__ void __launch_bounds__(kThr, 2)
         // columns c0 + 8k + cq + {0, 1}); transition columns have no dO term
         const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
         if (!phi) {
-            const float qa = sm.qc[i & 1][ra], qb = sm.qc[i & 1][rb];
+            const float qa = rec.qc[ra], qb = rec.qc[rb];
             const unsigned char *dos = sm.x + 2 * kBox;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -296,18 +273,11 @@ __global__ void __launch_bounds__(kThr, 2)
                 epi::put_pair(sm.a_do, rb, col, fb.x * qb, fb.y * qb);
             }
         }
-        // while the product runs: publish the next step's scalars (their buffer is not
-        // this one's), and fetch one step further, ahead of this step's global stores
-        float egl_next = egl;
-        if (i + 1 < nch) {
-            egl_next = publish((i + 1) & 1);
-            if (i + 2 < nch) fetch(i + 2);
-        }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
         if (tid == 0 && ok && i + 1 < nch) {  // K has been read by step 2
-            issue_xk(maps, sm, step_t0(i + 1), h);
+            issue_xk(maps, sm, a, step_c(i + 1), step_t0(i + 1), h, hv, par ^ 1);
             ++xk_issued;
         }
         // 3. dv_new = dv_loc + kc_t Pd on 16x256b fragments
@@ -316,7 +286,7 @@ __global__ void __launch_bounds__(kThr, 2)
             epi::tmem_ld16x256_x4(tP, p);
             tmem_ld_wait();
             const bool la = ra < L, lb = rb < L;
-            const float ka = sm.kc[i & 1][ra], kb = sm.kc[i & 1][rb];
+            const float ka = rec.kc[ra], kb = rec.kc[rb];
             const unsigned char *dls = sm.x + 3 * kBox;
             bf16 *da = a.dvnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
             bf16 *db = a.dvnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
@@ -367,7 +337,6 @@ __global__ void __launch_bounds__(kThr, 2)
             issue_y(maps, sm, a, step_c(i + 1), step_t0(i + 1), h, hv);
             ++y_issued;
         }
-        egl = egl_next;
     }
     ok = __syncthreads_and(ok);
     if (ok && to_final && a.dh0 && in_range(sbase, 32, n_states(a), a.status)) {

@@ -10,6 +10,18 @@
 
 namespace gdn {
 
+// Per (chunk, value head): the scalars the two state scans apply per token, written by
+// k_prep and copied into shared memory by the scans with their tiles (one 16-byte
+// aligned bulk copy), so that no scan step waits on scattered global loads.
+struct alignas(16) ScRec {
+    float kc[kChunk];   // e^{G_L - G_t} / r_k,t, 0 past L
+    float qc[kChunk];   // e^{G_t} scale / r_q,t, 0 past L
+    float egl;          // e^{G_L}
+    float pad[3];
+};
+static_assert(sizeof(ScRec) % 16 == 0, "bulk copies move multiples of 16 bytes");
+constexpr int kScRec = (int)(sizeof(ScRec) / sizeof(float));
+
 // Everything one chunk call touches.  Pointers the call does not use are null.
 struct ChunkArgs {
     int N, T, H, HV, num_chunks;
@@ -41,6 +53,9 @@ struct ChunkArgs {
     bf16 *Tm;               // [C_total,HV,64,64] (I + A)^-1
     float *rq, *rk;         // [T,H] sqrt(|x|^2 + eps)
     float *G;               // [T,HV] chunk-local cumulative log decay
+    float *sc;              // [C,HV] records of kScRec floats: the scans' per-token scalars
+                            // kc_t = e^{G_L-G_t} / r_k,t, qc_t = e^{G_t} scale / r_q,t (0 past
+                            // L) and e^{G_L} (see ScRec)
     // chunk table (device, rebuilt by every call)
     int *seq_chunk_off, *chunk_start, *chunk_len;
     int max_seq_chunks;     // chunks of the longest sequence (host copy of cu_seqlens)

@@ -19,9 +19,9 @@
 //   4. h[k][v'] += sum_t K[t][k] A_V[t][v']        (tcgen05, M=128 N=64 K=64; the
 //      raw key tile is read MN-major)
 // which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with Khat =
-// diag(1 / r_k) K.  w^T, K and this half of u^T stream in by TMA two chunks ahead,
-// the next chunk's per-token scalars are loaded a chunk ahead and published
-// during the current epilogue, and a chunk costs two block barriers.  Two CTAs
+// diag(1 / r_k) K.  w^T, K, this half of u^T and the chunk's scalar record
+// (e^{G_L - G_t} / r_k,t and e^{G_L}, written by k_prep) stream in two chunks ahead,
+// and a chunk costs two block barriers.  Two CTAs
 // share an SM.  Every wait is bounded; a timeout sets status bit 2 and the CTA
 // unwinds.  In paged-prefill mode the initial state comes from, and the final
 // state goes back to, a slot of the decode state pool [slots, HV, V, K] (the
@@ -48,7 +48,7 @@ struct StateSmem {
     unsigned char a_s[128 * 128];       // h bf16 [k][v']: 128 rows x 128 B
     unsigned char a_v[64 * 128];        // A_V bf16 [t][v']: 64 rows x 128 B
     unsigned char stage[2][kStageBytes];
-    float coef[2][64];                  // e^{G_L - G_t} / r_k,t, 0 past L (this and the next chunk)
+    ScRec sc[2];                        // the stages' scalar records (kc = coef_t, egl)
     uint64_t tma_bar[2];
     uint64_t mma_bar;
     uint32_t tmem_base;
@@ -64,7 +64,8 @@ __device__ __forceinline__ void issue_stage(const StateMaps &m, StateSmem &sm, c
                                             int c, int t0, int h, int hv, int vb, bool with_u) {
     unsigned char *b = sm.stage[st];
     const int row = (c * a.HV + hv) * kDim;
-    mbar_arrive_expect_tx(&sm.tma_bar[st], with_u ? kStageBytes : kStageBytes - kBox);
+    mbar_arrive_expect_tx(&sm.tma_bar[st], (with_u ? kStageBytes : kStageBytes - kBox) + (uint32_t)sizeof(ScRec));
+    bulk_load(&sm.sc[st], a.sc + ((size_t)c * a.HV + hv) * kScRec, sizeof(ScRec), &sm.tma_bar[st]);
     tma_load_3d(b + 0 * kBox, &m.w, 0, 0, row, &sm.tma_bar[st]);
     tma_load_3d(b + 2 * kBox, &m.k, 0, h, t0, &sm.tma_bar[st]);
     tma_load_3d(b + 3 * kBox, &m.k, 64, h, t0, &sm.tma_bar[st]);
@@ -196,32 +197,6 @@ __global__ void __launch_bounds__(kThr, 2)
         tmem_st32(tH, r);
         tmem_st_wait();
     }
-    // per-chunk scalars: the raw values are loaded one chunk ahead (pgl: G_L; pg,
-    // prk: G_t and r_k,t of thread t < 64) and turned into coef_t and e^{G_L} only
-    // when they are published a chunk later, so no thread waits on the loads
-    float pgl = 0.f, pg = 0.f, prk = 1.f;
-    bool pin = false;
-    auto fetch = [&](int j) {
-        const int tt0 = chunk_t0(j), LL = chunk_len(j);
-        const size_t gl = (size_t)(tt0 + LL - 1) * a.HV + hv;
-        pgl = in_range(gl, 1, n_tok_hv(a), a.status) ? a.G[gl] : 0.f;
-        pin = tid < LL && in_range((size_t)(tt0 + tid) * a.HV + hv, 1, n_tok_hv(a), a.status);
-        if (pin) {
-            const size_t t = (size_t)(tt0 + tid);
-            pg = a.G[t * a.HV + hv];
-            prk = a.rk[t * a.H + h];
-        }
-    };
-    auto publish = [&](int buf) {  // returns e^{G_L}
-        if (tid < 64) sm.coef[buf][tid] = pin ? __expf(fminf(pgl - pg, 0.f)) / prk : 0.f;
-        return __expf(pgl);
-    };
-    float egl = 1.f;
-    if (nch > 0) {
-        fetch(0);
-        egl = publish(0);
-        if (nch > 1) fetch(1);
-    }
     __syncthreads();
     const uint32_t idP = idesc_bf16(64, 64, 1, 1);    // P = w h       (w^T and h MN-major)
     const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // h += K^T A_V  (both MN-major)
@@ -230,6 +205,9 @@ __global__ void __launch_bounds__(kThr, 2)
     for (int i = 0; i < nch; ++i) {
         const int c = cb + jb + i, st = i & 1;
         const int t0 = chunk_t0(i), L = chunk_len(i);
+        // the chunk's tiles and scalar record (e^{G_L} is needed right below)
+        const bool got = mbar_wait(&sm.tma_bar[st], (i >> 1) & 1);
+        const float egl = sm.sc[st].egl;
         // 1. h -> bf16 operand (copied to h_c by TMA below), then h <- e^{G_L} h
         {
             float r[32];
@@ -247,7 +225,6 @@ __global__ void __launch_bounds__(kThr, 2)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        const bool got = mbar_wait(&sm.tma_bar[st], (i >> 1) & 1);  // u is read below by everyone
         ok = __syncthreads_and(ok && got);
         if (!ok) break;
         // 2. P = w h
@@ -264,13 +241,6 @@ __global__ void __launch_bounds__(kThr, 2)
                 tma_store_commit();
             }
         }
-        // while the product runs: publish the next chunk's scalars (their buffer is not
-        // this one's), and fetch one chunk further, ahead of this chunk's global stores
-        float egl_next = egl;
-        if (i + 1 < nch) {
-            egl_next = publish((i + 1) & 1);
-            if (i + 2 < nch) fetch(i + 2);
-        }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
@@ -282,7 +252,7 @@ __global__ void __launch_bounds__(kThr, 2)
             tmem_ld_wait();
             const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
             const bool la = ra < L, lb = rb < L;
-            const float cfa = sm.coef[i & 1][ra], cfb = sm.coef[i & 1][rb];
+            const float cfa = sm.sc[st].kc[ra], cfb = sm.sc[st].kc[rb];
             const unsigned char *us = sm.stage[st] + 4 * kBox;   // u^T [v'][t]
             auto u2 = [&](int t, int v) {  // u[t][v], u[t][v + 1]
                 const bf16 *e0 = reinterpret_cast<const bf16 *>(us + sw128_off(v, t));
@@ -325,7 +295,6 @@ __global__ void __launch_bounds__(kThr, 2)
         tc_fence_after();
         if (tid == 0 && ok && i + 2 < nch)
             issue_stage(maps, sm, a, st, c + 2, chunk_t0(i + 2), h, hv, vb, !phi);
-        egl = egl_next;
     }
     ok = __syncthreads_and(ok);
     if (ok && to_final && a.ht && in_range(sbase, 32, n_states(a), a.status)) {

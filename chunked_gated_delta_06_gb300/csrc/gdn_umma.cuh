@@ -221,6 +221,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int c0,
         "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
+// Plain bulk copy global -> shared (no tensor map): `bytes` a multiple of 16, both
+// addresses 16-byte aligned; completes on the mbarrier like a tensor load.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2,
                                             uint64_t *bar) {
     asm volatile(

@@ -54,9 +54,11 @@ def test_saved_and_workspace_sizes(lib):
     def al(x):
         return (x + 255) // 256 * 256
     # per-chunk h (bf16), v_new (bf16 per token), w^T per chunk (bf16 [C, HV, 128, 64]),
-    # the WY inverses (bf16 [C, HV, 64, 64]), r_q, r_k (per key head), G (per value head)
+    # the WY inverses (bf16 [C, HV, 64, 64]), r_q, r_k (per key head), G (per value head),
+    # the scans' scalar records (fp32 [C, HV, 132]: 64 + 64 per-token scalars, e^{G_L}, pad)
     saved = (al(C * HV * D * D * 2) + al(T * HV * D * 2) + al(C * HV * D * 64 * 2)
-             + al(C * HV * 64 * 64 * 2) + al(T * H * 4) + al(T * H * 4) + al(T * HV * 4))
+             + al(C * HV * 64 * 64 * 2) + al(T * H * 4) + al(T * H * 4) + al(T * HV * 4)
+             + al(C * HV * 132 * 4))
     assert gdn.gdn_chunk_saved_bytes(p) == saved
     fwd_ws = gdn.gdn_chunk_workspace_bytes(p, 0)
     assert fwd_ws >= saved + C * HV * D * 64 * 2  # and u^T per chunk
@@ -246,10 +248,12 @@ def test_sizes_at_the_largest_token_count(lib):
     p, keep = _problem([0, T], H=1, HV=1)
     C = (T + 63) // 64
     saved = gdn.gdn_chunk_saved_bytes(p)
-    # h_c (bf16 per chunk), v_new and w rows (bf16), T per chunk (bf16), r_q, r_k, G (fp32),
-    # each rounded up to 256 bytes
-    need = C * 128 * 128 * 2 + 2 * T * 128 * 2 + C * 64 * 64 * 2 + 3 * T * 4
-    assert need <= saved <= need + 7 * 256
+    # h_c (bf16 per chunk), v_new rows (bf16), w^T per chunk (bf16), T per chunk (bf16),
+    # r_q, r_k, G (fp32), the scans' scalar records (fp32, 132 per chunk), each rounded up
+    # to 256 bytes
+    need = (C * 128 * 128 * 2 + T * 128 * 2 + C * 128 * 64 * 2 + C * 64 * 64 * 2 + 3 * T * 4
+            + C * 132 * 4)
+    assert need <= saved <= need + 8 * 256
     for mode in (0, 1, 2):
         assert gdn.gdn_chunk_workspace_bytes(p, mode) > 0
     st, seg_len, nseg = gdn.gdn_chunk_scan_plan(p)

@@ -69,9 +69,10 @@ def kernel_work(name, T, H, HV, N, C_total):
     bf = 2
     b = dict(
         plan=4 * (N + 1 + 3 * C_total),
-        # q, k in; g in and G out; r_q, r_k out; the scans' scalar records out
-        prep=T * H * D * bf * 2 + TV * 4 * 2 + T * H * 8 + C_total * HV * 132 * 4,
-        intra=T * H * D * bf + TV * D * bf + TV * 6 + TV * D * bf * 2 + C_total * HV * C * C * 2,
+        prep=T * H * D * bf * 2 + TV * 4 * 2 + T * H * 8,
+        # k, v, G, beta, r_k, r_q in; w^T, u^T, T and the scans' scalar records out
+        intra=T * H * D * bf + TV * D * bf + TV * 6 + T * H * 8 + TV * D * bf * 2 + C_total * HV * C * C * 2
+        + C_total * HV * 132 * 4,
         state=TV * D * bf * 3 + T * H * D * bf + C_total * HV * D * D * bf + N * HV * D * D * 8
         + C_total * HV * 132 * 4,
         out=T * H * D * bf * 2 + TV * D * bf * 2 + C_total * HV * D * D * bf,

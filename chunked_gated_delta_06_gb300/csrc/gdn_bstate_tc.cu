@@ -23,7 +23,7 @@
 // soon as it is free: K after step 2, the halves of dO and dv_loc after step 3,
 // Q and w after step 4; every tile of the chunk after that is prefetched into L2
 // a step ahead.  The chunk's scalar record (kc_t = e^{G_L - G_t} / r_k,t, qc_t =
-// e^{G_t} scale / r_q,t and e^{G_L}, written by k_prep) comes with K, into one of two
+// e^{G_t} scale / r_q,t and e^{G_L}, written by the WY pass) comes with K, into one of two
 // buffers by the parity of the step; a chunk costs two block barriers.
 // Waits are bounded.  Long sequences with few heads can be scanned segment-
 // parallel (the plan of the forward scan; see k_bstate_tc).

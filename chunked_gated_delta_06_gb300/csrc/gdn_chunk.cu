@@ -5,9 +5,8 @@
 //            tokens never span sequences, the last one of a sequence may be
 //            partial), "[Cake 1/13] gdn: chunked gated delta rule ...", API;
 //   k_prep   q / k norms r = sqrt(sum x^2 + 1e-6) ("C6: GDN decode-step
-//            goldens ...", Provider: divide by the sqrt), the chunk-local
-//            cumulative sum G of g, and per (chunk, value head) the record of
-//            the per-token scalars the two state scans apply (ScRec).
+//            goldens ...", Provider: divide by the sqrt) and the chunk-local
+//            cumulative sum G of g.
 // The tensor-core kernels of the chunked (WY) form live in gdn_*_tc.cu.
 // Every reduction runs in a fixed order and no kernel uses atomics, so results
 // are bit-identical from run to run.
@@ -98,7 +97,6 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
     const int t0 = a.chunk_start[c], L = a.chunk_len[c];
     if (L <= 0) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ float s_rq[kChunk], s_rk[kChunk];  // this chunk's norms, for the scan records
     // warp w takes rows w, w + 8, ..., w + 56: all 16 row slices (8 bytes a lane) are
     // loaded before the first sum
     constexpr int kRows = kChunk / (kThreads / 32);
@@ -124,17 +122,11 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
         float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
         sq = warp_sum(sq);
         sk = warp_sum(sk);
-        const float rqi = sqrtf(sq + kNormEps), rki = sqrtf(sk + kNormEps);
-        if (lane == 0) {
-            s_rq[i] = rqi;
-            s_rk[i] = rki;
-        }
         if (lane == 0 && i < L && in_range((size_t)(t0 + i) * a.H + h, 1, n_tok_h(a), a.status)) {
-            a.rq[(size_t)(t0 + i) * a.H + h] = rqi;
-            a.rk[(size_t)(t0 + i) * a.H + h] = rki;
+            a.rq[(size_t)(t0 + i) * a.H + h] = sqrtf(sq + kNormEps);
+            a.rk[(size_t)(t0 + i) * a.H + h] = sqrtf(sk + kNormEps);
         }
     }
-    __syncthreads();
     const int r = a.HV / a.H;
     for (int j = warp; j < r; j += kThreads / 32) {
         const int hv = h * r + j;
@@ -148,24 +140,10 @@ __global__ void __launch_bounds__(kThreads) k_prep(ChunkArgs a) {
             if (lane >= off) s += y;
         }
         float excl = s - (x0 + x1);
-        const float G0 = excl + x0, G1 = excl + x0 + x1;
         if (i0 < L && in_range((size_t)(t0 + i0) * a.HV + hv, 1, n_tok_hv(a), a.status))
-            a.G[(size_t)(t0 + i0) * a.HV + hv] = G0;
+            a.G[(size_t)(t0 + i0) * a.HV + hv] = excl + x0;
         if (i1 < L && in_range((size_t)(t0 + i1) * a.HV + hv, 1, n_tok_hv(a), a.status))
-            a.G[(size_t)(t0 + i1) * a.HV + hv] = G1;
-        // the scans' record of (c, hv): G_L from the lane that holds token L - 1
-        const float Gl = __shfl_sync(0xffffffffu, ((L - 1) & 1) ? G1 : G0, (L - 1) >> 1);
-        if (in_range(((size_t)c * a.HV + hv) * kScRec, kScRec, (long long)a.num_chunks * a.HV * kScRec,
-                     a.status)) {
-            ScRec *rec = reinterpret_cast<ScRec *>(a.sc) + (size_t)c * a.HV + hv;
-            *reinterpret_cast<float2 *>(&rec->kc[i0]) =
-                make_float2(i0 < L ? __expf(fminf(Gl - G0, 0.f)) / s_rk[i0] : 0.f,
-                            i1 < L ? __expf(fminf(Gl - G1, 0.f)) / s_rk[i1] : 0.f);
-            *reinterpret_cast<float2 *>(&rec->qc[i0]) =
-                make_float2(i0 < L ? __expf(G0) * a.scale / s_rq[i0] : 0.f,
-                            i1 < L ? __expf(G1) * a.scale / s_rq[i1] : 0.f);
-            if (lane == 0) rec->egl = __expf(Gl);
-        }
+            a.G[(size_t)(t0 + i1) * a.HV + hv] = excl + x0 + x1;
     }
 }
 

@@ -18,6 +18,8 @@
 //                                                (tcgen05, M=128 N=64 K=64; the K
 //                                                 and V tiles are read MN-major, so
 //                                                 row d of w^T / u^T is TMEM lane d)
+// Each unit also writes the record of per-token scalars that the two state scans
+// apply (ScRec: e^{G_L - G_t} / r_k,t, e^{G_t} scale / r_q,t, e^{G_L}).
 // w^T, u^T and T (kept for the backward) go to HBM in bf16, w^T and u^T per chunk
 // as [C][HV][128][64]: thread d holds row d of both (the chunk's 64 tokens) and
 // stages it in the bytes of T (swizzled as the tile map expects); one TMA store per
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         issue_kv(maps, sm, x);
     }
     // per-token scalars of thread tid < 64, fetched one unit ahead
-    float pG = 0.f, pR = 1.f;
+    float pG = 0.f, pR = 1.f, pQ = 1.f;
     uint32_t pB = 0;   // raw beta bits, converted when published
     bool pin = false;
     auto fetch = [&](const IntraUnit &y) {
@@ -250,6 +252,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
                 pG = a.G[gi];
                 pB = load_beta_raw(a, gi);
                 pR = a.rk[ri];
+                pQ = a.rq[ri];
             }
         }
     };
@@ -284,6 +287,16 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
                 mma_bf16(tb, sdesc(ks + off, 16, 1024), sdesc(ks + off, 16, 1024), id, s > 0);
             }
             mma_commit(&sm.mma_bar);
+        }
+        if (tid < 64) {  // the unit's scalar record for the state scans (before the fetch below)
+            const float Gl = L > 0 ? sm.G[L - 1] : 0.f;
+            if (in_range(((size_t)c * a.HV + hv) * kScRec, kScRec, (long long)a.num_chunks * a.HV * kScRec,
+                         a.status)) {
+                ScRec *rec = reinterpret_cast<ScRec *>(a.sc) + (size_t)c * a.HV + hv;
+                rec->kc[tid] = pin ? __expf(fminf(Gl - pG, 0.f)) / pR : 0.f;
+                rec->qc[tid] = pin ? __expf(pG) * a.scale / pQ : 0.f;
+                if (tid == 0) rec->egl = __expf(Gl);
+            }
         }
         // the next unit (its table entries are a dependent load: after the MMA issue)
         const IntraUnit nx = has_next ? intra_next(a, x) : x;

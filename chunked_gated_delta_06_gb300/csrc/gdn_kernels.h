@@ -11,7 +11,7 @@
 namespace gdn {
 
 // Per (chunk, value head): the scalars the two state scans apply per token, written by
-// k_prep and copied into shared memory by the scans with their tiles (one 16-byte
+// the WY pass (k_intra_tc) and copied into shared memory by the scans with their tiles (one 16-byte
 // aligned bulk copy), so that no scan step waits on scattered global loads.
 struct alignas(16) ScRec {
     float kc[kChunk];   // e^{G_L - G_t} / r_k,t, 0 past L

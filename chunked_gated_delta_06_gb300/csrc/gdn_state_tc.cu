@@ -20,7 +20,7 @@
 //      raw key tile is read MN-major)
 // which is h <- e^{G_L} h + (diag(e^{G_L-G}) Khat)^T v_new with Khat =
 // diag(1 / r_k) K.  w^T, K, this half of u^T and the chunk's scalar record
-// (e^{G_L - G_t} / r_k,t and e^{G_L}, written by k_prep) stream in two chunks ahead,
+// (e^{G_L - G_t} / r_k,t and e^{G_L}, written by the WY pass) stream in two chunks ahead,
 // and a chunk costs two block barriers.  Two CTAs
 // share an SM.  Every wait is bounded; a timeout sets status bit 2 and the CTA
 // unwinds.  In paged-prefill mode the initial state comes from, and the final

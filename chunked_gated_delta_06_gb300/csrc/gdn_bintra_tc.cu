@@ -80,12 +80,12 @@ struct BaSmem {
     unsigned char stg[2 * kBox];  // rows of a full chunk staged for TMA stores: dW, then dkhat
     float pq[2][64], pk[2][64];   // per-warpgroup partial row dots
     float pn[2][64];              // per-warpgroup partial row dots q . (summed dqhat)
-    float iq[64];                 // 1 / r_q (0 past L)
+    float iq[2][64];              // 1 / r_q (0 past L); [2]: this unit's and the next one's
     float rp[2][64];              // per-warpgroup partial row sums of P1
     float cp[4][64];              // per-row-block column sums of P1
     float hdh[4];                 // per-warp partial <h, dh'> (warps 4..7)
-    float G[64], eg[64], egl_g[64];  // G, e^{G_t}, e^{G_L - G_t} (0 past L)
-    float qsc[64], rki[64];       // scale / r_q, 1 / r_k
+    float G[2][64], eg[64], egl_g[64];  // G, e^{G_t}, e^{G_L - G_t} (0 past L)
+    float qsc[2][64], rki[2][64];       // scale / r_q, 1 / r_k
     uint64_t a_bar, b_bar[2], mma_bar;   // group A (h, dh, dO, dv_new, v_new), group B (q, k) per buffer
     uint32_t tmem_base;
 };
@@ -210,16 +210,23 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     fetch(x);
     bool ok = true;
     uint32_t phase = 0;
+    // a unit's scalars go into buffer buf at the end of the unit before (the first
+    // unit's here), off the unit's own chain: the divides run while nothing waits on them
+    auto publish = [&](int Ly, int buf) {
+        if (scal) {
+            const bool in = ft < Ly;
+            sm.G[buf][ft] = pG;
+            sm.qsc[buf][ft] = in ? a.scale / pRq : 0.f;
+            sm.rki[buf][ft] = in ? 1.f / pRk : 0.f;
+            sm.iq[buf][ft] = in ? 1.f / pRq : 0.f;
+        }
+    };
+    publish(x.L, 0);
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int L = x.L;
-        if (scal) {
-            const bool in = ft < L;
-            sm.G[ft] = pG;
-            sm.qsc[ft] = in ? a.scale / pRq : 0.f;
-            sm.rki[ft] = in ? 1.f / pRk : 0.f;
-            sm.iq[ft] = in ? 1.f / pRq : 0.f;
-        }
+        const int cur = (u - ub) & 1;
+        const float *sG = sm.G[cur], *sQsc = sm.qsc[cur], *sRki = sm.rki[cur], *sIq = sm.iq[cur];
         bool got = mbar_wait(&sm.a_bar, a_waited & 1);
         if (need_b) got = mbar_wait(&sm.b_bar[bcur], (bpar >> bcur) & 1) && got;
         got = __syncthreads_and(got);
@@ -229,10 +236,10 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             bpend &= ~(1u << bcur);
         }
         if (!got) { ok = false; break; }
-        const float Gl = L > 0 ? sm.G[L - 1] : 0.f;
+        const float Gl = L > 0 ? sG[L - 1] : 0.f;
         if (scal) {
             const bool in = ft < L;
-            const float Gt = sm.G[ft];
+            const float Gt = sG[ft];
             sm.eg[ft] = in ? __expf(Gt) : 0.f;
             sm.egl_g[ft] = in ? __expf(fminf(Gl - Gt, 0.f)) : 0.f;
         }
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             tmem_ld16x256_x4(t_row + cQK + j0, qk);
             tmem_ld16x256_x4(t_row + cDM + j0, dm);
             tmem_ld_wait();
-            const float Ga = sm.G[ra], Gb = sm.G[rb], qsa = sm.qsc[ra], qsb = sm.qsc[rb];
+            const float Ga = sG[ra], Gb = sG[rb], qsa = sQsc[ra], qsb = sQsc[rb];
             float rsa = 0.f, rsb = 0.f, pc[8];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -316,14 +323,14 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                     const bool up = e & 2;
                     const int r = up ? rb : ra;
                     const float msk = ((up ? lb : la) && j <= r) ? 1.f : 0.f;
-                    dm[4 * k + e] *= msk * __expf(fminf((up ? Gb : Ga) - sm.G[j], 0.f));
-                    qk[4 * k + e] = dm[4 * k + e] * qk[4 * k + e] * (up ? qsb : qsa) * sm.rki[j];
+                    dm[4 * k + e] *= msk * __expf(fminf((up ? Gb : Ga) - sG[j], 0.f));
+                    qk[4 * k + e] = dm[4 * k + e] * qk[4 * k + e] * (up ? qsb : qsa) * sRki[j];
                     if (up) rsb += qk[4 * k + e]; else rsa += qk[4 * k + e];
                 }
                 pc[2 * k] = qk[4 * k] + qk[4 * k + 2];
                 pc[2 * k + 1] = qk[4 * k + 1] + qk[4 * k + 3];
                 const int j = j0 + 8 * k + cq;
-                const float r0 = sm.rki[j], r1 = sm.rki[j + 1];
+                const float r0 = sRki[j], r1 = sRki[j + 1];
                 put_pair(sm.op_dmg, ra, j, dm[4 * k] * r0, dm[4 * k + 1] * r1);
                 put_pair(sm.op_dmg, rb, j, dm[4 * k + 2] * r0, dm[4 * k + 3] * r1);
                 put_pair(sm.op_dmgt, ra, j, dm[4 * k] * qsa, dm[4 * k + 1] * qsa);
@@ -446,8 +453,8 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         __syncthreads();  // q / k tiles, TMEM and the row sums are all read or written
         if (last) {  // the key head's dq (L2-norm backward applied) and summed dkhat terms:
                      // full chunks staged for TMA stores, ragged ones stored directly
-            const float sa = la ? sm.qsc[ra] : 0.f, sb = lb ? sm.qsc[rb] : 0.f;
-            const float ia = la ? sm.iq[ra] : 0.f, ib = lb ? sm.iq[rb] : 0.f;
+            const float sa = la ? sQsc[ra] : 0.f, sb = lb ? sQsc[rb] : 0.f;
+            const float ia = la ? sIq[ra] : 0.f, ib = lb ? sIq[rb] : 0.f;
             const float Pa = (sm.pn[0][ra] + sm.pn[1][ra]) * ia * ia;
             const float Pb = (sm.pn[0][rb] + sm.pn[1][rb]) * ib * ib;
             const size_t oa = ((size_t)(x.t0 + (la ? ra : 0)) * a.H + x.h) * kDim;
@@ -500,9 +507,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 const int tt = 2 * lane + z;
                 float dg = 0.f, xi = 0.f;
                 if (tt < L) {
-                    xi = (sm.pk[0][tt] + sm.pk[1][tt]) * sm.rki[tt];
+                    xi = (sm.pk[0][tt] + sm.pk[1][tt]) * sRki[tt];
                     const float cps = ((sm.cp[0][tt] + sm.cp[1][tt]) + sm.cp[2][tt]) + sm.cp[3][tt];
-                    dg = (sm.pq[0][tt] + sm.pq[1][tt]) * sm.qsc[tt] - xi + (sm.rp[0][tt] + sm.rp[1][tt]) - cps;
+                    dg = (sm.pq[0][tt] + sm.pq[1][tt]) * sQsc[tt] - xi + (sm.rp[0][tt] + sm.rp[1][tt]) - cps;
                 }
                 sx += xi;
                 dgz[z] = dg;
@@ -520,6 +527,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                 }
             }
         }
+        if (has_next) publish(nx.L, cur ^ 1);
         __syncthreads();  // the per-unit scalars are free for the next unit
         if (need_next_b) bcur ^= 1;
         need_b = need_next_b;

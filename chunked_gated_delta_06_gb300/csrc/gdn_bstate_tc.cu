@@ -57,6 +57,7 @@ struct BStateSmem {
 
 struct BStateMaps {
     CUtensorMap k, q, w, dO, dl, dhc;
+    CUtensorMap dvn;   // dv_new [T][HV][128]: a full chunk's rows of this value half, stored by TMA
 };
 
 // K of chunk c (tokens from t0) and its scalar record, into record buffer rb
@@ -287,7 +288,9 @@ __global__ void __launch_bounds__(kThr, 2)
             tmem_ld_wait();
             const bool la = ra < L, lb = rb < L;
             const float ka = rec.kc[ra], kb = rec.kc[rb];
-            const unsigned char *dls = sm.x + 3 * kBox;
+            // a full chunk's dv_new rows replace, pair by pair, the dv_loc pairs each thread
+            // has just read, for one TMA store; a ragged chunk's rows are stored directly
+            unsigned char *dls = sm.x + 3 * kBox;
             bf16 *da = a.dvnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
             bf16 *db = a.dvnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
 #pragma unroll
@@ -297,10 +300,15 @@ __global__ void __launch_bounds__(kThr, 2)
                 const float2 lb2 = phi ? make_float2(0.f, 0.f) : epi::get_pair(dls, rb, col);
                 const float va0 = la ? la2.x + ka * p[4 * k] : 0.f, va1 = la ? la2.y + ka * p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? lb2.x + kb * p[4 * k + 2] : 0.f, vb1 = lb ? lb2.y + kb * p[4 * k + 3] : 0.f;
-                if (la && !pre && in_range(da + col - a.dvnew, 2, n_rows_hv(a), a.status))
-                    *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
-                if (lb && !pre && in_range(db + col - a.dvnew, 2, n_rows_hv(a), a.status))
-                    *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                if (!pre && !phi && L == 64) {
+                    epi::put_pair(dls, ra, col, va0, va1);
+                    epi::put_pair(dls, rb, col, vb0, vb1);
+                } else if (!pre) {
+                    if (la && in_range(da + col - a.dvnew, 2, n_rows_hv(a), a.status))
+                        *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                    if (lb && in_range(db + col - a.dvnew, 2, n_rows_hv(a), a.status))
+                        *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                }
                 epi::put_pair(sm.a_dv, ra, col, -va0, -va1);
                 epi::put_pair(sm.a_dv, rb, col, -vb0, -vb1);
             }
@@ -324,7 +332,12 @@ __global__ void __launch_bounds__(kThr, 2)
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase, sdesc(ws + s * 32, 16, 1024), sdesc(adv + s * 2048, kBox, 1024), idW, true);
             mma_commit(&sm.mma_bar);
+            if (!pre && !phi && L == 64) {  // the staged dv_new rows of this value half
+                tma_store_3d(&maps.dvn, 64 * vb, hv, t0, sm.x + 3 * kBox);
+                tma_store_commit();
+            }
             if (i + 1 < nch && !phi) {
+                tma_store_wait_read();  // the staged dv_new rows have left the dv_loc buffer
                 issue_xd(maps, sm, step_t0(i + 1), hv, vb);
                 ++xd_issued;
             }
@@ -383,7 +396,8 @@ cudaError_t launch_bstate_tc(const ChunkArgs &a, cudaStream_t s) {
                     !encode_rows_bf16(&m.dO, a.d_o, a.HV, a.T, rowb, rowb * a.HV, 64) ||
                     !encode_rows_bf16(&m.dl, a.dvloc, a.HV, a.T, rowb, rowb * a.HV, 64) ||
                     !encode_rows_bf16(&m.dhc, a.dhc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb,
-                                      rowb, 128)))
+                                      rowb, 128) ||
+                    !encode_rows_bf16(&m.dvn, a.dvnew, a.HV, a.T, rowb, rowb * a.HV, 64)))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(BStateSmem) + 1024;
     static_assert(2 * (sizeof(BStateSmem) + 2048) <= 233472, "two CTAs per SM");

@@ -56,6 +56,7 @@ struct StateSmem {
 
 struct StateMaps {
     CUtensorMap w, k, u, hc;
+    CUtensorMap vn;   // v_new [T][HV][128]: a full chunk's rows of this value half, stored by TMA
 };
 
 // Chunk c (tokens from t0): its w^T tile [k][t] (128 rows), K, and (unless the columns
@@ -261,6 +262,9 @@ __global__ void __launch_bounds__(kThr, 2)
             };
             bf16 *da = a.vnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
             bf16 *db = a.vnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
+            // a full chunk's v_new rows are staged over this stage's w^T tile (read by the
+            // product above) for one TMA store; a ragged chunk's rows are stored directly
+            unsigned char *vstg = sm.stage[st];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int col = c0 + 8 * k + cq;
@@ -268,10 +272,15 @@ __global__ void __launch_bounds__(kThr, 2)
                 const float2 ub = phi ? make_float2(0.f, 0.f) : u2(rb, col);
                 const float va0 = la ? ua.x - p[4 * k] : 0.f, va1 = la ? ua.y - p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? ub.x - p[4 * k + 2] : 0.f, vb1 = lb ? ub.y - p[4 * k + 3] : 0.f;
-                if (la && !pre && in_range(da + col - a.vnew, 2, n_rows_hv(a), a.status))
-                    *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
-                if (lb && !pre && in_range(db + col - a.vnew, 2, n_rows_hv(a), a.status))
-                    *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                if (!pre && L == 64) {
+                    epi::put_pair(vstg, ra, col, va0, va1);
+                    epi::put_pair(vstg, rb, col, vb0, vb1);
+                } else if (!pre) {
+                    if (la && in_range(da + col - a.vnew, 2, n_rows_hv(a), a.status))
+                        *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
+                    if (lb && in_range(db + col - a.vnew, 2, n_rows_hv(a), a.status))
+                        *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
+                }
                 epi::put_pair(sm.a_v, ra, col, va0 * cfa, va1 * cfa);
                 epi::put_pair(sm.a_v, rb, col, vb0 * cfb, vb1 * cfb);
             }
@@ -289,12 +298,18 @@ __global__ void __launch_bounds__(kThr, 2)
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase, sdesc(ks + s * 2048, kBox, 1024), sdesc(av + s * 2048, kBox, 1024), idS, true);
             mma_commit(&sm.mma_bar);
+            if (!pre && L == 64) {  // the staged v_new rows of this value half
+                tma_store_3d(&maps.vn, 64 * vb, hv, t0, sm.stage[st]);
+                tma_store_commit();
+            }
         }
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();
-        if (tid == 0 && ok && i + 2 < nch)
+        if (tid == 0 && ok && i + 2 < nch) {
+            tma_store_wait_read();  // the staged v_new rows have left the stage
             issue_stage(maps, sm, a, st, c + 2, chunk_t0(i + 2), h, hv, vb, !phi);
+        }
     }
     ok = __syncthreads_and(ok);
     if (ok && to_final && a.ht && in_range(sbase, 32, n_states(a), a.status)) {
@@ -396,7 +411,8 @@ cudaError_t launch_state_tc(const ChunkArgs &a, cudaStream_t s) {
     if (a.T > 0 && (!encode_rows_bf16(&m.w, a.w, 1, wrows, 128, 128, 128, kChunk) ||
         !encode_rows_bf16(&m.k, a.k, a.H, a.T, rowb, rowb * a.H, 64) ||
         !encode_rows_bf16(&m.u, a.u, 1, wrows, 128, 128, 64, kChunk) ||
-        !encode_rows_bf16(&m.hc, a.hc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb, rowb, 128)))
+        !encode_rows_bf16(&m.hc, a.hc, 1, (uint64_t)a.num_chunks * a.HV * 128, rowb, rowb, 128) ||
+        !encode_rows_bf16(&m.vn, a.vnew, a.HV, a.T, rowb, rowb * a.HV, 64)))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(StateSmem) + 1024;
     static_assert(2 * (sizeof(StateSmem) + 2048) <= 233472, "two CTAs per SM");

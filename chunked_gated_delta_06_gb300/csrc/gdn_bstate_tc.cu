@@ -12,11 +12,12 @@
 //      dh_c[chunk][hv][k][v'] by one TMA store), then dh <- e^{G_L} dh';
 //   2. Pd[t][v'] = sum_k K[t][k] dh'[k][v']          (M=64 N=64 K=128)
 //   3. on 16x256b fragments of Pd (two token rows and eight columns per lane):
-//      dv_new[t][v'] = dv_loc + e^{G_L-G_t}/r_k,t Pd (to HBM, bf16) and the
-//      operands c_t dO[t][v'] and -dv_new[t][v'], c_t = e^{G_t} scale / r_q,t;
+//      dv_new[t][v'] = dv_loc + e^{G_L-G_t}/r_k,t Pd (bf16) and the operands
+//      c_t dO[t][v'] and dv_new[t][v'], c_t = e^{G_t} scale / r_q,t; a full chunk's
+//      dv_new goes to HBM by one TMA store of that operand tile;
 //   4. dh += Q^T (c dO) - w^T dv_new                  (two M=128 N=64 K=64
 //      products; Q is the raw tile read MN-major, w^T the chunk's [k][t] tile
-//      read K-major)
+//      read K-major, and the minus sign is the descriptor's negate-B bit)
 // which is dh <- e^{G_L} dh' + Qtil^T dO - w^T dv_new and dv_new = dv_loc +
 // Ktil dh'.  dh0 = dh at the sequence start.  The tiles are single-buffered so
 // that two CTAs share an SM, and each group is reloaded for the next chunk as
@@ -215,7 +216,10 @@ __global__ void __launch_bounds__(kThr, 2)
     __syncthreads();
     const uint32_t idP = idesc_bf16(64, 64, 0, 1);    // Pd = K dh'          (dh' MN-major)
     const uint32_t idS = idesc_bf16(128, 64, 1, 1);   // dh += Q^T A       (both MN-major)
-    const uint32_t idW = idesc_bf16(128, 64, 0, 1);   // dh += w^T B       (w^T K-major, B MN-major)
+    // dh -= w^T dv_new: w^T K-major, dv_new MN-major and negated by the descriptor's
+    // negate-B bit (bit 14), so that the operand tile holds +dv_new and is also the
+    // source of dv_new's TMA store
+    const uint32_t idW = idesc_bf16(128, 64, 0, 1) | (1u << 14);
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0; i < nch; ++i) {
@@ -241,6 +245,7 @@ __global__ void __launch_bounds__(kThr, 2)
             tmem_st32(tS, r);
             tmem_st_wait();
         }
+        if (tid == 0) tma_store_wait_read();  // the last step's dv_new store has read a_dv
         fence_proxy_async_smem();
         tc_fence_before();
         const bool gx = gk && (phi || mbar_wait(&sm.xd_bar, par));
@@ -288,9 +293,9 @@ __global__ void __launch_bounds__(kThr, 2)
             tmem_ld_wait();
             const bool la = ra < L, lb = rb < L;
             const float ka = rec.kc[ra], kb = rec.kc[rb];
-            // a full chunk's dv_new rows replace, pair by pair, the dv_loc pairs each thread
-            // has just read, for one TMA store; a ragged chunk's rows are stored directly
-            unsigned char *dls = sm.x + 3 * kBox;
+            // dv_new goes to a_dv (the operand of step 4, and for a full chunk the source
+            // of one TMA store); a ragged chunk's rows are stored directly
+            const unsigned char *dls = sm.x + 3 * kBox;
             bf16 *da = a.dvnew + ((size_t)(t0 + (la ? ra : 0)) * a.HV + hv) * kDim + 64 * vb;
             bf16 *db = a.dvnew + ((size_t)(t0 + (lb ? rb : 0)) * a.HV + hv) * kDim + 64 * vb;
 #pragma unroll
@@ -300,17 +305,14 @@ __global__ void __launch_bounds__(kThr, 2)
                 const float2 lb2 = phi ? make_float2(0.f, 0.f) : epi::get_pair(dls, rb, col);
                 const float va0 = la ? la2.x + ka * p[4 * k] : 0.f, va1 = la ? la2.y + ka * p[4 * k + 1] : 0.f;
                 const float vb0 = lb ? lb2.x + kb * p[4 * k + 2] : 0.f, vb1 = lb ? lb2.y + kb * p[4 * k + 3] : 0.f;
-                if (!pre && !phi && L == 64) {
-                    epi::put_pair(dls, ra, col, va0, va1);
-                    epi::put_pair(dls, rb, col, vb0, vb1);
-                } else if (!pre) {
+                if (!pre && L < 64) {
                     if (la && in_range(da + col - a.dvnew, 2, n_rows_hv(a), a.status))
                         *reinterpret_cast<uint32_t *>(da + col) = pack_bf2(va0, va1);
                     if (lb && in_range(db + col - a.dvnew, 2, n_rows_hv(a), a.status))
                         *reinterpret_cast<uint32_t *>(db + col) = pack_bf2(vb0, vb1);
                 }
-                epi::put_pair(sm.a_dv, ra, col, -va0, -va1);
-                epi::put_pair(sm.a_dv, rb, col, -vb0, -vb1);
+                epi::put_pair(sm.a_dv, ra, col, va0, va1);
+                epi::put_pair(sm.a_dv, rb, col, vb0, vb1);
             }
         }
         if (tid == 0) tma_store_wait_read();  // dh_c has been read out of a_ds
@@ -332,12 +334,11 @@ __global__ void __launch_bounds__(kThr, 2)
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tbase, sdesc(ws + s * 32, 16, 1024), sdesc(adv + s * 2048, kBox, 1024), idW, true);
             mma_commit(&sm.mma_bar);
-            if (!pre && !phi && L == 64) {  // the staged dv_new rows of this value half
-                tma_store_3d(&maps.dvn, 64 * vb, hv, t0, sm.x + 3 * kBox);
+            if (!pre && L == 64) {  // this value half's dv_new rows, from the operand tile
+                tma_store_3d(&maps.dvn, 64 * vb, hv, t0, sm.a_dv);
                 tma_store_commit();
             }
             if (i + 1 < nch && !phi) {
-                tma_store_wait_read();  // the staged dv_new rows have left the dv_loc buffer
                 issue_xd(maps, sm, step_t0(i + 1), hv, vb);
                 ++xd_issued;
             }

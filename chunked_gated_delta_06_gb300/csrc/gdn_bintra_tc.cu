@@ -57,21 +57,23 @@ using epi::tmem_ld16x256_x4;
 constexpr int kThr = 512;   // two halves of two warpgroups: the dq side and the dk side
 constexpr uint32_t kBox = 64 * 128;       // 64 rows x 128 B
 constexpr uint32_t kBig = 128 * 128;      // 128 rows x 128 B
+constexpr uint32_t kHV = kBig + kBox;     // one v-half of h_c and of v_new
 
 // TMEM columns (512 allocated)
-constexpr uint32_t cDQ = 0, cDW = 128, cDK = 256, cQK = 384, cDM = 448;   // batch 1
-constexpr uint32_t cQI = 384, cKI = 128;                                   // batch 2
+// Dq and dM share their A operand (dO) and come out of one N = 192 product: B is a
+// v-half of h_c followed by the same v-half of v_new
+constexpr uint32_t cDQ = 0, cDM = 128, cQK = 192, cDW = 256, cDK = 384;   // batch 1
+constexpr uint32_t cQI = 128, cKI = 256;                                   // batch 2
 // Every product here is M = 64, which fills lanes 0..15 of each 32-lane quarter; the
 // key head's dqhat / dkhat sums live in lanes 16..31 of the Dq / Dk columns, in the
 // 16x256b fragment layout of the epilogue (the MMAs never write those lanes).
 constexpr uint32_t kAccLanes = 16u << 16;
 
 struct BaSmem {
-    unsigned char h[2 * kBig];    // h_c [k][v]: two v-halves of 128 rows
+    unsigned char hvn[2 * kHV];   // per v-half: h_c [k][v] (128 rows), then v_new [t][v] (64 rows)
     unsigned char dh[2 * kBig];   // dh_c [k][v]
     unsigned char dO[2 * kBox];   // [t][v]
     unsigned char dvn[2 * kBox];
-    unsigned char vn[2 * kBox];
     unsigned char q[2][2 * kBox];  // [t][k], two buffers (the next key head loads into the other)
     unsigned char k[2][2 * kBox];
     unsigned char op_dmg[kBox];   // dMG_tj / r_k,j        [t][j]  K-major A of dMG Khat
@@ -92,7 +94,7 @@ struct BaSmem {
 
 // Every TMA / SW128 tile starts on a 1024-byte boundary of the (1024-aligned) struct.
 static_assert(offsetof(BaSmem, dh) % 1024 == 0 && offsetof(BaSmem, dO) % 1024 == 0 &&
-                  offsetof(BaSmem, dvn) % 1024 == 0 && offsetof(BaSmem, vn) % 1024 == 0 &&
+                  offsetof(BaSmem, dvn) % 1024 == 0 && kHV % 1024 == 0 &&
                   offsetof(BaSmem, q) % 1024 == 0 && offsetof(BaSmem, k) % 1024 == 0 &&
                   offsetof(BaSmem, op_dmg) % 1024 == 0 && offsetof(BaSmem, op_dmgt) % 1024 == 0 &&
                   offsetof(BaSmem, stg) % 1024 == 0,
@@ -132,16 +134,16 @@ __device__ __forceinline__ Unit next_unit(const ChunkArgs &a, const Unit &x) {
 __device__ __forceinline__ void issue_a(const BaMaps &m, BaSmem &sm, const ChunkArgs &a, const Unit &x) {
     const int row = (x.c * a.HV + x.hv) * 128;
     mbar_arrive_expect_tx(&sm.a_bar, 4 * kBig + 6 * kBox);
-    tma_load_3d(sm.h, &m.h, 0, 0, row, &sm.a_bar);
-    tma_load_3d(sm.h + kBig, &m.h, 64, 0, row, &sm.a_bar);
+    tma_load_3d(sm.hvn, &m.h, 0, 0, row, &sm.a_bar);
+    tma_load_3d(sm.hvn + kHV, &m.h, 64, 0, row, &sm.a_bar);
     tma_load_3d(sm.dh, &m.dh, 0, 0, row, &sm.a_bar);
     tma_load_3d(sm.dh + kBig, &m.dh, 64, 0, row, &sm.a_bar);
     tma_load_3d(sm.dO, &m.dO, 0, x.hv, x.t0, &sm.a_bar);
     tma_load_3d(sm.dO + kBox, &m.dO, 64, x.hv, x.t0, &sm.a_bar);
     tma_load_3d(sm.dvn, &m.dvn, 0, x.hv, x.t0, &sm.a_bar);
     tma_load_3d(sm.dvn + kBox, &m.dvn, 64, x.hv, x.t0, &sm.a_bar);
-    tma_load_3d(sm.vn, &m.vn, 0, x.hv, x.t0, &sm.a_bar);
-    tma_load_3d(sm.vn + kBox, &m.vn, 64, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.hvn + kBig, &m.vn, 0, x.hv, x.t0, &sm.a_bar);
+    tma_load_3d(sm.hvn + kHV + kBig, &m.vn, 64, x.hv, x.t0, &sm.a_bar);
 }
 
 __device__ __forceinline__ void issue_b(const BaMaps &m, BaSmem &sm, const Unit &x, int bf) {
@@ -245,18 +247,19 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         }
         if (tid == 0) {  // batch 1
             tc_fence_after();
-            const uint32_t id128 = idesc_bf16(64, 128, 0, 0), id64 = idesc_bf16(64, 64, 0, 0);
-            const uint32_t hs = smem_u32(sm.h), dhs = smem_u32(sm.dh);
-            const uint32_t os = smem_u32(sm.dO), ds = smem_u32(sm.dvn), vs = smem_u32(sm.vn);
+            const uint32_t id192 = idesc_bf16(64, 192, 0, 0), id128 = idesc_bf16(64, 128, 0, 0),
+                           id64 = idesc_bf16(64, 64, 0, 0);
+            const uint32_t hs = smem_u32(sm.hvn), dhs = smem_u32(sm.dh);
+            const uint32_t os = smem_u32(sm.dO), ds = smem_u32(sm.dvn);
             const uint32_t qs = smem_u32(sm.q[bcur]), ks = smem_u32(sm.k[bcur]);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t ao = (s >> 2) * kBox + (s & 3) * 32, bo = (s >> 2) * kBig + (s & 3) * 32;
-                mma_bf16(tb + cDQ, sdesc(os + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
-                mma_bf16(tb + cDW, sdesc(ds + ao, 16, 1024), sdesc(hs + bo, 16, 1024), id128, s > 0);
-                mma_bf16(tb + cDK, sdesc(vs + ao, 16, 1024), sdesc(dhs + bo, 16, 1024), id128, s > 0);
+                const uint32_t ho = (s >> 2) * kHV + (s & 3) * 32;  // h_c, then v_new at + kBig
+                mma_bf16(tb + cDQ, sdesc(os + ao, 16, 1024), sdesc(hs + ho, 16, 1024), id192, s > 0);
+                mma_bf16(tb + cDW, sdesc(ds + ao, 16, 1024), sdesc(hs + ho, 16, 1024), id128, s > 0);
+                mma_bf16(tb + cDK, sdesc(hs + kBig + ho, 16, 1024), sdesc(dhs + bo, 16, 1024), id128, s > 0);
                 mma_bf16(tb + cQK, sdesc(qs + ao, 16, 1024), sdesc(ks + ao, 16, 1024), id64, s > 0);
-                mma_bf16(tb + cDM, sdesc(os + ao, 16, 1024), sdesc(vs + ao, 16, 1024), id64, s > 0);
             }
             mma_commit(&sm.mma_bar);
         }
@@ -279,9 +282,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             for (int half = 0; half < 2; ++half)
 #pragma unroll
                 for (int q8 = 0; q8 < 8; ++q8) {
-                    const uint32_t off = half * kBig + sw128_off(kr, q8 * 8);
-                    const uint4 xx = *reinterpret_cast<const uint4 *>(sm.h + off);
-                    const uint4 yy = *reinterpret_cast<const uint4 *>(sm.dh + off);
+                    const uint32_t off = sw128_off(kr, q8 * 8);
+                    const uint4 xx = *reinterpret_cast<const uint4 *>(sm.hvn + half * kHV + off);
+                    const uint4 yy = *reinterpret_cast<const uint4 *>(sm.dh + half * kBig + off);
                     const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xx);
                     const __nv_bfloat162 *yb = reinterpret_cast<const __nv_bfloat162 *>(&yy);
 #pragma unroll

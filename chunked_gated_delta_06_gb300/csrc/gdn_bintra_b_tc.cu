@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
     if (ub >= ue) return;
     const int grp = warp >> 2;                // warpgroup: which half of the columns
     const int sub = warp & 3;                 // TMEM lane quarter
+    if (tid == 0) tma_prefetch_maps(maps);
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 256);

@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
     if (ub >= ue) return;
+    if (tid == 0) tma_prefetch_maps(maps);
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 128);

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kThr, kForward ? 2 : 3) k_out_tc(const ChunkAr
     const int nunits = a.num_chunks * a.HV;
     const int ub = blockIdx.x * per, ue = min(nunits, ub + per);
     if (ub >= ue) return;
+    if (tid == 0) tma_prefetch_maps(maps);
 
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, kTmemCols<kForward>);

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThr, 2)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     StateSmem &sm = smem_struct<StateSmem>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) tma_prefetch_maps(maps);
     const int ncol = pass == 1 ? 4 : 2;            // column blocks of 64 per value head
     const int hv = blockIdx.x / ncol, cbk = blockIdx.x % ncol;
     const bool phi = pass == 1 && cbk >= 2;        // transition columns (pass 1 only)

@@ -239,6 +239,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
         : "memory");
 }
 
+// Fetch every tensor map of a kernel's map struct (CUtensorMap members only, 128 bytes
+// each) into the descriptor cache before the first copy that names it.
+template <class Maps>
+__device__ __forceinline__ void tma_prefetch_maps(const Maps &m) {
+    static_assert(sizeof(Maps) % 128 == 0, "a struct of tensor maps");
+    const unsigned char *p = reinterpret_cast<const unsigned char *>(&m);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(Maps) / 128); ++i)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(p + 128 * i) : "memory");
+}
+
 // Warm L2 with a tile that a later tma_load_3d of the same coordinates will read
 // (no shared memory, no barrier; out-of-range parts are ignored as in a load).
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {

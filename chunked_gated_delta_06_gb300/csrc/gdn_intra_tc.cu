@@ -11,9 +11,10 @@
 //   KK = K K^T                                   (tcgen05, M=64 N=64 K=128)
 // The M=64 KK result is read as 16x256b fragments (two rows, eight columns per lane).
 //   A  = strict_tril(diag(beta) KKhat (.) Gamma) (CUDA cores, fp32)
-//   T  = (I + A)^-1                              (fp32, in place over A:
-//        16x16 diagonal blocks by substitution, then T21 = -T22 (A21 T11) at
-//        block sizes 16 and 32, register-tiled)
+//   T  = (I + A)^-1                              (in place over A: 16x16 diagonal
+//        blocks by substitution and T21 = -T22 (A21 T11) at block size 16 in
+//        fp32 on the CUDA cores; the block-32 step on the tensor cores, every
+//        operand split into bf16 hi + lo parts, fp32 accumulation)
 //   w^T = K^T (T diag(beta e^G / r_k))^T,  u^T = V^T (T diag(beta))^T
 //                                                (tcgen05, M=128 N=64 K=64; the K
 //                                                 and V tiles are read MN-major, so
@@ -53,7 +54,7 @@ struct IntraSmem {
                                 // w / u operands (op_w, op_u below)
     float X[32 * kXs];          // A21 T11 of the current merge level
     float G[64], beta[64], wc[64], rki[64];
-    uint64_t ld_bar, mma_bar;
+    uint64_t ld_bar, v_bar, mma_bar;   // K (ld_bar), V (v_bar), products
     uint32_t tmem_base;
 };
 
@@ -67,10 +68,11 @@ __device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&t);
 }
 
-// T = (I + A)^-1 in place over M (64 x 64 fp32, row stride kS).  On entry M holds A
-// strictly below the diagonal and zeros on and above it; on exit it holds T below
-// and on the diagonal and zeros above, so every product below may run over full
-// block ranges.  All 128 threads call it; X is scratch.
+// The two 32x32 diagonal blocks of T = (I + A)^-1, in place over M (64 x 64 fp32, row
+// stride kS).  On entry M holds A strictly below the diagonal and zeros on and above
+// it; on exit its diagonal blocks hold T11 and T22 (zeros above the diagonal, so the
+// products below may run over full block ranges) and rows 32.. columns 0..31 still
+// hold A21.  All 128 threads call it; X is scratch.
 __device__ __forceinline__ void tri_inverse(float *M, float *X, int tid) {
     // 16x16 diagonal blocks: thread (b, c) forward-substitutes column c of block b.
     // t[m] stays 0 for m < c, so the fixed-range sums need no masks; a row of the
@@ -142,42 +144,6 @@ __device__ __forceinline__ void tri_inverse(float *M, float *X, int tid) {
         *reinterpret_cast<float2 *>(&M[(r0 + rr + 1) * kS + c0 + cc]) = make_float2(-y10, -y11);
         __syncthreads();
     }
-    // block size 32: rows 32.., columns 0..; 2x4 outputs a thread
-    {
-        const int rr = 2 * (tid >> 3), cc = 4 * (tid & 7);
-        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-#pragma unroll
-        for (int m4 = 0; m4 < 8; ++m4) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&M[(32 + rr) * kS + 4 * m4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&M[(32 + rr + 1) * kS + 4 * m4]);
-            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 b = *reinterpret_cast<const float4 *>(&M[(4 * m4 + e) * kS + cc]);
-                x0.x += av0[e] * b.x; x0.y += av0[e] * b.y; x0.z += av0[e] * b.z; x0.w += av0[e] * b.w;
-                x1.x += av1[e] * b.x; x1.y += av1[e] * b.y; x1.z += av1[e] * b.z; x1.w += av1[e] * b.w;
-            }
-        }
-        *reinterpret_cast<float4 *>(&X[rr * kXs + cc]) = x0;
-        *reinterpret_cast<float4 *>(&X[(rr + 1) * kXs + cc]) = x1;
-        __syncthreads();
-        float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-#pragma unroll
-        for (int m4 = 0; m4 < 8; ++m4) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&M[(32 + rr) * kS + 32 + 4 * m4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&M[(32 + rr + 1) * kS + 32 + 4 * m4]);
-            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 b = *reinterpret_cast<const float4 *>(&X[(4 * m4 + e) * kXs + cc]);
-                y0.x += av0[e] * b.x; y0.y += av0[e] * b.y; y0.z += av0[e] * b.z; y0.w += av0[e] * b.w;
-                y1.x += av1[e] * b.x; y1.y += av1[e] * b.y; y1.z += av1[e] * b.z; y1.w += av1[e] * b.w;
-            }
-        }
-        *reinterpret_cast<float4 *>(&M[(32 + rr) * kS + cc]) = make_float4(-y0.x, -y0.y, -y0.z, -y0.w);
-        *reinterpret_cast<float4 *>(&M[(32 + rr + 1) * kS + cc]) = make_float4(-y1.x, -y1.y, -y1.z, -y1.w);
-        __syncthreads();
-    }
 }
 
 struct IntraUnit {
@@ -206,12 +172,35 @@ __device__ __forceinline__ IntraUnit intra_next(const ChunkArgs &a, const IntraU
     return intra_unit(a, (x.c + 1) * a.HV);
 }
 
-__device__ __forceinline__ void issue_kv(const IntraMaps &m, IntraSmem &sm, const IntraUnit &x) {
-    mbar_arrive_expect_tx(&sm.ld_bar, 2 * kTile);
+__device__ __forceinline__ void issue_k(const IntraMaps &m, IntraSmem &sm, const IntraUnit &x) {
+    mbar_arrive_expect_tx(&sm.ld_bar, kTile);
     tma_load_3d(sm.k, &m.k, 0, x.h, x.t0, &sm.ld_bar);
     tma_load_3d(sm.k + kHalf, &m.k, 64, x.h, x.t0, &sm.ld_bar);
-    tma_load_3d(sm.v, &m.v, 0, x.hv, x.t0, &sm.ld_bar);
-    tma_load_3d(sm.v + kHalf, &m.v, 64, x.hv, x.t0, &sm.ld_bar);
+}
+// V is loaded once the block-32 step of the inverse (whose operands use its bytes) is
+// done; the L2 prefetch at the unit's start makes that load a short one.
+__device__ __forceinline__ void issue_v(const IntraMaps &m, IntraSmem &sm, const IntraUnit &x) {
+    mbar_arrive_expect_tx(&sm.v_bar, kTile);
+    tma_load_3d(sm.v, &m.v, 0, x.hv, x.t0, &sm.v_bar);
+    tma_load_3d(sm.v + kHalf, &m.v, 64, x.hv, x.t0, &sm.v_bar);
+}
+
+// Eight fp32 values as bf16 hi (rounded) and lo (the rounded remainder) parts, 16
+// bytes each, at (row, col) of two SW128 tiles (col a multiple of 8).
+__device__ __forceinline__ void split8(const float *src, unsigned char *hi, uint32_t hrow,
+                                       unsigned char *lo, uint32_t lrow, int col) {
+    const float4 a = *reinterpret_cast<const float4 *>(src), b = *reinterpret_cast<const float4 *>(src + 4);
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t ph[4], pl[4];
+#pragma unroll
+    for (int z = 0; z < 4; ++z) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * z], x[2 * z + 1]);
+        const float2 hf = __bfloat1622float2(h2);
+        ph[z] = *reinterpret_cast<const uint32_t *>(&h2);
+        pl[z] = pack_bf2(x[2 * z] - hf.x, x[2 * z + 1] - hf.y);
+    }
+    *reinterpret_cast<uint4 *>(hi + sw128_off(hrow, col)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    *reinterpret_cast<uint4 *>(lo + sw128_off(lrow, col)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
 }
 
 // Persistent: CTA b walks the units [b per, (b + 1) per) (unit u = chunk u / HV, value
@@ -234,9 +223,10 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
     IntraUnit x = intra_unit(a, ub);
     if (tid == 0) {
         mbar_init(&sm.ld_bar, 1);
+        mbar_init(&sm.v_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
-        issue_kv(maps, sm, x);
+        issue_k(maps, sm, x);
     }
     // per-token scalars of thread tid < 64, fetched one unit ahead
     float pG = 0.f, pR = 1.f, pQ = 1.f;
@@ -262,7 +252,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
     __syncthreads();  // the barriers are initialised before anyone waits on them
     const uint32_t tb = sm.tmem_base;
     const uint32_t t_row = tb + ((uint32_t)(warp * 32) << 16);
-    int issued = 1, waited = 0;
+    int issued = 1, waited = 0, v_issued = 0, v_waited = 0;
     uint32_t mphase = 0;
     bool ok = true;
     for (int u = ub; u < ue; ++u) {
@@ -288,6 +278,8 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
                 mma_bf16(tb, sdesc(ks + off, 16, 1024), sdesc(ks + off, 16, 1024), id, s > 0);
             }
             mma_commit(&sm.mma_bar);
+            tma_prefetch_3d(&maps.v, 0, hv, t0);   // V, loaded after the inverse
+            tma_prefetch_3d(&maps.v, 64, hv, t0);
         }
         if (tid < 64) {  // the unit's scalar record for the state scans (before the fetch below)
             const float Gl = L > 0 ? sm.G[L - 1] : 0.f;
@@ -333,6 +325,68 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         tc_fence_before();
         __syncthreads();  // KK has been read: its TMEM columns are free
         tri_inverse(sm.M, sm.X, tid);
+        // Block-32 step: T21 = -T22 (A21 T11), two M=64 N=64 K=32 products on bf16 hi / lo
+        // parts with fp32 accumulation.  The A operand holds the hi part of data row r at
+        // row 16 (r / 8) + r % 8 and its lo part 8 rows below, so that the 16x256b
+        // fragment of a lane holds both (rows ra, ra + 8) and their sum is the product
+        // row.  Operand space: the V tile (loaded afterwards); TMEM columns 0 / 64.
+        {
+            unsigned char *opA = sm.v, *opBh = sm.v + 2 * 4096, *opBl = sm.v + 3 * 4096;
+            const int r = tid >> 2, k8 = 8 * (tid & 3);          // data row, first of 8 columns
+            const uint32_t mh = 16 * (r >> 3) + (r & 7);         // its hi row in opA
+            split8(sm.M + (32 + r) * kS + k8, opA, mh, opA, mh + 8, k8);   // A21 (K-major)
+            split8(sm.M + r * kS + k8, opBh, r, opBl, r, k8);              // T11 [k][j] (MN-major)
+            const uint32_t id = idesc_bf16(64, 64, 0, 1);
+            const int xr = 8 * warp + (lane >> 2), cq = 2 * (lane & 3);    // fragment data row / column
+            auto merge_product = [&](uint32_t col) {
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                if (tid == 0 && ok) {
+                    tc_fence_after();
+                    const uint32_t as = smem_u32(opA), bh = smem_u32(opBh), bl = smem_u32(opBl);
+#pragma unroll
+                    for (int s = 0; s < 2; ++s)
+                        mma_bf16(tb + col, sdesc(as + s * 32, 16, 1024), sdesc(bh + s * 2048, 4096, 1024), id, s > 0);
+#pragma unroll
+                    for (int s = 0; s < 2; ++s)
+                        mma_bf16(tb + col, sdesc(as + s * 32, 16, 1024), sdesc(bl + s * 2048, 4096, 1024), id, true);
+                    mma_commit(&sm.mma_bar);
+                }
+                ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
+                mphase ^= 1;
+                tc_fence_after();
+            };
+            merge_product(0);   // A21 T11
+            {  // X = A21 T11 (hi + lo rows) as the hi / lo B operands; T22 split into opA
+                float d[16];
+                epi::tmem_ld16x256_x4(t_row, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float x0 = d[4 * k] + d[4 * k + 2], x1 = d[4 * k + 1] + d[4 * k + 3];
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                    const float2 hf = __bfloat1622float2(h2);
+                    *reinterpret_cast<__nv_bfloat162 *>(opBh + sw128_off(xr, 8 * k + cq)) = h2;
+                    *reinterpret_cast<uint32_t *>(opBl + sw128_off(xr, 8 * k + cq)) = pack_bf2(x0 - hf.x, x1 - hf.y);
+                }
+                split8(sm.M + (32 + r) * kS + 32 + k8, opA, mh, opA, mh + 8, k8);   // T22
+            }
+            merge_product(64);  // T22 (A21 T11)
+            {
+                float d[16];
+                epi::tmem_ld16x256_x4(t_row + 64, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<float2 *>(sm.M + (32 + xr) * kS + 8 * k + cq) =
+                        make_float2(-(d[4 * k] + d[4 * k + 2]), -(d[4 * k + 1] + d[4 * k + 3]));
+            }
+            tc_fence_before();
+            __syncthreads();   // T is complete in M; the V tile's bytes are free
+            if (tid == 0 && ok) issue_v(maps, sm, x);
+            if (ok) ++v_issued;
+        }
         {  // operands T diag(c) as bf16 rows, and T to HBM: thread -> row tid / 2, 32 columns
             const int i = tid >> 1, j0 = 32 * (tid & 1);
             const float *Mi = sm.M + i * kS + j0;
@@ -370,7 +424,8 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        ok = __syncthreads_and(ok && mbar_wait(&sm.v_bar, v_waited & 1));
+        ++v_waited;
         if (tid == 0 && ok) {  // w^T -> columns 0..63, u^T -> 64..127 (lane d, column i)
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 64, 1, 0);
@@ -385,7 +440,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         ok = __syncthreads_and(ok && mbar_wait(&sm.mma_bar, mphase));
         mphase ^= 1;
         tc_fence_after();
-        if (tid == 0 && ok && has_next) issue_kv(maps, sm, nx);  // K and V have been read
+        if (tid == 0 && ok && has_next) issue_k(maps, sm, nx);  // K has been read
         if (ok && has_next) ++issued;
         if (ok) {  // w^T, then u^T: thread d stages row d (64 tokens) in M, one TMA store each
             unsigned char *stg = reinterpret_cast<unsigned char *>(sm.M);
@@ -422,6 +477,7 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         if (issued > waited) mbar_wait(&sm.ld_bar, (issued - 1) & 1, kDrainLimitNs);  // drain (bounded)
+        if (v_issued > v_waited) mbar_wait(&sm.v_bar, (v_issued - 1) & 1, kDrainLimitNs);
     }
     if (tid == 0) tma_store_wait_all();
     tc_fence_before();

@@ -49,6 +49,10 @@ using epi::quad_sum;
 using epi::tmem_ld16x256_x4;
 
 constexpr int kThr = 256;   // two warpgroups share the 128 TMEM lanes
+// The products are issued by lane 0 of warp 7: an issuing thread stalls while the
+// tensor pipe's queue is full, and warps 0 and 1 have per-token work (the next
+// unit's scalars, dbeta and dG) that runs beside the products.
+constexpr int kIssuer = 224;
 constexpr uint32_t kHalf = 64 * 128;      // 64 rows x 128 B
 constexpr uint32_t kTile = 2 * kHalf;     // 64 rows x 128 bf16: two 8 KB halves
 
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
             tc_fence_after();
         };
         // ---- phase 1: KK, D1, D2 (64 x 64, contraction 128)
-        if (tid == 0 && ok) {
+        if (tid == kIssuer && ok) {
             if (hv % (a.HV / a.H) == a.HV / a.H - 1) {  // a last value head: warm L2 for its dk pass
                 tma_prefetch_3d(&maps.dkp, 0, x.h, t0);
                 tma_prefetch_3d(&maps.dkp, 64, x.h, t0);
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         tc_fence_before();
         __syncthreads();
         // ---- phase 1b: X = dT T^T  (A = dT rows, B = T rows as [N][K])
-        if (tid == 0 && ok) {
+        if (tid == kIssuer && ok) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(64, 64, 0, 0);
     #pragma unroll
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         tc_fence_before();
         __syncthreads();
         // ---- phase 1c: T^T X  (A = T rows read MN-major, B = X rows read MN-major)
-        if (tid == 0 && ok) {
+        if (tid == kIssuer && ok) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(64, 64, 1, 1);
     #pragma unroll
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThr, 2) k_bintra_b_tc(const ChunkArgs a,
         tc_fence_before();
         __syncthreads();
         // ---- phase 2 (M=128: row d of each product is TMEM lane d, column m is a token)
-        if (tid == 0 && ok) {
+        if (tid == kIssuer && ok) {
             tc_fence_after();
             const uint32_t kA = smem_u32(sm.k), wA = smem_u32(sm.dw), vA = smem_u32(sm.dvn);
             const uint32_t tB = smem_u32(sm.op_t), bB = smem_u32(sm.op_b), btB = smem_u32(sm.op_bt);

@@ -41,6 +41,10 @@ namespace {
 using namespace umma;
 
 constexpr int kThr = 256;
+// Step 2's product and the h_c store are issued by lane 0 of warp 7 (which also waits
+// for that store), so that warp 0 is not held up in the c_t dO work beside the
+// product: an issuing thread stalls while the tensor pipe's queue is full.
+constexpr int kPdIssuer = 224;
 constexpr uint32_t kBox = 64 * 128;       // one 64-row x 128-byte SW128 box
 constexpr uint32_t kXBytes = 4 * kBox;    // K (2 boxes), dO half, dv_loc half
 constexpr uint32_t kYBytes = 4 * kBox;    // Q (2 boxes), w^T (128 rows: 2 boxes)
@@ -253,7 +257,7 @@ __global__ void __launch_bounds__(kThr, 2)
         ok = __syncthreads_and(ok && gx);
         if (!ok) break;
         // 2. Pd = K dh'
-        if (tid == 0) {
+        if (tid == kPdIssuer) {
             tc_fence_after();
             const uint32_t as = smem_u32(sm.a_ds), ks = smem_u32(sm.x);
 #pragma unroll
@@ -316,7 +320,7 @@ __global__ void __launch_bounds__(kThr, 2)
                 epi::put_pair(sm.a_dv, rb, col, vb0, vb1);
             }
         }
-        if (tid == 0) tma_store_wait_read();  // dh_c has been read out of a_ds
+        if (tid == kPdIssuer) tma_store_wait_read();  // dh_c has been read out of a_ds
         const bool gy = mbar_wait(&sm.y_bar, par);
         fence_proxy_async_smem();
         tc_fence_before();
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kThr, 2)
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     }
-    if (tid == 0) tma_store_wait_all();
+    if (tid == 0 || tid == kPdIssuer) tma_store_wait_all();
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving

@@ -270,7 +270,10 @@ __global__ void __launch_bounds__(kThr, 4) k_intra_tc(const ChunkArgs a,
         ++waited;
         if (!ok) break;
         tc_fence_after();
-        if (tid == 0 && ok) {  // KK = K K^T into columns 0..63 (M=64: row m at lane 32 (m / 16) + m % 16)
+        // KK = K K^T into columns 0..63 (M=64: row m at lane 32 (m / 16) + m % 16), issued
+        // by lane 0 of warp 3 while warps 0 and 1 write the scalar record and fetch the
+        // next unit's scalars (an issuing thread stalls while the tensor pipe's queue is full)
+        if (tid == 96 && ok) {
             const uint32_t ks = smem_u32(sm.k);
             const uint32_t id = idesc_bf16(64, 64, 0, 0);
             for (int s = 0; s < 8; ++s) {

@@ -85,7 +85,7 @@ struct BaSmem {
     float iq[2][64];              // 1 / r_q (0 past L); [2]: this unit's and the next one's
     float rp[2][64];              // per-warpgroup partial row sums of P1
     float cp[4][64];              // per-row-block column sums of P1
-    float hdh[4];                 // per-warp partial <h, dh'> (warps 4..7)
+    float hdh[2][4];              // per-warp partial <h, dh'> (warps 8..11), by unit parity
     float G[2][64], eg[64], egl_g[64];  // G, e^{G_t}, e^{G_L - G_t} (0 past L)
     float qsc[2][64], rki[2][64];       // scale / r_q, 1 / r_k
     uint64_t a_bar, b_bar[2], mma_bar;   // group A (h, dh, dO, dv_new, v_new), group B (q, k) per buffer
@@ -224,6 +224,43 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         }
     };
     publish(x.L, 0);
+    // A unit's dG runs on warp 1 during the next unit's first product batch (warp 1 is
+    // idle there: warp 0 issues the products, warps 2 and 3 fetch scalars, warps 8..11
+    // take the <h, dh'> dot).
+    struct Pend {
+        bool on;
+        int t0, hv, L, buf;
+    };
+    Pend pend = {false, 0, 0, 0, 0};
+    auto finish_dg = [&](const Pend &p) {  // dG_t, and the G_L terms summed in a fixed order
+        const float *pRki = sm.rki[p.buf], *pQsc = sm.qsc[p.buf];
+        const float Gl = p.L > 0 ? sm.G[p.buf][p.L - 1] : 0.f;
+        float dgz[2], sx = 0.f;
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+            const int tt = 2 * lane + z;
+            float dg = 0.f, xi = 0.f;
+            if (tt < p.L) {
+                xi = (sm.pk[0][tt] + sm.pk[1][tt]) * pRki[tt];
+                const float cps = ((sm.cp[0][tt] + sm.cp[1][tt]) + sm.cp[2][tt]) + sm.cp[3][tt];
+                dg = (sm.pq[0][tt] + sm.pq[1][tt]) * pQsc[tt] - xi + (sm.rp[0][tt] + sm.rp[1][tt]) - cps;
+            }
+            sx += xi;
+            dgz[z] = dg;
+        }
+        sx = warp_sum(sx);
+        float hd = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) hd += sm.hdh[p.buf][w];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+            const int tt = 2 * lane + z;
+            if (tt < p.L && in_range((size_t)(p.t0 + tt) * a.HV + p.hv, 1, n_tok_hv(a), a.status)) {
+                const float extra = (tt == p.L - 1) ? sx + __expf(Gl) * hd : 0.f;
+                a.dGp[(size_t)(p.t0 + tt) * a.HV + p.hv] = dgz[z] + extra;
+            }
+        }
+    };
     for (int u = ub; u < ue; ++u) {
         const bool has_next = u + 1 < ue;
         const int L = x.L;
@@ -294,8 +331,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
                     }
                 }
             hdh = warp_sum(hdh);
-            if (lane == 0) sm.hdh[warp - 8] = hdh;
+            if (lane == 0) sm.hdh[cur][warp - 8] = hdh;
         }
+        if (pend.on && warp == 1) finish_dg(pend);  // the unit before's, while the products run
         if (tid == 0) tma_store_wait_read();  // the last unit's staged rows have been read
         bool done = __syncthreads_and(mbar_wait(&sm.mma_bar, phase));
         phase ^= 1;
@@ -503,39 +541,14 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
             }
         }
         tc_fence_before();
-        if (warp == 0) {  // dG_t, and the G_L terms summed in a fixed order
-            float dgz[2], sx = 0.f;
-#pragma unroll
-            for (int z = 0; z < 2; ++z) {
-                const int tt = 2 * lane + z;
-                float dg = 0.f, xi = 0.f;
-                if (tt < L) {
-                    xi = (sm.pk[0][tt] + sm.pk[1][tt]) * sRki[tt];
-                    const float cps = ((sm.cp[0][tt] + sm.cp[1][tt]) + sm.cp[2][tt]) + sm.cp[3][tt];
-                    dg = (sm.pq[0][tt] + sm.pq[1][tt]) * sQsc[tt] - xi + (sm.rp[0][tt] + sm.rp[1][tt]) - cps;
-                }
-                sx += xi;
-                dgz[z] = dg;
-            }
-            sx = warp_sum(sx);
-            float hd = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) hd += sm.hdh[w];
-#pragma unroll
-            for (int z = 0; z < 2; ++z) {
-                const int tt = 2 * lane + z;
-                if (tt < L && in_range((size_t)(x.t0 + tt) * a.HV + x.hv, 1, n_tok_hv(a), a.status)) {
-                    const float extra = (tt == L - 1) ? sx + __expf(Gl) * hd : 0.f;
-                    a.dGp[(size_t)(x.t0 + tt) * a.HV + x.hv] = dgz[z] + extra;
-                }
-            }
-        }
+        pend = {true, x.t0, x.hv, L, cur};
         if (has_next) publish(nx.L, cur ^ 1);
         __syncthreads();  // the per-unit scalars are free for the next unit
         if (need_next_b) bcur ^= 1;
         need_b = need_next_b;
         x = nx;
     }
+    if (ok && pend.on && warp == 1) finish_dg(pend);  // the last unit's
     if (!ok && tid == 0) {
         if (a.status) atomicOr(a.status, 2);
         // drain the loads still in flight (bounded) before leaving

@@ -68,6 +68,9 @@ constexpr uint32_t cQI = 128, cKI = 256;                                   // ba
 // key head's dqhat / dkhat sums live in lanes 16..31 of the Dq / Dk columns, in the
 // 16x256b fragment layout of the epilogue (the MMAs never write those lanes).
 constexpr uint32_t kAccLanes = 16u << 16;
+// The next unit's group-A tiles are issued by lane 0 of warp 8, on the dk side, whose
+// part of the epilogue that follows is the lighter one (an issuing thread can stall).
+constexpr int kLoader = 256;
 
 struct BaSmem {
     unsigned char hvn[2 * kHV];   // per v-half: h_c [k][v] (128 rows), then v_new [t][v] (64 rows)
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
         if (!done) { ok = false; break; }
         // group A has been consumed (batch 1 and the dot): load the next unit's
         if (has_next) {
-            if (tid == 0) issue_a(maps, sm, a, nx);
+            if (tid == kLoader) issue_a(maps, sm, a, nx);
             ++a_issued;
         }
         const int ra = sub * 16 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);  // fragment rows / column

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThr, 2)
     const uint32_t t_row = tbase + ((uint32_t)(sub * 32) << 16);
     const uint32_t tS = t_row + c0, tP = t_row + 64 + c0;   // this warpgroup's columns
 
-    int xk_issued = 0, xd_issued = 0, y_issued = 0;  // thread 0's load counts
+    int xk_issued = 0, xd_issued = 0, y_issued = 0;  // load counts (thread 0's are complete)
     if (tid == 0 && nch > 0) {
         issue_xk(maps, sm, a, step_c(0), step_t0(0), h, hv, 0);
         if (!phi) issue_xd(maps, sm, step_t0(0), hv, vb);
@@ -343,12 +343,15 @@ __global__ void __launch_bounds__(kThr, 2)
                 tma_store_3d(&maps.dvn, 64 * vb, hv, t0, sm.a_dv);
                 tma_store_commit();
             }
-            if (i + 1 < nch && !phi) {
-                issue_xd(maps, sm, step_t0(i + 1), hv, vb);
-                ++xd_issued;
-            }
-            if (i + 2 < nch) prefetch_chunk(maps, a, step_c(i + 2), step_t0(i + 2), h, hv, vb, !phi);
         }
+        // the next chunk's dO / dv_loc halves (read by step 3) and the L2 prefetch a step
+        // further, from warp 1 while thread 0 issues step 4: one thread issuing all of it
+        // reached step 4's wait late
+        if (i + 1 < nch && !phi) {
+            if (tid == 32) issue_xd(maps, sm, step_t0(i + 1), hv, vb);
+            ++xd_issued;
+        }
+        if (tid == 32 && i + 2 < nch) prefetch_chunk(maps, a, step_c(i + 2), step_t0(i + 2), h, hv, vb, !phi);
         ok = mbar_wait(&sm.mma_bar, phase) && ok;
         phase ^= 1;
         tc_fence_after();

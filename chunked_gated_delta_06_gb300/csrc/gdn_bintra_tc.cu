@@ -196,9 +196,9 @@ __global__ void __launch_bounds__(kThr, 1) k_bintra_a_tc(const ChunkArgs a,
     int bcur = 0;         // the q / k buffer of the current unit
     bool need_b = true;   // the current unit waits for a q / k load
     // Warp 0 issues the products and does nothing else while they run (its issuing
-    // thread stalls for as long as the tensor pipe is full); warps 2 and 3 own the
-    // per-token scalars (token ft = tid - 64), fetched one unit ahead, and warps 8..11
-    // the <h, dh'> dot.
+    // thread stalls for as long as the tensor pipe is full); meanwhile warp 1 finishes
+    // the unit before's dG, warps 2 and 3 own the per-token scalars (token ft = tid - 64),
+    // fetched one unit ahead, and warps 8..11 take the <h, dh'> dot.
     const int ft = tid - 64;
     const bool scal = ft >= 0 && ft < 64;
     float pG = 0.f, pRq = 1.f, pRk = 1.f;
